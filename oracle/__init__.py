@@ -1,0 +1,198 @@
+"""Float64 CPU oracle for bounded-tree speculative decoding.
+
+TEST INFRASTRUCTURE ONLY.  A plain, slow, obviously-correct restatement of
+what the CUDA library computes (``tsd_oracle.c``), loaded through ctypes.
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg may import it.  It shares no code with the CUDA library, and
+the product path never calls it.
+
+Every function takes and returns numpy arrays; floating inputs are converted
+to float64 exactly (bf16 and fp32 values are representable in float64).
+
+Parity status: each function is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tsd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+OK, ERR_ARG, ERR_BAD_TREE, ERR_NONFINITE = 0, 1, 4, 5
+
+
+def build(force: bool = False) -> str:
+    """Compile ``tsd_oracle.c`` into ``liboracle.so`` next to it (gcc, -O2)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i64, i32, f64, u64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_uint64
+        lib.orc_philox4x64_10.argtypes = [P, P, P]
+        lib.orc_philox4x64_10.restype = None
+        lib.orc_uniform.argtypes = [u64, u64, u64, u64]
+        lib.orc_uniform.restype = f64
+        lib.orc_drafter_stats.argtypes = [P, i64, i64, f64, i32, P, P, P]
+        lib.orc_build_tree.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        lib.orc_tree_mask.argtypes = [P, i32, i32, i32, P, P, P, i64]
+        lib.orc_row_probs.argtypes = [P, i64, f64, P]
+        lib.orc_tev.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P, P, P, P, P, P, P, P]
+        lib.orc_predraw.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P, P]
+        lib.orc_tev_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
+        lib.orc_predraw_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
+        for f in ("orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
+                  "orc_tev", "orc_predraw", "orc_tev_sample_many", "orc_predraw_sample_many"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s failed with status %d" % (what, code))
+        self.code = code
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise OracleError(code, what)
+
+
+def philox4x64_10(counter, key) -> np.ndarray:
+    """Philox4x64-10 block: 4 uint64 outputs for a 4-word counter, 2-word key."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
+    out = np.zeros(4, dtype=np.uint64)
+    _load().orc_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, tree: int, node: int, stream: int) -> float:
+    """The uniform the method uses for (seed; tree, node, stream)."""
+    return _load().orc_uniform(seed, tree, node, stream)
+
+
+def drafter_stats(z, temp: float, k: int):
+    """Per row: LSE of z/temp, top-k ids by (logit desc, id asc), their log q."""
+    z = _f64(z)
+    V = z.shape[-1]
+    rows = z.size // V
+    lse = np.zeros(rows)
+    tid = np.zeros((rows, k), dtype=np.int32)
+    tlq = np.zeros((rows, k))
+    _check(_load().orc_drafter_stats(_ptr(z), rows, V, temp, k, _ptr(lse), _ptr(tid), _ptr(tlq)),
+           "drafter_stats")
+    shp = z.shape[:-1]
+    return lse.reshape(shp), tid.reshape(shp + (k,)), tlq.reshape(shp + (k,))
+
+
+def build_tree(top_id, top_logq, B: int, push_rule: int = 0) -> dict:
+    """Best-first builder on one tree.  top_id/top_logq: [K, L, k] (or [L, k])."""
+    tid = _i32(top_id)
+    tlq = _f64(top_logq)
+    if tid.ndim == 2:
+        tid, tlq = tid[None], tlq[None]
+    K, L, k = tid.shape
+    out = {n: np.zeros(B + 1, dtype=np.int32) for n in ("parent", "token", "depth", "rank", "mode")}
+    out["score"] = np.zeros(B + 1)
+    nn = np.zeros(1, dtype=np.int32)
+    _check(_load().orc_build_tree(_ptr(tid), _ptr(tlq), K, L, k, B, push_rule,
+                                  _ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]),
+                                  _ptr(out["score"]), _ptr(out["rank"]), _ptr(out["mode"]), _ptr(nn)),
+           "build_tree")
+    out["n_nodes"] = int(nn[0])
+    return out
+
+
+def tree_mask(parent, n_nodes: int, B: int, prefix_len: int, with_additive: bool = False):
+    parent = _i32(parent)
+    W = (B + 1 + 31) // 32
+    bits = np.zeros((B + 1, W), dtype=np.uint32)
+    pos = np.zeros(B + 1, dtype=np.int32)
+    ld = prefix_len + B + 1
+    add = np.zeros((B + 1, ld)) if with_additive else None
+    _check(_load().orc_tree_mask(_ptr(parent), n_nodes, B, prefix_len, _ptr(bits), _ptr(pos),
+                                 _ptr(add) if add is not None else None, ld), "tree_mask")
+    return bits, pos, add
+
+
+def row_probs(z, T: float) -> np.ndarray:
+    z = _f64(z)
+    p = np.zeros_like(z)
+    _check(_load().orc_row_probs(_ptr(z), z.size, T, _ptr(p)), "row_probs")
+    return p
+
+
+def tev(z, parent, token, n_nodes: int, T: float, seed: int, tree: int = 0) -> dict:
+    """Tree Exit Verification on one tree; z: [>= n_nodes, V] target logits."""
+    z = _f64(z)
+    V = z.shape[-1]
+    z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
+    parent, token = _i32(parent), _i32(token)
+    n = n_nodes
+    P, rho, w, pedge = (np.zeros(n) for _ in range(4))
+    cov = np.zeros(1)
+    ex, bo, al = (np.zeros(1, dtype=np.int32) for _ in range(3))
+    ue, ub = np.zeros(1), np.zeros(1)
+    _check(_load().orc_tev(_ptr(z), _ptr(parent), _ptr(token), n, V, T, seed, tree, _ptr(P),
+                           _ptr(rho), _ptr(w), _ptr(pedge), _ptr(cov), _ptr(ex), _ptr(bo),
+                           _ptr(al), _ptr(ue), _ptr(ub)), "tev")
+    return dict(P=P, rho=rho, w=w, pedge=pedge, coverage=float(cov[0]), exit_node=int(ex[0]),
+                bonus=int(bo[0]), accept_len=int(al[0]), u_exit=float(ue[0]), u_bonus=float(ub[0]))
+
+
+def predraw(z, parent, token, n_nodes: int, T: float, seed: int, tree: int = 0) -> dict:
+    """Predraw-and-follow on one tree; z: [>= n_nodes, V] target logits."""
+    z = _f64(z)
+    V = z.shape[-1]
+    z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
+    parent, token = _i32(parent), _i32(token)
+    draws = np.zeros(n_nodes, dtype=np.int32)
+    ex, bo, al = (np.zeros(1, dtype=np.int32) for _ in range(3))
+    _check(_load().orc_predraw(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, seed, tree,
+                               _ptr(draws), _ptr(ex), _ptr(bo), _ptr(al)), "predraw")
+    return dict(draws=draws, exit_node=int(ex[0]), bonus=int(bo[0]), accept_len=int(al[0]))
+
+
+def sample_many(kind: str, z, parent, token, n_nodes: int, T: float, seed: int, n_draws: int,
+                first_tree: int = 0):
+    """(exit node, bonus token) of n_draws independent draws of the sampler
+    `kind` ("tev" or "predraw") on one tree; draw i uses tree index
+    first_tree + i."""
+    z = _f64(z)
+    V = z.shape[-1]
+    z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
+    parent, token = _i32(parent), _i32(token)
+    ex = np.zeros(n_draws, dtype=np.int32)
+    bo = np.zeros(n_draws, dtype=np.int32)
+    fn = _load().orc_tev_sample_many if kind == "tev" else _load().orc_predraw_sample_many
+    _check(fn(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, seed, first_tree, n_draws,
+              _ptr(ex), _ptr(bo)), kind + "_sample_many")
+    return ex, bo

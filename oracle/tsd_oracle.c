@@ -1,0 +1,573 @@
+/*
+ * tsd_oracle.c -- float64 CPU oracle for bounded-tree speculative decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, obviously-correct
+ * restatement of what the CUDA library computes, used to check it.  Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or helper with the CUDA library, and the
+ * product path never calls it.
+ *
+ * Sources (page title, section / equation):
+ *   [EXIT]  "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
+ *           Decoding" -- Sec. 3 Eq. 1-2 (p_v, P), Sec. 3.1 Eq. 4 (rho, w),
+ *           Eq. 6 (target coverage), Eq. 7 (residual law), App. A.4.1
+ *           (predraw-and-follow), App. B Algorithm 1 (TEV).
+ *   [CAST]  "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters"
+ *           -- Sec. 2 Eq. 1 (plug-in score), Thm. 1 (tie order), App. C
+ *           "Candidate construction" (top-K heap, push all K children) and
+ *           "Packed verification" (ancestor mask, position ids).
+ *   [MFD]   "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
+ *           Speculative Decoding" -- Sec. 3.4 Eq. 2 (best-mode score),
+ *           App. B "Merged heap" and Prop. 6 (sibling / first-child pushes,
+ *           node reuse across modes).
+ *   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ *           as 1, 2, 3", SC'11 -- the Philox4x64-10 counter-based generator.
+ *
+ * Readings where the pages are open (each also listed in the design doc):
+ *   - Uniforms: u = (x0 >> 40) * 2^-24 from Philox4x64-10 with
+ *     counter (tree, node, stream, 0) and key (seed, 0); stream 0 = TEV exit
+ *     draw, 1 = TEV bonus draw, 2 = predraw at node `node`.
+ *   - "Draw" (Alg. 1 lines 8-9) is inverse-CDF sampling: nodes in index
+ *     (build) order for the exit, token ids ascending (skipping the drafted
+ *     children) for the bonus; strict '>' so zero-mass items are never drawn;
+ *     the normaliser is the computed total, not 1.
+ *   - rho(v) is evaluated as the residual sum over non-child tokens (the
+ *     equality of Eq. 4 and Eq. 13 of [EXIT]); the test suite checks it
+ *     against 1 - sum of child probabilities.
+ *   - T = 0 is the greedy limit: p_v is one-hot at the arg-max (lowest id on
+ *     ties).
+ *   - Builder tie order: score desc, depth asc, mode asc, rank sequence
+ *     lexicographic asc; top-k per position ordered by (logit desc, id asc).
+ *   - Prefixes of zero drafter probability (score -inf) never become nodes.
+ *
+ * Parity status: every function here is pinned by tests/test_oracle_pins.py
+ * (brute force, closed forms, library routines, hand-computed fixtures).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_NONFINITE 5
+#define ORC_ERR_BAD_TREE 4
+#define ORC_MAX_DEPTH 64
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x64-10 [PHILOX]: ten rounds of two 64x64->128 multiplies, with a  */
+/* Weyl-sequence key schedule.                                               */
+/* ------------------------------------------------------------------------ */
+static const uint64_t PHILOX_M0 = 0xD2E7470EE14C6C93ULL;
+static const uint64_t PHILOX_M1 = 0xCA5A826395121157ULL;
+static const uint64_t PHILOX_W0 = 0x9E3779B97F4A7C15ULL;
+static const uint64_t PHILOX_W1 = 0xBB67AE8584CAA73BULL;
+
+void orc_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += PHILOX_W0;
+            k1 += PHILOX_W1;
+        }
+        unsigned __int128 p0 = (unsigned __int128)PHILOX_M0 * c0;
+        unsigned __int128 p1 = (unsigned __int128)PHILOX_M1 * c2;
+        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        uint64_t n0 = hi1 ^ c1 ^ k0;
+        uint64_t n1 = lo1;
+        uint64_t n2 = hi0 ^ c3 ^ k1;
+        uint64_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* One uniform in [0, 1) on a 2^-24 grid, for (seed; tree, node, stream). */
+double orc_uniform(uint64_t seed, uint64_t tree, uint64_t node, uint64_t stream)
+{
+    uint64_t ctr[4] = {tree, node, stream, 0};
+    uint64_t key[2] = {seed, 0};
+    uint64_t out[4];
+    orc_philox4x64_10(ctr, key, out);
+    return (double)(out[0] >> 40) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Drafter statistics [CAST Sec. 2 Eq. 1, App. C]: for each row j,           */
+/*   LSE_j = log sum_a exp(z_j(a)/T),  log q_j(a) = z_j(a)/T - LSE_j,       */
+/* and the top-k tokens ordered by (logit desc, id asc).                     */
+/* ------------------------------------------------------------------------ */
+int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int k,
+                      double *lse, int32_t *top_id, double *top_logq)
+{
+    if (!(temp > 0.0) || k < 1 || k > V || V < 1) return ORC_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *row = z + r * V;
+        double m = -INFINITY;
+        for (int64_t a = 0; a < V; ++a) {
+            if (isnan(row[a]) || row[a] == INFINITY) return ORC_ERR_NONFINITE;
+            if (row[a] > m) m = row[a];
+        }
+        if (m == -INFINITY) return ORC_ERR_NONFINITE;
+        double s = 0.0;
+        for (int64_t a = 0; a < V; ++a) s += exp((row[a] - m) / temp);
+        lse[r] = m / temp + log(s);
+        /* top-k by repeated selection: the best remaining token each time */
+        for (int i = 0; i < k; ++i) {
+            int64_t best = -1;
+            for (int64_t a = 0; a < V; ++a) {
+                int taken = 0;
+                for (int j = 0; j < i; ++j)
+                    if (top_id[r * k + j] == (int32_t)a) { taken = 1; break; }
+                if (taken) continue;
+                if (best < 0 || row[a] > row[best]) best = a;  /* ties keep the lower id */
+            }
+            top_id[r * k + i] = (int32_t)best;
+            top_logq[r * k + i] = row[best] / temp - lse[r];
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Best-first tree builder.                                                  */
+/*                                                                           */
+/* Universe: for each mode m (K modes; K = 1 is DDTree / CAST) and drafter   */
+/* position j = 1..L, the k retained tokens of that mode's row, with their   */
+/* unrenormalised log-probabilities.  A heap entry (m, v) is a prefix v      */
+/* scored under mode m: s_m(v) = sum_j log q_{m,j}(v_j) [CAST Eq. 1;         */
+/* MFD Eq. 2 with a uniform prior, whose constant log(1/K) is dropped from   */
+/* the ranking].                                                             */
+/*                                                                           */
+/* push_rule 0 [MFD App. B]: seed with each mode's rank-0 first token; a pop */
+/*   pushes its next sibling (rank r+1) and its first child (rank 0 at the   */
+/*   next position).                                                         */
+/* push_rule 1 [CAST App. C]: seed with each mode's k first tokens; a pop    */
+/*   pushes all k children at the next position.                             */
+/* A popped prefix already in the tree reuses its node and spends no budget; */
+/* its successors are pushed either way [MFD App. B].                        */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    double score;        /* s_m(v) */
+    double pscore;       /* s_m(parent of v) */
+    int32_t mode;
+    int32_t depth;       /* |v| >= 1 */
+    int32_t rank;        /* rank of v's last token in mode m's list */
+    int32_t pnode;       /* tree node of v's parent */
+    uint8_t ranks[ORC_MAX_DEPTH]; /* rank sequence r_1..r_depth */
+} orc_entry;
+
+/* 1 if a comes before b in the total order. */
+static int orc_before(const orc_entry *a, const orc_entry *b)
+{
+    if (a->score != b->score) return a->score > b->score;
+    if (a->depth != b->depth) return a->depth < b->depth;
+    if (a->mode != b->mode) return a->mode < b->mode;
+    for (int i = 0; i < a->depth; ++i)
+        if (a->ranks[i] != b->ranks[i]) return a->ranks[i] < b->ranks[i];
+    return 0;
+}
+
+typedef struct {
+    orc_entry *e;
+    int64_t n, cap;
+} orc_heap;
+
+static void heap_push(orc_heap *h, const orc_entry *x)
+{
+    int64_t i = h->n++;
+    h->e[i] = *x;
+    while (i > 0) {
+        int64_t p = (i - 1) / 2;
+        if (!orc_before(&h->e[i], &h->e[p])) break;
+        orc_entry t = h->e[i]; h->e[i] = h->e[p]; h->e[p] = t;
+        i = p;
+    }
+}
+
+static orc_entry heap_pop(orc_heap *h)
+{
+    orc_entry top = h->e[0];
+    h->e[0] = h->e[--h->n];
+    int64_t i = 0;
+    for (;;) {
+        int64_t l = 2 * i + 1, r = l + 1, b = i;
+        if (l < h->n && orc_before(&h->e[l], &h->e[b])) b = l;
+        if (r < h->n && orc_before(&h->e[r], &h->e[b])) b = r;
+        if (b == i) break;
+        orc_entry t = h->e[i]; h->e[i] = h->e[b]; h->e[b] = t;
+        i = b;
+    }
+    return top;
+}
+
+/*
+ * top_id, top_logq: [K][L][k] (mode-major, then position, then rank).
+ * Outputs have B+1 slots; node 0 is the root (parent -1, token -1, depth 0,
+ * score 0).  Slots past n_nodes are filled with -1 and score -inf.
+ */
+int orc_build_tree(const int32_t *top_id, const double *top_logq, int K, int L, int k, int B,
+                   int push_rule, int32_t *parent, int32_t *token, int32_t *depth,
+                   double *score, int32_t *rank, int32_t *mode, int32_t *n_nodes_out)
+{
+    if (K < 1 || L < 1 || L > ORC_MAX_DEPTH || k < 1 || k > 255 || B < 0) return ORC_ERR_ARG;
+    for (int i = 0; i <= B; ++i) {
+        parent[i] = token[i] = depth[i] = rank[i] = mode[i] = -1;
+        score[i] = -INFINITY;
+    }
+    parent[0] = -1; token[0] = -1; depth[0] = 0; score[0] = 0.0;
+    int32_t *first_child = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B + 1));
+    int32_t *next_sib = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B + 1));
+    for (int i = 0; i <= B; ++i) first_child[i] = next_sib[i] = -1;
+
+    orc_heap h;
+    h.cap = (int64_t)K * k + (int64_t)(k + 2) * K * (B + 1) + 16;
+    h.n = 0;
+    h.e = (orc_entry *)malloc(sizeof(orc_entry) * (size_t)h.cap);
+
+#define LQ(m, j, r) top_logq[((int64_t)(m) * L + (j)) * k + (r)]
+#define TK(m, j, r) top_id[((int64_t)(m) * L + (j)) * k + (r)]
+    for (int m = 0; m < K; ++m) {
+        int nseed = (push_rule == 0) ? 1 : k;
+        for (int r = 0; r < nseed; ++r) {
+            orc_entry x;
+            memset(&x, 0, sizeof x);
+            x.mode = m; x.depth = 1; x.rank = r; x.pnode = 0;
+            x.pscore = 0.0; x.score = 0.0 + LQ(m, 0, r);
+            x.ranks[0] = (uint8_t)r;
+            heap_push(&h, &x);
+        }
+    }
+    int n = 1;
+    int status = ORC_OK;
+    while (n <= B && h.n > 0) {
+        orc_entry e = heap_pop(&h);
+        if (isnan(e.score)) { status = ORC_ERR_NONFINITE; break; }
+        if (e.score == -INFINITY) break; /* only zero-probability prefixes remain */
+        int32_t t = TK(e.mode, e.depth - 1, e.rank);
+        /* find the node (pnode, t) if some mode already created it */
+        int node = -1;
+        for (int c = first_child[e.pnode]; c >= 0; c = next_sib[c])
+            if (token[c] == t) { node = c; break; }
+        if (node < 0) {
+            node = n++;
+            parent[node] = e.pnode; token[node] = t; depth[node] = e.depth;
+            score[node] = e.score; rank[node] = e.rank; mode[node] = e.mode;
+            /* append to the parent's child list */
+            if (first_child[e.pnode] < 0) first_child[e.pnode] = node;
+            else {
+                int c = first_child[e.pnode];
+                while (next_sib[c] >= 0) c = next_sib[c];
+                next_sib[c] = node;
+            }
+        }
+        if (push_rule == 0) {
+            if (e.rank + 1 < k) { /* next sibling: same parent, rank + 1 */
+                orc_entry s = e;
+                s.rank = e.rank + 1;
+                s.ranks[e.depth - 1] = (uint8_t)(e.rank + 1);
+                s.score = e.pscore + LQ(e.mode, e.depth - 1, e.rank + 1);
+                heap_push(&h, &s);
+            }
+            if (e.depth < L) { /* first child: rank 0 at the next position */
+                orc_entry c = e;
+                c.depth = e.depth + 1; c.rank = 0; c.pnode = node;
+                c.pscore = e.score; c.score = e.score + LQ(e.mode, e.depth, 0);
+                c.ranks[e.depth] = 0;
+                heap_push(&h, &c);
+            }
+        } else {
+            if (e.depth < L) {
+                for (int r = 0; r < k; ++r) {
+                    orc_entry c = e;
+                    c.depth = e.depth + 1; c.rank = r; c.pnode = node;
+                    c.pscore = e.score; c.score = e.score + LQ(e.mode, e.depth, r);
+                    c.ranks[e.depth] = (uint8_t)r;
+                    heap_push(&h, &c);
+                }
+            }
+        }
+    }
+#undef LQ
+#undef TK
+    *n_nodes_out = n;
+    free(h.e);
+    free(first_child);
+    free(next_sib);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ancestor mask and position ids [CAST App. C "Packed verification";       */
+/* Lemma 1]: row v sees the P prefix entries, its ancestors and itself;      */
+/* pos(root) = P, pos(v) = P + depth(v).  Rows past n_nodes are padding:     */
+/* they see the prefix and themselves only, at position P.                   */
+/* bits: [B+1][W] u32 with W = ceil((B+1)/32), bit u of row v = column u.    */
+/* addmask (nullable): [B+1][ld], 0 where visible and -inf elsewhere, over   */
+/* columns [0, P + B + 1).                                                   */
+/* ------------------------------------------------------------------------ */
+int orc_tree_mask(const int32_t *parent, int n_nodes, int B, int prefix_len,
+                  uint32_t *bits, int32_t *pos, double *addmask, int64_t ld)
+{
+    if (n_nodes < 1 || n_nodes > B + 1 || prefix_len < 0) return ORC_ERR_ARG;
+    int W = (B + 1 + 31) / 32;
+    memset(bits, 0, sizeof(uint32_t) * (size_t)(B + 1) * (size_t)W);
+    for (int v = 0; v <= B; ++v) {
+        int d = 0;
+        if (v < n_nodes) {
+            int u = v, steps = 0;
+            while (u >= 0) {
+                if (u >= n_nodes || steps > n_nodes) return ORC_ERR_BAD_TREE;
+                bits[(int64_t)v * W + u / 32] |= 1u << (u % 32);
+                u = parent[u];
+                ++steps;
+            }
+            d = steps - 1;
+        } else {
+            bits[(int64_t)v * W + v / 32] |= 1u << (v % 32);
+        }
+        pos[v] = prefix_len + d;
+        if (addmask) {
+            double *row = addmask + (int64_t)v * ld;
+            for (int c = 0; c < prefix_len; ++c) row[c] = 0.0;
+            for (int u = 0; u <= B; ++u)
+                row[prefix_len + u] = ((bits[(int64_t)v * W + u / 32] >> (u % 32)) & 1u) ? 0.0 : -INFINITY;
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Target distributions at one node [EXIT Eq. 1]: p(a) = softmax(z/T)(a),    */
+/* or one-hot at the arg-max (lowest id on ties) when T == 0.                */
+/* ------------------------------------------------------------------------ */
+int orc_row_probs(const double *z, int64_t V, double T, double *p)
+{
+    double m = -INFINITY;
+    int64_t am = -1;
+    for (int64_t a = 0; a < V; ++a) {
+        if (isnan(z[a]) || z[a] == INFINITY) return ORC_ERR_NONFINITE;
+        if (am < 0 || z[a] > m) { m = z[a]; am = a; }
+    }
+    if (m == -INFINITY) return ORC_ERR_NONFINITE;
+    if (T == 0.0) {
+        for (int64_t a = 0; a < V; ++a) p[a] = (a == am) ? 1.0 : 0.0;
+        return ORC_OK;
+    }
+    double s = 0.0;
+    for (int64_t a = 0; a < V; ++a) s += exp((z[a] - m) / T);
+    for (int64_t a = 0; a < V; ++a) p[a] = exp((z[a] - m) / T) / s;
+    return ORC_OK;
+}
+
+/* Check the tree: node 0 is the root, parents precede children, tokens lie in
+ * [0, V), sibling tokens are distinct.  Fills depth[]. */
+static int orc_check_tree(const int32_t *parent, const int32_t *token, int n, int64_t V,
+                          int32_t *depth)
+{
+    if (n < 1 || parent[0] != -1) return ORC_ERR_BAD_TREE;
+    depth[0] = 0;
+    for (int u = 1; u < n; ++u) {
+        if (parent[u] < 0 || parent[u] >= u) return ORC_ERR_BAD_TREE;
+        if (token[u] < 0 || token[u] >= V) return ORC_ERR_BAD_TREE;
+        depth[u] = depth[parent[u]] + 1;
+        for (int s = 1; s < u; ++s)
+            if (parent[s] == parent[u] && token[s] == token[u]) return ORC_ERR_BAD_TREE;
+    }
+    return ORC_OK;
+}
+
+/* Mark the drafted-child tokens of node v: mark[a] = child node index (>= 1)
+ * for a in A(v), 0 otherwise.  The caller clears the marks with
+ * orc_unmark_children. */
+static void orc_mark_children(const int32_t *parent, const int32_t *token, int n, int v,
+                              int32_t *mark)
+{
+    for (int u = 1; u < n; ++u)
+        if (parent[u] == v) mark[token[u]] = u;
+}
+
+static void orc_unmark_children(const int32_t *parent, const int32_t *token, int n, int v,
+                                int32_t *mark)
+{
+    for (int u = 1; u < n; ++u)
+        if (parent[u] == v) mark[token[u]] = 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tree Exit Verification [EXIT App. B Algorithm 1] on one tree.             */
+/*   z: [n][V] target logits, row v = node v.                                */
+/* Outputs (length n unless noted):                                          */
+/*   P      prefix probability, P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u)     */
+/*   rho    local exit probability (residual mass of non-child tokens)       */
+/*   w      exit mass w = P rho                                              */
+/*   pedge  p_pa(u)(x_u) for u >= 1 (pedge[0] = 1)                           */
+/*   *coverage = C_p = sum_{u != root} P(u)                  [EXIT Eq. 6]    */
+/*   *exit_node, *bonus, *accept_len = depth(exit) + 1                       */
+/*   *u_exit, *u_bonus: the two uniforms used                                */
+/* ------------------------------------------------------------------------ */
+int orc_tev(const double *z, const int32_t *parent, const int32_t *token, int n, int64_t V,
+            double T, uint64_t seed, uint64_t tree, double *P, double *rho, double *w,
+            double *pedge, double *coverage, int32_t *exit_node, int32_t *bonus,
+            int32_t *accept_len, double *u_exit, double *u_bonus)
+{
+    if (V < 1 || !(T >= 0.0)) return ORC_ERR_ARG;
+    int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int st = orc_check_tree(parent, token, n, V, depth);
+    if (st) { free(depth); return st; }
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    int32_t *mark = (int32_t *)calloc((size_t)V, sizeof(int32_t));
+
+    /* Alg. 1 lines 3-7: node-local quantities, then P by depth order.  Node
+     * indices are parent-before-child, so one pass in index order visits every
+     * parent before its children. */
+    P[0] = 1.0;
+    pedge[0] = 1.0;
+    for (int v = 0; v < n; ++v) {
+        st = orc_row_probs(z + (int64_t)v * V, V, T, p);
+        if (st) break;
+        orc_mark_children(parent, token, n, v, mark);
+        double res = 0.0;
+        for (int64_t a = 0; a < V; ++a)
+            if (!mark[a]) res += p[a];
+        orc_unmark_children(parent, token, n, v, mark);
+        rho[v] = res;
+        for (int u = v + 1; u < n; ++u)
+            if (parent[u] == v) {
+                pedge[u] = p[token[u]];
+                P[u] = P[v] * pedge[u];
+            }
+        w[v] = P[v] * rho[v];
+    }
+    if (st) { free(mark); free(p); free(depth); return st; }
+    double cp = 0.0;
+    for (int u = 1; u < n; ++u) cp += P[u];
+    *coverage = cp;
+
+    /* Alg. 1 line 8: V ~ Categorical(w), inverse CDF in node order. */
+    double wsum = 0.0;
+    for (int v = 0; v < n; ++v) wsum += w[v];
+    double u1 = orc_uniform(seed, tree, 0, 0);
+    double thr = u1 * wsum, cum = 0.0;
+    int ex = -1;
+    for (int v = 0; v < n; ++v) {
+        cum += w[v];
+        if (cum > thr) { ex = v; break; }
+    }
+    if (ex < 0) { /* rounding left the last item short: take the last node with mass */
+        for (int v = n - 1; v >= 0; --v)
+            if (w[v] > 0.0) { ex = v; break; }
+    }
+
+    /* Alg. 1 line 9: Y ~ p_V at a leaf, else the residual law of Eq. 7
+     * (children's tokens removed, renormalised by rho(V)). */
+    st = orc_row_probs(z + (int64_t)ex * V, V, T, p);
+    double u2 = orc_uniform(seed, tree, 0, 1);
+    double thr2 = u2 * rho[ex], cum2 = 0.0;
+    int64_t y = -1, last_pos = -1;
+    orc_mark_children(parent, token, n, ex, mark);
+    for (int64_t a = 0; a < V; ++a) {
+        if (mark[a]) continue;
+        if (p[a] > 0.0) last_pos = a;
+        cum2 += p[a];
+        if (cum2 > thr2) { y = a; break; }
+    }
+    orc_unmark_children(parent, token, n, ex, mark);
+    if (y < 0) y = last_pos;
+
+    *exit_node = ex;
+    *bonus = (int32_t)y;
+    *accept_len = depth[ex] + 1;
+    *u_exit = u1;
+    *u_bonus = u2;
+    free(mark);
+    free(p);
+    free(depth);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Predraw-and-follow [EXIT Sec. 2, App. A.4.1]: draw R_v ~ p_v at every     */
+/* node (inverse CDF over token ids, uniform stream 2 at node v); walk from  */
+/* the root into the child whose token equals R_v; exit at the first node    */
+/* with no matching child and return R_v as the bonus token.                 */
+/*   draws: [n] the per-node draws R_v.                                      */
+/* ------------------------------------------------------------------------ */
+int orc_predraw(const double *z, const int32_t *parent, const int32_t *token, int n, int64_t V,
+                double T, uint64_t seed, uint64_t tree, int32_t *draws, int32_t *exit_node,
+                int32_t *bonus, int32_t *accept_len)
+{
+    if (V < 1 || !(T >= 0.0)) return ORC_ERR_ARG;
+    int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int st = orc_check_tree(parent, token, n, V, depth);
+    if (st) { free(depth); return st; }
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    int32_t *mark = (int32_t *)calloc((size_t)V, sizeof(int32_t));
+    for (int v = 0; v < n && !st; ++v) {
+        st = orc_row_probs(z + (int64_t)v * V, V, T, p);
+        if (st) break;
+        double tot = 0.0;
+        for (int64_t a = 0; a < V; ++a) tot += p[a];
+        double thr = orc_uniform(seed, tree, (uint64_t)v, 2) * tot, cum = 0.0;
+        int64_t r = -1, last_pos = -1;
+        for (int64_t a = 0; a < V; ++a) {
+            if (p[a] > 0.0) last_pos = a;
+            cum += p[a];
+            if (cum > thr) { r = a; break; }
+        }
+        draws[v] = (int32_t)(r >= 0 ? r : last_pos);
+    }
+    if (!st) {
+        int v = 0;
+        for (;;) {
+            orc_mark_children(parent, token, n, v, mark);
+            int c = mark[draws[v]];
+            orc_unmark_children(parent, token, n, v, mark);
+            if (!c) break;
+            v = c;
+        }
+        *exit_node = v;
+        *bonus = draws[v];
+        *accept_len = depth[v] + 1;
+    }
+    free(mark);
+    free(p);
+    free(depth);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Repeated draws for the law tests: draw i uses tree index first_tree + i,  */
+/* so every draw has its own uniforms on the same tree and logits.           */
+/* ------------------------------------------------------------------------ */
+int orc_tev_sample_many(const double *z, const int32_t *parent, const int32_t *token, int n,
+                        int64_t V, double T, uint64_t seed, uint64_t first_tree, int64_t n_draws,
+                        int32_t *exit_out, int32_t *bonus_out)
+{
+    double *P = (double *)malloc(sizeof(double) * (size_t)n * 4);
+    double cov, ue, ub;
+    int32_t al;
+    int st = ORC_OK;
+    for (int64_t i = 0; i < n_draws && !st; ++i)
+        st = orc_tev(z, parent, token, n, V, T, seed, first_tree + (uint64_t)i, P, P + n, P + 2 * n,
+                     P + 3 * n, &cov, exit_out + i, bonus_out + i, &al, &ue, &ub);
+    free(P);
+    return st;
+}
+
+int orc_predraw_sample_many(const double *z, const int32_t *parent, const int32_t *token, int n,
+                            int64_t V, double T, uint64_t seed, uint64_t first_tree,
+                            int64_t n_draws, int32_t *exit_out, int32_t *bonus_out)
+{
+    int32_t *draws = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int32_t al;
+    int st = ORC_OK;
+    for (int64_t i = 0; i < n_draws && !st; ++i)
+        st = orc_predraw(z, parent, token, n, V, T, seed, first_tree + (uint64_t)i, draws,
+                         exit_out + i, bonus_out + i, &al);
+    free(draws);
+    return st;
+}

@@ -1,0 +1,601 @@
+"""Pins for the float64 oracle: each check compares it with something other
+than itself -- a library routine, brute force on tiny inputs, a closed form
+the pages print, or a fixture worked by hand from the definitions.
+
+Page titles cited below:
+  [EXIT] Where Draft Trees Lose Target Mass: Exit-Guided Speculative Decoding
+  [CAST] CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters
+  [MFD]  Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
+         Speculative Decoding
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# helpers written independently of the oracle
+# --------------------------------------------------------------------------
+def children_of(parent, n):
+    ch = {v: [] for v in range(n)}
+    for u in range(1, n):
+        ch[int(parent[u])].append(u)
+    return ch
+
+
+def depths_of(parent, n):
+    d = [0] * n
+    for u in range(1, n):
+        d[u] = d[int(parent[u])] + 1
+    return d
+
+
+def probs_library(z, T):
+    """p_v = softmax(z/T) via scipy, or one-hot at the lowest arg-max at T=0."""
+    z = np.asarray(z, dtype=np.float64)
+    if T == 0:
+        p = np.zeros_like(z)
+        p[int(np.argmax(z))] = 1.0  # numpy argmax returns the first maximum
+        return p
+    return scipy.special.softmax(z / T)
+
+
+def brute_force_continuations(z, parent, token, n, T):
+    """Enumerate every target continuation through the tree: the joint law of
+    (exit node, next token) and the reach probability of every node."""
+    ch = children_of(parent, n)
+    probs = [probs_library(z[v], T) for v in range(n)]
+    joint = np.zeros((n, z.shape[1]))
+    reach = np.zeros(n)
+
+    def walk(v, q):
+        reach[v] += q
+        kids = {int(token[u]): u for u in ch[v]}
+        for a in range(z.shape[1]):
+            pa = q * probs[v][a]
+            if a in kids:
+                walk(kids[a], pa)
+            else:
+                joint[v, a] += pa
+
+    walk(0, 1.0)
+    return joint, reach, probs
+
+
+def tiny_tree(orc, seed, B=8, k=4, T_d=1.0):
+    dr = synth.tiny_drafter(seed).numpy().astype(np.float64)
+    lse, tid, tlq = orc.drafter_stats(dr, T_d, k)
+    tr = orc.build_tree(tid, tlq, B)
+    n = tr["n_nodes"]
+    tgt = synth.tiny_target(synth.tiny_drafter(seed), tr["depth"][:n], seed + 7).numpy()
+    return dr, tr, n, tgt.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Philox4x64-10 and the uniforms
+# --------------------------------------------------------------------------
+def _numpy_philox_block(counter, key):
+    """numpy's Philox (4x64, 10 rounds) pre-increments its 256-bit counter, so
+    the block at counter c is produced from a generator set to c - 1."""
+    c = sum(int(x) << (64 * i) for i, x in enumerate(counter))
+    c = (c - 1) % (1 << 256)
+    words = np.array([(c >> (64 * i)) & ((1 << 64) - 1) for i in range(4)], dtype=np.uint64)
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=words)
+    return bg.random_raw(4).astype(np.uint64)
+
+
+@pytest.mark.parametrize("counter,key", [
+    ((0, 0, 0, 0), (0, 0)),
+    ((1, 0, 0, 0), (0, 0)),
+    ((5, 6, 7, 8), (123456789, 987654321)),
+    ((31, 512, 2, 0), (20261202, 0)),
+    ((2**64 - 1, 2**64 - 1, 3, 0), (2**64 - 1, 17)),
+])
+def test_philox_matches_numpy(orc, counter, key):
+    ours = orc.philox4x64_10(counter, key)
+    ref = _numpy_philox_block(counter, key)
+    assert [int(x) for x in ours] == [int(x) for x in ref]
+
+
+def test_uniform_grid_and_uniformity(orc):
+    us = np.array([orc.uniform(99, t, 0, 0) for t in range(40000)])
+    assert us.min() >= 0.0 and us.max() < 1.0
+    assert np.all(us * 2**24 == np.floor(us * 2**24))
+    # the stream and node fields change the draw
+    assert orc.uniform(1, 2, 3, 0) != orc.uniform(1, 2, 3, 1)
+    assert orc.uniform(1, 2, 3, 0) != orc.uniform(1, 2, 4, 0)
+    hist = np.histogram(us, bins=64, range=(0, 1))[0]
+    assert scipy.stats.chisquare(hist).pvalue > 1e-4
+    # lag-1 correlation near zero
+    assert abs(np.corrcoef(us[:-1], us[1:])[0, 1]) < 0.03
+
+
+# --------------------------------------------------------------------------
+# Drafter statistics [CAST Sec. 2 Eq. 1, App. C]
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1.0, 0.6, 2.5])
+def test_drafter_stats_vs_library(orc, T):
+    rng = np.random.default_rng(5)
+    z = np.round(rng.normal(0, 3, size=(6, 200)) * 2) / 2  # quantised: many exact ties
+    z[2, 17] = -np.inf  # a masked token
+    lse, tid, tlq = orc.drafter_stats(z, T, 8)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z / T, axis=1), rtol=0, atol=1e-12)
+    for r in range(z.shape[0]):
+        order = np.lexsort((np.arange(z.shape[1]), -z[r]))  # logit desc, id asc
+        assert list(tid[r]) == list(order[:8])
+        np.testing.assert_allclose(tlq[r], scipy.special.log_softmax(z[r] / T)[order[:8]], atol=1e-12)
+
+
+def test_drafter_stats_rejects_nonfinite(orc):
+    z = np.zeros((2, 16))
+    z[1, 3] = np.nan
+    with pytest.raises(orc.OracleError) as e:
+        orc.drafter_stats(z, 1.0, 4)
+    assert e.value.code == orc.ERR_NONFINITE
+
+
+# --------------------------------------------------------------------------
+# Builder [CAST Thm. 1, App. C; MFD Sec. 4.3, App. B Prop. 6]
+# --------------------------------------------------------------------------
+def exhaustive_topB(top_id, top_logq, B):
+    """Enumerate every prefix of every mode's capped universe, score it, keep
+    each distinct token sequence at its best entry in the order (score desc,
+    depth asc, mode asc, rank sequence asc), and return the first B."""
+    K, L, k = top_id.shape
+    entries = []
+    for m in range(K):
+        for d in range(1, L + 1):
+            for ranks in itertools.product(range(k), repeat=d):
+                s = 0.0
+                for j, r in enumerate(ranks):
+                    s = s + top_logq[m, j, r]  # same association as a path sum
+                if s == -np.inf:
+                    continue
+                toks = tuple(int(top_id[m, j, r]) for j, r in enumerate(ranks))
+                entries.append((-s, d, m, ranks, toks, s))
+    entries.sort(key=lambda e: (e[0], e[1], e[2], e[3]))
+    seen, out = set(), []
+    for e in entries:
+        if e[4] in seen:
+            continue
+        seen.add(e[4])
+        out.append(e)
+        if len(out) == B:
+            break
+    return out
+
+
+def tree_sequences(tr):
+    n = tr["n_nodes"]
+    seqs = {0: ()}
+    for u in range(1, n):
+        seqs[u] = seqs[int(tr["parent"][u])] + (int(tr["token"][u]),)
+    return [seqs[u] for u in range(n)]
+
+
+def _random_lists(rng, K, L, k, V, quantise=False):
+    tid = np.zeros((K, L, k), dtype=np.int32)
+    tlq = np.zeros((K, L, k))
+    for m in range(K):
+        for j in range(L):
+            z = rng.normal(0, 2, size=V)
+            if quantise:
+                z = np.round(z * 2) / 2
+            lq = scipy.special.log_softmax(z)
+            order = np.lexsort((np.arange(V), -z))[:k]
+            tid[m, j], tlq[m, j] = order, lq[order]
+    return tid, tlq
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_builder_single_mode_equals_exhaustive(orc, seed):
+    rng = np.random.default_rng(seed)
+    L, k, V = 4, 4, 12
+    tid, tlq = _random_lists(rng, 1, L, k, V, quantise=(seed % 2 == 1))
+    B = int(rng.integers(1, 60))
+    tr = orc.build_tree(tid, tlq, B)
+    ref = exhaustive_topB(tid, tlq, B)
+    seqs = tree_sequences(tr)
+    assert tr["n_nodes"] == len(ref) + 1
+    assert seqs[1:] == [e[4] for e in ref]
+    np.testing.assert_array_equal(tr["score"][1:tr["n_nodes"]], [e[5] for e in ref])
+    # prefix-closed [CAST Thm. 1]: every parent precedes its child
+    for u in range(1, tr["n_nodes"]):
+        assert 0 <= tr["parent"][u] < u
+        assert tr["depth"][u] == tr["depth"][tr["parent"][u]] + 1
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_push_rules_agree(orc, seed):
+    """Sibling+first-child pushes [MFD App. B] and push-all-k-children
+    [CAST App. C] pop the same prefixes in the same order."""
+    rng = np.random.default_rng(100 + seed)
+    K = 1 + seed % 3
+    tid, tlq = _random_lists(rng, K, 5, 6, 20, quantise=(seed % 2 == 0))
+    for B in (1, 7, 40, 90):
+        a = orc.build_tree(tid, tlq, B, push_rule=0)
+        b = orc.build_tree(tid, tlq, B, push_rule=1)
+        for key in ("parent", "token", "depth", "rank", "mode"):
+            np.testing.assert_array_equal(a[key], b[key])
+        np.testing.assert_array_equal(a["score"], b["score"])
+
+
+def test_mixture_equals_exhaustive_random_instances(orc):
+    """Random instances in the manner of [MFD App. B] (up to 8 modes, small
+    positions and vocabularies, budgets up to 40, cap = whole vocabulary so
+    Prop. 6 is exact): the merged heap returns the B best distinct prefixes
+    under the best-mode score."""
+    rng = np.random.default_rng(2026)
+    for inst in range(120):
+        K = int(rng.integers(1, 9))
+        L = int(rng.integers(1, 4))
+        V = int(rng.integers(2, 6))
+        tid, tlq = _random_lists(rng, K, L, V, V, quantise=(inst % 3 == 0))
+        B = int(rng.integers(1, 41))
+        tr = orc.build_tree(tid, tlq, B)
+        ref = exhaustive_topB(tid, tlq, B)
+        assert tree_sequences(tr)[1:] == [e[4] for e in ref], inst
+        np.testing.assert_array_equal(tr["score"][1:tr["n_nodes"]], [e[5] for e in ref])
+    # two instances at the page's full size: 5 positions, 10 tokens each
+    for inst in range(2):
+        K = 2 + inst
+        tid, tlq = _random_lists(rng, K, 5, 10, 10)
+        tr = orc.build_tree(tid, tlq, 40)
+        ref = exhaustive_topB(tid, tlq, 40)
+        assert tree_sequences(tr)[1:] == [e[4] for e in ref]
+
+
+def test_mixture_single_mode_is_ddtree(orc):
+    """With K = 1 the merged heap is DDTree's builder [MFD App. B Prop. 6]:
+    check the K = 1 call against the mixture call with the one mode duplicated
+    under a second copy -- the duplicate reuses every node."""
+    rng = np.random.default_rng(7)
+    tid, tlq = _random_lists(rng, 1, 6, 8, 40)
+    single = orc.build_tree(tid, tlq, 64)
+    dup = orc.build_tree(np.concatenate([tid, tid]), np.concatenate([tlq, tlq]), 64)
+    for key in ("parent", "token", "depth", "score"):
+        np.testing.assert_array_equal(single[key], dup[key])
+    assert np.all(dup["mode"][1:dup["n_nodes"]] == 0)
+
+
+def test_mixture_is_union_of_mode_trees(orc):
+    """[MFD Sec. 3.4 Prop. 4]: without ties the mixture tree is the union of
+    the per-mode top-n_k trees, n_k = #{v : log Q_k(v) >= theta}."""
+    rng = np.random.default_rng(11)
+    for _ in range(10):
+        K = int(rng.integers(2, 6))
+        tid, tlq = _random_lists(rng, K, 3, 5, 5)
+        B = int(rng.integers(5, 40))
+        tr = orc.build_tree(tid, tlq, B)
+        n = tr["n_nodes"]
+        theta = tr["score"][n - 1]
+        union = set()
+        for m in range(K):
+            one = exhaustive_topB(tid[m:m + 1], tlq[m:m + 1], 10**9)
+            nk = sum(1 for e in one if e[5] >= theta)
+            sub = orc.build_tree(tid[m:m + 1], tlq[m:m + 1], nk)
+            union |= set(tree_sequences(sub)[1:])
+        assert union == set(tree_sequences(tr)[1:])
+
+
+def test_product_tree_holds_chimeras(orc):
+    """[MFD Sec. 3.2 Lemma 1]: if a product's top-B tree (no ties) holds two
+    depth-d prefixes differing in m positions, it holds at least 2^(m-1) of
+    their splices."""
+    rng = np.random.default_rng(3)
+    for _ in range(6):
+        tid, tlq = _random_lists(rng, 1, 4, 4, 4)
+        tr = orc.build_tree(tid, tlq, 60)
+        seqs = set(tree_sequences(tr)[1:])
+        by_depth = {}
+        for s in seqs:
+            by_depth.setdefault(len(s), []).append(s)
+        for d, group in by_depth.items():
+            for v, w in itertools.combinations(group, 2):
+                diff = [i for i in range(d) if v[i] != w[i]]
+                m = len(diff)
+                splices = set()
+                for mask in range(1 << m):
+                    u = list(w)
+                    for b, i in enumerate(diff):
+                        if mask >> b & 1:
+                            u[i] = v[i]
+                    splices.add(tuple(u))
+                assert len(splices & seqs) >= 2 ** (m - 1)
+
+
+def _separation_lists(futures, modes_on, k, D):
+    """Point-mass modes: mode m puts all mass on future modes_on[m]."""
+    K = len(modes_on)
+    tid = np.zeros((K, D, k), dtype=np.int32)
+    tlq = np.full((K, D, k), -np.inf)
+    for m, f in enumerate(modes_on):
+        for i in range(D):
+            others = [t for t in range(k + len(futures)) if t != futures[f][i]][:k - 1]
+            tid[m, i] = [futures[f][i]] + others
+            tlq[m, i, 0] = 0.0
+    return tid, tlq
+
+
+def _acceptance(tr, futures, mu):
+    """E[alpha] = sum over tree nodes of the target prefix mass [MFD Prop. 1]."""
+    acc = 0.0
+    for s in tree_sequences(tr)[1:]:
+        for f, m in zip(futures, mu):
+            if tuple(f[:len(s)]) == s:
+                acc += m
+    return acc
+
+
+def test_separation_model_closed_forms(orc):
+    cases = json.load(open(os.path.join(GOLDEN, "mfd_separation.json")))["cases"]
+    # case 1: M=2, D=15, B=256
+    c = cases[0]
+    M, D, B = c["M"], c["D"], c["B"]
+    futures = [[2 * i for i in range(D)], [2 * i + 1 for i in range(D)]]
+    mix = orc.build_tree(*_separation_lists(futures, [0, 1], 2, D), B)
+    assert _acceptance(mix, futures, [0.5, 0.5]) == pytest.approx(c["optimal"])
+    rng = np.random.default_rng(1)
+    for _ in range(20):  # random products over the two futures' tokens, no ties
+        tid = np.zeros((1, D, 2), dtype=np.int32)
+        tlq = np.zeros((1, D, 2))
+        for i in range(D):
+            a = rng.uniform(0.05, 0.95)
+            pair = sorted([(a, futures[0][i]), (1 - a, futures[1][i])], reverse=True)
+            tid[0, i] = [pair[0][1], pair[1][1]]
+            tlq[0, i] = [math.log(pair[0][0]), math.log(pair[1][0])]
+        prod = orc.build_tree(tid, tlq, B)
+        assert _acceptance(prod, futures, [0.5, 0.5]) <= c["product_bound"] + 1e-12
+        assert D / M + (1 - 1 / M) * (1 + math.log2(B)) == pytest.approx(c["product_bound"])
+    # case 2: unequal futures
+    c = cases[1]
+    D, B, mu = c["D"], c["B"], c["mu"]
+    futures = [[2 * i for i in range(D)], [2 * i + 1 for i in range(D)]]
+    mix = orc.build_tree(*_separation_lists(futures, [0, 1], 2, D), B)
+    assert _acceptance(mix, futures, mu) == pytest.approx(c["uniform_prior_mixture"])
+    eps = 1e-3
+    tid = np.zeros((1, D, 2), dtype=np.int32)
+    tlq = np.zeros((1, D, 2))
+    for i in range(D):
+        tid[0, i] = [futures[0][i], futures[1][i]]
+        tlq[0, i] = [math.log(1 - eps), math.log(eps)]
+    prod = orc.build_tree(tid, tlq, B)
+    assert _acceptance(prod, futures, mu) == pytest.approx(c["product_on_first"])
+    # case 3: point-mass mixture accepts min(B, K D)/M
+    c = cases[2]
+    M, K, D = c["M"], c["K"], c["D"]
+    futures = [[M * i + f for i in range(D)] for f in range(M)]
+    for B in c["B_list"]:
+        mix = orc.build_tree(*_separation_lists(futures, list(range(K)), 2, D), B)
+        assert _acceptance(mix, futures, [1 / M] * M) == pytest.approx(min(B, K * D) / M)
+        assert mix["n_nodes"] == min(B, K * D) + 1  # zero-mass prefixes are never kept
+
+
+# --------------------------------------------------------------------------
+# Ancestor mask and position ids [CAST App. C, Lemma 1]
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(4))
+def test_tree_mask_vs_ancestor_sets(orc, seed):
+    rng = np.random.default_rng(seed)
+    tid, tlq = _random_lists(rng, 1, 6, 4, 10)
+    B = 40
+    tr = orc.build_tree(tid, tlq, B)
+    n = tr["n_nodes"]
+    P = int(rng.integers(0, 50))
+    bits, pos, add = orc.tree_mask(tr["parent"], n, B, P, with_additive=True)
+    dep = depths_of(tr["parent"], n)
+    for v in range(B + 1):
+        got = {u for u in range(B + 1) if bits[v, u // 32] >> (u % 32) & 1}
+        if v < n:
+            anc, u = set(), v
+            while u >= 0:
+                anc.add(u)
+                u = int(tr["parent"][u])
+            assert got == anc and len(got) == dep[v] + 1
+            assert pos[v] == P + dep[v]
+        else:
+            assert got == {v} and pos[v] == P
+        assert np.all(add[v, :P] == 0.0)
+        for u in range(B + 1):
+            assert add[v, P + u] == (0.0 if u in got else -np.inf)
+    # transitively closed: an ancestor's ancestors are ancestors
+    for v in range(n):
+        for u in range(n):
+            if bits[v, u // 32] >> (u % 32) & 1:
+                for x in range(n):
+                    if bits[u, x // 32] >> (x % 32) & 1:
+                        assert bits[v, x // 32] >> (x % 32) & 1
+
+
+# --------------------------------------------------------------------------
+# TEV [EXIT Sec. 3, App. A, App. B Algorithm 1]
+# --------------------------------------------------------------------------
+def test_tev_hand_fixture(orc):
+    g = json.load(open(os.path.join(GOLDEN, "tev_hand_v3.json")))
+    par, tok = g["tree"]["parent"], g["tree"]["token"]
+    z = np.log(np.array(g["p"]))
+    r = orc.tev(z, par, tok, 4, 1.0, seed=1)
+    e = g["expected"]
+    np.testing.assert_allclose(r["P"], e["P"], atol=1e-14)
+    np.testing.assert_allclose(r["rho"], e["rho"], atol=1e-14)
+    np.testing.assert_allclose(r["w"], e["w"], atol=1e-14)
+    assert r["coverage"] == pytest.approx(e["coverage"], abs=1e-14)
+    # the residual law the bonus is drawn from, by exhaustive draws over the
+    # uniform grid is too costly; check it through the brute-force joint law
+    joint, _, _ = brute_force_continuations(z, par, tok, 4, 1.0)
+    for v in range(4):
+        np.testing.assert_allclose(joint[v] / joint[v].sum(), e["residual"][v], atol=1e-14)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6, 0.0])
+@pytest.mark.parametrize("seed", range(5))
+def test_tev_exit_law_by_brute_force(orc, T, seed):
+    """Enumerating target continuations [EXIT Lemma 1, Eq. 5-6, 24-29]."""
+    _, tr, n, tgt = tiny_tree(orc, 1000 + seed)
+    par, tok = tr["parent"], tr["token"]
+    r = orc.tev(tgt, par, tok, n, T, seed=seed)
+    joint, reach, _ = brute_force_continuations(tgt, par, tok, n, T)
+    dep = depths_of(par, n)
+    ch = children_of(par, n)
+    np.testing.assert_allclose(r["w"], joint.sum(axis=1), atol=1e-13)   # Lemma 1
+    assert r["w"].sum() == pytest.approx(1.0, abs=1e-13)                  # Eq. 5
+    np.testing.assert_allclose(r["P"], reach, atol=1e-13)                # Eq. 2, 20
+    exp_len = sum(joint[v].sum() * (dep[v] + 1) for v in range(n))
+    assert exp_len == pytest.approx(1.0 + r["coverage"], abs=1e-12)       # Thm. 1 at equality
+    assert r["coverage"] == pytest.approx(sum(r["w"][v] * dep[v] for v in range(n)), abs=1e-12)
+    for v in range(n):  # local conservation, Eq. 24-25
+        assert r["w"][v] + sum(r["P"][u] for u in ch[v]) == pytest.approx(r["P"][v], abs=1e-13)
+        # Eq. 4 directly: rho = 1 - sum of child probabilities
+        assert r["rho"][v] == pytest.approx(1.0 - sum(r["pedge"][u] for u in ch[v]), abs=1e-12)
+    for u in range(n):  # subtree sums, Eq. 26
+        sub = [v for v in range(n) if _in_subtree(v, u, par)]
+        assert sum(r["w"][v] for v in sub) == pytest.approx(r["P"][u], abs=1e-12)
+    assert r["accept_len"] == dep[r["exit_node"]] + 1
+
+
+def _in_subtree(v, u, par):
+    while v >= 0:
+        if v == u:
+            return True
+        v = int(par[v])
+    return False
+
+
+def test_one_step_coverage_gain(orc):
+    """[EXIT Eq. 12-13]: adding child (v, a) raises C_p by P(v) p_v(a); the
+    sum over the missing tokens is w(v)."""
+    _, tr, n, tgt = tiny_tree(orc, 77)
+    par, tok = list(tr["parent"][:n]), list(tr["token"][:n])
+    base = orc.tev(tgt, par, tok, n, 1.0, seed=3)
+    ch = children_of(par, n)
+    v = max(range(n), key=lambda x: base["w"][x])
+    taken = {tok[u] for u in ch[v]}
+    gains = 0.0
+    p_v = probs_library(tgt[v], 1.0)
+    for a in range(tgt.shape[1]):
+        if a in taken:
+            continue
+        z2 = np.vstack([tgt, tgt[:1]])  # the new node's own row does not enter C_p
+        r2 = orc.tev(z2, par + [v], tok + [a], n + 1, 1.0, seed=3)
+        gain = r2["coverage"] - base["coverage"]
+        assert gain == pytest.approx(base["P"][v] * p_v[a], abs=1e-13)
+        gains += gain
+    assert gains == pytest.approx(base["w"][v], abs=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_greedy_is_argmax_walk(orc, seed):
+    """T = 0 reduces to following the target arg-max [CAST Sec. 2, Sec. 3.4]."""
+    _, tr, n, tgt = tiny_tree(orc, 500 + seed)
+    par, tok = tr["parent"], tr["token"]
+    ch = children_of(par, n)
+    v = 0
+    while True:
+        a = int(np.argmax(tgt[v]))
+        nxt = [u for u in ch[v] if int(tok[u]) == a]
+        if not nxt:
+            break
+        v = nxt[0]
+    for s in range(3):
+        r = orc.tev(tgt, par, tok, n, 0.0, seed=s)
+        assert (r["exit_node"], r["bonus"]) == (v, int(np.argmax(tgt[v])))
+        d = orc.predraw(tgt, par, tok, n, 0.0, seed=s)
+        assert (d["exit_node"], d["bonus"]) == (v, int(np.argmax(tgt[v])))
+
+
+def test_tev_and_predraw_share_the_exact_law(orc):
+    """Chi-square over 10^6 seeded draws of each sampler against the exact
+    joint law P(v) rho(v) p_v^res(a) from brute force [EXIT Thm. 1, Cor. 1,
+    Eq. 10, 56], and against each other; acceptance frequency = P(u) [Eq. 58]."""
+    _, tr, n, tgt = tiny_tree(orc, 4242)
+    par, tok = tr["parent"], tr["token"]
+    T = 1.0
+    joint, _, _ = brute_force_continuations(tgt, par, tok, n, T)
+    N = 1_000_000
+    draws = {}
+    for kind in ("tev", "predraw"):
+        ex, bo = orc.sample_many(kind, tgt, par, tok, n, T, seed=31337, n_draws=N)
+        draws[kind] = (ex, bo)
+        cells = ex.astype(np.int64) * tgt.shape[1] + bo
+        obs = np.bincount(cells, minlength=joint.size).astype(float)
+        exp = joint.ravel() * N
+        assert obs[exp == 0].sum() == 0, kind  # zero-mass events never happen
+        keep = exp >= 5
+        rest_o, rest_e = obs[~keep].sum(), exp[~keep].sum()
+        o = np.append(obs[keep], rest_o)
+        e = np.append(exp[keep], rest_e)
+        assert scipy.stats.chisquare(o, e * o.sum() / e.sum()).pvalue > 1e-4, kind
+        # exit-node law alone
+        eo = np.bincount(ex, minlength=n).astype(float)
+        ew = joint.sum(axis=1) * N
+        k2 = ew > 0
+        assert scipy.stats.chisquare(eo[k2], ew[k2] * eo[k2].sum() / ew[k2].sum()).pvalue > 1e-4
+    # the two samplers against each other (two-sample chi-square on exit nodes)
+    a = np.bincount(draws["tev"][0], minlength=n)
+    b = np.bincount(draws["predraw"][0], minlength=n)
+    m = (a + b) > 0
+    assert scipy.stats.chi2_contingency(np.vstack([a[m], b[m]]))[1] > 1e-4
+    # acceptance frequency of every node equals P(u)
+    r = orc.tev(tgt, par, tok, n, T, seed=0)
+    ex = draws["tev"][0]
+    for u in range(1, n):
+        sub = np.array([_in_subtree(v, u, par) for v in range(n)])
+        f = sub[ex].mean()
+        sd = math.sqrt(r["P"][u] * (1 - r["P"][u]) / N) + 1e-12
+        assert abs(f - r["P"][u]) < 5 * sd
+
+
+def test_tev_rejects_bad_trees(orc):
+    z = np.zeros((3, 8))
+    with pytest.raises(orc.OracleError):
+        orc.tev(z, [-1, 0, 0], [-1, 2, 2], 3, 1.0, 0)  # sibling tokens repeat
+    with pytest.raises(orc.OracleError):
+        orc.tev(z, [-1, 2, 0], [-1, 1, 2], 3, 1.0, 0)  # parent after child
+    with pytest.raises(orc.OracleError):
+        orc.tev(z, [-1, 0, 0], [-1, 1, 8], 3, 1.0, 0)  # token out of range
+
+
+def _numpy_uniform(seed, tree, node, stream):
+    """The uniform of the stated reading, from numpy's Philox: the top 24 bits
+    of the first output word of counter (tree, node, stream, 0), key (seed, 0)."""
+    x0 = int(_numpy_philox_block((tree, node, stream, 0), (seed, 0))[0])
+    return (x0 >> 40) * 2.0**-24
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_draws_are_inverse_cdf_of_the_stated_uniforms(orc, T):
+    """The reading of Alg. 1's two draws [EXIT App. B]: inverse CDF over nodes
+    in index order (exit) and over non-child token ids ascending (bonus), with
+    the uniforms of the counter layout above.  Exit law and residual law come
+    from brute force, the uniforms from numpy -- nothing from the oracle."""
+    _, tr, n, tgt = tiny_tree(orc, 9090)
+    par, tok = tr["parent"], tr["token"]
+    joint, _, probs = brute_force_continuations(tgt, par, tok, n, T)
+    w = joint.sum(axis=1)
+    ch = children_of(par, n)
+    for tree in range(300):
+        u1 = _numpy_uniform(5, tree, 0, 0)
+        u2 = _numpy_uniform(5, tree, 0, 1)
+        cw = np.cumsum(w)
+        ex = int(np.argmax(cw > u1 * cw[-1]))
+        kids = {int(tok[u]) for u in ch[ex]}
+        res = np.array([0.0 if a in kids else probs[ex][a] for a in range(tgt.shape[1])])
+        cr = np.cumsum(res)
+        bo = int(np.argmax(cr > u2 * cr[-1]))
+        r = orc.tev(tgt, par, tok, n, T, seed=5, tree=tree)
+        assert (r["exit_node"], r["bonus"]) == (ex, bo), tree
+        # predraw: R_v is the inverse CDF of p_v at the node's own uniform
+        d = orc.predraw(tgt, par, tok, n, T, seed=5, tree=tree)
+        for v in range(n):
+            cp = np.cumsum(probs[v])
+            assert d["draws"][v] == int(np.argmax(cp > _numpy_uniform(5, tree, v, 2) * cp[-1]))
