@@ -115,14 +115,14 @@ int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int
         double s = 0.0;
         for (int64_t a = 0; a < V; ++a) s += exp((row[a] - m) / temp);
         lse[r] = m / temp + log(s);
-        /* top-k by repeated selection: the best remaining token each time */
+        /* top-k by repeated selection: rank i is the best token that comes
+         * after rank i-1 in the order (logit desc, id asc) */
         for (int i = 0; i < k; ++i) {
             int64_t best = -1;
+            int64_t prev = i > 0 ? top_id[r * k + i - 1] : -1;
             for (int64_t a = 0; a < V; ++a) {
-                int taken = 0;
-                for (int j = 0; j < i; ++j)
-                    if (top_id[r * k + j] == (int32_t)a) { taken = 1; break; }
-                if (taken) continue;
+                if (prev >= 0 && !(row[a] < row[prev] || (row[a] == row[prev] && a > prev)))
+                    continue; /* a is rank i-1 or ranked before it */
                 if (best < 0 || row[a] > row[best]) best = a;  /* ties keep the lower id */
             }
             top_id[r * k + i] = (int32_t)best;
