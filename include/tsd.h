@@ -1,0 +1,192 @@
+/*
+ * tsd.h -- C ABI of the GB300 (sm_103a) library for the data-parallel hot path
+ * of bounded-tree speculative decoding.
+ *
+ * Pages the operations restate:
+ *   [EXIT] "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
+ *          Decoding": Sec. 3 Eq. 1-2, Sec. 3.1 Eq. 4, Eq. 6-7, App. A.4.1,
+ *          App. B Algorithm 1.
+ *   [CAST] "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters":
+ *          Sec. 2 Eq. 1, Thm. 1, App. C ("Candidate construction",
+ *          "Packed verification"), App. B Lemma 1.
+ *   [MFD]  "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
+ *          Speculative Decoding": Sec. 3.4 Eq. 2, Prop. 4, Sec. 4.3,
+ *          App. B "Merged heap", Prop. 6.
+ *
+ * Conventions shared by every entry point:
+ *   - Every array argument is DEVICE memory owned by the caller, contiguous and
+ *     row-major in the shape given.  The library allocates nothing and keeps
+ *     no state between calls.
+ *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
+ *     host before anything is launched and returned at once; nothing is
+ *     written in that case.  TSD_ERR_CUDA reports a launch failure.
+ *   - Errors in the data of one tree (a malformed tree, a NaN or +inf logit,
+ *     a row without mass) are written to status[tree] on the device and can be
+ *     read after the stream synchronises; that tree's outputs are then filled
+ *     with -1 / 0 and the other trees are unaffected.  No kernel traps.
+ *   - A tree has n_nodes[t] <= B+1 nodes.  Node 0 is the root (the pending
+ *     root token of [CAST] Sec. 2); nodes are numbered parent-before-child
+ *     (parent[0] = -1, 0 <= parent[u] < u), which is the builder's pop order.
+ *     Sibling tokens are distinct.  Slots past n_nodes are ignored on input.
+ *   - Logits rows follow node order: target_logits[t][v] is the target's
+ *     next-token logits at node v.  bf16 or fp32; rows need not be aligned,
+ *     but 16-byte aligned rows with V a multiple of 8 (bf16) or 4 (fp32) take
+ *     the vectorised path.
+ *   - `workspace` is device scratch of at least tsd_workspace_size(...) bytes,
+ *     16-byte aligned.  Its contents on entry do not matter.
+ *   - Randomness: the seed is the only source of the auxiliary randomness of
+ *     [EXIT] Sec. 3.  Uniforms are Philox4x64-10 (Salmon et al., SC'11) with
+ *     counter (tree, node, stream, 0) and key (seed, 0), u = (x0 >> 40) 2^-24;
+ *     stream 0 = TEV exit draw, 1 = TEV bonus draw, 2 = predraw at `node`.
+ */
+#ifndef TSD_H
+#define TSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TSD_OK = 0,
+    TSD_ERR_INVALID_ARG = 1, /* a null pointer, a size or option out of range */
+    TSD_ERR_CUDA = 2,        /* a kernel launch failed */
+    TSD_ERR_WORKSPACE = 3,   /* ws_bytes below tsd_workspace_size, or workspace misaligned */
+    TSD_ERR_BAD_TREE = 4,    /* per tree: parent/token/n_nodes violate the conventions */
+    TSD_ERR_NONFINITE = 5,   /* per tree: a NaN or +inf logit, or a row with no mass */
+    TSD_ERR_TIMEOUT = 6      /* reserved: no kernel of this library waits on another */
+} tsd_status;
+
+typedef enum { TSD_BF16 = 0, TSD_F32 = 1 } tsd_dtype;
+
+typedef enum {
+    TSD_OP_BUILD_TREE = 0,
+    TSD_OP_VERIFY_TEV = 1,
+    TSD_OP_VERIFY_DDTREE = 2
+} tsd_op;
+
+/* Limits checked by every entry point. */
+#define TSD_MAX_B 4095      /* non-root budget */
+#define TSD_MAX_TOPK 32     /* per-position top-k */
+#define TSD_MAX_MODES 8     /* mixture modes */
+#define TSD_MAX_L 31        /* drafter rows (= maximum depth) */
+
+/* A static English description of a status code.  Host only; never fails. */
+const char *tsd_status_string(tsd_status s);
+
+/*
+ * Bytes of workspace the operation `op` needs for these sizes (0 if the sizes
+ * are out of range).  Host only.  n_modes, L, topk matter for
+ * TSD_OP_BUILD_TREE; B matters for all three; V and dtype for all three.
+ */
+size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V, int topk, int B,
+                          tsd_dtype dtype);
+
+/*
+ * tsd_build_tree -- top-k drafter statistics and the best-first tree builder
+ * ([CAST] Sec. 2 Eq. 1, App. C "Candidate construction"; mixture: [MFD]
+ * Sec. 3.4 Eq. 2, Sec. 4.3, App. B "Merged heap", Prop. 6).
+ *
+ * drafter_logits  [n_trees][n_modes][L][V] (dtype): row (t, m, j) holds mode m's
+ *                 logits for future position j+1 of tree t.  Scores use
+ *                 log q = z/drafter_temp - logsumexp(z/drafter_temp) over the
+ *                 full V, not renormalised over the top-k.
+ * topk            tokens kept per (mode, position), ordered by (logit desc,
+ *                 id asc); 1 <= topk <= min(V, TSD_MAX_TOPK), and
+ *                 L * ceil(log2(topk)) <= 56.
+ * B               non-root node budget, 0 <= B <= TSD_MAX_B.
+ * drafter_temp    > 0.
+ * Outputs, [n_trees][B+1] (node 0 = root: parent -1, token -1, depth 0,
+ * score 0, rank -1, mode -1; slots >= n_nodes: -1 and score -inf):
+ *   parent, token, depth   the tree in pop order (parent before child);
+ *   score                  the node's best-mode score sum_j log q_{m,j}(y_j)
+ *                          (float32 copy of the float64 key);
+ *   rank, mode (nullable)  rank of the node's token in the creating mode's
+ *                          list, and that mode.
+ *   n_nodes [n_trees]      number of nodes including the root (<= B+1; fewer
+ *                          when the universe has fewer finite-score prefixes).
+ *   status  [n_trees]      TSD_OK or TSD_ERR_NONFINITE.
+ * Ties are broken by (depth asc, mode asc, rank sequence lexicographic asc).
+ * With n_modes = 1 this is DDTree's / CAST's builder.
+ */
+tsd_status tsd_build_tree(const void *drafter_logits, tsd_dtype dtype, int n_trees, int n_modes,
+                          int L, int64_t V, int topk, int B, float drafter_temp,
+                          int32_t *parent, int32_t *token, int32_t *depth, float *score,
+                          int32_t *rank, int32_t *mode, int32_t *n_nodes, int32_t *status,
+                          void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsd_tree_mask -- ancestor mask and position ids of the packed verification
+ * input ([CAST] App. C "Packed verification"; App. B Lemma 1).
+ *
+ * parent [n_trees][B+1], n_nodes [n_trees]: trees as above.
+ * prefix_len      P >= 0, the number of cached prefix tokens.
+ * anc_bits        [n_trees][B+1][W] uint32, W = (B+32)/32: bit u of row v is
+ *                 set iff node u is node v or one of its ancestors.
+ * position_ids    [n_trees][B+1]: P + depth(v).
+ * additive_mask   nullable [n_trees][B+1][mask_ld] float32, mask_ld >=
+ *                 P+B+1: columns [0, P) are 0 (the prefix is visible);
+ *                 column P+u is 0 if bit u of row v is set, else -inf.
+ *                 Columns past P+B+1 are not written.
+ * Rows v >= n_nodes are padding: only their own bit, position P.
+ * status [n_trees]: TSD_OK or TSD_ERR_BAD_TREE.
+ */
+tsd_status tsd_tree_mask(const int32_t *parent, const int32_t *n_nodes, int n_trees, int B,
+                         int prefix_len, uint32_t *anc_bits, int32_t *position_ids,
+                         float *additive_mask, int64_t mask_ld, int32_t *status,
+                         cudaStream_t stream);
+
+/*
+ * tsd_verify_tev -- Tree Exit Verification ([EXIT] App. B Algorithm 1).
+ *
+ * target_logits   [n_trees][B+1][V] (dtype); only rows v < n_nodes[t] are read.
+ * parent, token   [n_trees][B+1]; n_nodes [n_trees].
+ * temperature     T >= 0: p_v = softmax(z_v / T) ([EXIT] Eq. 1); T = 0 is
+ *                 greedy: p_v one-hot at the arg-max (lowest id on ties).
+ * seed            key of the uniforms (see the conventions above).
+ * Per tree, with P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u), rho(v) = mass of
+ * the non-child tokens under p_v, w = P rho ([EXIT] Eq. 2, 4):
+ *   exit_node [n_trees]    V ~ Categorical(w): inverse CDF over node index;
+ *   bonus_token [n_trees]  Y ~ p_V restricted to tokens that are not drafted
+ *                          children of V, renormalised ([EXIT] Eq. 7):
+ *                          inverse CDF over token id;
+ *   accept_len [n_trees]   depth(V) + 1 (accepted draft tokens + bonus).
+ *   exit_mass, prefix_prob nullable [n_trees][B+1]: w and P (0 past n_nodes);
+ *   coverage               nullable [n_trees]: C_p = sum_{u != root} P(u)
+ *                          ([EXIT] Eq. 6);
+ *   status [n_trees]       TSD_OK, TSD_ERR_BAD_TREE or TSD_ERR_NONFINITE; a
+ *                          failed tree gets exit_node = bonus = -1,
+ *                          accept_len = 0.
+ * The accepted path is the parent chain of exit_node.
+ */
+tsd_status tsd_verify_tev(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
+                          const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
+                          int64_t V, float temperature, uint64_t seed, int32_t *exit_node,
+                          int32_t *bonus_token, int32_t *accept_len, float *exit_mass,
+                          float *prefix_prob, float *coverage, int32_t *status, void *workspace,
+                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsd_verify_ddtree -- predraw-and-follow ([EXIT] Sec. 2, App. A.4.1), the
+ * verifier DDTree uses, kept as an equivalence check for TEV: it draws
+ * R_v ~ p_v at every node (inverse CDF over token id, uniform stream 2 at
+ * node v), walks from the root into the child whose token is R_v, and exits
+ * at the first node without one, returning R_v as the bonus token.
+ * Inputs as tsd_verify_tev.  Outputs: exit_node, bonus_token, accept_len
+ * [n_trees]; draws nullable [n_trees][B+1] (R_v; -1 past n_nodes); status.
+ */
+tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
+                             const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
+                             int64_t V, float temperature, uint64_t seed, int32_t *exit_node,
+                             int32_t *bonus_token, int32_t *accept_len, int32_t *draws,
+                             int32_t *status, void *workspace, size_t ws_bytes,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSD_H */

@@ -1,0 +1,98 @@
+"""Comparison helpers for the GPU parity tests: the CUDA path against the
+float64 oracle on the same seeded inputs.
+
+Tolerances (stated once, used by every GPU test):
+  * integer structure (tree, mask, greedy outputs, sampled indices given the
+    same uniforms): bit-exact, except that a sampled index may flip where the
+    oracle's CDF lies within FLIP_TOL (relative to the distribution's total) of
+    the threshold u * total; such flips are counted and reported, and the
+    tests bound their number;
+  * builder order: two prefixes may swap only when their oracle scores differ
+    by at most SCORE_TOL relative (the kernel's log-normaliser is accumulated
+    in fp32, the oracle's in fp64);
+  * probabilities, exit masses, coverage: RTOL relative; values below TINY
+    compared absolutely.
+"""
+import numpy as np
+
+RTOL = 1e-5
+TINY = 1e-30
+FLIP_TOL = 1e-6
+SCORE_TOL = 1e-6
+
+
+def close(got, want, rtol=RTOL, tiny=TINY):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    ok = (err <= rtol * np.abs(want)) | ((np.abs(want) < tiny) & (np.abs(got) < tiny * 1e3))
+    return bool(np.all(ok)), float(np.max(err / np.maximum(np.abs(want), tiny)))
+
+
+def sequences(parent, token, n):
+    seqs = [()]
+    for u in range(1, n):
+        seqs.append(seqs[int(parent[u])] + (int(token[u]),))
+    return seqs
+
+
+def prefix_score(seq, top_id, top_logq):
+    """Best-mode score of a token sequence in the capped universe (fp64), or
+    None if no mode holds it."""
+    K, L, k = top_id.shape
+    best = None
+    for m in range(K):
+        s = 0.0
+        for j, x in enumerate(seq):
+            hit = np.nonzero(top_id[m, j] == x)[0]
+            if hit.size == 0:
+                s = None
+                break
+            s = s + top_logq[m, j, hit[0]]
+        if s is not None and (best is None or s > best):
+            best = s
+    return best
+
+
+def compare_trees(gpu, ref, top_id, top_logq):
+    """Compare a GPU-built tree (numpy arrays for one tree) with the oracle's.
+    Returns the number of order flips (each within SCORE_TOL); raises on
+    anything else."""
+    n_g, n_o = int(gpu["n_nodes"]), int(ref["n_nodes"])
+    assert n_g == n_o, ("node count", n_g, n_o)
+    sg = sequences(gpu["parent"], gpu["token"], n_g)
+    so = sequences(ref["parent"], ref["token"], n_o)
+    if sg == so:
+        assert np.array_equal(gpu["depth"][:n_g], ref["depth"][:n_o])
+        ok, err = close(gpu["score"][1:n_g], ref["score"][1:n_o], rtol=SCORE_TOL)
+        assert ok, ("scores", err)
+        return 0
+    flips = 0
+    for i in range(1, n_g):
+        if sg[i] == so[i]:
+            continue
+        a = prefix_score(sg[i], top_id, top_logq)
+        b = prefix_score(so[i], top_id, top_logq)
+        assert a is not None, ("gpu node outside the universe", sg[i])
+        assert abs(a - b) <= SCORE_TOL * max(1.0, abs(b)), ("order", i, sg[i], so[i], a, b)
+        flips += 1
+    # same prefix-closed shape: every GPU node's parent precedes it
+    for u in range(1, n_g):
+        assert 0 <= gpu["parent"][u] < u
+    return flips
+
+
+def check_draw(idx_gpu, idx_ref, masses, u, tol=FLIP_TOL):
+    """Inverse-CDF draw check.  masses: the oracle's (fp64) masses in draw
+    order; u: the uniform.  Returns 0 if equal, 1 for an accepted near-
+    boundary flip; raises otherwise."""
+    if idx_gpu == idx_ref:
+        return 0
+    masses = np.asarray(masses, dtype=np.float64)
+    cum = np.cumsum(masses)
+    total = cum[-1]
+    thr = u * total
+    lo, hi = min(idx_gpu, idx_ref), max(idx_gpu, idx_ref)
+    assert abs(cum[lo] - thr) <= tol * total, ("draw", idx_gpu, idx_ref, cum[lo], thr)
+    assert masses[lo + 1:hi].sum() <= tol * total, ("draw skips mass", idx_gpu, idx_ref)
+    return 1

@@ -1,0 +1,95 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+entry point include/tsd.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tree_speculative_decoding_position_gb300 as tsd
+from tree_speculative_decoding_position_gb300 import build as tsd_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tsd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tsd_build.build()
+    return tsd.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsd_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted([
+        "tsd_build_tree", "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
+        "tsd_verify_tev", "tsd_workspace_size"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert tsd.tsd_status_string(code)
+    assert tsd.tsd_status_string(0) == "ok"
+    assert tsd.tsd_status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    import torch
+    V = 151936
+    n = tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 32, 1, 1, V, 1, 256, torch.bfloat16)
+    # per node: CSR/depth/stat arrays plus one 16-byte record per 4096-token chunk
+    assert n >= 32 * 257 * 38 * 16
+    assert n % 256 == 0
+    assert tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 0, 1, 1, V, 1, 256, torch.bfloat16) == 0
+    assert tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 16, 8, 16, V, 8, 128, torch.bfloat16) > 0
+    # top-k above the cap, or rank digits that do not fit the 56-bit tie key
+    assert tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 1, 1, 16, V, 33, 64, torch.bfloat16) == 0
+    assert tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 1, 1, 20, V, 16, 64, torch.bfloat16) == 0
+    assert tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 1, 9, 16, V, 8, 64, torch.bfloat16) == 0
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    """Null pointers and out-of-range sizes return TSD_ERR_INVALID_ARG before
+    anything touches a GPU (this runs on a machine without one)."""
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: the checks fail first
+    st = lib.tsd_verify_tev(None, 0, fake, fake, fake, 1, 8, 32, 1.0, 0, fake, fake, fake,
+                            None, None, None, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG
+    st = lib.tsd_verify_tev(fake, 0, fake, fake, fake, 1, 8, 32, -1.0, 0, fake, fake, fake,
+                            None, None, None, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG
+    st = lib.tsd_verify_tev(fake, 7, fake, fake, fake, 1, 8, 32, 1.0, 0, fake, fake, fake,
+                            None, None, None, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG
+    st = lib.tsd_verify_tev(fake, 0, fake, fake, fake, 1, 5000, 32, 1.0, 0, fake, fake, fake,
+                            None, None, None, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG
+    # workspace too small
+    st = lib.tsd_verify_tev(fake, 0, fake, fake, fake, 1, 8, 32, 1.0, 0, fake, fake, fake,
+                            None, None, None, fake, fake, 16, None)
+    assert st == tsd.TSD_ERR_WORKSPACE
+    st = lib.tsd_verify_ddtree(fake, 0, fake, fake, None, 1, 8, 32, 1.0, 0, fake, fake, fake,
+                               None, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG
+    st = lib.tsd_build_tree(fake, 0, 1, 1, 4, 32, 4, 8, 0.0, fake, fake, fake, fake, None, None,
+                            fake, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG  # drafter temperature must be > 0
+    st = lib.tsd_build_tree(fake, 0, 1, 1, 4, 32, 64, 8, 1.0, fake, fake, fake, fake, None, None,
+                            fake, fake, fake, 1 << 20, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG  # top-k above V
+    st = lib.tsd_tree_mask(fake, fake, 1, 8, 3, fake, fake, fake, 5, fake, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG  # mask_ld < P + B + 1
+    st = lib.tsd_tree_mask(fake, fake, 1, 8, -1, fake, fake, None, 0, fake, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG

@@ -1,0 +1,383 @@
+"""GPU parity: the CUDA library (through the C ABI binding) against the
+float64 oracle on the same seeded inputs, element by element.
+
+Sizes: the tiny configuration (V=32, L=4, k=4, B=8); a mid-size vocabulary
+that spans several 8 KB chunks plus a ragged tail; and the full Qwen-size
+vocabulary V=151936 with B=64 (one tree) and B=256 (32 trees, sampled trees
+checked against the oracle one by one).  Tolerances live in gpu_helpers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import RTOL, check_draw, close, compare_trees
+
+pytestmark = pytest.mark.gpu
+
+V_Q = synth.V_QWEN
+
+
+@pytest.fixture(scope="module")
+def tsd():
+    import tree_speculative_decoding_position_gb300 as m
+    from tree_speculative_decoding_position_gb300 import build
+    build.build()
+    m.load()
+    return m
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _tree_np(out, t=0):
+    return {k: _np(out[k][t]) for k in ("parent", "token", "depth", "score", "rank", "mode")} | \
+        {"n_nodes": int(out["n_nodes"][t])}
+
+
+def oracle_build(orc, drafter, k, B, temp=1.0):
+    """drafter: [K, L, V] torch (any float dtype) -> oracle tree + lists."""
+    z = drafter.float().cpu().numpy().astype(np.float64)
+    _, tid, tlq = orc.drafter_stats(z, temp, k)
+    return orc.build_tree(tid, tlq, B), tid, tlq
+
+
+# ---------------------------------------------------------------------------
+# builder
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(6))
+def test_build_tiny(tsd, dev, orc, seed):
+    dr = synth.tiny_drafter(synth.seed_for(0, seed))
+    out = tsd.tsd_build_tree(dr[None, None].to(dev), topk=4, B=8)
+    ref, tid, tlq = oracle_build(orc, dr[None], 4, 8)
+    g = _tree_np(out)
+    assert int(out["status"][0]) == 0
+    assert compare_trees(g, ref, tid, tlq) == 0
+    n = g["n_nodes"]
+    assert np.array_equal(g["rank"][:n], ref["rank"][:n])
+    assert np.array_equal(g["mode"][:n], ref["mode"][:n])
+    assert np.all(g["parent"][n:] == -1) and np.all(np.isneginf(g["score"][n:]))
+
+
+@pytest.mark.parametrize("V,B,k,temp", [(12805, 64, 8, 1.0), (4096 * 3, 200, 8, 0.7),
+                                         (1001, 40, 5, 1.0), (V_Q, 64, 8, 1.0)])
+def test_build_single_mode(tsd, dev, orc, V, B, k, temp):
+    dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device="cpu")  # [1, 1, 16, V] bf16
+    out = tsd.tsd_build_tree(dr.to(dev), topk=k, B=B, drafter_temp=temp)
+    ref, tid, tlq = oracle_build(orc, dr[0], k, B, temp)
+    flips = compare_trees(_tree_np(out), ref, tid, tlq)
+    assert flips <= 2, flips
+
+
+def test_build_fp32_and_misaligned(tsd, dev, orc):
+    """fp32 logits, and a row start that is not 16-byte aligned (generic path)."""
+    dr = synth.zipf_drafter(1, 6, 5000, synth.seed_for(1, 3), device="cpu", dtype=torch.float32)
+    buf = torch.empty(1 + dr.numel(), dtype=torch.float32, device=dev)
+    buf[1:] = dr.reshape(-1).to(dev)
+    view = buf[1:].view(dr.shape)
+    out = tsd.tsd_build_tree(view, topk=6, B=50)
+    ref, tid, tlq = oracle_build(orc, dr[0], 6, 50)
+    assert compare_trees(_tree_np(out), ref, tid, tlq) <= 1
+
+
+def test_build_mixture(tsd, dev, orc):
+    """K=8 modes from two latent futures (the mixture workload), B=128."""
+    dr, _, _ = synth.mixture_drafter(2, 8, 16, V_Q, synth.seed_for(3), device="cpu")
+    out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=128)
+    flips = 0
+    for t in range(2):
+        ref, tid, tlq = oracle_build(orc, dr[t], 8, 128)
+        flips += compare_trees(_tree_np(out, t), ref, tid, tlq)
+    assert flips <= 2
+
+
+def test_build_masked_and_small_universe(tsd, dev, orc):
+    """-inf logits outside a few tokens: only finite-score prefixes become
+    nodes, so n_nodes < B+1."""
+    z = torch.full((1, 1, 3, 64), -float("inf"))
+    z[0, 0, :, :2] = torch.tensor([1.0, 0.5])
+    out = tsd.tsd_build_tree(z.to(dev), topk=4, B=50)
+    ref, tid, tlq = oracle_build(orc, z[0], 4, 50)
+    assert ref["n_nodes"] == 1 + 2 + 4 + 8
+    assert compare_trees(_tree_np(out), ref, tid, tlq) == 0
+
+
+def test_build_nonfinite_status(tsd, dev):
+    z = torch.randn(2, 1, 4, 32)
+    z[1, 0, 2, 5] = float("nan")
+    out = tsd.tsd_build_tree(z.to(dev), topk=4, B=8)
+    assert _np(out["status"]).tolist() == [0, 5]
+    assert int(out["n_nodes"][1]) == 0 and int(out["n_nodes"][0]) == 9
+
+
+# ---------------------------------------------------------------------------
+# mask
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,P", [(8, 0), (64, 1024), (300, 17)])
+def test_tree_mask(tsd, dev, orc, B, P):
+    dr = synth.zipf_drafter(3, 16, 2048, synth.seed_for(4, B), device="cpu")
+    parents, nn = [], []
+    for t in range(3):
+        ref, _, _ = oracle_build(orc, dr[t], 8, B)
+        parents.append(ref["parent"])
+        nn.append(ref["n_nodes"])
+    nn[2] = max(1, nn[2] - 5)  # a ragged tree: trailing slots are padding
+    par = torch.tensor(np.stack(parents), dtype=torch.int32, device=dev)
+    n_nodes = torch.tensor(nn, dtype=torch.int32, device=dev)
+    out = tsd.tsd_tree_mask(par, n_nodes, prefix_len=P, additive=True)
+    for t in range(3):
+        bits, pos, add = orc.tree_mask(parents[t], nn[t], B, P, with_additive=True)
+        assert np.array_equal(_np(out["anc_bits"][t]).view(np.uint32), bits)
+        assert np.array_equal(_np(out["position_ids"][t]), pos)
+        assert np.array_equal(_np(out["additive_mask"][t]), add.astype(np.float32))
+    assert _np(out["status"]).tolist() == [0, 0, 0]
+
+
+def test_tree_mask_bad_tree(tsd, dev):
+    par = torch.tensor([[-1, 0, 2, 1]], dtype=torch.int32, device=dev)  # parent after child
+    out = tsd.tsd_tree_mask(par, torch.tensor([4], dtype=torch.int32, device=dev))
+    assert int(out["status"][0]) == 4
+    assert _np(out["position_ids"][0]).tolist() == [0, 0, 0, 0]
+
+
+# ---------------------------------------------------------------------------
+# TEV and predraw
+# ---------------------------------------------------------------------------
+def _target_for(orc, tree, drafter_rows, sigma, seed, B, dtype):
+    n = tree["n_nodes"]
+    rows = synth.target_from_rows(drafter_rows.float(), tree["depth"][:n], sigma, seed, dtype=dtype)
+    full = torch.zeros(B + 1, rows.shape[1], dtype=dtype)
+    full[:n] = rows
+    return full
+
+
+def _check_tev(out, t, o, tgt64, parent, token, n, T):
+    """One tree: masses within RTOL; exit/bonus exact up to counted flips."""
+    ok, err = close(_np(out["exit_mass"][t])[:n], o["w"])
+    assert ok, ("w", err)
+    ok, err = close(_np(out["prefix_prob"][t])[:n], o["P"])
+    assert ok, ("P", err)
+    ok, err = close(float(out["coverage"][t]), o["coverage"])
+    assert ok, ("C_p", err)
+    assert int(out["status"][t]) == 0
+    ex = int(out["exit_node"][t])
+    flips = check_draw(ex, o["exit_node"], o["w"], o["u_exit"])
+    if ex == o["exit_node"]:
+        import oracle
+        p = oracle.row_probs(tgt64[ex], T)
+        kids = [int(token[u]) for u in range(1, n) if int(parent[u]) == ex]
+        p[kids] = 0.0
+        flips += check_draw(int(out["bonus_token"][t]), o["bonus"], p, o["u_bonus"])
+        assert int(out["accept_len"][t]) == o["accept_len"]
+    return flips
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6, 0.0])
+@pytest.mark.parametrize("seed", range(4))
+def test_tev_tiny(tsd, dev, orc, T, seed):
+    s = synth.seed_for(0, seed)
+    dr = synth.tiny_drafter(s)
+    ref, _, _ = oracle_build(orc, dr[None], 4, 8)
+    n = ref["n_nodes"]
+    tgt = synth.tiny_target(dr, ref["depth"][:n], s + 7)
+    full = torch.zeros(1, 9, 32)
+    full[0, :n] = tgt
+    par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
+    tok = torch.tensor(ref["token"][None], dtype=torch.int32, device=dev)
+    nn = torch.tensor([n], dtype=torch.int32, device=dev)
+    for sd in range(5):
+        out = tsd.tsd_verify_tev(full.to(dev), par, tok, nn, T, seed=sd)
+        o = orc.tev(tgt.numpy(), ref["parent"], ref["token"], n, T, seed=sd)
+        assert _check_tev(out, 0, o, tgt.numpy().astype(np.float64), ref["parent"],
+                          ref["token"], n, T) == 0
+        d = tsd.tsd_verify_ddtree(full.to(dev), par, tok, nn, T, seed=sd)
+        od = orc.predraw(tgt.numpy(), ref["parent"], ref["token"], n, T, seed=sd)
+        assert _np(d["draws"][0])[:n].tolist() == od["draws"].tolist()
+        assert (int(d["exit_node"][0]), int(d["bonus_token"][0]), int(d["accept_len"][0])) == \
+            (od["exit_node"], od["bonus"], od["accept_len"])
+
+
+@pytest.mark.parametrize("V,dtype", [(12805, torch.bfloat16), (4096 * 2 + 100, torch.float32),
+                                     (3001, torch.bfloat16)])
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tev_midsize(tsd, dev, orc, V, dtype, T):
+    """Several chunks and a ragged tail (V=3001 bf16 is not a multiple of 8:
+    the generic path)."""
+    B = 64
+    dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1, 7), device="cpu")
+    ref, _, _ = oracle_build(orc, dr[0], 8, B)
+    tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 8), B, dtype)
+    par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
+    tok = torch.tensor(ref["token"][None], dtype=torch.int32, device=dev)
+    nn = torch.tensor([ref["n_nodes"]], dtype=torch.int32, device=dev)
+    n = ref["n_nodes"]
+    z64 = tgt.float().numpy().astype(np.float64)
+    flips = 0
+    for sd in range(6):
+        out = tsd.tsd_verify_tev(tgt[None].to(dev), par, tok, nn, T, seed=sd)
+        o = orc.tev(z64[:n], ref["parent"], ref["token"], n, T, seed=sd)
+        flips += _check_tev(out, 0, o, z64, ref["parent"], ref["token"], n, T)
+        d = tsd.tsd_verify_ddtree(tgt[None].to(dev), par, tok, nn, T, seed=sd)
+        od = orc.predraw(z64[:n], ref["parent"], ref["token"], n, T, seed=sd)
+        for v in range(n):
+            if int(d["draws"][0, v]) != int(od["draws"][v]):
+                p = orc.row_probs(z64[v], T)
+                flips += check_draw(int(d["draws"][0, v]), int(od["draws"][v]), p,
+                                    orc.uniform(sd, 0, v, 2))
+    assert flips <= 2, flips
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tev_qwen_vocab_b64(tsd, dev, orc, T):
+    """The batch-1 Qwen-vocabulary round: V=151936, L=16, k=8, B=64, bf16."""
+    B = 64
+    dr = synth.zipf_drafter(1, 16, V_Q, synth.seed_for(1), device="cpu")
+    ref, _, _ = oracle_build(orc, dr[0], 8, B)
+    tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 1), B, torch.bfloat16)
+    n = ref["n_nodes"]
+    par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
+    tok = torch.tensor(ref["token"][None], dtype=torch.int32, device=dev)
+    nn = torch.tensor([n], dtype=torch.int32, device=dev)
+    z64 = tgt.float().numpy().astype(np.float64)
+    flips = 0
+    for sd in range(3):
+        out = tsd.tsd_verify_tev(tgt[None].to(dev), par, tok, nn, T, seed=sd)
+        o = orc.tev(z64[:n], ref["parent"], ref["token"], n, T, seed=sd)
+        flips += _check_tev(out, 0, o, z64, ref["parent"], ref["token"], n, T)
+    assert flips <= 1
+
+
+def test_tev_batched_b256(tsd, dev, orc):
+    """32 independent trees, V=151936, B=256, T=0.6, bf16: every tree checked
+    for validity, four sampled trees against the oracle element by element."""
+    nt, B, T = 32, 256, 0.6
+    seeds = [synth.seed_for(2, t) for t in range(nt)]
+    dr = synth.zipf_drafter(nt, 16, V_Q, 0, device=dev, seeds=seeds)
+    tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+    assert _np(tr["status"]).tolist() == [0] * nt
+    tgt = torch.empty(nt, B + 1, V_Q, dtype=torch.bfloat16, device=dev)
+    for t in range(nt):
+        n = int(tr["n_nodes"][t])
+        synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=tgt[t, :n])
+        tgt[t, n:] = 0
+    out = tsd.tsd_verify_tev(tgt, tr["parent"], tr["token"], tr["n_nodes"], T, seed=123)
+    assert _np(out["status"]).tolist() == [0] * nt
+    w = _np(out["exit_mass"])
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-4)
+    for t in range(nt):
+        ex = int(out["exit_node"][t])
+        kids = [int(tr["token"][t, u]) for u in range(1, B + 1) if int(tr["parent"][t, u]) == ex]
+        assert int(out["bonus_token"][t]) not in kids
+    # sampled trees, element by element (the tree itself is the GPU's here; its
+    # parity with the oracle builder is checked in the builder tests)
+    flips = 0
+    for t in (0, 9, 22, 31):
+        n = int(tr["n_nodes"][t])
+        par, tok = _np(tr["parent"][t]), _np(tr["token"][t])
+        z64 = tgt[t, :n].float().cpu().numpy().astype(np.float64)
+        o = orc.tev(z64, par, tok, n, T, seed=123, tree=t)
+        flips += _check_tev(out, t, o, z64, par, tok, n, T)
+    assert flips <= 1
+
+
+def test_tev_edge_cases(tsd, dev, orc):
+    """Root-only tree, a chain, a star, a tree with masked tokens, and per-tree
+    error codes (bad tree, NaN logits) next to valid trees."""
+    V, B = 640, 12
+    g = torch.Generator().manual_seed(5)
+    z = torch.randn(5, B + 1, V, generator=g) * 2
+    parent = np.full((5, B + 1), -1, dtype=np.int32)
+    token = np.full((5, B + 1), -1, dtype=np.int32)
+    nn = [1, B + 1, B + 1, 6, 4]
+    for u in range(1, B + 1):  # tree 1: chain; tree 2: star
+        parent[1, u], token[1, u] = u - 1, (7 * u) % V
+        parent[2, u], token[2, u] = 0, 3 * u
+    parent[3, 1:6] = [0, 0, 1, 1, 2]
+    token[3, 1:6] = [5, 9, 5, 100, 639]
+    z[3, 1, 10:600] = -float("inf")  # masked tokens
+    parent[4, 1:4] = [0, 1, 1]
+    token[4, 1:4] = [1, 2, 2]  # repeated sibling token: a malformed tree
+    zz = z.clone()
+    zz[0, 0, 17] = float("nan")  # tree 0 gets a NaN
+    for T in (1.0, 0.0):
+        out = tsd.tsd_verify_tev(zz.to(dev), torch.tensor(parent, device=dev),
+                                 torch.tensor(token, device=dev),
+                                 torch.tensor(nn, dtype=torch.int32, device=dev), T, seed=9)
+        st = _np(out["status"]).tolist()
+        assert st == [5, 0, 0, 0, 4], st
+        assert int(out["exit_node"][4]) == -1 and int(out["accept_len"][4]) == 0
+        for t in (1, 2, 3):
+            n = nn[t]
+            z64 = z[t, :n].numpy().astype(np.float64)
+            o = orc.tev(z64, parent[t], token[t], n, T, seed=9, tree=t)
+            assert _check_tev(out, t, o, z64, parent[t], token[t], n, T) == 0
+        # the NaN-free copy of tree 0 (root only): exit at the root, bonus ~ p_root
+        out0 = tsd.tsd_verify_tev(z[:1].to(dev), torch.tensor(parent[:1], device=dev),
+                                  torch.tensor(token[:1], device=dev),
+                                  torch.tensor([1], dtype=torch.int32, device=dev), T, seed=9)
+        o = orc.tev(z[0, :1].numpy().astype(np.float64), parent[0], token[0], 1, T, seed=9)
+        assert (int(out0["exit_node"][0]), int(out0["bonus_token"][0]), int(out0["accept_len"][0])) \
+            == (0, o["bonus"], 1)
+
+
+def test_tev_outputs_fully_written(tsd, dev, orc):
+    """Every output slot is written (sentinel fill through a caller workspace
+    filled with NaN bytes)."""
+    V, B = 300, 10
+    z = torch.randn(2, B + 1, V)
+    parent = torch.tensor([[-1, 0, 0, 1] + [-1] * 7, [-1] + [-1] * 10], dtype=torch.int32)
+    token = torch.tensor([[-1, 4, 8, 15] + [-1] * 7, [-1] * 11], dtype=torch.int32)
+    nn = torch.tensor([4, 1], dtype=torch.int32)
+    nbytes = tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 2, 1, 1, V, 1, B, torch.float32)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev)
+    out = tsd.tsd_verify_tev(z.to(dev), parent.to(dev), token.to(dev), nn.to(dev), 1.0, seed=3,
+                             workspace=ws)
+    assert _np(out["status"]).tolist() == [0, 0]
+    w = _np(out["exit_mass"])
+    assert np.all(np.isfinite(w)) and np.all(w[0, 4:] == 0) and np.all(w[1, 1:] == 0)
+    assert w[1, 0] == 1.0
+
+
+def test_tev_and_predraw_law_on_gpu(tsd, dev, orc):
+    """10^6 GPU draws of each verifier on one tiny tree (replicated over
+    100000 tree slots with their own uniforms) against the exact joint law
+    from the oracle's masses: chi-square, as the pages' saturation theorem
+    requires of both."""
+    import scipy.stats
+    s = synth.seed_for(0, 99)
+    dr = synth.tiny_drafter(s)
+    ref, _, _ = oracle_build(orc, dr[None], 4, 8)
+    n = ref["n_nodes"]
+    tgt = synth.tiny_target(dr, ref["depth"][:n], s + 7).numpy().astype(np.float64)
+    o = orc.tev(tgt, ref["parent"], ref["token"], n, 1.0, seed=0)
+    law = np.zeros((n, 32))
+    for v in range(n):
+        p = orc.row_probs(tgt[v], 1.0)
+        kids = [int(ref["token"][u]) for u in range(1, n) if int(ref["parent"][u]) == v]
+        p[kids] = 0.0
+        law[v] = o["w"][v] * p / p.sum()
+    R = 100000
+    full = torch.zeros(R, 9, 32, device=dev)
+    full[:, :n] = torch.tensor(tgt, dtype=torch.float32, device=dev)
+    par = torch.tensor(ref["parent"], dtype=torch.int32, device=dev).expand(R, 9).contiguous()
+    tok = torch.tensor(ref["token"], dtype=torch.int32, device=dev).expand(R, 9).contiguous()
+    nn = torch.full((R,), n, dtype=torch.int32, device=dev)
+    for fn in (tsd.tsd_verify_tev, tsd.tsd_verify_ddtree):
+        counts = np.zeros(n * 32)
+        for rep in range(10):
+            out = fn(full, par, tok, nn, 1.0, seed=1000 + rep)
+            cell = _np(out["exit_node"]).astype(np.int64) * 32 + _np(out["bonus_token"])
+            counts += np.bincount(cell, minlength=n * 32)
+        exp = law.ravel() * counts.sum()
+        assert counts[exp == 0].sum() == 0
+        keep = exp >= 5
+        obs = np.append(counts[keep], counts[~keep].sum())
+        ex = np.append(exp[keep], exp[~keep].sum())
+        assert scipy.stats.chisquare(obs, ex * obs.sum() / ex.sum()).pvalue > 1e-4, fn.__name__

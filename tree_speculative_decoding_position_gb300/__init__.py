@@ -1,0 +1,229 @@
+"""GB300 (sm_103a) library for the data-parallel hot path of bounded-tree
+speculative decoding: the best-first draft-tree builder (with the mixture
+variant), the ancestor mask and position ids, and exact Tree Exit
+Verification, plus a predraw-and-follow verifier kept as an equivalence check.
+
+This module is a thin binding over the C ABI in ``include/tsd.h`` (loaded
+from ``libtsd.so`` with ctypes): it checks tensor dtypes, shapes, devices and
+contiguity, allocates outputs and the workspace with PyTorch, and passes raw
+pointers and the current CUDA stream.  Every step of the path runs in the
+library's CUDA kernels; there is no other implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
+           "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_ddtree", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
+
+TSD_OK, TSD_ERR_INVALID_ARG, TSD_ERR_CUDA, TSD_ERR_WORKSPACE = 0, 1, 2, 3
+TSD_ERR_BAD_TREE, TSD_ERR_NONFINITE, TSD_ERR_TIMEOUT = 4, 5, 6
+TSD_BF16, TSD_F32 = 0, 1
+TSD_OP_BUILD_TREE, TSD_OP_VERIFY_TEV, TSD_OP_VERIFY_DDTREE = 0, 1, 2
+
+_lib = None
+
+
+class TsdError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s: %s (status %d)" % (what, tsd_status_string(code), code))
+        self.code = code
+
+
+def load():
+    """Load libtsd.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libtsd.so is missing: build it with "
+                           "`python -m tree_speculative_decoding_position_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_uint64, ctypes.c_size_t)
+    lib.tsd_status_string.argtypes = [i32]
+    lib.tsd_status_string.restype = ctypes.c_char_p
+    lib.tsd_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32]
+    lib.tsd_workspace_size.restype = sz
+    lib.tsd_build_tree.argtypes = [P, i32, i32, i32, i32, i64, i32, i32, f32,
+                                   P, P, P, P, P, P, P, P, P, sz, P]
+    lib.tsd_tree_mask.argtypes = [P, P, i32, i32, i32, P, P, P, i64, P, P]
+    lib.tsd_verify_tev.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
+                                   P, P, P, P, P, P, P, P, sz, P]
+    lib.tsd_verify_ddtree.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
+                                      P, P, P, P, P, P, sz, P]
+    for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_ddtree"):
+        getattr(lib, f).restype = i32
+    _lib = lib
+    return lib
+
+
+def tsd_status_string(code: int) -> str:
+    return load().tsd_status_string(int(code)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TSD_BF16
+    if t.dtype == torch.float32:
+        return TSD_F32
+    raise TypeError("logits must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def tsd_workspace_size(op: int, n_trees: int, n_modes: int, L: int, V: int, topk: int, B: int,
+                       dtype: torch.dtype) -> int:
+    code = TSD_BF16 if dtype == torch.bfloat16 else TSD_F32
+    return int(load().tsd_workspace_size(op, n_trees, n_modes, L, V, topk, B, code))
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace holds fewer than %d bytes" % nbytes)
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def tsd_build_tree(drafter_logits: torch.Tensor, topk: int, B: int, drafter_temp: float = 1.0,
+                   workspace=None) -> dict:
+    """Best-first tree builder.  drafter_logits: [n_trees, n_modes, L, V]
+    (bf16/fp32).  Returns parent, token, depth, score, rank, mode
+    ([n_trees, B+1]), n_nodes and status ([n_trees])."""
+    x = _cuda(drafter_logits, "drafter_logits")
+    if x.dim() != 4:
+        raise ValueError("drafter_logits must be [n_trees, n_modes, L, V]")
+    n_trees, n_modes, L, V = x.shape
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, B + 1, **i32) for k in ("parent", "token", "depth", "rank", "mode")}
+    out["score"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+    out["n_nodes"] = torch.empty(n_trees, **i32)
+    out["status"] = torch.empty(n_trees, **i32)
+    nbytes = tsd_workspace_size(TSD_OP_BUILD_TREE, n_trees, n_modes, L, V, topk, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_build_tree")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_build_tree(_ptr(x), _dtype_code(x), n_trees, n_modes, L, V, topk, B,
+                                   drafter_temp, _ptr(out["parent"]), _ptr(out["token"]),
+                                   _ptr(out["depth"]), _ptr(out["score"]), _ptr(out["rank"]),
+                                   _ptr(out["mode"]), _ptr(out["n_nodes"]), _ptr(out["status"]),
+                                   _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_build_tree")
+    return out
+
+
+def tsd_tree_mask(parent: torch.Tensor, n_nodes: torch.Tensor, prefix_len: int = 0,
+                  additive: bool = False) -> dict:
+    """Ancestor bitmask [n_trees, B+1, W], position ids [n_trees, B+1] and,
+    if `additive`, the float mask [n_trees, B+1, prefix_len+B+1]."""
+    parent = _cuda(parent, "parent", torch.int32)
+    n_nodes = _cuda(n_nodes, "n_nodes", torch.int32)
+    n_trees, Bp1 = parent.shape
+    B = Bp1 - 1
+    W = (B + 32) // 32
+    dev = parent.device
+    bits = torch.empty(n_trees, Bp1, W, dtype=torch.int32, device=dev)
+    pos = torch.empty(n_trees, Bp1, dtype=torch.int32, device=dev)
+    status = torch.empty(n_trees, dtype=torch.int32, device=dev)
+    ld = prefix_len + B + 1
+    add = torch.empty(n_trees, Bp1, ld, dtype=torch.float32, device=dev) if additive else None
+    with torch.cuda.device(dev):
+        st = load().tsd_tree_mask(_ptr(parent), _ptr(n_nodes), n_trees, B, prefix_len, _ptr(bits),
+                                  _ptr(pos), _ptr(add), ld, _ptr(status), _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_tree_mask")
+    return dict(anc_bits=bits, position_ids=pos, additive_mask=add, status=status)
+
+
+def _verify_common(target_logits, parent, token, n_nodes):
+    x = _cuda(target_logits, "target_logits")
+    if x.dim() != 3:
+        raise ValueError("target_logits must be [n_trees, B+1, V]")
+    n_trees, Bp1, V = x.shape
+    parent = _cuda(parent, "parent", torch.int32)
+    token = _cuda(token, "token", torch.int32)
+    n_nodes = _cuda(n_nodes, "n_nodes", torch.int32)
+    if tuple(parent.shape) != (n_trees, Bp1) or tuple(token.shape) != (n_trees, Bp1) \
+            or tuple(n_nodes.shape) != (n_trees,):
+        raise ValueError("parent/token must be [n_trees, B+1] and n_nodes [n_trees]")
+    return x, parent, token, n_nodes, n_trees, Bp1 - 1, V
+
+
+def tsd_verify_tev(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
+                   n_nodes: torch.Tensor, temperature: float, seed: int, workspace=None,
+                   with_masses: bool = True) -> dict:
+    """Tree Exit Verification.  Returns exit_node, bonus_token, accept_len,
+    status ([n_trees]) and, with `with_masses`, exit_mass, prefix_prob
+    ([n_trees, B+1]) and coverage ([n_trees])."""
+    x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
+    if with_masses:
+        out["exit_mass"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+        out["prefix_prob"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+        out["coverage"] = torch.empty(n_trees, dtype=torch.float32, device=dev)
+    nbytes = tsd_workspace_size(TSD_OP_VERIFY_TEV, n_trees, 1, 1, V, 1, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_verify_tev")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_verify_tev(_ptr(x), _dtype_code(x), _ptr(parent), _ptr(token),
+                                   _ptr(n_nodes), n_trees, B, V, temperature, seed,
+                                   _ptr(out["exit_node"]), _ptr(out["bonus_token"]),
+                                   _ptr(out["accept_len"]), _ptr(out.get("exit_mass")),
+                                   _ptr(out.get("prefix_prob")), _ptr(out.get("coverage")),
+                                   _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_verify_tev")
+    return out
+
+
+def tsd_verify_ddtree(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
+                      n_nodes: torch.Tensor, temperature: float, seed: int,
+                      workspace=None) -> dict:
+    """Predraw-and-follow.  Returns exit_node, bonus_token, accept_len, status
+    ([n_trees]) and the per-node draws ([n_trees, B+1])."""
+    x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
+    out["draws"] = torch.empty(n_trees, B + 1, **i32)
+    nbytes = tsd_workspace_size(TSD_OP_VERIFY_DDTREE, n_trees, 1, 1, V, 1, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_verify_ddtree")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_verify_ddtree(_ptr(x), _dtype_code(x), _ptr(parent), _ptr(token),
+                                      _ptr(n_nodes), n_trees, B, V, temperature, seed,
+                                      _ptr(out["exit_node"]), _ptr(out["bonus_token"]),
+                                      _ptr(out["accept_len"]), _ptr(out["draws"]),
+                                      _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_verify_ddtree")
+    return out

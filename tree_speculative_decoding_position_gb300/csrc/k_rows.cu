@@ -1,0 +1,507 @@
+// k_rows.cu -- the node-row reduction of Tree Exit Verification.
+//
+// "Where Draft Trees Lose Target Mass: Exit-Guided Speculative Decoding",
+// Sec. 3 Eq. 1 (p_v = softmax(z_v / T)), Sec. 3.1 Eq. 4 (rho(v): the mass of
+// the tokens that are not drafted children of v) and Eq. 7 (the residual law
+// the bonus token is drawn from).  App. B calls these node-local reductions;
+// they read every logit of every tree node once and carry all of the path's
+// HBM traffic.
+//
+// Three kernels:
+//   verify_prep_kernel   one CTA per tree: validates the tree, computes
+//                        depths and a CSR list of each node's children sorted
+//                        by token (so a chunk finds its children by binary
+//                        search).
+//   rows_kernel          one warp per (node row, 8 KB chunk): max, sum of
+//                        exp2(z*c - mc), the same sum without the drafted
+//                        children, or the arg-max when T = 0.
+//   node_combine_kernel  one warp per node row: combines its chunks, the
+//                        child probabilities p_v(x_u) and rho(v).
+#include "tsd_internal.cuh"
+
+#include <float.h>
+
+namespace tsd {
+
+// ---------------------------------------------------------------------------
+// Tree preparation.
+// ---------------------------------------------------------------------------
+constexpr int kPrepThreads = 512;
+constexpr int kPrepMaxKeys = 4096;  // next power of two >= TSD_MAX_B
+
+// key = parent << 43 | token << 12 | node: sorting orders children by parent,
+// then token; parent < 4096 (12 bits), token < 2^31, node < 4096.
+__device__ __forceinline__ uint64_t child_key(int p, int tok, int u) {
+    return ((uint64_t)p << 43) | ((uint64_t)(uint32_t)tok << 12) | (uint64_t)u;
+}
+
+__device__ void block_bitonic_sort(uint64_t* keys, int n2) {
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint64_t a = keys[i], b = keys[l];
+                    const bool up = (i & k) == 0;
+                    if ((a > b) == up) {
+                        keys[i] = b;
+                        keys[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
+                   const int32_t* __restrict__ n_nodes, int B, int64_t V, VerifyWs ws) {
+    __shared__ uint64_t keys[kPrepMaxKeys];
+    __shared__ int bad;
+    const int t = blockIdx.x;
+    const int32_t* par = parent + (int64_t)t * (B + 1);
+    const int32_t* tok = token + (int64_t)t * (B + 1);
+    const int n = n_nodes[t];
+    if (threadIdx.x == 0) bad = (n < 1 || n > B + 1 || par[0] != -1) ? 1 : 0;
+    __syncthreads();
+    const int nn = bad ? 1 : n;
+    const int m = nn - 1;  // number of child edges
+    int n2 = 1;
+    while (n2 < m) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        uint64_t key = ~0ull;
+        if (i < m) {
+            const int u = i + 1, p = par[u], x = tok[u];
+            if (p < 0 || p >= u || x < 0 || (int64_t)x >= V) bad = 1;
+            else key = child_key(p, x, u);
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    if (!bad) {
+        block_bitonic_sort(keys, n2);
+        for (int i = threadIdx.x + 1; i < m; i += blockDim.x)
+            if ((keys[i] >> 12) == (keys[i - 1] >> 12)) bad = 1;  // repeated sibling token
+    }
+    __syncthreads();
+    const int stat = bad ? kStatBadTree : kStatOk;
+    if (threadIdx.x == 0) ws.tstat[t] = stat;
+    if (bad) return;
+    int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+    int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+    int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
+    int32_t* dep = ws.depth + (int64_t)t * (B + 1);
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        ctok[i] = (int32_t)((keys[i] >> 12) & 0x7fffffffu);
+        cnode[i] = (int32_t)(keys[i] & 0xfffu);
+    }
+    // child_ptr[v] = first sorted edge whose parent is >= v
+    for (int v = threadIdx.x; v <= nn; v += blockDim.x) {
+        int lo = 0, hi = m;
+        const uint64_t probe = (uint64_t)v << 43;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (keys[mid] < probe) lo = mid + 1;
+            else hi = mid;
+        }
+        cptr[v] = lo;
+    }
+    for (int u = threadIdx.x; u < nn; u += blockDim.x) {
+        int d = 0, x = u;
+        while (x > 0) {  // parents precede children, so this ends within u steps
+            x = par[x];
+            ++d;
+        }
+        dep[u] = d;
+    }
+}
+
+cudaError_t launch_verify_prep(const int32_t* parent, const int32_t* token, const int32_t* n_nodes,
+                               int n_trees, int B, int64_t V, const VerifyWs& ws,
+                               cudaStream_t stream) {
+    verify_prep_kernel<<<n_trees, kPrepThreads, 0, stream>>>(parent, token, n_nodes, B, V, ws);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Row reduction.
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 256;
+
+template <typename T>
+struct Lanes;
+template <>
+struct Lanes<__nv_bfloat16> {
+    static constexpr int kVec = 8;  // elements per 16-byte load
+    static __device__ __forceinline__ float get(const uint4& q, int j) {
+        const uint32_t w = (j >> 1) == 0 ? q.x : (j >> 1) == 1 ? q.y : (j >> 1) == 2 ? q.z : q.w;
+        return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    static __device__ __forceinline__ uint4 neg_inf() {
+        return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+    static __device__ __forceinline__ float vmax(const uint4& q) {
+        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
+        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.y));
+        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.z));
+        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.w));
+        return fmaxf(__low2float(a), __high2float(a));
+    }
+};
+template <>
+struct Lanes<float> {
+    static constexpr int kVec = 4;
+    static __device__ __forceinline__ float get(const uint4& q, int j) {
+        return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
+    }
+    static __device__ __forceinline__ uint4 neg_inf() {
+        return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    }
+    static __device__ __forceinline__ float vmax(const uint4& q) {
+        return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+};
+
+// First index in sorted a[lo, hi) with a[i] >= x.
+__device__ __forceinline__ int lower_bound_i32(const int32_t* a, int lo, int hi, int64_t x) {
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)a[mid] < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Vectorised path: the row chunk is 16-byte aligned and its length a multiple
+// of the vector width.  Lane l holds vectors l, l+32, ... of the chunk.
+template <typename T, bool GREEDY>
+__device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, int cn, float c,
+                                                      const int32_t* __restrict__ ctok, int clo,
+                                                      int chi, int64_t c0, int lane) {
+    constexpr int VEC = Lanes<T>::kVec;
+    uint4 buf[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const int e = (i * kWarp + lane) * VEC;
+        buf[i] = (e < cn) ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
+    }
+    ChunkStat st;
+    if (GREEDY) {
+        float bm = -INFINITY;
+        int bi = INT_MAX;
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+            const int e = (i * kWarp + lane) * VEC;
+            if (e < cn) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float x = Lanes<T>::get(buf[i], j);
+                    bad |= is_bad_logit(x);
+                    if (better(x, (int)c0 + e + j, bm, bi)) {
+                        bm = x;
+                        bi = (int)c0 + e + j;
+                    }
+                }
+            }
+        }
+        warp_argmax(bm, bi);
+        bad = __any_sync(0xffffffffu, bad);
+        st.m = bm;
+        st.s = bad ? __int_as_float(0x7fc00000) : 0.0f;
+        st.r = 0.0f;
+        st.amax = bi;
+        return st;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) m = fmaxf(m, Lanes<T>::vmax(buf[i]));
+    m = warp_max(m);
+    st.m = m;
+    st.amax = -1;
+    if (m == -INFINITY) {  // every token of the chunk is masked
+        st.s = 0.0f;
+        st.r = 0.0f;
+        return st;
+    }
+    const float mc = __fmul_rn(m, c);
+    float acc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+    if (chi == clo) {  // no drafted child in this chunk: the residual is the full sum
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] += ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mc));
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) s += acc[j];
+        s = warp_sum(s);
+        st.s = s;
+        st.r = s;
+        return st;
+    }
+    // Some children fall in this chunk: mark them in a per-lane bitmask over
+    // the lane's kVecPerLane * VEC elements, then sum with and without them.
+    uint32_t excl[(kVecPerLane * VEC + 31) / 32];
+#pragma unroll
+    for (int w = 0; w < (kVecPerLane * VEC + 31) / 32; ++w) excl[w] = 0u;
+    for (int q = clo; q < chi; ++q) {
+        const int o = (int)((int64_t)ctok[q] - c0);
+        if (((o / VEC) & (kWarp - 1)) == lane) {
+            const int bit = (o / (VEC * kWarp)) * VEC + (o % VEC);
+            const uint32_t sel = 1u << (bit & 31);
+#pragma unroll
+            for (int w = 0; w < (kVecPerLane * VEC + 31) / 32; ++w)
+                if (w == (bit >> 5)) excl[w] |= sel;
+        }
+    }
+    float racc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) racc[j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float e = ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mc));
+            const int bit = i * VEC + j;
+            acc[j] += e;
+            racc[j] += ((excl[bit >> 5] >> (bit & 31)) & 1u) ? 0.0f : e;
+        }
+    float s = 0.0f, r = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        s += acc[j];
+        r += racc[j];
+    }
+    st.s = warp_sum(s);
+    st.r = warp_sum(r);
+    return st;
+}
+
+// Generic path for unaligned rows or ragged V: element loads, two passes.
+template <typename T, bool GREEDY>
+__device__ __noinline__ ChunkStat reduce_chunk_scalar(const T* __restrict__ rp, int cn, float c,
+                                                      const int32_t* __restrict__ ctok, int clo,
+                                                      int chi, int64_t c0, int lane) {
+    ChunkStat st;
+    float bm = -INFINITY;
+    int bi = INT_MAX;
+    bool bad = false;
+    for (int e = lane; e < cn; e += kWarp) {
+        const float x = load_logit(rp + e);
+        bad |= is_bad_logit(x);
+        if (better(x, (int)c0 + e, bm, bi)) {
+            bm = x;
+            bi = (int)c0 + e;
+        }
+    }
+    warp_argmax(bm, bi);
+    st.m = bm;
+    if (GREEDY) {
+        st.s = __any_sync(0xffffffffu, bad) ? __int_as_float(0x7fc00000) : 0.0f;
+        st.r = 0.0f;
+        st.amax = bi;
+        return st;
+    }
+    st.amax = -1;
+    if (bm == -INFINITY) {
+        st.s = __any_sync(0xffffffffu, bad) ? __int_as_float(0x7fc00000) : 0.0f;
+        st.r = 0.0f;
+        return st;
+    }
+    const float mc = __fmul_rn(bm, c);
+    float s = 0.0f, r = 0.0f;
+    for (int e = lane; e < cn; e += kWarp) {
+        const float x = load_logit(rp + e);
+        const float v = ex2(fmaf(x, c, -mc));
+        bool child = false;
+        for (int q = clo; q < chi; ++q) child |= ((int64_t)ctok[q] == c0 + e);
+        s += v;
+        r += child ? 0.0f : v;
+    }
+    st.s = warp_sum(s);
+    st.r = warp_sum(r);
+    if (__any_sync(0xffffffffu, bad)) st.s = __int_as_float(0x7fc00000);
+    return st;
+}
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kRowThreads)
+rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
+            bool vec_ok, const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int wpb = blockDim.x / kWarp;
+    const int64_t total = (int64_t)n_trees * (B + 1) * nch;
+    const int64_t stride = (int64_t)gridDim.x * wpb;
+    for (int64_t item = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; item < total;
+         item += stride) {
+        const int64_t row = item / nch;
+        const int ch = (int)(item - row * nch);
+        const int t = (int)(row / (B + 1));
+        const int v = (int)(row - (int64_t)t * (B + 1));
+        if (v >= __ldg(n_nodes + t) || ws.tstat[t] != kStatOk) continue;
+        const int64_t c0 = (int64_t)ch * CE;
+        const int cn = (int)min((int64_t)CE, V - c0);
+        const T* rp = logits + row * V + c0;
+        int clo = 0, chi = 0;
+        const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+        if (!GREEDY) {
+            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+            const int b0 = cptr[v], b1 = cptr[v + 1];
+            if (b1 > b0) {
+                clo = lower_bound_i32(ctok, b0, b1, c0);
+                chi = lower_bound_i32(ctok, clo, b1, c0 + cn);
+            }
+        }
+        const ChunkStat st = vec_ok
+            ? reduce_chunk_vec<T, GREEDY>(rp, cn, c, ctok, clo, chi, c0, lane)
+            : reduce_chunk_scalar<T, GREEDY>(rp, cn, c, ctok, clo, chi, c0, lane);
+        if (lane == 0) ws.chunk[item] = st;
+    }
+}
+
+static int row_grid(int64_t items) {
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int wpb = kRowThreads / kWarp;
+    const int64_t want = (items + wpb - 1) / wpb;
+    const int64_t cap = (int64_t)sms * 8;  // a few resident CTAs per SM, grid-stride beyond
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+cudaError_t launch_rows(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                        float c, bool greedy, const int32_t* n_nodes, const VerifyWs& ws,
+                        cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
+    const int grid = row_grid((int64_t)n_trees * (B + 1) * nch);
+    if (dtype == TSD_BF16) {
+        const auto* p = static_cast<const __nv_bfloat16*>(logits);
+        if (greedy)
+            rows_kernel<__nv_bfloat16, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+        else
+            rows_kernel<__nv_bfloat16, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+    } else {
+        const auto* p = static_cast<const float*>(logits);
+        if (greedy)
+            rows_kernel<float, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+        else
+            rows_kernel<float, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Per-node combination: row max / sums, p_v(x_u) of each child, rho(v).
+// ---------------------------------------------------------------------------
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kRowThreads)
+node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
+                    const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int wpb = blockDim.x / kWarp;
+    const int64_t rows = (int64_t)n_trees * (B + 1);
+    for (int64_t row = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; row < rows;
+         row += (int64_t)gridDim.x * wpb) {
+        const int t = (int)(row / (B + 1));
+        const int v = (int)(row - (int64_t)t * (B + 1));
+        if (v >= n_nodes[t] || ws.tstat[t] != kStatOk) continue;
+        const ChunkStat* cs = ws.chunk + row * nch;
+        const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+        const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+        const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
+        float* pedge = ws.pedge + (int64_t)t * (B + 1);
+        const int b0 = cptr[v], b1 = cptr[v + 1];
+        NodeStat ns;
+        bool bad = false;
+        if (GREEDY) {
+            float bm = -INFINITY;
+            int bi = INT_MAX;
+            for (int q = lane; q < nch; q += kWarp) {
+                const ChunkStat s = cs[q];
+                bad |= (s.s != s.s);
+                if (better(s.m, s.amax, bm, bi)) {
+                    bm = s.m;
+                    bi = s.amax;
+                }
+            }
+            warp_argmax(bm, bi);
+            ns.mc = bm;
+            ns.s = 1.0f;
+            ns.amax = bi;
+            bool hit = false;  // is the arg-max a drafted child?
+            for (int q = b0 + lane; q < b1; q += kWarp) {
+                const bool h = (ctok[q] == bi);
+                pedge[cnode[q]] = h ? 1.0f : 0.0f;
+                hit |= h;
+            }
+            ns.r = __any_sync(0xffffffffu, hit) ? 0.0f : 1.0f;
+        } else {
+            float m = -INFINITY;
+            for (int q = lane; q < nch; q += kWarp) m = fmaxf(m, cs[q].m);
+            m = warp_max(m);
+            const float mc = __fmul_rn(m, c);
+            float s = 0.0f, r = 0.0f;
+            for (int q = lane; q < nch; q += kWarp) {
+                const ChunkStat x = cs[q];
+                bad |= (x.s != x.s);
+                if (x.m != -INFINITY) {
+                    const float f = ex2(__fmul_rn(x.m, c) - mc);
+                    s += x.s * f;
+                    r += x.r * f;
+                }
+            }
+            s = warp_sum(s);
+            r = warp_sum(r);
+            bad = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0f);
+            ns.mc = mc;
+            ns.s = s;
+            ns.r = r;
+            ns.amax = -1;
+            if (!bad) {
+                const T* rp = logits + row * V;
+                const float inv_s = 1.0f / s;
+                for (int q = b0 + lane; q < b1; q += kWarp) {
+                    const float z = load_logit(rp + ctok[q]);
+                    pedge[cnode[q]] = ex2(fmaf(z, c, -mc)) * inv_s;
+                }
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            ws.node[row] = ns;
+            ws.rho[row] = GREEDY ? ns.r : (bad ? 0.0f : ns.r / ns.s);
+            if (bad) atomicExch(ws.tstat + t, kStatNonFinite);
+        }
+    }
+}
+
+cudaError_t launch_node_combine(const void* logits, tsd_dtype dtype, int n_trees, int B,
+                                int64_t V, float c, bool greedy, const int32_t* n_nodes,
+                                const VerifyWs& ws, cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const int grid = row_grid((int64_t)n_trees * (B + 1));
+    if (dtype == TSD_BF16) {
+        const auto* p = static_cast<const __nv_bfloat16*>(logits);
+        if (greedy)
+            node_combine_kernel<__nv_bfloat16, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+        else
+            node_combine_kernel<__nv_bfloat16, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+    } else {
+        const auto* p = static_cast<const float*>(logits);
+        if (greedy)
+            node_combine_kernel<float, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+        else
+            node_combine_kernel<float, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tsd

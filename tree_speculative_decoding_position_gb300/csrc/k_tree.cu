@@ -1,0 +1,416 @@
+// k_tree.cu -- the per-tree part of Tree Exit Verification and the
+// predraw-and-follow check.
+//
+// TEV, "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
+// Decoding", App. B Algorithm 1:
+//   lines 3-7  P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u) (Eq. 2), rho(v) from the
+//              row reduction, w(v) = P(v) rho(v) (Eq. 4), C_p (Eq. 6);
+//   line 8     V ~ Categorical(w): inverse CDF over node index;
+//   line 9     Y ~ p_V restricted to non-child tokens and renormalised (Eq. 7;
+//              p_V at a leaf), inverse CDF over token id: the chunk is found
+//              from the stored per-chunk residual sums, then only that chunk
+//              of row V is read again.
+// Predraw-and-follow (same page, Sec. 2 and App. A.4.1): R_v ~ p_v at every
+// node, then a walk from the root into the child whose token is R_v.
+#include "tsd_internal.cuh"
+
+namespace tsd {
+
+constexpr int kTreeThreads = 512;
+
+// Exclusive prefix sum of one float per thread across the block; *total gets
+// the block sum.  `red` is shared scratch of 32 floats.
+__device__ float block_excl_scan(float x, float* red, float* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const float inc = warp_incl_scan(x, lane);
+    if (lane == 31) red[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const float y = lane < nw ? red[lane] : 0.0f;
+        const float yi = warp_incl_scan(y, lane);
+        red[lane] = yi - y;  // exclusive over warps
+        if (lane == 31) red[32] = yi;
+    }
+    __syncthreads();
+    const float r = red[wid] + inc - x;
+    *total = red[32];
+    __syncthreads();
+    return r;
+}
+
+// Residual bonus draw on one chunk of one row, by the whole block: the first
+// token a (ascending, skipping drafted children) whose running sum of
+// exp2(z*c - mc) exceeds frac * (the chunk's total).  Returns -1 only if the
+// chunk has no mass.
+template <typename T>
+__device__ int draw_in_chunk_block(const T* __restrict__ rp, int64_t c0, int cn, float c,
+                                   float mc, float frac, const int32_t* __restrict__ ctok,
+                                   int clo, int chi, float* red, int* pick) {
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    constexpr int per = CE / kTreeThreads;  // elements per thread (8 bf16, 4 fp32)
+    const int beg = threadIdx.x * per;
+    float e[8];
+    float sum = 0.0f;
+    for (int j = 0; j < per; ++j) {
+        const int o = beg + j;
+        float v = 0.0f;
+        if (o < cn) {
+            bool child = false;
+            for (int q = clo; q < chi; ++q) child |= ((int64_t)ctok[q] == c0 + o);
+            if (!child) v = ex2(fmaf(load_logit(rp + o), c, -mc));
+        }
+        e[j] = v;
+        sum += v;
+    }
+    float total;
+    const float before = block_excl_scan(sum, red, &total);
+    const float target = frac * total;
+    if (threadIdx.x == 0) {
+        pick[0] = INT_MAX;
+        pick[1] = -1;
+    }
+    __syncthreads();
+    float run = before;
+    int last = -1;
+    for (int j = 0; j < per; ++j) {
+        run += e[j];
+        if (e[j] > 0.0f) last = beg + j;
+        if (run > target && e[j] > 0.0f) {
+            atomicMin(pick, beg + j);
+            break;
+        }
+    }
+    if (last >= 0) atomicMax(pick + 1, last);
+    __syncthreads();
+    const int r = pick[0] != INT_MAX ? pick[0] : pick[1];
+    __syncthreads();
+    return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTreeThreads)
+tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, bool greedy,
+                uint64_t seed, const int32_t* __restrict__ parent,
+                const int32_t* __restrict__ n_nodes, VerifyWs ws, int32_t* __restrict__ exit_node,
+                int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
+                float* __restrict__ exit_mass, float* __restrict__ prefix_prob,
+                float* __restrict__ coverage, int32_t* __restrict__ status) {
+    extern __shared__ float sh[];  // w[B+1]
+    __shared__ float red[33];
+    __shared__ int pick[2];
+    __shared__ int exit_v;
+    const int t = blockIdx.x;
+    const int stride = B + 1;
+    const int n = n_nodes[t];
+    const int st = ws.tstat[t];
+    if (st != kStatOk) {
+        for (int v = threadIdx.x; v < stride; v += blockDim.x) {
+            if (exit_mass) exit_mass[(int64_t)t * stride + v] = 0.0f;
+            if (prefix_prob) prefix_prob[(int64_t)t * stride + v] = 0.0f;
+        }
+        if (threadIdx.x == 0) {
+            exit_node[t] = -1;
+            bonus[t] = -1;
+            accept_len[t] = 0;
+            if (coverage) coverage[t] = 0.0f;
+            status[t] = st;
+        }
+        return;
+    }
+    const int32_t* par = parent + (int64_t)t * stride;
+    const float* pedge = ws.pedge + (int64_t)t * stride;
+    const float* rho = ws.rho + (int64_t)t * stride;
+    float* w = sh;
+    // Alg. 1 lines 3-7: P(u) as the product of the edge probabilities on the
+    // root path (depth-parallel: every node walks its own ancestors).
+    float cov_part = 0.0f;
+    for (int u = threadIdx.x; u < stride; u += blockDim.x) {
+        float P = 0.0f, wu = 0.0f;
+        if (u < n) {
+            P = 1.0f;
+            for (int x = u; x > 0; x = par[x]) P *= pedge[x];
+            wu = P * rho[u];
+            if (u > 0) cov_part += P;
+        }
+        w[u] = wu;
+        if (exit_mass) exit_mass[(int64_t)t * stride + u] = wu;
+        if (prefix_prob) prefix_prob[(int64_t)t * stride + u] = P;
+    }
+    float cov;
+    block_excl_scan(cov_part, red, &cov);
+    // Line 8: inverse CDF over nodes.  Each thread owns a contiguous run of
+    // nodes so that the block scan follows node order.
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int nb = threadIdx.x * per, ne = min(n, nb + per);
+    float mine = 0.0f;
+    for (int v = nb; v < ne; ++v) mine += w[v];
+    float wsum;
+    float run = block_excl_scan(mine, red, &wsum);
+    const float thr = uniform24(seed, t, 0, 0) * wsum;
+    if (threadIdx.x == 0) {
+        pick[0] = INT_MAX;
+        pick[1] = -1;
+    }
+    __syncthreads();
+    int last = -1;
+    for (int v = nb; v < ne; ++v) {
+        run += w[v];
+        if (w[v] > 0.0f) last = v;
+        if (run > thr && w[v] > 0.0f) {
+            atomicMin(pick, v);
+            break;
+        }
+    }
+    if (last >= 0) atomicMax(pick + 1, last);
+    __syncthreads();
+    if (threadIdx.x == 0) exit_v = pick[0] != INT_MAX ? pick[0] : (pick[1] >= 0 ? pick[1] : 0);
+    __syncthreads();
+    const int V_ = exit_v;
+    const int64_t row = (int64_t)t * stride + V_;
+    const NodeStat ns = ws.node[row];
+    int y;
+    if (greedy) {
+        y = ns.amax;  // Line 9 at T = 0: the arg-max is not a child of the exit node
+    } else {
+        // Line 9: residual draw.  Chunk sums relative to the row reference.
+        const ChunkStat* cs = ws.chunk + row * nch;
+        const float thr2 = uniform24(seed, t, 0, 1) * ns.r;
+        __shared__ int chunk_sel;
+        __shared__ float chunk_frac;
+        if (threadIdx.x < kWarp) {
+            const int lane = threadIdx.x;
+            float base = 0.0f;
+            int sel = -1, lastc = -1;
+            float frac = 0.0f;
+            for (int q0 = 0; q0 < nch && sel < 0; q0 += kWarp) {
+                const int q = q0 + lane;
+                float rq = 0.0f;
+                if (q < nch && cs[q].m != -INFINITY) rq = cs[q].r * ex2(__fmul_rn(cs[q].m, c) - ns.mc);
+                const float inc = warp_incl_scan(rq, lane) + base;
+                const unsigned hit = __ballot_sync(0xffffffffu, inc > thr2 && rq > 0.0f);
+                const unsigned pos = __ballot_sync(0xffffffffu, rq > 0.0f);
+                if (pos) lastc = q0 + 31 - __clz(pos);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    sel = q0 + l;
+                    const float incl = __shfl_sync(0xffffffffu, inc, l);
+                    const float own = __shfl_sync(0xffffffffu, rq, l);
+                    frac = (thr2 - (incl - own)) / own;
+                }
+                base = __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (sel < 0) {  // rounding left the threshold past the last chunk
+                sel = lastc;
+                frac = 1.0f;
+            }
+            if (lane == 0) {
+                chunk_sel = sel;
+                chunk_frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
+            }
+        }
+        __syncthreads();
+        const int q = chunk_sel;
+        y = -1;
+        if (q >= 0) {
+            constexpr int CE = kChunkBytes / (int)sizeof(T);
+            const int64_t c0 = (int64_t)q * CE;
+            const int cn = (int)min((int64_t)CE, V - c0);
+            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+            const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+            int clo = cptr[V_], chi = cptr[V_ + 1];
+            while (clo < chi && ctok[clo] < c0) ++clo;  // children are sorted by token
+            int chh = clo;
+            while (chh < chi && ctok[chh] < c0 + cn) ++chh;
+            const int o = draw_in_chunk_block<T>(logits + row * V + c0, c0, cn, c,
+                                                 __fmul_rn(cs[q].m, c), chunk_frac, ctok, clo,
+                                                 chh, red, pick);
+            y = o >= 0 ? (int)(c0 + o) : -1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        exit_node[t] = V_;
+        bonus[t] = y;
+        accept_len[t] = ws.depth[(int64_t)t * stride + V_] + 1;
+        if (coverage) coverage[t] = cov;
+        status[t] = y >= 0 ? kStatOk : kStatNonFinite;
+    }
+}
+
+cudaError_t launch_tev_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                            float c, bool greedy, uint64_t seed, const int32_t* parent,
+                            const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                            int32_t* bonus, int32_t* accept_len, float* exit_mass,
+                            float* prefix_prob, float* coverage, int32_t* status,
+                            cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const size_t smem = sizeof(float) * (size_t)(B + 1);
+    if (dtype == TSD_BF16)
+        tev_tree_kernel<__nv_bfloat16><<<n_trees, kTreeThreads, smem, stream>>>(
+            static_cast<const __nv_bfloat16*>(logits), B, V, nch, c, greedy, seed, parent, n_nodes,
+            ws, exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status);
+    else
+        tev_tree_kernel<float><<<n_trees, kTreeThreads, smem, stream>>>(
+            static_cast<const float*>(logits), B, V, nch, c, greedy, seed, parent, n_nodes, ws,
+            exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Predraw-and-follow.
+// ---------------------------------------------------------------------------
+constexpr int kDrawThreads = 256;
+
+// One warp per node: R_v ~ p_v by inverse CDF over token id.
+template <typename T>
+__global__ void __launch_bounds__(kDrawThreads)
+predraw_nodes_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
+                     bool greedy, uint64_t seed, const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    constexpr int PER = CE / kWarp;  // tokens per lane in one chunk (128 bf16, 64 fp32)
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int wpb = blockDim.x / kWarp;
+    const int64_t rows = (int64_t)n_trees * (B + 1);
+    for (int64_t row = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; row < rows;
+         row += (int64_t)gridDim.x * wpb) {
+        const int t = (int)(row / (B + 1));
+        const int v = (int)(row - (int64_t)t * (B + 1));
+        if (v >= n_nodes[t] || ws.tstat[t] != kStatOk) continue;
+        const NodeStat ns = ws.node[row];
+        if (greedy) {
+            if (lane == 0) ws.draws[row] = ns.amax;
+            continue;
+        }
+        const ChunkStat* cs = ws.chunk + row * nch;
+        const float thr = uniform24(seed, t, v, 2) * ns.s;
+        float base = 0.0f, frac = 1.0f;
+        int sel = -1, lastc = -1;
+        for (int q0 = 0; q0 < nch && sel < 0; q0 += kWarp) {
+            const int q = q0 + lane;
+            float sq = 0.0f;
+            if (q < nch && cs[q].m != -INFINITY) sq = cs[q].s * ex2(__fmul_rn(cs[q].m, c) - ns.mc);
+            const float inc = warp_incl_scan(sq, lane) + base;
+            const unsigned hit = __ballot_sync(0xffffffffu, inc > thr && sq > 0.0f);
+            const unsigned pos = __ballot_sync(0xffffffffu, sq > 0.0f);
+            if (pos) lastc = q0 + 31 - __clz(pos);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                sel = q0 + l;
+                const float incl = __shfl_sync(0xffffffffu, inc, l);
+                const float own = __shfl_sync(0xffffffffu, sq, l);
+                frac = (thr - (incl - own)) / own;
+            }
+            base = __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (sel < 0) sel = lastc;
+        frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
+        int r = -1;
+        if (sel >= 0) {
+            const int64_t c0 = (int64_t)sel * CE;
+            const int cn = (int)min((int64_t)CE, V - c0);
+            const float mc = __fmul_rn(cs[sel].m, c);
+            const T* rp = logits + row * V + c0;
+            // lane l scans tokens [l*PER, (l+1)*PER) of the chunk
+            float sum = 0.0f;
+            for (int j = 0; j < PER; ++j) {
+                const int o = lane * PER + j;
+                if (o < cn) sum += ex2(fmaf(load_logit(rp + o), c, -mc));
+            }
+            const float inc = warp_incl_scan(sum, lane);
+            const float total = __shfl_sync(0xffffffffu, inc, 31);
+            const float target = frac * total;
+            float run = inc - sum;
+            int found = -1, lastp = -1;
+            for (int j = 0; j < PER; ++j) {
+                const int o = lane * PER + j;
+                if (o >= cn) break;
+                const float e = ex2(fmaf(load_logit(rp + o), c, -mc));
+                run += e;
+                if (e > 0.0f) lastp = o;
+                if (run > target && e > 0.0f) {
+                    found = o;
+                    break;
+                }
+            }
+            const unsigned f = __ballot_sync(0xffffffffu, found >= 0);
+            if (f) {
+                r = __shfl_sync(0xffffffffu, found, __ffs(f) - 1);
+            } else {
+                const unsigned lp = __ballot_sync(0xffffffffu, lastp >= 0);
+                r = lp ? __shfl_sync(0xffffffffu, lastp, 31 - __clz(lp)) : -1;
+            }
+            if (r >= 0) r += (int)c0;
+        }
+        if (lane == 0) {
+            ws.draws[row] = r;
+            if (r < 0) atomicExch(ws.tstat + t, kStatNonFinite);
+        }
+    }
+}
+
+// One thread per tree: follow R_v from the root.
+__global__ void predraw_walk_kernel(int n_trees, int B, const int32_t* __restrict__ n_nodes,
+                                    VerifyWs ws, int32_t* __restrict__ exit_node,
+                                    int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
+                                    int32_t* __restrict__ draws, int32_t* __restrict__ status) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_trees) return;
+    const int stride = B + 1;
+    const int n = n_nodes[t];
+    const int st = ws.tstat[t];
+    if (draws)
+        for (int v = 0; v < stride; ++v)
+            draws[(int64_t)t * stride + v] = (st == kStatOk && v < n) ? ws.draws[(int64_t)t * stride + v] : -1;
+    if (st != kStatOk) {
+        exit_node[t] = -1;
+        bonus[t] = -1;
+        accept_len[t] = 0;
+        status[t] = st;
+        return;
+    }
+    const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+    const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+    const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
+    int v = 0;
+    for (int step = 0; step < n; ++step) {
+        const int r = ws.draws[(int64_t)t * stride + v];
+        int lo = cptr[v], hi = cptr[v + 1];
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (ctok[mid] < r) lo = mid + 1;
+            else hi = mid;
+        }
+        if (lo < cptr[v + 1] && ctok[lo] == r) v = cnode[lo];
+        else break;
+    }
+    exit_node[t] = v;
+    bonus[t] = ws.draws[(int64_t)t * stride + v];
+    accept_len[t] = ws.depth[(int64_t)t * stride + v] + 1;
+    status[t] = kStatOk;
+}
+
+cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                           float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
+                           const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                           int32_t* accept_len, int32_t* draws, int32_t* status,
+                           cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const int64_t rows = (int64_t)n_trees * (B + 1);
+    const int wpb = kDrawThreads / kWarp;
+    const int64_t want = (rows + wpb - 1) / wpb;
+    const int grid = (int)(want < 65535 * 8 ? want : 65535 * 8);
+    if (dtype == TSD_BF16)
+        predraw_nodes_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws);
+    else
+        predraw_nodes_kernel<float><<<grid, kDrawThreads, 0, stream>>>(
+            static_cast<const float*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    predraw_walk_kernel<<<(n_trees + 127) / 128, 128, 0, stream>>>(n_trees, B, n_nodes, ws, exit_node,
+                                                                 bonus, accept_len, draws, status);
+    return cudaGetLastError();
+}
+
+}  // namespace tsd

@@ -1,0 +1,216 @@
+// tsd_api.cu -- the C entry points declared in include/tsd.h: argument
+// checks on the host, workspace layout, and the kernel launches.  Nothing here
+// allocates or synchronises.
+#include <math.h>
+
+#include "tsd_internal.cuh"
+
+namespace tsd {
+
+size_t heap_spill_bytes(int n_modes, int L, int topk, int B);  // k_heap.cu
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Carve {
+    uint8_t* base;
+    size_t off = 0;
+    template <typename T>
+    T* take(size_t count) {
+        off = (off + kAlign - 1) & ~(kAlign - 1);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += sizeof(T) * count;
+        return p;
+    }
+};
+
+int dtype_size(tsd_dtype d) { return d == TSD_BF16 ? 2 : (d == TSD_F32 ? 4 : 0); }
+
+bool temp_ok(float T) { return isfinite(T) && (T == 0.0f || T >= 1e-6f); }
+
+// c = log2(e) / T rounded once to float; the kernels evaluate
+// exp(z/T - m/T) as exp2(fma(z, c, -fl(m*c))).
+float exp2_scale(double T) { return (float)(1.4426950408889634 / T); }
+
+bool verify_args_ok(const void* logits, tsd_dtype dtype, const int32_t* parent,
+                    const int32_t* token, const int32_t* n_nodes, int n_trees, int B, int64_t V,
+                    float temperature, const int32_t* exit_node, const int32_t* bonus,
+                    const int32_t* accept_len, const int32_t* status) {
+    return logits && parent && token && n_nodes && exit_node && bonus && accept_len && status &&
+           dtype_size(dtype) && n_trees >= 1 && B >= 0 && B <= TSD_MAX_B && V >= 1 &&
+           V <= 0x7fffffff && temp_ok(temperature);
+}
+
+}  // namespace
+
+size_t verify_ws_layout(int n_trees, int B, int64_t V, int esize, void* base, VerifyWs* out) {
+    Carve cv{static_cast<uint8_t*>(base)};
+    const size_t nt = (size_t)n_trees, nodes = nt * (size_t)(B + 1);
+    VerifyWs ws;
+    ws.child_ptr = cv.take<int32_t>(nt * (size_t)(B + 2));
+    ws.child_tok = cv.take<int32_t>(nodes);
+    ws.child_node = cv.take<int32_t>(nodes);
+    ws.depth = cv.take<int32_t>(nodes);
+    ws.tstat = cv.take<int32_t>(nt);
+    ws.node = cv.take<NodeStat>(nodes);
+    ws.pedge = cv.take<float>(nodes);
+    ws.rho = cv.take<float>(nodes);
+    ws.draws = cv.take<int32_t>(nodes);
+    ws.chunk = cv.take<ChunkStat>(nodes * (size_t)n_chunks(V, esize));
+    if (out) *out = ws;
+    return (cv.off + kAlign - 1) & ~(kAlign - 1);
+}
+
+size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
+                       void* base, BuildWs* out) {
+    Carve cv{static_cast<uint8_t*>(base)};
+    const size_t rows = (size_t)n_trees * n_modes * L;
+    const size_t nch = (size_t)n_chunks(V, esize);
+    BuildWs ws;
+    ws.chunk = cv.take<ChunkStat>(rows * nch);
+    ws.cand_v = cv.take<float>(rows * nch * topk);
+    ws.cand_i = cv.take<int32_t>(rows * nch * topk);
+    ws.top_id = cv.take<int32_t>(rows * topk);
+    ws.top_lq = cv.take<double>(rows * topk);
+    ws.heap_stride = (heap_spill_bytes(n_modes, L, topk, B) + kAlign - 1) & ~(kAlign - 1);
+    ws.heap = cv.take<uint8_t>((size_t)n_trees * ws.heap_stride);
+    if (out) *out = ws;
+    return (cv.off + kAlign - 1) & ~(kAlign - 1);
+}
+
+}  // namespace tsd
+
+using namespace tsd;
+
+extern "C" {
+
+const char* tsd_status_string(tsd_status s) {
+    switch (s) {
+        case TSD_OK: return "ok";
+        case TSD_ERR_INVALID_ARG: return "invalid argument";
+        case TSD_ERR_CUDA: return "CUDA launch failed";
+        case TSD_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case TSD_ERR_BAD_TREE: return "malformed tree";
+        case TSD_ERR_NONFINITE: return "non-finite logits or a row without mass";
+        case TSD_ERR_TIMEOUT: return "timed out";
+    }
+    return "unknown status";
+}
+
+static bool build_sizes_ok(int n_trees, int n_modes, int L, int64_t V, int topk, int B) {
+    if (n_trees < 1 || n_modes < 1 || n_modes > TSD_MAX_MODES || L < 1 || L > TSD_MAX_L ||
+        V < 1 || V > 0x7fffffff || topk < 1 || topk > TSD_MAX_TOPK || topk > V || B < 0 ||
+        B > TSD_MAX_B)
+        return false;
+    int bits = 0;
+    while ((1 << bits) < topk) ++bits;
+    return (int64_t)L * bits <= 56;
+}
+
+size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V, int topk, int B,
+                          tsd_dtype dtype) {
+    const int es = dtype_size(dtype);
+    if (!es) return 0;
+    switch (op) {
+        case TSD_OP_BUILD_TREE:
+            if (!build_sizes_ok(n_trees, n_modes, L, V, topk, B)) return 0;
+            return build_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr);
+        case TSD_OP_VERIFY_TEV:
+        case TSD_OP_VERIFY_DDTREE:
+            if (n_trees < 1 || B < 0 || B > TSD_MAX_B || V < 1 || V > 0x7fffffff) return 0;
+            return verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+    }
+    return 0;
+}
+
+tsd_status tsd_build_tree(const void* drafter_logits, tsd_dtype dtype, int n_trees, int n_modes,
+                          int L, int64_t V, int topk, int B, float drafter_temp,
+                          int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                          int32_t* rank, int32_t* mode, int32_t* n_nodes, int32_t* status,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!drafter_logits || !parent || !token || !depth || !score || !n_nodes || !status ||
+        !dtype_size(dtype) || !build_sizes_ok(n_trees, n_modes, L, V, topk, B) ||
+        !(isfinite(drafter_temp) && drafter_temp >= 1e-6f))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = build_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    BuildWs ws;
+    build_ws_layout(n_trees, n_modes, L, V, topk, B, es, workspace, &ws);
+    const int64_t rows = (int64_t)n_trees * n_modes * L;
+    if (launch_drafter_stats(drafter_logits, dtype, rows, V, topk, exp2_scale(drafter_temp),
+                             (double)drafter_temp, ws, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    if (launch_build_heap(ws, n_trees, n_modes, L, topk, B, parent, token, depth, score, rank,
+                          mode, n_nodes, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_tree_mask(const int32_t* parent, const int32_t* n_nodes, int n_trees, int B,
+                         int prefix_len, uint32_t* anc_bits, int32_t* position_ids,
+                         float* additive_mask, int64_t mask_ld, int32_t* status,
+                         cudaStream_t stream) {
+    if (!parent || !n_nodes || !anc_bits || !position_ids || !status || n_trees < 1 || B < 0 ||
+        B > TSD_MAX_B || prefix_len < 0 ||
+        (additive_mask && mask_ld < (int64_t)prefix_len + B + 1))
+        return TSD_ERR_INVALID_ARG;
+    if (launch_tree_mask(parent, n_nodes, n_trees, B, prefix_len, anc_bits, position_ids,
+                         additive_mask, mask_ld, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_verify_tev(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                          const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                          int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
+                          int32_t* bonus_token, int32_t* accept_len, float* exit_mass,
+                          float* prefix_prob, float* coverage, int32_t* status, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+    if (!verify_args_ok(target_logits, dtype, parent, token, n_nodes, n_trees, B, V, temperature,
+                        exit_node, bonus_token, accept_len, status))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    VerifyWs ws;
+    verify_ws_layout(n_trees, B, V, es, workspace, &ws);
+    const bool greedy = temperature == 0.0f;
+    const float c = greedy ? 1.0f : exp2_scale(temperature);
+    if (launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
+        launch_rows(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        launch_tev_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, parent, n_nodes, ws,
+                        exit_node, bonus_token, accept_len, exit_mass, prefix_prob, coverage,
+                        status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                             const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                             int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
+                             int32_t* bonus_token, int32_t* accept_len, int32_t* draws,
+                             int32_t* status, void* workspace, size_t ws_bytes,
+                             cudaStream_t stream) {
+    if (!verify_args_ok(target_logits, dtype, parent, token, n_nodes, n_trees, B, V, temperature,
+                        exit_node, bonus_token, accept_len, status))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    VerifyWs ws;
+    verify_ws_layout(n_trees, B, V, es, workspace, &ws);
+    const bool greedy = temperature == 0.0f;
+    const float c = greedy ? 1.0f : exp2_scale(temperature);
+    if (launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
+        launch_rows(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        launch_predraw(target_logits, dtype, n_trees, B, V, c, greedy, seed, n_nodes, ws,
+                       exit_node, bonus_token, accept_len, draws, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,211 @@
+// tsd_internal.cuh -- device helpers and launch declarations shared by the
+// kernels of the GB300 bounded-tree speculative decoding library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tsd.h"
+
+namespace tsd {
+
+constexpr int kWarp = 32;
+
+// A logits row is processed in chunks of 8 KB (4096 bf16 or 2048 fp32
+// tokens); one warp reduces one chunk with sixteen 16-byte loads per lane.
+constexpr int kChunkBytes = 8192;
+constexpr int kVecPerLane = kChunkBytes / (16 * kWarp);  // 16
+
+__host__ __device__ constexpr int chunk_elems(int esize) { return kChunkBytes / esize; }
+__host__ __device__ inline int64_t n_chunks(int64_t V, int esize) {
+    return (V + chunk_elems(esize) - 1) / chunk_elems(esize);
+}
+
+// Per-(row, chunk) reduction of a logits row.
+//   m    the chunk's largest raw logit (-inf if every token is -inf)
+//   s    sum over the chunk of exp2(z*c - mc), mc = fl(m*c), c = log2(e)/T
+//   r    the same sum over tokens that are not drafted children of the row
+//   amax lowest token id holding m (greedy); at T = 0, s is NaN when the
+//        chunk holds a NaN or +inf logit and 0 otherwise.
+struct ChunkStat {
+    float m, s, r;
+    int32_t amax;
+};
+
+// Per-node combination of its chunks (same reference mc for s and r).
+struct NodeStat {
+    float mc;      // fl(m*c) of the row maximum (greedy: the maximum itself)
+    float s, r;    // row sums relative to mc
+    int32_t amax;  // arg-max (lowest id) of the row
+};
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 64x64 -> 128-bit multiplies with a Weyl key schedule.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t philox_x0(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3,
+                                              uint64_t k0, uint64_t k1) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    return c0;
+}
+
+// The uniform on the 2^-24 grid for (seed; tree, node, stream).
+__device__ __forceinline__ float uniform24(uint64_t seed, uint64_t tree, uint64_t node,
+                                           uint64_t stream) {
+    const uint64_t x0 = philox_x0(tree, node, stream, 0, seed, 0);
+    return (float)(x0 >> 40) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Element access.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float load_logit(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load_logit(const float* p) { return *p; }
+
+// 16-byte streaming load (read once; do not keep in L1).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// MUFU base-2 exponential (ex2.approx.ftz: about 2 ulp).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// (value desc, id asc) order on (logit, token) pairs.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+    return a > b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+// Arg-max with ties to the lower id; every lane gets the result.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (better(ov, oi, v, i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+// Inclusive prefix sum across the warp.
+__device__ __forceinline__ float warp_incl_scan(float x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+__device__ __forceinline__ bool is_bad_logit(float x) { return x != x || x == __int_as_float(0x7f800000); }
+
+// ---------------------------------------------------------------------------
+// Workspace layout of the verifiers (TEV and predraw), per call.
+// ---------------------------------------------------------------------------
+struct VerifyWs {
+    int32_t* child_ptr;   // [n_trees][B+2] CSR offsets of each node's children
+    int32_t* child_tok;   // [n_trees][B+1] children's tokens, sorted per node
+    int32_t* child_node;  // [n_trees][B+1] the matching child node ids
+    int32_t* depth;       // [n_trees][B+1]
+    int32_t* tstat;       // [n_trees] internal per-tree status
+    NodeStat* node;       // [n_trees][B+1]
+    float* pedge;         // [n_trees][B+1] p_pa(u)(x_u)
+    float* rho;           // [n_trees][B+1]
+    int32_t* draws;       // [n_trees][B+1] predraw R_v
+    ChunkStat* chunk;     // [n_trees][B+1][n_chunks]
+};
+size_t verify_ws_layout(int n_trees, int B, int64_t V, int esize, void* base, VerifyWs* out);
+
+struct BuildWs {
+    ChunkStat* chunk;    // [rows][n_chunks] (m, s)
+    float* cand_v;       // [rows][n_chunks][topk] chunk top-k logits
+    int32_t* cand_i;     // [rows][n_chunks][topk] and ids
+    int32_t* top_id;     // [rows][topk]
+    double* top_lq;      // [rows][topk]
+    uint8_t* heap;       // [n_trees][heap bytes] spill space when shared memory is short
+    size_t heap_stride;  // bytes per tree
+};
+size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
+                       void* base, BuildWs* out);
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (one per .cu file).  All return cudaGetLastError().
+// ---------------------------------------------------------------------------
+cudaError_t launch_verify_prep(const int32_t* parent, const int32_t* token, const int32_t* n_nodes,
+                               int n_trees, int B, int64_t V, const VerifyWs& ws,
+                               cudaStream_t stream);
+cudaError_t launch_rows(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                        float c, bool greedy, const int32_t* n_nodes, const VerifyWs& ws,
+                        cudaStream_t stream);
+cudaError_t launch_node_combine(const void* logits, tsd_dtype dtype, int n_trees, int B,
+                                int64_t V, float c, bool greedy, const int32_t* n_nodes,
+                                const VerifyWs& ws, cudaStream_t stream);
+cudaError_t launch_tev_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                            float c, bool greedy, uint64_t seed, const int32_t* parent,
+                            const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                            int32_t* bonus, int32_t* accept_len, float* exit_mass,
+                            float* prefix_prob, float* coverage, int32_t* status,
+                            cudaStream_t stream);
+cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                           float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
+                           const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                           int32_t* accept_len, int32_t* draws, int32_t* status,
+                           cudaStream_t stream);
+cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
+                                 int topk, float c, double temp, const BuildWs& ws,
+                                 cudaStream_t stream);
+cudaError_t launch_build_heap(const BuildWs& ws, int n_trees, int n_modes, int L, int topk, int B,
+                              int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                              int32_t* rank, int32_t* mode, int32_t* n_nodes, int32_t* status,
+                              cudaStream_t stream);
+cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int n_trees, int B,
+                             int prefix_len, uint32_t* anc_bits, int32_t* position_ids,
+                             float* additive_mask, int64_t mask_ld, int32_t* status,
+                             cudaStream_t stream);
+
+// Internal per-tree status values (tstat) match tsd_status codes.
+constexpr int32_t kStatOk = TSD_OK;
+constexpr int32_t kStatBadTree = TSD_ERR_BAD_TREE;
+constexpr int32_t kStatNonFinite = TSD_ERR_NONFINITE;
+
+}  // namespace tsd
