@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the bounded-tree speculative decoding hot path on GB300.
+
+One step = the whole path on one batch of synthetic input, resident in HBM:
+  tsd_build_tree  (drafter top-k + log-normaliser, best-first heap)
+  tsd_tree_mask   (ancestor bitmask + position ids)
+  tsd_verify_tev  (node-row reduction, per-node combination, exit and bonus draws)
+Workload (per GPU): 32 independent trees, V=151936, L=16, k=8, B=256, T=0.6,
+bf16 logits -- the batched verification configuration.  The metric is TEV
+rounds (trees verified) per second; the dominant kernel is the node-row
+reduction, reported against the measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+trees (weak scaling, no data-path collective); the step time is the max over
+ranks.  --impl reference times the float64 CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TEV verify rounds/sec and logits HBM GB/s (% of peak) at V=151936, B=64/256"
+WORKLOAD = dict(workload="batched verification: 32 independent trees, V=151936, L=16, "
+                         "top-k=8, B=256, T=0.6, bf16 (Gumbel-perturbed Zipf drafter; "
+                         "target = drafter row at node depth + N(0, 1.5^2))",
+                trees_per_gpu=32, V=151936, L=16, topk=8, B=256, temperature=0.6,
+                step="tsd_build_tree + tsd_tree_mask + tsd_verify_tev",
+                l2="inputs larger than L2: 2.66 GB of logits read per step per GPU, no flush")
+HBM_PEAK_FALLBACK = 6800.0
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_PEAK_FALLBACK, "fallback"
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the node-row reduction from the committed ncu
+    summary (null when absent)."""
+    p = os.path.join(ROOT, "profiles", "rows_kernel_b256.md")
+    try:
+        m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", open(p).read())
+        return float(m.group(1)) if m else None
+    except OSError:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Clocks: NVML read-only queries, polled during the timed region.
+# ---------------------------------------------------------------------------
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+            0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, uuid: str, period_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            return
+
+    def _poll(self):
+        mhz, reasons, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self._stop.is_set():
+            self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+            self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(reasons))
+            self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+            self.samples.append((int(mhz.value), int(reasons.value), pw.value / 1000.0))
+            time.sleep(self.period)
+
+    def start(self):
+        self.samples = []
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+
+    def stop(self) -> dict:
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        self._stop.set()
+        self._t.join()
+        s = self.samples
+        reasons = set()
+        for _, r, _ in s:
+            for bit, name in _REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in s) if s else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons), "samples": len(s),
+                "power_w_max": max((x[2] for x in s), default=None)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import synth
+    import tree_speculative_decoding_position_gb300 as tsd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tsd.load()
+
+    W = WORKLOAD
+    nt, V, L, k, B, T = W["trees_per_gpu"], W["V"], W["L"], W["topk"], W["B"], W["temperature"]
+    if args.trees:
+        nt = args.trees  # a smaller batch, for profiler captures only
+    seeds = [synth.seed_for(2, t) + 100000 * rank for t in range(nt)]
+    drafter = synth.zipf_drafter(nt, L, V, 0, device=dev, seeds=seeds)          # [nt,1,L,V]
+    tr = tsd.tsd_build_tree(drafter, topk=k, B=B)
+    target = torch.empty(nt, B + 1, V, dtype=torch.bfloat16, device=dev)
+    for t in range(nt):
+        n = int(tr["n_nodes"][t])
+        synth.target_from_rows(drafter[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1,
+                               out=target[t, :n])
+        target[t, n:] = 0
+    torch.cuda.synchronize()
+    ws_b = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, nt, 1, L, V, k, B,
+                                              torch.bfloat16), dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, nt, 1, 1, V, 1, B,
+                                              torch.bfloat16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        t_ = tsd.tsd_build_tree(drafter, topk=k, B=B, workspace=ws_b)
+        if ev is not None:
+            ev[1].record(stream)
+        tsd.tsd_tree_mask(t_["parent"], t_["n_nodes"], prefix_len=1024)
+        if ev is not None:
+            out = tsd.tsd_verify_tev_timed(target, t_["parent"], t_["token"], t_["n_nodes"], T,
+                                           seed=i, stage_events=ev[2:7], workspace=ws_v)
+        else:
+            out = tsd.tsd_verify_tev(target, t_["parent"], t_["token"], t_["n_nodes"], T,
+                                     seed=i, workspace=ws_v)
+        return t_, out
+
+    for i in range(args.warmup):
+        step(i)
+    evsets = [new_events(7) for _ in range(args.steps)]
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = new_events(2)
+    clocks.start()
+    start.record(stream)
+    last = None
+    for i in range(args.steps):
+        last = step(1000 + i, evsets[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    total_ms = float(ms_t.item())
+    assert int((last[1]["status"] != 0).sum()) == 0, "a tree failed in the timed region"
+
+    # stage durations from the events inside each step
+    def avg(a, b):
+        return statistics.mean(evsets[i][a].elapsed_time(evsets[i][b]) for i in range(args.steps))
+    stage = dict(build=avg(0, 1), mask=avg(1, 2), tev_prep=avg(2, 3), tev_rows=avg(3, 4),
+                 tev_combine=avg(4, 5), tev_draws=avg(5, 6))
+    n_nodes_total = int(last[0]["n_nodes"].sum())
+    rows_bytes = n_nodes_total * V * 2
+    peak, peak_kind = measured_peaks()
+    achieved = rows_bytes / (stage["tev_rows"] * 1e-3) / 1e9
+    ms_per_step = total_ms / args.steps
+    value = world * nt / (ms_per_step * 1e-3)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        drafter_h = torch.empty(drafter.shape, dtype=drafter.dtype, pin_memory=True)
+        target_h = torch.empty(target.shape, dtype=target.dtype, pin_memory=True)
+        drafter_h.copy_(drafter)
+        target_h.copy_(target)
+        res_h = torch.empty(3, nt, dtype=torch.int32, pin_memory=True)
+        ke = max(3, min(args.steps, 20))
+        for i in range(2):
+            drafter.copy_(drafter_h, non_blocking=True)
+            target.copy_(target_h, non_blocking=True)
+            _, o = step(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        s2, e2 = new_events(2)
+        s2.record(stream)
+        for i in range(ke):
+            drafter.copy_(drafter_h, non_blocking=True)
+            target.copy_(target_h, non_blocking=True)
+            _, o = step(2000 + i)
+            res_h[0].copy_(o["exit_node"], non_blocking=True)
+            res_h[1].copy_(o["bonus_token"], non_blocking=True)
+            res_h[2].copy_(o["accept_len"], non_blocking=True)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e_ms = torch.tensor([s2.elapsed_time(e2) / ke], dtype=torch.float64, device=dev)
+        if dist:
+            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * nt / (float(e_ms.item()) * 1e-3), "unit": "rounds/s",
+               "h2d_bytes_per_step": drafter.numel() * 2 + target.numel() * 2,
+               "d2h_bytes_per_step": res_h.numel() * 4, "steps": ke,
+               "ms_per_step": float(e_ms.item())}
+
+    # secondary measurements (not the headline): TEV alone vs predraw on the
+    # same trees, and the batch-1 Qwen-vocabulary round at B=64
+    extra = {"stage_ms": {k_: round(v, 4) for k_, v in stage.items()}}
+    if rank == 0 and not args.no_extra:
+        extra.update(secondary(tsd, torch, synth, dev, stream, last[0], target, T, ws_v, V))
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(drafter, target, last[0], k, B, T)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": dict(W, parallelism="replicas: dp%d over trees" % world),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": committed_traffic(),
+                     "kernel": "rows_kernel (node-row reduction)",
+                     "algorithmic_bytes_per_launch": rows_bytes,
+                     "peak_kind": peak_kind},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 8 * args.steps,
+        "clocks": clk, "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
+    out = {}
+    # verifier stage: TEV vs predraw-and-follow on the same 32 trees
+    for name, fn in (("tev", tsd.tsd_verify_tev), ("predraw", tsd.tsd_verify_ddtree)):
+        for i in range(3):
+            fn(target, tree["parent"], tree["token"], tree["n_nodes"], T, seed=i, workspace=ws_v)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for i in range(10):
+            fn(target, tree["parent"], tree["token"], tree["n_nodes"], T, seed=i, workspace=ws_v)
+        e.record(stream)
+        torch.cuda.synchronize()
+        out["verifier_ms_b256_x32_" + name] = s.elapsed_time(e) / 10
+    # batch-1 round, V=151936, B=64, T=1: 16 rotating copies (316 MB > 2x L2)
+    B1 = 64
+    dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device=dev)
+    t1 = tsd.tsd_build_tree(dr, topk=8, B=B1)
+    n = int(t1["n_nodes"][0])
+    copies = []
+    for c in range(16):
+        x = torch.zeros(1, B1 + 1, V, dtype=torch.bfloat16, device=dev)
+        synth.target_from_rows(dr[0, 0], t1["depth"][0, :n], 1.5, synth.seed_for(1, 1) + c,
+                               out=x[0, :n])
+        copies.append(x)
+    ws1 = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 1, 1, 1, V, 1, B1,
+                                             torch.bfloat16), dtype=torch.uint8, device=dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(48)]
+    for ev in evs:
+        for e in ev:
+            e.record(stream)
+    for i in range(8):
+        tsd.tsd_verify_tev(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
+                           seed=i, workspace=ws1)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(48):
+        tsd.tsd_verify_tev_timed(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
+                                 seed=i, stage_events=evs[i], workspace=ws1)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / 48
+    rows_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
+    out["b64_single_tree"] = {"tev_rounds_per_s": 1000.0 / ms, "tev_ms": ms,
+                              "rows_kernel_ms": rows_ms,
+                              "rows_kernel_gbs": n * V * 2 / (rows_ms * 1e-3) / 1e9}
+    return out
+
+
+def cpu_baseline(drafter, target, tree, k, B, T, budget_s=12.0):
+    """The float64 oracle as it stands, single-threaded on the host, on a
+    bounded sample of the same workload: whole trees (drafter statistics,
+    heap, mask, TEV) until about budget_s seconds of CPU work."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    nt = drafter.shape[0]
+    done, spent = 0, 0.0
+    for t in range(nt):
+        dr = drafter[t, 0].float().cpu().numpy()
+        n = int(tree["n_nodes"][t])
+        tg = target[t, :n].float().cpu().numpy()
+        t0 = time.perf_counter()
+        _, tid, tlq = oracle.drafter_stats(dr, 1.0, k)
+        ref = oracle.build_tree(tid, tlq, B)
+        oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
+        oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return {"value": done / spent, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of the %d trees of one step (build + mask + TEV per tree), "
+                      "float64, single thread, %.1f s" % (done, nt, spent)}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+    oracle.build()
+    W = WORKLOAD
+    nt, V, L, k, B, T = W["trees_per_gpu"], W["V"], W["L"], W["topk"], W["B"], W["temperature"]
+
+    cache = {}
+
+    def inputs(t):
+        """Synthetic inputs of tree t (generated once, outside the timing)."""
+        if t not in cache:
+            seed = synth.seed_for(2, t)
+            dr = synth.zipf_drafter(1, L, V, 0, device="cpu", seeds=[seed])[0, 0]
+            _, tid, tlq = oracle.drafter_stats(dr.float().numpy(), 1.0, k)
+            ref = oracle.build_tree(tid, tlq, B)
+            n = ref["n_nodes"]
+            tg = synth.target_from_rows(dr, ref["depth"][:n], 1.5, seed + 1).float().numpy()
+            cache[t] = (dr.float().numpy(), tg)
+        return cache[t]
+
+    def one_tree(t):
+        z, tg = inputs(t % 4)
+        t0 = time.perf_counter()
+        _, tid, tlq = oracle.drafter_stats(z, 1.0, k)
+        ref = oracle.build_tree(tid, tlq, B)
+        oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
+        oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+        return time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        one_tree(i % nt)
+    spent = sum(one_tree((args.warmup + i) % nt) for i in range(args.steps))
+    value = args.steps / spent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * spent / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(W, parallelism="host cores, one thread"),
+        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                         "sample": "one tree of the workload per step (build + mask + TEV; four "
+                                   "trees' inputs in rotation), float64 oracle, single thread"},
+        "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trees", type=int, default=0,
+                    help="trees per GPU (default: the workload's 32); for profiler captures")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

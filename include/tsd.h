@@ -170,6 +170,24 @@ tsd_status tsd_verify_tev(const void *target_logits, tsd_dtype dtype, const int3
                           size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * tsd_verify_tev_timed -- tsd_verify_tev that also records five caller-created
+ * CUDA events on `stream` around its four kernels, for measuring each stage
+ * with cudaEventElapsedTime: stage_events[0] before the tree preparation,
+ * [1] before the node-row reduction (Algorithm 1's node-local reductions over
+ * the logits), [2] after it, [3] after the per-node combination, [4] after the
+ * exit and bonus draws.  Same arguments, outputs and errors as
+ * tsd_verify_tev; TSD_ERR_INVALID_ARG if stage_events or one of its five
+ * entries is null.
+ */
+tsd_status tsd_verify_tev_timed(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
+                                const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
+                                int64_t V, float temperature, uint64_t seed, int32_t *exit_node,
+                                int32_t *bonus_token, int32_t *accept_len, float *exit_mass,
+                                float *prefix_prob, float *coverage, int32_t *status,
+                                void *workspace, size_t ws_bytes, cudaStream_t stream,
+                                cudaEvent_t *stage_events);
+
+/*
  * tsd_verify_ddtree -- predraw-and-follow ([EXIT] Sec. 2, App. A.4.1), the
  * verifier DDTree uses, kept as an equivalence check for TEV: it draws
  * R_v ~ p_v at every node (inverse CDF over token id, uniform stream 2 at

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "tsd_build_tree", "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
-        "tsd_verify_tev", "tsd_workspace_size"])
+        "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_workspace_size"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -80,6 +80,9 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     st = lib.tsd_verify_tev(fake, 0, fake, fake, fake, 1, 8, 32, 1.0, 0, fake, fake, fake,
                             None, None, None, fake, fake, 16, None)
     assert st == tsd.TSD_ERR_WORKSPACE
+    st = lib.tsd_verify_tev_timed(fake, 0, fake, fake, fake, 1, 8, 32, 1.0, 0, fake, fake, fake,
+                                  None, None, None, fake, fake, 1 << 20, None, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG  # no stage events
     st = lib.tsd_verify_ddtree(fake, 0, fake, fake, None, 1, 8, 32, 1.0, 0, fake, fake, fake,
                                None, fake, fake, 1 << 20, None)
     assert st == tsd.TSD_ERR_INVALID_ARG

@@ -17,7 +17,8 @@ import os
 import torch
 
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
-           "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_ddtree", "LIB_PATH"]
+           "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
+           "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
 
@@ -55,9 +56,11 @@ def load():
     lib.tsd_tree_mask.argtypes = [P, P, i32, i32, i32, P, P, P, i64, P, P]
     lib.tsd_verify_tev.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
                                    P, P, P, P, P, P, P, P, sz, P]
+    lib.tsd_verify_tev_timed.argtypes = lib.tsd_verify_tev.argtypes + [P]
     lib.tsd_verify_ddtree.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
                                       P, P, P, P, P, P, sz, P]
-    for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_ddtree"):
+    for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
+              "tsd_verify_ddtree"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -176,29 +179,56 @@ def _verify_common(target_logits, parent, token, n_nodes):
 
 def tsd_verify_tev(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
                    n_nodes: torch.Tensor, temperature: float, seed: int, workspace=None,
-                   with_masses: bool = True) -> dict:
+                   with_masses: bool = True, out: dict | None = None) -> dict:
     """Tree Exit Verification.  Returns exit_node, bonus_token, accept_len,
     status ([n_trees]) and, with `with_masses`, exit_mass, prefix_prob
-    ([n_trees, B+1]) and coverage ([n_trees])."""
+    ([n_trees, B+1]) and coverage ([n_trees]).  `out` may hold preallocated
+    output tensors of those shapes (int32 / float32)."""
+    return _tev(target_logits, parent, token, n_nodes, temperature, seed, workspace,
+                with_masses, out, None)
+
+
+def tsd_verify_tev_timed(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
+                         n_nodes: torch.Tensor, temperature: float, seed: int, stage_events,
+                         workspace=None, with_masses: bool = True,
+                         out: dict | None = None) -> dict:
+    """tsd_verify_tev that records five torch.cuda.Event objects (each recorded
+    once before, so that it exists) around its four kernels: before the tree
+    preparation, before and after the node-row reduction, after the per-node
+    combination, after the draws."""
+    if len(stage_events) != 5:
+        raise ValueError("stage_events must hold five CUDA events")
+    handles = (ctypes.c_void_p * 5)(*[int(e.cuda_event) for e in stage_events])
+    if not all(handles):
+        raise ValueError("record each event once before passing it")
+    return _tev(target_logits, parent, token, n_nodes, temperature, seed, workspace,
+                with_masses, out, handles)
+
+
+def _tev(target_logits, parent, token, n_nodes, temperature, seed, workspace, with_masses, out,
+         handles) -> dict:
     x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
     dev = x.device
     i32 = dict(dtype=torch.int32, device=dev)
-    out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
-    if with_masses:
-        out["exit_mass"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
-        out["prefix_prob"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
-        out["coverage"] = torch.empty(n_trees, dtype=torch.float32, device=dev)
+    if out is None:
+        out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
+        if with_masses:
+            out["exit_mass"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+            out["prefix_prob"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+            out["coverage"] = torch.empty(n_trees, dtype=torch.float32, device=dev)
     nbytes = tsd_workspace_size(TSD_OP_VERIFY_TEV, n_trees, 1, 1, V, 1, B, x.dtype)
     if nbytes == 0:
         raise TsdError(TSD_ERR_INVALID_ARG, "tsd_verify_tev")
     ws = _workspace(nbytes, dev, workspace)
+    args = [_ptr(x), _dtype_code(x), _ptr(parent), _ptr(token), _ptr(n_nodes), n_trees, B, V,
+            temperature, seed, _ptr(out["exit_node"]), _ptr(out["bonus_token"]),
+            _ptr(out["accept_len"]), _ptr(out.get("exit_mass")), _ptr(out.get("prefix_prob")),
+            _ptr(out.get("coverage")), _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev)]
     with torch.cuda.device(dev):
-        st = load().tsd_verify_tev(_ptr(x), _dtype_code(x), _ptr(parent), _ptr(token),
-                                   _ptr(n_nodes), n_trees, B, V, temperature, seed,
-                                   _ptr(out["exit_node"]), _ptr(out["bonus_token"]),
-                                   _ptr(out["accept_len"]), _ptr(out.get("exit_mass")),
-                                   _ptr(out.get("prefix_prob")), _ptr(out.get("coverage")),
-                                   _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
+        if handles is None:
+            st = load().tsd_verify_tev(*args)
+        else:
+            st = load().tsd_verify_tev_timed(*args, handles)
     if st != TSD_OK:
         raise TsdError(st, "tsd_verify_tev")
     return out

@@ -162,12 +162,14 @@ tsd_status tsd_tree_mask(const int32_t* parent, const int32_t* n_nodes, int n_tr
     return TSD_OK;
 }
 
-tsd_status tsd_verify_tev(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
-                          const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
-                          int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
-                          int32_t* bonus_token, int32_t* accept_len, float* exit_mass,
-                          float* prefix_prob, float* coverage, int32_t* status, void* workspace,
-                          size_t ws_bytes, cudaStream_t stream) {
+static tsd_status verify_tev_impl(const void* target_logits, tsd_dtype dtype,
+                                  const int32_t* parent, const int32_t* token,
+                                  const int32_t* n_nodes, int n_trees, int B, int64_t V,
+                                  float temperature, uint64_t seed, int32_t* exit_node,
+                                  int32_t* bonus_token, int32_t* accept_len, float* exit_mass,
+                                  float* prefix_prob, float* coverage, int32_t* status,
+                                  void* workspace, size_t ws_bytes, cudaStream_t stream,
+                                  cudaEvent_t* ev) {
     if (!verify_args_ok(target_logits, dtype, parent, token, n_nodes, n_trees, B, V, temperature,
                         exit_node, bonus_token, accept_len, status))
         return TSD_ERR_INVALID_ARG;
@@ -178,14 +180,47 @@ tsd_status tsd_verify_tev(const void* target_logits, tsd_dtype dtype, const int3
     verify_ws_layout(n_trees, B, V, es, workspace, &ws);
     const bool greedy = temperature == 0.0f;
     const float c = greedy ? 1.0f : exp2_scale(temperature);
-    if (launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
+    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+    if (mark(0) != cudaSuccess ||
+        launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
+        mark(1) != cudaSuccess ||
         launch_rows(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        mark(2) != cudaSuccess ||
         launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
+        mark(3) != cudaSuccess ||
         launch_tev_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, parent, n_nodes, ws,
                         exit_node, bonus_token, accept_len, exit_mass, prefix_prob, coverage,
-                        status, stream) != cudaSuccess)
+                        status, stream) != cudaSuccess ||
+        mark(4) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
+}
+
+tsd_status tsd_verify_tev(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                          const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                          int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
+                          int32_t* bonus_token, int32_t* accept_len, float* exit_mass,
+                          float* prefix_prob, float* coverage, int32_t* status, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+    return verify_tev_impl(target_logits, dtype, parent, token, n_nodes, n_trees, B, V,
+                           temperature, seed, exit_node, bonus_token, accept_len, exit_mass,
+                           prefix_prob, coverage, status, workspace, ws_bytes, stream, nullptr);
+}
+
+tsd_status tsd_verify_tev_timed(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                                const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                                int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
+                                int32_t* bonus_token, int32_t* accept_len, float* exit_mass,
+                                float* prefix_prob, float* coverage, int32_t* status,
+                                void* workspace, size_t ws_bytes, cudaStream_t stream,
+                                cudaEvent_t* stage_events) {
+    if (!stage_events) return TSD_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (!stage_events[i]) return TSD_ERR_INVALID_ARG;
+    return verify_tev_impl(target_logits, dtype, parent, token, n_nodes, n_trees, B, V,
+                           temperature, seed, exit_node, bonus_token, accept_len, exit_mass,
+                           prefix_prob, coverage, status, workspace, ws_bytes, stream,
+                           stage_events);
 }
 
 tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
