@@ -203,6 +203,42 @@ tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const i
                              int32_t *status, void *workspace, size_t ws_bytes,
                              cudaStream_t stream);
 
+/*
+ * tsd_verify_tev_noalloc -- tsd_verify_tev for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a deployment
+ * variant, not a step of the method.
+ *
+ * Some callers own no device allocator -- a plug-in that an inference engine
+ * hands only input and output pointers, or a decode loop that must not call
+ * cudaMalloc because it can synchronise the device and stall queued work.
+ * This entry point takes the same inputs and outputs as tsd_verify_tev and
+ * computes the same results, but takes no workspace: its scratch is a static
+ * device array of TSD_NOALLOC_SCRATCH_BYTES inside this library, which every
+ * GPU that loads the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Sizes: returns TSD_ERR_WORKSPACE, before launching anything, when
+ *   tsd_workspace_size(TSD_OP_VERIFY_TEV, n_trees, 1, 1, V, 1, B, dtype)
+ *   exceeds TSD_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 64 trees of B = 256 at
+ *   V = 151936 fit); other argument errors as tsd_verify_tev.
+ * - Set-up: the first call on a device (the current device, which must own
+ *   `stream` and the pointers) looks up the device address of the static
+ *   array once, with cudaGetSymbolAddress, and caches it; make that first
+ *   call before any stream capture.  TSD_ERR_CUDA if the look-up fails.
+ * - Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents; nothing in it needs to start at zero.  Calls that overlap
+ *   on the GPU (on different streams, or from several host threads without
+ *   ordering) race on the array and give wrong results: serialise them.
+ */
+#define TSD_NOALLOC_SCRATCH_BYTES (16u << 20)
+tsd_status tsd_verify_tev_noalloc(const void *target_logits, tsd_dtype dtype,
+                                  const int32_t *parent, const int32_t *token,
+                                  const int32_t *n_nodes, int n_trees, int B, int64_t V,
+                                  float temperature, uint64_t seed, int32_t *exit_node,
+                                  int32_t *bonus_token, int32_t *accept_len, float *exit_mass,
+                                  float *prefix_prob, float *coverage, int32_t *status,
+                                  cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

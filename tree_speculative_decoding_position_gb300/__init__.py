@@ -18,7 +18,7 @@ import torch
 
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
            "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
-           "LIB_PATH"]
+           "tsd_verify_tev_noalloc", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
 
@@ -57,10 +57,12 @@ def load():
     lib.tsd_verify_tev.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
                                    P, P, P, P, P, P, P, P, sz, P]
     lib.tsd_verify_tev_timed.argtypes = lib.tsd_verify_tev.argtypes + [P]
+    lib.tsd_verify_tev_noalloc.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
+                                           P, P, P, P, P, P, P, P]
     lib.tsd_verify_ddtree.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
                                       P, P, P, P, P, P, sz, P]
     for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
-              "tsd_verify_ddtree"):
+              "tsd_verify_ddtree", "tsd_verify_tev_noalloc"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -231,6 +233,33 @@ def _tev(target_logits, parent, token, n_nodes, temperature, seed, workspace, wi
             st = load().tsd_verify_tev_timed(*args, handles)
     if st != TSD_OK:
         raise TsdError(st, "tsd_verify_tev")
+    return out
+
+
+def tsd_verify_tev_noalloc(target_logits: torch.Tensor, parent: torch.Tensor,
+                           token: torch.Tensor, n_nodes: torch.Tensor, temperature: float,
+                           seed: int, with_masses: bool = True) -> dict:
+    """tsd_verify_tev without a workspace, for callers that cannot allocate
+    device memory: the library's static scratch is used instead (see
+    include/tsd.h for its size limit and the one-time set-up per device).
+    The outputs are allocated here only because this binding returns new
+    tensors."""
+    x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
+    if with_masses:
+        out["exit_mass"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+        out["prefix_prob"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+        out["coverage"] = torch.empty(n_trees, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = load().tsd_verify_tev_noalloc(
+            _ptr(x), _dtype_code(x), _ptr(parent), _ptr(token), _ptr(n_nodes), n_trees, B, V,
+            temperature, seed, _ptr(out["exit_node"]), _ptr(out["bonus_token"]),
+            _ptr(out["accept_len"]), _ptr(out.get("exit_mass")), _ptr(out.get("prefix_prob")),
+            _ptr(out.get("coverage")), _ptr(out["status"]), _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_verify_tev_noalloc")
     return out
 
 
