@@ -97,6 +97,7 @@ size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V,
  * topk            tokens kept per (mode, position), ordered by (logit desc,
  *                 id asc); 1 <= topk <= min(V, TSD_MAX_TOPK), and
  *                 L * ceil(log2(topk)) <= 56.
+ * V               1 <= V <= 8388608 for bf16, 4194304 for fp32.
  * B               non-root node budget, 0 <= B <= TSD_MAX_B.
  * drafter_temp    > 0.
  * Outputs, [n_trees][B+1] (node 0 = root: parent -1, token -1, depth 0,

@@ -381,3 +381,31 @@ def test_tev_and_predraw_law_on_gpu(tsd, dev, orc):
         obs = np.append(counts[keep], counts[~keep].sum())
         ex = np.append(exp[keep], exp[~keep].sum())
         assert scipy.stats.chisquare(obs, ex * obs.sum() / ex.sum()).pvalue > 1e-4, fn.__name__
+
+
+def test_build_edge_budgets(tsd, dev, orc):
+    """B = 0 (the root alone); budgets whose search buffers spill from shared
+    to global memory (8 modes at B = 512, one mode at the largest B); and rows
+    of equal logits, where every token ties (the drafter kernel's exact
+    fallback for an overflowing candidate set)."""
+    dr = synth.zipf_drafter(1, 6, 2048, synth.seed_for(5), device="cpu")
+    out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=0)
+    assert int(out["n_nodes"][0]) == 1 and int(out["status"][0]) == 0
+    assert _np(out["parent"][0]).tolist() == [-1]
+    mix, _, _ = synth.mixture_drafter(1, 8, 6, 1024, synth.seed_for(5, 1), device="cpu")
+    out = tsd.tsd_build_tree(mix.to(dev), topk=8, B=512)
+    ref, tid, tlq = oracle_build(orc, mix[0], 8, 512)
+    assert compare_trees(_tree_np(out), ref, tid, tlq) <= 1
+    out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=4095)
+    ref, tid, tlq = oracle_build(orc, dr[0], 8, 4095)
+    flips = compare_trees(_tree_np(out), ref, tid, tlq)  # each within SCORE_TOL
+    print("B=4095 order flips within tolerance:", flips)
+    assert flips <= 0.01 * 4095
+    flat = torch.zeros(2, 1, 5, 9000)
+    flat[1, 0, 2, 4444] = 1.0
+    out = tsd.tsd_build_tree(flat.to(dev), topk=8, B=100)
+    for t in range(2):
+        ref, tid, tlq = oracle_build(orc, flat[t], 8, 100)
+        g = _tree_np(out, t)
+        assert compare_trees(g, ref, tid, tlq) == 0
+        assert np.array_equal(g["rank"][:g["n_nodes"]], ref["rank"][:ref["n_nodes"]])

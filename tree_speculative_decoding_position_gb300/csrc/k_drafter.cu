@@ -55,27 +55,75 @@ __device__ __forceinline__ void warp_list_offer(float& ev, int& ei, float& tv, i
     }
 }
 
+constexpr int kCandCap = 256;  // candidates per warp before the exact fallback
+constexpr int kMaxListsPerLane = kMaxDrafterChunks / kWarp;
+
+// Exact fallback for a chunk whose candidate set overflowed (e.g. a row of
+// many equal logits): offer every token to the warp list, in a plain loop.
+template <typename T>
+__device__ __noinline__ void chunk_topk_fallback(const T* __restrict__ rp, int cn, int64_t c0,
+                                                 int k, int lane, float& ev, int& ei) {
+    float tv = -INFINITY;
+    int ti = INT_MAX;
+    ev = -INFINITY;
+    ei = INT_MAX;
+    for (int e0 = 0; e0 < cn; e0 += kWarp) {
+        const int e = e0 + lane;
+        const float x = e < cn ? load_logit(rp + e) : -INFINITY;
+        warp_list_offer(ev, ei, tv, ti, e < cn, x, (int)c0 + e, k, lane);
+    }
+}
+
+// Sort one float per lane, descending, across the warp (bitonic).
+__device__ __forceinline__ float warp_sort_desc(float x, int lane) {
+#pragma unroll
+    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            const float y = __shfl_xor_sync(0xffffffffu, x, j);
+            const bool lower = (lane & j) == 0;
+            const bool desc = (lane & k2) == 0;
+            // keep the larger value on the lower lane of a descending block
+            x = (lower == desc) ? fmaxf(x, y) : fminf(x, y);
+        }
+    }
+    return x;
+}
+
+// One warp per (row, 8 KB chunk).  Pass 1: the chunk max, the sum of
+// exp2(z*c - mc) and each vector's max.  Threshold: the k-th largest of the 32
+// lane maxima -- k distinct tokens reach it, so every token of the chunk's
+// top-k does too.  Pass 2: only vectors whose max reaches the threshold are
+// opened; their qualifying tokens go to a per-warp shared list.  Then k rounds
+// of warp arg-max pick the top-k by (logit desc, id asc).
 template <typename T>
 __global__ void __launch_bounds__(kDThreads)
 drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, int k,
                      float c, bool vec_ok, BuildWs ws) {
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     constexpr int VEC = 16 / (int)sizeof(T);
+    __shared__ float cand_v[kDThreads / kWarp][kCandCap];
+    __shared__ int cand_i[kDThreads / kWarp][kCandCap];
+    __shared__ int cand_n[kDThreads / kWarp];
     const int lane = threadIdx.x & (kWarp - 1);
+    const int wid = threadIdx.x / kWarp;
     const int wpb = blockDim.x / kWarp;
     const int64_t total = rows * nch;
-    for (int64_t item = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; item < total;
+    for (int64_t item = (int64_t)blockIdx.x * wpb + wid; item < total;
          item += (int64_t)gridDim.x * wpb) {
         const int64_t row = item / nch;
         const int ch = (int)(item - row * nch);
         const int64_t c0 = (int64_t)ch * CE;
         const int cn = (int)min((int64_t)CE, V - c0);
         const T* rp = logits + row * V + c0;
-        float ev = -INFINITY, tv = -INFINITY;
-        int ei = INT_MAX, ti = INT_MAX;
-        float m = -INFINITY, s = 0.0f;
+        float m = -INFINITY, s = 0.0f, lm = -INFINITY;
+        float ev = -INFINITY;
+        int ei = INT_MAX;
+        if (lane == 0) cand_n[wid] = 0;
+        __syncwarp();
         if (vec_ok) {
             uint4 buf[kVecPerLane];
+            float vmax[kVecPerLane];
 #pragma unroll
             for (int i = 0; i < kVecPerLane; ++i) {
                 const int e = (i * kWarp + lane) * VEC;
@@ -83,39 +131,105 @@ drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int 
                 buf[i] = (e < cn) ? ld_stream16(rp + e) : make_uint4(ninf, ninf, ninf, ninf);
             }
 #pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i)
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
-                                       : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
-                    const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
-                                                   : __uint_as_float(w);
-                    m = fmaxf(m, x);
+            for (int i = 0; i < kVecPerLane; ++i) {
+                if (sizeof(T) == 2) {
+                    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&buf[i].x);
+                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].y));
+                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].z));
+                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].w));
+                    vmax[i] = fmaxf(__low2float(a), __high2float(a));
+                } else {
+                    vmax[i] = fmaxf(fmaxf(__uint_as_float(buf[i].x), __uint_as_float(buf[i].y)),
+                                    fmaxf(__uint_as_float(buf[i].z), __uint_as_float(buf[i].w)));
                 }
-            m = warp_max(m);
+                lm = fmaxf(lm, vmax[i]);
+            }
+            m = warp_max(lm);
             const float mc = __fmul_rn(m, c);
+            if (m != -INFINITY) {
+                float acc[VEC];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kVecPerLane; ++i)
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
+                                           : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
+                        const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
+                                                       : __uint_as_float(w);
+                        acc[j] += ex2(fmaf(x, c, -mc));
+                    }
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) s += acc[j];
+            }
+            const float theta = __shfl_sync(0xffffffffu, warp_sort_desc(lm, lane), k - 1);
 #pragma unroll
             for (int i = 0; i < kVecPerLane; ++i) {
                 const int e = (i * kWarp + lane) * VEC;
+                if (e < cn && vmax[i] >= theta) {
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
-                                       : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
-                    const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
-                                                   : __uint_as_float(w);
-                    if (m != -INFINITY) s += ex2(fmaf(x, c, -mc));
-                    warp_list_offer(ev, ei, tv, ti, e < cn, x, (int)c0 + e + j, k, lane);
+                    for (int j = 0; j < VEC; ++j) {
+                        const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
+                                           : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
+                        const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
+                                                       : __uint_as_float(w);
+                        if (x >= theta) {
+                            const int pos = atomicAdd(&cand_n[wid], 1);
+                            if (pos < kCandCap) {
+                                cand_v[wid][pos] = x;
+                                cand_i[wid][pos] = (int)c0 + e + j;
+                            }
+                        }
+                    }
                 }
             }
         } else {
-            for (int e = lane; e < cn; e += kWarp) m = fmaxf(m, load_logit(rp + e));
-            m = warp_max(m);
+            for (int e = lane; e < cn; e += kWarp) lm = fmaxf(lm, load_logit(rp + e));
+            m = warp_max(lm);
             const float mc = __fmul_rn(m, c);
-            for (int e0 = 0; e0 < cn; e0 += kWarp) {
-                const int e = e0 + lane;
-                const float x = e < cn ? load_logit(rp + e) : -INFINITY;
-                if (e < cn && m != -INFINITY) s += ex2(fmaf(x, c, -mc));
-                warp_list_offer(ev, ei, tv, ti, e < cn, x, (int)c0 + e, k, lane);
+            if (m != -INFINITY)
+                for (int e = lane; e < cn; e += kWarp) s += ex2(fmaf(load_logit(rp + e), c, -mc));
+            const float theta = __shfl_sync(0xffffffffu, warp_sort_desc(lm, lane), k - 1);
+            for (int e = lane; e < cn; e += kWarp) {
+                const float x = load_logit(rp + e);
+                if (x >= theta) {
+                    const int pos = atomicAdd(&cand_n[wid], 1);
+                    if (pos < kCandCap) {
+                        cand_v[wid][pos] = x;
+                        cand_i[wid][pos] = (int)c0 + e;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        const int nc = cand_n[wid];
+        if (nc > kCandCap) {
+            chunk_topk_fallback<T>(rp, cn, c0, k, lane, ev, ei);
+        } else {
+            // k rounds of arg-max over the candidates; a taken one becomes
+            // (-inf, INT_MAX), which every real token beats.
+            for (int r = 0; r < k; ++r) {
+                float bv = -INFINITY;
+                int bi = INT_MAX, bp = -1;
+                for (int q = lane; q < nc; q += kWarp)
+                    if (better(cand_v[wid][q], cand_i[wid][q], bv, bi)) {
+                        bv = cand_v[wid][q];
+                        bi = cand_i[wid][q];
+                        bp = q;
+                    }
+                float wv = bv;
+                int wi = bi;
+                warp_argmax(wv, wi);
+                if (lane == r) {
+                    ev = wv;
+                    ei = wi;
+                }
+                if (wi != INT_MAX && bi == wi) {
+                    cand_v[wid][bp] = -INFINITY;
+                    cand_i[wid][bp] = INT_MAX;
+                }
+                __syncwarp();
             }
         }
         s = warp_sum(s);
@@ -131,9 +245,14 @@ drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int 
             ws.cand_v[item * k + lane] = ev;
             ws.cand_i[item * k + lane] = ei;
         }
+        __syncwarp();
     }
 }
 
+// One warp per row: the row's log-normaliser from the chunk sums (float64),
+// and its top-k merged from the chunks' sorted lists -- lane l walks the
+// lists of chunks l, l+32, ...; k rounds of warp arg-max over the lanes'
+// current heads.
 __global__ void __launch_bounds__(kDThreads)
 drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs ws) {
     const int lane = threadIdx.x & (kWarp - 1);
@@ -157,13 +276,38 @@ drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs w
         // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
         const double lse = bad ? __longlong_as_double(0x7ff8000000000000ll)
                                : 0.6931471805599453 * ((double)mc + log2(s));
-        float ev = -INFINITY, tv = -INFINITY;
-        int ei = INT_MAX, ti = INT_MAX;
-        for (int q = 0; q < nch; ++q) {
-            const bool has = lane < k;
-            const float x = has ? ws.cand_v[(row * nch + q) * k + lane] : -INFINITY;
-            const int xi = has ? ws.cand_i[(row * nch + q) * k + lane] : INT_MAX;
-            warp_list_offer(ev, ei, tv, ti, has && xi != INT_MAX, x, xi, k, lane);
+        const float* cv = ws.cand_v + row * nch * k;
+        const int* ci = ws.cand_i + row * nch * k;
+        // lane cursors: chunk q = lane + 32 j, position pos[j] within its list
+        int pos[kMaxListsPerLane];
+        const int nj = (nch + kWarp - 1) / kWarp;
+        for (int j = 0; j < nj; ++j) pos[j] = 0;
+        float ev = -INFINITY;
+        int ei = INT_MAX;
+        for (int r = 0; r < k; ++r) {
+            float hv = -INFINITY;
+            int hi = INT_MAX, hj = -1;
+            for (int j = 0; j < nj; ++j) {
+                const int q = lane + kWarp * j;
+                const int p = pos[j];
+                if (q < nch && p < k) {
+                    const float x = cv[q * k + p];
+                    const int xi = ci[q * k + p];
+                    if (xi != INT_MAX && better(x, xi, hv, hi)) {
+                        hv = x;
+                        hi = xi;
+                        hj = j;
+                    }
+                }
+            }
+            float wv = hv;
+            int wi = hi;
+            warp_argmax(wv, wi);
+            if (lane == r) {
+                ev = wv;
+                ei = wi;
+            }
+            if (wi != INT_MAX && hi == wi) ++pos[hj];
         }
         if (lane < k) {
             ws.top_id[row * k + lane] = ei;

@@ -1,37 +1,49 @@
-// k_heap.cu -- best-first tree builder over the top-k universe.
+// k_heap.cu -- best-first tree builder over the top-k universe, batched.
 //
 // "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters", Thm. 1
 // and App. C "Candidate construction": the B prefixes with the largest
-// plug-in score sum_j log q_j(y_j), expanded best-first from a heap keyed by
-// cumulative log-probability; ties toward shorter prefixes, then
-// lexicographic.
+// plug-in score sum_j log q_j(y_j), expanded best-first; ties toward shorter
+// prefixes, then lexicographic.
 // "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
-// Speculative Decoding", Sec. 3.4 Eq. 2, Sec. 4.3 and App. B "Merged heap"
-// (Prop. 6): one heap of (mode, prefix) entries keyed by that mode's score;
-// popping an entry pushes its next sibling (rank r+1) and its first child
-// (rank 0 at the next position); a prefix popped again from another mode
-// reuses its node and spends no budget.  With one mode this is DDTree.
+// Speculative Decoding", Sec. 3.4 Eq. 2, Sec. 4.3, App. B "Merged heap" and
+// Prop. 6: entries (mode, prefix) keyed by that mode's score; taking an entry
+// adds its next sibling (rank r+1) and its first child (rank 0 at the next
+// position); a prefix taken again from another mode keeps its first node.
 //
-// One warp per tree.  The heap operations are sequential, so lane 0 runs
-// them on a binary heap in shared memory (global workspace when a very large
-// budget does not fit); the other lanes load the lists and fill the tail.
-// Scores are float64 sums like the pages' host builders; comparisons use a
-// 64-bit order-preserving integer of the score plus a 64-bit tie key
-// (depth << 59 | mode << 56 | rank sequence).
+// The pages run this as a sequential heap on the host.  Here one CTA per tree
+// runs it in rounds: the frontier is a sorted array; each round takes its best
+// M entries at once, merges them into the sorted list X of taken entries, and
+// merges their sorted successors back into the frontier.  Taking several
+// entries per round may take some that a one-at-a-time heap would not reach,
+// but never misses one: every entry not yet taken is worse than the frontier
+// head, and the search stops only when the frontier holds nothing better than
+// the B-th distinct prefix of X.  The result is therefore exactly the heap's:
+// the B best distinct prefixes under the total order (score desc, depth asc,
+// mode asc, rank sequence asc), listed in that order (= pop order).
+//
+// Entries are 32 bytes: a 64-bit order-preserving image of the float64 score,
+// the 64-bit tie key depth << 59 | mode << 56 | rank digits (which also names
+// the prefix within its mode), the parent's score in the same mode (to score
+// the next sibling), and a 64-bit hash of the parent's token sequence (to tell
+// equal prefixes of different modes apart; every hash match is confirmed by
+// comparing the token sequences).
 #include "tsd_internal.cuh"
 
 namespace tsd {
 
-struct __align__(16) HEntry {
-    unsigned long long key;  // order-preserving image of the score
-    unsigned long long tb;   // depth << 59 | mode << 56 | rank digits
-    double pscore;           // the same mode's score of the parent prefix
-    int32_t pnode;           // tree node of the parent prefix
-    int16_t rank;            // rank of the last token in this mode's list
-    int8_t mode;
-    int8_t depth;
+constexpr int kBuildThreads = 256;
+
+struct __align__(16) FEntry {
+    unsigned long long key;   // order-preserving image of the score
+    unsigned long long tb;    // depth << 59 | mode << 56 | rank digits
+    double pscore;            // same mode's score of the parent prefix
+    unsigned long long hpar;  // hash of the parent's token sequence
 };
-static_assert(sizeof(HEntry) == 32, "heap entry layout");
+static_assert(sizeof(FEntry) == 32, "entry layout");
+
+constexpr unsigned long long kSentinelKey = 0ull;  // below every real key
+constexpr unsigned long long kRootHash = 0x243F6A8885A308D3ull;
+constexpr unsigned long long kRsMask = (1ull << 56) - 1;
 
 __device__ __forceinline__ unsigned long long order_key(double s) {
     const unsigned long long u = (unsigned long long)__double_as_longlong(s);
@@ -41,184 +53,469 @@ __device__ __forceinline__ double key_score(unsigned long long k) {
     const unsigned long long u = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
     return __longlong_as_double((long long)u);
 }
-__device__ __forceinline__ bool hbefore(const HEntry& a, const HEntry& b) {
+__device__ __forceinline__ bool before(const FEntry& a, const FEntry& b) {
     return a.key > b.key || (a.key == b.key && a.tb < b.tb);
 }
-
-__device__ __forceinline__ void heap_push(HEntry* h, int& hn, const HEntry& x) {
-    int i = hn++;
-    while (i > 0) {
-        const int p = (i - 1) >> 1;
-        if (!hbefore(x, h[p])) break;
-        h[i] = h[p];
-        i = p;
-    }
-    h[i] = x;
+__device__ __forceinline__ int tb_depth(unsigned long long tb) { return (int)(tb >> 59); }
+__device__ __forceinline__ int tb_mode(unsigned long long tb) { return (int)((tb >> 56) & 7); }
+// A strong 64-bit mix of (parent hash, token) (a SplitMix64-style finaliser).
+__device__ __forceinline__ unsigned long long hash_step(unsigned long long h, int tok) {
+    unsigned long long x = h ^ ((unsigned long long)(uint32_t)tok * 0x9E3779B97F4A7C15ull);
+    x ^= x >> 30;
+    x *= 0xBF58476D1CE4E5B9ull;
+    x ^= x >> 27;
+    x *= 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    return x;
 }
 
-__device__ __forceinline__ HEntry heap_pop(HEntry* h, int& hn) {
-    const HEntry top = h[0];
-    const HEntry x = h[--hn];
-    int i = 0;
-    for (;;) {
-        const int l = 2 * i + 1;
-        if (l >= hn) break;
-        const int r = l + 1;
-        const int c = (r < hn && hbefore(h[r], h[l])) ? r : l;
-        if (!hbefore(h[c], x)) break;
-        h[i] = h[c];
-        i = c;
-    }
-    if (hn > 0) h[i] = x;
-    return top;
-}
-
-struct HeapSmem {
-    size_t lists, nodes, heap, total;
-    bool heap_in_smem;
+struct BuildPlan {
+    int M;          // entries taken per round
+    int fcap, xcap; // frontier / taken-list capacity
+    int hcap;       // hash table size (power of two)
+    size_t lists, fbytes, xbytes, sbytes, hbytes, flag_bytes, smem_total;
+    bool big_in_smem;
+    size_t global_per_tree;
 };
 
-static int digit_bits(int k) {
-    int b = 0;
-    while ((1 << b) < k) ++b;
-    return b;
+__host__ __device__ inline int pow2_at_least(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
 }
 
-static HeapSmem heap_smem_plan(int n_modes, int L, int topk, int B) {
-    HeapSmem p;
-    p.lists = (size_t)n_modes * L * topk * (sizeof(int32_t) + sizeof(double));
-    p.lists = (p.lists + 15) & ~(size_t)15;
-    p.nodes = (size_t)(B + 1) * (2 * sizeof(int16_t) + sizeof(int32_t));
-    p.nodes = (p.nodes + 15) & ~(size_t)15;
-    p.heap = sizeof(HEntry) * ((size_t)n_modes * (B + 1) + 1);
-    p.heap_in_smem = p.lists + p.nodes + p.heap <= 200 * 1024;
-    p.total = p.lists + p.nodes + (p.heap_in_smem ? p.heap : 0);
+static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
+    BuildPlan p;
+    p.M = n_modes > 1 ? 64 : 128;
+    p.xcap = n_modes * (B + 1) + p.M;
+    p.fcap = n_modes * (B + 1) + 2 * p.M + n_modes;
+    p.hcap = pow2_at_least(2 * p.xcap);
+    auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
+    p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)));
+    p.sbytes = r16(sizeof(FEntry) * 2 * (size_t)p.M);
+    p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
+    p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
+    p.fbytes = r16(sizeof(FEntry) * 2 * (size_t)p.fcap);
+    p.xbytes = r16(sizeof(FEntry) * 2 * (size_t)p.xcap);
+    // frontier, taken list, hash table and marks go to global memory (one
+    // region per tree) when shared memory cannot hold them
+    const size_t big = p.fbytes + p.xbytes + p.hbytes + p.flag_bytes;
+    p.big_in_smem = p.lists + p.sbytes + big <= 225 * 1024;  // of 227 KB per block
+    p.smem_total = p.lists + p.sbytes + (p.big_in_smem ? big : 0);
+    p.global_per_tree = p.big_in_smem ? 0 : big;
     return p;
 }
 
 size_t heap_spill_bytes(int n_modes, int L, int topk, int B) {
-    const HeapSmem p = heap_smem_plan(n_modes, L, topk, B);
-    return p.heap_in_smem ? 0 : p.heap;
+    return build_plan(n_modes, L, topk, B).global_per_tree;
 }
 
-__global__ void __launch_bounds__(kWarp)
-build_heap_kernel(BuildWs ws, int K, int L, int k, int B, int bits, size_t lists_bytes,
-                  size_t nodes_bytes, bool heap_in_smem, int32_t* __restrict__ parent,
-                  int32_t* __restrict__ token, int32_t* __restrict__ depth,
-                  float* __restrict__ score, int32_t* __restrict__ rank,
-                  int32_t* __restrict__ mode, int32_t* __restrict__ n_nodes_out,
-                  int32_t* __restrict__ status) {
+// ---------------------------------------------------------------------------
+// Block-wide helpers (all threads call them).
+// ---------------------------------------------------------------------------
+// Bitonic sort of a[0, n2) (n2 a power of two) into the total order.
+__device__ void sort_entries(FEntry* a, int n2) {
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const FEntry x = a[i], y = a[l];
+                    const bool up = (i & k) == 0;
+                    if (up ? before(y, x) : before(x, y)) {
+                        a[i] = y;
+                        a[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// dst[0, na+nb) = merge of sorted a[0, na) and sorted b[0, nb) (merge path).
+__device__ void merge_entries(FEntry* dst, const FEntry* a, int na, const FEntry* b, int nb) {
+    const int total = na + nb;
+    const int per = (total + blockDim.x - 1) / blockDim.x;
+    const int d0 = min(total, (int)threadIdx.x * per), d1 = min(total, d0 + per);
+    if (d0 < d1) {
+        int lo = max(0, d0 - nb), hi = min(d0, na);
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (before(a[mid], b[d0 - mid - 1])) lo = mid + 1;
+            else hi = mid;
+        }
+        int ia = lo, ib = d0 - lo;
+        for (int d = d0; d < d1; ++d) {
+            if (ib >= nb || (ia < na && before(a[ia], b[ib]))) dst[d] = a[ia++];
+            else dst[d] = b[ib++];
+        }
+    }
+    __syncthreads();
+}
+
+// Inclusive block scan of one int per thread; *total = block sum.
+__device__ int block_incl_scan_int(int x, int* red, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) red[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int y = lane < nw ? red[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += z;
+        }
+        red[lane] = y;
+    }
+    __syncthreads();
+    const int r = x + (wid > 0 ? red[wid - 1] : 0);
+    *total = red[nw - 1];
+    __syncthreads();
+    return r;
+}
+
+struct Lists {
+    const double* lq;
+    const int32_t* ids;
+    int L, k, bits;
+    __device__ int token(int m, int d, int r) const { return ids[(m * L + d - 1) * k + r]; }
+    __device__ double logq(int m, int d, int r) const { return lq[(m * L + d - 1) * k + r]; }
+    // token at depth j+1 (j < d) of the prefix named by tie key tb
+    __device__ int token_at(unsigned long long tb, int j) const {
+        const int d = tb_depth(tb), m = tb_mode(tb);
+        const int r = (int)(((tb & kRsMask) >> (bits * (d - 1 - j))) & ((1ull << bits) - 1));
+        return token(m, j + 1, r);
+    }
+    __device__ int last_rank(unsigned long long tb) const {
+        return (int)((tb & kRsMask) & ((1ull << bits) - 1));
+    }
+};
+
+// Same token sequence for the first `len` positions of two prefixes.
+__device__ bool same_tokens(const Lists& ls, unsigned long long ta, unsigned long long tbb, int len) {
+    for (int j = 0; j < len; ++j)
+        if (ls.token_at(ta, j) != ls.token_at(tbb, j)) return false;
+    return true;
+}
+
+__device__ __forceinline__ unsigned long long entry_hash(const Lists& ls, const FEntry& e) {
+    const int d = tb_depth(e.tb);
+    return hash_step(e.hpar, ls.token(tb_mode(e.tb), d, ls.last_rank(e.tb)));
+}
+
+// Open addressing on the prefix hash: the bucket of entry i (claimed or found).
+// Equal hashes of different prefixes are caught afterwards by comparing token
+// sequences (a 2^-64 event per pair, reported as a failed tree, never merged).
+__device__ int hash_bucket(unsigned long long h, unsigned long long* hkey, int hcap) {
+    unsigned int b = (unsigned int)(h ^ (h >> 32)) & (hcap - 1);
+    for (int probe = 0; probe < hcap; ++probe, b = (b + 1) & (hcap - 1)) {
+        const unsigned long long old = atomicCAS(&hkey[b], 0ull, h);
+        if (old == 0ull || old == h) return (int)b;
+    }
+    return -1;
+}
+
+__global__ void __launch_bounds__(kBuildThreads)
+build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bits,
+                  int32_t* __restrict__ parent, int32_t* __restrict__ token,
+                  int32_t* __restrict__ depth, float* __restrict__ score,
+                  int32_t* __restrict__ rank, int32_t* __restrict__ mode,
+                  int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ status) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int t = blockIdx.x;
-    const int lane = threadIdx.x;
+    __shared__ int s_bad, s_nF, s_nX, s_nS, s_D, s_posB;
+    __shared__ int red[32];
+    const int t = blockIdx.x, tid = threadIdx.x;
     const int nl = K * L * k;
-    double* lq = reinterpret_cast<double*>(smem);
-    int32_t* ids = reinterpret_cast<int32_t*>(smem + (size_t)nl * sizeof(double));
-    int16_t* first_child = reinterpret_cast<int16_t*>(smem + lists_bytes);
-    int16_t* next_sib = first_child + (B + 1);
-    int32_t* ntok = reinterpret_cast<int32_t*>(next_sib + (B + 1));
-    HEntry* heap = heap_in_smem ? reinterpret_cast<HEntry*>(smem + lists_bytes + nodes_bytes)
-                                : reinterpret_cast<HEntry*>(ws.heap + (size_t)t * ws.heap_stride);
+    uint8_t* p = smem;
+    double* lq = reinterpret_cast<double*>(p);
+    int32_t* ids = reinterpret_cast<int32_t*>(p + sizeof(double) * nl);
+    p += plan.lists;
+    FEntry* S = reinterpret_cast<FEntry*>(p);
+    p += plan.sbytes;
+    uint8_t* big = plan.big_in_smem ? p : ws.heap + (size_t)t * ws.heap_stride;
+    FEntry* F[2] = {reinterpret_cast<FEntry*>(big), reinterpret_cast<FEntry*>(big) + plan.fcap};
+    big += plan.fbytes;
+    FEntry* X[2] = {reinterpret_cast<FEntry*>(big), reinterpret_cast<FEntry*>(big) + plan.xcap};
+    big += plan.xbytes;
+    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(big);
+    int* hval = reinterpret_cast<int*>(big + sizeof(unsigned long long) * plan.hcap);
+    big += plan.hbytes;
+    int* flag = reinterpret_cast<int*>(big);  // [xcap] first-occurrence marks, then ranks
+    const Lists ls{lq, ids, L, k, bits};
     const int stride = B + 1;
-    bool bad = false;
-    for (int i = lane; i < nl; i += kWarp) {
+
+    if (tid == 0) {
+        s_bad = 0;
+        s_nF = 0;
+        s_nX = 0;
+        s_D = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < nl; i += blockDim.x) {
         const double x = ws.top_lq[(int64_t)t * nl + i];
         lq[i] = x;
         ids[i] = ws.top_id[(int64_t)t * nl + i];
-        bad |= (x != x);
+        if (x != x) s_bad = 1;
     }
-    for (int i = lane; i <= B; i += kWarp) first_child[i] = next_sib[i] = -1;
-    bad = __any_sync(0xffffffffu, bad);
-    __syncwarp();
-    int n = 0;
-    if (!bad && lane == 0) {
-        int32_t* par = parent + (int64_t)t * stride;
-        int32_t* tok = token + (int64_t)t * stride;
-        int32_t* dep = depth + (int64_t)t * stride;
-        float* sc = score + (int64_t)t * stride;
-        int32_t* rk = rank ? rank + (int64_t)t * stride : nullptr;
-        int32_t* md = mode ? mode + (int64_t)t * stride : nullptr;
-        par[0] = -1;
-        tok[0] = -1;
-        dep[0] = 0;
-        sc[0] = 0.0f;
-        if (rk) rk[0] = -1;
-        if (md) md[0] = -1;
-        int hn = 0;
-        const unsigned long long rs_mask = (1ull << 56) - 1;
-        for (int m = 0; m < K; ++m) {  // each mode's best first token
-            HEntry e;
-            e.key = order_key(0.0 + lq[(m * L + 0) * k + 0]);
-            e.tb = (1ull << 59) | ((unsigned long long)m << 56);
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    int fc = 0, xc = 0;  // current buffer indices
+    if (!bad && B > 0) {  // B = 0: the tree is the root alone
+        // seeds: each mode's best first token
+        const int n2 = pow2_at_least(K);
+        for (int i = tid; i < n2; i += blockDim.x) {
+            FEntry e;
+            e.key = kSentinelKey;
+            e.tb = ~0ull;
             e.pscore = 0.0;
-            e.pnode = 0;
-            e.rank = 0;
-            e.mode = (int8_t)m;
-            e.depth = 1;
-            heap_push(heap, hn, e);
+            e.hpar = kRootHash;
+            if (i < K && ls.logq(i, 1, 0) != -INFINITY) {
+                e.key = order_key(0.0 + ls.logq(i, 1, 0));
+                e.tb = (1ull << 59) | ((unsigned long long)i << 56);
+            }
+            F[0][i] = e;
         }
-        n = 1;
-        while (n <= B && hn > 0) {
-            const HEntry e = heap_pop(heap, hn);
-            const double s = key_score(e.key);
-            if (s == -INFINITY) break;  // only zero-probability prefixes remain
-            const int m = e.mode, d = e.depth, r = e.rank;
-            const int x = ids[(m * L + d - 1) * k + r];
-            int node = -1;
-            if (K > 1)
-                for (int cch = first_child[e.pnode]; cch >= 0; cch = next_sib[cch])
-                    if (ntok[cch] == x) {
-                        node = cch;
-                        break;
+        __syncthreads();
+        sort_entries(F[0], n2);
+        if (tid == 0) {
+            int nF = 0;
+            while (nF < K && F[0][nF].key != kSentinelKey) ++nF;
+            s_nF = nF;
+        }
+        __syncthreads();
+        const int M = plan.M;
+        for (int round = 0; round < (1 << 20); ++round) {
+            const int nF = s_nF, nX = s_nX;
+            if (nF == 0) break;
+            const int bn = min(M, nF);
+            // Successors of the taken entries, then sort them.
+            if (tid == 0) s_nS = 0;
+            for (int i = tid; i < 2 * M; i += blockDim.x) {
+                FEntry snt;
+                snt.key = kSentinelKey;
+                snt.tb = ~0ull;
+                snt.pscore = 0.0;
+                snt.hpar = 0;
+                S[i] = snt;
+            }
+            __syncthreads();
+            for (int i = tid; i < bn; i += blockDim.x) {
+                const FEntry e = F[fc][i];
+                const int d = tb_depth(e.tb), m = tb_mode(e.tb), r = ls.last_rank(e.tb);
+                const double s = key_score(e.key);
+                if (r + 1 < k) {  // next sibling
+                    const double sv = e.pscore + ls.logq(m, d, r + 1);
+                    if (sv != -INFINITY) {
+                        FEntry sb;
+                        sb.key = order_key(sv);
+                        sb.tb = e.tb + 1;
+                        sb.pscore = e.pscore;
+                        sb.hpar = e.hpar;
+                        S[2 * i] = sb;
+                        atomicAdd(&s_nS, 1);
                     }
-            if (node < 0) {
-                node = n++;
-                ntok[node] = x;
-                next_sib[node] = first_child[e.pnode];  // child lists are only searched
-                first_child[e.pnode] = (int16_t)node;
-                par[node] = e.pnode;
-                tok[node] = x;
-                dep[node] = d;
-                sc[node] = (float)s;
-                if (rk) rk[node] = r;
-                if (md) md[node] = m;
+                }
+                if (d < L) {  // first child
+                    const double sv = s + ls.logq(m, d + 1, 0);
+                    if (sv != -INFINITY) {
+                        FEntry ch;
+                        ch.key = order_key(sv);
+                        ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
+                                (((e.tb & kRsMask) << bits) & kRsMask);
+                        ch.pscore = s;
+                        ch.hpar = entry_hash(ls, e);
+                        S[2 * i + 1] = ch;
+                        atomicAdd(&s_nS, 1);
+                    }
+                }
             }
-            if (r + 1 < k) {  // next sibling: same parent, next rank
-                HEntry sb = e;
-                sb.key = order_key(e.pscore + lq[(m * L + d - 1) * k + r + 1]);
-                sb.tb = e.tb + 1;
-                sb.rank = (int16_t)(r + 1);
-                heap_push(heap, hn, sb);
+            __syncthreads();
+            sort_entries(S, 2 * M);
+            const int nS = s_nS;
+            if (nX + bn > plan.xcap || nF - bn + nS > plan.fcap) {  // cannot happen (see plan)
+                if (tid == 0) s_bad = 3;
+                __syncthreads();
+                break;
             }
-            if (d < L) {  // first child: rank 0 at the next position
-                HEntry ch;
-                ch.key = order_key(s + lq[(m * L + d) * k + 0]);
-                ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
-                        (((e.tb & rs_mask) << bits) & rs_mask);
-                ch.pscore = s;
-                ch.pnode = node;
-                ch.rank = 0;
-                ch.mode = (int8_t)m;
-                ch.depth = (int8_t)(d + 1);
-                heap_push(heap, hn, ch);
+            // Taken entries join X (both sorted); the rest of the frontier
+            // merges with the successors.
+            merge_entries(X[xc ^ 1], X[xc], nX, F[fc], bn);
+            merge_entries(F[fc ^ 1], F[fc] + bn, nF - bn, S, nS);
+            xc ^= 1;
+            fc ^= 1;
+            int nXn = nX + bn, nFn = nF - bn + nS;
+            // Distinct prefixes in X: first occurrences in the sorted list.
+            int D;
+            if (K == 1) {
+                D = nXn;
+            } else {
+                for (int i = tid; i < plan.hcap; i += blockDim.x) {
+                    hkey[i] = 0ull;
+                    hval[i] = INT_MAX;
+                }
+                __syncthreads();
+                // first occurrence of each prefix = smallest X position in its bucket
+                for (int i = tid; i < nXn; i += blockDim.x) {
+                    const int b = hash_bucket(entry_hash(ls, X[xc][i]) | 1ull, hkey, plan.hcap);
+                    flag[i] = b;
+                    if (b < 0) s_bad = 2;
+                    else atomicMin(&hval[b], i);
+                }
+                __syncthreads();
+                for (int i = tid; i < nXn; i += blockDim.x) {
+                    const int b = flag[i];
+                    if (b < 0) continue;
+                    const int j = hval[b];
+                    if (j != i) {
+                        const int d = tb_depth(X[xc][i].tb);
+                        if (tb_depth(X[xc][j].tb) != d || !same_tokens(ls, X[xc][j].tb, X[xc][i].tb, d))
+                            s_bad = 2;  // a hash collision: refuse rather than merge
+                    }
+                }
+                __syncthreads();
+                for (int i = tid; i < nXn; i += blockDim.x) flag[i] = (flag[i] >= 0 && hval[flag[i]] == i) ? 1 : 0;
+                __syncthreads();
+                // ranks of the first occurrences (block scan over chunks)
+                int base = 0;
+                for (int c0 = 0; c0 < nXn; c0 += blockDim.x) {
+                    const int i = c0 + tid;
+                    const int f = i < nXn ? flag[i] : 0;
+                    int tot;
+                    const int inc = block_incl_scan_int(f, red, &tot);
+                    if (i < nXn) flag[plan.xcap + i] = f ? base + inc - 1 : -1;
+                    base += tot;
+                }
+                D = base;
+                __syncthreads();
             }
+            if (D >= B) {
+                // the B-th distinct prefix bounds everything worth keeping
+                if (tid == 0) s_posB = (K == 1) ? B - 1 : -1;
+                __syncthreads();
+                if (K > 1)
+                    for (int i = tid; i < nXn; i += blockDim.x)
+                        if (flag[plan.xcap + i] == B - 1) s_posB = i;
+                __syncthreads();
+                const int posB = s_posB;
+                const FEntry th = X[xc][posB];
+                nXn = posB + 1;
+                // frontier entries not before the bound can never be kept
+                if (tid == 0) {
+                    int lo = 0, hi = nFn;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (before(F[fc][mid], th)) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    s_nF = lo;
+                }
+            } else if (tid == 0) {
+                s_nF = nFn;
+            }
+            if (tid == 0) {
+                s_nX = nXn;
+                s_D = min(D, B);
+            }
+            __syncthreads();
+        }
+        __syncthreads();
+    }
+    // ---- output: nodes in X order (first occurrences), parents resolved ----
+    const bool failed = bad || s_bad != 0;
+    const int nX = failed ? 0 : s_nX;
+    const int nn = failed ? 0 : s_D + 1;
+    int32_t* par = parent + (int64_t)t * stride;
+    int32_t* tok = token + (int64_t)t * stride;
+    int32_t* dep = depth + (int64_t)t * stride;
+    float* sc = score + (int64_t)t * stride;
+    int32_t* rk = rank ? rank + (int64_t)t * stride : nullptr;
+    int32_t* md = mode ? mode + (int64_t)t * stride : nullptr;
+    if (!failed) {
+        // node index of each kept entry: K == 1 -> position + 1; K > 1 ->
+        // distinct rank + 1 for first occurrences
+        // table: prefix -> node (keyed by the prefix hash, confirmed by tokens)
+        for (int i = tid; i < plan.hcap; i += blockDim.x) {
+            hkey[i] = 0ull;
+            hval[i] = INT_MAX;
+        }
+        __syncthreads();
+        for (int i = tid; i < nX; i += blockDim.x) {
+            const int node = (K == 1) ? i + 1 : flag[plan.xcap + i] + 1;
+            if (node <= 0) continue;
+            const FEntry e = X[xc][i];
+            const unsigned long long h = entry_hash(ls, e) | 1ull;
+            unsigned int b = (unsigned int)(h ^ (h >> 32)) & (plan.hcap - 1);
+            for (int probe = 0; probe < plan.hcap; ++probe, b = (b + 1) & (plan.hcap - 1)) {
+                const unsigned long long old = atomicCAS(&hkey[b], 0ull, h);
+                if (old == 0ull) {
+                    hval[b] = i;  // X position of this node's entry
+                    break;
+                }
+                if (old == h) {  // two distinct nodes with one hash
+                    s_bad = 2;
+                    break;
+                }
+            }
+            const int d = tb_depth(e.tb), m = tb_mode(e.tb), r = ls.last_rank(e.tb);
+            tok[node] = ls.token(m, d, r);
+            dep[node] = d;
+            sc[node] = (float)key_score(e.key);
+            if (rk) rk[node] = r;
+            if (md) md[node] = m;
+        }
+        __syncthreads();
+        for (int i = tid; i < nX; i += blockDim.x) {
+            const int node = (K == 1) ? i + 1 : flag[plan.xcap + i] + 1;
+            if (node <= 0) continue;
+            const FEntry e = X[xc][i];
+            const int d = tb_depth(e.tb);
+            int pn = 0;
+            if (d > 1) {
+                const unsigned long long h = e.hpar | 1ull;
+                unsigned int b = (unsigned int)(h ^ (h >> 32)) & (plan.hcap - 1);
+                pn = -1;
+                for (int probe = 0; probe < plan.hcap; ++probe, b = (b + 1) & (plan.hcap - 1)) {
+                    const unsigned long long kk = hkey[b];
+                    if (kk == 0ull) break;
+                    if (kk == h) {
+                        const int j = hval[b];
+                        if (tb_depth(X[xc][j].tb) == d - 1 && same_tokens(ls, X[xc][j].tb, e.tb, d - 1)) {
+                            pn = (K == 1) ? j + 1 : flag[plan.xcap + j] + 1;
+                            break;
+                        }
+                    }
+                }
+            }
+            par[node] = pn;
+            if (pn < 0) s_bad = 2;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            par[0] = -1;
+            tok[0] = -1;
+            dep[0] = 0;
+            sc[0] = 0.0f;
+            if (rk) rk[0] = -1;
+            if (md) md[0] = -1;
         }
     }
-    n = __shfl_sync(0xffffffffu, n, 0);
-    __syncwarp();
-    // Tail slots (and every slot of a failed tree).
-    const int from = bad ? 0 : n;
-    for (int i = from + lane; i <= B; i += kWarp) {
-        parent[(int64_t)t * stride + i] = -1;
-        token[(int64_t)t * stride + i] = -1;
-        depth[(int64_t)t * stride + i] = -1;
-        score[(int64_t)t * stride + i] = -INFINITY;
-        if (rank) rank[(int64_t)t * stride + i] = -1;
-        if (mode) mode[(int64_t)t * stride + i] = -1;
+    for (int i = (failed ? 0 : nn) + tid; i <= B; i += blockDim.x) {
+        par[i] = -1;
+        tok[i] = -1;
+        dep[i] = -1;
+        sc[i] = -INFINITY;
+        if (rk) rk[i] = -1;
+        if (md) md[i] = -1;
     }
-    if (lane == 0) {
-        n_nodes_out[t] = bad ? 0 : n;
-        status[t] = bad ? kStatNonFinite : kStatOk;
+    if (tid == 0) {
+        n_nodes_out[t] = nn;
+        status[t] = failed ? kStatNonFinite : kStatOk;
     }
 }
 
@@ -226,14 +523,15 @@ cudaError_t launch_build_heap(const BuildWs& ws, int n_trees, int n_modes, int L
                               int32_t* parent, int32_t* token, int32_t* depth, float* score,
                               int32_t* rank, int32_t* mode, int32_t* n_nodes, int32_t* status,
                               cudaStream_t stream) {
-    const HeapSmem p = heap_smem_plan(n_modes, L, topk, B);
-    cudaError_t e = cudaFuncSetAttribute(build_heap_kernel,
+    const BuildPlan p = build_plan(n_modes, L, topk, B);
+    cudaError_t e = cudaFuncSetAttribute(build_tree_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.total);
+                                         (int)p.smem_total);
     if (e != cudaSuccess) return e;
-    build_heap_kernel<<<n_trees, kWarp, p.total, stream>>>(
-        ws, n_modes, L, topk, B, digit_bits(topk), p.lists, p.nodes, p.heap_in_smem, parent,
-        token, depth, score, rank, mode, n_nodes, status);
+    int bits = 0;
+    while ((1 << bits) < topk) ++bits;
+    build_tree_kernel<<<n_trees, kBuildThreads, p.smem_total, stream>>>(
+        ws, p, n_modes, L, topk, B, bits, parent, token, depth, score, rank, mode, n_nodes, status);
     return cudaGetLastError();
 }
 

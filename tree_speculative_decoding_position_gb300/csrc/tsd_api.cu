@@ -98,7 +98,9 @@ const char* tsd_status_string(tsd_status s) {
     return "unknown status";
 }
 
-static bool build_sizes_ok(int n_trees, int n_modes, int L, int64_t V, int topk, int B) {
+static bool build_sizes_ok(int n_trees, int n_modes, int L, int64_t V, int topk, int B,
+                           int esize) {
+    if (n_chunks(V, esize) > kMaxDrafterChunks) return false;
     if (n_trees < 1 || n_modes < 1 || n_modes > TSD_MAX_MODES || L < 1 || L > TSD_MAX_L ||
         V < 1 || V > 0x7fffffff || topk < 1 || topk > TSD_MAX_TOPK || topk > V || B < 0 ||
         B > TSD_MAX_B)
@@ -114,7 +116,7 @@ size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V,
     if (!es) return 0;
     switch (op) {
         case TSD_OP_BUILD_TREE:
-            if (!build_sizes_ok(n_trees, n_modes, L, V, topk, B)) return 0;
+            if (!build_sizes_ok(n_trees, n_modes, L, V, topk, B, es)) return 0;
             return build_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr);
         case TSD_OP_VERIFY_TEV:
         case TSD_OP_VERIFY_DDTREE:
@@ -130,7 +132,7 @@ tsd_status tsd_build_tree(const void* drafter_logits, tsd_dtype dtype, int n_tre
                           int32_t* rank, int32_t* mode, int32_t* n_nodes, int32_t* status,
                           void* workspace, size_t ws_bytes, cudaStream_t stream) {
     if (!drafter_logits || !parent || !token || !depth || !score || !n_nodes || !status ||
-        !dtype_size(dtype) || !build_sizes_ok(n_trees, n_modes, L, V, topk, B) ||
+        !dtype_size(dtype) || !build_sizes_ok(n_trees, n_modes, L, V, topk, B, dtype_size(dtype)) ||
         !(isfinite(drafter_temp) && drafter_temp >= 1e-6f))
         return TSD_ERR_INVALID_ARG;
     const int es = dtype_size(dtype);

@@ -18,6 +18,9 @@ constexpr int kChunkBytes = 8192;
 constexpr int kVecPerLane = kChunkBytes / (16 * kWarp);  // 16
 
 __host__ __device__ constexpr int chunk_elems(int esize) { return kChunkBytes / esize; }
+// The builder merges per-chunk top-k lists with 64 cursors per lane, so a
+// drafter row may span at most 2048 chunks (V <= 8388608 bf16 / 4194304 fp32).
+constexpr int kMaxDrafterChunks = 2048;
 __host__ __device__ inline int64_t n_chunks(int64_t V, int esize) {
     return (V + chunk_elems(esize) - 1) / chunk_elems(esize);
 }
