@@ -11,21 +11,27 @@
 // position); a prefix taken again from another mode keeps its first node.
 //
 // The pages run this as a sequential heap on the host.  Here one CTA per tree
-// runs it in rounds: the frontier is a sorted array; each round takes its best
-// M entries at once, merges them into the sorted list X of taken entries, and
-// merges their sorted successors back into the frontier.  Taking several
-// entries per round may take some that a one-at-a-time heap would not reach,
-// but never misses one: every entry not yet taken is worse than the frontier
-// head, and the search stops only when the frontier holds nothing better than
-// the B-th distinct prefix of X.  The result is therefore exactly the heap's:
-// the B best distinct prefixes under the total order (score desc, depth asc,
-// mode asc, rank sequence asc), listed in that order (= pop order).
+// runs it in rounds over a sorted frontier: each round takes the frontier's
+// best M entries at once, merges them into the sorted list X of taken
+// entries, and merges all k children of each (CAST App. C's push rule; the
+// oracle's pins show it pops the same prefixes in the same order as the
+// sibling + first-child rule) back into the frontier.  Because a prefix's
+// children arrive one round after it, the number of rounds is about the depth
+// of the tree.  Taking several entries per round may take some that a
+// one-at-a-time heap would not reach, but never misses one: every entry not
+// yet taken is worse than the frontier head, and the search stops only when
+// the frontier holds nothing better than the B-th distinct prefix of X.  The
+// frontier is pruned every round to entries no worse than the (K*B)-th entry
+// of X and the frontier merged (at least B distinct prefixes are that good).
+// The result is exactly the heap's: the B best distinct prefixes under the
+// total order (score desc, depth asc, mode asc, rank sequence asc), listed in
+// that order (= pop order).
 //
 // Entries are 32 bytes: a 64-bit order-preserving image of the float64 score,
 // the 64-bit tie key depth << 59 | mode << 56 | rank digits (which also names
-// the prefix within its mode), the parent's score in the same mode (to score
-// the next sibling), and a 64-bit hash of the parent's token sequence (to tell
-// equal prefixes of different modes apart; every hash match is confirmed by
+// the prefix within its mode), the entry's score in float64 (kept for the
+// record), and a 64-bit hash of the parent's token sequence (to tell equal
+// prefixes of different modes apart; every hash match is confirmed by
 // comparing the token sequences).
 #include "tsd_internal.cuh"
 
@@ -86,13 +92,16 @@ __host__ __device__ inline int pow2_at_least(int x) {
 
 static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     BuildPlan p;
-    p.M = n_modes > 1 ? 64 : 128;
+    // entries taken per round: their children (k each) fill the successor buffer
+    p.M = (n_modes > 1 ? 256 : 512) / topk;
+    if (p.M < 8) p.M = 8;
+    if (p.M > 128) p.M = 128;
     p.xcap = n_modes * (B + 1) + p.M;
-    p.fcap = n_modes * (B + 1) + 2 * p.M + n_modes;
-    p.hcap = pow2_at_least(2 * p.xcap);
+    p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk;
+    p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
     auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
     p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)));
-    p.sbytes = r16(sizeof(FEntry) * 2 * (size_t)p.M);
+    p.sbytes = r16(sizeof(FEntry) * (size_t)pow2_at_least(topk * p.M));
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
     p.fbytes = r16(sizeof(FEntry) * 2 * (size_t)p.fcap);
@@ -228,7 +237,8 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                   int32_t* __restrict__ rank, int32_t* __restrict__ mode,
                   int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ status) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int s_bad, s_nF, s_nX, s_nS, s_D, s_posB;
+    __shared__ int s_bad, s_nF, s_nX, s_nS, s_D, s_posB, s_thr_on;
+    __shared__ FEntry s_thr;  // pruning bound: entries not before it are dead
     __shared__ int red[32];
     const int t = blockIdx.x, tid = threadIdx.x;
     const int nl = K * L * k;
@@ -267,17 +277,22 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     const bool bad = s_bad != 0;
     int fc = 0, xc = 0;  // current buffer indices
     if (!bad && B > 0) {  // B = 0: the tree is the root alone
-        // seeds: each mode's best first token
-        const int n2 = pow2_at_least(K);
+        // seeds: the root's children, all k first tokens of every mode
+        const int n2 = pow2_at_least(K * k);
         for (int i = tid; i < n2; i += blockDim.x) {
             FEntry e;
             e.key = kSentinelKey;
             e.tb = ~0ull;
             e.pscore = 0.0;
             e.hpar = kRootHash;
-            if (i < K && ls.logq(i, 1, 0) != -INFINITY) {
-                e.key = order_key(0.0 + ls.logq(i, 1, 0));
-                e.tb = (1ull << 59) | ((unsigned long long)i << 56);
+            if (i < K * k) {
+                const int m = i / k, r = i % k;
+                const double sv = 0.0 + ls.logq(m, 1, r);
+                if (sv != -INFINITY) {
+                    e.key = order_key(sv);
+                    e.tb = (1ull << 59) | ((unsigned long long)m << 56) | (unsigned long long)r;
+                    e.pscore = sv;
+                }
             }
             F[0][i] = e;
         }
@@ -285,8 +300,9 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         sort_entries(F[0], n2);
         if (tid == 0) {
             int nF = 0;
-            while (nF < K && F[0][nF].key != kSentinelKey) ++nF;
+            while (nF < K * k && F[0][nF].key != kSentinelKey) ++nF;
             s_nF = nF;
+            s_thr_on = 0;
         }
         __syncthreads();
         const int M = plan.M;
@@ -294,50 +310,54 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const int nF = s_nF, nX = s_nX;
             if (nF == 0) break;
             const int bn = min(M, nF);
-            // Successors of the taken entries, then sort them.
+            // All k children of each taken entry (each run is already sorted:
+            // q is sorted by rank), skipping those that cannot beat the bound.
             if (tid == 0) s_nS = 0;
-            for (int i = tid; i < 2 * M; i += blockDim.x) {
-                FEntry snt;
-                snt.key = kSentinelKey;
-                snt.tb = ~0ull;
-                snt.pscore = 0.0;
-                snt.hpar = 0;
-                S[i] = snt;
-            }
             __syncthreads();
+            const FEntry thr = s_thr;
+            const bool thr_on = s_thr_on != 0;
             for (int i = tid; i < bn; i += blockDim.x) {
                 const FEntry e = F[fc][i];
-                const int d = tb_depth(e.tb), m = tb_mode(e.tb), r = ls.last_rank(e.tb);
+                const int d = tb_depth(e.tb), m = tb_mode(e.tb);
+                if (d >= L) continue;
                 const double s = key_score(e.key);
-                if (r + 1 < k) {  // next sibling
-                    const double sv = e.pscore + ls.logq(m, d, r + 1);
-                    if (sv != -INFINITY) {
-                        FEntry sb;
-                        sb.key = order_key(sv);
-                        sb.tb = e.tb + 1;
-                        sb.pscore = e.pscore;
-                        sb.hpar = e.hpar;
-                        S[2 * i] = sb;
-                        atomicAdd(&s_nS, 1);
-                    }
+                const unsigned long long hp = entry_hash(ls, e);
+                const unsigned long long base = ((unsigned long long)(d + 1) << 59) |
+                                                ((unsigned long long)m << 56) |
+                                                (((e.tb & kRsMask) << bits) & kRsMask);
+                // pass 1 counts the children worth keeping, pass 2 writes them
+                int cnt = 0;
+                for (int r = 0; r < k; ++r) {
+                    const double sv = s + ls.logq(m, d + 1, r);
+                    if (sv == -INFINITY) break;  // the rest of the list is -inf too
+                    FEntry c;
+                    c.key = order_key(sv);
+                    c.tb = base | (unsigned long long)r;
+                    if (thr_on && !before(c, thr)) break;  // worse ranks are worse still
+                    ++cnt;
                 }
-                if (d < L) {  // first child
-                    const double sv = s + ls.logq(m, d + 1, 0);
-                    if (sv != -INFINITY) {
-                        FEntry ch;
-                        ch.key = order_key(sv);
-                        ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
-                                (((e.tb & kRsMask) << bits) & kRsMask);
-                        ch.pscore = s;
-                        ch.hpar = entry_hash(ls, e);
-                        S[2 * i + 1] = ch;
-                        atomicAdd(&s_nS, 1);
+                if (cnt) {
+                    const int at = atomicAdd(&s_nS, cnt);
+                    for (int r = 0; r < cnt; ++r) {
+                        const double sv = s + ls.logq(m, d + 1, r);
+                        FEntry c;
+                        c.key = order_key(sv);
+                        c.tb = base | (unsigned long long)r;
+                        c.pscore = sv;
+                        c.hpar = hp;
+                        S[at + r] = c;
                     }
                 }
             }
             __syncthreads();
-            sort_entries(S, 2 * M);
             const int nS = s_nS;
+            const int n2S = pow2_at_least(nS < 2 ? 2 : nS);
+            for (int i = nS + tid; i < n2S; i += blockDim.x) {
+                S[i].key = kSentinelKey;
+                S[i].tb = ~0ull;
+            }
+            __syncthreads();
+            sort_entries(S, n2S);
             if (nX + bn > plan.xcap || nF - bn + nS > plan.fcap) {  // cannot happen (see plan)
                 if (tid == 0) s_bad = 3;
                 __syncthreads();
@@ -414,9 +434,34 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                         else hi = mid;
                     }
                     s_nF = lo;
+                    s_thr = th;
+                    s_thr_on = 1;
                 }
             } else if (tid == 0) {
-                s_nF = nFn;
+                // the (K*B)-th entry of X and the frontier merged: at least B
+                // distinct prefixes are that good, so worse entries are dead
+                const int want = K * B;
+                int keepF = nFn;
+                if (nXn + nFn >= want) {
+                    // co-rank: ia entries of X and want - ia of F form the best `want`
+                    int lo = max(0, want - nFn), hi = min(want, nXn);
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (before(X[xc][mid], F[fc][want - mid - 1])) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    const int ia = lo, ib = want - lo;
+                    // the want-th best is the worse of X[ia-1] and F[ib-1]
+                    FEntry th;
+                    if (ia == 0) th = F[fc][ib - 1];
+                    else if (ib == 0) th = X[xc][ia - 1];
+                    else th = before(X[xc][ia - 1], F[fc][ib - 1]) ? F[fc][ib - 1] : X[xc][ia - 1];
+                    keepF = ib;  // F[ib..] are all after th
+                    s_thr = th;
+                    s_thr_on = 1;
+                    // th itself may be kept (not "before" itself); keep F entries up to it
+                }
+                s_nF = keepF;
             }
             if (tid == 0) {
                 s_nX = nXn;
