@@ -101,7 +101,7 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
     auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
     p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)));
-    p.sbytes = r16(sizeof(FEntry) * (size_t)pow2_at_least(topk * p.M));
+    p.sbytes = r16(sizeof(FEntry) * 2 * (size_t)topk * p.M);  // runs + merge buffer
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
     p.fbytes = r16(sizeof(FEntry) * 2 * (size_t)p.fcap);
@@ -161,6 +161,47 @@ __device__ void merge_entries(FEntry* dst, const FEntry* a, int na, const FEntry
         }
     }
     __syncthreads();
+}
+
+// Sort a[0, nruns*runlen) made of nruns sorted runs of runlen entries by
+// merging adjacent runs pairwise (merge path), ping-ponging with tmp.
+// Returns the buffer that holds the result.
+__device__ FEntry* merge_runs(FEntry* a, FEntry* tmp, int nruns, int runlen) {
+    const int n = nruns * runlen;
+    FEntry* src = a;
+    FEntry* dst = tmp;
+    for (int w = runlen; w < n; w <<= 1) {
+        const int per = (n + blockDim.x - 1) / blockDim.x;
+        for (int o0 = threadIdx.x * per; o0 < n && o0 < (int)(threadIdx.x + 1) * per; o0 += per) {
+            const int o1 = min(n, o0 + per);
+            for (int o = o0; o < o1;) {
+                const int base = (o / (2 * w)) * (2 * w);
+                const int la = base, na = min(w, n - base);
+                const int lb = base + na, nb = min(w, n - lb);
+                const int d0 = o - base;
+                const int dend = min(o1 - base, na + nb);
+                int lo = max(0, d0 - nb), hi = min(d0, na);
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (before(src[la + mid], src[lb + d0 - mid - 1])) lo = mid + 1;
+                    else hi = mid;
+                }
+                int ia = lo, ib = d0 - lo;
+                for (int d = d0; d < dend; ++d) {
+                    if (ib >= nb || (ia < na && before(src[la + ia], src[lb + ib])))
+                        dst[base + d] = src[la + ia++];
+                    else
+                        dst[base + d] = src[lb + ib++];
+                }
+                o = base + dend;
+            }
+        }
+        __syncthreads();
+        FEntry* t = src;
+        src = dst;
+        dst = t;
+    }
+    return src;
 }
 
 // Inclusive block scan of one int per thread; *total = block sum.
@@ -310,54 +351,44 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const int nF = s_nF, nX = s_nX;
             if (nF == 0) break;
             const int bn = min(M, nF);
-            // All k children of each taken entry (each run is already sorted:
-            // q is sorted by rank), skipping those that cannot beat the bound.
+            // Slot e*k + r holds child r of taken entry e, or a sentinel.  A
+            // taken entry's children are sorted by rank (its list is), and the
+            // unusable ones (-inf, or not better than the pruning bound) form
+            // a suffix, so every run of k slots is sorted.
             if (tid == 0) s_nS = 0;
             __syncthreads();
             const FEntry thr = s_thr;
             const bool thr_on = s_thr_on != 0;
-            for (int i = tid; i < bn; i += blockDim.x) {
+            const int nslot = bn * k;
+            int mine = 0;
+            for (int c = tid; c < nslot; c += blockDim.x) {
+                const int i = c / k, r = c - i * k;
                 const FEntry e = F[fc][i];
                 const int d = tb_depth(e.tb), m = tb_mode(e.tb);
-                if (d >= L) continue;
-                const double s = key_score(e.key);
-                const unsigned long long hp = entry_hash(ls, e);
-                const unsigned long long base = ((unsigned long long)(d + 1) << 59) |
-                                                ((unsigned long long)m << 56) |
-                                                (((e.tb & kRsMask) << bits) & kRsMask);
-                // pass 1 counts the children worth keeping, pass 2 writes them
-                int cnt = 0;
-                for (int r = 0; r < k; ++r) {
-                    const double sv = s + ls.logq(m, d + 1, r);
-                    if (sv == -INFINITY) break;  // the rest of the list is -inf too
-                    FEntry c;
-                    c.key = order_key(sv);
-                    c.tb = base | (unsigned long long)r;
-                    if (thr_on && !before(c, thr)) break;  // worse ranks are worse still
-                    ++cnt;
-                }
-                if (cnt) {
-                    const int at = atomicAdd(&s_nS, cnt);
-                    for (int r = 0; r < cnt; ++r) {
-                        const double sv = s + ls.logq(m, d + 1, r);
-                        FEntry c;
-                        c.key = order_key(sv);
-                        c.tb = base | (unsigned long long)r;
-                        c.pscore = sv;
-                        c.hpar = hp;
-                        S[at + r] = c;
+                FEntry ch;
+                ch.key = kSentinelKey;
+                ch.tb = ~0ull;
+                ch.pscore = 0.0;
+                ch.hpar = 0;
+                if (d < L) {
+                    const double sv = key_score(e.key) + ls.logq(m, d + 1, r);
+                    FEntry cand;
+                    cand.key = order_key(sv);
+                    cand.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
+                              (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
+                    if (sv != -INFINITY && (!thr_on || before(cand, thr))) {
+                        ch = cand;
+                        ch.pscore = sv;
+                        ch.hpar = entry_hash(ls, e);
+                        ++mine;
                     }
                 }
+                S[c] = ch;
             }
+            if (mine) atomicAdd(&s_nS, mine);
             __syncthreads();
             const int nS = s_nS;
-            const int n2S = pow2_at_least(nS < 2 ? 2 : nS);
-            for (int i = nS + tid; i < n2S; i += blockDim.x) {
-                S[i].key = kSentinelKey;
-                S[i].tb = ~0ull;
-            }
-            __syncthreads();
-            sort_entries(S, n2S);
+            FEntry* Ssorted = merge_runs(S, S + (size_t)k * M, bn, k);
             if (nX + bn > plan.xcap || nF - bn + nS > plan.fcap) {  // cannot happen (see plan)
                 if (tid == 0) s_bad = 3;
                 __syncthreads();
@@ -366,7 +397,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             // Taken entries join X (both sorted); the rest of the frontier
             // merges with the successors.
             merge_entries(X[xc ^ 1], X[xc], nX, F[fc], bn);
-            merge_entries(F[fc ^ 1], F[fc] + bn, nF - bn, S, nS);
+            merge_entries(F[fc ^ 1], F[fc] + bn, nF - bn, Ssorted, nS);
             xc ^= 1;
             fc ^= 1;
             int nXn = nX + bn, nFn = nF - bn + nS;
