@@ -97,11 +97,11 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     if (p.M < 8) p.M = 8;
     if (p.M > 128) p.M = 128;
     p.xcap = n_modes * (B + 1) + p.M;
-    p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk;
+    p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk + 32;
     p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
     auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
     p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)));
-    p.sbytes = r16(sizeof(FEntry) * 2 * (size_t)topk * p.M);  // runs + merge buffer
+    p.sbytes = r16(sizeof(FEntry) * (size_t)pow2_at_least(topk * p.M < 32 ? 32 : topk * p.M));
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
     p.fbytes = r16(sizeof(FEntry) * 2 * (size_t)p.fcap);
@@ -122,10 +122,44 @@ size_t heap_spill_bytes(int n_modes, int L, int topk, int B) {
 // ---------------------------------------------------------------------------
 // Block-wide helpers (all threads call them).
 // ---------------------------------------------------------------------------
-// Bitonic sort of a[0, n2) (n2 a power of two) into the total order.
+__device__ __forceinline__ FEntry shfl_xor_entry(const FEntry& x, int j) {
+    FEntry y;
+    y.key = __shfl_xor_sync(0xffffffffu, x.key, j);
+    y.tb = __shfl_xor_sync(0xffffffffu, x.tb, j);
+    y.pscore = __shfl_xor_sync(0xffffffffu, x.pscore, j);
+    y.hpar = __shfl_xor_sync(0xffffffffu, x.hpar, j);
+    return y;
+}
+
+// Bitonic steps (k, j) for j from jtop down to 1 on one 32-entry block held
+// one entry per lane: partners differ in lane bits, so shuffles replace
+// shared-memory exchanges and no block barrier is needed.
+__device__ __forceinline__ FEntry bitonic_lane_steps(FEntry x, int e, int lane, int k, int jtop) {
+    for (int j = jtop; j > 0; j >>= 1) {
+        const FEntry y = shfl_xor_entry(x, j);
+        const bool lower = (lane & j) == 0;
+        const bool asc = (e & k) == 0;  // this k-block ends up in the total order
+        const bool x_first = before(x, y);
+        if ((lower == asc) != x_first) x = y;
+    }
+    return x;
+}
+
+// Bitonic sort of a[0, n2) (n2 a power of two, at least 32) into the total
+// order.  Steps with partner distance below 32 run in registers per warp;
+// only distances of 32 and more exchange through memory between barriers.
 __device__ void sort_entries(FEntry* a, int n2) {
-    for (int k = 2; k <= n2; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nblk = n2 >> 5;
+    for (int b = wid; b < nblk; b += nw) {  // k = 2 .. 32 inside each block
+        const int e = (b << 5) + lane;
+        FEntry x = a[e];
+        for (int k = 2; k <= 32; k <<= 1) x = bitonic_lane_steps(x, e, lane, k, k >> 1);
+        a[e] = x;
+    }
+    __syncthreads();
+    for (int k = 64; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j >= 32; j >>= 1) {
             for (int i = threadIdx.x; i < n2; i += blockDim.x) {
                 const int l = i ^ j;
                 if (l > i) {
@@ -139,6 +173,11 @@ __device__ void sort_entries(FEntry* a, int n2) {
             }
             __syncthreads();
         }
+        for (int b = wid; b < nblk; b += nw) {
+            const int e = (b << 5) + lane;
+            a[e] = bitonic_lane_steps(a[e], e, lane, k, 16);
+        }
+        __syncthreads();
     }
 }
 
@@ -161,47 +200,6 @@ __device__ void merge_entries(FEntry* dst, const FEntry* a, int na, const FEntry
         }
     }
     __syncthreads();
-}
-
-// Sort a[0, nruns*runlen) made of nruns sorted runs of runlen entries by
-// merging adjacent runs pairwise (merge path), ping-ponging with tmp.
-// Returns the buffer that holds the result.
-__device__ FEntry* merge_runs(FEntry* a, FEntry* tmp, int nruns, int runlen) {
-    const int n = nruns * runlen;
-    FEntry* src = a;
-    FEntry* dst = tmp;
-    for (int w = runlen; w < n; w <<= 1) {
-        const int per = (n + blockDim.x - 1) / blockDim.x;
-        for (int o0 = threadIdx.x * per; o0 < n && o0 < (int)(threadIdx.x + 1) * per; o0 += per) {
-            const int o1 = min(n, o0 + per);
-            for (int o = o0; o < o1;) {
-                const int base = (o / (2 * w)) * (2 * w);
-                const int la = base, na = min(w, n - base);
-                const int lb = base + na, nb = min(w, n - lb);
-                const int d0 = o - base;
-                const int dend = min(o1 - base, na + nb);
-                int lo = max(0, d0 - nb), hi = min(d0, na);
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (before(src[la + mid], src[lb + d0 - mid - 1])) lo = mid + 1;
-                    else hi = mid;
-                }
-                int ia = lo, ib = d0 - lo;
-                for (int d = d0; d < dend; ++d) {
-                    if (ib >= nb || (ia < na && before(src[la + ia], src[lb + ib])))
-                        dst[base + d] = src[la + ia++];
-                    else
-                        dst[base + d] = src[lb + ib++];
-                }
-                o = base + dend;
-            }
-        }
-        __syncthreads();
-        FEntry* t = src;
-        src = dst;
-        dst = t;
-    }
-    return src;
 }
 
 // Inclusive block scan of one int per thread; *total = block sum.
@@ -319,7 +317,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     int fc = 0, xc = 0;  // current buffer indices
     if (!bad && B > 0) {  // B = 0: the tree is the root alone
         // seeds: the root's children, all k first tokens of every mode
-        const int n2 = pow2_at_least(K * k);
+        const int n2 = pow2_at_least(K * k < 32 ? 32 : K * k);
         for (int i = tid; i < n2; i += blockDim.x) {
             FEntry e;
             e.key = kSentinelKey;
@@ -351,44 +349,50 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const int nF = s_nF, nX = s_nX;
             if (nF == 0) break;
             const int bn = min(M, nF);
-            // Slot e*k + r holds child r of taken entry e, or a sentinel.  A
-            // taken entry's children are sorted by rank (its list is), and the
-            // unusable ones (-inf, or not better than the pruning bound) form
-            // a suffix, so every run of k slots is sorted.
-            if (tid == 0) s_nS = 0;
-            __syncthreads();
+            // Children of the taken entries, one thread per (entry, rank) slot.
+            // An entry's children are sorted by rank (its list is), and the
+            // unusable ones (-inf, or not better than the pruning bound) form a
+            // suffix; a block scan over the slots' flags packs the usable ones.
             const FEntry thr = s_thr;
             const bool thr_on = s_thr_on != 0;
             const int nslot = bn * k;
-            int mine = 0;
-            for (int c = tid; c < nslot; c += blockDim.x) {
-                const int i = c / k, r = c - i * k;
-                const FEntry e = F[fc][i];
-                const int d = tb_depth(e.tb), m = tb_mode(e.tb);
+            int written = 0;
+            for (int c0 = 0; c0 < nslot; c0 += blockDim.x) {
+                const int c = c0 + tid;
                 FEntry ch;
-                ch.key = kSentinelKey;
-                ch.tb = ~0ull;
-                ch.pscore = 0.0;
-                ch.hpar = 0;
-                if (d < L) {
-                    const double sv = key_score(e.key) + ls.logq(m, d + 1, r);
-                    FEntry cand;
-                    cand.key = order_key(sv);
-                    cand.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
-                              (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
-                    if (sv != -INFINITY && (!thr_on || before(cand, thr))) {
-                        ch = cand;
+                int ok = 0;
+                if (c < nslot) {
+                    const int i = c / k, r = c - i * k;
+                    const FEntry e = F[fc][i];
+                    const int d = tb_depth(e.tb), m = tb_mode(e.tb);
+                    if (d < L) {
+                        const double sv = key_score(e.key) + ls.logq(m, d + 1, r);
+                        ch.key = order_key(sv);
+                        ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
+                                (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
                         ch.pscore = sv;
-                        ch.hpar = entry_hash(ls, e);
-                        ++mine;
+                        ok = sv != -INFINITY && (!thr_on || before(ch, thr));
+                        if (ok) ch.hpar = entry_hash(ls, e);
                     }
                 }
-                S[c] = ch;
+                int tot;
+                const int pos = written + block_incl_scan_int(ok, red, &tot) - 1;
+                if (ok) S[pos] = ch;
+                written += tot;
             }
-            if (mine) atomicAdd(&s_nS, mine);
+            if (tid == 0) s_nS = written;
             __syncthreads();
             const int nS = s_nS;
-            FEntry* Ssorted = merge_runs(S, S + (size_t)k * M, bn, k);
+            FEntry* Ssorted = S;
+            if (nS > 1) {
+                const int n2S = pow2_at_least(nS < 32 ? 32 : nS);
+                for (int i = nS + tid; i < n2S; i += blockDim.x) {
+                    S[i].key = kSentinelKey;
+                    S[i].tb = ~0ull;
+                }
+                __syncthreads();
+                sort_entries(S, n2S);
+            }
             if (nX + bn > plan.xcap || nF - bn + nS > plan.fcap) {  // cannot happen (see plan)
                 if (tid == 0) s_bad = 3;
                 __syncthreads();
