@@ -9,10 +9,9 @@
 //   the top-k tokens by (logit desc, id asc) and log q_j = z / T_d - LSE_j.
 //
 // drafter_chunk_kernel  one warp per (row, 8 KB chunk): chunk max, sum of
-//                       exp2(z*c - mc), and the chunk's top-k, kept as a
-//                       warp-distributed sorted list (lane i holds the i-th
-//                       best) that a candidate enters by one shuffle step.
-// drafter_row_kernel    one warp per row: merges the chunk lists and sums.
+//                       exp2(z*c - mc), and the chunk's top-k.
+// drafter_row_kernel    one warp per row: merges the chunk lists into the
+//                       row's top-k, and the chunk sums into its LSE.
 #include "tsd_internal.cuh"
 
 namespace tsd {
@@ -88,6 +87,26 @@ __device__ __forceinline__ float warp_sort_desc(float x, int lane) {
         }
     }
     return x;
+}
+
+// Sort one (value, id) pair per lane across the warp into (value desc, id
+// asc) order (bitonic; lane 0 ends with the best).
+__device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
+#pragma unroll
+    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+            const int oi = __shfl_xor_sync(0xffffffffu, id, j);
+            const bool lower = (lane & j) == 0;
+            const bool first = (lane & k2) == 0;  // this block ends up best-first
+            const bool mine_first = better(v, id, ov, oi);
+            if ((lower == first) != mine_first) {
+                v = ov;
+                id = oi;
+            }
+        }
+    }
 }
 
 // One warp per (row, 8 KB chunk).  Pass 1: the chunk max, the sum of
@@ -206,6 +225,11 @@ drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int 
         const int nc = cand_n[wid];
         if (nc > kCandCap) {
             chunk_topk_fallback<T>(rp, cn, c0, k, lane, ev, ei);
+        } else if (nc <= kWarp) {
+            // the usual case: one warp sort of the candidates
+            ev = lane < nc ? cand_v[wid][lane] : -INFINITY;
+            ei = lane < nc ? cand_i[wid][lane] : INT_MAX;
+            warp_sort_pairs(ev, ei, lane);
         } else {
             // k rounds of arg-max over the candidates; a taken one becomes
             // (-inf, INT_MAX), which every real token beats.
@@ -249,17 +273,32 @@ drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int 
     }
 }
 
-// One warp per row: the row's log-normaliser from the chunk sums (float64),
-// and its top-k merged from the chunks' sorted lists -- lane l walks the
-// lists of chunks l, l+32, ...; k rounds of warp arg-max over the lanes'
-// current heads.
+constexpr int kRowStage = 1024;  // candidates staged in shared memory per warp
+
+// One warp per row: the row's log-normaliser from its chunk sums (float64),
+// and its top-k merged from the chunks' sorted lists.  The lists are first
+// copied to shared memory in one coalesced pass (when they fit), then lane l
+// walks the lists of chunks l, l+32, ...; k rounds of warp arg-max over the
+// lanes' current heads.
 __global__ void __launch_bounds__(kDThreads)
 drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs ws) {
+    __shared__ float sv[kDThreads / kWarp][kRowStage];
+    __shared__ int si[kDThreads / kWarp][kRowStage];
     const int lane = threadIdx.x & (kWarp - 1);
+    const int wid = threadIdx.x / kWarp;
     const int wpb = blockDim.x / kWarp;
-    for (int64_t row = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; row < rows;
+    for (int64_t row = (int64_t)blockIdx.x * wpb + wid; row < rows;
          row += (int64_t)gridDim.x * wpb) {
         const ChunkStat* cs = ws.chunk + row * nch;
+        const int ncand = nch * k;
+        const bool staged = ncand <= kRowStage;
+        const float* gv = ws.cand_v + row * ncand;
+        const int* gi = ws.cand_i + row * ncand;
+        if (staged)
+            for (int q = lane; q < ncand; q += kWarp) {
+                sv[wid][q] = gv[q];
+                si[wid][q] = gi[q];
+            }
         float m = -INFINITY;
         bool bad = false;
         for (int q = lane; q < nch; q += kWarp) {
@@ -276,9 +315,9 @@ drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs w
         // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
         const double lse = bad ? __longlong_as_double(0x7ff8000000000000ll)
                                : 0.6931471805599453 * ((double)mc + log2(s));
-        const float* cv = ws.cand_v + row * nch * k;
-        const int* ci = ws.cand_i + row * nch * k;
-        // lane cursors: chunk q = lane + 32 j, position pos[j] within its list
+        __syncwarp();
+        const float* cv = staged ? sv[wid] : gv;
+        const int* ci = staged ? si[wid] : gi;
         int pos[kMaxListsPerLane];
         const int nj = (nch + kWarp - 1) / kWarp;
         for (int j = 0; j < nj; ++j) pos[j] = 0;
@@ -313,6 +352,7 @@ drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs w
             ws.top_id[row * k + lane] = ei;
             ws.top_lq[row * k + lane] = (double)ev / temp - lse;
         }
+        __syncwarp();
     }
 }
 
