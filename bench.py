@@ -37,7 +37,7 @@ WORKLOAD = dict(workload="batched verification: 32 independent trees, V=151936, 
                          "top-k=8, B=256, T=0.6, bf16 (Gumbel-perturbed Zipf drafter; "
                          "target = drafter row at node depth + N(0, 1.5^2))",
                 trees_per_gpu=32, V=151936, L=16, topk=8, B=256, temperature=0.6,
-                step="tsd_build_tree + tsd_tree_mask + tsd_verify_tev",
+                step="tsd_build_tree, then tsd_tree_mask (side stream) alongside tsd_verify_tev",
                 l2="inputs larger than L2: 2.66 GB of logits read per step per GPU, no flush")
 HBM_PEAK_FALLBACK = 6800.0
 
@@ -161,6 +161,7 @@ def run_ours(args):
     ws_v = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, nt, 1, 1, V, 1, B,
                                               torch.bfloat16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)  # the mask does not depend on TEV: run it alongside
 
     def new_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -174,13 +175,16 @@ def run_ours(args):
         t_ = tsd.tsd_build_tree(drafter, topk=k, B=B, workspace=ws_b)
         if ev is not None:
             ev[1].record(stream)
-        tsd.tsd_tree_mask(t_["parent"], t_["n_nodes"], prefix_len=1024)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            tsd.tsd_tree_mask(t_["parent"], t_["n_nodes"], prefix_len=1024)
         if ev is not None:
             out = tsd.tsd_verify_tev_timed(target, t_["parent"], t_["token"], t_["n_nodes"], T,
                                            seed=i, stage_events=ev[2:7], workspace=ws_v)
         else:
             out = tsd.tsd_verify_tev(target, t_["parent"], t_["token"], t_["n_nodes"], T,
                                      seed=i, workspace=ws_v)
+        stream.wait_stream(side)
         return t_, out
 
     for i in range(args.warmup):
@@ -213,8 +217,8 @@ def run_ours(args):
     # stage durations from the events inside each step
     def avg(a, b):
         return statistics.mean(evsets[i][a].elapsed_time(evsets[i][b]) for i in range(args.steps))
-    stage = dict(build=avg(0, 1), mask=avg(1, 2), tev_prep=avg(2, 3), tev_rows=avg(3, 4),
-                 tev_combine=avg(4, 5), tev_draws=avg(5, 6))
+    stage = dict(build=avg(0, 1), tev_prep=avg(2, 3), tev_rows=avg(3, 4),
+                 tev_combine=avg(4, 5), tev_draws=avg(5, 6))  # the mask runs on a side stream
     n_nodes_total = int(last[0]["n_nodes"].sum())
     rows_bytes = n_nodes_total * V * 2
     peak, peak_kind = measured_peaks()

@@ -35,9 +35,33 @@ __device__ __forceinline__ uint64_t child_key(int p, int tok, int u) {
     return ((uint64_t)p << 43) | ((uint64_t)(uint32_t)tok << 12) | (uint64_t)u;
 }
 
+// Bitonic sort of keys[0, n2) ascending (n2 a power of two, at least 32).
+// Steps with partner distance below 32 run in registers with warp shuffles;
+// only longer distances exchange through shared memory between barriers.
+__device__ __forceinline__ uint64_t bitonic_lane_steps_u64(uint64_t x, int e, int lane, int k,
+                                                           int jtop) {
+    for (int j = jtop; j > 0; j >>= 1) {
+        const uint64_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        const bool lower = (lane & j) == 0;
+        const bool asc = (e & k) == 0;
+        const uint64_t lo = x < y ? x : y, hi = x < y ? y : x;
+        x = (lower == asc) ? lo : hi;
+    }
+    return x;
+}
+
 __device__ void block_bitonic_sort(uint64_t* keys, int n2) {
-    for (int k = 2; k <= n2; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nblk = n2 >> 5;
+    for (int b = wid; b < nblk; b += nw) {
+        const int e = (b << 5) + lane;
+        uint64_t x = keys[e];
+        for (int k = 2; k <= 32; k <<= 1) x = bitonic_lane_steps_u64(x, e, lane, k, k >> 1);
+        keys[e] = x;
+    }
+    __syncthreads();
+    for (int k = 64; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j >= 32; j >>= 1) {
             for (int i = threadIdx.x; i < n2; i += blockDim.x) {
                 const int l = i ^ j;
                 if (l > i) {
@@ -51,6 +75,11 @@ __device__ void block_bitonic_sort(uint64_t* keys, int n2) {
             }
             __syncthreads();
         }
+        for (int b = wid; b < nblk; b += nw) {
+            const int e = (b << 5) + lane;
+            keys[e] = bitonic_lane_steps_u64(keys[e], e, lane, k, 16);
+        }
+        __syncthreads();
     }
 }
 
@@ -67,7 +96,7 @@ verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
     __syncthreads();
     const int nn = bad ? 1 : n;
     const int m = nn - 1;  // number of child edges
-    int n2 = 1;
+    int n2 = 32;
     while (n2 < m) n2 <<= 1;
     for (int i = threadIdx.x; i < n2; i += blockDim.x) {
         uint64_t key = ~0ull;

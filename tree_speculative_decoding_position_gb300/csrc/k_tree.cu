@@ -95,7 +95,7 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
                 int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
                 float* __restrict__ exit_mass, float* __restrict__ prefix_prob,
                 float* __restrict__ coverage, int32_t* __restrict__ status) {
-    extern __shared__ float sh[];  // w[B+1]
+    extern __shared__ float sh[];  // w[B+1], pedge[B+1], and parents as int[B+1]
     __shared__ float red[33];
     __shared__ int pick[2];
     __shared__ int exit_v;
@@ -117,10 +117,19 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
         }
         return;
     }
-    const int32_t* par = parent + (int64_t)t * stride;
-    const float* pedge = ws.pedge + (int64_t)t * stride;
+    const int32_t* gpar = parent + (int64_t)t * stride;
+    const float* gpedge = ws.pedge + (int64_t)t * stride;
     const float* rho = ws.rho + (int64_t)t * stride;
     float* w = sh;
+    float* pedge = sh + stride;
+    int* par = reinterpret_cast<int*>(sh + 2 * stride);
+    // the tree's parents and edge probabilities in shared memory (one
+    // coalesced read) so that the ancestor walks below stay on chip
+    for (int u = threadIdx.x; u < n; u += blockDim.x) {
+        par[u] = gpar[u];
+        pedge[u] = gpedge[u];
+    }
+    __syncthreads();
     // Alg. 1 lines 3-7: P(u) as the product of the edge probabilities on the
     // root path (depth-parallel: every node walks its own ancestors).
     float cov_part = 0.0f;
@@ -244,7 +253,11 @@ cudaError_t launch_tev_tree(const void* logits, tsd_dtype dtype, int n_trees, in
                             cudaStream_t stream) {
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
-    const size_t smem = sizeof(float) * (size_t)(B + 1);
+    const size_t smem = 3 * sizeof(float) * (size_t)(B + 1);
+    cudaError_t e = cudaFuncSetAttribute(dtype == TSD_BF16 ? (const void*)tev_tree_kernel<__nv_bfloat16>
+                                                           : (const void*)tev_tree_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     if (dtype == TSD_BF16)
         tev_tree_kernel<__nv_bfloat16><<<n_trees, kTreeThreads, smem, stream>>>(
             static_cast<const __nv_bfloat16*>(logits), B, V, nch, c, greedy, seed, parent, n_nodes,
