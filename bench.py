@@ -353,8 +353,7 @@ def cpu_baseline(drafter, target, tree, k, B, T, budget_s=12.0):
         n = int(tree["n_nodes"][t])
         tg = target[t, :n].float().cpu().numpy()
         t0 = time.perf_counter()
-        _, tid, tlq = oracle.drafter_stats(dr, 1.0, k)
-        ref = oracle.build_tree(tid, tlq, B)
+        ref = oracle.build_tree(oracle.drafter_lists(dr, 1.0, k), B)
         oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
         oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
         spent += time.perf_counter() - t0
@@ -388,8 +387,7 @@ def run_reference(args):
         if t not in cache:
             seed = synth.seed_for(2, t)
             dr = synth.zipf_drafter(1, L, V, 0, device="cpu", seeds=[seed])[0, 0]
-            _, tid, tlq = oracle.drafter_stats(dr.float().numpy(), 1.0, k)
-            ref = oracle.build_tree(tid, tlq, B)
+            ref = oracle.build_tree(oracle.drafter_lists(dr.float().numpy(), 1.0, k), B)
             n = ref["n_nodes"]
             tg = synth.target_from_rows(dr, ref["depth"][:n], 1.5, seed + 1).float().numpy()
             cache[t] = (dr.float().numpy(), tg)
@@ -398,8 +396,7 @@ def run_reference(args):
     def one_tree(t):
         z, tg = inputs(t % 4)
         t0 = time.perf_counter()
-        _, tid, tlq = oracle.drafter_stats(z, 1.0, k)
-        ref = oracle.build_tree(tid, tlq, B)
+        ref = oracle.build_tree(oracle.drafter_lists(z, 1.0, k), B)
         oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
         oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
         return time.perf_counter() - t0

@@ -47,8 +47,8 @@ def _load():
         lib.orc_philox4x64_10.restype = None
         lib.orc_uniform.argtypes = [u64, u64, u64, u64]
         lib.orc_uniform.restype = f64
-        lib.orc_drafter_stats.argtypes = [P, i64, i64, f64, i32, P, P, P]
-        lib.orc_build_tree.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        lib.orc_drafter_stats.argtypes = [P, i64, i64, f64, i32, P, P, P, P]
+        lib.orc_build_tree.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
         lib.orc_tree_mask.argtypes = [P, i32, i32, i32, P, P, P, i64]
         lib.orc_row_probs.argtypes = [P, i64, f64, P]
         lib.orc_tev.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P, P, P, P, P, P, P, P]
@@ -101,34 +101,53 @@ def uniform(seed: int, tree: int, node: int, stream: int) -> float:
 
 def drafter_stats(z, temp: float, k: int):
     """Per row: LSE of z/temp, top-k ids by (logit desc, id asc), their log q."""
+    d = drafter_lists(z, temp, k)
+    return d["lse"], d["top_id"], d["top_logq"]
+
+
+def drafter_lists(z, temp: float, k: int) -> dict:
+    """The builder's input, per row: lse (log-normaliser of z/temp), top_id
+    (top-k by logit desc, id asc), top_logq (their log q) and top_zt (their
+    z/temp).  z: [..., V]; leading dims are kept (e.g. [K, L])."""
     z = _f64(z)
     V = z.shape[-1]
     rows = z.size // V
     lse = np.zeros(rows)
     tid = np.zeros((rows, k), dtype=np.int32)
     tlq = np.zeros((rows, k))
-    _check(_load().orc_drafter_stats(_ptr(z), rows, V, temp, k, _ptr(lse), _ptr(tid), _ptr(tlq)),
-           "drafter_stats")
+    tzt = np.zeros((rows, k))
+    _check(_load().orc_drafter_stats(_ptr(z), rows, V, temp, k, _ptr(lse), _ptr(tid), _ptr(tlq),
+                                     _ptr(tzt)), "drafter_stats")
     shp = z.shape[:-1]
-    return lse.reshape(shp), tid.reshape(shp + (k,)), tlq.reshape(shp + (k,))
+    return dict(lse=lse.reshape(shp), top_id=tid.reshape(shp + (k,)),
+                top_logq=tlq.reshape(shp + (k,)), top_zt=tzt.reshape(shp + (k,)))
 
 
-def build_tree(top_id, top_logq, B: int, push_rule: int = 0) -> dict:
-    """Best-first builder on one tree.  top_id/top_logq: [K, L, k] (or [L, k])."""
-    tid = _i32(top_id)
-    tlq = _f64(top_logq)
+def build_tree(lists: dict, B: int, push_rule: int = 0) -> dict:
+    """Best-first builder on one tree.  lists: top_id, top_zt [K, L, k] (or
+    [L, k]) and lse [K, L] (or [L]), as drafter_lists returns them."""
+    tid = _i32(lists["top_id"])
+    tzt = _f64(lists["top_zt"])
+    lse = _f64(lists["lse"])
     if tid.ndim == 2:
-        tid, tlq = tid[None], tlq[None]
+        tid, tzt, lse = tid[None], tzt[None], lse[None]
     K, L, k = tid.shape
     out = {n: np.zeros(B + 1, dtype=np.int32) for n in ("parent", "token", "depth", "rank", "mode")}
     out["score"] = np.zeros(B + 1)
     nn = np.zeros(1, dtype=np.int32)
-    _check(_load().orc_build_tree(_ptr(tid), _ptr(tlq), K, L, k, B, push_rule,
-                                  _ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]),
-                                  _ptr(out["score"]), _ptr(out["rank"]), _ptr(out["mode"]), _ptr(nn)),
-           "build_tree")
+    _check(_load().orc_build_tree(_ptr(tid), _ptr(tzt), _ptr(np.ascontiguousarray(lse)), K, L, k,
+                                  B, push_rule, _ptr(out["parent"]), _ptr(out["token"]),
+                                  _ptr(out["depth"]), _ptr(out["score"]), _ptr(out["rank"]),
+                                  _ptr(out["mode"]), _ptr(nn)), "build_tree")
     out["n_nodes"] = int(nn[0])
     return out
+
+
+def lists_from_logq(top_id, top_logq) -> dict:
+    """Builder lists from log-probabilities alone (z/T = log q, LSE = 0): for
+    tests that state a universe directly by its log q."""
+    tlq = _f64(top_logq)
+    return dict(top_id=_i32(top_id), top_zt=tlq, lse=np.zeros(tlq.shape[:-1]))
 
 
 def tree_mask(parent, n_nodes: int, B: int, prefix_len: int, with_additive: bool = False):

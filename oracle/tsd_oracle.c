@@ -98,10 +98,11 @@ double orc_uniform(uint64_t seed, uint64_t tree, uint64_t node, uint64_t stream)
 /* ------------------------------------------------------------------------ */
 /* Drafter statistics [CAST Sec. 2 Eq. 1, App. C]: for each row j,           */
 /*   LSE_j = log sum_a exp(z_j(a)/T),  log q_j(a) = z_j(a)/T - LSE_j,       */
-/* and the top-k tokens ordered by (logit desc, id asc).                     */
+/* and the top-k tokens ordered by (logit desc, id asc), with their log q    */
+/* and their scaled logits z/T (top_zt, nullable).                           */
 /* ------------------------------------------------------------------------ */
 int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int k,
-                      double *lse, int32_t *top_id, double *top_logq)
+                      double *lse, int32_t *top_id, double *top_logq, double *top_zt)
 {
     if (!(temp > 0.0) || k < 1 || k > V || V < 1) return ORC_ERR_ARG;
     for (int64_t r = 0; r < rows; ++r) {
@@ -127,6 +128,7 @@ int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int
             }
             top_id[r * k + i] = (int32_t)best;
             top_logq[r * k + i] = row[best] / temp - lse[r];
+            if (top_zt) top_zt[r * k + i] = row[best] / temp;
         }
     }
     return ORC_OK;
@@ -136,11 +138,15 @@ int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int
 /* Best-first tree builder.                                                  */
 /*                                                                           */
 /* Universe: for each mode m (K modes; K = 1 is DDTree / CAST) and drafter   */
-/* position j = 1..L, the k retained tokens of that mode's row, with their   */
-/* unrenormalised log-probabilities.  A heap entry (m, v) is a prefix v      */
-/* scored under mode m: s_m(v) = sum_j log q_{m,j}(v_j) [CAST Eq. 1;         */
-/* MFD Eq. 2 with a uniform prior, whose constant log(1/K) is dropped from   */
-/* the ranking].                                                             */
+/* position j = 1..L, the k retained tokens of that mode's row.  A heap      */
+/* entry (m, v) is a prefix v scored under mode m by its unrenormalised      */
+/* log-probability s_m(v) = sum_j log q_{m,j}(v_j) [CAST Eq. 1; MFD Eq. 2    */
+/* with a uniform prior, whose constant log(1/K) is dropped from the         */
+/* ranking], evaluated as                                                    */
+/*   s_m(v) = (sum_j z_{m,j}(v_j)/T) - C_m(|v|),  C_m(d) = sum_{j<=d} LSE_{m,j} */
+/* with the path sum taken left to right: equal in exact arithmetic to the  */
+/* sum of log q, and two prefixes of one depth and mode whose scaled logits  */
+/* sum to the same value tie exactly, so the tie order decides them.         */
 /*                                                                           */
 /* push_rule 0 [MFD App. B]: seed with each mode's rank-0 first token; a pop */
 /*   pushes its next sibling (rank r+1) and its first child (rank 0 at the   */
@@ -151,8 +157,9 @@ int orc_drafter_stats(const double *z, int64_t rows, int64_t V, double temp, int
 /* its successors are pushed either way [MFD App. B].                        */
 /* ------------------------------------------------------------------------ */
 typedef struct {
-    double score;        /* s_m(v) */
-    double pscore;       /* s_m(parent of v) */
+    double score;        /* s_m(v) = zsum - C_m(depth) */
+    double zsum;         /* sum of z/T along v */
+    double pzsum;        /* the same sum along v's parent */
     int32_t mode;
     int32_t depth;       /* |v| >= 1 */
     int32_t rank;        /* rank of v's last token in mode m's list */
@@ -205,13 +212,16 @@ static orc_entry heap_pop(orc_heap *h)
 }
 
 /*
- * top_id, top_logq: [K][L][k] (mode-major, then position, then rank).
+ * top_id, top_zt: [K][L][k] (mode-major, then position, then rank): the
+ * retained tokens and their scaled logits z/T; lse: [K][L] the rows'
+ * log-normalisers.
  * Outputs have B+1 slots; node 0 is the root (parent -1, token -1, depth 0,
  * score 0).  Slots past n_nodes are filled with -1 and score -inf.
  */
-int orc_build_tree(const int32_t *top_id, const double *top_logq, int K, int L, int k, int B,
-                   int push_rule, int32_t *parent, int32_t *token, int32_t *depth,
-                   double *score, int32_t *rank, int32_t *mode, int32_t *n_nodes_out)
+int orc_build_tree(const int32_t *top_id, const double *top_zt, const double *lse, int K, int L,
+                   int k, int B, int push_rule, int32_t *parent, int32_t *token,
+                   int32_t *depth, double *score, int32_t *rank, int32_t *mode,
+                   int32_t *n_nodes_out)
 {
     if (K < 1 || L < 1 || L > ORC_MAX_DEPTH || k < 1 || k > 255 || B < 0) return ORC_ERR_ARG;
     for (int i = 0; i <= B; ++i) {
@@ -228,15 +238,23 @@ int orc_build_tree(const int32_t *top_id, const double *top_logq, int K, int L, 
     h.n = 0;
     h.e = (orc_entry *)malloc(sizeof(orc_entry) * (size_t)h.cap);
 
-#define LQ(m, j, r) top_logq[((int64_t)(m) * L + (j)) * k + (r)]
+#define ZT(m, j, r) top_zt[((int64_t)(m) * L + (j)) * k + (r)]
 #define TK(m, j, r) top_id[((int64_t)(m) * L + (j)) * k + (r)]
+    /* C_m(d): cumulative log-normaliser of mode m over positions 1..d */
+    double *cum = (double *)malloc(sizeof(double) * (size_t)K * (size_t)(L + 1));
+    for (int m = 0; m < K; ++m) {
+        cum[m * (L + 1)] = 0.0;
+        for (int d = 1; d <= L; ++d) cum[m * (L + 1) + d] = cum[m * (L + 1) + d - 1] + lse[m * L + d - 1];
+    }
+#define CUM(m, d) cum[(m) * (L + 1) + (d)]
     for (int m = 0; m < K; ++m) {
         int nseed = (push_rule == 0) ? 1 : k;
         for (int r = 0; r < nseed; ++r) {
             orc_entry x;
             memset(&x, 0, sizeof x);
             x.mode = m; x.depth = 1; x.rank = r; x.pnode = 0;
-            x.pscore = 0.0; x.score = 0.0 + LQ(m, 0, r);
+            x.pzsum = 0.0; x.zsum = 0.0 + ZT(m, 0, r);
+            x.score = x.zsum - CUM(m, 1);
             x.ranks[0] = (uint8_t)r;
             heap_push(&h, &x);
         }
@@ -269,13 +287,15 @@ int orc_build_tree(const int32_t *top_id, const double *top_logq, int K, int L, 
                 orc_entry s = e;
                 s.rank = e.rank + 1;
                 s.ranks[e.depth - 1] = (uint8_t)(e.rank + 1);
-                s.score = e.pscore + LQ(e.mode, e.depth - 1, e.rank + 1);
+                s.zsum = e.pzsum + ZT(e.mode, e.depth - 1, e.rank + 1);
+                s.score = s.zsum - CUM(e.mode, e.depth);
                 heap_push(&h, &s);
             }
             if (e.depth < L) { /* first child: rank 0 at the next position */
                 orc_entry c = e;
                 c.depth = e.depth + 1; c.rank = 0; c.pnode = node;
-                c.pscore = e.score; c.score = e.score + LQ(e.mode, e.depth, 0);
+                c.pzsum = e.zsum; c.zsum = e.zsum + ZT(e.mode, e.depth, 0);
+                c.score = c.zsum - CUM(e.mode, e.depth + 1);
                 c.ranks[e.depth] = 0;
                 heap_push(&h, &c);
             }
@@ -284,15 +304,18 @@ int orc_build_tree(const int32_t *top_id, const double *top_logq, int K, int L, 
                 for (int r = 0; r < k; ++r) {
                     orc_entry c = e;
                     c.depth = e.depth + 1; c.rank = r; c.pnode = node;
-                    c.pscore = e.score; c.score = e.score + LQ(e.mode, e.depth, r);
+                    c.pzsum = e.zsum; c.zsum = e.zsum + ZT(e.mode, e.depth, r);
+                    c.score = c.zsum - CUM(e.mode, e.depth + 1);
                     c.ranks[e.depth] = (uint8_t)r;
                     heap_push(&h, &c);
                 }
             }
         }
     }
-#undef LQ
+#undef ZT
 #undef TK
+#undef CUM
+    free(cum);
     *n_nodes_out = n;
     free(h.e);
     free(first_child);

@@ -36,25 +36,28 @@ def sequences(parent, token, n):
     return seqs
 
 
-def prefix_score(seq, top_id, top_logq):
-    """Best-mode score of a token sequence in the capped universe (fp64), or
-    None if no mode holds it."""
+def prefix_score(seq, lists):
+    """Best-mode score of a token sequence in the capped universe (fp64),
+    evaluated like the builder (path sum of z/T minus the summed row
+    log-normalisers), or None if no mode holds it."""
+    top_id, top_zt, lse = lists["top_id"], lists["top_zt"], lists["lse"]
     K, L, k = top_id.shape
     best = None
     for m in range(K):
-        s = 0.0
+        z, c = 0.0, 0.0
         for j, x in enumerate(seq):
             hit = np.nonzero(top_id[m, j] == x)[0]
             if hit.size == 0:
-                s = None
+                z = None
                 break
-            s = s + top_logq[m, j, hit[0]]
-        if s is not None and (best is None or s > best):
-            best = s
+            z = z + top_zt[m, j, hit[0]]
+            c = c + lse[m, j]
+        if z is not None and (best is None or z - c > best):
+            best = z - c
     return best
 
 
-def compare_trees(gpu, ref, top_id, top_logq):
+def compare_trees(gpu, ref, lists):
     """Compare a GPU-built tree (numpy arrays for one tree) with the oracle's.
     Returns the number of order flips (each within SCORE_TOL); raises on
     anything else."""
@@ -71,8 +74,8 @@ def compare_trees(gpu, ref, top_id, top_logq):
     for i in range(1, n_g):
         if sg[i] == so[i]:
             continue
-        a = prefix_score(sg[i], top_id, top_logq)
-        b = prefix_score(so[i], top_id, top_logq)
+        a = prefix_score(sg[i], lists)
+        b = prefix_score(so[i], lists)
         assert a is not None, ("gpu node outside the universe", sg[i])
         assert abs(a - b) <= SCORE_TOL * max(1.0, abs(b)), ("order", i, sg[i], so[i], a, b)
         flips += 1

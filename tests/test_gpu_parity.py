@@ -45,8 +45,8 @@ def _tree_np(out, t=0):
 def oracle_build(orc, drafter, k, B, temp=1.0):
     """drafter: [K, L, V] torch (any float dtype) -> oracle tree + lists."""
     z = drafter.float().cpu().numpy().astype(np.float64)
-    _, tid, tlq = orc.drafter_stats(z, temp, k)
-    return orc.build_tree(tid, tlq, B), tid, tlq
+    lists = orc.drafter_lists(z, temp, k)
+    return orc.build_tree(lists, B), lists
 
 
 # ---------------------------------------------------------------------------
@@ -56,10 +56,10 @@ def oracle_build(orc, drafter, k, B, temp=1.0):
 def test_build_tiny(tsd, dev, orc, seed):
     dr = synth.tiny_drafter(synth.seed_for(0, seed))
     out = tsd.tsd_build_tree(dr[None, None].to(dev), topk=4, B=8)
-    ref, tid, tlq = oracle_build(orc, dr[None], 4, 8)
+    ref, lists = oracle_build(orc, dr[None], 4, 8)
     g = _tree_np(out)
     assert int(out["status"][0]) == 0
-    assert compare_trees(g, ref, tid, tlq) == 0
+    assert compare_trees(g, ref, lists) == 0
     n = g["n_nodes"]
     assert np.array_equal(g["rank"][:n], ref["rank"][:n])
     assert np.array_equal(g["mode"][:n], ref["mode"][:n])
@@ -71,8 +71,8 @@ def test_build_tiny(tsd, dev, orc, seed):
 def test_build_single_mode(tsd, dev, orc, V, B, k, temp):
     dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device="cpu")  # [1, 1, 16, V] bf16
     out = tsd.tsd_build_tree(dr.to(dev), topk=k, B=B, drafter_temp=temp)
-    ref, tid, tlq = oracle_build(orc, dr[0], k, B, temp)
-    flips = compare_trees(_tree_np(out), ref, tid, tlq)
+    ref, lists = oracle_build(orc, dr[0], k, B, temp)
+    flips = compare_trees(_tree_np(out), ref, lists)
     assert flips <= 2, flips
 
 
@@ -83,8 +83,8 @@ def test_build_fp32_and_misaligned(tsd, dev, orc):
     buf[1:] = dr.reshape(-1).to(dev)
     view = buf[1:].view(dr.shape)
     out = tsd.tsd_build_tree(view, topk=6, B=50)
-    ref, tid, tlq = oracle_build(orc, dr[0], 6, 50)
-    assert compare_trees(_tree_np(out), ref, tid, tlq) <= 1
+    ref, lists = oracle_build(orc, dr[0], 6, 50)
+    assert compare_trees(_tree_np(out), ref, lists) <= 1
 
 
 def test_build_mixture(tsd, dev, orc):
@@ -93,8 +93,8 @@ def test_build_mixture(tsd, dev, orc):
     out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=128)
     flips = 0
     for t in range(2):
-        ref, tid, tlq = oracle_build(orc, dr[t], 8, 128)
-        flips += compare_trees(_tree_np(out, t), ref, tid, tlq)
+        ref, lists = oracle_build(orc, dr[t], 8, 128)
+        flips += compare_trees(_tree_np(out, t), ref, lists)
     assert flips <= 2
 
 
@@ -104,9 +104,9 @@ def test_build_masked_and_small_universe(tsd, dev, orc):
     z = torch.full((1, 1, 3, 64), -float("inf"))
     z[0, 0, :, :2] = torch.tensor([1.0, 0.5])
     out = tsd.tsd_build_tree(z.to(dev), topk=4, B=50)
-    ref, tid, tlq = oracle_build(orc, z[0], 4, 50)
+    ref, lists = oracle_build(orc, z[0], 4, 50)
     assert ref["n_nodes"] == 1 + 2 + 4 + 8
-    assert compare_trees(_tree_np(out), ref, tid, tlq) == 0
+    assert compare_trees(_tree_np(out), ref, lists) == 0
 
 
 def test_build_nonfinite_status(tsd, dev):
@@ -125,7 +125,7 @@ def test_tree_mask(tsd, dev, orc, B, P):
     dr = synth.zipf_drafter(3, 16, 2048, synth.seed_for(4, B), device="cpu")
     parents, nn = [], []
     for t in range(3):
-        ref, _, _ = oracle_build(orc, dr[t], 8, B)
+        ref, _ = oracle_build(orc, dr[t], 8, B)
         parents.append(ref["parent"])
         nn.append(ref["n_nodes"])
     nn[2] = max(1, nn[2] - 5)  # a ragged tree: trailing slots are padding
@@ -184,7 +184,7 @@ def _check_tev(out, t, o, tgt64, parent, token, n, T):
 def test_tev_tiny(tsd, dev, orc, T, seed):
     s = synth.seed_for(0, seed)
     dr = synth.tiny_drafter(s)
-    ref, _, _ = oracle_build(orc, dr[None], 4, 8)
+    ref, _ = oracle_build(orc, dr[None], 4, 8)
     n = ref["n_nodes"]
     tgt = synth.tiny_target(dr, ref["depth"][:n], s + 7)
     full = torch.zeros(1, 9, 32)
@@ -212,7 +212,7 @@ def test_tev_midsize(tsd, dev, orc, V, dtype, T):
     the generic path)."""
     B = 64
     dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1, 7), device="cpu")
-    ref, _, _ = oracle_build(orc, dr[0], 8, B)
+    ref, _ = oracle_build(orc, dr[0], 8, B)
     tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 8), B, dtype)
     par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
     tok = torch.tensor(ref["token"][None], dtype=torch.int32, device=dev)
@@ -239,7 +239,7 @@ def test_tev_qwen_vocab_b64(tsd, dev, orc, T):
     """The batch-1 Qwen-vocabulary round: V=151936, L=16, k=8, B=64, bf16."""
     B = 64
     dr = synth.zipf_drafter(1, 16, V_Q, synth.seed_for(1), device="cpu")
-    ref, _, _ = oracle_build(orc, dr[0], 8, B)
+    ref, _ = oracle_build(orc, dr[0], 8, B)
     tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 1), B, torch.bfloat16)
     n = ref["n_nodes"]
     par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
@@ -353,7 +353,7 @@ def test_tev_and_predraw_law_on_gpu(tsd, dev, orc):
     import scipy.stats
     s = synth.seed_for(0, 99)
     dr = synth.tiny_drafter(s)
-    ref, _, _ = oracle_build(orc, dr[None], 4, 8)
+    ref, _ = oracle_build(orc, dr[None], 4, 8)
     n = ref["n_nodes"]
     tgt = synth.tiny_target(dr, ref["depth"][:n], s + 7).numpy().astype(np.float64)
     o = orc.tev(tgt, ref["parent"], ref["token"], n, 1.0, seed=0)
@@ -394,18 +394,18 @@ def test_build_edge_budgets(tsd, dev, orc):
     assert _np(out["parent"][0]).tolist() == [-1]
     mix, _, _ = synth.mixture_drafter(1, 8, 6, 1024, synth.seed_for(5, 1), device="cpu")
     out = tsd.tsd_build_tree(mix.to(dev), topk=8, B=512)
-    ref, tid, tlq = oracle_build(orc, mix[0], 8, 512)
-    assert compare_trees(_tree_np(out), ref, tid, tlq) <= 1
+    ref, lists = oracle_build(orc, mix[0], 8, 512)
+    assert compare_trees(_tree_np(out), ref, lists) <= 1
     out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=4095)
-    ref, tid, tlq = oracle_build(orc, dr[0], 8, 4095)
-    flips = compare_trees(_tree_np(out), ref, tid, tlq)  # each within SCORE_TOL
+    ref, lists = oracle_build(orc, dr[0], 8, 4095)
+    flips = compare_trees(_tree_np(out), ref, lists)  # each within SCORE_TOL
     print("B=4095 order flips within tolerance:", flips)
-    assert flips <= 0.01 * 4095
+    assert flips <= 2
     flat = torch.zeros(2, 1, 5, 9000)
     flat[1, 0, 2, 4444] = 1.0
     out = tsd.tsd_build_tree(flat.to(dev), topk=8, B=100)
     for t in range(2):
-        ref, tid, tlq = oracle_build(orc, flat[t], 8, 100)
+        ref, lists = oracle_build(orc, flat[t], 8, 100)
         g = _tree_np(out, t)
-        assert compare_trees(g, ref, tid, tlq) == 0
+        assert compare_trees(g, ref, lists) == 0
         assert np.array_equal(g["rank"][:g["n_nodes"]], ref["rank"][:ref["n_nodes"]])

@@ -74,8 +74,7 @@ def brute_force_continuations(z, parent, token, n, T):
 
 def tiny_tree(orc, seed, B=8, k=4, T_d=1.0):
     dr = synth.tiny_drafter(seed).numpy().astype(np.float64)
-    lse, tid, tlq = orc.drafter_stats(dr, T_d, k)
-    tr = orc.build_tree(tid, tlq, B)
+    tr = orc.build_tree(orc.drafter_lists(dr, T_d, k), B)
     n = tr["n_nodes"]
     tgt = synth.tiny_target(synth.tiny_drafter(seed), tr["depth"][:n], seed + 7).numpy()
     return dr, tr, n, tgt.astype(np.float64)
@@ -147,18 +146,25 @@ def test_drafter_stats_rejects_nonfinite(orc):
 # --------------------------------------------------------------------------
 # Builder [CAST Thm. 1, App. C; MFD Sec. 4.3, App. B Prop. 6]
 # --------------------------------------------------------------------------
-def exhaustive_topB(top_id, top_logq, B):
+def exhaustive_topB(lists, B):
     """Enumerate every prefix of every mode's capped universe, score it, keep
     each distinct token sequence at its best entry in the order (score desc,
-    depth asc, mode asc, rank sequence asc), and return the first B."""
+    depth asc, mode asc, rank sequence asc), and return the first B.  A score
+    is the left-to-right sum of the scaled logits along the prefix minus the
+    sum of the rows' log-normalisers up to its depth (the sum of log q)."""
+    top_id, top_zt, lse = lists["top_id"], lists["top_zt"], lists["lse"]
     K, L, k = top_id.shape
     entries = []
     for m in range(K):
+        cum = [0.0]
+        for j in range(L):
+            cum.append(cum[-1] + lse[m, j])
         for d in range(1, L + 1):
             for ranks in itertools.product(range(k), repeat=d):
-                s = 0.0
+                z = 0.0
                 for j, r in enumerate(ranks):
-                    s = s + top_logq[m, j, r]  # same association as a path sum
+                    z = z + top_zt[m, j, r]
+                s = z - cum[d]
                 if s == -np.inf:
                     continue
                 toks = tuple(int(top_id[m, j, r]) for j, r in enumerate(ranks))
@@ -185,26 +191,34 @@ def tree_sequences(tr):
 
 def _random_lists(rng, K, L, k, V, quantise=False):
     tid = np.zeros((K, L, k), dtype=np.int32)
-    tlq = np.zeros((K, L, k))
+    tzt = np.zeros((K, L, k))
+    lse = np.zeros((K, L))
     for m in range(K):
         for j in range(L):
             z = rng.normal(0, 2, size=V)
             if quantise:
                 z = np.round(z * 2) / 2
-            lq = scipy.special.log_softmax(z)
             order = np.lexsort((np.arange(V), -z))[:k]
-            tid[m, j], tlq[m, j] = order, lq[order]
-    return tid, tlq
+            tid[m, j], tzt[m, j], lse[m, j] = order, z[order], scipy.special.logsumexp(z)
+    return dict(top_id=tid, top_zt=tzt, lse=lse)
+
+
+def _sub(lists, m0, m1):
+    return {key: v[m0:m1] for key, v in lists.items()}
+
+
+def _cat(a, b):
+    return {key: np.concatenate([a[key], b[key]]) for key in a}
 
 
 @pytest.mark.parametrize("seed", range(12))
 def test_builder_single_mode_equals_exhaustive(orc, seed):
     rng = np.random.default_rng(seed)
     L, k, V = 4, 4, 12
-    tid, tlq = _random_lists(rng, 1, L, k, V, quantise=(seed % 2 == 1))
+    ls = _random_lists(rng, 1, L, k, V, quantise=(seed % 2 == 1))
     B = int(rng.integers(1, 60))
-    tr = orc.build_tree(tid, tlq, B)
-    ref = exhaustive_topB(tid, tlq, B)
+    tr = orc.build_tree(ls, B)
+    ref = exhaustive_topB(ls, B)
     seqs = tree_sequences(tr)
     assert tr["n_nodes"] == len(ref) + 1
     assert seqs[1:] == [e[4] for e in ref]
@@ -221,10 +235,10 @@ def test_push_rules_agree(orc, seed):
     [CAST App. C] pop the same prefixes in the same order."""
     rng = np.random.default_rng(100 + seed)
     K = 1 + seed % 3
-    tid, tlq = _random_lists(rng, K, 5, 6, 20, quantise=(seed % 2 == 0))
+    ls = _random_lists(rng, K, 5, 6, 20, quantise=(seed % 2 == 0))
     for B in (1, 7, 40, 90):
-        a = orc.build_tree(tid, tlq, B, push_rule=0)
-        b = orc.build_tree(tid, tlq, B, push_rule=1)
+        a = orc.build_tree(ls, B, push_rule=0)
+        b = orc.build_tree(ls, B, push_rule=1)
         for key in ("parent", "token", "depth", "rank", "mode"):
             np.testing.assert_array_equal(a[key], b[key])
         np.testing.assert_array_equal(a["score"], b["score"])
@@ -240,18 +254,18 @@ def test_mixture_equals_exhaustive_random_instances(orc):
         K = int(rng.integers(1, 9))
         L = int(rng.integers(1, 4))
         V = int(rng.integers(2, 6))
-        tid, tlq = _random_lists(rng, K, L, V, V, quantise=(inst % 3 == 0))
+        ls = _random_lists(rng, K, L, V, V, quantise=(inst % 3 == 0))
         B = int(rng.integers(1, 41))
-        tr = orc.build_tree(tid, tlq, B)
-        ref = exhaustive_topB(tid, tlq, B)
+        tr = orc.build_tree(ls, B)
+        ref = exhaustive_topB(ls, B)
         assert tree_sequences(tr)[1:] == [e[4] for e in ref], inst
         np.testing.assert_array_equal(tr["score"][1:tr["n_nodes"]], [e[5] for e in ref])
     # two instances at the page's full size: 5 positions, 10 tokens each
     for inst in range(2):
         K = 2 + inst
-        tid, tlq = _random_lists(rng, K, 5, 10, 10)
-        tr = orc.build_tree(tid, tlq, 40)
-        ref = exhaustive_topB(tid, tlq, 40)
+        ls = _random_lists(rng, K, 5, 10, 10)
+        tr = orc.build_tree(ls, 40)
+        ref = exhaustive_topB(ls, 40)
         assert tree_sequences(tr)[1:] == [e[4] for e in ref]
 
 
@@ -260,9 +274,9 @@ def test_mixture_single_mode_is_ddtree(orc):
     check the K = 1 call against the mixture call with the one mode duplicated
     under a second copy -- the duplicate reuses every node."""
     rng = np.random.default_rng(7)
-    tid, tlq = _random_lists(rng, 1, 6, 8, 40)
-    single = orc.build_tree(tid, tlq, 64)
-    dup = orc.build_tree(np.concatenate([tid, tid]), np.concatenate([tlq, tlq]), 64)
+    ls = _random_lists(rng, 1, 6, 8, 40)
+    single = orc.build_tree(ls, 64)
+    dup = orc.build_tree(_cat(ls, ls), 64)
     for key in ("parent", "token", "depth", "score"):
         np.testing.assert_array_equal(single[key], dup[key])
     assert np.all(dup["mode"][1:dup["n_nodes"]] == 0)
@@ -274,16 +288,16 @@ def test_mixture_is_union_of_mode_trees(orc):
     rng = np.random.default_rng(11)
     for _ in range(10):
         K = int(rng.integers(2, 6))
-        tid, tlq = _random_lists(rng, K, 3, 5, 5)
+        ls = _random_lists(rng, K, 3, 5, 5)
         B = int(rng.integers(5, 40))
-        tr = orc.build_tree(tid, tlq, B)
+        tr = orc.build_tree(ls, B)
         n = tr["n_nodes"]
         theta = tr["score"][n - 1]
         union = set()
         for m in range(K):
-            one = exhaustive_topB(tid[m:m + 1], tlq[m:m + 1], 10**9)
+            one = exhaustive_topB(_sub(ls, m, m + 1), 10**9)
             nk = sum(1 for e in one if e[5] >= theta)
-            sub = orc.build_tree(tid[m:m + 1], tlq[m:m + 1], nk)
+            sub = orc.build_tree(_sub(ls, m, m + 1), nk)
             union |= set(tree_sequences(sub)[1:])
         assert union == set(tree_sequences(tr)[1:])
 
@@ -294,8 +308,8 @@ def test_product_tree_holds_chimeras(orc):
     their splices."""
     rng = np.random.default_rng(3)
     for _ in range(6):
-        tid, tlq = _random_lists(rng, 1, 4, 4, 4)
-        tr = orc.build_tree(tid, tlq, 60)
+        ls = _random_lists(rng, 1, 4, 4, 4)
+        tr = orc.build_tree(ls, 60)
         seqs = set(tree_sequences(tr)[1:])
         by_depth = {}
         for s in seqs:
@@ -324,7 +338,7 @@ def _separation_lists(futures, modes_on, k, D):
             others = [t for t in range(k + len(futures)) if t != futures[f][i]][:k - 1]
             tid[m, i] = [futures[f][i]] + others
             tlq[m, i, 0] = 0.0
-    return tid, tlq
+    return {"top_id": tid, "top_zt": tlq, "lse": np.zeros((K, D))}
 
 
 def _acceptance(tr, futures, mu):
@@ -343,7 +357,7 @@ def test_separation_model_closed_forms(orc):
     c = cases[0]
     M, D, B = c["M"], c["D"], c["B"]
     futures = [[2 * i for i in range(D)], [2 * i + 1 for i in range(D)]]
-    mix = orc.build_tree(*_separation_lists(futures, [0, 1], 2, D), B)
+    mix = orc.build_tree(_separation_lists(futures, [0, 1], 2, D), B)
     assert _acceptance(mix, futures, [0.5, 0.5]) == pytest.approx(c["optimal"])
     rng = np.random.default_rng(1)
     for _ in range(20):  # random products over the two futures' tokens, no ties
@@ -354,14 +368,14 @@ def test_separation_model_closed_forms(orc):
             pair = sorted([(a, futures[0][i]), (1 - a, futures[1][i])], reverse=True)
             tid[0, i] = [pair[0][1], pair[1][1]]
             tlq[0, i] = [math.log(pair[0][0]), math.log(pair[1][0])]
-        prod = orc.build_tree(tid, tlq, B)
+        prod = orc.build_tree(orc.lists_from_logq(tid, tlq), B)
         assert _acceptance(prod, futures, [0.5, 0.5]) <= c["product_bound"] + 1e-12
         assert D / M + (1 - 1 / M) * (1 + math.log2(B)) == pytest.approx(c["product_bound"])
     # case 2: unequal futures
     c = cases[1]
     D, B, mu = c["D"], c["B"], c["mu"]
     futures = [[2 * i for i in range(D)], [2 * i + 1 for i in range(D)]]
-    mix = orc.build_tree(*_separation_lists(futures, [0, 1], 2, D), B)
+    mix = orc.build_tree(_separation_lists(futures, [0, 1], 2, D), B)
     assert _acceptance(mix, futures, mu) == pytest.approx(c["uniform_prior_mixture"])
     eps = 1e-3
     tid = np.zeros((1, D, 2), dtype=np.int32)
@@ -369,14 +383,14 @@ def test_separation_model_closed_forms(orc):
     for i in range(D):
         tid[0, i] = [futures[0][i], futures[1][i]]
         tlq[0, i] = [math.log(1 - eps), math.log(eps)]
-    prod = orc.build_tree(tid, tlq, B)
+    prod = orc.build_tree(orc.lists_from_logq(tid, tlq), B)
     assert _acceptance(prod, futures, mu) == pytest.approx(c["product_on_first"])
     # case 3: point-mass mixture accepts min(B, K D)/M
     c = cases[2]
     M, K, D = c["M"], c["K"], c["D"]
     futures = [[M * i + f for i in range(D)] for f in range(M)]
     for B in c["B_list"]:
-        mix = orc.build_tree(*_separation_lists(futures, list(range(K)), 2, D), B)
+        mix = orc.build_tree(_separation_lists(futures, list(range(K)), 2, D), B)
         assert _acceptance(mix, futures, [1 / M] * M) == pytest.approx(min(B, K * D) / M)
         assert mix["n_nodes"] == min(B, K * D) + 1  # zero-mass prefixes are never kept
 
@@ -387,9 +401,9 @@ def test_separation_model_closed_forms(orc):
 @pytest.mark.parametrize("seed", range(4))
 def test_tree_mask_vs_ancestor_sets(orc, seed):
     rng = np.random.default_rng(seed)
-    tid, tlq = _random_lists(rng, 1, 6, 4, 10)
+    ls = _random_lists(rng, 1, 6, 4, 10)
     B = 40
-    tr = orc.build_tree(tid, tlq, B)
+    tr = orc.build_tree(ls, B)
     n = tr["n_nodes"]
     P = int(rng.integers(0, 50))
     bits, pos, add = orc.tree_mask(tr["parent"], n, B, P, with_additive=True)

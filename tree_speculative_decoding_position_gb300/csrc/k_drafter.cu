@@ -6,7 +6,9 @@
 // each future position; scores use the original q_j, not a top-K
 // renormalisation).  For every row j of drafter logits this computes
 //   LSE_j = log sum_a exp(z_j(a) / T_d)      (over the full vocabulary)
-//   the top-k tokens by (logit desc, id asc) and log q_j = z / T_d - LSE_j.
+//   the top-k tokens by (logit desc, id asc) with their z / T_d; the builder
+//   scores a prefix as (sum of its z / T_d) - (sum of the rows' LSE), which
+//   is its sum of log q_j = z / T_d - LSE_j.
 //
 // drafter_chunk_kernel  one warp per (row, 8 KB chunk): chunk max, sum of
 //                       exp2(z*c - mc), and the chunk's top-k.
@@ -350,8 +352,9 @@ drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs w
         }
         if (lane < k) {
             ws.top_id[row * k + lane] = ei;
-            ws.top_lq[row * k + lane] = (double)ev / temp - lse;
+            ws.top_zt[row * k + lane] = (double)ev / temp;
         }
+        if (lane == 0) ws.lse[row] = lse;
         __syncwarp();
     }
 }

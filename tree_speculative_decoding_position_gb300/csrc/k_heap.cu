@@ -27,12 +27,17 @@
 // total order (score desc, depth asc, mode asc, rank sequence asc), listed in
 // that order (= pop order).
 //
+// Scores: a prefix's sum of log q_j is evaluated as (the left-to-right sum of
+// its tokens' z / T_d) - C_m(depth), with C_m(d) the sum of mode m's first d
+// row log-normalisers.  Two prefixes of one depth and mode whose scaled logits
+// sum to the same value therefore tie exactly (as they do in exact
+// arithmetic), and the tie order decides them.
+//
 // Entries are 32 bytes: a 64-bit order-preserving image of the float64 score,
 // the 64-bit tie key depth << 59 | mode << 56 | rank digits (which also names
-// the prefix within its mode), the entry's score in float64 (kept for the
-// record), and a 64-bit hash of the parent's token sequence (to tell equal
-// prefixes of different modes apart; every hash match is confirmed by
-// comparing the token sequences).
+// the prefix within its mode), the prefix's z / T_d sum, and a 64-bit hash of
+// the parent's token sequence (to tell equal prefixes of different modes
+// apart; every hash match is confirmed by comparing the token sequences).
 #include "tsd_internal.cuh"
 
 namespace tsd {
@@ -42,7 +47,7 @@ constexpr int kBuildThreads = 256;
 struct __align__(16) FEntry {
     unsigned long long key;   // order-preserving image of the score
     unsigned long long tb;    // depth << 59 | mode << 56 | rank digits
-    double pscore;            // same mode's score of the parent prefix
+    double zsum;              // sum of z / T_d along the prefix (left to right)
     unsigned long long hpar;  // hash of the parent's token sequence
 };
 static_assert(sizeof(FEntry) == 32, "entry layout");
@@ -100,7 +105,8 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk + 32;
     p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
     auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
-    p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)));
+    p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)) +
+                  sizeof(double) * (size_t)n_modes * (L + 1));
     p.sbytes = r16(sizeof(FEntry) * (size_t)pow2_at_least(topk * p.M < 32 ? 32 : topk * p.M));
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
@@ -126,7 +132,7 @@ __device__ __forceinline__ FEntry shfl_xor_entry(const FEntry& x, int j) {
     FEntry y;
     y.key = __shfl_xor_sync(0xffffffffu, x.key, j);
     y.tb = __shfl_xor_sync(0xffffffffu, x.tb, j);
-    y.pscore = __shfl_xor_sync(0xffffffffu, x.pscore, j);
+    y.zsum = __shfl_xor_sync(0xffffffffu, x.zsum, j);
     y.hpar = __shfl_xor_sync(0xffffffffu, x.hpar, j);
     return y;
 }
@@ -229,11 +235,13 @@ __device__ int block_incl_scan_int(int x, int* red, int* total) {
 }
 
 struct Lists {
-    const double* lq;
+    const double* zt;   // [K][L][k] z / T_d of the kept tokens
+    const double* cum;  // [K][L+1] cumulative row log-normalisers
     const int32_t* ids;
     int L, k, bits;
     __device__ int token(int m, int d, int r) const { return ids[(m * L + d - 1) * k + r]; }
-    __device__ double logq(int m, int d, int r) const { return lq[(m * L + d - 1) * k + r]; }
+    __device__ double zlog(int m, int d, int r) const { return zt[(m * L + d - 1) * k + r]; }
+    __device__ double c(int m, int d) const { return cum[m * (L + 1) + d]; }
     // token at depth j+1 (j < d) of the prefix named by tie key tb
     __device__ int token_at(unsigned long long tb, int j) const {
         const int d = tb_depth(tb), m = tb_mode(tb);
@@ -282,8 +290,9 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     const int t = blockIdx.x, tid = threadIdx.x;
     const int nl = K * L * k;
     uint8_t* p = smem;
-    double* lq = reinterpret_cast<double*>(p);
-    int32_t* ids = reinterpret_cast<int32_t*>(p + sizeof(double) * nl);
+    double* zt = reinterpret_cast<double*>(p);
+    double* cum = zt + nl;
+    int32_t* ids = reinterpret_cast<int32_t*>(cum + K * (L + 1));
     p += plan.lists;
     FEntry* S = reinterpret_cast<FEntry*>(p);
     p += plan.sbytes;
@@ -296,7 +305,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     int* hval = reinterpret_cast<int*>(big + sizeof(unsigned long long) * plan.hcap);
     big += plan.hbytes;
     int* flag = reinterpret_cast<int*>(big);  // [xcap] first-occurrence marks, then ranks
-    const Lists ls{lq, ids, L, k, bits};
+    const Lists ls{zt, cum, ids, L, k, bits};
     const int stride = B + 1;
 
     if (tid == 0) {
@@ -307,10 +316,20 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     }
     __syncthreads();
     for (int i = tid; i < nl; i += blockDim.x) {
-        const double x = ws.top_lq[(int64_t)t * nl + i];
-        lq[i] = x;
+        const double x = ws.top_zt[(int64_t)t * nl + i];
+        zt[i] = x;
         ids[i] = ws.top_id[(int64_t)t * nl + i];
         if (x != x) s_bad = 1;
+    }
+    for (int m = tid; m < K; m += blockDim.x) {  // C_m(d), summed left to right
+        double c = 0.0;
+        cum[m * (L + 1)] = 0.0;
+        for (int d = 1; d <= L; ++d) {
+            const double l = ws.lse[((int64_t)t * K + m) * L + d - 1];
+            if (l != l) s_bad = 1;
+            c = c + l;
+            cum[m * (L + 1) + d] = c;
+        }
     }
     __syncthreads();
     const bool bad = s_bad != 0;
@@ -322,15 +341,16 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             FEntry e;
             e.key = kSentinelKey;
             e.tb = ~0ull;
-            e.pscore = 0.0;
+            e.zsum = 0.0;
             e.hpar = kRootHash;
             if (i < K * k) {
                 const int m = i / k, r = i % k;
-                const double sv = 0.0 + ls.logq(m, 1, r);
+                const double z = 0.0 + ls.zlog(m, 1, r);
+                const double sv = z - ls.c(m, 1);
                 if (sv != -INFINITY) {
                     e.key = order_key(sv);
                     e.tb = (1ull << 59) | ((unsigned long long)m << 56) | (unsigned long long)r;
-                    e.pscore = sv;
+                    e.zsum = z;
                 }
             }
             F[0][i] = e;
@@ -366,11 +386,12 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                     const FEntry e = F[fc][i];
                     const int d = tb_depth(e.tb), m = tb_mode(e.tb);
                     if (d < L) {
-                        const double sv = key_score(e.key) + ls.logq(m, d + 1, r);
+                        const double z = e.zsum + ls.zlog(m, d + 1, r);
+                        const double sv = z - ls.c(m, d + 1);
                         ch.key = order_key(sv);
                         ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
                                 (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
-                        ch.pscore = sv;
+                        ch.zsum = z;
                         ok = sv != -INFINITY && (!thr_on || before(ch, thr));
                         if (ok) ch.hpar = entry_hash(ls, e);
                     }

@@ -72,7 +72,8 @@ size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int
     ws.cand_v = cv.take<float>(rows * nch * topk);
     ws.cand_i = cv.take<int32_t>(rows * nch * topk);
     ws.top_id = cv.take<int32_t>(rows * topk);
-    ws.top_lq = cv.take<double>(rows * topk);
+    ws.top_zt = cv.take<double>(rows * topk);
+    ws.lse = cv.take<double>(rows);
     ws.heap_stride = (heap_spill_bytes(n_modes, L, topk, B) + kAlign - 1) & ~(kAlign - 1);
     ws.heap = cv.take<uint8_t>((size_t)n_trees * ws.heap_stride);
     if (out) *out = ws;

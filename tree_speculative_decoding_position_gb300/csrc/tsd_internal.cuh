@@ -164,7 +164,8 @@ struct BuildWs {
     float* cand_v;       // [rows][n_chunks][topk] chunk top-k logits
     int32_t* cand_i;     // [rows][n_chunks][topk] and ids
     int32_t* top_id;     // [rows][topk]
-    double* top_lq;      // [rows][topk]
+    double* top_zt;      // [rows][topk] the kept tokens' z / T_d
+    double* lse;         // [rows] log sum exp(z / T_d) over the row
     uint8_t* heap;       // [n_trees][heap bytes] spill space when shared memory is short
     size_t heap_stride;  // bytes per tree
 };
