@@ -335,7 +335,108 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
     out["b64_single_tree"] = {"tev_rounds_per_s": 1000.0 / ms, "tev_ms": ms,
                               "rows_kernel_ms": rows_ms,
                               "rows_kernel_gbs": n * V * 2 / (rows_ms * 1e-3) / 1e9}
+    # the same round, greedy (T = 0)
+    s.record(stream)
+    for i in range(48):
+        tsd.tsd_verify_tev(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 0.0,
+                           seed=i, workspace=ws1)
+    e.record(stream)
+    torch.cuda.synchronize()
+    out["b64_single_tree"]["tev_ms_T0"] = s.elapsed_time(e) / 48
+    del copies
+    # mixture-of-futures workload: 16 trees, K = 8 modes from two latent
+    # futures, B = 128; the mixture builder, then TEV at T = 1 on its trees
+    nt_m, K_m, B_m = 16, 8, 128
+    mix, _, choice = synth.mixture_drafter(nt_m, K_m, 16, V, synth.seed_for(3), device=dev)
+    for i in range(3):
+        tm = tsd.tsd_build_tree(mix, topk=8, B=B_m)
+    s.record(stream)
+    for i in range(10):
+        tm = tsd.tsd_build_tree(mix, topk=8, B=B_m)
+    e.record(stream)
+    torch.cuda.synchronize()
+    build_ms = s.elapsed_time(e) / 10
+    tgt_m = torch.zeros(nt_m, B_m + 1, V, dtype=torch.bfloat16, device=dev)
+    for t in range(nt_m):
+        n_t = int(tm["n_nodes"][t])
+        # the target follows the future the tree's seed chose, at its node depths
+        fut = synth.mixture_drafter(1, 2, 16, V, synth.seed_for(3) + t, device=dev)[1][0, choice[t]]
+        synth.target_from_rows(fut, tm["depth"][t, :n_t], 1.5, synth.seed_for(3, 500 + t),
+                               out=tgt_m[t, :n_t])
+    for i in range(3):
+        tsd.tsd_verify_tev(tgt_m, tm["parent"], tm["token"], tm["n_nodes"], 1.0, seed=i)
+    s.record(stream)
+    for i in range(10):
+        ov = tsd.tsd_verify_tev(tgt_m, tm["parent"], tm["token"], tm["n_nodes"], 1.0, seed=i)
+    e.record(stream)
+    torch.cuda.synchronize()
+    tev_ms = s.elapsed_time(e) / 10
+    out["mixture_k8_b128_x16"] = {
+        "build_ms": build_ms, "tev_ms": tev_ms,
+        "rounds_per_s": nt_m / ((build_ms + tev_ms) * 1e-3),
+        "mean_accept_len": float(ov["accept_len"].float().mean()),
+        "mean_coverage_plus_1": float(ov["coverage"].mean()) + 1.0,
+        "status_ok": int((ov["status"] == 0).sum())}
     return out
+
+
+def run_sweep(args):
+    """TEV throughput over B x trees x T (V = 151936, bf16): one JSON table
+    written to --sweep-out.  Trees come from the GPU builder on zipf drafter
+    logits; target rows are the drafter row at node depth + N(0, 1.5^2)."""
+    import torch
+
+    import synth
+    import tree_speculative_decoding_position_gb300 as tsd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    V, L = 151936, 16
+    rows = []
+    for B in (16, 64, 256, 512):
+        for nt in (1, 8, 64, 256):
+            need = nt * (B + 1) * V * 2
+            free = torch.cuda.mem_get_info(dev)[0]
+            if need * 1.2 > free:
+                rows.append(dict(B=B, trees=nt, skipped="needs %.1f GB, %.1f GB free" % (need / 1e9, free / 1e9)))
+                continue
+            seeds = [synth.seed_for(4, 1000 * B + t) for t in range(nt)]
+            dr = synth.zipf_drafter(nt, L, V, 0, device=dev, seeds=seeds)
+            tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+            x = torch.zeros(nt, B + 1, V, dtype=torch.bfloat16, device=dev)
+            for t in range(nt):
+                n = int(tr["n_nodes"][t])
+                synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=x[t, :n])
+            del dr
+            ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, nt, 1, 1, V, 1, B,
+                                                    torch.bfloat16), dtype=torch.uint8, device=dev)
+            nbytes = int(tr["n_nodes"].sum()) * V * 2
+            reps = max(3, min(50, int(4e9 // max(nbytes, 1))))
+            for T in (0.0, 0.6, 1.0):
+                for i in range(3):
+                    tsd.tsd_verify_tev(x, tr["parent"], tr["token"], tr["n_nodes"], T, seed=i,
+                                       workspace=ws, with_masses=False)
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps)]
+                for ev in evs:
+                    for e_ in ev:
+                        e_.record(stream)
+                torch.cuda.synchronize()
+                for i in range(reps):
+                    tsd.tsd_verify_tev_timed(x, tr["parent"], tr["token"], tr["n_nodes"], T,
+                                             seed=i, stage_events=evs[i], workspace=ws,
+                                             with_masses=False)
+                torch.cuda.synchronize()
+                tot = statistics.mean(ev[0].elapsed_time(ev[4]) for ev in evs)
+                rk = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
+                rows.append(dict(B=B, trees=nt, T=T, tev_ms=tot, rounds_per_s=nt / (tot * 1e-3),
+                                 rows_kernel_gbs=nbytes / (rk * 1e-3) / 1e9,
+                                 rows_frac_of_measured=nbytes / (rk * 1e-3) / 1e9 / measured_peaks()[0],
+                                 logits_gb=nbytes / 1e9, reps=reps))
+            del x, ws, tr
+            torch.cuda.empty_cache()
+    with open(args.sweep_out, "w") as f:
+        json.dump(rows, f, indent=1)
+    print(json.dumps({"sweep_points": len(rows), "out": args.sweep_out}))
 
 
 def cpu_baseline(drafter, target, tree, k, B, T, budget_s=12.0):
@@ -430,10 +531,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trees", type=int, default=0,
                     help="trees per GPU (default: the workload's 32); for profiler captures")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time TEV over B x trees x T instead (writes --sweep-out)")
+    ap.add_argument("--sweep-out", default="gpurun_out/sweep.json")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
