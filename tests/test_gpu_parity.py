@@ -327,6 +327,99 @@ def test_tev_edge_cases(tsd, dev, orc):
             == (0, o["bonus"], 1)
 
 
+def _greedy_tie_case(V, B, rng):
+    """A random tree and integer-valued target logits whose row maxima tie
+    exactly at several tokens spread over lanes, vectors and chunks.  At
+    about 70% of the nodes with children, a drafted child is the smallest id
+    among the tied maxima (accepted at T = 0); elsewhere a smaller id ties
+    with it (rejected).  Two rows have maxima of 0 tied between -0.0 and
+    +0.0; one row has its only maximum at the last token."""
+    parent = np.full(B + 1, -1, dtype=np.int32)
+    token = np.full(B + 1, -1, dtype=np.int32)
+    for u in range(1, B + 1):
+        parent[u] = rng.integers(max(0, u - 5), u) if u > 3 else u - 1
+        used = {int(token[s]) for s in range(1, u) if parent[s] == parent[u]}
+        while True:
+            x = int(rng.integers(0, V))
+            if x not in used:
+                break
+        token[u] = x
+    z = rng.integers(-8, 1, size=(B + 1, V)).astype(np.float32)
+    for v in range(B + 1):
+        kids = [int(token[u]) for u in range(1, B + 1) if parent[u] == v]
+        ties = set(int(x) for x in rng.integers(0, V, size=int(rng.integers(1, 5))))
+        if kids:
+            c = kids[int(rng.integers(0, len(kids)))]
+            if rng.random() < 0.7:  # the child is the first of the tied maxima
+                ties = {x for x in ties if x > c} | {c}
+            else:  # a smaller id ties with it
+                ties |= {c, int(rng.integers(0, c))} if c > 0 else {c}
+        z[v, sorted(ties)] = 3.0
+    # rows 1 and 2: maxima of 0, signed zeros tied
+    for v, first_neg in ((1, True), (2, False)):
+        z[v] = np.minimum(z[v], -1.0)
+        pos = np.sort(rng.choice(V, size=6, replace=False))
+        z[v, pos] = 0.0
+        z[v, pos[0::2] if first_neg else pos[1::2]] = -0.0
+    # row 3: one maximum, at the last token
+    z[3] = np.minimum(z[3], 2.0)
+    z[3, V - 1] = 5.0
+    return parent, token, z
+
+
+@pytest.mark.parametrize("V,dtype", [(3 * 4096 + 512, torch.bfloat16), (2 * 2048 + 256, torch.float32),
+                                     (3001, torch.bfloat16)])
+def test_tev_greedy_exact_ties(tsd, dev, orc, V, dtype):
+    """T = 0 with exact ties at the row maxima: the arg-max must be the
+    smallest tied id on both sides, so exit node, bonus token, accepted
+    length and the predraw-and-follow draws are bit-exact."""
+    B, nt = 24, 6
+    rng = np.random.default_rng(synth.seed_for(1, 40))
+    cases = [_greedy_tie_case(V, B, rng) for _ in range(nt)]
+    par = torch.tensor(np.stack([c[0] for c in cases]), device=dev)
+    tok = torch.tensor(np.stack([c[1] for c in cases]), device=dev)
+    zt = torch.tensor(np.stack([c[2] for c in cases])).to(dtype)
+    nn = torch.full((nt,), B + 1, dtype=torch.int32, device=dev)
+    out = tsd.tsd_verify_tev(zt.to(dev), par, tok, nn, 0.0, seed=3)
+    d = tsd.tsd_verify_ddtree(zt.to(dev), par, tok, nn, 0.0, seed=3)
+    accepted = 0
+    for t, (parent, token, _) in enumerate(cases):
+        z64 = zt[t].float().numpy().astype(np.float64)
+        o = orc.tev(z64, parent, token, B + 1, 0.0, seed=3, tree=t)
+        assert _check_tev(out, t, o, z64, parent, token, B + 1, 0.0) == 0
+        assert int(out["exit_node"][t]) == o["exit_node"] and int(out["bonus_token"][t]) == o["bonus"]
+        od = orc.predraw(z64, parent, token, B + 1, 0.0, seed=3, tree=t)
+        assert _np(d["draws"][t]).tolist() == od["draws"].tolist()
+        assert (int(d["exit_node"][t]), int(d["bonus_token"][t])) == (od["exit_node"], od["bonus"])
+        accepted += o["accept_len"] - 1
+    assert accepted > 0  # some drafted children were accepted
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_tev_greedy_nonfinite_rows(tsd, dev, orc, dtype):
+    """At T = 0 as at T > 0, a node row holding +inf or NaN, or with every
+    token at -inf, is an error for its tree (status 5); other trees are
+    unaffected."""
+    V, B = 4096 + 1024, 3
+    g = torch.Generator().manual_seed(11)
+    z = torch.randn(4, B + 1, V, generator=g)
+    parent = np.array([[-1, 0, 0, 1]] * 4, dtype=np.int32)
+    token = np.array([[-1, 5, 9, 7]] * 4, dtype=np.int32)
+    z[0, 2, 4500] = float("inf")
+    z[1, 3, :] = -float("inf")
+    z[2, 1, 77] = float("nan")
+    zt = z.to(dtype)
+    nn = torch.full((4,), B + 1, dtype=torch.int32, device=dev)
+    for T in (0.0, 1.0):
+        out = tsd.tsd_verify_tev(zt.to(dev), torch.tensor(parent, device=dev),
+                                 torch.tensor(token, device=dev), nn, T, seed=1)
+        st = _np(out["status"]).tolist()
+        assert st == [5, 5, 5, 0], (T, st)
+        for t in range(3):  # the oracle rejects the same rows
+            with pytest.raises(orc.OracleError):
+                orc.tev(zt[t].float().numpy().astype(np.float64), parent[t], token[t], B + 1, T, seed=1)
+
+
 def test_tev_outputs_fully_written(tsd, dev, orc):
     """Every output slot is written (sentinel fill through a caller workspace
     filled with NaN bytes)."""

@@ -170,14 +170,42 @@ struct Lanes<__nv_bfloat16> {
     static __device__ __forceinline__ uint4 neg_inf() {
         return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
     }
-    static __device__ __forceinline__ float vmax(const uint4& q) {
-        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
-        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.y));
-        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.z));
-        a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&q.w));
-        return fmaxf(__low2float(a), __high2float(a));
+    // Elements 2p and 2p+1 of a vector, widened to fp32.
+    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
+        const uint32_t w = p == 0 ? q.x : p == 1 ? q.y : p == 2 ? q.z : q.w;
+        return make_float2(bf16_lo(w), bf16_hi(w));
+    }
+    // Maximum over a lane's whole chunk slice: packed bf16 maxima in four
+    // independent chains, widened once at the end.
+    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
+        __nv_bfloat162 a0 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].x);
+        __nv_bfloat162 a1 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].y);
+        __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].z);
+        __nv_bfloat162 a3 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].w);
+#pragma unroll
+        for (int i = 1; i < kVecPerLane; ++i) {
+            a0 = __hmax2(a0, *reinterpret_cast<const __nv_bfloat162*>(&b[i].x));
+            a1 = __hmax2(a1, *reinterpret_cast<const __nv_bfloat162*>(&b[i].y));
+            a2 = __hmax2(a2, *reinterpret_cast<const __nv_bfloat162*>(&b[i].z));
+            a3 = __hmax2(a3, *reinterpret_cast<const __nv_bfloat162*>(&b[i].w));
+        }
+        a0 = __hmax2(__hmax2(a0, a1), __hmax2(a2, a3));
+        return fmaxf(__low2float(a0), __high2float(a0));
+    }
+    // Maximum that is NaN when any element is NaN.
+    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
+        __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&q.x),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&q.y));
+        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.z));
+        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.w));
+        return __bfloat162float(__hmax_nan(__low2bfloat16(a), __high2bfloat16(a)));
     }
 };
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 template <>
 struct Lanes<float> {
     static constexpr int kVec = 4;
@@ -187,9 +215,24 @@ struct Lanes<float> {
     static __device__ __forceinline__ uint4 neg_inf() {
         return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
     }
-    static __device__ __forceinline__ float vmax(const uint4& q) {
-        return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
-                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
+        return p == 0 ? make_float2(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
+    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+            a0 = fmaxf(a0, __uint_as_float(b[i].x));
+            a1 = fmaxf(a1, __uint_as_float(b[i].y));
+            a2 = fmaxf(a2, __uint_as_float(b[i].z));
+            a3 = fmaxf(a3, __uint_as_float(b[i].w));
+        }
+        return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+    }
+    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
+        return fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                        fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
     }
 };
 
@@ -203,51 +246,56 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int lo, int hi,
     return lo;
 }
 
-// Vectorised path: the row chunk is 16-byte aligned and its length a multiple
-// of the vector width.  Lane l holds vectors l, l+32, ... of the chunk.
+// Statistics of one row chunk held in registers: lane l holds vectors l,
+// l+32, ... of the chunk (16 bytes each); vectors at or past cn elements hold
+// -inf.  The chunk length cn is a multiple of the vector width.
 template <typename T, bool GREEDY>
-__device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, int cn, float c,
-                                                      const int32_t* __restrict__ ctok, int clo,
-                                                      int chi, int64_t c0, int lane) {
+__device__ __forceinline__ ChunkStat chunk_stat(const uint4 (&buf)[kVecPerLane], int cn, float c,
+                                                const int32_t* __restrict__ ctok, int clo, int chi,
+                                                int64_t c0, int lane) {
     constexpr int VEC = Lanes<T>::kVec;
-    uint4 buf[kVecPerLane];
-#pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-        const int e = (i * kWarp + lane) * VEC;
-        buf[i] = (e < cn) ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
-    }
     ChunkStat st;
     if (GREEDY) {
-        float bm = -INFINITY;
-        int bi = INT_MAX;
+        // Argmax with the smallest id among equal maxima: the warp-wide
+        // maximum first (packed per-vector maxima), then the first element
+        // equal to it in index order.  Vector i*32 + lane sits in lane
+        // `lane`, so a lane's first hit is at its smallest i.  A NaN or +inf
+        // anywhere marks the chunk (its sum is set to NaN).
+        float vm[kVecPerLane];
+        float lm = -INFINITY;
         bool bad = false;
 #pragma unroll
         for (int i = 0; i < kVecPerLane; ++i) {
-            const int e = (i * kWarp + lane) * VEC;
-            if (e < cn) {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const float x = Lanes<T>::get(buf[i], j);
-                    bad |= is_bad_logit(x);
-                    if (better(x, (int)c0 + e + j, bm, bi)) {
-                        bm = x;
-                        bi = (int)c0 + e + j;
-                    }
-                }
-            }
+            vm[i] = Lanes<T>::vmax_nan(buf[i]);
+            bad |= is_bad_logit(vm[i]);
+            lm = fmaxf(lm, vm[i]);
         }
-        warp_argmax(bm, bi);
+        const float m = warp_max(lm);
+        int hit = -1;
+        uint4 hv = buf[0];
+#pragma unroll
+        for (int i = kVecPerLane - 1; i >= 0; --i)
+            if (vm[i] == m && (i * kWarp + lane) * VEC < cn) {
+                hit = i;
+                hv = buf[i];
+            }
+        int bi = INT_MAX;
+        if (hit >= 0) {
+            int j0 = VEC - 1;
+#pragma unroll
+            for (int j = VEC - 1; j >= 0; --j)
+                if (Lanes<T>::get(hv, j) == m) j0 = j;
+            bi = (int)c0 + (hit * kWarp + lane) * VEC + j0;
+        }
+        bi = __reduce_min_sync(0xffffffffu, bi);
         bad = __any_sync(0xffffffffu, bad);
-        st.m = bm;
+        st.m = m;
         st.s = bad ? __int_as_float(0x7fc00000) : 0.0f;
         st.r = 0.0f;
         st.amax = bi;
         return st;
     }
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) m = fmaxf(m, Lanes<T>::vmax(buf[i]));
-    m = warp_max(m);
+    const float m = warp_max(Lanes<T>::block_max(buf));
     st.m = m;
     st.amax = -1;
     if (m == -INFINITY) {  // every token of the chunk is masked
@@ -256,17 +304,27 @@ __device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, 
         return st;
     }
     const float mc = __fmul_rn(m, c);
-    float acc[VEC];
+    // Packed fp32x2 fma/add (each lane rounds like fmaf / +); accumulator
+    // pair p holds element slots 2p and 2p+1 of every vector.
+    constexpr int NP = VEC / 2;
+    const float2 cc = make_float2(c, c), nmc = make_float2(-mc, -mc);
+    float2 acc[NP];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+    for (int p = 0; p < NP; ++p) acc[p] = make_float2(0.0f, 0.0f);
     if (chi == clo) {  // no drafted child in this chunk: the residual is the full sum
 #pragma unroll
         for (int i = 0; i < kVecPerLane; ++i)
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) acc[j] += ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mc));
+            for (int p = 0; p < NP; ++p) {
+                const float2 y = __ffma2_rn(Lanes<T>::pair(buf[i], p), cc, nmc);
+                acc[p] = __fadd2_rn(acc[p], make_float2(ex2(y.x), ex2(y.y)));
+            }
         float s = 0.0f;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) s += acc[j];
+        for (int p = 0; p < NP; ++p) {
+            s += acc[p].x;
+            s += acc[p].y;
+        }
         s = warp_sum(s);
         st.s = s;
         st.r = s;
@@ -287,27 +345,48 @@ __device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, 
                 if (w == (bit >> 5)) excl[w] |= sel;
         }
     }
-    float racc[VEC];
+    float2 racc[NP];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) racc[j] = 0.0f;
+    for (int p = 0; p < NP; ++p) racc[p] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i)
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            const float e = ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mc));
-            const int bit = i * VEC + j;
-            acc[j] += e;
-            racc[j] += ((excl[bit >> 5] >> (bit & 31)) & 1u) ? 0.0f : e;
+        for (int p = 0; p < NP; ++p) {
+            const float2 y = __ffma2_rn(Lanes<T>::pair(buf[i], p), cc, nmc);
+            const float2 e = make_float2(ex2(y.x), ex2(y.y));
+            const int b0 = i * VEC + 2 * p, b1 = b0 + 1;
+            acc[p] = __fadd2_rn(acc[p], e);
+            racc[p] = __fadd2_rn(racc[p],
+                                 make_float2(((excl[b0 >> 5] >> (b0 & 31)) & 1u) ? 0.0f : e.x,
+                                             ((excl[b1 >> 5] >> (b1 & 31)) & 1u) ? 0.0f : e.y));
         }
     float s = 0.0f, r = 0.0f;
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-        s += acc[j];
-        r += racc[j];
+    for (int p = 0; p < NP; ++p) {
+        s += acc[p].x;
+        s += acc[p].y;
+        r += racc[p].x;
+        r += racc[p].y;
     }
     st.s = warp_sum(s);
     st.r = warp_sum(r);
     return st;
+}
+
+// Vectorised path: the row chunk is 16-byte aligned and its length a multiple
+// of the vector width; streaming 16-byte loads straight into registers.
+template <typename T, bool GREEDY>
+__device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, int cn, float c,
+                                                      const int32_t* __restrict__ ctok, int clo,
+                                                      int chi, int64_t c0, int lane) {
+    constexpr int VEC = Lanes<T>::kVec;
+    uint4 buf[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const int e = (i * kWarp + lane) * VEC;
+        buf[i] = (e < cn) ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
+    }
+    return chunk_stat<T, GREEDY>(buf, cn, c, ctok, clo, chi, c0, lane);
 }
 
 // Generic path for unaligned rows or ragged V: element loads, two passes.
@@ -461,6 +540,7 @@ node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V,
                 }
             }
             warp_argmax(bm, bi);
+            bad |= (bm == -INFINITY);  // every token masked: no arg-max
             ns.mc = bm;
             ns.s = 1.0f;
             ns.amax = bi;
