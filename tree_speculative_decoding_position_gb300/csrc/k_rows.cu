@@ -246,28 +246,45 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int lo, int hi,
     return lo;
 }
 
-// Statistics of one row chunk held in registers: lane l holds vectors l,
-// l+32, ... of the chunk (16 bytes each); vectors at or past cn elements hold
-// -inf.  The chunk length cn is a multiple of the vector width.
+// Statistics of one row chunk held in registers, in two parts so that a
+// caller can start the next chunk's loads between them.  chunk_lane() uses
+// the buffer: lane l holds vectors l, l+32, ... of the chunk (16 bytes each;
+// vectors at or past cn elements hold -inf; cn is a multiple of the vector
+// width).  It reduces the chunk maximum across the warp (the exponentials
+// need it) but leaves the sums, or the arg-max candidates, per lane.
+// chunk_finish() does the remaining warp reductions.
+struct LanePart {
+    float m;   // chunk maximum (warp-reduced)
+    float s;   // this lane's sum of exp2(z*c - mc)
+    float r;   // the same without drafted children
+    int amax;  // T = 0: this lane's first index holding m (INT_MAX: none)
+    bool bad;  // T = 0: a NaN or +inf in this lane's slice
+    bool kids; // T > 0: r differs from s (children fall in the chunk)
+};
+
 template <typename T, bool GREEDY>
-__device__ __forceinline__ ChunkStat chunk_stat(const uint4 (&buf)[kVecPerLane], int cn, float c,
-                                                const int32_t* __restrict__ ctok, int clo, int chi,
-                                                int64_t c0, int lane) {
+__device__ __forceinline__ LanePart chunk_lane(const uint4 (&buf)[kVecPerLane], int cn, float c,
+                                               const int32_t* __restrict__ ctok, int clo, int chi,
+                                               int64_t c0, int lane) {
     constexpr int VEC = Lanes<T>::kVec;
-    ChunkStat st;
+    LanePart lp;
+    lp.s = 0.0f;
+    lp.r = 0.0f;
+    lp.amax = INT_MAX;
+    lp.bad = false;
+    lp.kids = false;
     if (GREEDY) {
         // Argmax with the smallest id among equal maxima: the warp-wide
         // maximum first (packed per-vector maxima), then the first element
         // equal to it in index order.  Vector i*32 + lane sits in lane
         // `lane`, so a lane's first hit is at its smallest i.  A NaN or +inf
-        // anywhere marks the chunk (its sum is set to NaN).
+        // anywhere marks the chunk.
         float vm[kVecPerLane];
         float lm = -INFINITY;
-        bool bad = false;
 #pragma unroll
         for (int i = 0; i < kVecPerLane; ++i) {
             vm[i] = Lanes<T>::vmax_nan(buf[i]);
-            bad |= is_bad_logit(vm[i]);
+            lp.bad |= is_bad_logit(vm[i]);
             lm = fmaxf(lm, vm[i]);
         }
         const float m = warp_max(lm);
@@ -279,30 +296,19 @@ __device__ __forceinline__ ChunkStat chunk_stat(const uint4 (&buf)[kVecPerLane],
                 hit = i;
                 hv = buf[i];
             }
-        int bi = INT_MAX;
         if (hit >= 0) {
             int j0 = VEC - 1;
 #pragma unroll
             for (int j = VEC - 1; j >= 0; --j)
                 if (Lanes<T>::get(hv, j) == m) j0 = j;
-            bi = (int)c0 + (hit * kWarp + lane) * VEC + j0;
+            lp.amax = (int)c0 + (hit * kWarp + lane) * VEC + j0;
         }
-        bi = __reduce_min_sync(0xffffffffu, bi);
-        bad = __any_sync(0xffffffffu, bad);
-        st.m = m;
-        st.s = bad ? __int_as_float(0x7fc00000) : 0.0f;
-        st.r = 0.0f;
-        st.amax = bi;
-        return st;
+        lp.m = m;
+        return lp;
     }
     const float m = warp_max(Lanes<T>::block_max(buf));
-    st.m = m;
-    st.amax = -1;
-    if (m == -INFINITY) {  // every token of the chunk is masked
-        st.s = 0.0f;
-        st.r = 0.0f;
-        return st;
-    }
+    lp.m = m;
+    if (m == -INFINITY) return lp;  // every token of the chunk is masked
     const float mc = __fmul_rn(m, c);
     // Packed fp32x2 fma/add (each lane rounds like fmaf / +); accumulator
     // pair p holds element slots 2p and 2p+1 of every vector.
@@ -319,19 +325,17 @@ __device__ __forceinline__ ChunkStat chunk_stat(const uint4 (&buf)[kVecPerLane],
                 const float2 y = __ffma2_rn(Lanes<T>::pair(buf[i], p), cc, nmc);
                 acc[p] = __fadd2_rn(acc[p], make_float2(ex2(y.x), ex2(y.y)));
             }
-        float s = 0.0f;
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-            s += acc[p].x;
-            s += acc[p].y;
+            lp.s += acc[p].x;
+            lp.s += acc[p].y;
         }
-        s = warp_sum(s);
-        st.s = s;
-        st.r = s;
-        return st;
+        lp.r = lp.s;
+        return lp;
     }
     // Some children fall in this chunk: mark them in a per-lane bitmask over
     // the lane's kVecPerLane * VEC elements, then sum with and without them.
+    lp.kids = true;
     uint32_t excl[(kVecPerLane * VEC + 31) / 32];
 #pragma unroll
     for (int w = 0; w < (kVecPerLane * VEC + 31) / 32; ++w) excl[w] = 0u;
@@ -360,33 +364,41 @@ __device__ __forceinline__ ChunkStat chunk_stat(const uint4 (&buf)[kVecPerLane],
                                  make_float2(((excl[b0 >> 5] >> (b0 & 31)) & 1u) ? 0.0f : e.x,
                                              ((excl[b1 >> 5] >> (b1 & 31)) & 1u) ? 0.0f : e.y));
         }
-    float s = 0.0f, r = 0.0f;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        s += acc[p].x;
-        s += acc[p].y;
-        r += racc[p].x;
-        r += racc[p].y;
+        lp.s += acc[p].x;
+        lp.s += acc[p].y;
+        lp.r += racc[p].x;
+        lp.r += racc[p].y;
     }
-    st.s = warp_sum(s);
-    st.r = warp_sum(r);
+    return lp;
+}
+
+template <bool GREEDY>
+__device__ __forceinline__ ChunkStat chunk_finish(const LanePart& lp) {
+    ChunkStat st;
+    st.m = lp.m;
+    if (GREEDY) {
+        st.amax = __reduce_min_sync(0xffffffffu, lp.amax);
+        st.s = __any_sync(0xffffffffu, lp.bad) ? __int_as_float(0x7fc00000) : 0.0f;
+        st.r = 0.0f;
+        return st;
+    }
+    st.amax = -1;
+    st.s = warp_sum(lp.s);
+    st.r = __any_sync(0xffffffffu, lp.kids) ? warp_sum(lp.r) : st.s;
     return st;
 }
 
-// Vectorised path: the row chunk is 16-byte aligned and its length a multiple
-// of the vector width; streaming 16-byte loads straight into registers.
-template <typename T, bool GREEDY>
-__device__ __forceinline__ ChunkStat reduce_chunk_vec(const T* __restrict__ rp, int cn, float c,
-                                                      const int32_t* __restrict__ ctok, int clo,
-                                                      int chi, int64_t c0, int lane) {
+template <typename T>
+__device__ __forceinline__ void load_chunk(uint4 (&buf)[kVecPerLane], const T* __restrict__ rp,
+                                           int cn, int lane) {
     constexpr int VEC = Lanes<T>::kVec;
-    uint4 buf[kVecPerLane];
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
         const int e = (i * kWarp + lane) * VEC;
         buf[i] = (e < cn) ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
     }
-    return chunk_stat<T, GREEDY>(buf, cn, c, ctok, clo, chi, c0, lane);
 }
 
 // Generic path for unaligned rows or ragged V: element loads, two passes.
@@ -436,6 +448,41 @@ __device__ __noinline__ ChunkStat reduce_chunk_scalar(const T* __restrict__ rp, 
     return st;
 }
 
+// Position of a warp's work item, item = (t * (B+1) + v) * nch + ch, walked
+// by a fixed stride with carries instead of divisions.
+struct ItemPos {
+    int64_t item;
+    int t, v, ch;
+};
+struct ItemStep {
+    int64_t stride;
+    int dt, dv, dch;
+};
+__device__ __forceinline__ ItemPos item_pos(int64_t item, int R, int nch) {
+    const int64_t row = item / nch;
+    ItemPos p;
+    p.item = item;
+    p.ch = (int)(item - row * nch);
+    p.t = (int)(row / R);
+    p.v = (int)(row - (int64_t)p.t * R);
+    return p;
+}
+__device__ __forceinline__ void item_advance(ItemPos& p, const ItemStep& s, int R, int nch) {
+    p.item += s.stride;
+    p.ch += s.dch;
+    const int carry = p.ch >= nch;
+    p.ch -= carry ? nch : 0;
+    p.v += s.dv + carry;
+    const int wrap = p.v >= R;
+    p.v -= wrap ? R : 0;
+    p.t += s.dt + wrap;
+}
+
+// One warp per (node row, 8 KB chunk), persistent over a grid stride.  On the
+// vectorised path a warp issues the next live chunk's loads as soon as the
+// current chunk's per-lane partials are done, and finishes the current
+// chunk's warp reductions while they are in flight; a chunk's child lookup
+// likewise runs while its own loads are in flight.
 template <typename T, bool GREEDY>
 __global__ void __launch_bounds__(kRowThreads)
 rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
@@ -443,32 +490,70 @@ rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     const int lane = threadIdx.x & (kWarp - 1);
     const int wpb = blockDim.x / kWarp;
-    const int64_t total = (int64_t)n_trees * (B + 1) * nch;
-    const int64_t stride = (int64_t)gridDim.x * wpb;
-    for (int64_t item = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; item < total;
-         item += stride) {
-        const int64_t row = item / nch;
-        const int ch = (int)(item - row * nch);
-        const int t = (int)(row / (B + 1));
-        const int v = (int)(row - (int64_t)t * (B + 1));
-        if (v >= __ldg(n_nodes + t) || ws.tstat[t] != kStatOk) continue;
-        const int64_t c0 = (int64_t)ch * CE;
-        const int cn = (int)min((int64_t)CE, V - c0);
-        const T* rp = logits + row * V + c0;
-        int clo = 0, chi = 0;
-        const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+    const int R = B + 1;
+    const int64_t total = (int64_t)n_trees * R * nch;
+    ItemStep step;
+    step.stride = (int64_t)gridDim.x * wpb;
+    {
+        const ItemPos d = item_pos(step.stride, R, nch);
+        step.dt = d.t;
+        step.dv = d.v;
+        step.dch = d.ch;
+    }
+    ItemPos p = item_pos((int64_t)blockIdx.x * wpb + threadIdx.x / kWarp, R, nch);
+    auto live = [&](const ItemPos& q) {
+        return __ldg(n_nodes + q.t) > q.v && ws.tstat[q.t] == kStatOk;
+    };
+    auto children = [&](const ItemPos& q, int64_t c0, int cn, int& clo, int& chi) {
+        clo = chi = 0;
         if (!GREEDY) {
-            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-            const int b0 = cptr[v], b1 = cptr[v + 1];
+            const int32_t* cptr = ws.child_ptr + (int64_t)q.t * (B + 2);
+            const int32_t* ctok = ws.child_tok + (int64_t)q.t * R;
+            const int b0 = cptr[q.v], b1 = cptr[q.v + 1];
             if (b1 > b0) {
                 clo = lower_bound_i32(ctok, b0, b1, c0);
                 chi = lower_bound_i32(ctok, clo, b1, c0 + cn);
             }
         }
-        const ChunkStat st = vec_ok
-            ? reduce_chunk_vec<T, GREEDY>(rp, cn, c, ctok, clo, chi, c0, lane)
-            : reduce_chunk_scalar<T, GREEDY>(rp, cn, c, ctok, clo, chi, c0, lane);
-        if (lane == 0) ws.chunk[item] = st;
+    };
+    auto chunk_ptr = [&](const ItemPos& q, int64_t& c0, int& cn) {
+        c0 = (int64_t)q.ch * CE;
+        cn = (int)min((int64_t)CE, V - c0);
+        return logits + ((int64_t)q.t * R + q.v) * V + c0;
+    };
+
+    if (!vec_ok) {
+        for (; p.item < total; item_advance(p, step, R, nch)) {
+            if (!live(p)) continue;
+            int64_t c0;
+            int cn, clo, chi;
+            const T* rp = chunk_ptr(p, c0, cn);
+            children(p, c0, cn, clo, chi);
+            const ChunkStat st = reduce_chunk_scalar<T, GREEDY>(
+                rp, cn, c, ws.child_tok + (int64_t)p.t * R, clo, chi, c0, lane);
+            if (lane == 0) ws.chunk[p.item] = st;
+        }
+        return;
+    }
+    while (p.item < total && !live(p)) item_advance(p, step, R, nch);
+    if (p.item >= total) return;
+    uint4 buf[kVecPerLane];
+    int64_t c0;
+    int cn;
+    load_chunk<T>(buf, chunk_ptr(p, c0, cn), cn, lane);
+    for (;;) {
+        int clo, chi;
+        children(p, c0, cn, clo, chi);
+        const LanePart lp =
+            chunk_lane<T, GREEDY>(buf, cn, c, ws.child_tok + (int64_t)p.t * R, clo, chi, c0, lane);
+        const int64_t done = p.item;
+        do {
+            item_advance(p, step, R, nch);
+        } while (p.item < total && !live(p));
+        if (p.item < total) load_chunk<T>(buf, chunk_ptr(p, c0, cn), cn, lane);
+        const ChunkStat st = chunk_finish<GREEDY>(lp);
+        if (lane == 0) ws.chunk[done] = st;
+        if (p.item >= total) break;
     }
 }
 
