@@ -502,3 +502,33 @@ def test_build_edge_budgets(tsd, dev, orc):
         g = _tree_np(out, t)
         assert compare_trees(g, ref, lists) == 0
         assert np.array_equal(g["rank"][:g["n_nodes"]], ref["rank"][:ref["n_nodes"]])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_build_topk_selection_paths(tsd, dev, orc, dtype):
+    """The drafter top-k through each of its selection paths, checked against
+    the oracle builder tree for tree: a handful of tokens at or above the
+    bound (one warp sort); dozens of tokens tied at the row maximum, spread
+    over every chunk (the bound admits all of them: a longer list); a row
+    with fewer than k chunks (the bound is -inf: every token is scanned);
+    and a row whose top tokens all sit in one chunk."""
+    V, L = 40960, 4
+    g = torch.Generator().manual_seed(synth.seed_for(5, 9))
+    z = torch.randint(-20, 1, (4, 1, L, V), generator=g).float()
+    # row pattern 1: 60 tokens tied at 5.0, spread over all chunks
+    ties = torch.randperm(V, generator=g)[:60]
+    z[1, 0, :, ties] = 5.0
+    # pattern 3: the 30 largest logits packed into chunk 2
+    z[3, 0, :, 2 * 4096 + 100: 2 * 4096 + 130] = torch.arange(30, dtype=torch.float32) * 0.25 + 3.0
+    # pattern 0: Zipf-like distinct values
+    z[0] = synth.zipf_drafter(1, L, V, synth.seed_for(5, 10), device="cpu", dtype=torch.float32)[0]
+    small = synth.zipf_drafter(1, L, 3000, synth.seed_for(5, 11), device="cpu", dtype=torch.float32)
+    zz = z.to(dtype)
+    out = tsd.tsd_build_tree(zz.to(dev), topk=8, B=40)
+    for t in range(4):
+        ref, lists = oracle_build(orc, zz[t], 8, 40)
+        assert compare_trees(_tree_np(out, t), ref, lists) == 0, t
+    zs = small.to(dtype)  # 3000 tokens: one chunk in bf16, two in fp32 (fewer than k)
+    out = tsd.tsd_build_tree(zs.to(dev), topk=8, B=40)
+    ref, lists = oracle_build(orc, zs[0], 8, 40)
+    assert compare_trees(_tree_np(out, 0), ref, lists) == 0

@@ -10,10 +10,15 @@
 //   scores a prefix as (sum of its z / T_d) - (sum of the rows' LSE), which
 //   is its sum of log q_j = z / T_d - LSE_j.
 //
-// drafter_chunk_kernel  one warp per (row, 8 KB chunk): chunk max, sum of
-//                       exp2(z*c - mc), and the chunk's top-k.
-// drafter_row_kernel    one warp per row: merges the chunk lists into the
-//                       row's top-k, and the chunk sums into its LSE.
+// drafter_chunk_kernel  one warp per (row, 8 KB chunk), streaming: the chunk
+//                       max, the sum of exp2(z*c - mc), and the maximum of
+//                       each lane's slice of the chunk.
+// drafter_row_kernel    one CTA per row: the LSE from the chunk sums; a
+//                       bound theta <= the row's k-th largest logit (the k-th
+//                       largest chunk maximum: k distinct chunks each hold a
+//                       token at or above it); then only the lane slices
+//                       whose maximum reaches theta are read again, and their
+//                       tokens at or above theta give the exact top-k.
 #include "tsd_internal.cuh"
 
 namespace tsd {
@@ -56,39 +61,108 @@ __device__ __forceinline__ void warp_list_offer(float& ev, int& ei, float& tv, i
     }
 }
 
-constexpr int kCandCap = 256;  // candidates per warp before the exact fallback
-constexpr int kMaxListsPerLane = kMaxDrafterChunks / kWarp;
+// Lane l's slice of a chunk: on the vectorised path the 16-byte vectors
+// i*32 + l (i = 0..15); otherwise the tokens l, l+32, ....
 
-// Exact fallback for a chunk whose candidate set overflowed (e.g. a row of
-// many equal logits): offer every token to the warp list, in a plain loop.
+// One warp per (row, 8 KB chunk), persistent over a grid stride.  Writes the
+// chunk max and sum of exp2(z*c - mc) (ChunkStat) and the 32 lane-slice
+// maxima.  On the vectorised path the next chunk's loads are issued as soon
+// as the current chunk's per-lane work is done, so the warp sum and the
+// stores overlap them; positions advance by carries.
 template <typename T>
-__device__ __noinline__ void chunk_topk_fallback(const T* __restrict__ rp, int cn, int64_t c0,
-                                                 int k, int lane, float& ev, int& ei) {
-    float tv = -INFINITY;
-    int ti = INT_MAX;
-    ev = -INFINITY;
-    ei = INT_MAX;
-    for (int e0 = 0; e0 < cn; e0 += kWarp) {
-        const int e = e0 + lane;
-        const float x = e < cn ? load_logit(rp + e) : -INFINITY;
-        warp_list_offer(ev, ei, tv, ti, e < cn, x, (int)c0 + e, k, lane);
-    }
-}
-
-// Sort one float per lane, descending, across the warp (bitonic).
-__device__ __forceinline__ float warp_sort_desc(float x, int lane) {
-#pragma unroll
-    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
-#pragma unroll
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-            const float y = __shfl_xor_sync(0xffffffffu, x, j);
-            const bool lower = (lane & j) == 0;
-            const bool desc = (lane & k2) == 0;
-            // keep the larger value on the lower lane of a descending block
-            x = (lower == desc) ? fmaxf(x, y) : fminf(x, y);
+__global__ void __launch_bounds__(kDThreads)
+drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, float c,
+                     bool vec_ok, BuildWs ws) {
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    constexpr int VEC = Lanes<T>::kVec;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int wpb = blockDim.x / kWarp;
+    const int64_t total = rows * nch;
+    const int64_t stride = (int64_t)gridDim.x * wpb;
+    int64_t item = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp;
+    if (item >= total) return;
+    int64_t row = item / nch;
+    int ch = (int)(item - row * nch);
+    const int64_t drow = stride / nch;
+    const int dch = (int)(stride - drow * nch);
+    auto advance = [&]() {
+        item += stride;
+        ch += dch;
+        const int carry = ch >= nch;
+        ch -= carry ? nch : 0;
+        row += drow + carry;
+    };
+    auto store = [&](int64_t it, float m, float s_lane, float lm) {
+        const float s = warp_sum(s_lane);
+        if (lane == 0) {
+            ChunkStat st;
+            st.m = m;
+            st.s = s;
+            st.r = 0.0f;
+            st.amax = -1;
+            ws.chunk[it] = st;
         }
+        ws.lane_max[it * kWarp + lane] = lm;
+    };
+
+    if (!vec_ok) {  // unaligned rows or ragged V: element loads
+        for (; item < total; advance()) {
+            const int64_t c0 = (int64_t)ch * CE;
+            const int cn = (int)min((int64_t)CE, V - c0);
+            const T* rp = logits + row * V + c0;
+            float lm = -INFINITY, s = 0.0f;
+            for (int e = lane; e < cn; e += kWarp) lm = fmaxf(lm, load_logit(rp + e));
+            const float m = warp_max(lm);
+            const float mc = __fmul_rn(m, c);
+            if (m != -INFINITY)
+                for (int e = lane; e < cn; e += kWarp) s += ex2(fmaf(load_logit(rp + e), c, -mc));
+            store(item, m, s, lm);
+        }
+        return;
     }
-    return x;
+
+    uint4 buf[kVecPerLane];
+    auto load = [&]() {
+        const int64_t c0 = (int64_t)ch * CE;
+        const int cn = (int)min((int64_t)CE, V - c0);
+        const T* rp = logits + row * V + c0;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+            const int e = (i * kWarp + lane) * VEC;
+            buf[i] = (e < cn) ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
+        }
+    };
+    load();
+    for (;;) {
+        const float lm = Lanes<T>::block_max(buf);
+        const float m = warp_max(lm);
+        float s = 0.0f;
+        if (m != -INFINITY) {
+            const float mc = __fmul_rn(m, c);
+            constexpr int NP = VEC / 2;
+            const float2 cc = make_float2(c, c), nmc = make_float2(-mc, -mc);
+            float2 acc[NP];
+#pragma unroll
+            for (int p = 0; p < NP; ++p) acc[p] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i)
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    const float2 y = __ffma2_rn(Lanes<T>::pair(buf[i], p), cc, nmc);
+                    acc[p] = __fadd2_rn(acc[p], make_float2(ex2(y.x), ex2(y.y)));
+                }
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                s += acc[p].x;
+                s += acc[p].y;
+            }
+        }
+        const int64_t cur = item;
+        advance();
+        if (item < total) load();
+        store(cur, m, s, lm);
+        if (item >= total) break;
+    }
 }
 
 // Sort one (value, id) pair per lane across the warp into (value desc, id
@@ -111,251 +185,183 @@ __device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
     }
 }
 
-// One warp per (row, 8 KB chunk).  Pass 1: the chunk max, the sum of
-// exp2(z*c - mc) and each vector's max.  Threshold: the k-th largest of the 32
-// lane maxima -- k distinct tokens reach it, so every token of the chunk's
-// top-k does too.  Pass 2: only vectors whose max reaches the threshold are
-// opened; their qualifying tokens go to a per-warp shared list.  Then k rounds
-// of warp arg-max pick the top-k by (logit desc, id asc).
+constexpr int kRThreads = 256;   // one CTA per drafter row
+constexpr int kSliceCap = 2048;  // qualifying lane slices listed per row
+constexpr int kRowCandCap = 1024;
+
+// One CTA per row.  (1) The chunk statistics go to shared memory; theta =
+// the k-th largest chunk maximum in (value desc, id asc) order, found by
+// ranking every chunk maximum against the others (-inf when the row has fewer
+// than k chunks).  (2) The slice maxima of every chunk whose maximum reaches
+// theta are read at once; the slices reaching theta are listed.  (3) All
+// 16-byte vectors (or tokens) of the listed slices are read at once, and the
+// tokens at or above theta are listed.  Every token of the row's top-k is at
+// or above theta, so (4) warp 0 selecting the top-k of that list by (logit
+// desc, id asc) is exact; meanwhile warp 1 forms the log-normaliser from the
+// chunk sums in float64.  A row whose lists overflow (many equal logits)
+// is scanned token by token instead, still exactly.
 template <typename T>
-__global__ void __launch_bounds__(kDThreads)
-drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, int k,
-                     float c, bool vec_ok, BuildWs ws) {
+__global__ void __launch_bounds__(kRThreads)
+drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, int k, float c,
+                   double temp, bool vec_ok, BuildWs ws) {
     constexpr int CE = kChunkBytes / (int)sizeof(T);
-    constexpr int VEC = 16 / (int)sizeof(T);
-    __shared__ float cand_v[kDThreads / kWarp][kCandCap];
-    __shared__ int cand_i[kDThreads / kWarp][kCandCap];
-    __shared__ int cand_n[kDThreads / kWarp];
-    const int lane = threadIdx.x & (kWarp - 1);
-    const int wid = threadIdx.x / kWarp;
-    const int wpb = blockDim.x / kWarp;
-    const int64_t total = rows * nch;
-    for (int64_t item = (int64_t)blockIdx.x * wpb + wid; item < total;
-         item += (int64_t)gridDim.x * wpb) {
-        const int64_t row = item / nch;
-        const int ch = (int)(item - row * nch);
-        const int64_t c0 = (int64_t)ch * CE;
-        const int cn = (int)min((int64_t)CE, V - c0);
-        const T* rp = logits + row * V + c0;
-        float m = -INFINITY, s = 0.0f, lm = -INFINITY;
-        float ev = -INFINITY;
-        int ei = INT_MAX;
-        if (lane == 0) cand_n[wid] = 0;
-        __syncwarp();
+    constexpr int VEC = Lanes<T>::kVec;
+    __shared__ float cm[kMaxDrafterChunks];
+    __shared__ int qlist[kMaxDrafterChunks];
+    __shared__ int slist[kSliceCap];
+    __shared__ float cand_v[kRowCandCap];
+    __shared__ int cand_i[kRowCandCap];
+    __shared__ float wmax[kRThreads / kWarp];
+    __shared__ int wbad[kRThreads / kWarp];
+    __shared__ int n_q, n_s, n_c;
+    __shared__ float s_theta;
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), wid = tid / kWarp;
+    const int64_t row = blockIdx.x;
+    const ChunkStat* cs = ws.chunk + row * nch;
+    if (tid == 0) {
+        n_q = 0;
+        n_s = 0;
+        n_c = 0;
+        s_theta = -INFINITY;
+    }
+    // (1) chunk maxima, the row maximum, NaN sums
+    float mloc = -INFINITY;
+    bool bad = false;
+    for (int q = tid; q < nch; q += kRThreads) {
+        const ChunkStat st = cs[q];
+        cm[q] = st.m;
+        mloc = fmaxf(mloc, st.m);
+        bad |= (st.s != st.s);
+    }
+    mloc = warp_max(mloc);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        wmax[wid] = mloc;
+        wbad[wid] = bad;
+    }
+    __syncthreads();
+    float m = -INFINITY;
+    bad = false;
+#pragma unroll
+    for (int w = 0; w < kRThreads / kWarp; ++w) {
+        m = fmaxf(m, wmax[w]);
+        bad |= wbad[w] != 0;
+    }
+    for (int q = tid; q < nch; q += kRThreads) {
+        const float v = cm[q];
+        if (v != v) continue;  // a NaN maximum ranks nowhere
+        int rank = 0;
+        for (int p = 0; p < nch; ++p) {
+            const float w = cm[p];
+            rank += (w > v) || (w == v && p < q);
+        }
+        if (rank == k - 1) s_theta = v;
+    }
+    __syncthreads();
+    const float theta = s_theta;
+    for (int q = tid; q < nch; q += kRThreads)
+        if (cm[q] >= theta) qlist[atomicAdd(&n_q, 1)] = q;
+    __syncthreads();
+    // (2) qualifying slices
+    const int nq = n_q;
+    for (int t = tid; t < nq * kWarp; t += kRThreads) {
+        const int q = qlist[t / kWarp], l = t & (kWarp - 1);
+        if (ws.lane_max[(row * nch + q) * kWarp + l] >= theta) {
+            const int pos = atomicAdd(&n_s, 1);
+            if (pos < kSliceCap) slist[pos] = q * kWarp + l;
+        }
+    }
+    __syncthreads();
+    const int ns = n_s;
+    bool overflow = ns > kSliceCap;
+    // (3) candidate tokens
+    if (!overflow) {
+        const T* rrow = logits + row * V;
+        auto offer = [&](float x, int id) {
+            const int pos = atomicAdd(&n_c, 1);
+            if (pos < kRowCandCap) {
+                cand_v[pos] = x;
+                cand_i[pos] = id;
+            }
+        };
         if (vec_ok) {
-            uint4 buf[kVecPerLane];
-            float vmax[kVecPerLane];
+            for (int t = tid; t < ns * kVecPerLane; t += kRThreads) {
+                const int sl = slist[t / kVecPerLane], i = t % kVecPerLane;
+                const int q = sl / kWarp, l = sl & (kWarp - 1);
+                const int64_t c0 = (int64_t)q * CE;
+                const int e = (i * kWarp + l) * VEC;
+                if (e < (int)min((int64_t)CE, V - c0)) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(rrow + c0 + e));
+                    if (Lanes<T>::vmax(v) >= theta) {
 #pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                const int e = (i * kWarp + lane) * VEC;
-                const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
-                buf[i] = (e < cn) ? ld_stream16(rp + e) : make_uint4(ninf, ninf, ninf, ninf);
-            }
-#pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                if (sizeof(T) == 2) {
-                    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&buf[i].x);
-                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].y));
-                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].z));
-                    a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&buf[i].w));
-                    vmax[i] = fmaxf(__low2float(a), __high2float(a));
-                } else {
-                    vmax[i] = fmaxf(fmaxf(__uint_as_float(buf[i].x), __uint_as_float(buf[i].y)),
-                                    fmaxf(__uint_as_float(buf[i].z), __uint_as_float(buf[i].w)));
-                }
-                lm = fmaxf(lm, vmax[i]);
-            }
-            m = warp_max(lm);
-            const float mc = __fmul_rn(m, c);
-            if (m != -INFINITY) {
-                float acc[VEC];
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
-#pragma unroll
-                for (int i = 0; i < kVecPerLane; ++i)
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
-                                           : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
-                        const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
-                                                       : __uint_as_float(w);
-                        acc[j] += ex2(fmaf(x, c, -mc));
-                    }
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) s += acc[j];
-            }
-            const float theta = __shfl_sync(0xffffffffu, warp_sort_desc(lm, lane), k - 1);
-#pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                const int e = (i * kWarp + lane) * VEC;
-                if (e < cn && vmax[i] >= theta) {
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const uint32_t w = j / (VEC / 4) == 0 ? buf[i].x : j / (VEC / 4) == 1 ? buf[i].y
-                                           : j / (VEC / 4) == 2 ? buf[i].z : buf[i].w;
-                        const float x = sizeof(T) == 2 ? ((j & 1) ? bf16_hi(w) : bf16_lo(w))
-                                                       : __uint_as_float(w);
-                        if (x >= theta) {
-                            const int pos = atomicAdd(&cand_n[wid], 1);
-                            if (pos < kCandCap) {
-                                cand_v[wid][pos] = x;
-                                cand_i[wid][pos] = (int)c0 + e + j;
-                            }
+                        for (int j = 0; j < VEC; ++j) {
+                            const float x = Lanes<T>::get(v, j);
+                            if (x >= theta) offer(x, (int)c0 + e + j);
                         }
                     }
                 }
             }
         } else {
-            for (int e = lane; e < cn; e += kWarp) lm = fmaxf(lm, load_logit(rp + e));
-            m = warp_max(lm);
-            const float mc = __fmul_rn(m, c);
-            if (m != -INFINITY)
-                for (int e = lane; e < cn; e += kWarp) s += ex2(fmaf(load_logit(rp + e), c, -mc));
-            const float theta = __shfl_sync(0xffffffffu, warp_sort_desc(lm, lane), k - 1);
-            for (int e = lane; e < cn; e += kWarp) {
-                const float x = load_logit(rp + e);
-                if (x >= theta) {
-                    const int pos = atomicAdd(&cand_n[wid], 1);
-                    if (pos < kCandCap) {
-                        cand_v[wid][pos] = x;
-                        cand_i[wid][pos] = (int)c0 + e;
-                    }
+            constexpr int per = CE / kWarp;  // tokens of one slice: l, l+32, ...
+            for (int t = tid; t < ns * per; t += kRThreads) {
+                const int sl = slist[t / per], jj = t % per;
+                const int q = sl / kWarp, l = sl & (kWarp - 1);
+                const int64_t c0 = (int64_t)q * CE;
+                const int e = l + kWarp * jj;
+                if (e < (int)min((int64_t)CE, V - c0)) {
+                    const float x = load_logit(rrow + c0 + e);
+                    if (x >= theta) offer(x, (int)c0 + e);
                 }
             }
         }
-        __syncwarp();
-        const int nc = cand_n[wid];
-        if (nc > kCandCap) {
-            chunk_topk_fallback<T>(rp, cn, c0, k, lane, ev, ei);
-        } else if (nc <= kWarp) {
-            // the usual case: one warp sort of the candidates
-            ev = lane < nc ? cand_v[wid][lane] : -INFINITY;
-            ei = lane < nc ? cand_i[wid][lane] : INT_MAX;
-            warp_sort_pairs(ev, ei, lane);
-        } else {
-            // k rounds of arg-max over the candidates; a taken one becomes
-            // (-inf, INT_MAX), which every real token beats.
-            for (int r = 0; r < k; ++r) {
-                float bv = -INFINITY;
-                int bi = INT_MAX, bp = -1;
-                for (int q = lane; q < nc; q += kWarp)
-                    if (better(cand_v[wid][q], cand_i[wid][q], bv, bi)) {
-                        bv = cand_v[wid][q];
-                        bi = cand_i[wid][q];
-                        bp = q;
-                    }
-                float wv = bv;
-                int wi = bi;
-                warp_argmax(wv, wi);
-                if (lane == r) {
-                    ev = wv;
-                    ei = wi;
-                }
-                if (wi != INT_MAX && bi == wi) {
-                    cand_v[wid][bp] = -INFINITY;
-                    cand_i[wid][bp] = INT_MAX;
-                }
-                __syncwarp();
-            }
-        }
-        s = warp_sum(s);
-        if (lane == 0) {
-            ChunkStat st;
-            st.m = m;
-            st.s = s;
-            st.r = 0.0f;
-            st.amax = -1;
-            ws.chunk[item] = st;
-        }
-        if (lane < k) {
-            ws.cand_v[item * k + lane] = ev;
-            ws.cand_i[item * k + lane] = ei;
-        }
-        __syncwarp();
     }
-}
-
-constexpr int kRowStage = 1024;  // candidates staged in shared memory per warp
-
-// One warp per row: the row's log-normaliser from its chunk sums (float64),
-// and its top-k merged from the chunks' sorted lists.  The lists are first
-// copied to shared memory in one coalesced pass (when they fit), then lane l
-// walks the lists of chunks l, l+32, ...; k rounds of warp arg-max over the
-// lanes' current heads.
-__global__ void __launch_bounds__(kDThreads)
-drafter_row_kernel(int64_t rows, int nch, int k, float c, double temp, BuildWs ws) {
-    __shared__ float sv[kDThreads / kWarp][kRowStage];
-    __shared__ int si[kDThreads / kWarp][kRowStage];
-    const int lane = threadIdx.x & (kWarp - 1);
-    const int wid = threadIdx.x / kWarp;
-    const int wpb = blockDim.x / kWarp;
-    for (int64_t row = (int64_t)blockIdx.x * wpb + wid; row < rows;
-         row += (int64_t)gridDim.x * wpb) {
-        const ChunkStat* cs = ws.chunk + row * nch;
-        const int ncand = nch * k;
-        const bool staged = ncand <= kRowStage;
-        const float* gv = ws.cand_v + row * ncand;
-        const int* gi = ws.cand_i + row * ncand;
-        if (staged)
-            for (int q = lane; q < ncand; q += kWarp) {
-                sv[wid][q] = gv[q];
-                si[wid][q] = gi[q];
+    __syncthreads();
+    const int nc = n_c;
+    overflow |= nc > kRowCandCap;
+    // (4) selection | log-normaliser
+    if (wid == 0) {
+        float ev = -INFINITY, tv = -INFINITY;
+        int ei = INT_MAX, ti = INT_MAX;
+        if (!overflow && nc <= kWarp) {
+            ev = lane < nc ? cand_v[lane] : -INFINITY;
+            ei = lane < nc ? cand_i[lane] : INT_MAX;
+            warp_sort_pairs(ev, ei, lane);
+        } else if (!overflow) {
+            for (int b0 = 0; b0 < nc; b0 += kWarp) {
+                const bool has = b0 + lane < nc;
+                warp_list_offer(ev, ei, tv, ti, has, has ? cand_v[b0 + lane] : -INFINITY,
+                                has ? cand_i[b0 + lane] : INT_MAX, k, lane);
             }
-        float m = -INFINITY;
-        bool bad = false;
-        for (int q = lane; q < nch; q += kWarp) {
-            m = fmaxf(m, cs[q].m);
-            bad |= (cs[q].s != cs[q].s);
-        }
-        m = warp_max(m);
-        const float mc = __fmul_rn(m, c);
-        double s = 0.0;
-        for (int q = lane; q < nch; q += kWarp)
-            if (cs[q].m != -INFINITY) s += (double)cs[q].s * (double)ex2(__fmul_rn(cs[q].m, c) - mc);
-        s = warp_sum_d(s);
-        bad = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0);
-        // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
-        const double lse = bad ? __longlong_as_double(0x7ff8000000000000ll)
-                               : 0.6931471805599453 * ((double)mc + log2(s));
-        __syncwarp();
-        const float* cv = staged ? sv[wid] : gv;
-        const int* ci = staged ? si[wid] : gi;
-        int pos[kMaxListsPerLane];
-        const int nj = (nch + kWarp - 1) / kWarp;
-        for (int j = 0; j < nj; ++j) pos[j] = 0;
-        float ev = -INFINITY;
-        int ei = INT_MAX;
-        for (int r = 0; r < k; ++r) {
-            float hv = -INFINITY;
-            int hi = INT_MAX, hj = -1;
-            for (int j = 0; j < nj; ++j) {
-                const int q = lane + kWarp * j;
-                const int p = pos[j];
-                if (q < nch && p < k) {
-                    const float x = cv[q * k + p];
-                    const int xi = ci[q * k + p];
-                    if (xi != INT_MAX && better(x, xi, hv, hi)) {
-                        hv = x;
-                        hi = xi;
-                        hj = j;
-                    }
+        } else {
+            // every token of every chunk reaching theta, in order
+            for (int q = 0; q < nch; ++q) {
+                if (!(cm[q] >= theta)) continue;
+                const int64_t c0 = (int64_t)q * CE;
+                const int cn = (int)min((int64_t)CE, V - c0);
+                const T* rp = logits + row * V + c0;
+                for (int e0 = 0; e0 < cn; e0 += kWarp) {
+                    const int e = e0 + lane;
+                    const float x = e < cn ? load_logit(rp + e) : -INFINITY;
+                    warp_list_offer(ev, ei, tv, ti, e < cn && x >= theta, x, (int)c0 + e, k, lane);
                 }
             }
-            float wv = hv;
-            int wi = hi;
-            warp_argmax(wv, wi);
-            if (lane == r) {
-                ev = wv;
-                ei = wi;
-            }
-            if (wi != INT_MAX && hi == wi) ++pos[hj];
         }
         if (lane < k) {
             ws.top_id[row * k + lane] = ei;
             ws.top_zt[row * k + lane] = (double)ev / temp;
         }
-        if (lane == 0) ws.lse[row] = lse;
-        __syncwarp();
+    } else if (wid == 1) {
+        const float mc = __fmul_rn(m, c);
+        double sum = 0.0;
+        for (int q = lane; q < nch; q += kWarp)
+            if (cm[q] != -INFINITY) sum += (double)cs[q].s * (double)ex2(__fmul_rn(cm[q], c) - mc);
+        sum = warp_sum_d(sum);
+        if (lane == 0) {
+            const bool b = bad || m == -INFINITY || !(sum > 0.0);
+            // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
+            ws.lse[row] = b ? __longlong_as_double(0x7ff8000000000000ll)
+                            : 0.6931471805599453 * ((double)mc + log2(sum));
+        }
     }
 }
 
@@ -365,23 +371,24 @@ cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t ro
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
     const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int wpb = kDThreads / kWarp;
-    int64_t want = (rows * nch + wpb - 1) / wpb;
-    int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-    if (dtype == TSD_BF16)
-        drafter_chunk_kernel<__nv_bfloat16><<<grid, kDThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(logits), rows, V, nch, topk, c, vec_ok, ws);
-    else
-        drafter_chunk_kernel<float><<<grid, kDThreads, 0, stream>>>(
-            static_cast<const float*>(logits), rows, V, nch, topk, c, vec_ok, ws);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    want = (rows + wpb - 1) / wpb;
-    grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-    drafter_row_kernel<<<grid, kDThreads, 0, stream>>>(rows, nch, topk, c, temp, ws);
+    const int64_t want_chunks = (rows * nch + wpb - 1) / wpb;
+    // persistent: one wave of resident CTAs, each warp streaming many chunks
+    if (dtype == TSD_BF16) {
+        const auto* p = static_cast<const __nv_bfloat16*>(logits);
+        auto kc = drafter_chunk_kernel<__nv_bfloat16>;
+        kc<<<resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream>>>(
+            p, rows, V, nch, c, vec_ok, ws);
+        drafter_row_kernel<__nv_bfloat16><<<(unsigned)rows, kRThreads, 0, stream>>>(
+            p, rows, V, nch, topk, c, temp, vec_ok, ws);
+    } else {
+        const auto* p = static_cast<const float*>(logits);
+        auto kc = drafter_chunk_kernel<float>;
+        kc<<<resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream>>>(
+            p, rows, V, nch, c, vec_ok, ws);
+        drafter_row_kernel<float><<<(unsigned)rows, kRThreads, 0, stream>>>(
+            p, rows, V, nch, topk, c, temp, vec_ok, ws);
+    }
     return cudaGetLastError();
 }
 

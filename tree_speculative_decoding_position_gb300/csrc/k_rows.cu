@@ -158,84 +158,6 @@ cudaError_t launch_verify_prep(const int32_t* parent, const int32_t* token, cons
 // ---------------------------------------------------------------------------
 constexpr int kRowThreads = 256;
 
-template <typename T>
-struct Lanes;
-template <>
-struct Lanes<__nv_bfloat16> {
-    static constexpr int kVec = 8;  // elements per 16-byte load
-    static __device__ __forceinline__ float get(const uint4& q, int j) {
-        const uint32_t w = (j >> 1) == 0 ? q.x : (j >> 1) == 1 ? q.y : (j >> 1) == 2 ? q.z : q.w;
-        return (j & 1) ? bf16_hi(w) : bf16_lo(w);
-    }
-    static __device__ __forceinline__ uint4 neg_inf() {
-        return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-    }
-    // Elements 2p and 2p+1 of a vector, widened to fp32.
-    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
-        const uint32_t w = p == 0 ? q.x : p == 1 ? q.y : p == 2 ? q.z : q.w;
-        return make_float2(bf16_lo(w), bf16_hi(w));
-    }
-    // Maximum over a lane's whole chunk slice: packed bf16 maxima in four
-    // independent chains, widened once at the end.
-    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
-        __nv_bfloat162 a0 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].x);
-        __nv_bfloat162 a1 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].y);
-        __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].z);
-        __nv_bfloat162 a3 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].w);
-#pragma unroll
-        for (int i = 1; i < kVecPerLane; ++i) {
-            a0 = __hmax2(a0, *reinterpret_cast<const __nv_bfloat162*>(&b[i].x));
-            a1 = __hmax2(a1, *reinterpret_cast<const __nv_bfloat162*>(&b[i].y));
-            a2 = __hmax2(a2, *reinterpret_cast<const __nv_bfloat162*>(&b[i].z));
-            a3 = __hmax2(a3, *reinterpret_cast<const __nv_bfloat162*>(&b[i].w));
-        }
-        a0 = __hmax2(__hmax2(a0, a1), __hmax2(a2, a3));
-        return fmaxf(__low2float(a0), __high2float(a0));
-    }
-    // Maximum that is NaN when any element is NaN.
-    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
-        __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&q.x),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&q.y));
-        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.z));
-        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.w));
-        return __bfloat162float(__hmax_nan(__low2bfloat16(a), __high2bfloat16(a)));
-    }
-};
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-template <>
-struct Lanes<float> {
-    static constexpr int kVec = 4;
-    static __device__ __forceinline__ float get(const uint4& q, int j) {
-        return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
-    }
-    static __device__ __forceinline__ uint4 neg_inf() {
-        return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-    }
-    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
-        return p == 0 ? make_float2(__uint_as_float(q.x), __uint_as_float(q.y))
-                      : make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
-    }
-    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i) {
-            a0 = fmaxf(a0, __uint_as_float(b[i].x));
-            a1 = fmaxf(a1, __uint_as_float(b[i].y));
-            a2 = fmaxf(a2, __uint_as_float(b[i].z));
-            a3 = fmaxf(a3, __uint_as_float(b[i].w));
-        }
-        return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-    }
-    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
-        return fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
-                        fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
-    }
-};
-
 // First index in sorted a[lo, hi) with a[i] >= x.
 __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int lo, int hi, int64_t x) {
     while (lo < hi) {
@@ -573,6 +495,8 @@ cudaError_t launch_rows(const void* logits, tsd_dtype dtype, int n_trees, int B,
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
     const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
+    // grid-stride over a few waves of CTAs (measured slightly faster here than
+    // one persistent wave of resident CTAs)
     const int grid = row_grid((int64_t)n_trees * (B + 1) * nch);
     if (dtype == TSD_BF16) {
         const auto* p = static_cast<const __nv_bfloat16*>(logits);

@@ -3,9 +3,39 @@
 // allocates or synchronises.
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "tsd_internal.cuh"
 
 namespace tsd {
+
+int resident_grid(const void* kernel, int threads, size_t smem, int64_t want) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, std::pair<int, int>> cache;  // -> (SMs, CTAs/SM)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::pair<int, int> r;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find({dev, kernel});
+        if (it == cache.end()) {
+            int sms = 0, per = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sms < 1)
+                sms = 1;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) !=
+                    cudaSuccess ||
+                per < 1)
+                per = 1;
+            it = cache.emplace(std::make_pair(dev, kernel), std::make_pair(sms, per)).first;
+        }
+        r = it->second;
+    }
+    const int64_t cap = (int64_t)r.first * r.second;
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
 
 size_t heap_spill_bytes(int n_modes, int L, int topk, int B);  // k_heap.cu
 
@@ -69,8 +99,7 @@ size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int
     const size_t nch = (size_t)n_chunks(V, esize);
     BuildWs ws;
     ws.chunk = cv.take<ChunkStat>(rows * nch);
-    ws.cand_v = cv.take<float>(rows * nch * topk);
-    ws.cand_i = cv.take<int32_t>(rows * nch * topk);
+    ws.lane_max = cv.take<float>(rows * nch * kWarp);
     ws.top_id = cv.take<int32_t>(rows * topk);
     ws.top_zt = cv.take<double>(rows * topk);
     ws.lse = cv.take<double>(rows);

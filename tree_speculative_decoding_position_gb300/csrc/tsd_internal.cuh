@@ -18,8 +18,8 @@ constexpr int kChunkBytes = 8192;
 constexpr int kVecPerLane = kChunkBytes / (16 * kWarp);  // 16
 
 __host__ __device__ constexpr int chunk_elems(int esize) { return kChunkBytes / esize; }
-// The builder merges per-chunk top-k lists with 64 cursors per lane, so a
-// drafter row may span at most 2048 chunks (V <= 8388608 bf16 / 4194304 fp32).
+// The drafter's row kernel marks picked chunks in one 64-bit mask per lane, so
+// a drafter row may span at most 2048 chunks (V <= 8388608 bf16 / 4194304 fp32).
 constexpr int kMaxDrafterChunks = 2048;
 __host__ __device__ inline int64_t n_chunks(int64_t V, int esize) {
     return (V + chunk_elems(esize) - 1) / chunk_elems(esize);
@@ -98,6 +98,96 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Per-type access to one 16-byte vector of logits (8 bf16 or 4 fp32).
+template <typename T>
+struct Lanes;
+template <>
+struct Lanes<__nv_bfloat16> {
+    static constexpr int kVec = 8;  // elements per 16-byte load
+    static __device__ __forceinline__ float get(const uint4& q, int j) {
+        const uint32_t w = (j >> 1) == 0 ? q.x : (j >> 1) == 1 ? q.y : (j >> 1) == 2 ? q.z : q.w;
+        return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    static __device__ __forceinline__ uint4 neg_inf() {
+        return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+    // Elements 2p and 2p+1 of a vector, widened to fp32.
+    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
+        const uint32_t w = p == 0 ? q.x : p == 1 ? q.y : p == 2 ? q.z : q.w;
+        return make_float2(bf16_lo(w), bf16_hi(w));
+    }
+    static __device__ __forceinline__ float vmax(const uint4& q) {
+        __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&q.x),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&q.y));
+        a = __hmax2(a, __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&q.z),
+                               *reinterpret_cast<const __nv_bfloat162*>(&q.w)));
+        return fmaxf(__low2float(a), __high2float(a));
+    }
+    // Maximum over a lane's whole chunk slice: packed bf16 maxima in four
+    // independent chains, widened once at the end.
+    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
+        __nv_bfloat162 a0 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].x);
+        __nv_bfloat162 a1 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].y);
+        __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].z);
+        __nv_bfloat162 a3 = *reinterpret_cast<const __nv_bfloat162*>(&b[0].w);
+#pragma unroll
+        for (int i = 1; i < kVecPerLane; ++i) {
+            a0 = __hmax2(a0, *reinterpret_cast<const __nv_bfloat162*>(&b[i].x));
+            a1 = __hmax2(a1, *reinterpret_cast<const __nv_bfloat162*>(&b[i].y));
+            a2 = __hmax2(a2, *reinterpret_cast<const __nv_bfloat162*>(&b[i].z));
+            a3 = __hmax2(a3, *reinterpret_cast<const __nv_bfloat162*>(&b[i].w));
+        }
+        a0 = __hmax2(__hmax2(a0, a1), __hmax2(a2, a3));
+        return fmaxf(__low2float(a0), __high2float(a0));
+    }
+    // Maximum that is NaN when any element is NaN.
+    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
+        __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&q.x),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&q.y));
+        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.z));
+        a = __hmax2_nan(a, *reinterpret_cast<const __nv_bfloat162*>(&q.w));
+        return __bfloat162float(__hmax_nan(__low2bfloat16(a), __high2bfloat16(a)));
+    }
+};
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+template <>
+struct Lanes<float> {
+    static constexpr int kVec = 4;
+    static __device__ __forceinline__ float get(const uint4& q, int j) {
+        return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
+    }
+    static __device__ __forceinline__ uint4 neg_inf() {
+        return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    }
+    static __device__ __forceinline__ float2 pair(const uint4& q, int p) {
+        return p == 0 ? make_float2(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
+    static __device__ __forceinline__ float vmax(const uint4& q) {
+        return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+    static __device__ __forceinline__ float block_max(const uint4 (&b)[kVecPerLane]) {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+            a0 = fmaxf(a0, __uint_as_float(b[i].x));
+            a1 = fmaxf(a1, __uint_as_float(b[i].y));
+            a2 = fmaxf(a2, __uint_as_float(b[i].z));
+            a3 = fmaxf(a3, __uint_as_float(b[i].w));
+        }
+        return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+    }
+    static __device__ __forceinline__ float vmax_nan(const uint4& q) {
+        return fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                        fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+};
+
 // (value desc, id asc) order on (logit, token) pairs.
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
@@ -161,8 +251,7 @@ size_t verify_ws_layout(int n_trees, int B, int64_t V, int esize, void* base, Ve
 
 struct BuildWs {
     ChunkStat* chunk;    // [rows][n_chunks] (m, s)
-    float* cand_v;       // [rows][n_chunks][topk] chunk top-k logits
-    int32_t* cand_i;     // [rows][n_chunks][topk] and ids
+    float* lane_max;     // [rows][n_chunks][32] maximum of each lane's slice of a chunk
     int32_t* top_id;     // [rows][topk]
     double* top_zt;      // [rows][topk] the kept tokens' z / T_d
     double* lse;         // [rows] log sum exp(z / T_d) over the row
@@ -206,6 +295,12 @@ cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int 
                              int prefix_len, uint32_t* anc_bits, int32_t* position_ids,
                              float* additive_mask, int64_t mask_ld, int32_t* status,
                              cudaStream_t stream);
+
+// Grid for a persistent (grid-stride) kernel: min(want, SMs x the CTAs of
+// `kernel` resident per SM at this block size and dynamic shared memory), at
+// least 1.  Residency comes from the occupancy calculator, cached per device
+// and kernel.
+int resident_grid(const void* kernel, int threads, size_t smem, int64_t want);
 
 // Internal per-tree status values (tstat) match tsd_status codes.
 constexpr int32_t kStatOk = TSD_OK;
