@@ -84,7 +84,7 @@ struct BuildPlan {
     int M;          // entries taken per round
     int fcap, xcap; // frontier / taken-list capacity
     int hcap;       // hash table size (power of two)
-    size_t lists, fbytes, xbytes, sbytes, hbytes, flag_bytes, smem_total;
+    size_t lists, fbytes, xbytes, sbytes, scode_bytes, hbytes, flag_bytes, smem_total;
     bool big_in_smem;
     size_t global_per_tree;
 };
@@ -101,13 +101,17 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.M = (n_modes > 1 ? 256 : 512) / topk;
     if (p.M < 8) p.M = 8;
     if (p.M > 128) p.M = 128;
+    // M * topk <= 512 (TSD_MAX_TOPK = 32): child generation gives each of the
+    // 256 threads at most two slots
     p.xcap = n_modes * (B + 1) + p.M;
     p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk + 32;
     p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
     auto r16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
     p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)) +
                   sizeof(double) * (size_t)n_modes * (L + 1));
-    p.sbytes = r16(sizeof(FEntry) * (size_t)pow2_at_least(topk * p.M < 32 ? 32 : topk * p.M));
+    const size_t n2s = (size_t)pow2_at_least(topk * p.M < 32 ? 32 : topk * p.M);
+    p.scode_bytes = r16(sizeof(unsigned long long) * n2s);  // successor order codes
+    p.sbytes = r16(sizeof(FEntry) * n2s) + p.scode_bytes;
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
     p.fbytes = r16(sizeof(FEntry) * 2 * (size_t)p.fcap);
@@ -187,25 +191,142 @@ __device__ void sort_entries(FEntry* a, int n2) {
     }
 }
 
-// dst[0, na+nb) = merge of sorted a[0, na) and sorted b[0, nb) (merge path).
-__device__ void merge_entries(FEntry* dst, const FEntry* a, int na, const FEntry* b, int nb) {
+// Part `part` of `nparts` of dst[0, na+nb) = merge of sorted a[0, na) and
+// sorted b[0, nb) (merge path).  With `ord`, the j-th entry of b is
+// b[ord[j] & 0xffff] (b itself unsorted).  No barrier.
+__device__ void merge_part(FEntry* dst, const FEntry* a, int na, const FEntry* b, int nb,
+                           const unsigned long long* ord, int part, int nparts) {
+    auto bj = [&](int j) -> const FEntry& { return ord ? b[ord[j] & 0xffffull] : b[j]; };
     const int total = na + nb;
-    const int per = (total + blockDim.x - 1) / blockDim.x;
-    const int d0 = min(total, (int)threadIdx.x * per), d1 = min(total, d0 + per);
+    const int per = (total + nparts - 1) / nparts;
+    const int d0 = min(total, part * per), d1 = min(total, d0 + per);
     if (d0 < d1) {
         int lo = max(0, d0 - nb), hi = min(d0, na);
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (before(a[mid], b[d0 - mid - 1])) lo = mid + 1;
+            if (before(a[mid], bj(d0 - mid - 1))) lo = mid + 1;
             else hi = mid;
         }
         int ia = lo, ib = d0 - lo;
         for (int d = d0; d < d1; ++d) {
-            if (ib >= nb || (ia < na && before(a[ia], b[ib]))) dst[d] = a[ia++];
-            else dst[d] = b[ib++];
+            if (ib >= nb || (ia < na && before(a[ia], bj(ib)))) dst[d] = a[ia++];
+            else dst[d] = bj(ib++);
+        }
+    }
+}
+
+// Two independent merges in one phase, the block's threads split between
+// them in proportion to their lengths; one barrier at the end.
+__device__ void merge_two(FEntry* d1, const FEntry* a1, int na1, const FEntry* b1, int nb1,
+                          FEntry* d2, const FEntry* a2, int na2, const FEntry* b2, int nb2,
+                          const unsigned long long* ord2) {
+    const int n1 = na1 + nb1, n2 = na2 + nb2, nt = blockDim.x;
+    int t1 = n1 + n2 > 0 ? (int)(((long long)nt * n1 + (n1 + n2) / 2) / (n1 + n2)) : 0;
+    if (n1 > 0 && t1 < 1) t1 = 1;
+    if (n2 > 0 && t1 > nt - 1) t1 = nt - 1;
+    if ((int)threadIdx.x < t1) merge_part(d1, a1, na1, b1, nb1, nullptr, threadIdx.x, t1);
+    else merge_part(d2, a2, na2, b2, nb2, ord2, threadIdx.x - t1, nt - t1);
+    __syncthreads();
+}
+
+// Smallest i in [lo, hi) with pred(i) false, for pred true then false over
+// the range (hi if none): a 32-ary search by one warp (all lanes call it).
+template <class P>
+__device__ int warp_first_false(int lo, int hi, P pred) {
+    const int lane = threadIdx.x & 31;
+    while (hi - lo > 32) {
+        const long long span = hi - lo;
+        const bool tr = pred(lo + (int)(span * (lane + 1) / 33));
+        const int c = __popc(__ballot_sync(0xffffffffu, tr));  // probes 0..c-1 hold
+        const int nlo = c == 0 ? lo : lo + (int)(span * c / 33) + 1;
+        const int nhi = c == 32 ? hi : lo + (int)(span * (c + 1) / 33);
+        lo = nlo;
+        hi = nhi;
+    }
+    const bool tr = lo + lane < hi && pred(lo + lane);
+    return lo + __popc(__ballot_sync(0xffffffffu, tr));
+}
+
+// Bitonic sort of 64-bit codes c[0, n2) ascending (n2 a power of two, at
+// least 32); sub-32 distances in registers, the rest through memory.
+__device__ void sort_codes(unsigned long long* c, int n2) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nblk = n2 >> 5;
+    auto lane_steps = [&](unsigned long long x, int e, int k, int jtop) {
+        for (int j = jtop; j > 0; j >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+            const bool lower = (lane & j) == 0;
+            const bool asc = (e & k) == 0;
+            const unsigned long long lo = x < y ? x : y, hi = x < y ? y : x;
+            x = (lower == asc) ? lo : hi;
+        }
+        return x;
+    };
+    for (int b = wid; b < nblk; b += nw) {
+        const int e = (b << 5) + lane;
+        unsigned long long x = c[e];
+        for (int k = 2; k <= 32; k <<= 1) x = lane_steps(x, e, k, k >> 1);
+        c[e] = x;
+    }
+    __syncthreads();
+    for (int k = 64; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j >= 32; j >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long x = c[i], y = c[l];
+                    if (((i & k) == 0) == (y < x)) {
+                        c[i] = y;
+                        c[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        for (int b = wid; b < nblk; b += nw) {
+            const int e = (b << 5) + lane;
+            c[e] = lane_steps(c[e], e, k, 16);
+        }
+        __syncthreads();
+    }
+}
+
+// The total order of a[0, n) (n <= 65536) as codes ord[0, n): bits 63..16
+// hold the complement of the top 48 bits of the score image (ascending code =
+// descending score), bits 15..0 the entry's index.  Runs of equal 48-bit
+// prefixes (scores within 2^-36 relative, exact ties among them) are then
+// re-ordered by the full total order, one thread per run.  Returns false,
+// leaving ord unusable, when a run is longer than 32 (the caller then sorts
+// the entries themselves).  ord must hold n2 = pow2 >= max(n, 32) codes.
+__device__ bool sort_order(const FEntry* a, int n, unsigned long long* ord, int n2, int* flag) {
+    for (int i = threadIdx.x; i < n2; i += blockDim.x)
+        ord[i] = i < n ? ((~a[i].key & 0xffffffffffff0000ull) | (unsigned long long)i) : ~0ull;
+    if (threadIdx.x == 0) *flag = 0;
+    __syncthreads();
+    sort_codes(ord, n2);
+    for (int p = threadIdx.x; p < n; p += blockDim.x) {
+        const unsigned long long hp = ord[p] >> 16;
+        if ((p > 0 && (ord[p - 1] >> 16) == hp) || p + 1 >= n || (ord[p + 1] >> 16) != hp) continue;
+        int q = p + 1;  // run [p, q) of equal prefixes, p its first element
+        while (q < n && (ord[q] >> 16) == hp && q - p <= 32) ++q;
+        if (q - p > 32) {
+            *flag = 1;
+            continue;
+        }
+        for (int u = p + 1; u < q; ++u) {  // insertion sort by the total order
+            const unsigned long long cu = ord[u];
+            int w = u - 1;
+            while (w >= p && before(a[cu & 0xffffull], a[ord[w] & 0xffffull])) {
+                ord[w + 1] = ord[w];
+                --w;
+            }
+            ord[w + 1] = cu;
         }
     }
     __syncthreads();
+    const bool ok = *flag == 0;
+    __syncthreads();
+    return ok;
 }
 
 // Inclusive block scan of one int per thread; *total = block sum.
@@ -295,6 +416,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     int32_t* ids = reinterpret_cast<int32_t*>(cum + K * (L + 1));
     p += plan.lists;
     FEntry* S = reinterpret_cast<FEntry*>(p);
+    unsigned long long* Scode = reinterpret_cast<unsigned long long*>(p + plan.sbytes - plan.scode_bytes);
     p += plan.sbytes;
     uint8_t* big = plan.big_in_smem ? p : ws.heap + (size_t)t * ws.heap_stride;
     FEntry* F[2] = {reinterpret_cast<FEntry*>(big), reinterpret_cast<FEntry*>(big) + plan.fcap};
@@ -321,13 +443,17 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         ids[i] = ws.top_id[(int64_t)t * nl + i];
         if (x != x) s_bad = 1;
     }
-    for (int m = tid; m < K; m += blockDim.x) {  // C_m(d), summed left to right
+    for (int i = tid; i < K * L; i += blockDim.x) {  // the row log-normalisers, all at once
+        const double l = ws.lse[(int64_t)t * K * L + i];
+        if (l != l) s_bad = 1;
+        cum[(i / L) * (L + 1) + i % L + 1] = l;
+    }
+    __syncthreads();
+    for (int m = tid; m < K; m += blockDim.x) {  // C_m(d), summed left to right in place
         double c = 0.0;
         cum[m * (L + 1)] = 0.0;
         for (int d = 1; d <= L; ++d) {
-            const double l = ws.lse[((int64_t)t * K + m) * L + d - 1];
-            if (l != l) s_bad = 1;
-            c = c + l;
+            c = c + cum[m * (L + 1) + d];
             cum[m * (L + 1) + d] = c;
         }
     }
@@ -376,11 +502,13 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const FEntry thr = s_thr;
             const bool thr_on = s_thr_on != 0;
             const int nslot = bn * k;
-            int written = 0;
-            for (int c0 = 0; c0 < nslot; c0 += blockDim.x) {
-                const int c = c0 + tid;
-                FEntry ch;
-                int ok = 0;
+            // at most 2 slots per thread (the plan keeps M * k <= 512), kept in
+            // slot order: thread tid owns slots 2 tid and 2 tid + 1
+            FEntry ch[2];
+            int okc[2] = {0, 0};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = 2 * tid + u;
                 if (c < nslot) {
                     const int i = c / k, r = c - i * k;
                     const FEntry e = F[fc][i];
@@ -388,31 +516,39 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                     if (d < L) {
                         const double z = e.zsum + ls.zlog(m, d + 1, r);
                         const double sv = z - ls.c(m, d + 1);
-                        ch.key = order_key(sv);
-                        ch.tb = ((unsigned long long)(d + 1) << 59) | ((unsigned long long)m << 56) |
-                                (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
-                        ch.zsum = z;
-                        ok = sv != -INFINITY && (!thr_on || before(ch, thr));
-                        if (ok) ch.hpar = entry_hash(ls, e);
+                        ch[u].key = order_key(sv);
+                        ch[u].tb = ((unsigned long long)(d + 1) << 59) |
+                                   ((unsigned long long)m << 56) |
+                                   (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
+                        ch[u].zsum = z;
+                        okc[u] = sv != -INFINITY && (!thr_on || before(ch[u], thr));
+                        // one mode: a prefix is named by its tie key, no hash needed
+                        ch[u].hpar = (okc[u] && K > 1) ? entry_hash(ls, e) : 0ull;
                     }
                 }
-                int tot;
-                const int pos = written + block_incl_scan_int(ok, red, &tot) - 1;
-                if (ok) S[pos] = ch;
-                written += tot;
             }
+            int written;
+            int pos = block_incl_scan_int(okc[0] + okc[1], red, &written) - (okc[0] + okc[1]);
+            if (okc[0]) S[pos++] = ch[0];
+            if (okc[1]) S[pos] = ch[1];
             if (tid == 0) s_nS = written;
             __syncthreads();
             const int nS = s_nS;
-            FEntry* Ssorted = S;
+            // the successors' order: sorted 64-bit codes (S itself stays put),
+            // or, after a long run of tied scores, S sorted in place
+            const unsigned long long* Sord = nullptr;
             if (nS > 1) {
                 const int n2S = pow2_at_least(nS < 32 ? 32 : nS);
-                for (int i = nS + tid; i < n2S; i += blockDim.x) {
-                    S[i].key = kSentinelKey;
-                    S[i].tb = ~0ull;
+                if (sort_order(S, nS, Scode, n2S, &red[31])) {
+                    Sord = Scode;
+                } else {
+                    for (int i = nS + tid; i < n2S; i += blockDim.x) {
+                        S[i].key = kSentinelKey;
+                        S[i].tb = ~0ull;
+                    }
+                    __syncthreads();
+                    sort_entries(S, n2S);
                 }
-                __syncthreads();
-                sort_entries(S, n2S);
             }
             if (nX + bn > plan.xcap || nF - bn + nS > plan.fcap) {  // cannot happen (see plan)
                 if (tid == 0) s_bad = 3;
@@ -421,8 +557,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             }
             // Taken entries join X (both sorted); the rest of the frontier
             // merges with the successors.
-            merge_entries(X[xc ^ 1], X[xc], nX, F[fc], bn);
-            merge_entries(F[fc ^ 1], F[fc] + bn, nF - bn, Ssorted, nS);
+            merge_two(X[xc ^ 1], X[xc], nX, F[fc], bn, F[fc ^ 1], F[fc] + bn, nF - bn, S, nS, Sord);
             xc ^= 1;
             fc ^= 1;
             int nXn = nX + bn, nFn = nF - bn + nS;
@@ -482,42 +617,40 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                 const FEntry th = X[xc][posB];
                 nXn = posB + 1;
                 // frontier entries not before the bound can never be kept
-                if (tid == 0) {
-                    int lo = 0, hi = nFn;
-                    while (lo < hi) {
-                        const int mid = (lo + hi) >> 1;
-                        if (before(F[fc][mid], th)) lo = mid + 1;
-                        else hi = mid;
+                if (tid < 32) {
+                    const FEntry* Fc = F[fc];
+                    const int lo = warp_first_false(0, nFn, [&](int i) { return before(Fc[i], th); });
+                    if (tid == 0) {
+                        s_nF = lo;
+                        s_thr = th;
+                        s_thr_on = 1;
                     }
-                    s_nF = lo;
-                    s_thr = th;
-                    s_thr_on = 1;
                 }
-            } else if (tid == 0) {
+            } else if (tid < 32) {
                 // the (K*B)-th entry of X and the frontier merged: at least B
                 // distinct prefixes are that good, so worse entries are dead
                 const int want = K * B;
                 int keepF = nFn;
                 if (nXn + nFn >= want) {
                     // co-rank: ia entries of X and want - ia of F form the best `want`
-                    int lo = max(0, want - nFn), hi = min(want, nXn);
-                    while (lo < hi) {
-                        const int mid = (lo + hi) >> 1;
-                        if (before(X[xc][mid], F[fc][want - mid - 1])) lo = mid + 1;
-                        else hi = mid;
-                    }
-                    const int ia = lo, ib = want - lo;
+                    const FEntry *Xc = X[xc], *Fc = F[fc];
+                    const int ia = warp_first_false(max(0, want - nFn), min(want, nXn), [&](int mid) {
+                        return before(Xc[mid], Fc[want - mid - 1]);
+                    });
+                    const int ib = want - ia;
                     // the want-th best is the worse of X[ia-1] and F[ib-1]
                     FEntry th;
                     if (ia == 0) th = F[fc][ib - 1];
                     else if (ib == 0) th = X[xc][ia - 1];
                     else th = before(X[xc][ia - 1], F[fc][ib - 1]) ? F[fc][ib - 1] : X[xc][ia - 1];
                     keepF = ib;  // F[ib..] are all after th
-                    s_thr = th;
-                    s_thr_on = 1;
+                    if (tid == 0) {
+                        s_thr = th;
+                        s_thr_on = 1;
+                    }
                     // th itself may be kept (not "before" itself); keep F entries up to it
                 }
-                s_nF = keepF;
+                if (tid == 0) s_nF = keepF;
             }
             if (tid == 0) {
                 s_nX = nXn;
@@ -546,12 +679,21 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             hval[i] = INT_MAX;
         }
         __syncthreads();
+        // key of a node's prefix: its tie key for one mode (exact), else the
+        // hash of its token sequence (matches confirmed by the tokens)
+        auto node_key = [&](const FEntry& e) {
+            return K == 1 ? e.tb : (entry_hash(ls, e) | 1ull);
+        };
+        auto first_bucket = [&](unsigned long long h) {
+            const unsigned long long x = hash_step(h, 0);
+            return (unsigned int)(x ^ (x >> 32)) & (plan.hcap - 1);
+        };
         for (int i = tid; i < nX; i += blockDim.x) {
             const int node = (K == 1) ? i + 1 : flag[plan.xcap + i] + 1;
             if (node <= 0) continue;
             const FEntry e = X[xc][i];
-            const unsigned long long h = entry_hash(ls, e) | 1ull;
-            unsigned int b = (unsigned int)(h ^ (h >> 32)) & (plan.hcap - 1);
+            const unsigned long long h = node_key(e);
+            unsigned int b = first_bucket(h);
             for (int probe = 0; probe < plan.hcap; ++probe, b = (b + 1) & (plan.hcap - 1)) {
                 const unsigned long long old = atomicCAS(&hkey[b], 0ull, h);
                 if (old == 0ull) {
@@ -578,15 +720,21 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const int d = tb_depth(e.tb);
             int pn = 0;
             if (d > 1) {
-                const unsigned long long h = e.hpar | 1ull;
-                unsigned int b = (unsigned int)(h ^ (h >> 32)) & (plan.hcap - 1);
+                // the parent's key: its tie key (this one without its last rank
+                // digit) for one mode, else the hash of its token sequence
+                const unsigned long long h =
+                    K == 1 ? (((unsigned long long)(d - 1) << 59) |
+                              ((unsigned long long)tb_mode(e.tb) << 56) | ((e.tb & kRsMask) >> bits))
+                           : (e.hpar | 1ull);
+                unsigned int b = first_bucket(h);
                 pn = -1;
                 for (int probe = 0; probe < plan.hcap; ++probe, b = (b + 1) & (plan.hcap - 1)) {
                     const unsigned long long kk = hkey[b];
                     if (kk == 0ull) break;
                     if (kk == h) {
                         const int j = hval[b];
-                        if (tb_depth(X[xc][j].tb) == d - 1 && same_tokens(ls, X[xc][j].tb, e.tb, d - 1)) {
+                        if (K == 1 || (tb_depth(X[xc][j].tb) == d - 1 &&
+                                       same_tokens(ls, X[xc][j].tb, e.tb, d - 1))) {
                             pn = (K == 1) ? j + 1 : flag[plan.xcap + j] + 1;
                             break;
                         }
