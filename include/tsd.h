@@ -15,8 +15,14 @@
  *
  * Conventions shared by every entry point:
  *   - Every array argument is DEVICE memory owned by the caller, contiguous and
- *     row-major in the shape given.  The library allocates nothing and keeps
- *     no state between calls.
+ *     row-major in the shape given, except the logits (drafter_logits,
+ *     target_logits), which may also be page-locked host memory
+ *     (cudaHostAlloc / cudaMallocHost / cudaHostRegister): the kernels then
+ *     read them in place over the host link, through the device address the
+ *     runtime maps for them.  Each call resolves the logits pointer with
+ *     cudaPointerGetAttributes; pageable host memory, or a pointer the runtime
+ *     does not know, is TSD_ERR_INVALID_ARG.  The library allocates nothing
+ *     and keeps no state between calls.
  *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
  *     host before anything is launched and returned at once; nothing is
  *     written in that case.  TSD_ERR_CUDA reports a launch failure.

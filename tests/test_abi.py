@@ -97,3 +97,15 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert st == tsd.TSD_ERR_INVALID_ARG  # mask_ld < P + B + 1
     st = lib.tsd_tree_mask(fake, fake, 1, 8, -1, fake, fake, None, 0, fake, None)
     assert st == tsd.TSD_ERR_INVALID_ARG
+
+
+def test_pageable_host_logits_are_refused(lib):
+    """Logits may live on the GPU or in page-locked host memory; ordinary
+    (pageable) host tensors are refused before any CUDA call."""
+    import torch
+    with pytest.raises(ValueError):
+        tsd.tsd_build_tree(torch.zeros(1, 1, 4, 32), topk=4, B=8)
+    with pytest.raises(ValueError):
+        tsd.tsd_verify_tev(torch.zeros(1, 9, 32), torch.zeros(1, 9, dtype=torch.int32),
+                           torch.zeros(1, 9, dtype=torch.int32), torch.ones(1, dtype=torch.int32),
+                           1.0, seed=0)

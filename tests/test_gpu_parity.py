@@ -532,3 +532,32 @@ def test_build_topk_selection_paths(tsd, dev, orc, dtype):
     out = tsd.tsd_build_tree(zs.to(dev), topk=8, B=40)
     ref, lists = oracle_build(orc, zs[0], 8, 40)
     assert compare_trees(_tree_np(out, 0), ref, lists) == 0
+
+
+def test_logits_in_pinned_host_memory(tsd, dev, orc):
+    """Drafter and target logits read straight from page-locked host memory
+    give the same trees and the same verification outputs as the same logits
+    in device memory."""
+    nt, V, B = 3, 20000, 24
+    seeds = [synth.seed_for(6, t) for t in range(nt)]
+    dr = synth.zipf_drafter(nt, 6, V, 0, device="cpu", seeds=seeds)
+    dr_h = dr.pin_memory()
+    tr_d = tsd.tsd_build_tree(dr.to(dev), topk=8, B=B)
+    tr_h = tsd.tsd_build_tree(dr_h, topk=8, B=B, device=dev)
+    for key in ("parent", "token", "depth", "score", "n_nodes", "status"):
+        assert torch.equal(tr_d[key], tr_h[key]), key
+    tgt = torch.zeros(nt, B + 1, V, dtype=torch.bfloat16)
+    for t in range(nt):
+        n = int(tr_d["n_nodes"][t])
+        tgt[t, :n] = synth.target_from_rows(dr[t, 0].float(), _np(tr_d["depth"][t, :n]), 1.5,
+                                            seeds[t] + 1)
+    tgt_h = tgt.pin_memory()
+    for T in (0.6, 0.0):
+        o_d = tsd.tsd_verify_tev(tgt.to(dev), tr_d["parent"], tr_d["token"], tr_d["n_nodes"], T, seed=5)
+        o_h = tsd.tsd_verify_tev(tgt_h, tr_d["parent"], tr_d["token"], tr_d["n_nodes"], T, seed=5)
+        for key in o_d:
+            assert torch.equal(o_d[key], o_h[key]), (T, key)
+        p_h = tsd.tsd_verify_ddtree(tgt_h, tr_d["parent"], tr_d["token"], tr_d["n_nodes"], T, seed=5)
+        p_d = tsd.tsd_verify_ddtree(tgt.to(dev), tr_d["parent"], tr_d["token"], tr_d["n_nodes"], T, seed=5)
+        for key in p_d:
+            assert torch.equal(p_d[key], p_h[key]), (T, key)

@@ -96,6 +96,17 @@ def _cuda(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
     return t
 
 
+def _logits(t: torch.Tensor, name: str) -> torch.Tensor:
+    """Logits may sit in device memory or in page-locked host memory, which
+    the kernels read directly over the host link (the library checks that the
+    host memory is mapped for the device)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+        raise ValueError("%s must be a CUDA tensor or a pinned (page-locked) CPU tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -113,15 +124,21 @@ def _workspace(nbytes: int, device, workspace):
 
 
 def tsd_build_tree(drafter_logits: torch.Tensor, topk: int, B: int, drafter_temp: float = 1.0,
-                   workspace=None) -> dict:
+                   workspace=None, device=None) -> dict:
     """Best-first tree builder.  drafter_logits: [n_trees, n_modes, L, V]
-    (bf16/fp32).  Returns parent, token, depth, score, rank, mode
-    ([n_trees, B+1]), n_nodes and status ([n_trees])."""
-    x = _cuda(drafter_logits, "drafter_logits")
+    (bf16/fp32), on the GPU or in pinned host memory (then the outputs go to
+    `device`, default the current CUDA device).  Returns parent, token,
+    depth, score, rank, mode ([n_trees, B+1]), n_nodes and status
+    ([n_trees])."""
+    x = _logits(drafter_logits, "drafter_logits")
     if x.dim() != 4:
         raise ValueError("drafter_logits must be [n_trees, n_modes, L, V]")
     n_trees, n_modes, L, V = x.shape
-    dev = x.device
+    if x.is_cuda:
+        dev = x.device
+    else:
+        dev = torch.device(device) if device is not None else \
+            torch.device("cuda", torch.cuda.current_device())
     i32 = dict(dtype=torch.int32, device=dev)
     out = {k: torch.empty(n_trees, B + 1, **i32) for k in ("parent", "token", "depth", "rank", "mode")}
     out["score"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
@@ -166,7 +183,7 @@ def tsd_tree_mask(parent: torch.Tensor, n_nodes: torch.Tensor, prefix_len: int =
 
 
 def _verify_common(target_logits, parent, token, n_nodes):
-    x = _cuda(target_logits, "target_logits")
+    x = _logits(target_logits, "target_logits")
     if x.dim() != 3:
         raise ValueError("target_logits must be [n_trees, B+1, V]")
     n_trees, Bp1, V = x.shape
@@ -176,6 +193,8 @@ def _verify_common(target_logits, parent, token, n_nodes):
     if tuple(parent.shape) != (n_trees, Bp1) or tuple(token.shape) != (n_trees, Bp1) \
             or tuple(n_nodes.shape) != (n_trees,):
         raise ValueError("parent/token must be [n_trees, B+1] and n_nodes [n_trees]")
+    if x.is_cuda and x.device != parent.device:
+        raise ValueError("target_logits and the tree must be on one device")
     return x, parent, token, n_nodes, n_trees, Bp1 - 1, V
 
 
@@ -210,7 +229,7 @@ def tsd_verify_tev_timed(target_logits: torch.Tensor, parent: torch.Tensor, toke
 def _tev(target_logits, parent, token, n_nodes, temperature, seed, workspace, with_masses, out,
          handles) -> dict:
     x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
-    dev = x.device
+    dev = parent.device
     i32 = dict(dtype=torch.int32, device=dev)
     if out is None:
         out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
@@ -245,7 +264,7 @@ def tsd_verify_tev_noalloc(target_logits: torch.Tensor, parent: torch.Tensor,
     The outputs are allocated here only because this binding returns new
     tensors."""
     x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
-    dev = x.device
+    dev = parent.device
     i32 = dict(dtype=torch.int32, device=dev)
     out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
     if with_masses:
@@ -269,7 +288,7 @@ def tsd_verify_ddtree(target_logits: torch.Tensor, parent: torch.Tensor, token: 
     """Predraw-and-follow.  Returns exit_node, bonus_token, accept_len, status
     ([n_trees]) and the per-node draws ([n_trees, B+1])."""
     x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
-    dev = x.device
+    dev = parent.device
     i32 = dict(dtype=torch.int32, device=dev)
     out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
     out["draws"] = torch.empty(n_trees, B + 1, **i32)

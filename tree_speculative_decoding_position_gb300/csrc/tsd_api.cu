@@ -72,6 +72,27 @@ bool verify_args_ok(const void* logits, tsd_dtype dtype, const int32_t* parent,
            V <= 0x7fffffff && temp_ok(temperature);
 }
 
+// The address through which the kernels read caller logits: device or
+// managed memory as given; page-locked host memory through its mapped device
+// address (the kernels then stream it over the host link).  Pageable host
+// memory, or a pointer the runtime does not know, is refused.
+bool logits_view(const void* p, const void** out) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of this query
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return true;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        *out = a.devicePointer;
+        return true;
+    }
+    return false;
+}
+
 }  // namespace
 
 size_t verify_ws_layout(int n_trees, int B, int64_t V, int esize, void* base, VerifyWs* out) {
@@ -168,6 +189,7 @@ tsd_status tsd_build_tree(const void* drafter_logits, tsd_dtype dtype, int n_tre
     const int es = dtype_size(dtype);
     const size_t need = build_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr);
     if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(drafter_logits, &drafter_logits)) return TSD_ERR_INVALID_ARG;
     BuildWs ws;
     build_ws_layout(n_trees, n_modes, L, V, topk, B, es, workspace, &ws);
     const int64_t rows = (int64_t)n_trees * n_modes * L;
@@ -208,6 +230,7 @@ static tsd_status verify_tev_impl(const void* target_logits, tsd_dtype dtype,
     const int es = dtype_size(dtype);
     const size_t need = verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
     if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(target_logits, &target_logits)) return TSD_ERR_INVALID_ARG;
     VerifyWs ws;
     verify_ws_layout(n_trees, B, V, es, workspace, &ws);
     const bool greedy = temperature == 0.0f;
@@ -267,6 +290,7 @@ tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const i
     const int es = dtype_size(dtype);
     const size_t need = verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
     if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(target_logits, &target_logits)) return TSD_ERR_INVALID_ARG;
     VerifyWs ws;
     verify_ws_layout(n_trees, B, V, es, workspace, &ws);
     const bool greedy = temperature == 0.0f;
