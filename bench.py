@@ -329,13 +329,13 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         e.record(stream)
         torch.cuda.synchronize()
         out["verifier_ms_b256_x32_" + name] = s.elapsed_time(e) / 10
-    # batch-1 round, V=151936, B=64, T=1: 16 rotating copies (316 MB > 2x L2)
+    # batch-1 round, V=151936, B=64, T=1: 32 rotating copies (632 MB > 4x L2)
     B1 = 64
     dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device=dev)
     t1 = tsd.tsd_build_tree(dr, topk=8, B=B1)
     n = int(t1["n_nodes"][0])
     copies = []
-    for c in range(16):
+    for c in range(32):
         x = torch.zeros(1, B1 + 1, V, dtype=torch.bfloat16, device=dev)
         synth.target_from_rows(dr[0, 0], t1["depth"][0, :n], 1.5, synth.seed_for(1, 1) + c,
                                out=x[0, :n])
@@ -347,12 +347,12 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         for e in ev:
             e.record(stream)
     for i in range(8):
-        tsd.tsd_verify_tev(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
+        tsd.tsd_verify_tev(copies[i % 32], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
                            seed=i, workspace=ws1)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
     for i in range(48):
-        tsd.tsd_verify_tev_timed(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
+        tsd.tsd_verify_tev_timed(copies[i % 32], t1["parent"], t1["token"], t1["n_nodes"], 1.0,
                                  seed=i, stage_events=evs[i], workspace=ws1)
     e.record(stream)
     torch.cuda.synchronize()
@@ -364,12 +364,48 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
     # the same round, greedy (T = 0)
     s.record(stream)
     for i in range(48):
-        tsd.tsd_verify_tev(copies[i % 16], t1["parent"], t1["token"], t1["n_nodes"], 0.0,
+        tsd.tsd_verify_tev(copies[i % 32], t1["parent"], t1["token"], t1["n_nodes"], 0.0,
                            seed=i, workspace=ws1)
     e.record(stream)
     torch.cuda.synchronize()
     out["b64_single_tree"]["tev_ms_T0"] = s.elapsed_time(e) / 48
-    del copies
+    # the same round as a decode loop would issue it: build + mask + TEV captured
+    # once in a CUDA graph and replayed (GPU latency without the Python calls),
+    # L2 flushed before every replay
+    ws1b = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 1, 1, 16, V, 8, B1,
+                                              torch.bfloat16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
+                        dtype=torch.float32, device=dev)
+
+    def round1(i):
+        t_ = tsd.tsd_build_tree(dr, topk=8, B=B1, workspace=ws1b)
+        tsd.tsd_tree_mask(t_["parent"], t_["n_nodes"], prefix_len=1024)
+        return tsd.tsd_verify_tev(copies[0], t_["parent"], t_["token"], t_["n_nodes"], 1.0,
+                                  seed=i, workspace=ws1)
+
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for i in range(3):
+            round1(i)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        round1(0)
+    lat = []
+    for i in range(45):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            lat.append(a.elapsed_time(b))
+    out["b64_single_tree"]["round_graph_ms"] = statistics.median(lat)
+    out["b64_single_tree"]["round_graph_ms_best"] = min(lat)
+    del copies, graph
     # mixture-of-futures workload: 16 trees, K = 8 modes from two latent
     # futures, B = 128; the mixture builder, then TEV at T = 1 on its trees
     nt_m, K_m, B_m = 16, 8, 128
@@ -408,16 +444,27 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
 
 def run_sweep(args):
     """TEV throughput over B x trees x T (V = 151936, bf16): one JSON table
-    written to --sweep-out.  Trees come from the GPU builder on zipf drafter
-    logits; target rows are the drafter row at node depth + N(0, 1.5^2)."""
+    written to --sweep-out.  Trees come from the GPU builder on Zipf drafter
+    logits; target rows are the drafter row at node depth + N(0, 1.5^2).
+    Per point: 10 warm-up launches, then 50 timed ones, each bracketed by
+    CUDA events (median and best reported); when the point's logits are
+    under 4x the L2 size, a 2x-L2 write flushes L2 before every launch.  At
+    the points with at most 8 trees the float64 oracle is timed on every
+    tree, single-threaded on the host."""
+    import numpy as np
     import torch
 
+    import oracle
     import synth
     import tree_speculative_decoding_position_gb300 as tsd
+    oracle.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
     V, L = 151936, 16
+    peak = measured_peaks()[0]
     rows = []
     for B in (16, 64, 256, 512):
         for nt in (1, 8, 64, 256):
@@ -437,59 +484,102 @@ def run_sweep(args):
             ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, nt, 1, 1, V, 1, B,
                                                     torch.bfloat16), dtype=torch.uint8, device=dev)
             nbytes = int(tr["n_nodes"].sum()) * V * 2
-            reps = max(3, min(50, int(4e9 // max(nbytes, 1))))
+            small = nbytes < 4 * l2
+            host = None
+            if nt <= 8:  # the oracle's inputs, copied once
+                host = [(x[t, :int(tr["n_nodes"][t])].float().cpu().numpy().astype(np.float64),
+                         tr["parent"][t].cpu().numpy(), tr["token"][t].cpu().numpy(),
+                         int(tr["n_nodes"][t])) for t in range(nt)]
             for T in (0.0, 0.6, 1.0):
-                for i in range(3):
+                for i in range(10):
                     tsd.tsd_verify_tev(x, tr["parent"], tr["token"], tr["n_nodes"], T, seed=i,
                                        workspace=ws, with_masses=False)
-                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps)]
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(50)]
                 for ev in evs:
                     for e_ in ev:
                         e_.record(stream)
                 torch.cuda.synchronize()
-                for i in range(reps):
+                for i in range(50):
+                    if small:
+                        flush.fill_(float(i))
                     tsd.tsd_verify_tev_timed(x, tr["parent"], tr["token"], tr["n_nodes"], T,
                                              seed=i, stage_events=evs[i], workspace=ws,
                                              with_masses=False)
                 torch.cuda.synchronize()
-                tot = statistics.mean(ev[0].elapsed_time(ev[4]) for ev in evs)
-                rk = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
-                rows.append(dict(B=B, trees=nt, T=T, tev_ms=tot, rounds_per_s=nt / (tot * 1e-3),
-                                 rows_kernel_gbs=nbytes / (rk * 1e-3) / 1e9,
-                                 rows_frac_of_measured=nbytes / (rk * 1e-3) / 1e9 / measured_peaks()[0],
-                                 logits_gb=nbytes / 1e9, reps=reps))
-            del x, ws, tr
+                tot = [ev[0].elapsed_time(ev[4]) for ev in evs]
+                rk = [ev[1].elapsed_time(ev[2]) for ev in evs]
+                med, best, rmed = statistics.median(tot), min(tot), statistics.median(rk)
+                pt = dict(B=B, trees=nt, T=T, tev_ms=med, tev_ms_best=best,
+                          rounds_per_s=nt / (med * 1e-3), rounds_per_s_best=nt / (best * 1e-3),
+                          rows_kernel_ms=rmed, rows_kernel_gbs=nbytes / (rmed * 1e-3) / 1e9,
+                          rows_frac_of_measured=nbytes / (rmed * 1e-3) / 1e9 / peak,
+                          logits_gb=nbytes / 1e9, launches=50,
+                          l2="flushed before each launch" if small else "inputs >= 4x L2")
+                if host is not None:
+                    t0 = time.perf_counter()
+                    for t, (z, par, tok, n) in enumerate(host):
+                        oracle.tev(z, par, tok, n, T, seed=0, tree=t)
+                    o_s = time.perf_counter() - t0
+                    pt.update(oracle_ms_per_tree=1e3 * o_s / nt, oracle_rounds_per_s=nt / o_s,
+                              oracle_threads=1, gpu_over_oracle=(nt / (med * 1e-3)) / (nt / o_s))
+                rows.append(pt)
+            del x, ws, tr, host
             torch.cuda.empty_cache()
     with open(args.sweep_out, "w") as f:
         json.dump(rows, f, indent=1)
     print(json.dumps({"sweep_points": len(rows), "out": args.sweep_out}))
 
 
-def cpu_baseline(drafter, target, tree, k, B, T, budget_s=12.0):
-    """The float64 oracle as it stands, single-threaded on the host, on a
-    bounded sample of the same workload: whole trees (drafter statistics,
-    heap, mask, TEV) until about budget_s seconds of CPU work."""
-    import numpy as np
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_round(oracle, z, tg, k, B, T, t):
+    """One round of the workload in the float64 oracle: drafter statistics and
+    heap, mask, TEV.  z: [L, V] drafter logits, tg: [n, V] target rows."""
+    ref = oracle.build_tree(oracle.drafter_lists(z, 1.0, k), B)
+    oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
+    oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+
+
+def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0):
+    """The float64 oracle as it stands on the host, on a bounded sample of the
+    same workload (whole rounds: drafter statistics, heap, mask, TEV): first
+    single-threaded, then with one thread per host core over trees (the
+    oracle's C code runs outside the interpreter lock).  About budget_s
+    seconds each."""
+    from concurrent.futures import ThreadPoolExecutor
 
     import oracle
     oracle.build()
     nt = drafter.shape[0]
+    inputs = []
+    for t in range(nt):
+        n = int(tree["n_nodes"][t])
+        inputs.append((drafter[t, 0].float().cpu().numpy(), target[t, :n].float().cpu().numpy()))
     done, spent = 0, 0.0
     for t in range(nt):
-        dr = drafter[t, 0].float().cpu().numpy()
-        n = int(tree["n_nodes"][t])
-        tg = target[t, :n].float().cpu().numpy()
         t0 = time.perf_counter()
-        ref = oracle.build_tree(oracle.drafter_lists(dr, 1.0, k), B)
-        oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
-        oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+        oracle_round(oracle, *inputs[t], k, B, T, t)
         spent += time.perf_counter() - t0
         done += 1
         if spent >= budget_s:
             break
-    return {"value": done / spent, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of the %d trees of one step (build + mask + TEV per tree), "
-                      "float64, single thread, %.1f s" % (done, nt, spent)}
+    single = {"value": done / spent, "cores": 1,
+              "sample": "%d of the %d trees of one step, %.1f s" % (done, nt, spent)}
+    nth = host_threads()
+    n_rounds = max(nth, int(round(budget_s * single["value"] * nth)))
+    with ThreadPoolExecutor(max_workers=nth) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(lambda t: oracle_round(oracle, *inputs[t % nt], k, B, T, t), range(n_rounds)))
+        wall = time.perf_counter() - t0
+    return {"value": n_rounds / wall, "unit": "rounds/s", "cores": nth, "kind": "oracle",
+            "sample": "%d rounds over the workload's %d trees (build + mask + TEV per tree), "
+                      "float64, %d threads over trees, %.1f s wall" % (n_rounds, nt, nth, wall),
+            "single_thread": single}
 
 
 # ---------------------------------------------------------------------------
@@ -520,26 +610,32 @@ def run_reference(args):
             cache[t] = (dr.float().numpy(), tg)
         return cache[t]
 
-    def one_tree(t):
-        z, tg = inputs(t % 4)
+    from concurrent.futures import ThreadPoolExecutor
+    nth = host_threads()
+    for t in range(4):
+        inputs(t)  # generated before any timing
+
+    def step(i):
+        """One step: `nth` rounds of the workload, one tree per host thread."""
         t0 = time.perf_counter()
-        ref = oracle.build_tree(oracle.drafter_lists(z, 1.0, k), B)
-        oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
-        oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+        list(pool.map(lambda j: oracle_round(oracle, *inputs((i * nth + j) % 4), k, B, T, j),
+                      range(nth)))
         return time.perf_counter() - t0
 
-    for i in range(args.warmup):
-        one_tree(i % nt)
-    spent = sum(one_tree((args.warmup + i) % nt) for i in range(args.steps))
-    value = args.steps / spent
+    with ThreadPoolExecutor(max_workers=nth) as pool:
+        for i in range(args.warmup):
+            step(i)
+        spent = sum(step(args.warmup + i) for i in range(args.steps))
+    value = args.steps * nth / spent
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * spent / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": dict(W, parallelism="host cores, one thread"),
-        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-                         "sample": "one tree of the workload per step (build + mask + TEV; four "
-                                   "trees' inputs in rotation), float64 oracle, single thread"},
+        "data": "synthetic",
+        "config": dict(W, parallelism="host cores: %d threads, one tree each per step" % nth),
+        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": nth, "kind": "oracle",
+                         "sample": "%d trees per step, one per host thread (build + mask + TEV; "
+                                   "four trees' inputs in rotation), float64 oracle" % nth},
         "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

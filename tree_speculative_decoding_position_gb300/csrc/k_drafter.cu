@@ -73,6 +73,7 @@ template <typename T>
 __global__ void __launch_bounds__(kDThreads)
 drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, float c,
                      bool vec_ok, BuildWs ws) {
+    pdl_entry();
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     constexpr int VEC = Lanes<T>::kVec;
     const int lane = threadIdx.x & (kWarp - 1);
@@ -204,6 +205,7 @@ template <typename T>
 __global__ void __launch_bounds__(kRThreads)
 drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, int k, float c,
                    double temp, bool vec_ok, BuildWs ws) {
+    pdl_entry();
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     constexpr int VEC = Lanes<T>::kVec;
     __shared__ float cm[kMaxDrafterChunks];
@@ -377,17 +379,17 @@ cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t ro
     if (dtype == TSD_BF16) {
         const auto* p = static_cast<const __nv_bfloat16*>(logits);
         auto kc = drafter_chunk_kernel<__nv_bfloat16>;
-        kc<<<resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream>>>(
-            p, rows, V, nch, c, vec_ok, ws);
-        drafter_row_kernel<__nv_bfloat16><<<(unsigned)rows, kRThreads, 0, stream>>>(
-            p, rows, V, nch, topk, c, temp, vec_ok, ws);
+        if (cudaError_t e_ = launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream, 
+            p, rows, V, nch, c, vec_ok, ws); e_ != cudaSuccess) return e_;
+        if (cudaError_t e_ = launch_pdl(drafter_row_kernel<__nv_bfloat16>, (unsigned)rows, kRThreads, 0, stream, 
+            p, rows, V, nch, topk, c, temp, vec_ok, ws); e_ != cudaSuccess) return e_;
     } else {
         const auto* p = static_cast<const float*>(logits);
         auto kc = drafter_chunk_kernel<float>;
-        kc<<<resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream>>>(
-            p, rows, V, nch, c, vec_ok, ws);
-        drafter_row_kernel<float><<<(unsigned)rows, kRThreads, 0, stream>>>(
-            p, rows, V, nch, topk, c, temp, vec_ok, ws);
+        if (cudaError_t e_ = launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream, 
+            p, rows, V, nch, c, vec_ok, ws); e_ != cudaSuccess) return e_;
+        if (cudaError_t e_ = launch_pdl(drafter_row_kernel<float>, (unsigned)rows, kRThreads, 0, stream, 
+            p, rows, V, nch, topk, c, temp, vec_ok, ws); e_ != cudaSuccess) return e_;
     }
     return cudaGetLastError();
 }

@@ -404,6 +404,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                   int32_t* __restrict__ depth, float* __restrict__ score,
                   int32_t* __restrict__ rank, int32_t* __restrict__ mode,
                   int32_t* __restrict__ n_nodes_out, int32_t* __restrict__ status) {
+    pdl_entry();
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_bad, s_nF, s_nX, s_nS, s_D, s_posB, s_thr_on;
     __shared__ FEntry s_thr;  // pruning bound: entries not before it are dead
@@ -779,8 +780,8 @@ cudaError_t launch_build_heap(const BuildWs& ws, int n_trees, int n_modes, int L
     if (e != cudaSuccess) return e;
     int bits = 0;
     while ((1 << bits) < topk) ++bits;
-    build_tree_kernel<<<n_trees, kBuildThreads, p.smem_total, stream>>>(
-        ws, p, n_modes, L, topk, B, bits, parent, token, depth, score, rank, mode, n_nodes, status);
+    if (cudaError_t e_ = launch_pdl(build_tree_kernel, n_trees, kBuildThreads, p.smem_total, stream, 
+        ws, p, n_modes, L, topk, B, bits, parent, token, depth, score, rank, mode, n_nodes, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
 

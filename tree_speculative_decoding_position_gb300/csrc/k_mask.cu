@@ -19,6 +19,7 @@ tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__
                  int prefix_len, uint32_t* __restrict__ anc_bits,
                  int32_t* __restrict__ position_ids, float* __restrict__ additive_mask,
                  int64_t mask_ld, int32_t* __restrict__ status) {
+    pdl_entry();
     __shared__ int bad;
     const int t = blockIdx.x;
     const int stride = B + 1;
@@ -82,9 +83,9 @@ cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int 
                              int prefix_len, uint32_t* anc_bits, int32_t* position_ids,
                              float* additive_mask, int64_t mask_ld, int32_t* status,
                              cudaStream_t stream) {
-    tree_mask_kernel<<<n_trees, kMaskThreads, 0, stream>>>(parent, n_nodes, B, prefix_len,
+    if (cudaError_t e_ = launch_pdl(tree_mask_kernel, n_trees, kMaskThreads, 0, stream, parent, n_nodes, B, prefix_len,
                                                            anc_bits, position_ids, additive_mask,
-                                                           mask_ld, status);
+                                                           mask_ld, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
 

@@ -86,7 +86,9 @@ __device__ void block_bitonic_sort(uint64_t* keys, int n2) {
 __global__ void __launch_bounds__(kPrepThreads)
 verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
                    const int32_t* __restrict__ n_nodes, int B, int64_t V, VerifyWs ws) {
+    pdl_entry();
     __shared__ uint64_t keys[kPrepMaxKeys];
+    __shared__ int16_t spar[kPrepMaxKeys];  // parents, for the depth walks on chip
     __shared__ int bad;
     const int t = blockIdx.x;
     const int32_t* par = parent + (int64_t)t * (B + 1);
@@ -104,6 +106,7 @@ verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
             const int u = i + 1, p = par[u], x = tok[u];
             if (p < 0 || p >= u || x < 0 || (int64_t)x >= V) bad = 1;
             else key = child_key(p, x, u);
+            spar[u] = (int16_t)p;
         }
         keys[i] = key;
     }
@@ -139,7 +142,7 @@ verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
     for (int u = threadIdx.x; u < nn; u += blockDim.x) {
         int d = 0, x = u;
         while (x > 0) {  // parents precede children, so this ends within u steps
-            x = par[x];
+            x = spar[x];
             ++d;
         }
         dep[u] = d;
@@ -149,7 +152,7 @@ verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
 cudaError_t launch_verify_prep(const int32_t* parent, const int32_t* token, const int32_t* n_nodes,
                                int n_trees, int B, int64_t V, const VerifyWs& ws,
                                cudaStream_t stream) {
-    verify_prep_kernel<<<n_trees, kPrepThreads, 0, stream>>>(parent, token, n_nodes, B, V, ws);
+    if (cudaError_t e_ = launch_pdl(verify_prep_kernel, n_trees, kPrepThreads, 0, stream, parent, token, n_nodes, B, V, ws); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
 
@@ -409,6 +412,7 @@ template <typename T, bool GREEDY>
 __global__ void __launch_bounds__(kRowThreads)
 rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
             bool vec_ok, const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    pdl_entry();
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     const int lane = threadIdx.x & (kWarp - 1);
     const int wpb = blockDim.x / kWarp;
@@ -500,16 +504,18 @@ cudaError_t launch_rows(const void* logits, tsd_dtype dtype, int n_trees, int B,
     const int grid = row_grid((int64_t)n_trees * (B + 1) * nch);
     if (dtype == TSD_BF16) {
         const auto* p = static_cast<const __nv_bfloat16*>(logits);
-        if (greedy)
-            rows_kernel<__nv_bfloat16, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
-        else
-            rows_kernel<__nv_bfloat16, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+        if (greedy) {
+            if (cudaError_t e_ = launch_pdl(rows_kernel<__nv_bfloat16, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
+        } else {
+            if (cudaError_t e_ = launch_pdl(rows_kernel<__nv_bfloat16, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
+        }
     } else {
         const auto* p = static_cast<const float*>(logits);
-        if (greedy)
-            rows_kernel<float, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
-        else
-            rows_kernel<float, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws);
+        if (greedy) {
+            if (cudaError_t e_ = launch_pdl(rows_kernel<float, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
+        } else {
+            if (cudaError_t e_ = launch_pdl(rows_kernel<float, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
+        }
     }
     return cudaGetLastError();
 }
@@ -521,6 +527,7 @@ template <typename T, bool GREEDY>
 __global__ void __launch_bounds__(kRowThreads)
 node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
                     const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    pdl_entry();
     const int lane = threadIdx.x & (kWarp - 1);
     const int wpb = blockDim.x / kWarp;
     const int64_t rows = (int64_t)n_trees * (B + 1);
@@ -608,16 +615,18 @@ cudaError_t launch_node_combine(const void* logits, tsd_dtype dtype, int n_trees
     const int grid = row_grid((int64_t)n_trees * (B + 1));
     if (dtype == TSD_BF16) {
         const auto* p = static_cast<const __nv_bfloat16*>(logits);
-        if (greedy)
-            node_combine_kernel<__nv_bfloat16, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
-        else
-            node_combine_kernel<__nv_bfloat16, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+        if (greedy) {
+            if (cudaError_t e_ = launch_pdl(node_combine_kernel<__nv_bfloat16, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, n_nodes, ws); e_ != cudaSuccess) return e_;
+        } else {
+            if (cudaError_t e_ = launch_pdl(node_combine_kernel<__nv_bfloat16, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, n_nodes, ws); e_ != cudaSuccess) return e_;
+        }
     } else {
         const auto* p = static_cast<const float*>(logits);
-        if (greedy)
-            node_combine_kernel<float, true><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
-        else
-            node_combine_kernel<float, false><<<grid, kRowThreads, 0, stream>>>(p, n_trees, B, V, nch, c, n_nodes, ws);
+        if (greedy) {
+            if (cudaError_t e_ = launch_pdl(node_combine_kernel<float, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, n_nodes, ws); e_ != cudaSuccess) return e_;
+        } else {
+            if (cudaError_t e_ = launch_pdl(node_combine_kernel<float, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, n_nodes, ws); e_ != cudaSuccess) return e_;
+        }
     }
     return cudaGetLastError();
 }

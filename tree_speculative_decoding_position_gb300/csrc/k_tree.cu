@@ -95,6 +95,7 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
                 int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
                 float* __restrict__ exit_mass, float* __restrict__ prefix_prob,
                 float* __restrict__ coverage, int32_t* __restrict__ status) {
+    pdl_entry();
     extern __shared__ float sh[];  // w[B+1], pedge[B+1], and parents as int[B+1]
     __shared__ float red[33];
     __shared__ int pick[2];
@@ -258,14 +259,15 @@ cudaError_t launch_tev_tree(const void* logits, tsd_dtype dtype, int n_trees, in
                                                            : (const void*)tev_tree_kernel<float>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dtype == TSD_BF16)
-        tev_tree_kernel<__nv_bfloat16><<<n_trees, kTreeThreads, smem, stream>>>(
+    if (dtype == TSD_BF16) {
+        if (cudaError_t e_ = launch_pdl(tev_tree_kernel<__nv_bfloat16>, n_trees, kTreeThreads, smem, stream, 
             static_cast<const __nv_bfloat16*>(logits), B, V, nch, c, greedy, seed, parent, n_nodes,
-            ws, exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status);
-    else
-        tev_tree_kernel<float><<<n_trees, kTreeThreads, smem, stream>>>(
+            ws, exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status); e_ != cudaSuccess) return e_;
+    } else {
+        if (cudaError_t e_ = launch_pdl(tev_tree_kernel<float>, n_trees, kTreeThreads, smem, stream, 
             static_cast<const float*>(logits), B, V, nch, c, greedy, seed, parent, n_nodes, ws,
-            exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status);
+            exit_node, bonus, accept_len, exit_mass, prefix_prob, coverage, status); e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 
@@ -279,6 +281,7 @@ template <typename T>
 __global__ void __launch_bounds__(kDrawThreads)
 predraw_nodes_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
                      bool greedy, uint64_t seed, const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+    pdl_entry();
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     constexpr int PER = CE / kWarp;  // tokens per lane in one chunk (128 bf16, 64 fp32)
     const int lane = threadIdx.x & (kWarp - 1);
@@ -366,6 +369,7 @@ __global__ void predraw_walk_kernel(int n_trees, int B, const int32_t* __restric
                                     VerifyWs ws, int32_t* __restrict__ exit_node,
                                     int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
                                     int32_t* __restrict__ draws, int32_t* __restrict__ status) {
+    pdl_entry();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n_trees) return;
     const int stride = B + 1;
@@ -413,16 +417,17 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
     const int wpb = kDrawThreads / kWarp;
     const int64_t want = (rows + wpb - 1) / wpb;
     const int grid = (int)(want < 65535 * 8 ? want : 65535 * 8);
-    if (dtype == TSD_BF16)
-        predraw_nodes_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws);
-    else
-        predraw_nodes_kernel<float><<<grid, kDrawThreads, 0, stream>>>(
-            static_cast<const float*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws);
+    if (dtype == TSD_BF16) {
+        if (cudaError_t e_ = launch_pdl(predraw_nodes_kernel<__nv_bfloat16>, grid, kDrawThreads, 0, stream, 
+            static_cast<const __nv_bfloat16*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws); e_ != cudaSuccess) return e_;
+    } else {
+        if (cudaError_t e_ = launch_pdl(predraw_nodes_kernel<float>, grid, kDrawThreads, 0, stream, 
+            static_cast<const float*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws); e_ != cudaSuccess) return e_;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    predraw_walk_kernel<<<(n_trees + 127) / 128, 128, 0, stream>>>(n_trees, B, n_nodes, ws, exit_node,
-                                                                 bonus, accept_len, draws, status);
+    if (cudaError_t e_ = launch_pdl(predraw_walk_kernel, (n_trees + 127) / 128, 128, 0, stream, n_trees, B, n_nodes, ws, exit_node,
+                                                                 bonus, accept_len, draws, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
 

@@ -91,6 +91,20 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization (launch_pdl below): it may be
+// scheduled while the previous kernel in the stream is still finishing, and
+// its first statement is pdl_entry(), which lets the next kernel be scheduled
+// as early and then waits until the previous kernel has completed and its
+// memory is visible.  No global memory is touched before that wait, so the
+// stream's ordering is unchanged; only launch latency is hidden.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_entry() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // MUFU base-2 exponential (ex2.approx.ftz: about 2 ulp).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -295,6 +309,22 @@ cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int 
                              int prefix_len, uint32_t* anc_bits, int32_t* position_ids,
                              float* additive_mask, int64_t mask_ld, int32_t* status,
                              cudaStream_t stream);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Grid for a persistent (grid-stride) kernel: min(want, SMs x the CTAs of
 // `kernel` resident per SM at this block size and dynamic shared memory), at
