@@ -55,7 +55,8 @@ def _load():
         lib.orc_predraw.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P, P]
         lib.orc_tev_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_predraw_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
-        for f in ("orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
+        lib.orc_exit_loss.argtypes = [P, i32, i64, f64, P, P, i32, P, P, P]
+        for f in ("orc_exit_loss", "orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
                   "orc_tev", "orc_predraw", "orc_tev_sample_many", "orc_predraw_sample_many"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -215,3 +216,17 @@ def sample_many(kind: str, z, parent, token, n_nodes: int, T: float, seed: int, 
     _check(fn(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, seed, first_tree, n_draws,
               _ptr(ex), _ptr(bo)), kind + "_sample_many")
     return ex, bo
+
+
+def exit_loss(z, T: float, token, depth, n_nodes: int, omega, with_grad: bool = False):
+    """Exit-guided loss numerator of one example ([EXIT] Eq. 14 / 66) and,
+    optionally, its gradient with respect to the drafter logits z [L, V]."""
+    z = _f64(z)
+    L, V = z.shape
+    token, depth = _i32(token), _i32(depth)
+    omega = _f64(omega)
+    num = np.zeros(1)
+    grad = np.zeros((L, V)) if with_grad else None
+    _check(_load().orc_exit_loss(_ptr(z), L, V, T, _ptr(token), _ptr(depth), n_nodes, _ptr(omega),
+                                 _ptr(num), _ptr(grad) if grad is not None else None), "exit_loss")
+    return (float(num[0]), grad) if with_grad else float(num[0])

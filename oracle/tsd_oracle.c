@@ -16,6 +16,7 @@
  *           -- Sec. 2 Eq. 1 (plug-in score), Thm. 1 (tie order), App. C
  *           "Candidate construction" (top-K heap, push all K children) and
  *           "Packed verification" (ancestor mask, position ids).
+ *           Sec. 5 Eq. 14 and App. C.2 Eq. 66 (the exit-guided loss).
  *   [MFD]   "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
  *           Speculative Decoding" -- Sec. 3.4 Eq. 2 (best-mode score),
  *           App. B "Merged heap" and Prop. 6 (sibling / first-child pushes,
@@ -593,4 +594,48 @@ int orc_predraw_sample_many(const double *z, const int32_t *parent, const int32_
                          exit_out + i, bonus_out + i, &al);
     free(draws);
     return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exit-guided loss [EXIT Sec. 5 Eq. 14, App. C.2 Eq. 66], one example.      */
+/* The numerator of Eq. 14: the sum over non-root nodes v of                 */
+/*   omega(v) * (-log q_{depth(v)}(x_v)),                                    */
+/* where x_v is scored by the drafter row of future position depth(v)        */
+/* (row depth(v) - 1 of z) and log q = z/T_d - logsumexp(z/T_d) over the     */
+/* row.  Every node's term is formed on its own, as Eq. 66 writes it (not    */
+/* through the per-row regrouping of Eq. 67).                                */
+/*   z: [L][V] drafter logits; token, depth: [n] (node 0 is the root and     */
+/*   is skipped); omega: [n] detached weights (the exit masses w(v)).        */
+/*   *num: the numerator.  grad (nullable): [L][V] d(num)/dz, i.e.           */
+/*   sum over nodes v on row m of omega(v) (softmax(z_m/T)(a) - [a = x_v])/T. */
+/* ------------------------------------------------------------------------ */
+int orc_exit_loss(const double *z, int L, int64_t V, double T, const int32_t *token,
+                  const int32_t *depth, int n, const double *omega, double *num, double *grad)
+{
+    if (L < 1 || V < 1 || n < 1 || !(T > 0.0)) return ORC_ERR_ARG;
+    for (int v = 1; v < n; ++v)
+        if (depth[v] < 1 || depth[v] > L || token[v] < 0 || (int64_t)token[v] >= V)
+            return ORC_ERR_BAD_TREE;
+    if (grad) memset(grad, 0, sizeof(double) * (size_t)L * (size_t)V);
+    double total = 0.0;
+    for (int v = 1; v < n; ++v) {
+        const double *row = z + (int64_t)(depth[v] - 1) * V;
+        double m = -INFINITY;
+        for (int64_t a = 0; a < V; ++a)
+            if (row[a] / T > m) m = row[a] / T;
+        if (!isfinite(m)) return ORC_ERR_NONFINITE;
+        double s = 0.0;
+        for (int64_t a = 0; a < V; ++a) s += exp(row[a] / T - m);
+        const double lse = m + log(s);
+        const double nlq = lse - row[token[v]] / T; /* -log q_{depth(v)}(x_v) */
+        if (!isfinite(nlq)) return ORC_ERR_NONFINITE;
+        total += omega[v] * nlq;
+        if (grad) {
+            double *g = grad + (int64_t)(depth[v] - 1) * V;
+            for (int64_t a = 0; a < V; ++a) g[a] += omega[v] * exp(row[a] / T - lse) / T;
+            g[token[v]] -= omega[v] / T;
+        }
+    }
+    *num = total;
+    return ORC_OK;
 }

@@ -613,3 +613,79 @@ def test_draws_are_inverse_cdf_of_the_stated_uniforms(orc, T):
         for v in range(n):
             cp = np.cumsum(probs[v])
             assert d["draws"][v] == int(np.argmax(cp > _numpy_uniform(5, tree, v, 2) * cp[-1]))
+
+
+# ---------------------------------------------------------------------------
+# Exit-guided loss ([EXIT] Sec. 5 Eq. 14, App. C.2 Eq. 66)
+# ---------------------------------------------------------------------------
+def _exit_loss_case(seed, L=4, V=50, n=12):
+    rng = np.random.default_rng(seed)
+    z = rng.normal(0, 2, size=(L, V))
+    depth = np.zeros(n, dtype=np.int32)
+    token = np.full(n, -1, dtype=np.int32)
+    for v in range(1, n):
+        depth[v] = int(rng.integers(1, L + 1))
+        token[v] = int(rng.integers(0, V))
+    omega = rng.random(n)
+    return z, token, depth, omega
+
+
+def test_exit_loss_hand_fixture(orc):
+    g = json.load(open(os.path.join(GOLDEN, "exit_loss_hand.json")))
+    num, grad = orc.exit_loss(np.array(g["z"]), g["T"], g["token"], g["depth"], len(g["token"]),
+                              g["omega"], with_grad=True)
+    assert num == pytest.approx(g["numerator"], rel=1e-14)
+    assert np.allclose(grad, np.array(g["grad"]), rtol=1e-13, atol=1e-15)
+
+
+def test_exit_loss_constant_rows_cost_log_V(orc):
+    """Every token equally likely: -log q = log V at every node."""
+    z, token, depth, omega = _exit_loss_case(3)
+    z[:] = 1.7
+    num = orc.exit_loss(z, 0.8, token, depth, len(token), omega)
+    assert num == pytest.approx(np.log(z.shape[1]) * omega[1:].sum(), rel=1e-12)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7, 2.5])
+def test_exit_loss_matches_library_log_softmax(orc, T):
+    from scipy.special import log_softmax
+    z, token, depth, omega = _exit_loss_case(5)
+    want = -sum(omega[v] * log_softmax(z[depth[v] - 1] / T)[token[v]] for v in range(1, len(token)))
+    assert orc.exit_loss(z, T, token, depth, len(token), omega) == pytest.approx(want, rel=1e-12)
+
+
+def test_exit_loss_per_row_regrouping(orc):
+    """Eq. 67: one log-normaliser per row, weighted by the row's summed weight,
+    minus a gather -- equal to the node-by-node sum of Eq. 66."""
+    from scipy.special import logsumexp
+    z, token, depth, omega = _exit_loss_case(7)
+    W = np.zeros(z.shape[0])
+    gather = 0.0
+    for v in range(1, len(token)):
+        W[depth[v] - 1] += omega[v]
+        gather += omega[v] * z[depth[v] - 1, token[v]]
+    want = sum(W[m] * logsumexp(z[m]) for m in range(z.shape[0])) - gather
+    assert orc.exit_loss(z, 1.0, token, depth, len(token), omega) == pytest.approx(want, rel=1e-12)
+
+
+def test_exit_loss_gradient_by_finite_differences(orc):
+    z, token, depth, omega = _exit_loss_case(9, L=3, V=20)
+    T = 0.9
+    _, grad = orc.exit_loss(z, T, token, depth, len(token), omega, with_grad=True)
+    rng = np.random.default_rng(1)
+    h = 1e-6
+    for _ in range(12):
+        m, a = int(rng.integers(0, z.shape[0])), int(rng.integers(0, z.shape[1]))
+        zp, zm = z.copy(), z.copy()
+        zp[m, a] += h
+        zm[m, a] -= h
+        fd = (orc.exit_loss(zp, T, token, depth, len(token), omega)
+              - orc.exit_loss(zm, T, token, depth, len(token), omega)) / (2 * h)
+        assert fd == pytest.approx(grad[m, a], rel=1e-5, abs=1e-8)
+
+
+def test_exit_loss_temperature_is_a_logit_scale(orc):
+    z, token, depth, omega = _exit_loss_case(11)
+    a = orc.exit_loss(z, 1.6, token, depth, len(token), omega)
+    b = orc.exit_loss(z / 1.6, 1.0, token, depth, len(token), omega)
+    assert a == pytest.approx(b, rel=1e-12)
