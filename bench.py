@@ -292,6 +292,7 @@ def run_ours(args):
         extra["e2e_explicit_copies"] = e2e_copy
     if rank == 0 and not args.no_extra:
         extra.update(secondary(tsd, torch, synth, dev, stream, last[0], target, T, ws_v, V))
+        extra.update(exit_loss_bench(tsd, torch, stream, drafter, last[0], last[1], V))
 
     if rank != 0:
         return
@@ -314,6 +315,50 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def exit_loss_bench(tsd, torch, stream, drafter, tree, tev, V):
+    """The exit-guided loss on the workload's drafter rows (32 trees x 16 rows),
+    weighted by the step's TEV exit masses: loss alone, and loss with its
+    gradient (an fp32 row per drafter row).  Algorithmic bytes: one read of
+    the drafter logits for the loss; for the gradient a second read plus the
+    fp32 write."""
+    out = {}
+    rows = drafter.shape[0] * drafter.shape[2]
+    dbytes = rows * V * 2
+    nt, L = drafter.shape[0], drafter.shape[2]
+    ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_EXIT_LOSS, nt, 1, L, V, 1,
+                                            tree["token"].shape[1] - 1, drafter.dtype),
+                     dtype=torch.uint8, device=drafter.device)
+    for grad in (False, True):
+        fn = lambda: tsd.tsd_exit_loss(drafter, tree["token"], tree["depth"], tree["n_nodes"],
+                                       tev["exit_mass"], with_grad=grad, workspace=ws)
+        # captured once in a CUDA graph and replayed, as a training step would
+        cap = torch.cuda.Stream(drafter.device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for i in range(3):
+                fn()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        for i in range(3):
+            graph.replay()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for i in range(20):
+            graph.replay()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / 20
+        del graph
+        nbytes = dbytes + (dbytes + rows * V * 4 if grad else 0)
+        out["exit_loss" + ("_with_grad" if grad else "")] = {
+            "ms": ms, "algorithmic_gb": nbytes / 1e9, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_measured": nbytes / (ms * 1e-3) / 1e9 / measured_peaks()[0]}
+    return out
 
 
 def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):

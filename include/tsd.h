@@ -71,7 +71,8 @@ typedef enum { TSD_BF16 = 0, TSD_F32 = 1 } tsd_dtype;
 typedef enum {
     TSD_OP_BUILD_TREE = 0,
     TSD_OP_VERIFY_TEV = 1,
-    TSD_OP_VERIFY_DDTREE = 2
+    TSD_OP_VERIFY_DDTREE = 2,
+    TSD_OP_EXIT_LOSS = 3
 } tsd_op;
 
 /* Limits checked by every entry point. */
@@ -209,6 +210,39 @@ tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const i
                              int32_t *bonus_token, int32_t *accept_len, int32_t *draws,
                              int32_t *status, void *workspace, size_t ws_bytes,
                              cudaStream_t stream);
+
+/*
+ * tsd_exit_loss -- the exit-guided loss of ExitTrain ([EXIT] Sec. 5 Eq. 14),
+ * evaluated as App. C.2 Eq. 67 does: one log-normaliser per drafter row,
+ * weighted by the summed exit mass of the nodes the row scores, minus a
+ * gather of those nodes' logits.  Node v's incoming token x_v is scored by
+ * the drafter row of future position depth(v), i.e. row depth(v) - 1, with
+ * log q = z/T_d - logsumexp(z/T_d).
+ *   L_exit = sum over trees of sum_{v != root} w(v) (-log q_{depth(v)}(x_v))
+ *            / sum over trees of (n_nodes - 1).
+ *
+ * drafter_logits  [n_trees][L][V] (dtype), one mode; device or page-locked
+ *                 host memory.  L <= TSD_MAX_L.  drafter_temp: T_d > 0.
+ * token, depth    [n_trees][B+1] int32: each node's token and depth (the
+ *                 builder's outputs); node 0 is the root and is skipped.
+ * n_nodes         [n_trees].
+ * omega           [n_trees][B+1] fp32: the detached weights, normally the
+ *                 exit masses w(v) that tsd_verify_tev returns.
+ * Outputs (device): loss_tree [n_trees] float64, each tree's numerator;
+ *   loss [1] float64, the scalar L_exit over the valid trees; grad
+ *   (nullable) [n_trees][L][V] fp32, d L_exit / d drafter_logits (rows no
+ *   node scores are zero); status [n_trees]: TSD_ERR_BAD_TREE for a depth
+ *   outside [1, L] or a token outside [0, V), TSD_ERR_NONFINITE for a
+ *   non-finite term; such trees count nowhere and get zero gradient.
+ * workspace: tsd_workspace_size(TSD_OP_EXIT_LOSS, n_trees, 1, L, V, 1, B,
+ *   dtype) bytes.
+ */
+tsd_status tsd_exit_loss(const void *drafter_logits, tsd_dtype dtype, int n_trees, int L,
+                         int64_t V, float drafter_temp, const int32_t *token,
+                         const int32_t *depth, const int32_t *n_nodes, int B,
+                         const float *omega, double *loss_tree, double *loss, float *grad,
+                         int32_t *status, void *workspace, size_t ws_bytes,
+                         cudaStream_t stream);
 
 /*
  * tsd_verify_tev_noalloc -- tsd_verify_tev for callers that cannot allocate

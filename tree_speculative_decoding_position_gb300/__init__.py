@@ -18,14 +18,14 @@ import torch
 
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
            "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
-           "tsd_verify_tev_noalloc", "LIB_PATH"]
+           "tsd_verify_tev_noalloc", "tsd_exit_loss", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
 
 TSD_OK, TSD_ERR_INVALID_ARG, TSD_ERR_CUDA, TSD_ERR_WORKSPACE = 0, 1, 2, 3
 TSD_ERR_BAD_TREE, TSD_ERR_NONFINITE, TSD_ERR_TIMEOUT = 4, 5, 6
 TSD_BF16, TSD_F32 = 0, 1
-TSD_OP_BUILD_TREE, TSD_OP_VERIFY_TEV, TSD_OP_VERIFY_DDTREE = 0, 1, 2
+TSD_OP_BUILD_TREE, TSD_OP_VERIFY_TEV, TSD_OP_VERIFY_DDTREE, TSD_OP_EXIT_LOSS = 0, 1, 2, 3
 
 _lib = None
 
@@ -61,8 +61,10 @@ def load():
                                            P, P, P, P, P, P, P, P]
     lib.tsd_verify_ddtree.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64,
                                       P, P, P, P, P, P, sz, P]
+    lib.tsd_exit_loss.argtypes = [P, i32, i32, i32, i64, f32, P, P, P, i32, P, P, P, P, P, P,
+                                  sz, P]
     for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
-              "tsd_verify_ddtree", "tsd_verify_tev_noalloc"):
+              "tsd_verify_ddtree", "tsd_verify_tev_noalloc", "tsd_exit_loss"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -304,4 +306,49 @@ def tsd_verify_ddtree(target_logits: torch.Tensor, parent: torch.Tensor, token: 
                                       _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
     if st != TSD_OK:
         raise TsdError(st, "tsd_verify_ddtree")
+    return out
+
+
+def tsd_exit_loss(drafter_logits: torch.Tensor, token: torch.Tensor, depth: torch.Tensor,
+                  n_nodes: torch.Tensor, omega: torch.Tensor, drafter_temp: float = 1.0,
+                  with_grad: bool = False, workspace=None) -> dict:
+    """Exit-guided loss ([EXIT] Eq. 14 via Eq. 67).  drafter_logits:
+    [n_trees, L, V] (or [n_trees, 1, L, V]); token, depth: [n_trees, B+1];
+    n_nodes: [n_trees]; omega: [n_trees, B+1] float32 (TEV's exit_mass).
+    Returns loss (float64 scalar tensor), loss_tree ([n_trees] float64
+    numerators), status and, with `with_grad`, grad ([n_trees, L, V] float32,
+    d loss / d drafter_logits)."""
+    x = _logits(drafter_logits, "drafter_logits")
+    if x.dim() == 4:
+        if x.shape[1] != 1:
+            raise ValueError("the exit loss takes one mode")
+        x = x.reshape(x.shape[0], x.shape[2], x.shape[3])
+    if x.dim() != 3:
+        raise ValueError("drafter_logits must be [n_trees, L, V]")
+    n_trees, L, V = x.shape
+    token = _cuda(token, "token", torch.int32)
+    depth = _cuda(depth, "depth", torch.int32)
+    n_nodes = _cuda(n_nodes, "n_nodes", torch.int32)
+    omega = _cuda(omega, "omega", torch.float32)
+    Bp1 = token.shape[1]
+    if tuple(token.shape) != (n_trees, Bp1) or tuple(depth.shape) != (n_trees, Bp1) \
+            or tuple(omega.shape) != (n_trees, Bp1) or tuple(n_nodes.shape) != (n_trees,):
+        raise ValueError("token/depth/omega must be [n_trees, B+1] and n_nodes [n_trees]")
+    dev = token.device
+    out = {"loss_tree": torch.empty(n_trees, dtype=torch.float64, device=dev),
+           "loss": torch.empty((), dtype=torch.float64, device=dev),
+           "status": torch.empty(n_trees, dtype=torch.int32, device=dev)}
+    if with_grad:
+        out["grad"] = torch.empty(n_trees, L, V, dtype=torch.float32, device=dev)
+    nbytes = tsd_workspace_size(TSD_OP_EXIT_LOSS, n_trees, 1, L, V, 1, Bp1 - 1, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_exit_loss")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_exit_loss(_ptr(x), _dtype_code(x), n_trees, L, V, drafter_temp, _ptr(token),
+                                  _ptr(depth), _ptr(n_nodes), Bp1 - 1, _ptr(omega),
+                                  _ptr(out["loss_tree"]), _ptr(out["loss"]), _ptr(out.get("grad")),
+                                  _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_exit_loss")
     return out

@@ -367,9 +367,8 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
     }
 }
 
-cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
-                                 int topk, float c, double temp, const BuildWs& ws,
-                                 cudaStream_t stream) {
+cudaError_t launch_drafter_chunks(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
+                                  float c, const BuildWs& ws, cudaStream_t stream) {
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
     const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
@@ -377,21 +376,30 @@ cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t ro
     const int64_t want_chunks = (rows * nch + wpb - 1) / wpb;
     // persistent: one wave of resident CTAs, each warp streaming many chunks
     if (dtype == TSD_BF16) {
-        const auto* p = static_cast<const __nv_bfloat16*>(logits);
         auto kc = drafter_chunk_kernel<__nv_bfloat16>;
-        if (cudaError_t e_ = launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream, 
-            p, rows, V, nch, c, vec_ok, ws); e_ != cudaSuccess) return e_;
-        if (cudaError_t e_ = launch_pdl(drafter_row_kernel<__nv_bfloat16>, (unsigned)rows, kRThreads, 0, stream, 
-            p, rows, V, nch, topk, c, temp, vec_ok, ws); e_ != cudaSuccess) return e_;
-    } else {
-        const auto* p = static_cast<const float*>(logits);
-        auto kc = drafter_chunk_kernel<float>;
-        if (cudaError_t e_ = launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0, stream, 
-            p, rows, V, nch, c, vec_ok, ws); e_ != cudaSuccess) return e_;
-        if (cudaError_t e_ = launch_pdl(drafter_row_kernel<float>, (unsigned)rows, kRThreads, 0, stream, 
-            p, rows, V, nch, topk, c, temp, vec_ok, ws); e_ != cudaSuccess) return e_;
+        return launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads,
+                          0, stream, static_cast<const __nv_bfloat16*>(logits), rows, V, nch, c,
+                          vec_ok, ws);
     }
-    return cudaGetLastError();
+    auto kc = drafter_chunk_kernel<float>;
+    return launch_pdl(kc, resident_grid((const void*)kc, kDThreads, 0, want_chunks), kDThreads, 0,
+                      stream, static_cast<const float*>(logits), rows, V, nch, c, vec_ok, ws);
+}
+
+cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
+                                 int topk, float c, double temp, const BuildWs& ws,
+                                 cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
+    if (cudaError_t e = launch_drafter_chunks(logits, dtype, rows, V, c, ws, stream); e != cudaSuccess)
+        return e;
+    if (dtype == TSD_BF16)
+        return launch_pdl(drafter_row_kernel<__nv_bfloat16>, (unsigned)rows, kRThreads, 0, stream,
+                          static_cast<const __nv_bfloat16*>(logits), rows, V, nch, topk, c, temp,
+                          vec_ok, ws);
+    return launch_pdl(drafter_row_kernel<float>, (unsigned)rows, kRThreads, 0, stream,
+                      static_cast<const float*>(logits), rows, V, nch, topk, c, temp, vec_ok, ws);
 }
 
 }  // namespace tsd

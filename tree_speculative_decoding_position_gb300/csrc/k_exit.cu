@@ -1,0 +1,267 @@
+// k_exit.cu -- the exit-guided loss of ExitTrain.
+//
+// "Where Draft Trees Lose Target Mass: Exit-Guided Speculative Decoding",
+// Sec. 5 Eq. 14 and App. C.2 Eq. 66-67:
+//   L_exit = sum_v w(v) (-log q_{depth(v)}(x_v)) / sum_i (|V_i| - 1),
+// summed over the non-root nodes of every tree, evaluated as Eq. 67 does:
+// each drafter row m needs one log-normaliser LSE_m, weighted by the summed
+// weight W_m of the nodes it scores, minus a gather of the scored logits:
+//   numerator = sum_m W_m LSE_m - sum_v w(v) z_{row(v), x_v} / T_d.
+// Node v is scored by the row of future position depth(v) (row depth(v) - 1).
+//
+// Kernels:
+//   drafter_chunk_kernel (k_drafter.cu)  the streaming pass over the rows;
+//   exit_tree_kernel  one CTA per tree: its rows' LSE_m, W_m, the gather and
+//                     the numerator; the last CTA to finish forms the scalar;
+//   exit_grad_kernel  optional streaming pass: d loss / dz = (W_m softmax_m -
+//                     sum_v w(v) [a = x_v]) / (T_d N), written as the dense
+//                     part, then exit_scatter_kernel subtracts the gathers.
+#include "tsd_internal.cuh"
+
+namespace tsd {
+
+constexpr int kExitThreads = 256;
+
+// LSE of one row of z / T_d, ln 2 * (mc + log2 S), from its chunk statistics
+// as the builder's row kernel forms it, by one warp; NaN when a chunk saw a
+// NaN or +inf or the row has no mass.
+__device__ double row_lse(const ChunkStat* __restrict__ cs, int nch, float c, int lane) {
+    float m = -INFINITY;
+    bool bad = false;
+    for (int q = lane; q < nch; q += kWarp) {
+        m = fmaxf(m, cs[q].m);
+        bad |= (cs[q].s != cs[q].s);
+    }
+    m = warp_max(m);
+    const float mc = __fmul_rn(m, c);
+    double s = 0.0;
+    for (int q = lane; q < nch; q += kWarp)
+        if (cs[q].m != -INFINITY) s += (double)cs[q].s * (double)ex2(__fmul_rn(cs[q].m, c) - mc);
+    s = warp_sum_d(s);
+    bad = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0);
+    return bad ? __longlong_as_double(0x7ff8000000000000ll)
+               : 0.6931471805599453 * ((double)mc + log2(s));
+}
+
+// One CTA per tree: the LSE of its L rows (one warp per row), then the
+// tree's numerator and the per-row weights W_m.  The last CTA to finish
+// (a completion counter; no CTA waits for another) forms the scalar loss
+// from the valid trees' numerators and (n_nodes - 1).
+template <typename T>
+__global__ void __launch_bounds__(kExitThreads)
+exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, int nch, float c,
+                 double temp, const int32_t* __restrict__ token, const int32_t* __restrict__ depth,
+                 const int32_t* __restrict__ n_nodes, int B, const float* __restrict__ omega,
+                 double* __restrict__ loss_tree, double* __restrict__ loss,
+                 int32_t* __restrict__ status, ExitWs ws) {
+    pdl_entry();
+    __shared__ double W[TSD_MAX_L];
+    __shared__ double lse[TSD_MAX_L];
+    __shared__ double red[kExitThreads / kWarp], red2[kExitThreads / kWarp];
+    __shared__ int bad, last;
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), wid = tid / kWarp;
+    const int nw = blockDim.x / kWarp;
+    const int stride = B + 1;
+    const int n = n_nodes[t];
+    if (tid == 0) bad = (n < 1 || n > stride) ? kStatBadTree : kStatOk;
+    for (int m = tid; m < L; m += blockDim.x) W[m] = 0.0;
+    for (int m = wid; m < L; m += nw) {
+        const int64_t row = (int64_t)t * L + m;
+        const double l = row_lse(ws.rows.chunk + row * nch, nch, c, lane);
+        if (lane == 0) {
+            lse[m] = l;
+            ws.lse[row] = l;
+        }
+    }
+    __syncthreads();
+    const double inv_temp = 1.0 / temp;  // z / T_d as one multiply per node
+    double part = 0.0;
+    if (bad == kStatOk) {
+        for (int v = 1 + tid; v < n; v += blockDim.x) {
+            const int d = depth[(int64_t)t * stride + v];
+            const int x = token[(int64_t)t * stride + v];
+            if (d < 1 || d > L || x < 0 || (int64_t)x >= V) {
+                atomicExch(&bad, kStatBadTree);
+                continue;
+            }
+            const double w = (double)omega[(int64_t)t * stride + v];
+            const int64_t row = (int64_t)t * L + d - 1;
+            const double z = (double)load_logit(logits + row * V + x);
+            const double term = w * (lse[d - 1] - z * inv_temp);  // w(v) * -log q_{depth(v)}(x_v)
+            if (!(term == term) || isinf(term)) atomicCAS(&bad, kStatOk, kStatNonFinite);
+            part += term;
+            atomicAdd(&W[d - 1], w);
+        }
+    }
+    part = warp_sum_d(part);
+    if (lane == 0) red[wid] = part;
+    __syncthreads();
+    const int st = bad;
+    if (tid == 0) {
+        double num = 0.0;
+        for (int i = 0; i < nw; ++i) num += red[i];
+        loss_tree[t] = st == kStatOk ? num : 0.0;
+        status[t] = st;
+        ws.tstat[t] = st;
+    }
+    for (int m = tid; m < L; m += blockDim.x) ws.wrow[(int64_t)t * L + m] = st == kStatOk ? W[m] : 0.0;
+    // completion: the last CTA reads every tree's results
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(ws.done, 1u) == (unsigned)n_trees - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double a = 0.0, b2 = 0.0;
+    for (int u = tid; u < n_trees; u += blockDim.x) {
+        const int su = *(volatile const int32_t*)(ws.tstat + u);
+        if (su == kStatOk) {
+            a += *(volatile const double*)(loss_tree + u);
+            b2 += (double)(n_nodes[u] - 1);
+        }
+    }
+    a = warp_sum_d(a);
+    b2 = warp_sum_d(b2);
+    if (lane == 0) {
+        red[wid] = a;
+        red2[wid] = b2;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double A = 0.0, Bn = 0.0;
+        for (int i = 0; i < nw; ++i) {
+            A += red[i];
+            Bn += red2[i];
+        }
+        *ws.norm = Bn;
+        *loss = Bn > 0.0 ? A / Bn : 0.0;
+    }
+}
+
+// Dense part of the gradient, streaming: grad[row][a] = W_row softmax(z/T_d)(a)
+// / (T_d N), with softmax = 2^(z c - LSE_row log2 e); rows of invalid trees
+// and rows no node scores are zero.  One warp per (row, 8 KB chunk of logits)
+// with all of the chunk's 16-byte loads in flight, then 16-byte streaming
+// stores; rows that are not 16-byte aligned take an element-wise loop.
+template <typename T>
+__global__ void __launch_bounds__(kExitThreads)
+exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, int nch, float c,
+                 double temp, float* __restrict__ grad, ExitWs ws) {
+    pdl_entry();
+    constexpr int VEC = Lanes<T>::kVec;
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    const int lane = threadIdx.x & (kWarp - 1);
+    const double nrm = *ws.norm;
+    const bool vec = ((uintptr_t)logits % 16 == 0) && ((V * (int64_t)sizeof(T)) % 16 == 0) &&
+                     ((uintptr_t)grad % 16 == 0);
+    const int64_t total = rows * nch;
+    const int wpb = blockDim.x / kWarp;
+    for (int64_t item = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; item < total;
+         item += (int64_t)gridDim.x * wpb) {
+        const int64_t row = item / nch;
+        const int64_t c0 = (item - row * nch) * (int64_t)CE;
+        const int cn = (int)min((int64_t)CE, V - c0);
+        const int t = (int)(row / L);
+        const double wr = ws.wrow[row];
+        float* g = grad + row * V + c0;
+        const T* z = logits + row * V + c0;
+        const bool zero = ws.tstat[t] != kStatOk || wr == 0.0 || !(nrm > 0.0);
+        const float scale = zero ? 0.0f : (float)(wr / (temp * nrm));
+        const float l2 = zero ? 0.0f : (float)(ws.lse[row] * 1.4426950408889634);
+        if (vec) {
+            uint4 buf[kVecPerLane];
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const int e = (i * kWarp + lane) * VEC;
+                buf[i] = (!zero && e < cn) ? ld_stream16(z + e) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const int e = (i * kWarp + lane) * VEC;
+                if (e < cn) {
+#pragma unroll
+                    for (int j = 0; j < VEC; j += 4) {
+                        float4 o;
+                        o.x = zero ? 0.0f : scale * ex2(fmaf(Lanes<T>::get(buf[i], j), c, -l2));
+                        o.y = zero ? 0.0f : scale * ex2(fmaf(Lanes<T>::get(buf[i], j + 1), c, -l2));
+                        o.z = zero ? 0.0f : scale * ex2(fmaf(Lanes<T>::get(buf[i], j + 2), c, -l2));
+                        o.w = zero ? 0.0f : scale * ex2(fmaf(Lanes<T>::get(buf[i], j + 3), c, -l2));
+                        __stcs(reinterpret_cast<float4*>(g + e + j), o);
+                    }
+                }
+            }
+        } else {
+            for (int e = lane; e < cn; e += kWarp)
+                g[e] = zero ? 0.0f : scale * ex2(fmaf(load_logit(z + e), c, -l2));
+        }
+    }
+}
+
+// The gathered part: grad[row(v)][x_v] -= w(v) / (T_d N) for every node.
+__global__ void __launch_bounds__(kExitThreads)
+exit_scatter_kernel(int n_trees, int L, int64_t V, double temp, const int32_t* __restrict__ token,
+                    const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes, int B,
+                    const float* __restrict__ omega, float* __restrict__ grad, ExitWs ws) {
+    pdl_entry();
+    const double nrm = *ws.norm;
+    const int64_t total = (int64_t)n_trees * (B + 1);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / (B + 1)), v = (int)(i - (int64_t)t * (B + 1));
+        if (v == 0 || v >= n_nodes[t] || ws.tstat[t] != kStatOk || !(nrm > 0.0)) continue;
+        const int d = depth[i], x = token[i];
+        atomicAdd(grad + ((int64_t)t * L + d - 1) * V + x, (float)(-(double)omega[i] / (temp * nrm)));
+    }
+}
+
+cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, int L, int64_t V,
+                             float c, double temp, const int32_t* token, const int32_t* depth,
+                             const int32_t* n_nodes, int B, const float* omega, double* loss_tree,
+                             double* loss, float* grad, int32_t* status, const ExitWs& ws,
+                             cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    const int64_t rows = (int64_t)n_trees * L;
+    // the per-tree kernel's completion counter starts at zero on every call
+    if (cudaError_t e = cudaMemsetAsync(ws.done, 0, sizeof(unsigned), stream); e != cudaSuccess)
+        return e;
+    if (cudaError_t e = launch_drafter_chunks(logits, dtype, rows, V, c, ws.rows, stream);
+        e != cudaSuccess)
+        return e;
+    cudaError_t e;
+    if (dtype == TSD_BF16)
+        e = launch_pdl(exit_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kExitThreads, 0, stream,
+                       static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, temp,
+                       token, depth, n_nodes, B, omega, loss_tree, loss, status, ws);
+    else
+        e = launch_pdl(exit_tree_kernel<float>, (unsigned)n_trees, kExitThreads, 0, stream,
+                       static_cast<const float*>(logits), n_trees, L, V, nch, c, temp, token,
+                       depth, n_nodes, B, omega, loss_tree, loss, status, ws);
+    if (e != cudaSuccess) return e;
+    if (grad) {
+        int dev = 0, sms = 152;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int wpb = kExitThreads / kWarp;
+        const int64_t want = (rows * nch + wpb - 1) / wpb;
+        const int64_t cap = (int64_t)sms * 8;
+        const unsigned g2 = (unsigned)(want < cap ? want : cap);
+        if (dtype == TSD_BF16)
+            e = launch_pdl(exit_grad_kernel<__nv_bfloat16>, g2, kExitThreads, 0, stream,
+                           static_cast<const __nv_bfloat16*>(logits), rows, L, V, nch, c, temp,
+                           grad, ws);
+        else
+            e = launch_pdl(exit_grad_kernel<float>, g2, kExitThreads, 0, stream,
+                           static_cast<const float*>(logits), rows, L, V, nch, c, temp, grad, ws);
+        if (e != cudaSuccess) return e;
+        const int64_t nodes = (int64_t)n_trees * (B + 1);
+        const int64_t gs = (nodes + kExitThreads - 1) / kExitThreads;
+        if ((e = launch_pdl(exit_scatter_kernel, (unsigned)(gs < 65535 ? (gs > 0 ? gs : 1) : 65535),
+                            kExitThreads, 0, stream, n_trees, L, V, temp, token, depth, n_nodes, B,
+                            omega, grad, ws)) != cudaSuccess)
+            return e;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tsd

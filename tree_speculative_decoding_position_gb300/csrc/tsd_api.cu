@@ -113,6 +113,23 @@ size_t verify_ws_layout(int n_trees, int B, int64_t V, int esize, void* base, Ve
     return (cv.off + kAlign - 1) & ~(kAlign - 1);
 }
 
+size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* base, ExitWs* out) {
+    (void)B;
+    Carve cv{static_cast<uint8_t*>(base)};
+    const size_t rows = (size_t)n_trees * L;
+    const size_t nch = (size_t)n_chunks(V, esize);
+    ExitWs ws = {};
+    ws.rows.chunk = cv.take<ChunkStat>(rows * nch);
+    ws.rows.lane_max = cv.take<float>(rows * nch * kWarp);
+    ws.lse = cv.take<double>(rows);
+    ws.wrow = cv.take<double>(rows);
+    ws.tstat = cv.take<int32_t>((size_t)n_trees);
+    ws.norm = cv.take<double>(1);
+    ws.done = cv.take<unsigned>(1);
+    if (out) *out = ws;
+    return (cv.off + kAlign - 1) & ~(kAlign - 1);
+}
+
 size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
                        void* base, BuildWs* out) {
     Carve cv{static_cast<uint8_t*>(base)};
@@ -173,6 +190,11 @@ size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V,
         case TSD_OP_VERIFY_DDTREE:
             if (n_trees < 1 || B < 0 || B > TSD_MAX_B || V < 1 || V > 0x7fffffff) return 0;
             return verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+        case TSD_OP_EXIT_LOSS:
+            if (n_trees < 1 || L < 1 || L > TSD_MAX_L || B < 0 || B > TSD_MAX_B || V < 1 ||
+                V > 0x7fffffff || n_chunks(V, es) > kMaxDrafterChunks)
+                return 0;
+            return exit_ws_layout(n_trees, L, V, B, es, nullptr, nullptr);
     }
     return 0;
 }
@@ -300,6 +322,29 @@ tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const i
         launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
         launch_predraw(target_logits, dtype, n_trees, B, V, c, greedy, seed, n_nodes, ws,
                        exit_node, bonus_token, accept_len, draws, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_exit_loss(const void* drafter_logits, tsd_dtype dtype, int n_trees, int L,
+                         int64_t V, float drafter_temp, const int32_t* token, const int32_t* depth,
+                         const int32_t* n_nodes, int B, const float* omega, double* loss_tree,
+                         double* loss, float* grad, int32_t* status, void* workspace,
+                         size_t ws_bytes, cudaStream_t stream) {
+    const int es = dtype_size(dtype);
+    if (!drafter_logits || !token || !depth || !n_nodes || !omega || !loss_tree || !loss ||
+        !status || !es || n_trees < 1 || L < 1 || L > TSD_MAX_L || B < 0 || B > TSD_MAX_B ||
+        V < 1 || V > 0x7fffffff || n_chunks(V, es) > kMaxDrafterChunks ||
+        !(isfinite(drafter_temp) && drafter_temp >= 1e-6f))
+        return TSD_ERR_INVALID_ARG;
+    const size_t need = exit_ws_layout(n_trees, L, V, B, es, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(drafter_logits, &drafter_logits)) return TSD_ERR_INVALID_ARG;
+    ExitWs ws;
+    exit_ws_layout(n_trees, L, V, B, es, workspace, &ws);
+    if (launch_exit_loss(drafter_logits, dtype, n_trees, L, V, exp2_scale(drafter_temp),
+                         (double)drafter_temp, token, depth, n_nodes, B, omega, loss_tree, loss,
+                         grad, status, ws, stream) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
 }

@@ -301,6 +301,25 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
 cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
                                  int topk, float c, double temp, const BuildWs& ws,
                                  cudaStream_t stream);
+// The drafter's streaming pass alone (ws.chunk and ws.lane_max).
+cudaError_t launch_drafter_chunks(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
+                                  float c, const BuildWs& ws, cudaStream_t stream);
+
+// Workspace of the exit-guided loss, per call.
+struct ExitWs {
+    BuildWs rows;       // chunk statistics and lane maxima of the drafter rows
+    double* lse;        // [n_trees][L] row log-normalisers of z / T_d
+    double* wrow;       // [n_trees][L] summed weight of the nodes each row scores
+    int32_t* tstat;     // [n_trees]
+    double* norm;       // [1] sum over valid trees of (n_nodes - 1)
+    unsigned* done;     // [1] completion counter of the per-tree kernel (zero between calls)
+};
+size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* base, ExitWs* out);
+cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, int L, int64_t V,
+                             float c, double temp, const int32_t* token, const int32_t* depth,
+                             const int32_t* n_nodes, int B, const float* omega, double* loss_tree,
+                             double* loss, float* grad, int32_t* status, const ExitWs& ws,
+                             cudaStream_t stream);
 cudaError_t launch_build_heap(const BuildWs& ws, int n_trees, int n_modes, int L, int topk, int B,
                               int32_t* parent, int32_t* token, int32_t* depth, float* score,
                               int32_t* rank, int32_t* mode, int32_t* n_nodes, int32_t* status,
