@@ -56,7 +56,14 @@ def _load():
         lib.orc_tev_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_predraw_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_exit_loss.argtypes = [P, i32, i64, f64, P, P, i32, P, P, P]
-        for f in ("orc_exit_loss", "orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
+        lib.orc_uniform_sub.argtypes = [u64, u64, u64, u64, u64]
+        lib.orc_uniform_sub.restype = f64
+        lib.orc_seqres.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P]
+        lib.orc_proposal.argtypes = [P, P, P, i32, i64, f64, P, u64, u64, P, P, P]
+        lib.orc_seqres_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
+        lib.orc_proposal_sample_many.argtypes = [P, P, P, i32, i64, f64, P, u64, u64, i64, P, P]
+        for f in ("orc_seqres", "orc_proposal", "orc_seqres_sample_many",
+                  "orc_proposal_sample_many", "orc_exit_loss", "orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
                   "orc_tev", "orc_predraw", "orc_tev_sample_many", "orc_predraw_sample_many"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -202,20 +209,58 @@ def predraw(z, parent, token, n_nodes: int, T: float, seed: int, tree: int = 0) 
 
 
 def sample_many(kind: str, z, parent, token, n_nodes: int, T: float, seed: int, n_draws: int,
-                first_tree: int = 0):
+                first_tree: int = 0, q_child=None):
     """(exit node, bonus token) of n_draws independent draws of the sampler
-    `kind` ("tev" or "predraw") on one tree; draw i uses tree index
-    first_tree + i."""
+    `kind` ("tev", "predraw", "seqres" or "proposal", the last with
+    q_child) on one tree; draw i uses tree index first_tree + i."""
     z = _f64(z)
     V = z.shape[-1]
     z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
     parent, token = _i32(parent), _i32(token)
     ex = np.zeros(n_draws, dtype=np.int32)
     bo = np.zeros(n_draws, dtype=np.int32)
-    fn = _load().orc_tev_sample_many if kind == "tev" else _load().orc_predraw_sample_many
+    lib = _load()
+    if kind == "proposal":
+        q = _f64(q_child)
+        _check(lib.orc_proposal_sample_many(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T,
+                                            _ptr(q), seed, first_tree, n_draws, _ptr(ex), _ptr(bo)),
+               "proposal_sample_many")
+        return ex, bo
+    fn = {"tev": lib.orc_tev_sample_many, "predraw": lib.orc_predraw_sample_many,
+          "seqres": lib.orc_seqres_sample_many}[kind]
     _check(fn(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, seed, first_tree, n_draws,
               _ptr(ex), _ptr(bo)), kind + "_sample_many")
     return ex, bo
+
+
+def uniform_sub(seed: int, tree: int, node: int, stream: int, sub: int) -> float:
+    return float(_load().orc_uniform_sub(seed, tree, node, stream, sub))
+
+
+def seqres(z, parent, token, n_nodes: int, T: float, seed: int, tree: int = 0) -> dict:
+    """Exact sequential residual verification ([EXIT] App. A.4.2) on one tree."""
+    z = _f64(z)
+    V = z.shape[-1]
+    z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
+    parent, token = _i32(parent), _i32(token)
+    ex, bo, al = (np.zeros(1, dtype=np.int32) for _ in range(3))
+    _check(_load().orc_seqres(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, seed, tree,
+                              _ptr(ex), _ptr(bo), _ptr(al)), "seqres")
+    return dict(exit_node=int(ex[0]), bonus=int(bo[0]), accept_len=int(al[0]))
+
+
+def proposal(z, parent, token, n_nodes: int, T: float, q_child, seed: int, tree: int = 0) -> dict:
+    """Proposal-aware verification ([CAST] App. B.1 Thm. 3) on one tree;
+    q_child[u] = the proposal's probability of node u's token (u >= 1)."""
+    z = _f64(z)
+    V = z.shape[-1]
+    z = np.ascontiguousarray(z.reshape(-1, V)[:n_nodes])
+    parent, token = _i32(parent), _i32(token)
+    q = _f64(q_child)
+    ex, bo, al = (np.zeros(1, dtype=np.int32) for _ in range(3))
+    _check(_load().orc_proposal(_ptr(z), _ptr(parent), _ptr(token), n_nodes, V, T, _ptr(q), seed,
+                                tree, _ptr(ex), _ptr(bo), _ptr(al)), "proposal")
+    return dict(exit_node=int(ex[0]), bonus=int(bo[0]), accept_len=int(al[0]))
 
 
 def exit_loss(z, T: float, token, depth, n_nodes: int, omega, with_grad: bool = False):

@@ -15,8 +15,10 @@
  *   [CAST]  "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters"
  *           -- Sec. 2 Eq. 1 (plug-in score), Thm. 1 (tie order), App. C
  *           "Candidate construction" (top-K heap, push all K children) and
- *           "Packed verification" (ancestor mask, position ids).
- *           Sec. 5 Eq. 14 and App. C.2 Eq. 66 (the exit-guided loss).
+ *           "Packed verification" (ancestor mask, position ids), App. B.1
+ *           Thm. 3 (recursive speculative sampling without replacement).
+ *           Sec. 5 Eq. 14 and App. C.2 Eq. 66 (the exit-guided loss), App.
+ *           A.4.2 Eq. 45-53 (exact sequential residual verification).
  *   [MFD]   "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
  *           Speculative Decoding" -- Sec. 3.4 Eq. 2 (best-mode score),
  *           App. B "Merged heap" and Prop. 6 (sibling / first-child pushes,
@@ -26,8 +28,14 @@
  *
  * Readings where the pages are open (each also listed in the design doc):
  *   - Uniforms: u = (x0 >> 40) * 2^-24 from Philox4x64-10 with
- *     counter (tree, node, stream, 0) and key (seed, 0); stream 0 = TEV exit
- *     draw, 1 = TEV bonus draw, 2 = predraw at node `node`.
+ *     counter (tree, node, stream, sub) and key (seed, 0); stream 0 = TEV exit
+ *     draw, 1 = TEV bonus draw, 2 = predraw at node `node` (sub 0); 3 =
+ *     sequential-residual test of the node's child number `sub`, 4 = its
+ *     bonus draw; 5 / 6 = proposal-aware candidate draw / acceptance test at
+ *     step `sub`, 7 = its final residual draw.
+ *   - The sequential-residual and proposal-aware verifiers take a node's
+ *     children in ascending token order; their decisions compare without
+ *     dividing (u (1 - M) < p, u q~ < mu).
  *   - "Draw" (Alg. 1 lines 8-9) is inverse-CDF sampling: nodes in index
  *     (build) order for the exit, token ids ascending (skipping the drafted
  *     children) for the bonus; strict '>' so zero-mass items are never drawn;
@@ -86,14 +94,20 @@ void orc_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t ou
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* One uniform in [0, 1) on a 2^-24 grid, for (seed; tree, node, stream). */
-double orc_uniform(uint64_t seed, uint64_t tree, uint64_t node, uint64_t stream)
+/* One uniform in [0, 1) on a 2^-24 grid, for (seed; tree, node, stream, sub). */
+double orc_uniform_sub(uint64_t seed, uint64_t tree, uint64_t node, uint64_t stream,
+                       uint64_t sub)
 {
-    uint64_t ctr[4] = {tree, node, stream, 0};
+    uint64_t ctr[4] = {tree, node, stream, sub};
     uint64_t key[2] = {seed, 0};
     uint64_t out[4];
     orc_philox4x64_10(ctr, key, out);
     return (double)(out[0] >> 40) * (1.0 / 16777216.0);
+}
+
+double orc_uniform(uint64_t seed, uint64_t tree, uint64_t node, uint64_t stream)
+{
+    return orc_uniform_sub(seed, tree, node, stream, 0);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -638,4 +652,197 @@ int orc_exit_loss(const double *z, int L, int64_t V, double T, const int32_t *to
     }
     *num = total;
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Children of v in ascending token order (the order both verifiers below    */
+/* test them in); returns their count.                                       */
+/* ------------------------------------------------------------------------ */
+static int orc_children_by_token(const int32_t *parent, const int32_t *token, int n, int v,
+                                 int32_t *kids)
+{
+    int k = 0;
+    for (int u = 1; u < n; ++u)
+        if (parent[u] == v) kids[k++] = u;
+    for (int i = 1; i < k; ++i) { /* insertion sort by token (sibling tokens are distinct) */
+        int x = kids[i], j = i - 1;
+        while (j >= 0 && token[kids[j]] > token[x]) { kids[j + 1] = kids[j]; --j; }
+        kids[j + 1] = x;
+    }
+    return k;
+}
+
+/* Inverse-CDF draw over token ids ascending of the masses m[0..V) with total
+ * `tot` and uniform u: the first a whose running sum exceeds u * tot (strict),
+ * or the last token with mass when rounding leaves the threshold past it. */
+static int64_t orc_draw_tokens(const double *m, int64_t V, double tot, double u)
+{
+    double thr = u * tot, cum = 0.0;
+    int64_t last = -1;
+    for (int64_t a = 0; a < V; ++a) {
+        if (m[a] > 0.0) last = a;
+        cum += m[a];
+        if (cum > thr) return a;
+    }
+    return last;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exact sequential residual verification [EXIT App. A.4.2, Eq. 45-53].      */
+/* At the current node v, children u_1..u_k (ascending token) are tested in  */
+/* turn: with p_j = p_v(x_j) and M_{j-1} = p_1 + ... + p_{j-1}, child u_j is  */
+/* followed with the conditional probability g^(j-1)(x_j) = p_j/(1-M_{j-1})  */
+/* (Eq. 49), decided as u_j (1 - M_{j-1}) < p_j with u_j the uniform of      */
+/* stream 3, sub j-1, at node v.  If every child is rejected the walk exits  */
+/* at v and draws the bonus token from g^(k), which is p_v without the       */
+/* children's tokens renormalised (Eq. 53; p_v at a leaf), by inverse CDF     */
+/* over token ids with the uniform of stream 4 at v.                         */
+/* ------------------------------------------------------------------------ */
+int orc_seqres(const double *z, const int32_t *parent, const int32_t *token, int n, int64_t V,
+               double T, uint64_t seed, uint64_t tree, int32_t *exit_node, int32_t *bonus,
+               int32_t *accept_len)
+{
+    if (V < 1 || !(T >= 0.0)) return ORC_ERR_ARG;
+    int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int st = orc_check_tree(parent, token, n, V, depth);
+    if (st) { free(depth); return st; }
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    int32_t *kids = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int v = 0;
+    for (;;) {
+        st = orc_row_probs(z + (int64_t)v * V, V, T, p);
+        if (st) break;
+        const int k = orc_children_by_token(parent, token, n, v, kids);
+        double M = 0.0;
+        int next = -1;
+        for (int j = 0; j < k; ++j) {
+            const double pj = p[token[kids[j]]];
+            const double u = orc_uniform_sub(seed, tree, (uint64_t)v, 3, (uint64_t)j);
+            if (u * (1.0 - M) < pj) { next = kids[j]; break; }
+            M += pj;
+        }
+        if (next >= 0) { v = next; continue; }
+        /* exit at v: the residual law of Eq. 53 */
+        for (int j = 0; j < k; ++j) p[token[kids[j]]] = 0.0;
+        double tot = 0.0;
+        for (int64_t a = 0; a < V; ++a) tot += p[a];
+        const int64_t y = orc_draw_tokens(p, V, tot, orc_uniform_sub(seed, tree, (uint64_t)v, 4, 0));
+        *exit_node = v;
+        *bonus = (int32_t)y;
+        *accept_len = depth[v] + 1;
+        break;
+    }
+    free(kids);
+    free(p);
+    free(depth);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Proposal-aware verification [CAST App. B.1 Thm. 3]: recursive            */
+/* speculative sampling without replacement at each visited node.  The       */
+/* residual mu starts at p_v.  While retained siblings remain, a candidate c */
+/* is drawn from the proposal renormalised over them, q~ (inverse CDF over   */
+/* the retained children in ascending token order, uniform of stream 5, sub  */
+/* = step), and accepted with probability min(1, mu(c)/q~(c)), decided as    */
+/* u q~(c) < mu(c) (stream 6, sub = step).  Acceptance follows the child.    */
+/* Rejection sets mu <- (mu - q~)_+ / ||(mu - q~)_+||_1 (q~ is zero off the   */
+/* retained siblings) and retires c.  When every sibling is retired, the     */
+/* committed token is drawn from mu (stream 7) and the walk exits at v with  */
+/* it as the bonus token; at a leaf mu = p_v.                                */
+/*   q_child: [n] the proposal's probability of each node's token under its  */
+/*   parent, q_{pa(u)}(x_u) (q_child[0] unused); positive on every child.     */
+/* ------------------------------------------------------------------------ */
+int orc_proposal(const double *z, const int32_t *parent, const int32_t *token, int n, int64_t V,
+                 double T, const double *q_child, uint64_t seed, uint64_t tree, int32_t *exit_node,
+                 int32_t *bonus, int32_t *accept_len)
+{
+    if (V < 1 || !(T >= 0.0)) return ORC_ERR_ARG;
+    int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int st = orc_check_tree(parent, token, n, V, depth);
+    if (st) { free(depth); return st; }
+    for (int u = 1; u < n; ++u)
+        if (!(q_child[u] > 0.0) || !isfinite(q_child[u])) { free(depth); return ORC_ERR_ARG; }
+    double *mu = (double *)malloc(sizeof(double) * (size_t)V);
+    int32_t *kids = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    char *avail = (char *)malloc((size_t)n);
+    int v = 0;
+    for (;;) {
+        st = orc_row_probs(z + (int64_t)v * V, V, T, mu);
+        if (st) break;
+        const int k = orc_children_by_token(parent, token, n, v, kids);
+        for (int j = 0; j < k; ++j) avail[j] = 1;
+        int next = -1, left = k;
+        for (int step = 0; left > 0; ++step) {
+            double Q = 0.0;
+            for (int j = 0; j < k; ++j)
+                if (avail[j]) Q += q_child[kids[j]];
+            const double u1 = orc_uniform_sub(seed, tree, (uint64_t)v, 5, (uint64_t)step);
+            double thr = u1 * Q, cum = 0.0;
+            int c = -1, lastj = -1;
+            for (int j = 0; j < k; ++j) {
+                if (!avail[j]) continue;
+                lastj = j;
+                cum += q_child[kids[j]];
+                if (cum > thr) { c = j; break; }
+            }
+            if (c < 0) c = lastj;
+            const double qc = q_child[kids[c]] / Q;
+            const double u2 = orc_uniform_sub(seed, tree, (uint64_t)v, 6, (uint64_t)step);
+            if (u2 * qc < mu[token[kids[c]]]) { next = kids[c]; break; }
+            /* rejection: mu <- (mu - q~)_+ normalised */
+            double norm = 0.0;
+            for (int j = 0; j < k; ++j)
+                if (avail[j]) {
+                    const int64_t a = token[kids[j]];
+                    const double d = mu[a] - q_child[kids[j]] / Q;
+                    mu[a] = d > 0.0 ? d : 0.0;
+                }
+            for (int64_t a = 0; a < V; ++a) norm += mu[a];
+            if (!(norm > 0.0)) { st = ORC_ERR_NONFINITE; break; }
+            for (int64_t a = 0; a < V; ++a) mu[a] /= norm;
+            avail[c] = 0;
+            --left;
+        }
+        if (st) break;
+        if (next >= 0) { v = next; continue; }
+        double tot = 0.0;
+        for (int64_t a = 0; a < V; ++a) tot += mu[a];
+        const int64_t y = orc_draw_tokens(mu, V, tot, orc_uniform_sub(seed, tree, (uint64_t)v, 7, 0));
+        *exit_node = v;
+        *bonus = (int32_t)y;
+        *accept_len = depth[v] + 1;
+        break;
+    }
+    free(avail);
+    free(kids);
+    free(mu);
+    free(depth);
+    return st;
+}
+
+/* Repeated draws of the two verifiers above (draw i on tree index first_tree + i). */
+int orc_seqres_sample_many(const double *z, const int32_t *parent, const int32_t *token, int n,
+                           int64_t V, double T, uint64_t seed, uint64_t first_tree,
+                           int64_t n_draws, int32_t *exit_out, int32_t *bonus_out)
+{
+    int32_t al;
+    int st = ORC_OK;
+    for (int64_t i = 0; i < n_draws && !st; ++i)
+        st = orc_seqres(z, parent, token, n, V, T, seed, first_tree + (uint64_t)i, exit_out + i,
+                        bonus_out + i, &al);
+    return st;
+}
+
+int orc_proposal_sample_many(const double *z, const int32_t *parent, const int32_t *token, int n,
+                             int64_t V, double T, const double *q_child, uint64_t seed,
+                             uint64_t first_tree, int64_t n_draws, int32_t *exit_out,
+                             int32_t *bonus_out)
+{
+    int32_t al;
+    int st = ORC_OK;
+    for (int64_t i = 0; i < n_draws && !st; ++i)
+        st = orc_proposal(z, parent, token, n, V, T, q_child, seed, first_tree + (uint64_t)i,
+                          exit_out + i, bonus_out + i, &al);
+    return st;
 }

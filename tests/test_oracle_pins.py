@@ -689,3 +689,99 @@ def test_exit_loss_temperature_is_a_logit_scale(orc):
     a = orc.exit_loss(z, 1.6, token, depth, len(token), omega)
     b = orc.exit_loss(z / 1.6, 1.0, token, depth, len(token), omega)
     assert a == pytest.approx(b, rel=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Sequential residual ([EXIT] App. A.4.2) and proposal-aware ([CAST] App. B.1
+# Thm. 3) verification
+# ---------------------------------------------------------------------------
+def _proposal_for(tr, n, dr, T_d=1.0, flat=False):
+    """q_child[u]: the drafter's probability of node u's token at u's position,
+    or (flat) a deliberately mismatched proposal -- the same for every child."""
+    q = np.zeros(n)
+    for u in range(1, n):
+        d = int(tr["depth"][u])
+        q[u] = 1.0 if flat else scipy.special.softmax(dr[d - 1] / T_d)[int(tr["token"][u])]
+    return q
+
+
+@pytest.mark.parametrize("kind,flat", [("seqres", False), ("proposal", False), ("proposal", True)])
+def test_new_verifiers_realise_the_exact_law(orc, kind, flat):
+    """Chi-square over 10^6 seeded draws against the brute-force joint law of
+    (exit node, bonus token), and against TEV's draws [EXIT Eq. 51-53; CAST
+    Thm. 3: each committed token follows p_v]."""
+    dr, tr, n, tgt = tiny_tree(orc, 4243)
+    par, tok = tr["parent"], tr["token"]
+    T = 1.0
+    joint, _, _ = brute_force_continuations(tgt, par, tok, n, T)
+    N = 1_000_000
+    q = _proposal_for(tr, n, dr, flat=flat) if kind == "proposal" else None
+    ex, bo = orc.sample_many(kind, tgt, par, tok, n, T, seed=777, n_draws=N, q_child=q)
+    cells = ex.astype(np.int64) * tgt.shape[1] + bo
+    obs = np.bincount(cells, minlength=joint.size).astype(float)
+    exp = joint.ravel() * N
+    assert obs[exp == 0].sum() == 0
+    keep = exp >= 5
+    o = np.append(obs[keep], obs[~keep].sum())
+    e = np.append(exp[keep], exp[~keep].sum())
+    assert scipy.stats.chisquare(o, e * o.sum() / e.sum()).pvalue > 1e-4
+    ta, _ = orc.sample_many("tev", tgt, par, tok, n, T, seed=778, n_draws=N)
+    a, b = np.bincount(ta, minlength=n), np.bincount(ex, minlength=n)
+    m = (a + b) > 0
+    assert scipy.stats.chi2_contingency(np.vstack([a[m], b[m]]))[1] > 1e-4
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_new_verifiers_greedy_is_argmax_walk(orc, seed):
+    dr, tr, n, tgt = tiny_tree(orc, 600 + seed)
+    par, tok = tr["parent"], tr["token"]
+    ch = children_of(par, n)
+    v = 0
+    while True:
+        a = int(np.argmax(tgt[v]))
+        nxt = [u for u in ch[v] if int(tok[u]) == a]
+        if not nxt:
+            break
+        v = nxt[0]
+    q = _proposal_for(tr, n, dr)
+    for s in range(3):
+        r = orc.seqres(tgt, par, tok, n, 0.0, seed=s)
+        assert (r["exit_node"], r["bonus"]) == (v, int(np.argmax(tgt[v])))
+        r = orc.proposal(tgt, par, tok, n, 0.0, q, seed=s)
+        assert (r["exit_node"], r["bonus"]) == (v, int(np.argmax(tgt[v])))
+
+
+def _numpy_uniform_sub(seed, tree, node, stream, sub):
+    x0 = int(_numpy_philox_block((tree, node, stream, sub), (seed, 0))[0])
+    return (x0 >> 40) * 2.0**-24
+
+
+def test_seqres_decisions_from_the_stated_uniforms(orc):
+    """The walk recomputed from brute-force probabilities and numpy-Philox
+    uniforms (stream 3 sub j for child j in token order, stream 4 for the
+    bonus): nothing from the oracle."""
+    _, tr, n, tgt = tiny_tree(orc, 9191)
+    par, tok = tr["parent"], tr["token"]
+    T = 0.8
+    probs = [probs_library(tgt[v], T) for v in range(n)]
+    ch = children_of(par, n)
+    for tree in range(200):
+        v = 0
+        while True:
+            kids = sorted(ch[v], key=lambda u: int(tok[u]))
+            M, nxt = 0.0, None
+            for j, u in enumerate(kids):
+                pj = probs[v][int(tok[u])]
+                if _numpy_uniform_sub(3, tree, v, 3, j) * (1.0 - M) < pj:
+                    nxt = u
+                    break
+                M += pj
+            if nxt is None:
+                break
+            v = nxt
+        res = probs[v].copy()
+        res[[int(tok[u]) for u in ch[v]]] = 0.0
+        cr = np.cumsum(res)
+        bo = int(np.argmax(cr > _numpy_uniform_sub(3, tree, v, 4, 0) * cr[-1]))
+        r = orc.seqres(tgt, par, tok, n, T, seed=3, tree=tree)
+        assert (r["exit_node"], r["bonus"]) == (v, bo), tree
