@@ -291,7 +291,8 @@ def run_ours(args):
     if e2e_copy is not None:
         extra["e2e_explicit_copies"] = e2e_copy
     if rank == 0 and not args.no_extra:
-        extra.update(secondary(tsd, torch, synth, dev, stream, last[0], target, T, ws_v, V))
+        extra.update(secondary(tsd, torch, synth, dev, stream, dict(last[0], _drafter=drafter),
+                               target, T, ws_v, V))
         extra.update(exit_loss_bench(tsd, torch, stream, drafter, last[0], last[1], V))
 
     if rank != 0:
@@ -363,8 +364,20 @@ def exit_loss_bench(tsd, torch, stream, drafter, tree, tev, V):
 
 def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
     out = {}
-    # verifier stage: TEV vs predraw-and-follow on the same 32 trees
-    for name, fn in (("tev", tsd.tsd_verify_tev), ("predraw", tsd.tsd_verify_ddtree)):
+    # verifier stage: TEV vs predraw-and-follow, sequential residual and
+    # proposal-aware verification on the same 32 trees; the proposal is the
+    # drafter's own probability of each child's token (setup, not timed)
+    drafter = tree["_drafter"]
+    depth = tree["depth"].clamp(min=1).long() - 1
+    logq = torch.log_softmax(drafter[:, 0].float(), dim=-1)           # [nt, L, V]
+    q = torch.stack([logq[t, depth[t], tree["token"][t].clamp(min=0).long()].exp()
+                     for t in range(drafter.shape[0])]).float().contiguous()
+    del logq
+    verifiers = (("tev", tsd.tsd_verify_tev), ("predraw", tsd.tsd_verify_ddtree),
+                 ("seqres", tsd.tsd_verify_seqres),
+                 ("proposal", lambda x, p_, t_, n_, T_, seed, workspace:
+                  tsd.tsd_verify_proposal(x, p_, t_, n_, q, T_, seed=seed, workspace=workspace)))
+    for name, fn in verifiers:
         for i in range(3):
             fn(target, tree["parent"], tree["token"], tree["n_nodes"], T, seed=i, workspace=ws_v)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

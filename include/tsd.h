@@ -43,7 +43,9 @@
  *   - Randomness: the seed is the only source of the auxiliary randomness of
  *     [EXIT] Sec. 3.  Uniforms are Philox4x64-10 (Salmon et al., SC'11) with
  *     counter (tree, node, stream, 0) and key (seed, 0), u = (x0 >> 40) 2^-24;
- *     stream 0 = TEV exit draw, 1 = TEV bonus draw, 2 = predraw at `node`.
+ *     stream 0 = TEV exit draw, 1 = TEV bonus draw, 2 = predraw at `node`;
+ *     streams 3-7 (with a sub-index in the counter's last word) belong to the
+ *     sequential-residual and proposal-aware verifiers below.
  */
 #ifndef TSD_H
 #define TSD_H
@@ -210,6 +212,45 @@ tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const i
                              int32_t *bonus_token, int32_t *accept_len, int32_t *draws,
                              int32_t *status, void *workspace, size_t ws_bytes,
                              cudaStream_t stream);
+
+/*
+ * tsd_verify_seqres -- exact sequential residual verification ([EXIT] App.
+ * A.4.2 Eq. 45-53), another exact verifier over the same row statistics as
+ * TEV: from the root, the children of the current node are tested in
+ * ascending token order; child j is followed when u (1 - M_{j-1}) < p_j
+ * (Eq. 49; p_j = p_v(x_j), M the sum of the earlier p's; uniform stream 3,
+ * sub-index j).  If every child is rejected the walk exits and the bonus
+ * token is drawn from the residual of Eq. 53 (stream 4), as TEV draws its
+ * own.  Arguments, workspace (tsd_workspace_size(TSD_OP_VERIFY_TEV, ...)) and
+ * errors as tsd_verify_tev; outputs exit_node, bonus_token, accept_len,
+ * status [n_trees].
+ */
+tsd_status tsd_verify_seqres(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
+                             const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
+                             int64_t V, float temperature, uint64_t seed, int32_t *exit_node,
+                             int32_t *bonus_token, int32_t *accept_len, int32_t *status,
+                             void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsd_verify_proposal -- proposal-aware verification ([CAST] App. B.1 Thm. 3,
+ * recursive speculative sampling without replacement) at every visited
+ * node: the residual mu starts at p_v; a candidate child c is drawn from the
+ * proposal renormalised over the retained children, q~ (inverse CDF in
+ * ascending token order, stream 5, sub-index = step), and followed when
+ * u q~(c) < mu(c) (stream 6); a rejection sets mu <- (mu - q~)_+ normalised
+ * and retires c.  With every child retired, the committed token is drawn
+ * from mu (stream 7) and the walk exits.
+ * q_child  [n_trees][B+1] fp32 (device): q_{pa(u)}(x_u), the proposal's
+ *          probability of node u's token (entry 0 unused); it must be
+ *          positive and finite on every child, else the tree's status is
+ *          TSD_ERR_NONFINITE.  Other arguments as tsd_verify_seqres.
+ */
+tsd_status tsd_verify_proposal(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
+                               const int32_t *token, const int32_t *n_nodes, const float *q_child,
+                               int n_trees, int B, int64_t V, float temperature, uint64_t seed,
+                               int32_t *exit_node, int32_t *bonus_token, int32_t *accept_len,
+                               int32_t *status, void *workspace, size_t ws_bytes,
+                               cudaStream_t stream);
 
 /*
  * tsd_exit_loss -- the exit-guided loss of ExitTrain ([EXIT] Sec. 5 Eq. 14),

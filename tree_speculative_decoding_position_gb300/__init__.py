@@ -18,7 +18,8 @@ import torch
 
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
            "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
-           "tsd_verify_tev_noalloc", "tsd_exit_loss", "LIB_PATH"]
+           "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
+           "tsd_verify_proposal", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
 
@@ -63,8 +64,12 @@ def load():
                                       P, P, P, P, P, P, sz, P]
     lib.tsd_exit_loss.argtypes = [P, i32, i32, i32, i64, f32, P, P, P, i32, P, P, P, P, P, P,
                                   sz, P]
+    lib.tsd_verify_seqres.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64, P, P, P, P, P, sz, P]
+    lib.tsd_verify_proposal.argtypes = [P, i32, P, P, P, P, i32, i32, i64, f32, u64, P, P, P, P, P,
+                                        sz, P]
     for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
-              "tsd_verify_ddtree", "tsd_verify_tev_noalloc", "tsd_exit_loss"):
+              "tsd_verify_ddtree", "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
+              "tsd_verify_proposal"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -352,3 +357,48 @@ def tsd_exit_loss(drafter_logits: torch.Tensor, token: torch.Tensor, depth: torc
     if st != TSD_OK:
         raise TsdError(st, "tsd_exit_loss")
     return out
+
+
+def _walk_verifier(name, target_logits, parent, token, n_nodes, temperature, seed, workspace,
+                   q_child=None):
+    x, parent, token, n_nodes, n_trees, B, V = _verify_common(target_logits, parent, token, n_nodes)
+    dev = parent.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, **i32) for k in ("exit_node", "bonus_token", "accept_len", "status")}
+    nbytes = tsd_workspace_size(TSD_OP_VERIFY_TEV, n_trees, 1, 1, V, 1, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, name)
+    ws = _workspace(nbytes, dev, workspace)
+    lib = load()
+    with torch.cuda.device(dev):
+        head = [_ptr(x), _dtype_code(x), _ptr(parent), _ptr(token), _ptr(n_nodes)]
+        if q_child is not None:
+            q_child = _cuda(q_child, "q_child", torch.float32)
+            if tuple(q_child.shape) != (n_trees, B + 1):
+                raise ValueError("q_child must be [n_trees, B+1]")
+            head.append(_ptr(q_child))
+        st = getattr(lib, name)(*head, n_trees, B, V, temperature, seed, _ptr(out["exit_node"]),
+                                _ptr(out["bonus_token"]), _ptr(out["accept_len"]),
+                                _ptr(out["status"]), _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, name)
+    return out
+
+
+def tsd_verify_seqres(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
+                      n_nodes: torch.Tensor, temperature: float, seed: int,
+                      workspace=None) -> dict:
+    """Exact sequential residual verification ([EXIT] App. A.4.2).  Returns
+    exit_node, bonus_token, accept_len, status ([n_trees])."""
+    return _walk_verifier("tsd_verify_seqres", target_logits, parent, token, n_nodes, temperature,
+                          seed, workspace)
+
+
+def tsd_verify_proposal(target_logits: torch.Tensor, parent: torch.Tensor, token: torch.Tensor,
+                        n_nodes: torch.Tensor, q_child: torch.Tensor, temperature: float, seed: int,
+                        workspace=None) -> dict:
+    """Proposal-aware verification ([CAST] App. B.1 Thm. 3).  q_child:
+    [n_trees, B+1] float32, the proposal's probability of each node's token
+    under its parent.  Returns exit_node, bonus_token, accept_len, status."""
+    return _walk_verifier("tsd_verify_proposal", target_logits, parent, token, n_nodes, temperature,
+                          seed, workspace, q_child=q_child)

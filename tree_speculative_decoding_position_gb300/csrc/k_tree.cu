@@ -87,6 +87,82 @@ __device__ int draw_in_chunk_block(const T* __restrict__ rp, int64_t c0, int cn,
     return r;
 }
 
+// The residual draw of [EXIT] Eq. 7 at exit node V_ of tree t, by the whole
+// block (every thread calls it; the result is the same in all): the token a
+// (ascending, drafted children skipped) at which the running residual mass
+// first exceeds u * rho(V_), from the stored per-chunk residual sums, then
+// only that chunk of row V_ is read again.  At T = 0 it is the row's
+// arg-max, which is not a child of V_.  Returns -1 if the row has no
+// residual mass.
+template <typename T>
+__device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, int B, int64_t V,
+                                   int nch, float c, bool greedy, float u, const VerifyWs& ws,
+                                   float* red, int* pick) {
+    const int stride = B + 1;
+    const int64_t row = (int64_t)t * stride + V_;
+    const NodeStat ns = ws.node[row];
+    int y;
+    if (greedy) {
+        y = ns.amax;  // Line 9 at T = 0: the arg-max is not a child of the exit node
+    } else {
+        // Line 9: residual draw.  Chunk sums relative to the row reference.
+        const ChunkStat* cs = ws.chunk + row * nch;
+        const float thr2 = u * ns.r;
+        __shared__ int chunk_sel;
+        __shared__ float chunk_frac;
+        if (threadIdx.x < kWarp) {
+            const int lane = threadIdx.x;
+            float base = 0.0f;
+            int sel = -1, lastc = -1;
+            float frac = 0.0f;
+            for (int q0 = 0; q0 < nch && sel < 0; q0 += kWarp) {
+                const int q = q0 + lane;
+                float rq = 0.0f;
+                if (q < nch && cs[q].m != -INFINITY) rq = cs[q].r * ex2(__fmul_rn(cs[q].m, c) - ns.mc);
+                const float inc = warp_incl_scan(rq, lane) + base;
+                const unsigned hit = __ballot_sync(0xffffffffu, inc > thr2 && rq > 0.0f);
+                const unsigned pos = __ballot_sync(0xffffffffu, rq > 0.0f);
+                if (pos) lastc = q0 + 31 - __clz(pos);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    sel = q0 + l;
+                    const float incl = __shfl_sync(0xffffffffu, inc, l);
+                    const float own = __shfl_sync(0xffffffffu, rq, l);
+                    frac = (thr2 - (incl - own)) / own;
+                }
+                base = __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (sel < 0) {  // rounding left the threshold past the last chunk
+                sel = lastc;
+                frac = 1.0f;
+            }
+            if (lane == 0) {
+                chunk_sel = sel;
+                chunk_frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
+            }
+        }
+        __syncthreads();
+        const int q = chunk_sel;
+        y = -1;
+        if (q >= 0) {
+            constexpr int CE = kChunkBytes / (int)sizeof(T);
+            const int64_t c0 = (int64_t)q * CE;
+            const int cn = (int)min((int64_t)CE, V - c0);
+            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+            const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+            int clo = cptr[V_], chi = cptr[V_ + 1];
+            while (clo < chi && ctok[clo] < c0) ++clo;  // children are sorted by token
+            int chh = clo;
+            while (chh < chi && ctok[chh] < c0 + cn) ++chh;
+            const int o = draw_in_chunk_block<T>(logits + row * V + c0, c0, cn, c,
+                                                 __fmul_rn(cs[q].m, c), chunk_frac, ctok, clo,
+                                                 chh, red, pick);
+            y = o >= 0 ? (int)(c0 + o) : -1;
+        }
+    }
+    return y;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kTreeThreads)
 tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, bool greedy,
@@ -176,67 +252,8 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
     if (threadIdx.x == 0) exit_v = pick[0] != INT_MAX ? pick[0] : (pick[1] >= 0 ? pick[1] : 0);
     __syncthreads();
     const int V_ = exit_v;
-    const int64_t row = (int64_t)t * stride + V_;
-    const NodeStat ns = ws.node[row];
-    int y;
-    if (greedy) {
-        y = ns.amax;  // Line 9 at T = 0: the arg-max is not a child of the exit node
-    } else {
-        // Line 9: residual draw.  Chunk sums relative to the row reference.
-        const ChunkStat* cs = ws.chunk + row * nch;
-        const float thr2 = uniform24(seed, t, 0, 1) * ns.r;
-        __shared__ int chunk_sel;
-        __shared__ float chunk_frac;
-        if (threadIdx.x < kWarp) {
-            const int lane = threadIdx.x;
-            float base = 0.0f;
-            int sel = -1, lastc = -1;
-            float frac = 0.0f;
-            for (int q0 = 0; q0 < nch && sel < 0; q0 += kWarp) {
-                const int q = q0 + lane;
-                float rq = 0.0f;
-                if (q < nch && cs[q].m != -INFINITY) rq = cs[q].r * ex2(__fmul_rn(cs[q].m, c) - ns.mc);
-                const float inc = warp_incl_scan(rq, lane) + base;
-                const unsigned hit = __ballot_sync(0xffffffffu, inc > thr2 && rq > 0.0f);
-                const unsigned pos = __ballot_sync(0xffffffffu, rq > 0.0f);
-                if (pos) lastc = q0 + 31 - __clz(pos);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    sel = q0 + l;
-                    const float incl = __shfl_sync(0xffffffffu, inc, l);
-                    const float own = __shfl_sync(0xffffffffu, rq, l);
-                    frac = (thr2 - (incl - own)) / own;
-                }
-                base = __shfl_sync(0xffffffffu, inc, 31);
-            }
-            if (sel < 0) {  // rounding left the threshold past the last chunk
-                sel = lastc;
-                frac = 1.0f;
-            }
-            if (lane == 0) {
-                chunk_sel = sel;
-                chunk_frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
-            }
-        }
-        __syncthreads();
-        const int q = chunk_sel;
-        y = -1;
-        if (q >= 0) {
-            constexpr int CE = kChunkBytes / (int)sizeof(T);
-            const int64_t c0 = (int64_t)q * CE;
-            const int cn = (int)min((int64_t)CE, V - c0);
-            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-            const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
-            int clo = cptr[V_], chi = cptr[V_ + 1];
-            while (clo < chi && ctok[clo] < c0) ++clo;  // children are sorted by token
-            int chh = clo;
-            while (chh < chi && ctok[chh] < c0 + cn) ++chh;
-            const int o = draw_in_chunk_block<T>(logits + row * V + c0, c0, cn, c,
-                                                 __fmul_rn(cs[q].m, c), chunk_frac, ctok, clo,
-                                                 chh, red, pick);
-            y = o >= 0 ? (int)(c0 + o) : -1;
-        }
-    }
+    const int y = residual_draw_block<T>(logits, t, V_, B, V, nch, c, greedy,
+                                         uniform24(seed, t, 0, 1), ws, red, pick);
     if (threadIdx.x == 0) {
         exit_node[t] = V_;
         bonus[t] = y;
@@ -429,6 +446,214 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
     if (cudaError_t e_ = launch_pdl(predraw_walk_kernel, (n_trees + 127) / 128, 128, 0, stream, n_trees, B, n_nodes, ws, exit_node,
                                                                  bonus, accept_len, draws, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Exact sequential residual verification ([EXIT] App. A.4.2) and
+// proposal-aware verification ([CAST] App. B.1 Thm. 3): one CTA per tree.
+// Thread 0 walks from the root on the per-node statistics of the row
+// reduction (p_v(x_u) of every child, rho(v)); the whole block then draws the
+// bonus token from the exit node's residual, as TEV's last step does.  At
+// each node the children are taken in ascending token order (the CSR lists
+// are sorted by token).
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ void finish_walk(const T* __restrict__ logits, int t, int v, int B, int64_t V, int nch,
+                            float c, bool greedy, float u_bonus, const VerifyWs& ws,
+                            int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
+                            int32_t* status, float* red, int* pick) {
+    const int y = residual_draw_block<T>(logits, t, v, B, V, nch, c, greedy, u_bonus, ws, red, pick);
+    if (threadIdx.x == 0) {
+        exit_node[t] = v;
+        bonus[t] = y;
+        accept_len[t] = ws.depth[(int64_t)t * (B + 1) + v] + 1;
+        status[t] = y >= 0 ? kStatOk : kStatNonFinite;
+    }
+}
+
+__device__ __forceinline__ bool tree_failed(int t, int st, int32_t* exit_node, int32_t* bonus,
+                                            int32_t* accept_len, int32_t* status) {
+    if (st == kStatOk) return false;
+    if (threadIdx.x == 0) {
+        exit_node[t] = -1;
+        bonus[t] = -1;
+        accept_len[t] = 0;
+        status[t] = st;
+    }
+    return true;
+}
+
+// Children u_1..u_k of the current node are tested in turn; u_j is followed
+// when u_j (1 - M_{j-1}) < p_j (Eq. 49, uniform stream 3, sub j-1), where p_j
+// = p_v(x_j) and M_{j-1} sums the earlier p's.  With every child rejected the
+// walk exits and the bonus is drawn from the Eq. 53 residual (stream 4).
+template <typename T>
+__global__ void __launch_bounds__(kTreeThreads)
+seqres_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, bool greedy,
+                   uint64_t seed, VerifyWs ws, int32_t* __restrict__ exit_node,
+                   int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
+                   int32_t* __restrict__ status) {
+    pdl_entry();
+    __shared__ float red[33];
+    __shared__ int pick[2];
+    __shared__ int exit_v;
+    const int t = blockIdx.x;
+    if (tree_failed(t, ws.tstat[t], exit_node, bonus, accept_len, status)) return;
+    if (threadIdx.x == 0) {
+        const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+        const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
+        const float* pedge = ws.pedge + (int64_t)t * (B + 1);
+        int v = 0;
+        for (;;) {
+            float M = 0.0f;
+            int next = -1;
+            for (int q = cptr[v]; q < cptr[v + 1]; ++q) {
+                const float pj = pedge[cnode[q]];
+                if (uniform24(seed, t, v, 3, q - cptr[v]) * (1.0f - M) < pj) {
+                    next = cnode[q];
+                    break;
+                }
+                M += pj;
+            }
+            if (next < 0) break;
+            v = next;
+        }
+        exit_v = v;
+    }
+    __syncthreads();
+    const int v = exit_v;
+    finish_walk<T>(logits, t, v, B, V, nch, c, greedy, uniform24(seed, t, v, 4), ws, exit_node,
+                   bonus, accept_len, status, red, pick);
+}
+
+// Recursive speculative sampling without replacement at each visited node.
+// mu starts at p_v: on the children it is held explicitly (mu_c), on the
+// other tokens as s * p_v (s starts at 1; their total is s * rho(v)).  Each
+// step draws a candidate from q~ = q over the retained children, normalised
+// (inverse CDF in token order, stream 5, sub = step), and accepts it when
+// u q~(c) < mu_c (stream 6, sub = step).  A rejection sets mu <- (mu - q~)_+
+// normalised and retires c.  With every child retired the committed token is
+// drawn from mu, which is then zero on the children: the residual draw of
+// the exit node (stream 7).  q_child[u] = q_{pa(u)}(x_u); a non-positive or
+// non-finite value marks the tree TSD_ERR_NONFINITE.
+template <typename T>
+__global__ void __launch_bounds__(kTreeThreads)
+proposal_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c,
+                     bool greedy, uint64_t seed, const float* __restrict__ q_child, VerifyWs ws,
+                     int32_t* __restrict__ exit_node, int32_t* __restrict__ bonus,
+                     int32_t* __restrict__ accept_len, int32_t* __restrict__ status) {
+    pdl_entry();
+    extern __shared__ float shp[];  // mu_c and q of the current node's children, [2][B]
+    __shared__ float red[33];
+    __shared__ int pick[2];
+    __shared__ int exit_v, bad;
+    const int t = blockIdx.x;
+    if (tree_failed(t, ws.tstat[t], exit_node, bonus, accept_len, status)) return;
+    if (threadIdx.x == 0) {
+        const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+        const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
+        const float* pedge = ws.pedge + (int64_t)t * (B + 1);
+        const float* qc = q_child + (int64_t)t * (B + 1);
+        float* mu = shp;
+        float* qv = shp + B;
+        int v = 0;
+        bad = 0;
+        for (;;) {
+            const int b0 = cptr[v], k = cptr[v + 1] - b0;
+            for (int j = 0; j < k; ++j) {
+                mu[j] = pedge[cnode[b0 + j]];
+                qv[j] = qc[cnode[b0 + j]];
+                if (!(qv[j] > 0.0f) || isinf(qv[j])) bad = 1;
+            }
+            if (bad) break;
+            const float rho = ws.rho[(int64_t)t * (B + 1) + v];
+            float s = 1.0f;  // scale of the non-child tokens
+            int next = -1;
+            for (int step = 0; step < k; ++step) {
+                float Q = 0.0f;
+                for (int j = 0; j < k; ++j)
+                    if (qv[j] > 0.0f) Q += qv[j];
+                const float thr = uniform24(seed, t, v, 5, step) * Q;
+                float cum = 0.0f;
+                int cand = -1, lastj = -1;
+                for (int j = 0; j < k; ++j) {
+                    if (!(qv[j] > 0.0f)) continue;  // retired
+                    lastj = j;
+                    cum += qv[j];
+                    if (cum > thr) {
+                        cand = j;
+                        break;
+                    }
+                }
+                if (cand < 0) cand = lastj;
+                const float qt = qv[cand] / Q;
+                if (uniform24(seed, t, v, 6, step) * qt < mu[cand]) {
+                    next = cnode[b0 + cand];
+                    break;
+                }
+                float z = s * rho;  // (mu - q~)_+ and its total
+                for (int j = 0; j < k; ++j) {
+                    if (!(qv[j] > 0.0f)) continue;
+                    mu[j] = fmaxf(mu[j] - qv[j] / Q, 0.0f);
+                    z += mu[j];
+                }
+                if (!(z > 0.0f)) {
+                    bad = 1;
+                    break;
+                }
+                const float inv = 1.0f / z;
+                s *= inv;
+                for (int j = 0; j < k; ++j) mu[j] *= inv;
+                mu[cand] = 0.0f;
+                qv[cand] = -1.0f;  // retired
+            }
+            if (bad || next < 0) break;
+            v = next;
+        }
+        exit_v = v;
+    }
+    __syncthreads();
+    if (bad) {
+        tree_failed(t, kStatNonFinite, exit_node, bonus, accept_len, status);
+        return;
+    }
+    const int v = exit_v;
+    finish_walk<T>(logits, t, v, B, V, nch, c, greedy, uniform24(seed, t, v, 7), ws, exit_node,
+                   bonus, accept_len, status, red, pick);
+}
+
+cudaError_t launch_seqres_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                               float c, bool greedy, uint64_t seed, const VerifyWs& ws,
+                               int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
+                               int32_t* status, cudaStream_t stream) {
+    const int nch = (int)n_chunks(V, dtype == TSD_BF16 ? 2 : 4);
+    if (dtype == TSD_BF16)
+        return launch_pdl(seqres_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kTreeThreads, 0,
+                          stream, static_cast<const __nv_bfloat16*>(logits), B, V, nch, c, greedy,
+                          seed, ws, exit_node, bonus, accept_len, status);
+    return launch_pdl(seqres_tree_kernel<float>, (unsigned)n_trees, kTreeThreads, 0, stream,
+                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, ws, exit_node,
+                      bonus, accept_len, status);
+}
+
+cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                                 float c, bool greedy, uint64_t seed, const float* q_child,
+                                 const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                                 int32_t* accept_len, int32_t* status, cudaStream_t stream) {
+    const int nch = (int)n_chunks(V, dtype == TSD_BF16 ? 2 : 4);
+    const size_t smem = 2 * sizeof(float) * (size_t)(B > 0 ? B : 1);
+    cudaError_t e = cudaFuncSetAttribute(dtype == TSD_BF16
+                                             ? (const void*)proposal_tree_kernel<__nv_bfloat16>
+                                             : (const void*)proposal_tree_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dtype == TSD_BF16)
+        return launch_pdl(proposal_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kTreeThreads,
+                          smem, stream, static_cast<const __nv_bfloat16*>(logits), B, V, nch, c,
+                          greedy, seed, q_child, ws, exit_node, bonus, accept_len, status);
+    return launch_pdl(proposal_tree_kernel<float>, (unsigned)n_trees, kTreeThreads, smem, stream,
+                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, q_child, ws,
+                      exit_node, bonus, accept_len, status);
 }
 
 }  // namespace tsd

@@ -326,6 +326,69 @@ tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const i
     return TSD_OK;
 }
 
+// Argument checks, workspace and the three kernels every verifier shares
+// (tree preparation, row reduction, per-node combination).
+static tsd_status verify_front(const void** target_logits, tsd_dtype dtype, const int32_t* parent,
+                               const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                               int64_t V, float temperature, const int32_t* exit_node,
+                               const int32_t* bonus_token, const int32_t* accept_len,
+                               const int32_t* status, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream, VerifyWs* ws, float* c, bool* greedy) {
+    if (!verify_args_ok(*target_logits, dtype, parent, token, n_nodes, n_trees, B, V, temperature,
+                        exit_node, bonus_token, accept_len, status))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(*target_logits, target_logits)) return TSD_ERR_INVALID_ARG;
+    verify_ws_layout(n_trees, B, V, es, workspace, ws);
+    *greedy = temperature == 0.0f;
+    *c = *greedy ? 1.0f : exp2_scale(temperature);
+    if (launch_verify_prep(parent, token, n_nodes, n_trees, B, V, *ws, stream) != cudaSuccess ||
+        launch_rows(*target_logits, dtype, n_trees, B, V, *c, *greedy, n_nodes, *ws, stream) != cudaSuccess ||
+        launch_node_combine(*target_logits, dtype, n_trees, B, V, *c, *greedy, n_nodes, *ws, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_verify_seqres(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                             const int32_t* token, const int32_t* n_nodes, int n_trees, int B,
+                             int64_t V, float temperature, uint64_t seed, int32_t* exit_node,
+                             int32_t* bonus_token, int32_t* accept_len, int32_t* status,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    VerifyWs ws;
+    float c;
+    bool greedy;
+    const tsd_status st = verify_front(&target_logits, dtype, parent, token, n_nodes, n_trees, B, V,
+                                       temperature, exit_node, bonus_token, accept_len, status,
+                                       workspace, ws_bytes, stream, &ws, &c, &greedy);
+    if (st != TSD_OK) return st;
+    if (launch_seqres_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, ws, exit_node,
+                           bonus_token, accept_len, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_verify_proposal(const void* target_logits, tsd_dtype dtype, const int32_t* parent,
+                               const int32_t* token, const int32_t* n_nodes, const float* q_child,
+                               int n_trees, int B, int64_t V, float temperature, uint64_t seed,
+                               int32_t* exit_node, int32_t* bonus_token, int32_t* accept_len,
+                               int32_t* status, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream) {
+    if (!q_child) return TSD_ERR_INVALID_ARG;
+    VerifyWs ws;
+    float c;
+    bool greedy;
+    const tsd_status st = verify_front(&target_logits, dtype, parent, token, n_nodes, n_trees, B, V,
+                                       temperature, exit_node, bonus_token, accept_len, status,
+                                       workspace, ws_bytes, stream, &ws, &c, &greedy);
+    if (st != TSD_OK) return st;
+    if (launch_proposal_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, q_child, ws,
+                             exit_node, bonus_token, accept_len, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
 tsd_status tsd_exit_loss(const void* drafter_logits, tsd_dtype dtype, int n_trees, int L,
                          int64_t V, float drafter_temp, const int32_t* token, const int32_t* depth,
                          const int32_t* n_nodes, int B, const float* omega, double* loss_tree,

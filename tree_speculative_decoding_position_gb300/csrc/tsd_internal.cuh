@@ -68,8 +68,8 @@ __device__ __forceinline__ uint64_t philox_x0(uint64_t c0, uint64_t c1, uint64_t
 
 // The uniform on the 2^-24 grid for (seed; tree, node, stream).
 __device__ __forceinline__ float uniform24(uint64_t seed, uint64_t tree, uint64_t node,
-                                           uint64_t stream) {
-    const uint64_t x0 = philox_x0(tree, node, stream, 0, seed, 0);
+                                           uint64_t stream, uint64_t sub = 0) {
+    const uint64_t x0 = philox_x0(tree, node, stream, sub, seed, 0);
     return (float)(x0 >> 40) * (1.0f / 16777216.0f);
 }
 
@@ -301,6 +301,14 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
 cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
                                  int topk, float c, double temp, const BuildWs& ws,
                                  cudaStream_t stream);
+cudaError_t launch_seqres_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                               float c, bool greedy, uint64_t seed, const VerifyWs& ws,
+                               int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
+                               int32_t* status, cudaStream_t stream);
+cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                                 float c, bool greedy, uint64_t seed, const float* q_child,
+                                 const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                                 int32_t* accept_len, int32_t* status, cudaStream_t stream);
 // The drafter's streaming pass alone (ws.chunk and ws.lane_max).
 cudaError_t launch_drafter_chunks(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
                                   float c, const BuildWs& ws, cudaStream_t stream);
