@@ -56,13 +56,14 @@ def _load():
         lib.orc_tev_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_predraw_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_exit_loss.argtypes = [P, i32, i64, f64, P, P, i32, P, P, P]
+        lib.orc_forest_select.argtypes = [P, P, P, i32, i32, i32, f64, f64, P, P, P]
         lib.orc_uniform_sub.argtypes = [u64, u64, u64, u64, u64]
         lib.orc_uniform_sub.restype = f64
         lib.orc_seqres.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P]
         lib.orc_proposal.argtypes = [P, P, P, i32, i64, f64, P, u64, u64, P, P, P]
         lib.orc_seqres_sample_many.argtypes = [P, P, P, i32, i64, f64, u64, u64, i64, P, P]
         lib.orc_proposal_sample_many.argtypes = [P, P, P, i32, i64, f64, P, u64, u64, i64, P, P]
-        for f in ("orc_seqres", "orc_proposal", "orc_seqres_sample_many",
+        for f in ("orc_forest_select", "orc_seqres", "orc_proposal", "orc_seqres_sample_many",
                   "orc_proposal_sample_many", "orc_exit_loss", "orc_drafter_stats", "orc_build_tree", "orc_tree_mask", "orc_row_probs",
                   "orc_tev", "orc_predraw", "orc_tev_sample_many", "orc_predraw_sample_many"):
             getattr(lib, f).restype = ctypes.c_int
@@ -275,3 +276,19 @@ def exit_loss(z, T: float, token, depth, n_nodes: int, omega, with_grad: bool = 
     _check(_load().orc_exit_loss(_ptr(z), L, V, T, _ptr(token), _ptr(depth), n_nodes, _ptr(omega),
                                  _ptr(num), _ptr(grad) if grad is not None else None), "exit_loss")
     return (float(num[0]), grad) if with_grad else float(num[0])
+
+
+def forest_select(scores, depth, n_nodes, M_max: int, l0: float, c1: float) -> dict:
+    """Shared-budget selection over R requests ([CAST] App. B.4 Prop. 2-3):
+    scores, depth [R, stride] in each request's pop order (node 0 the root);
+    returns the per-request widths, the total M* and G(M*)."""
+    scores = _f64(scores)
+    depth = _i32(depth)
+    n_nodes = _i32(n_nodes)
+    R, stride = scores.shape
+    width = np.zeros(R, dtype=np.int32)
+    ms = np.zeros(1, dtype=np.int32)
+    g = np.zeros(1)
+    _check(_load().orc_forest_select(_ptr(scores), _ptr(depth), _ptr(n_nodes), R, stride, M_max,
+                                     l0, c1, _ptr(width), _ptr(ms), _ptr(g)), "forest_select")
+    return dict(width=width, M=int(ms[0]), G=float(g[0]))

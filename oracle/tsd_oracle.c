@@ -16,7 +16,9 @@
  *           -- Sec. 2 Eq. 1 (plug-in score), Thm. 1 (tie order), App. C
  *           "Candidate construction" (top-K heap, push all K children) and
  *           "Packed verification" (ancestor mask, position ids), App. B.1
- *           Thm. 3 (recursive speculative sampling without replacement).
+ *           Thm. 3 (recursive speculative sampling without replacement),
+ *           Sec. 3.3 Thm. 2 and App. B.3-B.4 Prop. 2-3 (cost-aware width,
+ *           shared budget under load).
  *           Sec. 5 Eq. 14 and App. C.2 Eq. 66 (the exit-guided loss), App.
  *           A.4.2 Eq. 45-53 (exact sequential residual verification).
  *   [MFD]   "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
@@ -845,4 +847,57 @@ int orc_proposal_sample_many(const double *z, const int32_t *parent, const int32
         st = orc_proposal(z, parent, token, n, V, T, q_child, seed, first_tree + (uint64_t)i,
                           exit_out + i, bonus_out + i, &al);
     return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Shared budget under load [CAST Sec. 3.3, App. B.4 Prop. 2-3].            */
+/* Each of R requests brings its candidate prefixes in its best-first order  */
+/* (the builder's pop order: scores[r][1..n_r-1] nonincreasing, node 0 the   */
+/* root).  The disjoint union is ranked by prefix mass rho = exp(score)      */
+/* (score desc), ties toward shorter prefixes (depth asc), then request      */
+/* index, then the request's own order (node index).  With the affine round  */
+/* time l(M) = l0 + c1 M, global node M+1 is added while                     */
+/*   rho_(M+1) >= (G(M) + R) / l(M) * c1,   G(M) = sum of the M largest,     */
+/* at most M_max nodes in all.  width[r] = how many of request r's prefixes  */
+/* are among the M* selected; they are its first width[r] nodes.            */
+/*   scores, depth: [R][stride] (stride >= max n_r), n_nodes: [R].          */
+/* ------------------------------------------------------------------------ */
+int orc_forest_select(const double *scores, const int32_t *depth, const int32_t *n_nodes, int R,
+                      int stride, int M_max, double l0, double c1, int32_t *width,
+                      int32_t *M_star, double *G_star)
+{
+    if (R < 1 || stride < 1 || M_max < 0 || !(l0 > 0.0) || !(c1 >= 0.0)) return ORC_ERR_ARG;
+    int *pos = (int *)malloc(sizeof(int) * (size_t)R); /* next node of each request */
+    for (int r = 0; r < R; ++r) {
+        pos[r] = 1;
+        width[r] = 0;
+        if (n_nodes[r] < 0 || n_nodes[r] > stride) { free(pos); return ORC_ERR_ARG; }
+    }
+    double G = 0.0;
+    int M = 0;
+    while (M < M_max) {
+        /* the next global node: the best head among the requests */
+        int best = -1;
+        for (int r = 0; r < R; ++r) {
+            if (pos[r] >= n_nodes[r]) continue;
+            if (best < 0) { best = r; continue; }
+            const double a = scores[(int64_t)r * stride + pos[r]];
+            const double b = scores[(int64_t)best * stride + pos[best]];
+            const int da = depth[(int64_t)r * stride + pos[r]];
+            const int db = depth[(int64_t)best * stride + pos[best]];
+            if (a > b || (a == b && da < db)) best = r; /* equal: the lower index stays */
+        }
+        if (best < 0) break;
+        const double rho = exp(scores[(int64_t)best * stride + pos[best]]);
+        const double l = l0 + c1 * (double)M;
+        if (!(rho >= (G + (double)R) / l * c1)) break;
+        G += rho;
+        ++width[best];
+        ++pos[best];
+        ++M;
+    }
+    *M_star = M;
+    *G_star = G;
+    free(pos);
+    return ORC_OK;
 }

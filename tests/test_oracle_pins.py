@@ -785,3 +785,104 @@ def test_seqres_decisions_from_the_stated_uniforms(orc):
         bo = int(np.argmax(cr > _numpy_uniform_sub(3, tree, v, 4, 0) * cr[-1]))
         r = orc.seqres(tgt, par, tok, n, T, seed=3, tree=tree)
         assert (r["exit_node"], r["bonus"]) == (v, bo), tree
+
+
+# ---------------------------------------------------------------------------
+# Shared budget under load ([CAST] Sec. 3.3 Thm. 2, App. B.4 Prop. 2-3)
+# ---------------------------------------------------------------------------
+def _forest_instance(rng, R, max_n=12):
+    """R requests with random nonincreasing prefix scores (node 0 the root)."""
+    stride = max_n + 1
+    scores = np.full((R, stride), -np.inf)
+    depth = np.zeros((R, stride), dtype=np.int32)
+    n = np.zeros(R, dtype=np.int32)
+    for r in range(R):
+        k = int(rng.integers(0, max_n + 1))
+        s = -rng.exponential(1.0, size=k).cumsum() * rng.uniform(0.05, 0.6)  # decreasing
+        scores[r, 0] = 0.0
+        scores[r, 1:k + 1] = s
+        depth[r, 1:k + 1] = rng.integers(1, 5, size=k)
+        n[r] = k + 1
+    return scores, depth, n
+
+
+def _throughput(masses_sorted, R, l0, c1, M):
+    return (masses_sorted[:M].sum() + R) / (l0 + c1 * M)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_forest_select_maximises_batch_throughput(orc, seed):
+    """Prop. 3 / Thm. 2: the stopping rule's M* maximises (G(M) + R) / l(M)
+    over every allowed total M, G from a brute-force sort of all masses."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 5))
+    scores, depth, n = _forest_instance(rng, R)
+    l0, c1 = float(rng.uniform(0.5, 5)), float(rng.uniform(0.0, 0.4))
+    total = int((n - 1).sum())
+    M_max = int(rng.integers(0, total + 3))
+    out = orc.forest_select(scores, depth, n, M_max, l0, c1)
+    masses = np.sort(np.concatenate([np.exp(scores[r, 1:n[r]]) for r in range(R)]))[::-1]
+    best = max(_throughput(masses, R, l0, c1, M) for M in range(0, min(M_max, total) + 1))
+    assert _throughput(masses, R, l0, c1, out["M"]) == pytest.approx(best, rel=1e-12)
+    assert out["G"] == pytest.approx(masses[:out["M"]].sum(), rel=1e-12)
+    assert out["width"].sum() == out["M"]
+
+
+def test_forest_select_cost_slope_limits(orc):
+    rng = np.random.default_rng(3)
+    scores, depth, n = _forest_instance(rng, 3)
+    total = int((n - 1).sum())
+    assert orc.forest_select(scores, depth, n, 10**6, 1.0, 0.0)["M"] == total  # width is free
+    assert orc.forest_select(scores, depth, n, 5, 1.0, 0.0)["M"] == min(5, total)
+    assert orc.forest_select(scores, depth, n, 10**6, 1.0, 1e9)["M"] == 0  # width is ruinous
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_forest_select_is_the_best_split(orc, seed):
+    """Prop. 2: at its total M*, the selection's summed mass equals the best
+    over every split of M* among the requests (each taking a prefix of its
+    own best-first list), found by exhaustive enumeration."""
+    import itertools
+    rng = np.random.default_rng(100 + seed)
+    R = int(rng.integers(2, 4))
+    scores, depth, n = _forest_instance(rng, R, max_n=6)
+    out = orc.forest_select(scores, depth, n, 10**6, float(rng.uniform(0.5, 3)),
+                            float(rng.uniform(0.0, 0.3)))
+    M = out["M"]
+    best = -1.0
+    for split in itertools.product(*[range(int(n[r])) for r in range(R)]):
+        if sum(split) == M:
+            best = max(best, sum(np.exp(scores[r, 1:1 + split[r]]).sum() for r in range(R)))
+    got = sum(np.exp(scores[r, 1:1 + out["width"][r]]).sum() for r in range(R))
+    assert got == pytest.approx(best, rel=1e-12)
+
+
+def test_forest_select_with_builder_trees_is_prefix_closed(orc):
+    """Composed with the oracle builder: every request keeps the first
+    width[r] nodes of its pop order, a prefix-closed tree."""
+    R, B = 4, 30
+    scores = np.full((R, B + 1), -np.inf)
+    depth = np.zeros((R, B + 1), dtype=np.int32)
+    parents, n = [], np.zeros(R, dtype=np.int32)
+    for r in range(R):
+        dr = synth.tiny_drafter(synth.seed_for(0, 300 + r)).numpy().astype(np.float64)
+        tr = orc.build_tree(orc.drafter_lists(dr, 1.0, 4), B)
+        scores[r, :tr["n_nodes"]] = tr["score"][:tr["n_nodes"]]
+        depth[r, :tr["n_nodes"]] = tr["depth"][:tr["n_nodes"]]
+        n[r] = tr["n_nodes"]
+        parents.append(tr["parent"])
+    out = orc.forest_select(scores, depth, n, 60, 2.0, 0.05)
+    assert 0 < out["M"] <= 60
+    for r in range(R):
+        for u in range(1, 1 + int(out["width"][r])):
+            assert parents[r][u] < 1 + out["width"][r]
+
+
+def test_forest_select_tie_order(orc):
+    """Equal masses: the shorter prefix first, then the lower request index."""
+    scores = np.array([[0.0, -0.5, -0.5], [0.0, -0.5, -0.5]])
+    depth = np.array([[0, 2, 2], [0, 1, 2]], dtype=np.int32)
+    out = orc.forest_select(scores, depth, np.array([3, 3]), 1, 1.0, 0.0)
+    assert out["width"].tolist() == [0, 1]  # request 1's depth-1 node comes first
+    out = orc.forest_select(scores, depth, np.array([3, 3]), 2, 1.0, 0.0)
+    assert out["width"].tolist() == [1, 1]  # then request 0 (depth 2, lower index) before request 1's depth 2
