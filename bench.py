@@ -294,6 +294,7 @@ def run_ours(args):
         extra.update(secondary(tsd, torch, synth, dev, stream, dict(last[0], _drafter=drafter),
                                target, T, ws_v, V))
         extra.update(exit_loss_bench(tsd, torch, stream, drafter, last[0], last[1], V))
+        extra.update(forest_bench(tsd, torch, stream, drafter, k, B))
 
     if rank != 0:
         return
@@ -359,6 +360,48 @@ def exit_loss_bench(tsd, torch, stream, drafter, tree, tev, V):
         out["exit_loss" + ("_with_grad" if grad else "")] = {
             "ms": ms, "algorithmic_gb": nbytes / 1e9, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_of_measured": nbytes / (ms * 1e-3) / 1e9 / measured_peaks()[0]}
+    return out
+
+
+def forest_bench(tsd, torch, stream, drafter, k, B):
+    """Shared-budget widths on the workload's 32 requests, each built to the
+    cap B = 256 and then cut to the globally best M* prefixes under a
+    synthetic linear round-time law t(M) = l0 + c1 M, l0 = 1 (one target
+    call) and c1 = 1/S for a target that doubles its latency at S extra
+    tree tokens.  Times the whole call (builder + selection + trim) against
+    the plain builder on the same inputs, and reports M*, the width spread and
+    the law's objective (G + R) / t(M*)."""
+    out = {}
+    nt, L, V = drafter.shape[0], drafter.shape[2], drafter.shape[3]
+    ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_FOREST, nt, 1, L, V, k, B,
+                                            drafter.dtype), dtype=torch.uint8, device=drafter.device)
+    wsb = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, nt, 1, L, V, k, B,
+                                             drafter.dtype), dtype=torch.uint8, device=drafter.device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(3):
+        tsd.tsd_build_tree(drafter, topk=k, B=B, workspace=wsb)
+    s.record(stream)
+    for i in range(10):
+        tsd.tsd_build_tree(drafter, topk=k, B=B, workspace=wsb)
+    e.record(stream)
+    torch.cuda.synchronize()
+    out["forest_build_tree_ms"] = s.elapsed_time(e) / 10
+    for S in (512, 2048, 8192):
+        c1, M_max = 1.0 / S, nt * B
+        for i in range(3):
+            f = tsd.tsd_build_forest(drafter, topk=k, B=B, M_max=M_max, l0=1.0, c1=c1, workspace=ws)
+        s.record(stream)
+        for i in range(10):
+            f = tsd.tsd_build_forest(drafter, topk=k, B=B, M_max=M_max, l0=1.0, c1=c1, workspace=ws)
+        e.record(stream)
+        torch.cuda.synchronize()
+        w = (f["n_nodes"] - 1).clamp(min=0)
+        M = int(f["total"])
+        G = float(torch.where(f["score"][:, 1:] > -float("inf"), f["score"][:, 1:].double().exp(),
+                              torch.zeros((), dtype=torch.float64, device=w.device)).sum())
+        out["forest_S%d" % S] = {"ms": s.elapsed_time(e) / 10, "M_star": M,
+                                 "width_min": int(w.min()), "width_max": int(w.max()),
+                                 "objective": (G + nt) / (1.0 + c1 * M)}
     return out
 
 

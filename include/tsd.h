@@ -74,7 +74,8 @@ typedef enum {
     TSD_OP_BUILD_TREE = 0,
     TSD_OP_VERIFY_TEV = 1,
     TSD_OP_VERIFY_DDTREE = 2,
-    TSD_OP_EXIT_LOSS = 3
+    TSD_OP_EXIT_LOSS = 3,
+    TSD_OP_BUILD_FOREST = 4
 } tsd_op;
 
 /* Limits checked by every entry point. */
@@ -212,6 +213,33 @@ tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const i
                              int32_t *bonus_token, int32_t *accept_len, int32_t *draws,
                              int32_t *status, void *workspace, size_t ws_bytes,
                              cudaStream_t stream);
+
+/*
+ * tsd_build_forest -- cost-aware tree widths under a budget shared by the
+ * requests of one launch ([CAST] Sec. 3.3 Thm. 2, App. B.4 Prop. 2-3).  Each
+ * request's candidate tree is built as tsd_build_tree builds it (one mode) at
+ * the per-request cap B; the union of the candidates is ranked by prefix mass
+ * exp(score) (ties toward shorter prefixes, then the lower request index,
+ * then the request's own order), and with the affine round time
+ * l(M) = l0 + c1 M the global node M+1 is added while
+ *   mass_(M+1) >= c1 (G(M) + n_trees) / l(M),  G(M) = sum of the M largest,
+ * up to M_max nodes in all.  Every request keeps the first width nodes of its
+ * tree (a prefix-closed tree in pop order); n_nodes = width + 1.
+ *
+ * Inputs as tsd_build_tree with n_modes = 1, plus M_max >= 0, l0 > 0, c1 >= 0
+ * (the round time's intercept and slope, in any one time unit).  The
+ * candidates, n_trees * B, must not exceed 8192 (TSD_ERR_INVALID_ARG).
+ * Outputs: parent, token, depth, score [n_trees][B+1] and n_nodes, status
+ * [n_trees] as tsd_build_tree's (slots past n_nodes cleared); total [1]
+ * int32: the selected node count M*.  Workspace:
+ * tsd_workspace_size(TSD_OP_BUILD_FOREST, n_trees, 1, L, V, topk, B, dtype).
+ */
+#define TSD_MAX_FOREST_CANDIDATES 8192
+tsd_status tsd_build_forest(const void *drafter_logits, tsd_dtype dtype, int n_trees, int L,
+                            int64_t V, int topk, int B, float drafter_temp, int M_max, double l0,
+                            double c1, int32_t *parent, int32_t *token, int32_t *depth,
+                            float *score, int32_t *n_nodes, int32_t *status, int32_t *total,
+                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * tsd_verify_seqres -- exact sequential residual verification ([EXIT] App.

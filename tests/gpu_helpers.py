@@ -24,6 +24,8 @@ SCORE_TOL = 1e-6
 def close(got, want, rtol=RTOL, tiny=TINY):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
+    if got.size == 0 and want.size == 0:
+        return True, 0.0
     err = np.abs(got - want)
     ok = (err <= rtol * np.abs(want)) | ((np.abs(want) < tiny) & (np.abs(got) < tiny * 1e3))
     return bool(np.all(ok)), float(np.max(err / np.maximum(np.abs(want), tiny)))

@@ -19,7 +19,7 @@ import torch
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
            "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
            "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
-           "tsd_verify_proposal", "LIB_PATH"]
+           "tsd_verify_proposal", "tsd_build_forest", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
 
@@ -27,6 +27,7 @@ TSD_OK, TSD_ERR_INVALID_ARG, TSD_ERR_CUDA, TSD_ERR_WORKSPACE = 0, 1, 2, 3
 TSD_ERR_BAD_TREE, TSD_ERR_NONFINITE, TSD_ERR_TIMEOUT = 4, 5, 6
 TSD_BF16, TSD_F32 = 0, 1
 TSD_OP_BUILD_TREE, TSD_OP_VERIFY_TEV, TSD_OP_VERIFY_DDTREE, TSD_OP_EXIT_LOSS = 0, 1, 2, 3
+TSD_OP_BUILD_FOREST = 4
 
 _lib = None
 
@@ -67,9 +68,12 @@ def load():
     lib.tsd_verify_seqres.argtypes = [P, i32, P, P, P, i32, i32, i64, f32, u64, P, P, P, P, P, sz, P]
     lib.tsd_verify_proposal.argtypes = [P, i32, P, P, P, P, i32, i32, i64, f32, u64, P, P, P, P, P,
                                         sz, P]
+    f64 = ctypes.c_double
+    lib.tsd_build_forest.argtypes = [P, i32, i32, i32, i64, i32, i32, f32, i32, f64, f64,
+                                     P, P, P, P, P, P, P, P, sz, P]
     for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
               "tsd_verify_ddtree", "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
-              "tsd_verify_proposal"):
+              "tsd_verify_proposal", "tsd_build_forest"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -402,3 +406,39 @@ def tsd_verify_proposal(target_logits: torch.Tensor, parent: torch.Tensor, token
     under its parent.  Returns exit_node, bonus_token, accept_len, status."""
     return _walk_verifier("tsd_verify_proposal", target_logits, parent, token, n_nodes, temperature,
                           seed, workspace, q_child=q_child)
+
+
+def tsd_build_forest(drafter_logits: torch.Tensor, topk: int, B: int, M_max: int, l0: float,
+                     c1: float, drafter_temp: float = 1.0, workspace=None, device=None) -> dict:
+    """Cost-aware widths under a shared budget ([CAST] App. B.4): one tree per
+    request, built to the cap B, then the globally best M* <= M_max prefixes
+    by the batched stopping rule with round time l0 + c1 M.  drafter_logits:
+    [n_trees, L, V] or [n_trees, 1, L, V].  Returns parent, token, depth,
+    score ([n_trees, B+1]), n_nodes, status ([n_trees]) and total (M*)."""
+    x = _logits(drafter_logits, "drafter_logits")
+    if x.dim() == 3:
+        x = x.reshape(x.shape[0], 1, x.shape[1], x.shape[2])
+    if x.dim() != 4 or x.shape[1] != 1:
+        raise ValueError("drafter_logits must be [n_trees, L, V] (one mode)")
+    n_trees, _, L, V = x.shape
+    dev = x.device if x.is_cuda else (torch.device(device) if device is not None else
+                                      torch.device("cuda", torch.cuda.current_device()))
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, B + 1, **i32) for k in ("parent", "token", "depth")}
+    out["score"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+    out["n_nodes"] = torch.empty(n_trees, **i32)
+    out["status"] = torch.empty(n_trees, **i32)
+    out["total"] = torch.empty((), **i32)
+    nbytes = tsd_workspace_size(TSD_OP_BUILD_FOREST, n_trees, 1, L, V, topk, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_build_forest")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_build_forest(_ptr(x), _dtype_code(x), n_trees, L, V, topk, B, drafter_temp,
+                                     int(M_max), float(l0), float(c1), _ptr(out["parent"]),
+                                     _ptr(out["token"]), _ptr(out["depth"]), _ptr(out["score"]),
+                                     _ptr(out["n_nodes"]), _ptr(out["status"]), _ptr(out["total"]),
+                                     _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_build_forest")
+    return out

@@ -56,14 +56,6 @@ constexpr unsigned long long kSentinelKey = 0ull;  // below every real key
 constexpr unsigned long long kRootHash = 0x243F6A8885A308D3ull;
 constexpr unsigned long long kRsMask = (1ull << 56) - 1;
 
-__device__ __forceinline__ unsigned long long order_key(double s) {
-    const unsigned long long u = (unsigned long long)__double_as_longlong(s);
-    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
-}
-__device__ __forceinline__ double key_score(unsigned long long k) {
-    const unsigned long long u = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
-    return __longlong_as_double((long long)u);
-}
 __device__ __forceinline__ bool before(const FEntry& a, const FEntry& b) {
     return a.key > b.key || (a.key == b.key && a.tb < b.tb);
 }
@@ -710,6 +702,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             tok[node] = ls.token(m, d, r);
             dep[node] = d;
             sc[node] = (float)key_score(e.key);
+            if (ws.score64) ws.score64[(int64_t)t * stride + node] = key_score(e.key);
             if (rk) rk[node] = r;
             if (md) md[node] = m;
         }
@@ -751,6 +744,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             tok[0] = -1;
             dep[0] = 0;
             sc[0] = 0.0f;
+            if (ws.score64) ws.score64[(int64_t)t * stride] = 0.0;
             if (rk) rk[0] = -1;
             if (md) md[0] = -1;
         }
@@ -760,6 +754,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         tok[i] = -1;
         dep[i] = -1;
         sc[i] = -INFINITY;
+        if (ws.score64) ws.score64[(int64_t)t * stride + i] = -INFINITY;
         if (rk) rk[i] = -1;
         if (md) md[i] = -1;
     }

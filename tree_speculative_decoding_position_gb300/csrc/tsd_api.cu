@@ -130,6 +130,23 @@ size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* bas
     return (cv.off + kAlign - 1) & ~(kAlign - 1);
 }
 
+size_t forest_ws_layout(int n_trees, int L, int64_t V, int topk, int B, int esize, void* base,
+                        BuildWs* out, ForestWs* fout) {
+    const size_t b = build_ws_layout(n_trees, 1, L, V, topk, B, esize, base, out);
+    Carve cv{static_cast<uint8_t*>(base), b};
+    const size_t slots = (size_t)n_trees * (size_t)(B + 1);
+    double* s64 = cv.take<double>(slots);
+    if (out) out->score64 = s64;
+    ForestWs f;
+    f.rho = cv.take<double>(slots);
+    f.pre = cv.take<double>(slots);
+    f.rank = cv.take<int32_t>(slots);
+    f.cnt = cv.take<int32_t>((size_t)n_trees);
+    f.ctl = cv.take<int32_t>(2);
+    if (fout) *fout = f;
+    return (cv.off + kAlign - 1) & ~(kAlign - 1);
+}
+
 size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
                        void* base, BuildWs* out) {
     Carve cv{static_cast<uint8_t*>(base)};
@@ -143,6 +160,7 @@ size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int
     ws.lse = cv.take<double>(rows);
     ws.heap_stride = (heap_spill_bytes(n_modes, L, topk, B) + kAlign - 1) & ~(kAlign - 1);
     ws.heap = cv.take<uint8_t>((size_t)n_trees * ws.heap_stride);
+    ws.score64 = nullptr;
     if (out) *out = ws;
     return (cv.off + kAlign - 1) & ~(kAlign - 1);
 }
@@ -190,6 +208,11 @@ size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V,
         case TSD_OP_VERIFY_DDTREE:
             if (n_trees < 1 || B < 0 || B > TSD_MAX_B || V < 1 || V > 0x7fffffff) return 0;
             return verify_ws_layout(n_trees, B, V, es, nullptr, nullptr);
+        case TSD_OP_BUILD_FOREST:
+            if (n_modes != 1 || !build_sizes_ok(n_trees, 1, L, V, topk, B, es) ||
+                (int64_t)n_trees * B > kMaxForestCandidates)
+                return 0;
+            return forest_ws_layout(n_trees, L, V, topk, B, es, nullptr, nullptr, nullptr);
         case TSD_OP_EXIT_LOSS:
             if (n_trees < 1 || L < 1 || L > TSD_MAX_L || B < 0 || B > TSD_MAX_B || V < 1 ||
                 V > 0x7fffffff || n_chunks(V, es) > kMaxDrafterChunks)
@@ -322,6 +345,34 @@ tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const i
         launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
         launch_predraw(target_logits, dtype, n_trees, B, V, c, greedy, seed, n_nodes, ws,
                        exit_node, bonus_token, accept_len, draws, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_build_forest(const void* drafter_logits, tsd_dtype dtype, int n_trees, int L,
+                            int64_t V, int topk, int B, float drafter_temp, int M_max, double l0,
+                            double c1, int32_t* parent, int32_t* token, int32_t* depth,
+                            float* score, int32_t* n_nodes, int32_t* status, int32_t* total,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!drafter_logits || !parent || !token || !depth || !score || !n_nodes || !status || !total ||
+        !dtype_size(dtype) || !build_sizes_ok(n_trees, 1, L, V, topk, B, dtype_size(dtype)) ||
+        (int64_t)n_trees * B > kMaxForestCandidates || M_max < 0 || !(isfinite(l0) && l0 > 0.0) ||
+        !(isfinite(c1) && c1 >= 0.0) || !(isfinite(drafter_temp) && drafter_temp >= 1e-6f))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = forest_ws_layout(n_trees, L, V, topk, B, es, nullptr, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(drafter_logits, &drafter_logits)) return TSD_ERR_INVALID_ARG;
+    BuildWs ws;
+    ForestWs fws;
+    forest_ws_layout(n_trees, L, V, topk, B, es, workspace, &ws, &fws);
+    const int64_t rows = (int64_t)n_trees * L;
+    if (launch_drafter_stats(drafter_logits, dtype, rows, V, topk, exp2_scale(drafter_temp),
+                             (double)drafter_temp, ws, stream) != cudaSuccess ||
+        launch_build_heap(ws, n_trees, 1, L, topk, B, parent, token, depth, score, nullptr, nullptr,
+                          n_nodes, status, stream) != cudaSuccess ||
+        launch_forest_select(ws.score64, depth, n_trees, B, M_max, l0, c1, n_nodes, status, total,
+                             parent, token, score, fws, stream) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
 }

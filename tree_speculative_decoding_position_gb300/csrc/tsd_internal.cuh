@@ -202,6 +202,17 @@ struct Lanes<float> {
     }
 };
 
+// Order-preserving 64-bit image of a float64 score (larger score, larger
+// key; -inf the smallest of the finite-or-infinite values), and its inverse.
+__device__ __forceinline__ unsigned long long order_key(double s) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(s);
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+__device__ __forceinline__ double key_score(unsigned long long k) {
+    const unsigned long long u = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
+    return __longlong_as_double((long long)u);
+}
+
 // (value desc, id asc) order on (logit, token) pairs.
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
@@ -271,6 +282,7 @@ struct BuildWs {
     double* lse;         // [rows] log sum exp(z / T_d) over the row
     uint8_t* heap;       // [n_trees][heap bytes] spill space when shared memory is short
     size_t heap_stride;  // bytes per tree
+    double* score64;     // nullable [n_trees][B+1]: each node's score in float64 (-inf past n_nodes)
 };
 size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
                        void* base, BuildWs* out);
@@ -309,6 +321,23 @@ cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_tree
                                  float c, bool greedy, uint64_t seed, const float* q_child,
                                  const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
                                  int32_t* accept_len, int32_t* status, cudaStream_t stream);
+// Shared-budget selection over the trees of a launch (CAST App. B.4): each
+// tree's candidates get their rank in the global merge and the batched
+// stopping rule is tested there; every tree keeps its candidates ranked below
+// the first failure (n_nodes = width + 1) and its slots past that are cleared.
+constexpr int kMaxForestCandidates = 8192;
+struct ForestWs {
+    double* rho;    // [n_trees][B+1] candidate masses, candidate j at j
+    double* pre;    // [n_trees][B+1] exclusive prefix sums of rho (entry cnt = total)
+    int32_t* rank;  // [n_trees][B+1] place of candidate j in the global merge
+    int32_t* cnt;   // [n_trees] candidates per tree (0 for a failed tree)
+    int32_t* ctl;   // [2] first failing rank, candidate count
+};
+cudaError_t launch_forest_select(const double* score64, int32_t* depth, int n_trees, int B,
+                                 int M_max, double l0, double c1, int32_t* n_nodes,
+                                 const int32_t* status, int32_t* total, int32_t* parent,
+                                 int32_t* token, float* score, const ForestWs& ws,
+                                 cudaStream_t stream);
 // The drafter's streaming pass alone (ws.chunk and ws.lane_max).
 cudaError_t launch_drafter_chunks(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
                                   float c, const BuildWs& ws, cudaStream_t stream);
@@ -338,10 +367,10 @@ cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int 
                              cudaStream_t stream);
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem,
                        cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
