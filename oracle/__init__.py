@@ -58,6 +58,7 @@ def _load():
         lib.orc_exit_loss.argtypes = [P, i32, i64, f64, P, P, i32, P, P, P]
         lib.orc_forest_select.argtypes = [P, P, P, i32, i32, i32, f64, f64, P, P, P]
         lib.orc_uniform_sub.argtypes = [u64, u64, u64, u64, u64]
+        lib.orc_lse_tree.argtypes = [P, i32, i32, i64, f64, i32, i32, P, P, P, P, P, P, P]
         lib.orc_uniform_sub.restype = f64
         lib.orc_seqres.argtypes = [P, P, P, i32, i64, f64, u64, u64, P, P, P]
         lib.orc_proposal.argtypes = [P, P, P, i32, i64, f64, P, u64, u64, P, P, P]
@@ -292,3 +293,24 @@ def forest_select(scores, depth, n_nodes, M_max: int, l0: float, c1: float) -> d
     _check(_load().orc_forest_select(_ptr(scores), _ptr(depth), _ptr(n_nodes), R, stride, M_max,
                                      l0, c1, _ptr(width), _ptr(ms), _ptr(g)), "forest_select")
     return dict(width=width, M=int(ms[0]), G=float(g[0]))
+
+
+def lse_tree(z, temp: float, k: int, B: int, log_prior=None) -> dict:
+    """Mixture tree under the log-sum-exp score ([MFD] App. B Eq. 6): the B
+    best distinct prefixes of the modes' per-depth top-B lists, ranked by
+    log sum_m pi_m Q_m(v).  z: [K, L, V] drafter logits; log_prior: [K] or
+    None (uniform).  Returns parent, token, depth, score ([B+1]; score = the
+    ranking key), n_nodes and n_cand (distinct candidates)."""
+    z = _f64(z)
+    K, L, V = z.shape
+    lp = None if log_prior is None else _f64(log_prior)
+    out = {n: np.zeros(B + 1, dtype=np.int32) for n in ("parent", "token", "depth")}
+    out["score"] = np.zeros(B + 1)
+    nn = np.zeros(1, dtype=np.int32)
+    nc = np.zeros(1, dtype=np.int32)
+    _check(_load().orc_lse_tree(_ptr(z), K, L, V, temp, k, B, _ptr(lp) if lp is not None else None,
+                                _ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]),
+                                _ptr(out["score"]), _ptr(nn), _ptr(nc)), "lse_tree")
+    out["n_nodes"] = int(nn[0])
+    out["n_cand"] = int(nc[0])
+    return out

@@ -24,7 +24,8 @@
  *   [MFD]   "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
  *           Speculative Decoding" -- Sec. 3.4 Eq. 2 (best-mode score),
  *           App. B "Merged heap" and Prop. 6 (sibling / first-child pushes,
- *           node reuse across modes).
+ *           node reuse across modes), App. B "Max or log-sum-exp" Eq. 6
+ *           (mixture-probability score over the modes' per-depth lists).
  *   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *           as 1, 2, 3", SC'11 -- the Philox4x64-10 counter-based generator.
  *
@@ -50,6 +51,11 @@
  *   - Builder tie order: score desc, depth asc, mode asc, rank sequence
  *     lexicographic asc; top-k per position ordered by (logit desc, id asc).
  *   - Prefixes of zero drafter probability (score -inf) never become nodes.
+ *   - Log-sum-exp tree: a mode's depth-d list is its B most probable
+ *     length-d prefixes in the capped universe, built depth by depth and
+ *     ordered by (path sum desc, parent's place asc, token rank asc); a
+ *     distinct prefix is known by its first (depth, mode, place); the ranking
+ *     key is s_lse clamped to the parent's key, ties by (depth, mode, place).
  *
  * Parity status: every function here is pinned by tests/test_oracle_pins.py
  * (brute force, closed forms, library routines, hand-computed fixtures).
@@ -900,4 +906,198 @@ int orc_forest_select(const double *scores, const int32_t *depth, const int32_t 
     *G_star = G;
     free(pos);
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mixture tree under the log-sum-exp score [MFD App. B "Max or log-sum-exp", */
+/* Eq. 6]: s_lse(v) = log sum_m pi_m Q_m(v), Q_m(v) = prod_j q_{m,j}(v_j).   */
+/* No heap merge yields it: the pages rank by the mixture probability the     */
+/* distinct prefixes of the modes' per-depth top-B lists.                    */
+/*                                                                           */
+/* Reading: mode m's depth-d list holds its B most probable length-d         */
+/* prefixes whose tokens are among the mode's k retained tokens per position */
+/* (the builder's capped universe).  Q_m factorises over positions, so the    */
+/* parent of a listed prefix is listed one depth up, and the depth-d list is  */
+/* the best B children of the depth-(d-1) list, ordered by (path sum of z/T   */
+/* desc, parent's place asc, token rank asc); zero-probability prefixes are   */
+/* left out.  Each distinct prefix is known by its first appearance in       */
+/* (depth, mode, place) order.  It gets log Q_m(v) for every mode from the    */
+/* full rows (the path sum of z_{m,j}(v_j)/T minus the summed row            */
+/* log-normalisers, as the builder scores), and s_lse = log sum_m            */
+/* exp(log pi_m + log Q_m(v)); pi is uniform when no prior is given.  The     */
+/* ranking key is s_lse clamped to its parent's key (equal in exact          */
+/* arithmetic: Q_m only falls along a path), and the tree takes the B best   */
+/* distinct prefixes by (key desc, depth asc, mode asc, place asc), which is */
+/* prefix-closed.                                                            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    double ps;   /* path sum of z/T along the prefix */
+    int32_t par; /* place of the parent in the previous depth's list (-1: root) */
+    int32_t r;   /* rank of the last token in the mode's list at this position */
+} orc_beam_entry;
+
+static int orc_beam_cmp(const void *a, const void *b)
+{
+    const orc_beam_entry *x = (const orc_beam_entry *)a, *y = (const orc_beam_entry *)b;
+    if (x->ps != y->ps) return x->ps > y->ps ? -1 : 1;
+    if (x->par != y->par) return x->par < y->par ? -1 : 1;
+    return (x->r > y->r) - (x->r < y->r);
+}
+
+typedef struct {
+    double key;
+    int64_t flat; /* (depth, mode, place) flattened: the tie order */
+} orc_lse_cand;
+
+static int orc_lse_cmp(const void *a, const void *b)
+{
+    const orc_lse_cand *x = (const orc_lse_cand *)a, *y = (const orc_lse_cand *)b;
+    if (x->key != y->key) return x->key > y->key ? -1 : 1;
+    return (x->flat > y->flat) - (x->flat < y->flat);
+}
+
+/*
+ * z: [K][L][V] drafter logits; log_prior: [K] or NULL (uniform).
+ * Outputs have B+1 slots as orc_build_tree's (score = the ranking key);
+ * n_cand_out: the number of distinct candidate prefixes.
+ */
+int orc_lse_tree(const double *z, int K, int L, int64_t V, double temp, int k, int B,
+                 const double *log_prior, int32_t *parent, int32_t *token, int32_t *depth,
+                 double *score, int32_t *n_nodes_out, int32_t *n_cand_out)
+{
+    if (K < 1 || K > 64 || L < 1 || L > ORC_MAX_DEPTH || k < 1 || k > V || B < 0 ||
+        !(temp > 0.0))
+        return ORC_ERR_ARG;
+    for (int i = 0; i <= B; ++i) {
+        parent[i] = token[i] = depth[i] = -1;
+        score[i] = -INFINITY;
+    }
+    parent[0] = -1; token[0] = -1; depth[0] = 0; score[0] = 0.0;
+    *n_nodes_out = 1;
+    *n_cand_out = 0;
+    const int64_t rows = (int64_t)K * L;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)rows);
+    int32_t *top_id = (int32_t *)malloc(sizeof(int32_t) * (size_t)(rows * k));
+    double *top_logq = (double *)malloc(sizeof(double) * (size_t)(rows * k));
+    double *top_zt = (double *)malloc(sizeof(double) * (size_t)(rows * k));
+    int st = orc_drafter_stats(z, rows, V, temp, k, lse, top_id, top_logq, top_zt);
+    if (st != ORC_OK || B == 0) {
+        free(lse); free(top_id); free(top_logq); free(top_zt);
+        return st;
+    }
+    /* lists[m][d][i], sizes nb[m][d] */
+    const int64_t per = (int64_t)B;
+    orc_beam_entry *lists = (orc_beam_entry *)malloc(sizeof(orc_beam_entry) * (size_t)(rows * per));
+    int32_t *nb = (int32_t *)calloc((size_t)rows, sizeof(int32_t));
+    orc_beam_entry *kids = (orc_beam_entry *)malloc(sizeof(orc_beam_entry) * (size_t)(per * k + k));
+    for (int m = 0; m < K; ++m) {
+        for (int d = 0; d < L; ++d) {
+            const int64_t row = (int64_t)m * L + d;
+            int n = 0;
+            const int np = d == 0 ? 1 : nb[row - 1];
+            for (int i = 0; i < np; ++i) {
+                const double base = d == 0 ? 0.0 : lists[(row - 1) * per + i].ps;
+                for (int r = 0; r < k; ++r) {
+                    const double ps = d == 0 ? top_zt[row * k + r] : base + top_zt[row * k + r];
+                    if (ps == -INFINITY) continue;
+                    kids[n].ps = ps;
+                    kids[n].par = d == 0 ? -1 : i;
+                    kids[n].r = r;
+                    ++n;
+                }
+            }
+            qsort(kids, (size_t)n, sizeof(orc_beam_entry), orc_beam_cmp);
+            nb[row] = n < B ? n : B;
+            memcpy(lists + row * per, kids, sizeof(orc_beam_entry) * (size_t)nb[row]);
+        }
+    }
+    /* distinct prefixes: rep[flat] = flat index of the first appearance */
+    const int64_t nflat = (int64_t)L * K * per;
+#define FLAT(d, m, i) (((int64_t)(d) * K + (m)) * per + (i))
+    int64_t *rep = (int64_t *)malloc(sizeof(int64_t) * (size_t)nflat);
+    int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)nflat);
+    int64_t *prep = (int64_t *)malloc(sizeof(int64_t) * (size_t)nflat); /* parent's rep, -1 root */
+    double *key = (double *)malloc(sizeof(double) * (size_t)nflat);
+    orc_lse_cand *cand = (orc_lse_cand *)malloc(sizeof(orc_lse_cand) * (size_t)nflat);
+    int32_t *path = (int32_t *)malloc(sizeof(int32_t) * (size_t)L);
+    int64_t nc = 0;
+    for (int d = 0; d < L; ++d) {
+        for (int m = 0; m < K; ++m) {
+            const int64_t row = (int64_t)m * L + d;
+            for (int i = 0; i < nb[row]; ++i) {
+                const orc_beam_entry *e = lists + row * per + i;
+                const int64_t f = FLAT(d, m, i);
+                tok[f] = top_id[row * k + e->r];
+                prep[f] = d == 0 ? -1 : rep[FLAT(d - 1, m, e->par)];
+                rep[f] = f;
+                /* an earlier appearance of the same prefix at this depth */
+                for (int m2 = 0; m2 <= m && rep[f] == f; ++m2) {
+                    const int n2 = m2 < m ? nb[(int64_t)m2 * L + d] : i;
+                    for (int i2 = 0; i2 < n2; ++i2) {
+                        const int64_t g = FLAT(d, m2, i2);
+                        if (rep[g] == g && tok[g] == tok[f] && prep[g] == prep[f]) {
+                            rep[f] = g;
+                            break;
+                        }
+                    }
+                }
+                if (rep[f] != f) continue;
+                /* the token path, root first */
+                int64_t u = f;
+                for (int j = d; j >= 0; --j) {
+                    path[j] = tok[u];
+                    u = prep[u];
+                }
+                double tmax = -INFINITY;
+                double t[64];
+                for (int mm = 0; mm < K; ++mm) {
+                    double ps = 0.0, c = 0.0;
+                    for (int j = 0; j <= d; ++j) {
+                        const int64_t rr = (int64_t)mm * L + j;
+                        ps = ps + z[rr * V + path[j]] / temp;
+                        c = c + lse[rr];
+                    }
+                    const double lp = log_prior ? log_prior[mm] : -log((double)K);
+                    t[mm] = lp + (ps - c);
+                    if (t[mm] > tmax) tmax = t[mm];
+                }
+                double s = -INFINITY;
+                if (tmax > -INFINITY) {
+                    double acc = 0.0;
+                    for (int mm = 0; mm < K; ++mm) acc += exp(t[mm] - tmax);
+                    s = tmax + log(acc);
+                }
+                const double up = d == 0 ? INFINITY : key[prep[f]];
+                key[f] = s < up ? s : up;
+                if (key[f] > -INFINITY) {
+                    cand[nc].key = key[f];
+                    cand[nc].flat = f;
+                    ++nc;
+                }
+            }
+        }
+    }
+    *n_cand_out = (int32_t)nc;
+    qsort(cand, (size_t)nc, sizeof(orc_lse_cand), orc_lse_cmp);
+    /* the B best, in order; a parent always precedes its children */
+    int32_t *node_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)nflat);
+    for (int64_t f = 0; f < nflat; ++f) node_of[f] = -1;
+    const int64_t take = nc < B ? nc : B;
+    st = ORC_OK;
+    for (int64_t q = 0; q < take; ++q) {
+        const int64_t f = cand[q].flat;
+        const int n = (int)q + 1;
+        node_of[f] = n;
+        const int pn = prep[f] < 0 ? 0 : node_of[prep[f]];
+        if (pn < 0) { st = ORC_ERR_BAD_TREE; break; }
+        parent[n] = pn;
+        token[n] = tok[f];
+        depth[n] = (int32_t)(f / ((int64_t)K * per)) + 1;
+        score[n] = cand[q].key;
+    }
+    *n_nodes_out = (int32_t)take + 1;
+#undef FLAT
+    free(lse); free(top_id); free(top_logq); free(top_zt); free(lists); free(nb); free(kids);
+    free(rep); free(tok); free(prep); free(key); free(cand); free(path); free(node_of);
+    return st;
 }

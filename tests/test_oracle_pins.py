@@ -886,3 +886,135 @@ def test_forest_select_tie_order(orc):
     assert out["width"].tolist() == [0, 1]  # request 1's depth-1 node comes first
     out = orc.forest_select(scores, depth, np.array([3, 3]), 2, 1.0, 0.0)
     assert out["width"].tolist() == [1, 1]  # then request 0 (depth 2, lower index) before request 1's depth 2
+
+
+# --------------------------------------------------------------------------
+# mixture tree under the log-sum-exp score ([MFD] App. B Eq. 6)
+# --------------------------------------------------------------------------
+def _paths(tr):
+    return sequences_of(tr["parent"], tr["token"], tr["n_nodes"])[1:]
+
+
+def sequences_of(parent, token, n):
+    seqs = [()]
+    for u in range(1, n):
+        seqs.append(seqs[int(parent[u])] + (int(token[u]),))
+    return seqs
+
+
+def _brute_lse_tree(z, T, k, B, log_prior=None):
+    """From the definitions: each mode's capped universe enumerated, its
+    per-depth top-B by the product of softmax probabilities, the union ranked
+    by log sum_m pi_m prod_j p_{m,j}(x_j)."""
+    K, L, V = z.shape
+    with np.errstate(divide="ignore"):
+        p = scipy.special.softmax(z / T, axis=-1)
+    pi = np.full(K, 1.0 / K) if log_prior is None else np.exp(np.asarray(log_prior, dtype=float))
+    caps = [[np.lexsort((np.arange(V), -z[m, j]))[:k] for j in range(L)] for m in range(K)]
+    cands = set()
+    for m in range(K):
+        for d in range(1, L + 1):
+            seqs = [s for s in itertools.product(*caps[m][:d])]
+            q = [float(np.prod([p[m, j, x] for j, x in enumerate(s)])) for s in seqs]
+            ranked = sorted([(qq, tuple(int(x) for x in s)) for qq, s in zip(q, seqs) if qq > 0],
+                            key=lambda t: -t[0])
+            cands.update(s for _, s in ranked[:B])
+
+    def qbar(s):
+        return sum(pi[m] * np.prod([p[m, j, x] for j, x in enumerate(s)]) for m in range(K))
+
+    scored = sorted(((math.log(qbar(s)), s) for s in cands), key=lambda t: -t[0])
+    return scored[:B], len(cands), qbar
+
+
+def test_lse_tree_hand_fixture(orc):
+    g = json.load(open(os.path.join(GOLDEN, "lse_tree_hand.json")))
+    for ex in g["examples"]:
+        z = np.log(np.array(ex["p"]))
+        for case in ex["cases"]:
+            tr = orc.lse_tree(z, 1.0, ex["k"], case["B"])
+            assert tr["n_cand"] == case["n_cand"]
+            assert [list(s) for s in _paths(tr)] == case["paths"]
+            np.testing.assert_allclose(tr["score"][1:tr["n_nodes"]], np.log(case["qbar"]), rtol=0,
+                                       atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_lse_tree_matches_brute_force(orc, seed):
+    rng = np.random.default_rng(800 + seed)
+    K, L, V = int(rng.integers(1, 4)), int(rng.integers(1, 4)), int(rng.integers(3, 8))
+    k, B = int(rng.integers(1, min(V, 4) + 1)), int(rng.integers(1, 13))
+    z = rng.normal(size=(K, L, V)) * 1.5
+    if seed % 5 == 4:
+        z[rng.random(z.shape) < 0.2] = -np.inf      # masked tokens: zero-probability prefixes
+        z[..., 0] = np.maximum(z[..., 0], 0.0)      # every row keeps a finite token
+    log_prior = None if seed % 2 == 0 else rng.normal(size=K)
+    T = [1.0, 0.7, 1.8][seed % 3]
+    tr = orc.lse_tree(z, T, k, B, log_prior=log_prior)
+    want, n_cand, _ = _brute_lse_tree(z, T, k, B, log_prior)
+    assert tr["n_cand"] == n_cand
+    assert _paths(tr) == [s for _, s in want]
+    np.testing.assert_allclose(tr["score"][1:tr["n_nodes"]], [s for s, _ in want], rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_lse_tree_one_mode_is_the_ddtree_builder(orc, seed):
+    rng = np.random.default_rng(900 + seed)
+    L, V, k, B = 4, 40, 6, 30
+    z = rng.normal(size=(1, L, V)) * 2
+    tr = orc.lse_tree(z, 1.0, k, B)
+    ref = orc.build_tree(orc.drafter_lists(z, 1.0, k), B)
+    assert tr["n_nodes"] == ref["n_nodes"]
+    for key in ("parent", "token", "depth"):
+        assert np.array_equal(tr[key], ref[key]), key
+    assert np.array_equal(tr["score"][1:], ref["score"][1:])
+
+
+def test_lse_tree_identical_modes_and_prior_shift(orc):
+    rng = np.random.default_rng(950)
+    z1 = rng.normal(size=(1, 3, 25)) * 2
+    one = orc.lse_tree(z1, 1.0, 5, 20)
+    for K in (2, 5):
+        many = orc.lse_tree(np.repeat(z1, K, axis=0), 1.0, 5, 20)
+        assert many["n_cand"] == one["n_cand"]
+        assert _paths(many) == _paths(one)
+        np.testing.assert_allclose(many["score"], one["score"], rtol=0, atol=1e-12)
+    z = rng.normal(size=(3, 3, 25)) * 2
+    lp = rng.normal(size=3)
+    a = orc.lse_tree(z, 1.0, 5, 20, log_prior=lp)
+    b = orc.lse_tree(z, 1.0, 5, 20, log_prior=lp + 2.5)
+    assert _paths(a) == _paths(b)
+    np.testing.assert_allclose(b["score"][1:], a["score"][1:] + 2.5, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_lse_tree_bounds_and_coverage_against_max_rule(orc, seed):
+    """s(v) <= s_lse(v) <= s(v) + log K for every node, with s the best-mode
+    score; the tree is prefix-closed with scores falling along paths; its
+    mixture mass is at least that of the max rule's tree of the same budget,
+    which lies inside the candidate set."""
+    rng = np.random.default_rng(1000 + seed)
+    K, L, V, k, B = int(rng.integers(2, 6)), 3, 12, 4, int(rng.integers(4, 25))
+    z = rng.normal(size=(K, L, V)) * 2
+    tr = orc.lse_tree(z, 1.0, k, B)
+    _, _, qbar = _brute_lse_tree(z, 1.0, k, B)
+    p = scipy.special.softmax(z, axis=-1)
+    n = tr["n_nodes"]
+    seqs = sequences_of(tr["parent"], tr["token"], n)
+    for u in range(1, n):
+        s = seqs[u]
+        best = max(math.log(np.prod([p[m, j, x] for j, x in enumerate(s)]) / K) for m in range(K))
+        assert best - 1e-12 <= tr["score"][u] <= best + math.log(K) + 1e-12
+        assert 0 <= tr["parent"][u] < u
+        assert tr["score"][u] <= tr["score"][tr["parent"][u]] or tr["parent"][u] == 0
+    mx = orc.build_tree(orc.drafter_lists(z, 1.0, k), B)
+    mseqs = sequences_of(mx["parent"], mx["token"], mx["n_nodes"])
+    assert sum(qbar(s) for s in seqs[1:]) >= sum(qbar(s) for s in mseqs[1:]) - 1e-12
+
+
+def test_lse_tree_edge_budgets(orc):
+    rng = np.random.default_rng(1100)
+    z = rng.normal(size=(2, 3, 6))
+    assert orc.lse_tree(z, 1.0, 2, 0)["n_nodes"] == 1
+    big = orc.lse_tree(z, 1.0, 2, 200)                   # every candidate taken
+    assert big["n_nodes"] == big["n_cand"] + 1
