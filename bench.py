@@ -540,6 +540,39 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         "mean_accept_len": float(ov["accept_len"].float().mean()),
         "mean_coverage_plus_1": float(ov["coverage"].mean()) + 1.0,
         "status_ok": int((ov["status"] == 0).sum())}
+    # the same workload under the log-sum-exp score ([MFD] Eq. 6): build time,
+    # and TEV at T = 1 on its trees against targets built the same way
+    ws_l = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_LSE, nt_m, K_m, 16, V, 8, B_m,
+                                              torch.bfloat16), dtype=torch.uint8, device=dev)
+    for i in range(3):
+        tl = tsd.tsd_build_lse_tree(mix, topk=8, B=B_m, workspace=ws_l)
+    s.record(stream)
+    for i in range(10):
+        tl = tsd.tsd_build_lse_tree(mix, topk=8, B=B_m, workspace=ws_l)
+    e.record(stream)
+    torch.cuda.synchronize()
+    lse_ms = s.elapsed_time(e) / 10
+    tgt_l = torch.zeros(nt_m, B_m + 1, V, dtype=torch.bfloat16, device=dev)
+    for t in range(nt_m):
+        n_t = int(tl["n_nodes"][t])
+        fut = synth.mixture_drafter(1, 2, 16, V, synth.seed_for(3) + t, device=dev)[1][0, choice[t]]
+        synth.target_from_rows(fut, tl["depth"][t, :n_t], 1.5, synth.seed_for(3, 500 + t),
+                               out=tgt_l[t, :n_t])
+    acc_l, cov_l = [], []
+    for i in range(8):
+        o = tsd.tsd_verify_tev(tgt_l, tl["parent"], tl["token"], tl["n_nodes"], 1.0, seed=100 + i)
+        acc_l.append(float(o["accept_len"].float().mean()))
+        cov_l.append(float(o["coverage"].mean()))
+    acc_m = []
+    for i in range(8):
+        o = tsd.tsd_verify_tev(tgt_m, tm["parent"], tm["token"], tm["n_nodes"], 1.0, seed=100 + i)
+        acc_m.append(float(o["accept_len"].float().mean()))
+    out["mixture_lse_k8_b128_x16"] = {
+        "build_ms": lse_ms, "max_rule_build_ms": build_ms,
+        "mean_accept_len": statistics.mean(acc_l), "max_rule_mean_accept_len": statistics.mean(acc_m),
+        "mean_coverage_plus_1": statistics.mean(cov_l) + 1.0,
+        "mean_candidates": float(tl["n_cand"].float().mean()),
+        "status_ok": int((tl["status"] == 0).sum())}
     return out
 
 
@@ -743,6 +776,61 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _op_setup(name, tsd, torch, synth, dev):
+    """The workload of one secondary operation, as the extras time it; returns
+    a callable that issues one call."""
+    V = WORKLOAD["V"]
+    if name in ("build_lse", "build_mixture"):
+        mix, _, _ = synth.mixture_drafter(16, 8, 16, V, synth.seed_for(3), device=dev)
+        op = tsd.TSD_OP_BUILD_LSE if name == "build_lse" else tsd.TSD_OP_BUILD_TREE
+        ws = torch.empty(tsd.tsd_workspace_size(op, 16, 8, 16, V, 8, 128, torch.bfloat16),
+                         dtype=torch.uint8, device=dev)
+        if name == "build_lse":
+            return lambda: tsd.tsd_build_lse_tree(mix, topk=8, B=128, workspace=ws)
+        return lambda: tsd.tsd_build_tree(mix, topk=8, B=128, workspace=ws)
+    nt, L, k, B = WORKLOAD["trees_per_gpu"], WORKLOAD["L"], WORKLOAD["topk"], WORKLOAD["B"]
+    drafter = synth.zipf_drafter(nt, L, V, 0, device=dev,
+                                 seeds=[synth.seed_for(2, t) for t in range(nt)])
+    if name == "build_forest":
+        ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_FOREST, nt, 1, L, V, k, B,
+                                                torch.bfloat16), dtype=torch.uint8, device=dev)
+        return lambda: tsd.tsd_build_forest(drafter, topk=k, B=B, M_max=nt * B, l0=1.0,
+                                            c1=1.0 / 2048, workspace=ws)
+    tr = tsd.tsd_build_tree(drafter, topk=k, B=B)
+    w = torch.rand(nt, B + 1, generator=torch.Generator(device=dev).manual_seed(5),
+                   device=dev) * (tr["depth"] >= 0)
+    ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_EXIT_LOSS, nt, 1, L, V, 1, B,
+                                            torch.bfloat16), dtype=torch.uint8, device=dev)
+    grad = name == "exit_loss_grad"
+    return lambda: tsd.tsd_exit_loss(drafter, tr["token"], tr["depth"], tr["n_nodes"], w,
+                                     with_grad=grad, workspace=ws)
+
+
+OPS = ("build_lse", "build_mixture", "build_forest", "exit_loss", "exit_loss_grad")
+
+
+def run_op(args):
+    import torch
+
+    import synth
+    import tree_speculative_decoding_position_gb300 as tsd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    tsd.load()
+    fn = _op_setup(args.op, tsd, torch, synth, dev)
+    for i in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(args.steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"op": args.op, "calls": args.steps, "ms_per_call": s.elapsed_time(e) / args.steps}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -757,10 +845,15 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time TEV over B x trees x T instead (writes --sweep-out)")
     ap.add_argument("--sweep-out", default="gpurun_out/sweep.json")
+    ap.add_argument("--op", choices=sorted(OPS), default=None,
+                    help="run one secondary operation alone on its workload (for profiler "
+                         "captures): warm-up calls, then --steps timed calls")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.sweep:
+    if args.op:
+        run_op(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

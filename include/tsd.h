@@ -75,7 +75,8 @@ typedef enum {
     TSD_OP_VERIFY_TEV = 1,
     TSD_OP_VERIFY_DDTREE = 2,
     TSD_OP_EXIT_LOSS = 3,
-    TSD_OP_BUILD_FOREST = 4
+    TSD_OP_BUILD_FOREST = 4,
+    TSD_OP_BUILD_LSE = 5
 } tsd_op;
 
 /* Limits checked by every entry point. */
@@ -240,6 +241,46 @@ tsd_status tsd_build_forest(const void *drafter_logits, tsd_dtype dtype, int n_t
                             double c1, int32_t *parent, int32_t *token, int32_t *depth,
                             float *score, int32_t *n_nodes, int32_t *status, int32_t *total,
                             void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsd_build_lse_tree -- the mixture tree under the log-sum-exp score ([MFD]
+ * App. B "Max or log-sum-exp", Eq. 6): prefixes ranked by their mixture
+ * probability s_lse(v) = log sum_m pi_m Q_m(v), Q_m(v) = prod_j q_{m,j}(v_j).
+ * No merge of per-mode searches yields that ranking, so the candidates are
+ * the distinct prefixes of the modes' per-depth lists.  Mode m's depth-d list
+ * holds its B most probable length-d prefixes whose tokens are among its topk
+ * kept tokens per position, ordered by (path sum of z/T desc, parent's place
+ * in the depth-(d-1) list asc, token rank asc); zero-probability prefixes are
+ * left out.  Every candidate is scored under every mode from the full rows
+ * (log Q_m = path sum of z/T minus the summed row log-normalisers), also
+ * where its tokens fall outside a mode's kept lists.  The ranking key is
+ * s_lse clamped to its parent's key (equal in exact arithmetic), and the tree
+ * takes the B best distinct candidates by (key desc, depth asc, mode asc,
+ * place asc) in that order, which is prefix-closed.  A candidate reached by
+ * several modes counts once, under its first (depth, mode, place).
+ *
+ * drafter_logits  [n_trees][n_modes][L][V] as tsd_build_tree's (device or
+ *                 page-locked host memory).
+ * log_prior       nullable [n_trees][n_modes] float32 log pi (finite or
+ *                 -inf; need not be normalised); NULL = uniform 1/n_modes.
+ * Sizes as tsd_build_tree's, and also B <= 2048, n_modes * B <= 4096,
+ * n_trees <= 65535, and one mode's lists must fit in a block's shared memory:
+ * 16 n_modes B + 40 B + 12 P + 2496 bytes <= 227 KB, P the power of two at or
+ * above sum_{r < topk} floor(B / (r+1)) (the children that can be kept);
+ * else TSD_ERR_INVALID_ARG.
+ * Outputs: parent, token, depth [n_trees][B+1] int32 and score (the ranking
+ * key, float32 copy of the float64 value), n_nodes, status [n_trees] as
+ * tsd_build_tree's; n_cand (nullable) [n_trees]: distinct candidates with
+ * non-zero mixture mass.  A tree with a non-finite row gets status
+ * TSD_ERR_NONFINITE and n_nodes 0.  Workspace:
+ * tsd_workspace_size(TSD_OP_BUILD_LSE, n_trees, n_modes, L, V, topk, B, dtype).
+ */
+tsd_status tsd_build_lse_tree(const void *drafter_logits, tsd_dtype dtype, int n_trees,
+                              int n_modes, int L, int64_t V, int topk, int B, float drafter_temp,
+                              const float *log_prior, int32_t *parent, int32_t *token,
+                              int32_t *depth, float *score, int32_t *n_nodes, int32_t *status,
+                              int32_t *n_cand, void *workspace, size_t ws_bytes,
+                              cudaStream_t stream);
 
 /*
  * tsd_verify_seqres -- exact sequential residual verification ([EXIT] App.

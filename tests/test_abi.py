@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "tsd_build_forest", "tsd_build_tree", "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
+        "tsd_build_forest", "tsd_build_lse_tree", "tsd_build_tree", "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
         "tsd_exit_loss", "tsd_verify_proposal", "tsd_verify_seqres", "tsd_verify_tev",
         "tsd_verify_tev_noalloc", "tsd_verify_tev_timed", "tsd_workspace_size"])
 

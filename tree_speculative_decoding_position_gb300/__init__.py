@@ -27,7 +27,7 @@ TSD_OK, TSD_ERR_INVALID_ARG, TSD_ERR_CUDA, TSD_ERR_WORKSPACE = 0, 1, 2, 3
 TSD_ERR_BAD_TREE, TSD_ERR_NONFINITE, TSD_ERR_TIMEOUT = 4, 5, 6
 TSD_BF16, TSD_F32 = 0, 1
 TSD_OP_BUILD_TREE, TSD_OP_VERIFY_TEV, TSD_OP_VERIFY_DDTREE, TSD_OP_EXIT_LOSS = 0, 1, 2, 3
-TSD_OP_BUILD_FOREST = 4
+TSD_OP_BUILD_FOREST, TSD_OP_BUILD_LSE = 4, 5
 
 _lib = None
 
@@ -71,9 +71,11 @@ def load():
     f64 = ctypes.c_double
     lib.tsd_build_forest.argtypes = [P, i32, i32, i32, i64, i32, i32, f32, i32, f64, f64,
                                      P, P, P, P, P, P, P, P, sz, P]
+    lib.tsd_build_lse_tree.argtypes = [P, i32, i32, i32, i32, i64, i32, i32, f32, P,
+                                       P, P, P, P, P, P, P, P, sz, P]
     for f in ("tsd_build_tree", "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed",
               "tsd_verify_ddtree", "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
-              "tsd_verify_proposal", "tsd_build_forest"):
+              "tsd_verify_proposal", "tsd_build_forest", "tsd_build_lse_tree"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -167,6 +169,47 @@ def tsd_build_tree(drafter_logits: torch.Tensor, topk: int, B: int, drafter_temp
                                    _ptr(ws), nbytes, _stream(dev))
     if st != TSD_OK:
         raise TsdError(st, "tsd_build_tree")
+    return out
+
+
+def tsd_build_lse_tree(drafter_logits: torch.Tensor, topk: int, B: int, drafter_temp: float = 1.0,
+                       log_prior=None, workspace=None, device=None) -> dict:
+    """Mixture tree under the log-sum-exp score ([MFD] App. B Eq. 6): the B
+    best distinct prefixes of the modes' per-depth lists, ranked by
+    log sum_m pi_m Q_m(v).  drafter_logits: [n_trees, n_modes, L, V]
+    (bf16/fp32, GPU or pinned host); log_prior: None (uniform) or
+    [n_trees, n_modes] float32.  Returns parent, token, depth, score
+    ([n_trees, B+1]), n_nodes, status and n_cand ([n_trees])."""
+    x = _logits(drafter_logits, "drafter_logits")
+    if x.dim() != 4:
+        raise ValueError("drafter_logits must be [n_trees, n_modes, L, V]")
+    n_trees, n_modes, L, V = x.shape
+    dev = x.device if x.is_cuda else (torch.device(device) if device is not None else
+                                      torch.device("cuda", torch.cuda.current_device()))
+    lp = None
+    if log_prior is not None:
+        lp = log_prior
+        if not (lp.dtype == torch.float32 and lp.shape == (n_trees, n_modes) and lp.is_contiguous()
+                and (lp.is_cuda or lp.is_pinned())):
+            raise ValueError("log_prior must be a contiguous float32 [n_trees, n_modes] tensor on "
+                             "the GPU or in pinned host memory")
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {k: torch.empty(n_trees, B + 1, **i32) for k in ("parent", "token", "depth")}
+    out["score"] = torch.empty(n_trees, B + 1, dtype=torch.float32, device=dev)
+    for k in ("n_nodes", "status", "n_cand"):
+        out[k] = torch.empty(n_trees, **i32)
+    nbytes = tsd_workspace_size(TSD_OP_BUILD_LSE, n_trees, n_modes, L, V, topk, B, x.dtype)
+    if nbytes == 0:
+        raise TsdError(TSD_ERR_INVALID_ARG, "tsd_build_lse_tree")
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = load().tsd_build_lse_tree(_ptr(x), _dtype_code(x), n_trees, n_modes, L, V, topk, B,
+                                       drafter_temp, _ptr(lp) if lp is not None else None,
+                                       _ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]),
+                                       _ptr(out["score"]), _ptr(out["n_nodes"]), _ptr(out["status"]),
+                                       _ptr(out["n_cand"]), _ptr(ws), nbytes, _stream(dev))
+    if st != TSD_OK:
+        raise TsdError(st, "tsd_build_lse_tree")
     return out
 
 

@@ -1,0 +1,669 @@
+// k_lse.cu -- the mixture tree under the log-sum-exp score.
+//
+// "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
+// Speculative Decoding", App. B "Max or log-sum-exp", Eq. 6: a prefix is
+// scored by its mixture probability s_lse(v) = log sum_m pi_m Q_m(v).  That
+// ranking is not a merge of per-mode searches, so the candidates are the
+// distinct prefixes of the modes' per-depth lists, ranked by s_lse.
+//
+// A mode's depth-d list holds its B most probable length-d prefixes within
+// the capped universe (the mode's k kept tokens per position).  Q_m
+// factorises over positions, so the list is the best B children of the
+// depth-(d-1) list, ordered by (path sum of z/T desc, parent's place asc,
+// token rank asc).  Within one mode and depth every child carries the same
+// summed log-normaliser, so path sums of z/T decide the order.
+//
+// lse_beam_kernel    one CTA per (mode, tree), depth by depth.  The children
+//                    of the previous list form k lists, one per token rank,
+//                    each already sorted; a child's place in their merge is
+//                    its own parent's place plus one binary search per other
+//                    rank.  Children placed below B are kept.  Each kept
+//                    entry then gathers its token's logit under every mode
+//                    (full rows), extends the per-mode path sums, and takes
+//                    s_lse = log sum_m exp(log pi_m + path sum - summed LSE),
+//                    clamped to its parent's key.  Equal prefixes reached by
+//                    several modes get bit-identical keys.
+// lse_select_kernel  one CTA per tree.  Duplicates across modes are merged
+//                    depth by depth through a shared-memory hash on (parent's
+//                    representative, token) that keeps the first appearance
+//                    in (depth, mode, place) order.  A radix select on the
+//                    64-bit key image finds the B-th best, ties at it go by
+//                    that order, and a bitonic sort of the kept entries gives
+//                    the node order (parents first).
+#include "tsd_internal.cuh"
+
+namespace tsd {
+
+constexpr int kBeamThreads = 512;
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ double load_logit(const void* logits, tsd_dtype dtype, int64_t off) {
+    if (dtype == TSD_BF16)
+        return (double)__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(logits)[off]);
+    return (double)reinterpret_cast<const float*>(logits)[off];
+}
+
+// Ascending bitonic sort of the pairs (k0[i], k1[i]), i < n2 (a power of two,
+// at least 32), by the whole block: strides below 32 with warp shuffles on
+// one element a lane, strides of 32 and up through shared memory.
+__device__ __forceinline__ void lane_steps(unsigned long long& x0, unsigned& x1, int e, int kk,
+                                           int jtop) {
+    const int lane = threadIdx.x & 31;
+    for (int j = jtop; j > 0; j >>= 1) {
+        const unsigned long long y0 = __shfl_xor_sync(0xffffffffu, x0, j);
+        const unsigned y1 = __shfl_xor_sync(0xffffffffu, x1, j);
+        const bool lower = (lane & j) == 0, asc = (e & kk) == 0;
+        const bool x_first = x0 < y0 || (x0 == y0 && x1 < y1);
+        if ((lower == asc) != x_first) {
+            x0 = y0;
+            x1 = y1;
+        }
+    }
+}
+
+__device__ void block_sort_pairs(unsigned long long* k0, unsigned* k1, int n2) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nblk = n2 >> 5;
+    for (int b = wid; b < nblk; b += nw) {
+        const int e = (b << 5) + lane;
+        unsigned long long x0 = k0[e];
+        unsigned x1 = k1[e];
+        for (int kk = 2; kk <= 32; kk <<= 1) lane_steps(x0, x1, e, kk, kk >> 1);
+        k0[e] = x0;
+        k1[e] = x1;
+    }
+    __syncthreads();
+    for (int kk = 64; kk <= n2; kk <<= 1) {
+        for (int jj = kk >> 1; jj >= 32; jj >>= 1) {
+            const int sh = __ffs(jj) - 1;
+            for (int x = threadIdx.x; x < (n2 >> 1); x += blockDim.x) {
+                const int i = ((x >> sh) << (sh + 1)) | (x & (jj - 1)), l = i | jj;
+                const unsigned long long a0 = k0[i], b0 = k0[l];
+                const unsigned a1 = k1[i], b1 = k1[l];
+                const bool l_first = b0 < a0 || (b0 == a0 && b1 < a1);
+                if (((i & kk) == 0) == l_first) {
+                    k0[i] = b0;
+                    k0[l] = a0;
+                    k1[i] = b1;
+                    k1[l] = a1;
+                }
+            }
+            __syncthreads();
+        }
+        for (int b = wid; b < nblk; b += nw) {
+            const int e = (b << 5) + lane;
+            unsigned long long x0 = k0[e];
+            unsigned x1 = k1[e];
+            lane_steps(x0, x1, e, kk, 16);
+            k0[e] = x0;
+            k1[e] = x1;
+        }
+        __syncthreads();
+    }
+}
+
+// Image of -inf under order_key: the smallest image of a non-NaN double.
+constexpr unsigned long long kNegInfImage = 0x000FFFFFFFFFFFFFull;
+
+// Children that can be kept: sum over ranks r of min(B, B / (r+1)), padded to
+// a power of two for the sort.
+static __host__ __device__ int lse_sort_cap(int B, int k) {
+    int n = 0;
+    for (int r = 0; r < k; ++r) n += B / (r + 1);
+    return pow2_ceil(n < 32 ? 32 : n);
+}
+
+size_t lse_beam_smem(int K, int B, int k) {
+    return sizeof(double) * (size_t)(2 * B * K + 4 * B + TSD_MAX_TOPK * (1 + TSD_MAX_MODES) +
+                                     3 * TSD_MAX_MODES) +
+           (sizeof(unsigned long long) + sizeof(unsigned)) * (size_t)lse_sort_cap(B, k) +
+           sizeof(int) * (size_t)(2 * B);
+}
+
+__global__ void __launch_bounds__(kBeamThreads, 1)
+lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, int64_t V, int k,
+                int B, double temp, const float* __restrict__ log_prior, BuildWs bws, LseWs ws) {
+    pdl_entry();
+    extern __shared__ __align__(16) unsigned char sml[];
+    const int m = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
+    double* pm[2] = {reinterpret_cast<double*>(sml), reinterpret_cast<double*>(sml) + B * K};
+    double* ps[2] = {pm[1] + B * K, pm[1] + B * K + B};
+    double* sk[2] = {ps[1] + B, ps[1] + 2 * B};
+    double* zt = sk[1] + B;                     // [k] this mode's kept z/T at the current position
+    double* zall = zt + TSD_MAX_TOPK;           // [k][K] those tokens' z/T under every mode
+    double* cum = zall + TSD_MAX_TOPK * TSD_MAX_MODES;  // [K] summed log-normalisers so far
+    double* lp = cum + TSD_MAX_MODES;           // [K] log prior
+    double* cst = lp + TSD_MAX_MODES;           // [K] log prior - summed log-normalisers
+    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(cst + TSD_MAX_MODES);
+    unsigned* cidx = reinterpret_cast<unsigned*>(ckey + lse_sort_cap(B, k));
+    int* par = reinterpret_cast<int*>(cidx + lse_sort_cap(B, k));  // [B] parent place of each kept child
+    int* rk = par + B;                                        // [B] token rank of each kept child
+    __shared__ int s_n, s_bad, s_kf;
+    __shared__ int s_off[TSD_MAX_TOPK + 1];  // offsets of the ranks' possible children
+    const int64_t KB = (int64_t)K * B;
+    const int64_t tree_rows = (int64_t)t * K * L;
+    if (tid == 0) s_bad = 0;
+    if (tid < K) {
+        cum[tid] = 0.0;
+        lp[tid] = log_prior ? (double)log_prior[(int64_t)t * K + tid] : -log((double)K);
+    }
+    __syncthreads();
+    // a row without a finite log-normaliser poisons the tree: no lists at all
+    for (int i = tid; i < K * L; i += blockDim.x)
+        if (bws.lse[tree_rows + i] != bws.lse[tree_rows + i]) s_bad = 1;
+    __syncthreads();
+    int np = 1, cur = 0;
+    // one depth ahead: this mode's kept z/T, every mode's log-normaliser, and
+    // the kept tokens' logits under every mode (gathered from the full rows)
+    double f_zt = 0.0, f_lse = 0.0, f_z = 0.0;
+    auto fetch = [&](int d) {
+        const int64_t row = tree_rows + (int64_t)m * L + d;
+        if (tid < k) f_zt = bws.top_zt[row * k + tid];
+        if (tid < K) f_lse = bws.lse[tree_rows + (int64_t)tid * L + d];
+        if (tid < k * K) {
+            const int r = tid / K, m2 = tid - r * K;
+            const int32_t tok = bws.top_id[row * k + r];
+            f_z = load_logit(logits, dtype, (tree_rows + (int64_t)m2 * L + d) * V + tok);
+        }
+    };
+    if (!s_bad) fetch(0);
+    for (int d = 0; d < L; ++d) {
+        const int64_t row = tree_rows + (int64_t)m * L + d;
+        int32_t* nb_out = ws.nb + ((int64_t)t * L + d) * K + m;
+        if (s_bad) {
+            if (tid == 0) *nb_out = 0;
+            continue;
+        }
+        if (tid < k) zt[tid] = f_zt;
+        if (tid < K) {
+            cum[tid] = cum[tid] + f_lse;
+            cst[tid] = lp[tid] - cum[tid];
+        }
+        if (tid < k * K) zall[tid] = f_z / temp;
+        if (d + 1 < L) fetch(d + 1);
+        if (tid == 0) s_n = 0;
+        const double* prev = ps[cur ^ 1];
+        __syncthreads();
+        // Lists are sorted, and a lower rank has a larger z/T, so every child
+        // (i', r2) with i' <= i and r2 < r precedes child (i, r): its place is
+        // at least (r+1)(i+1) - 1, and only children with (r+1)(i+1) <= B can
+        // be kept.  Those with mass are sorted by (path sum desc, i asc, r asc)
+        // -- complemented order image, then c = i k + r -- and the first B
+        // form the new list.
+        if (tid == 0) {
+            int kf = 0, tot = 0;
+            while (kf < k && zt[kf] != -INFINITY) {  // ranks with mass come first
+                s_off[kf] = tot;
+                tot += min(np, B / (kf + 1));
+                ++kf;
+            }
+            s_off[kf] = tot;
+            s_kf = kf;
+        }
+        __syncthreads();
+        const int kf = s_kf, nc = s_off[kf];
+        const int n2 = pow2_ceil(nc < 32 ? 32 : nc);
+        for (int j = tid; j < n2; j += blockDim.x) {
+            unsigned long long a = ~0ull;
+            unsigned b = ~0u;
+            if (j < nc) {
+                int r = 0;
+                while (s_off[r + 1] <= j) ++r;
+                const int i = j - s_off[r];
+                a = ~order_key((d == 0 ? 0.0 : prev[i]) + zt[r]);
+                b = (unsigned)(i * k + r);
+            }
+            ckey[j] = a;
+            cidx[j] = b;
+        }
+        __syncthreads();
+        block_sort_pairs(ckey, cidx, n2);
+        double* nps = ps[cur];
+        const int nkeep = nc < B ? nc : B;
+        for (int j = tid; j < nkeep; j += blockDim.x) {
+            nps[j] = key_score(~ckey[j]);
+            par[j] = (int)(cidx[j] / (unsigned)k);
+            rk[j] = (int)(cidx[j] % (unsigned)k);
+        }
+        if (tid == 0) s_n = nkeep;
+        __syncthreads();
+        const int nb = s_n;
+        // path sums under every mode
+        const double* opm = pm[cur ^ 1];
+        double* npm = pm[cur];
+        for (int e = tid; e < nb * K; e += blockDim.x) {
+            const int j = e / K, m2 = e - j * K;
+            npm[e] = (d == 0 ? 0.0 : opm[par[j] * K + m2]) + zall[rk[j] * K + m2];
+        }
+        __syncthreads();
+        const double* osk = sk[cur ^ 1];
+        double* nsk = sk[cur];
+        // s_lse of each entry: the terms log pi + log Q in float64 (path sum
+        // plus the depth's constant log pi - summed LSE), the sum of
+        // exp(term - largest) in fp32
+        for (int j = tid; j < nb; j += blockDim.x) {
+            double a[TSD_MAX_MODES];
+            double amax = -INFINITY;
+            for (int m2 = 0; m2 < K; ++m2) {
+                a[m2] = npm[j * K + m2] + cst[m2];
+                amax = fmax(amax, a[m2]);
+            }
+            double s = -INFINITY;
+            if (amax > -INFINITY) {
+                float acc = 0.0f;
+                for (int m2 = 0; m2 < K; ++m2) acc += expf((float)(a[m2] - amax));
+                s = amax + (double)logf(acc);
+            }
+            const double up = d == 0 ? INFINITY : osk[par[j]];
+            const double key = s < up ? s : up;
+            nsk[j] = key;
+            const int64_t f = (int64_t)t * L * KB + (int64_t)d * KB + (int64_t)m * B + j;
+            ws.tok[f] = bws.top_id[row * k + rk[j]];
+            ws.par[f] = par[j];
+            ws.kimg[f] = ~order_key(key);
+        }
+        if (tid == 0) *nb_out = nb;
+        np = nb;
+        cur ^= 1;
+        __syncthreads();
+        if (np == 0) {  // nothing finite at this depth: deeper lists are empty too
+            for (int d2 = d + 1 + tid; d2 < L; d2 += blockDim.x)
+                ws.nb[((int64_t)t * L + d2) * K + m] = 0;
+            break;
+        }
+    }
+}
+
+// Exclusive block scan of one int per thread; *total gets the block sum.
+__device__ int block_excl_scan_i(int x, int* red, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) red[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const int y = lane < nw ? red[lane] : 0;
+        int yi = y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xffffffffu, yi, o);
+            if (lane >= o) yi += z;
+        }
+        red[lane] = yi - y;
+        if (lane == 31) red[32] = yi;
+    }
+    __syncthreads();
+    const int r = red[wid] + inc - x;
+    *total = red[32];
+    __syncthreads();
+    return r;
+}
+
+// Exclusive block scan of one 64-bit value per thread (two packed 32-bit
+// counts add without carry as long as each stays below 2^32).
+__device__ unsigned long long block_excl_scan_u64(unsigned long long x, unsigned long long* red,
+                                                  unsigned long long* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    unsigned long long inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) red[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const unsigned long long y = lane < nw ? red[lane] : 0ull;
+        unsigned long long yi = y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long z = __shfl_up_sync(0xffffffffu, yi, o);
+            if (lane >= o) yi += z;
+        }
+        red[lane] = yi - y;
+        if (lane == 31) red[32] = yi;
+    }
+    __syncthreads();
+    const unsigned long long r = red[wid] + inc - x;
+    *total = red[32];
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ bool pair_less(unsigned long long a0, unsigned long long a1,
+                                          unsigned long long b0, unsigned long long b1) {
+    return a0 < b0 || (a0 == b0 && a1 < b1);
+}
+
+constexpr unsigned long long kEmpty = ~0ull;
+constexpr int kMaxSlotsPerThread = 4;  // n_modes * B <= 4096 over 1024 threads
+
+size_t lse_select_smem(int K, int B) {
+    const size_t H = (size_t)pow2_ceil(2 * K * B);
+    const size_t dedupe = H * (sizeof(unsigned long long) + sizeof(int)) + sizeof(int) * 2 * K * B;
+    const size_t sel = (size_t)2 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
+    return dedupe > sel ? dedupe : sel;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __restrict__ parent,
+                  int32_t* __restrict__ token, int32_t* __restrict__ depth,
+                  float* __restrict__ score, int32_t* __restrict__ n_nodes,
+                  int32_t* __restrict__ status, int32_t* __restrict__ n_cand) {
+    pdl_entry();
+    extern __shared__ __align__(16) unsigned char sms[];
+    __shared__ int red[33];
+    __shared__ unsigned hist[256];
+    __shared__ int nbs[TSD_MAX_L * TSD_MAX_MODES];
+    __shared__ int s_bad, s_bucket, s_need;
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int KB = K * B;
+    const int64_t N = (int64_t)L * KB;
+    const int64_t base = (int64_t)t * N;
+    const int64_t out0 = (int64_t)t * (B + 1);
+    const int H = pow2_ceil(2 * KB);
+    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(sms);
+    int* hval = reinterpret_cast<int*>(hkey + H);
+    int* rep_buf[2] = {hval + H, hval + H + KB};  // representatives of one depth, by (mode, place)
+    if (tid == 0) s_bad = 0;
+    for (int i = tid; i < L * K; i += blockDim.x) nbs[i] = ws.nb[(int64_t)t * L * K + i];
+    __syncthreads();
+    for (int i = tid; i < K * L * k; i += blockDim.x) {
+        const double x = bws.top_zt[(int64_t)t * K * L * k + i];
+        if (x != x) s_bad = 1;
+    }
+    for (int i = tid; i < K * L; i += blockDim.x) {
+        const double x = bws.lse[(int64_t)t * K * L + i];
+        if (x != x) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad) {
+        for (int i = tid; i <= B; i += blockDim.x) {
+            parent[out0 + i] = -1;
+            token[out0 + i] = -1;
+            depth[out0 + i] = -1;
+            score[out0 + i] = -INFINITY;
+        }
+        if (tid == 0) {
+            n_nodes[t] = 0;
+            status[t] = kStatNonFinite;
+            if (n_cand) n_cand[t] = 0;
+        }
+        return;
+    }
+    // 1. distinct prefixes, depth by depth: rep = flat index of the first
+    //    appearance; every list entry is compacted, in flat order, into the
+    //    candidate arrays when it is its own representative with mass
+    int n_f = 0;
+    // thread tid holds entries e = S tid + q, q < S, of each depth (S = K B /
+    // threads rounded up, at most 4); the next depth's tokens, parents and
+    // images are loaded while this one hashes
+    int32_t tk[kMaxSlotsPerThread], pp[kMaxSlotsPerThread];
+    unsigned long long im[kMaxSlotsPerThread];
+    bool lv[kMaxSlotsPerThread];
+    const int S = (KB + blockDim.x - 1) / blockDim.x;
+    auto load_depth = [&](int d, int32_t* tk_, int32_t* pp_, unsigned long long* im_, bool* lv_) {
+#pragma unroll
+        for (int q = 0; q < kMaxSlotsPerThread; ++q) {
+            const int e = S * tid + q;
+            lv_[q] = q < S && e < KB && (e % B) < nbs[d * K + e / B];
+            const int64_t f = base + (int64_t)d * KB + e;
+            tk_[q] = lv_[q] ? ws.tok[f] : 0;
+            pp_[q] = lv_[q] && d > 0 ? ws.par[f] : -1;
+            im_[q] = lv_[q] ? ws.kimg[f] : ~kNegInfImage;
+        }
+    };
+    load_depth(0, tk, pp, im, lv);
+    for (int d = 0; d < L; ++d) {
+        int* rep_prev = rep_buf[(d & 1) ^ 1];
+        int* rep_cur = rep_buf[d & 1];
+        int32_t tk2[kMaxSlotsPerThread], pp2[kMaxSlotsPerThread];
+        unsigned long long im2[kMaxSlotsPerThread];
+        bool lv2[kMaxSlotsPerThread];
+        if (d + 1 < L) load_depth(d + 1, tk2, pp2, im2, lv2);
+        for (int h = tid; h < H; h += blockDim.x) {
+            hkey[h] = kEmpty;
+            hval[h] = INT_MAX;
+        }
+        __syncthreads();
+        int slot[kMaxSlotsPerThread];
+#pragma unroll
+        for (int q = 0; q < kMaxSlotsPerThread; ++q) {
+            slot[q] = -1;
+            if (!lv[q]) continue;
+            const int e = S * tid + q, m = e / B;
+            const int f = d * KB + e;
+            const int pr = d == 0 ? -1 : rep_prev[m * B + pp[q]];
+            const unsigned long long key =
+                ((unsigned long long)(unsigned)(pr + 1) << 32) | (unsigned)tk[q];
+            unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (unsigned)(H - 1);
+            for (int probe = 0; probe < H; ++probe) {
+                const unsigned long long old = atomicCAS(&hkey[h], kEmpty, key);
+                if (old == kEmpty || old == key) {
+                    atomicMin(&hval[h], f);
+                    slot[q] = (int)h;
+                    break;
+                }
+                h = (h + 1) & (unsigned)(H - 1);
+            }
+        }
+        __syncthreads();
+        // representatives, and the compaction of those with mass in flat order
+        int cnt = 0;
+        bool keep[kMaxSlotsPerThread];
+#pragma unroll
+        for (int q = 0; q < kMaxSlotsPerThread; ++q) {
+            const int e = S * tid + q;
+            keep[q] = false;
+            if (slot[q] < 0) continue;
+            const int r = hval[slot[q]];
+            rep_cur[e] = r;
+            ws.rep[base + (int64_t)d * KB + e] = r;
+            keep[q] = r == d * KB + e && im[q] != ~kNegInfImage;
+            cnt += keep[q];
+        }
+        int tot;
+        int pos = n_f + block_excl_scan_i(cnt, red, &tot);  // also orders rep_cur's writes
+#pragma unroll
+        for (int q = 0; q < kMaxSlotsPerThread; ++q) {
+            if (!keep[q]) continue;
+            ws.cimg[base + pos] = im[q];
+            ws.cflat[base + pos] = d * KB + S * tid + q;
+            ++pos;
+        }
+        n_f += tot;
+#pragma unroll
+        for (int q = 0; q < kMaxSlotsPerThread; ++q) {
+            tk[q] = tk2[q];
+            pp[q] = pp2[q];
+            im[q] = im2[q];
+            lv[q] = d + 1 < L && lv2[q];
+        }
+    }
+    const unsigned long long* cimg = ws.cimg + base;
+    const int32_t* cflat = ws.cflat + base;
+    // 2. radix select of the B-th best image among the candidates
+    int take = n_f < B ? n_f : B;
+    unsigned long long prefix = 0, mask = 0;
+    int need = take;  // 1-based rank of the threshold among the remaining
+    const bool cut = n_f > B;
+    if (take > 0 && cut) {
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+            for (int c0 = 0; c0 < n_f; c0 += 4 * blockDim.x) {
+                unsigned long long v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + q * blockDim.x + tid;
+                    v[q] = c < n_f ? cimg[c] : ~0ull;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + q * blockDim.x + tid;
+                    if (c < n_f && (v[q] & mask) == prefix)
+                        atomicAdd(&hist[(unsigned)(v[q] >> shift) & 255u], 1u);
+                }
+            }
+            __syncthreads();
+            if (tid < 32) {
+                unsigned run = 0;
+                unsigned v[8];
+                for (int q = 0; q < 8; ++q) {
+                    v[q] = hist[tid * 8 + q];
+                    run += v[q];
+                }
+                unsigned incl = run;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                unsigned before = incl - run;
+                // the lane whose range holds the need-th element
+                if (before < (unsigned)need && (unsigned)need <= incl) {
+                    for (int q = 0; q < 8; ++q) {
+                        if ((unsigned)need <= before + v[q]) {
+                            s_bucket = tid * 8 + q;
+                            s_need = need - (int)before;
+                            break;
+                        }
+                        before += v[q];
+                    }
+                }
+            }
+            __syncthreads();
+            prefix |= (unsigned long long)s_bucket << shift;
+            mask |= 255ull << shift;
+            need = s_need;
+            __syncthreads();
+        }
+    }
+    const unsigned long long theta = prefix;
+    // 3. compaction in flat order: every candidate below theta, and the first
+    //    `need` equal to it
+    unsigned long long* sk0 = reinterpret_cast<unsigned long long*>(sms);
+    const int n2 = pow2_ceil(take < 32 ? 32 : take);
+    unsigned long long* sk1 = sk0 + n2;
+    __syncthreads();  // the hash table's space is reused
+    {
+        // position of a kept candidate = (candidates below theta before it) +
+        // min(candidates equal to theta before it, need); one packed scan of
+        // (below, equal) counts per four candidates a thread
+        __shared__ unsigned long long red64[33];
+        unsigned long long carry = 0;
+        for (int c0 = 0; c0 < n_f; c0 += 4 * blockDim.x) {
+            unsigned long long img[4];
+            unsigned long long cnt = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = c0 + 4 * tid + q;
+                img[q] = c < n_f ? cimg[c] : ~0ull;
+                if (c < n_f) cnt += (!cut || img[q] < theta) ? 1ull : (img[q] == theta ? 1ull << 32 : 0ull);
+            }
+            unsigned long long tot;
+            unsigned long long run = carry + block_excl_scan_u64(cnt, red64, &tot);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = c0 + 4 * tid + q;
+                if (c >= n_f) continue;
+                const int lt = (int)(run & 0xffffffffull), eq = (int)(run >> 32);
+                const bool below = !cut || img[q] < theta;
+                const bool equal = !below && img[q] == theta;
+                if (below || (equal && eq < need)) {
+                    const int pos = lt + min(eq, need);
+                    if (pos < take) {
+                        sk0[pos] = img[q];
+                        sk1[pos] = (unsigned long long)cflat[c];
+                    }
+                }
+                run += below ? 1ull : (equal ? 1ull << 32 : 0ull);
+            }
+            carry += tot;
+        }
+        const int kept = (int)(carry & 0xffffffffull) + min((int)(carry >> 32), cut ? need : 0);
+        take = kept < take ? kept : take;  // equal unless the counts disagree
+    }
+    for (int i = take + tid; i < n2; i += blockDim.x) {
+        sk0[i] = kEmpty;
+        sk1[i] = kEmpty;
+    }
+    __syncthreads();
+    // 4. order the kept entries by (image asc, flat index asc)
+    for (int kk = 2; kk <= n2; kk <<= 1) {
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < n2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a0 = sk0[i], a1 = sk1[i], b0 = sk0[l], b1 = sk1[l];
+                    if (((i & kk) == 0) == pair_less(b0, b1, a0, a1)) {
+                        sk0[i] = b0;
+                        sk1[i] = b1;
+                        sk0[l] = a0;
+                        sk1[l] = a1;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // 5. emit: node q+1 is the q-th kept entry; parents come first
+    for (int q = tid; q < take; q += blockDim.x)
+        if (sk1[q] < (unsigned long long)N) ws.node_of[base + (int64_t)sk1[q]] = q + 1;
+    __syncthreads();
+    for (int q = tid; q < B; q += blockDim.x) {
+        const int64_t o = out0 + 1 + q;
+        if (q < take && sk1[q] < (unsigned long long)N) {
+            const int64_t f = (int64_t)sk1[q];
+            const int d = (int)(f / KB), e = (int)(f - (int64_t)d * KB), m = e / B;
+            int pn = 0;
+            if (d > 0)
+                pn = ws.node_of[base + ws.rep[base + (int64_t)(d - 1) * KB + (int64_t)m * B +
+                                              ws.par[base + f]]];
+            parent[o] = pn;
+            token[o] = ws.tok[base + f];
+            depth[o] = d + 1;
+            const double key = key_score(~ws.kimg[base + f]);
+            score[o] = (float)key;
+            if (bws.score64) bws.score64[out0 + 1 + q] = key;
+        } else {
+            parent[o] = -1;
+            token[o] = -1;
+            depth[o] = -1;
+            score[o] = -INFINITY;
+        }
+    }
+    if (tid == 0) {
+        parent[out0] = -1;
+        token[out0] = -1;
+        depth[out0] = 0;
+        score[out0] = 0.0f;
+        n_nodes[t] = take + 1;
+        status[t] = kStatOk;
+        if (n_cand) n_cand[t] = n_f;
+    }
+}
+
+cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, int K, int L,
+                            int64_t V, int k, int B, double temp, const float* log_prior,
+                            const BuildWs& bws, const LseWs& ws, int32_t* parent, int32_t* token,
+                            int32_t* depth, float* score, int32_t* n_nodes, int32_t* status,
+                            int32_t* n_cand, cudaStream_t stream) {
+    const size_t sb = lse_beam_smem(K, B, k);
+    cudaError_t e = cudaFuncSetAttribute(lse_beam_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(lse_beam_kernel, dim3((unsigned)K, (unsigned)n_trees), kBeamThreads, sb, stream,
+                   logits, dtype, K, L, V, k, B, temp, log_prior, bws, ws);
+    if (e != cudaSuccess) return e;
+    const size_t ss = lse_select_smem(K, B);
+    e = cudaFuncSetAttribute(lse_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(lse_select_kernel, (unsigned)n_trees, kSelThreads, ss, stream, K, L, k, B, bws,
+                      ws, parent, token, depth, score, n_nodes, status, n_cand);
+}
+
+}  // namespace tsd

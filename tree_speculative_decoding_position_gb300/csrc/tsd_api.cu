@@ -147,6 +147,35 @@ size_t forest_ws_layout(int n_trees, int L, int64_t V, int topk, int B, int esiz
     return (cv.off + kAlign - 1) & ~(kAlign - 1);
 }
 
+size_t lse_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
+                     void* base, BuildWs* out, LseWs* lout) {
+    Carve cv{static_cast<uint8_t*>(base)};
+    const size_t rows = (size_t)n_trees * n_modes * L;
+    const size_t nch = (size_t)n_chunks(V, esize);
+    BuildWs ws;
+    ws.chunk = cv.take<ChunkStat>(rows * nch);
+    ws.lane_max = cv.take<float>(rows * nch * kWarp);
+    ws.top_id = cv.take<int32_t>(rows * topk);
+    ws.top_zt = cv.take<double>(rows * topk);
+    ws.lse = cv.take<double>(rows);
+    ws.heap = nullptr;
+    ws.heap_stride = 0;
+    ws.score64 = nullptr;
+    const size_t ent = rows * (size_t)B;  // L * K * B entries per tree
+    LseWs l;
+    l.tok = cv.take<int32_t>(ent);
+    l.par = cv.take<int32_t>(ent);
+    l.kimg = cv.take<unsigned long long>(ent);
+    l.rep = cv.take<int32_t>(ent);
+    l.node_of = cv.take<int32_t>(ent);
+    l.cimg = cv.take<unsigned long long>(ent);
+    l.cflat = cv.take<int32_t>(ent);
+    l.nb = cv.take<int32_t>(rows);
+    if (out) *out = ws;
+    if (lout) *lout = l;
+    return (cv.off + kAlign - 1) & ~(kAlign - 1);
+}
+
 size_t build_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize,
                        void* base, BuildWs* out) {
     Carve cv{static_cast<uint8_t*>(base)};
@@ -196,6 +225,12 @@ static bool build_sizes_ok(int n_trees, int n_modes, int L, int64_t V, int topk,
     return (int64_t)L * bits <= 56;
 }
 
+static bool lse_sizes_ok(int n_trees, int n_modes, int L, int64_t V, int topk, int B, int esize) {
+    return build_sizes_ok(n_trees, n_modes, L, V, topk, B, esize) && n_trees <= 65535 &&
+           B <= kMaxLseB && n_modes * B <= kMaxLseModeBudget &&
+           lse_beam_smem(n_modes, B, topk) <= kMaxLseSmem;
+}
+
 size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V, int topk, int B,
                           tsd_dtype dtype) {
     const int es = dtype_size(dtype);
@@ -213,6 +248,9 @@ size_t tsd_workspace_size(tsd_op op, int n_trees, int n_modes, int L, int64_t V,
                 (int64_t)n_trees * B > kMaxForestCandidates)
                 return 0;
             return forest_ws_layout(n_trees, L, V, topk, B, es, nullptr, nullptr, nullptr);
+        case TSD_OP_BUILD_LSE:
+            if (!lse_sizes_ok(n_trees, n_modes, L, V, topk, B, es)) return 0;
+            return lse_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr, nullptr);
         case TSD_OP_EXIT_LOSS:
             if (n_trees < 1 || L < 1 || L > TSD_MAX_L || B < 0 || B > TSD_MAX_B || V < 1 ||
                 V > 0x7fffffff || n_chunks(V, es) > kMaxDrafterChunks)
@@ -243,6 +281,38 @@ tsd_status tsd_build_tree(const void* drafter_logits, tsd_dtype dtype, int n_tre
         return TSD_ERR_CUDA;
     if (launch_build_heap(ws, n_trees, n_modes, L, topk, B, parent, token, depth, score, rank,
                           mode, n_nodes, status, stream) != cudaSuccess)
+        return TSD_ERR_CUDA;
+    return TSD_OK;
+}
+
+tsd_status tsd_build_lse_tree(const void* drafter_logits, tsd_dtype dtype, int n_trees,
+                              int n_modes, int L, int64_t V, int topk, int B, float drafter_temp,
+                              const float* log_prior, int32_t* parent, int32_t* token,
+                              int32_t* depth, float* score, int32_t* n_nodes, int32_t* status,
+                              int32_t* n_cand, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream) {
+    if (!drafter_logits || !parent || !token || !depth || !score || !n_nodes || !status ||
+        !dtype_size(dtype) || !lse_sizes_ok(n_trees, n_modes, L, V, topk, B, dtype_size(dtype)) ||
+        !(isfinite(drafter_temp) && drafter_temp >= 1e-6f))
+        return TSD_ERR_INVALID_ARG;
+    const int es = dtype_size(dtype);
+    const size_t need = lse_ws_layout(n_trees, n_modes, L, V, topk, B, es, nullptr, nullptr, nullptr);
+    if (!workspace || ws_bytes < need || (uintptr_t)workspace % 16) return TSD_ERR_WORKSPACE;
+    if (!logits_view(drafter_logits, &drafter_logits)) return TSD_ERR_INVALID_ARG;
+    if (log_prior) {
+        const void* lp = log_prior;
+        if (!logits_view(lp, &lp)) return TSD_ERR_INVALID_ARG;
+        log_prior = static_cast<const float*>(lp);
+    }
+    BuildWs ws;
+    LseWs lws;
+    lse_ws_layout(n_trees, n_modes, L, V, topk, B, es, workspace, &ws, &lws);
+    const int64_t rows = (int64_t)n_trees * n_modes * L;
+    if (launch_drafter_stats(drafter_logits, dtype, rows, V, topk, exp2_scale(drafter_temp),
+                             (double)drafter_temp, ws, stream) != cudaSuccess ||
+        launch_lse_tree(drafter_logits, dtype, n_trees, n_modes, L, V, topk, B,
+                        (double)drafter_temp, log_prior, ws, lws, parent, token, depth, score,
+                        n_nodes, status, n_cand, stream) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
 }

@@ -338,6 +338,35 @@ cudaError_t launch_forest_select(const double* score64, int32_t* depth, int n_tr
                                  const int32_t* status, int32_t* total, int32_t* parent,
                                  int32_t* token, float* score, const ForestWs& ws,
                                  cudaStream_t stream);
+// Mixture tree under the log-sum-exp score (MFD App. B Eq. 6): per-mode
+// per-depth lists, then distinct prefixes ranked by log sum_m pi_m Q_m(v).
+// Entries are indexed flat by (depth, mode, place): f = (d K + m) B + i.
+constexpr int kMaxLseModeBudget = 4096;  // n_modes * B: one depth's entries in the hash
+constexpr int kMaxLseB = 2048;
+struct LseWs {
+    int32_t* tok;      // [n_trees][L*K*B] last token of each list entry
+    int32_t* par;      // [n_trees][L*K*B] its parent's place one depth up (same mode)
+    unsigned long long* kimg;  // [n_trees][L*K*B] ~order_key of the ranking key (s_lse clamped
+                               // to the parent's key): ascending = better
+    int32_t* rep;      // [n_trees][L*K*B] flat index of the first entry holding the same prefix
+    int32_t* node_of;  // [n_trees][L*K*B] node index of a kept entry
+    unsigned long long* cimg;  // [n_trees][L*K*B] candidates' images, compacted in flat order
+    int32_t* cflat;            // [n_trees][L*K*B] their flat indices
+    int32_t* nb;       // [n_trees][L][K] list sizes
+};
+__host__ __device__ inline int pow2_ceil(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+size_t lse_beam_smem(int K, int B, int k);
+constexpr size_t kMaxLseSmem = 227 * 1024;
+size_t lse_select_smem(int K, int B);
+cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, int K, int L,
+                            int64_t V, int k, int B, double temp, const float* log_prior,
+                            const BuildWs& bws, const LseWs& ws, int32_t* parent, int32_t* token,
+                            int32_t* depth, float* score, int32_t* n_nodes, int32_t* status,
+                            int32_t* n_cand, cudaStream_t stream);
 // The drafter's streaming pass alone (ws.chunk and ws.lane_max).
 cudaError_t launch_drafter_chunks(const void* logits, tsd_dtype dtype, int64_t rows, int64_t V,
                                   float c, const BuildWs& ws, cudaStream_t stream);
