@@ -81,12 +81,14 @@ forest_prep_kernel(const double* __restrict__ score64, int B, int M_max,
     double carry = 0.0;
     for (int j0 = 0; j0 < m; j0 += blockDim.x) {
         const int j = j0 + tid;
-        const double x = j < m ? exp(score64[base + 1 + j]) : 0.0;
+        const double sc = j < m ? score64[base + 1 + j] : -INFINITY;
+        const double x = j < m ? exp(sc) : 0.0;
         double tot;
         const double ex = block_excl_scan_d(x, red, &tot);
         if (j < m) {
             ws.rho[base + j] = x;
             ws.pre[base + j] = carry + ex;
+            ws.img[base + j] = order_key(sc);
         }
         carry += tot;
     }
@@ -94,7 +96,7 @@ forest_prep_kernel(const double* __restrict__ score64, int B, int M_max,
 }
 
 __global__ void __launch_bounds__(kForestThreads)
-forest_rank_kernel(const double* __restrict__ score64, const int32_t* __restrict__ depth,
+forest_rank_kernel(const int32_t* __restrict__ depth,
                    int n_trees, int B, int M_max, double l0, double c1, ForestWs ws) {
     pdl_entry();
     __shared__ int fail_min, count_max;
@@ -109,7 +111,7 @@ forest_rank_kernel(const double* __restrict__ score64, const int32_t* __restrict
     const int m = ws.cnt[r];
     if (j < m) {
         const int64_t me = (int64_t)r * stride + 1 + j;
-        const double sc = score64[me];
+        const unsigned long long sc = ws.img[(int64_t)r * stride + j];  // score order image
         const int dc = depth[me];
         int ahead = 0;
         double G = 0.0;
@@ -120,7 +122,7 @@ forest_rank_kernel(const double* __restrict__ score64, const int32_t* __restrict
             int lo = 0, hi = ws.cnt[q];
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
-                const double sx = score64[qb + 1 + mid];
+                const unsigned long long sx = ws.img[qb + mid];
                 bool before = sx > sc;
                 if (sx == sc) {
                     const int dx = depth[qb + 1 + mid];
@@ -200,8 +202,7 @@ cudaError_t launch_forest_select(const double* score64, int32_t* depth, int n_tr
                                score64, B, M_max, (const int32_t*)n_nodes, status, ws);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((B + kRankWarps - 1) / kRankWarps), (unsigned)n_trees);
-    e = launch_pdl(forest_rank_kernel, grid, kForestThreads, 0, stream, score64,
-                   (const int32_t*)depth, n_trees, B, M_max, l0, c1, ws);
+    e = launch_pdl(forest_rank_kernel, grid, kForestThreads, 0, stream, (const int32_t*)depth, n_trees, B, M_max, l0, c1, ws);
     if (e != cudaSuccess) return e;
     return launch_pdl(forest_finish_kernel, (unsigned)n_trees, kForestThreads, 0, stream, B, ws,
                       n_nodes, status, total, parent, token, depth, score);

@@ -330,6 +330,7 @@ struct ForestWs {
     double* rho;    // [n_trees][B+1] candidate masses, candidate j at j
     double* pre;    // [n_trees][B+1] exclusive prefix sums of rho (entry cnt = total)
     int32_t* rank;  // [n_trees][B+1] place of candidate j in the global merge
+    unsigned long long* img;  // [n_trees][B+1] order image of candidate j's score
     int32_t* cnt;   // [n_trees] candidates per tree (0 for a failed tree)
     int32_t* ctl;   // [2] first failing rank, candidate count
 };
@@ -378,6 +379,8 @@ struct ExitWs {
     double* wrow;       // [n_trees][L] summed weight of the nodes each row scores
     int32_t* tstat;     // [n_trees]
     double* norm;       // [1] sum over valid trees of (n_nodes - 1)
+    float* gscale;      // [n_trees][L] gradient factor W_m / (T_d N) (0: no gradient)
+    float* gl2;         // [n_trees][L] LSE_m log2 e
     unsigned* done;     // [1] completion counter of the per-tree kernel (zero between calls)
 };
 size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* base, ExitWs* out);
