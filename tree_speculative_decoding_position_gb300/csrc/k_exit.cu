@@ -53,10 +53,9 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
                  double temp, const int32_t* __restrict__ token, const int32_t* __restrict__ depth,
                  const int32_t* __restrict__ n_nodes, int B, const float* __restrict__ omega,
                  double* __restrict__ loss_tree, double* __restrict__ loss,
-                 int32_t* __restrict__ status, bool want_grad, ExitWs ws) {
+                 int32_t* __restrict__ status, ExitWs ws) {
     pdl_entry();
     __shared__ double W[TSD_MAX_L];
-    __shared__ double s_norm;
     __shared__ double lse[TSD_MAX_L];
     __shared__ double red[kExitThreads / kWarp], red2[kExitThreads / kWarp];
     __shared__ int bad, last;
@@ -136,18 +135,6 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
         }
         *ws.norm = Bn;
         *loss = Bn > 0.0 ? A / Bn : 0.0;
-        s_norm = Bn;
-    }
-    if (!want_grad) return;
-    // the gradient's per-row factors, once: W_m / (T_d N) and LSE_m log2 e
-    __syncthreads();
-    const double Bn = s_norm;
-    for (int64_t r = tid; r < (int64_t)n_trees * L; r += blockDim.x) {
-        const int tr = (int)(r / L);
-        const double wr = *(volatile const double*)(ws.wrow + r);
-        const bool ok = *(volatile const int32_t*)(ws.tstat + tr) == kStatOk && wr != 0.0 && Bn > 0.0;
-        ws.gscale[r] = ok ? (float)(wr / (temp * Bn)) : 0.0f;
-        ws.gl2[r] = ok ? (float)(*(volatile const double*)(ws.lse + r) * 1.4426950408889634) : 0.0f;
     }
 }
 
@@ -157,13 +144,14 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
 // with all of the chunk's 16-byte loads in flight, then 16-byte streaming
 // stores; rows that are not 16-byte aligned take an element-wise loop.
 template <typename T>
-__global__ void __launch_bounds__(kExitThreads, 3)
+__global__ void __launch_bounds__(kExitThreads)
 exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, int nch, float c,
                  double temp, float* __restrict__ grad, ExitWs ws) {
     pdl_entry();
     constexpr int VEC = Lanes<T>::kVec;
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     const int lane = threadIdx.x & (kWarp - 1);
+    const double nrm = *ws.norm;
     const bool vec = ((uintptr_t)logits % 16 == 0) && ((V * (int64_t)sizeof(T)) % 16 == 0) &&
                      ((uintptr_t)grad % 16 == 0);
     const int64_t total = rows * nch;
@@ -173,10 +161,13 @@ exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, i
         const int64_t row = item / nch;
         const int64_t c0 = (item - row * nch) * (int64_t)CE;
         const int cn = (int)min((int64_t)CE, V - c0);
+        const int t = (int)(row / L);
+        const double wr = ws.wrow[row];
         float* g = grad + row * V + c0;
         const T* z = logits + row * V + c0;
-        const float scale = ws.gscale[row], l2 = ws.gl2[row];  // scale 0: a row with no gradient
-        const bool zero = scale == 0.0f;
+        const bool zero = ws.tstat[t] != kStatOk || wr == 0.0 || !(nrm > 0.0);
+        const float scale = zero ? 0.0f : (float)(wr / (temp * nrm));
+        const float l2 = zero ? 0.0f : (float)(ws.lse[row] * 1.4426950408889634);
         if (vec) {
             uint4 buf[kVecPerLane];
 #pragma unroll
@@ -241,12 +232,11 @@ cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, i
     if (dtype == TSD_BF16)
         e = launch_pdl(exit_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kExitThreads, 0, stream,
                        static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, temp,
-                       token, depth, n_nodes, B, omega, loss_tree, loss, status, grad != nullptr,
-                       ws);
+                       token, depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     else
         e = launch_pdl(exit_tree_kernel<float>, (unsigned)n_trees, kExitThreads, 0, stream,
                        static_cast<const float*>(logits), n_trees, L, V, nch, c, temp, token,
-                       depth, n_nodes, B, omega, loss_tree, loss, status, grad != nullptr, ws);
+                       depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     if (e != cudaSuccess) return e;
     if (grad) {
         int dev = 0, sms = 152;

@@ -125,8 +125,6 @@ size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* bas
     ws.wrow = cv.take<double>(rows);
     ws.tstat = cv.take<int32_t>((size_t)n_trees);
     ws.norm = cv.take<double>(1);
-    ws.gscale = cv.take<float>(rows);
-    ws.gl2 = cv.take<float>(rows);
     ws.done = cv.take<unsigned>(1);
     if (out) *out = ws;
     return (cv.off + kAlign - 1) & ~(kAlign - 1);

@@ -379,8 +379,6 @@ struct ExitWs {
     double* wrow;       // [n_trees][L] summed weight of the nodes each row scores
     int32_t* tstat;     // [n_trees]
     double* norm;       // [1] sum over valid trees of (n_nodes - 1)
-    float* gscale;      // [n_trees][L] gradient factor W_m / (T_d N) (0: no gradient)
-    float* gl2;         // [n_trees][L] LSE_m log2 e
     unsigned* done;     // [1] completion counter of the per-tree kernel (zero between calls)
 };
 size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* base, ExitWs* out);
