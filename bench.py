@@ -125,6 +125,28 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+def rank_seeds(rank: int, nt: int) -> list:
+    """Seeds of one rank's trees: each rank verifies its own trees (replicas
+    over disjoint inputs)."""
+    import synth
+    return [synth.seed_for(2, t) + 100000 * rank for t in range(nt)]
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: every rank's elapsed time, all-reduced by max."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, nt: int, ms_per_step: float) -> float:
+    """Trees verified per second by the whole job: every rank's trees per step
+    over the slowest rank's step time."""
+    return world * nt / (ms_per_step * 1e-3)
+
+
 def run_ours(args):
     import torch
 
@@ -146,7 +168,7 @@ def run_ours(args):
     nt, V, L, k, B, T = W["trees_per_gpu"], W["V"], W["L"], W["topk"], W["B"], W["temperature"]
     if args.trees:
         nt = args.trees  # a smaller batch, for profiler captures only
-    seeds = [synth.seed_for(2, t) + 100000 * rank for t in range(nt)]
+    seeds = rank_seeds(rank, nt)
     drafter = synth.zipf_drafter(nt, L, V, 0, device=dev, seeds=seeds)          # [nt,1,L,V]
     tr = tsd.tsd_build_tree(drafter, topk=k, B=B)
     target = torch.empty(nt, B + 1, V, dtype=torch.bfloat16, device=dev)
@@ -207,11 +229,7 @@ def run_ours(args):
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    total_ms = float(ms_t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     assert int((last[1]["status"] != 0).sum()) == 0, "a tree failed in the timed region"
 
     # stage durations from the events inside each step
@@ -224,7 +242,7 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     achieved = rows_bytes / (stage["tev_rows"] * 1e-3) / 1e9
     ms_per_step = total_ms / args.steps
-    value = world * nt / (ms_per_step * 1e-3)
+    value = whole_job_value(world, nt, ms_per_step)
 
     # end to end through the public API with host buffers: the drafter and
     # target logits sit in page-locked host memory and the library's kernels
@@ -272,13 +290,11 @@ def run_ours(args):
             e2.record(stream)
             torch.cuda.synchronize()
             assert int((o["status"] != 0).sum()) == 0, "a tree failed in the end-to-end run"
-            e_ms = torch.tensor([s2.elapsed_time(e2) / ke], dtype=torch.float64, device=dev)
-            if dist:
-                dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-            return {"value": world * nt / (float(e_ms.item()) * 1e-3), "unit": "rounds/s",
+            e_ms = max_over_ranks(s2.elapsed_time(e2) / ke, dist, dev)
+            return {"value": whole_job_value(world, nt, e_ms), "unit": "rounds/s",
                     "h2d_bytes_per_step": drafter.numel() * 2 + target.numel() * 2,
                     "d2h_bytes_per_step": res_h.numel() * 4, "steps": ke,
-                    "ms_per_step": float(e_ms.item())}
+                    "ms_per_step": e_ms}
 
         e2e = timed(step_host)
         e2e["how"] = "logits in pinned host memory, read by the kernels over the host link"
