@@ -136,3 +136,24 @@ def test_lse_tree_edges(tsd, dev, orc):
         tsd.tsd_build_lse_tree(torch.zeros(1, 8, 2, 64, device=dev), topk=4, B=600)
     with pytest.raises(tsd.TsdError):
         tsd.tsd_build_lse_tree(torch.zeros(1, 1, 2, 64, device=dev), topk=4, B=2049)
+
+
+def test_lse_tree_large_budget_from_pinned_host(tsd, dev, orc):
+    """B = 1024 with two modes: several entries per thread in the dedupe and a
+    4096-entry sort per depth; the logits are read from page-locked host
+    memory, and the result equals the device-resident one."""
+    nt, K, L, V, k, B = 2, 2, 4, 5000, 8, 1024
+    dr, _, _ = synth.mixture_drafter(nt, K, L, V, synth.seed_for(13), dtype=torch.float32)
+    host = dr.pin_memory()
+    out = tsd.tsd_build_lse_tree(host, topk=k, B=B, device=dev)
+    same = tsd.tsd_build_lse_tree(dr.to(dev), topk=k, B=B)
+    torch.cuda.synchronize()
+    for key in ("parent", "token", "depth", "score", "n_nodes", "n_cand"):
+        assert torch.equal(out[key], same[key]), key
+    flips = 0
+    for t in range(nt):
+        z = dr[t].double().numpy()
+        ref = orc.lse_tree(z, 1.0, k, B)
+        assert int(out["n_cand"][t]) == ref["n_cand"]
+        flips += _compare(out, t, ref, z, 1.0, k, None)
+    assert flips <= 4
