@@ -335,6 +335,15 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def oracle_ms(fn) -> float:
+    """Wall time of one call of the float64 oracle on the host (one thread)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    fn(oracle)
+    return 1e3 * (time.perf_counter() - t0)
+
+
 def exit_loss_bench(tsd, torch, stream, drafter, tree, tev, V):
     """The exit-guided loss on the workload's drafter rows (32 trees x 16 rows),
     weighted by the step's TEV exit masses: loss alone, and loss with its
@@ -376,6 +385,14 @@ def exit_loss_bench(tsd, torch, stream, drafter, tree, tev, V):
         out["exit_loss" + ("_with_grad" if grad else "")] = {
             "ms": ms, "algorithmic_gb": nbytes / 1e9, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_of_measured": nbytes / (ms * 1e-3) / 1e9 / measured_peaks()[0]}
+    # the oracle beside it: one tree's loss and gradient, float64, one host thread
+    z0 = drafter[0, 0].float().cpu().numpy()
+    tk, dp = tree["token"][0].cpu().numpy(), tree["depth"][0].cpu().numpy()
+    n0, w0 = int(tree["n_nodes"][0]), tev["exit_mass"][0].float().cpu().numpy()
+    o_ms = oracle_ms(lambda orc: orc.exit_loss(z0, 1.0, tk, dp, n0, w0, with_grad=True))
+    out["exit_loss_with_grad"].update(oracle_ms_per_tree=o_ms,
+                                      ms_per_tree=out["exit_loss_with_grad"]["ms"] / nt,
+                                      oracle_sample="one tree (16 rows), loss and gradient")
     return out
 
 
@@ -418,6 +435,18 @@ def forest_bench(tsd, torch, stream, drafter, k, B):
         out["forest_S%d" % S] = {"ms": s.elapsed_time(e) / 10, "M_star": M,
                                  "width_min": int(w.min()), "width_max": int(w.max()),
                                  "objective": (G + nt) / (1.0 + c1 * M)}
+    # the oracle beside it: one request's tree, and the selection over all 32
+    # requests' builder trees (S = 2048)
+    import numpy as np
+    z0 = drafter[0, 0].float().cpu().numpy()
+    tb = tsd.tsd_build_tree(drafter, topk=k, B=B, workspace=wsb)
+    sc = tb["score"].double().cpu().numpy()
+    dp, nn = tb["depth"].cpu().numpy(), tb["n_nodes"].cpu().numpy()
+    b_ms = oracle_ms(lambda orc: orc.build_tree(orc.drafter_lists(z0, 1.0, k), B))
+    s_ms = oracle_ms(lambda orc: orc.forest_select(sc, dp, nn, nt * B, 1.0, 1.0 / 2048))
+    out["forest_S2048"].update(oracle_ms=b_ms * nt + s_ms, oracle_select_ms=s_ms,
+                               oracle_sample="one request's tree (x 32 requests) plus the selection "
+                                             "over 32 trees; float64, one host thread")
     return out
 
 
@@ -446,6 +475,16 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         e.record(stream)
         torch.cuda.synchronize()
         out["verifier_ms_b256_x32_" + name] = s.elapsed_time(e) / 10
+    # the oracle beside them: one tree of the 32, float64, one host thread
+    n0 = int(tree["n_nodes"][0])
+    z0 = target[0, :n0].float().cpu().numpy()
+    p0, t0_ = tree["parent"][0].cpu().numpy(), tree["token"][0].cpu().numpy()
+    q0 = q[0].double().cpu().numpy()
+    out["verifier_oracle_ms_per_tree"] = {
+        "seqres": oracle_ms(lambda orc: orc.seqres(z0, p0, t0_, n0, T, 1)),
+        "proposal": oracle_ms(lambda orc: orc.proposal(z0, p0, t0_, n0, T, q0, 1)),
+        "tev": oracle_ms(lambda orc: orc.tev(z0, p0, t0_, n0, T, 1)),
+        "sample": "tree 0 of the 32 (B=256, V=151936)"}
     # batch-1 round, V=151936, B=64, T=1: 32 rotating copies (632 MB > 4x L2)
     B1 = 64
     dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device=dev)
@@ -588,7 +627,12 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         "mean_accept_len": statistics.mean(acc_l), "max_rule_mean_accept_len": statistics.mean(acc_m),
         "mean_coverage_plus_1": statistics.mean(cov_l) + 1.0,
         "mean_candidates": float(tl["n_cand"].float().mean()),
-        "status_ok": int((tl["status"] == 0).sum())}
+        "status_ok": int((tl["status"] == 0).sum()),
+        "ms_per_tree": lse_ms / nt_m}
+    zm = mix[0].float().cpu().numpy()
+    out["mixture_lse_k8_b128_x16"].update(
+        oracle_ms_per_tree=oracle_ms(lambda orc: orc.lse_tree(zm, 1.0, 8, B_m)),
+        oracle_sample="tree 0 of the 16 (K=8, L=16, B=128), float64, one host thread")
     return out
 
 
