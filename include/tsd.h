@@ -265,7 +265,7 @@ tsd_status tsd_build_forest(const void *drafter_logits, tsd_dtype dtype, int n_t
  *                 -inf; need not be normalised); NULL = uniform 1/n_modes.
  * Sizes as tsd_build_tree's, and also B <= 2048, n_modes * B <= 4096,
  * n_trees <= 65535, and one mode's lists must fit in a block's shared memory:
- * 16 n_modes B + 40 B + 12 P + 2496 bytes <= 227 KB, P the power of two at or
+ * 16 n_modes B + 40 B + 24 P + 2496 bytes <= 227 KB, P the power of two at or
  * above sum_{r < topk} floor(B / (r+1)) (the children that can be kept);
  * else TSD_ERR_INVALID_ARG.
  * Outputs: parent, token, depth [n_trees][B+1] int32 and score (the ranking

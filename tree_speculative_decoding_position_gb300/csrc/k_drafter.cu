@@ -350,7 +350,7 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
         }
         if (lane < k) {
             ws.top_id[row * k + lane] = ei;
-            ws.top_zt[row * k + lane] = (double)ev / temp;
+            ws.top_zt[row * k + lane] = temp == 1.0 ? (double)ev : (double)ev / temp;  // z / T_d
         }
     } else if (wid == 1) {
         const float mc = __fmul_rn(m, c);

@@ -14,10 +14,10 @@
 // summed log-normaliser, so path sums of z/T decide the order.
 //
 // lse_beam_kernel    one CTA per (mode, tree), depth by depth.  The children
-//                    of the previous list form k lists, one per token rank,
-//                    each already sorted; a child's place in their merge is
-//                    its own parent's place plus one binary search per other
-//                    rank.  Children placed below B are kept.  Each kept
+//                    of the previous list form k runs, one per token rank,
+//                    each already sorted; only children with (r+1)(i+1) <= B
+//                    can be kept, and those runs are merged in log2(k) rounds
+//                    of binary searches.  The first B are kept.  Each kept
 //                    entry then gathers its token's logit under every mode
 //                    (full rows), extends the per-mode path sums, and takes
 //                    s_lse = log sum_m exp(log pi_m + path sum - summed LSE),
@@ -43,70 +43,50 @@ __device__ __forceinline__ double load_logit(const void* logits, tsd_dtype dtype
     return (double)reinterpret_cast<const float*>(logits)[off];
 }
 
-// Ascending bitonic sort of the pairs (k0[i], k1[i]), i < n2 (a power of two,
-// at least 32), by the whole block: strides below 32 with warp shuffles on
-// one element a lane, strides of 32 and up through shared memory.
-__device__ __forceinline__ void lane_steps(unsigned long long& x0, unsigned& x1, int e, int kk,
-                                           int jtop) {
-    const int lane = threadIdx.x & 31;
-    for (int j = jtop; j > 0; j >>= 1) {
-        const unsigned long long y0 = __shfl_xor_sync(0xffffffffu, x0, j);
-        const unsigned y1 = __shfl_xor_sync(0xffffffffu, x1, j);
-        const bool lower = (lane & j) == 0, asc = (e & kk) == 0;
-        const bool x_first = x0 < y0 || (x0 == y0 && x1 < y1);
-        if ((lower == asc) != x_first) {
-            x0 = y0;
-            x1 = y1;
-        }
-    }
-}
-
-__device__ void block_sort_pairs(unsigned long long* k0, unsigned* k1, int n2) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nblk = n2 >> 5;
-    for (int b = wid; b < nblk; b += nw) {
-        const int e = (b << 5) + lane;
-        unsigned long long x0 = k0[e];
-        unsigned x1 = k1[e];
-        for (int kk = 2; kk <= 32; kk <<= 1) lane_steps(x0, x1, e, kk, kk >> 1);
-        k0[e] = x0;
-        k1[e] = x1;
-    }
-    __syncthreads();
-    for (int kk = 64; kk <= n2; kk <<= 1) {
-        for (int jj = kk >> 1; jj >= 32; jj >>= 1) {
-            const int sh = __ffs(jj) - 1;
-            for (int x = threadIdx.x; x < (n2 >> 1); x += blockDim.x) {
-                const int i = ((x >> sh) << (sh + 1)) | (x & (jj - 1)), l = i | jj;
-                const unsigned long long a0 = k0[i], b0 = k0[l];
-                const unsigned a1 = k1[i], b1 = k1[l];
-                const bool l_first = b0 < a0 || (b0 == a0 && b1 < a1);
-                if (((i & kk) == 0) == l_first) {
-                    k0[i] = b0;
-                    k0[l] = a0;
-                    k1[i] = b1;
-                    k1[l] = a1;
-                }
+// Merge of kf sorted runs of (k0, k1) pairs, run r at [off[r], off[r+1]), in
+// ceil(log2 kf) rounds: each round merges neighbouring groups of runs, and
+// every element finds its place by one binary search in the other half of its
+// group (keys are unique, so "less than" decides).  The second key is
+// (i << 5) | r, so an element's run is its rank r (its low 5 bits).  Returns 1 when the result is
+// in (d0, d1), 0 when in (k0, k1).
+__device__ int merge_runs(unsigned long long* k0, unsigned* k1, unsigned long long* d0,
+                          unsigned* d1, const int* off, int kf) {
+    int flip = 0;
+    for (int w = 1; w < kf; w <<= 1) {
+        const unsigned long long* a0 = flip ? d0 : k0;
+        const unsigned* a1 = flip ? d1 : k1;
+        unsigned long long* b0 = flip ? k0 : d0;
+        unsigned* b1 = flip ? k1 : d1;
+        const int n = off[kf];
+        for (int j = threadIdx.x; j < n; j += blockDim.x) {
+            const unsigned long long x0 = a0[j];
+            const unsigned x1 = a1[j];
+            const int g = (int)(x1 & 31u) / (2 * w);  // the element's run is its rank
+            const int lo = off[g * 2 * w], mid = off[min(g * 2 * w + w, kf)];
+            const int hi = off[min(g * 2 * w + 2 * w, kf)];
+            const bool left = j < mid;
+            int blo = left ? mid : lo, bhi = left ? hi : mid;  // the other half
+            while (blo < bhi) {
+                const int m = (blo + bhi) >> 1;
+                const bool less = a0[m] < x0 || (a0[m] == x0 && a1[m] < x1);
+                if (less) blo = m + 1;
+                else bhi = m;
             }
-            __syncthreads();
-        }
-        for (int b = wid; b < nblk; b += nw) {
-            const int e = (b << 5) + lane;
-            unsigned long long x0 = k0[e];
-            unsigned x1 = k1[e];
-            lane_steps(x0, x1, e, kk, 16);
-            k0[e] = x0;
-            k1[e] = x1;
+            const int pos = lo + (left ? j - lo : j - mid) + (blo - (left ? mid : lo));
+            b0[pos] = x0;
+            b1[pos] = x1;
         }
         __syncthreads();
+        flip ^= 1;
     }
+    return flip;
 }
 
 // Image of -inf under order_key: the smallest image of a non-NaN double.
 constexpr unsigned long long kNegInfImage = 0x000FFFFFFFFFFFFFull;
 
-// Children that can be kept: sum over ranks r of min(B, B / (r+1)), padded to
-// a power of two for the sort.
+// Children that can be kept: at most sum over ranks r of B / (r+1) (rounded
+// up to a power of two, at least 32).
 static __host__ __device__ int lse_sort_cap(int B, int k) {
     int n = 0;
     for (int r = 0; r < k; ++r) n += B / (r + 1);
@@ -116,7 +96,7 @@ static __host__ __device__ int lse_sort_cap(int B, int k) {
 size_t lse_beam_smem(int K, int B, int k) {
     return sizeof(double) * (size_t)(2 * B * K + 4 * B + TSD_MAX_TOPK * (1 + TSD_MAX_MODES) +
                                      3 * TSD_MAX_MODES) +
-           (sizeof(unsigned long long) + sizeof(unsigned)) * (size_t)lse_sort_cap(B, k) +
+           2 * (sizeof(unsigned long long) + sizeof(unsigned)) * (size_t)lse_sort_cap(B, k) +
            sizeof(int) * (size_t)(2 * B);
 }
 
@@ -135,8 +115,10 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
     double* lp = cum + TSD_MAX_MODES;           // [K] log prior
     double* cst = lp + TSD_MAX_MODES;           // [K] log prior - summed log-normalisers
     unsigned long long* ckey = reinterpret_cast<unsigned long long*>(cst + TSD_MAX_MODES);
-    unsigned* cidx = reinterpret_cast<unsigned*>(ckey + lse_sort_cap(B, k));
-    int* par = reinterpret_cast<int*>(cidx + lse_sort_cap(B, k));  // [B] parent place of each kept child
+    unsigned long long* ckey2 = ckey + lse_sort_cap(B, k);  // merge buffer
+    unsigned* cidx = reinterpret_cast<unsigned*>(ckey2 + lse_sort_cap(B, k));
+    unsigned* cidx2 = cidx + lse_sort_cap(B, k);
+    int* par = reinterpret_cast<int*>(cidx2 + lse_sort_cap(B, k));  // [B] parent place of each kept child
     int* rk = par + B;                                        // [B] token rank of each kept child
     __shared__ int s_n, s_bad, s_kf;
     __shared__ int s_off[TSD_MAX_TOPK + 1];  // offsets of the ranks' possible children
@@ -154,19 +136,25 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
     __syncthreads();
     int np = 1, cur = 0;
     // one depth ahead: this mode's kept z/T, every mode's log-normaliser, and
-    // the kept tokens' logits under every mode (gathered from the full rows)
+    // the kept tokens' logits under every mode (gathered from the full rows);
+    // the kept tokens' ids two depths ahead, so that no gather waits for them
     double f_zt = 0.0, f_lse = 0.0, f_z = 0.0;
+    int32_t f_tok = 0;
+    auto fetch_tok = [&](int d) {
+        if (tid < k * K) f_tok = bws.top_id[(tree_rows + (int64_t)m * L + d) * k + tid / K];
+    };
     auto fetch = [&](int d) {
         const int64_t row = tree_rows + (int64_t)m * L + d;
         if (tid < k) f_zt = bws.top_zt[row * k + tid];
         if (tid < K) f_lse = bws.lse[tree_rows + (int64_t)tid * L + d];
-        if (tid < k * K) {
-            const int r = tid / K, m2 = tid - r * K;
-            const int32_t tok = bws.top_id[row * k + r];
-            f_z = load_logit(logits, dtype, (tree_rows + (int64_t)m2 * L + d) * V + tok);
-        }
+        if (tid < k * K)
+            f_z = load_logit(logits, dtype, (tree_rows + (int64_t)(tid % K) * L + d) * V + f_tok);
     };
-    if (!s_bad) fetch(0);
+    if (!s_bad) {
+        fetch_tok(0);
+        fetch(0);
+        if (L > 1) fetch_tok(1);
+    }
     for (int d = 0; d < L; ++d) {
         const int64_t row = tree_rows + (int64_t)m * L + d;
         int32_t* nb_out = ws.nb + ((int64_t)t * L + d) * K + m;
@@ -179,51 +167,54 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
             cum[tid] = cum[tid] + f_lse;
             cst[tid] = lp[tid] - cum[tid];
         }
-        if (tid < k * K) zall[tid] = f_z / temp;
-        if (d + 1 < L) fetch(d + 1);
+        if (tid < k * K) zall[tid] = temp == 1.0 ? f_z : f_z / temp;  // z / T_d
+        if (d + 1 < L) fetch(d + 1);  // f_tok holds depth d+1's ids
+        if (d + 2 < L) fetch_tok(d + 2);
         if (tid == 0) s_n = 0;
         const double* prev = ps[cur ^ 1];
         __syncthreads();
         // Lists are sorted, and a lower rank has a larger z/T, so every child
         // (i', r2) with i' <= i and r2 < r precedes child (i, r): its place is
         // at least (r+1)(i+1) - 1, and only children with (r+1)(i+1) <= B can
-        // be kept.  Those with mass are sorted by (path sum desc, i asc, r asc)
-        // -- complemented order image, then c = i k + r -- and the first B
-        // form the new list.
-        if (tid == 0) {
-            int kf = 0, tot = 0;
-            while (kf < k && zt[kf] != -INFINITY) {  // ranks with mass come first
-                s_off[kf] = tot;
-                tot += min(np, B / (kf + 1));
-                ++kf;
+        // be kept.  Those with mass are ordered by (path sum desc, i asc, r
+        // asc) -- complemented order image, then (i << 5) | r -- by merging
+        // the per-rank runs, and the first B form the new list.
+        if (tid < kWarp) {  // ranks with mass come first: kf of them
+            const bool fin = tid < k && zt[tid] != -INFINITY;
+            const int kf = __popc(__ballot_sync(0xffffffffu, fin));
+            const int len = tid < kf ? min(np, B / (tid + 1)) : 0;
+            int incl = len;
+            for (int o = 1; o < kWarp; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
             }
-            s_off[kf] = tot;
-            s_kf = kf;
+            if (tid < kf) s_off[tid] = incl - len;  // exclusive offsets
+            if (tid == kWarp - 1) {                 // lane 31's inclusive sum is the total
+                s_off[kf] = incl;
+                s_kf = kf;
+            }
         }
         __syncthreads();
         const int kf = s_kf, nc = s_off[kf];
-        const int n2 = pow2_ceil(nc < 32 ? 32 : nc);
-        for (int j = tid; j < n2; j += blockDim.x) {
-            unsigned long long a = ~0ull;
-            unsigned b = ~0u;
-            if (j < nc) {
-                int r = 0;
-                while (s_off[r + 1] <= j) ++r;
-                const int i = j - s_off[r];
-                a = ~order_key((d == 0 ? 0.0 : prev[i]) + zt[r]);
-                b = (unsigned)(i * k + r);
-            }
-            ckey[j] = a;
-            cidx[j] = b;
+        // run r holds rank r's possible children in parent order: already
+        // sorted by (complemented path-sum image, i k + r)
+        for (int j = tid; j < nc; j += blockDim.x) {
+            int r = 0;
+            while (s_off[r + 1] <= j) ++r;
+            const int i = j - s_off[r];
+            ckey[j] = ~order_key((d == 0 ? 0.0 : prev[i]) + zt[r]);
+            cidx[j] = ((unsigned)i << 5) | (unsigned)r;  // orders as (i, r); k <= 32
         }
         __syncthreads();
-        block_sort_pairs(ckey, cidx, n2);
+        const bool in2 = merge_runs(ckey, cidx, ckey2, cidx2, s_off, kf) != 0;
+        const unsigned long long* sk0 = in2 ? ckey2 : ckey;
+        const unsigned* sk1 = in2 ? cidx2 : cidx;
         double* nps = ps[cur];
         const int nkeep = nc < B ? nc : B;
         for (int j = tid; j < nkeep; j += blockDim.x) {
-            nps[j] = key_score(~ckey[j]);
-            par[j] = (int)(cidx[j] / (unsigned)k);
-            rk[j] = (int)(cidx[j] % (unsigned)k);
+            nps[j] = key_score(~sk0[j]);
+            par[j] = (int)(sk1[j] >> 5);
+            rk[j] = (int)(sk1[j] & 31u);
         }
         if (tid == 0) s_n = nkeep;
         __syncthreads();
