@@ -109,3 +109,50 @@ def test_pageable_host_logits_are_refused(lib):
         tsd.tsd_verify_tev(torch.zeros(1, 9, 32), torch.zeros(1, 9, dtype=torch.int32),
                            torch.zeros(1, 9, dtype=torch.int32), torch.ones(1, dtype=torch.int32),
                            1.0, seed=0)
+
+
+def test_newer_operations_check_sizes_and_arguments_on_the_host(lib):
+    """Workspace sizes and argument errors of the exit loss, the shared-budget
+    widths, the log-sum-exp tree and the two walk verifiers, with no GPU."""
+    import torch
+    V, bf = 151936, torch.bfloat16
+    ws = tsd.tsd_workspace_size
+    assert ws(tsd.TSD_OP_EXIT_LOSS, 32, 1, 16, V, 1, 256, bf) > 0
+    assert ws(tsd.TSD_OP_EXIT_LOSS, 32, 1, 32, V, 1, 256, bf) == 0        # L above TSD_MAX_L
+    assert ws(tsd.TSD_OP_BUILD_FOREST, 32, 1, 16, V, 8, 256, bf) > 0
+    assert ws(tsd.TSD_OP_BUILD_FOREST, 33, 1, 16, V, 8, 256, bf) == 0     # > 8192 candidates
+    assert ws(tsd.TSD_OP_BUILD_FOREST, 2, 2, 16, V, 8, 64, bf) == 0       # one mode only
+    assert ws(tsd.TSD_OP_BUILD_LSE, 16, 8, 16, V, 8, 128, bf) > 0
+    assert ws(tsd.TSD_OP_BUILD_LSE, 1, 8, 16, V, 8, 600, bf) == 0         # n_modes * B > 4096
+    assert ws(tsd.TSD_OP_BUILD_LSE, 1, 1, 16, V, 8, 2049, bf) == 0        # B > 2048
+    assert ws(tsd.TSD_OP_BUILD_LSE, 1, 1, 16, V, 32, 2048, bf) == 0       # lists beyond shared memory
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: the checks fail first
+    big = 1 << 30
+    st = lib.tsd_build_forest(fake, 0, 4, 4, 32, 4, 8, 1.0, 10, 1.0, -0.5, fake, fake, fake, fake,
+                              fake, fake, fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # c1 < 0
+    st = lib.tsd_build_forest(fake, 0, 4, 4, 32, 4, 8, 1.0, 10, 0.0, 0.5, fake, fake, fake, fake,
+                              fake, fake, fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # l0 must be > 0
+    st = lib.tsd_build_forest(fake, 0, 64, 4, 512, 4, 200, 1.0, 10, 1.0, 0.5, fake, fake, fake,
+                              fake, fake, fake, fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # 12800 candidates
+    st = lib.tsd_build_lse_tree(fake, 0, 1, 2, 4, 512, 4, 2049, 1.0, None, fake, fake, fake, fake,
+                                fake, fake, None, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # B > 2048
+    st = lib.tsd_build_lse_tree(fake, 0, 1, 8, 4, 512, 4, 600, 1.0, None, fake, fake, fake, fake,
+                                fake, fake, None, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # n_modes * B > 4096
+    st = lib.tsd_build_lse_tree(fake, 0, 1, 2, 4, 512, 4, 64, 0.0, None, fake, fake, fake, fake,
+                                fake, fake, None, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # drafter temperature 0
+    st = lib.tsd_exit_loss(fake, 0, 1, 4, 32, 1.0, None, fake, fake, 8, fake, fake, fake, None,
+                           fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # no tokens
+    st = lib.tsd_verify_seqres(fake, 0, fake, fake, fake, 1, 8, 32, -1.0, 0, fake, fake, fake,
+                               fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # negative temperature
+    st = lib.tsd_verify_proposal(fake, 0, fake, fake, fake, None, 1, 8, 32, 1.0, 0, fake, fake,
+                                 fake, fake, fake, big, None)
+    assert st == tsd.TSD_ERR_INVALID_ARG                                   # no proposal
