@@ -904,7 +904,7 @@ def main():
                     help="trees per GPU (default: the workload's 32); for profiler captures")
     ap.add_argument("--sweep", action="store_true",
                     help="time TEV over B x trees x T instead (writes --sweep-out)")
-    ap.add_argument("--sweep-out", default="gpurun_out/sweep.json")
+    ap.add_argument("--sweep-out", default="sweep.json")
     ap.add_argument("--op", choices=sorted(OPS), default=None,
                     help="run one secondary operation alone on its workload (for profiler "
                          "captures): warm-up calls, then --steps timed calls")

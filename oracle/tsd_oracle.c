@@ -29,7 +29,7 @@
  *   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *           as 1, 2, 3", SC'11 -- the Philox4x64-10 counter-based generator.
  *
- * Readings where the pages are open (each also listed in the design doc):
+ * Readings where the pages are open:
  *   - Uniforms: u = (x0 >> 40) * 2^-24 from Philox4x64-10 with
  *     counter (tree, node, stream, sub) and key (seed, 0); stream 0 = TEV exit
  *     draw, 1 = TEV bonus draw, 2 = predraw at node `node` (sub 0); 3 =
