@@ -840,6 +840,21 @@ def _op_setup(name, tsd, torch, synth, dev):
     """The workload of one secondary operation, as the extras time it; returns
     a callable that issues one call."""
     V = WORKLOAD["V"]
+    if name in ("tev_b64", "build_b64"):
+        # the batch-1 round: one tree, L=16, top-k 8, B=64, TEV at T=1
+        dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device=dev)
+        t1 = tsd.tsd_build_tree(dr, topk=8, B=64)
+        n = int(t1["n_nodes"][0])
+        x = torch.zeros(1, 65, V, dtype=torch.bfloat16, device=dev)
+        synth.target_from_rows(dr[0, 0], t1["depth"][0, :n], 1.5, synth.seed_for(1, 1), out=x[0, :n])
+        wv = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 1, 1, 1, V, 1, 64,
+                                                torch.bfloat16), dtype=torch.uint8, device=dev)
+        wb = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_TREE, 1, 1, 16, V, 8, 64,
+                                                torch.bfloat16), dtype=torch.uint8, device=dev)
+        if name == "build_b64":
+            return lambda: tsd.tsd_build_tree(dr, topk=8, B=64, workspace=wb)
+        return lambda: tsd.tsd_verify_tev(x, t1["parent"], t1["token"], t1["n_nodes"], 1.0, seed=1,
+                                          workspace=wv)
     if name in ("build_lse", "build_mixture"):
         mix, _, _ = synth.mixture_drafter(16, 8, 16, V, synth.seed_for(3), device=dev)
         op = tsd.TSD_OP_BUILD_LSE if name == "build_lse" else tsd.TSD_OP_BUILD_TREE
@@ -866,7 +881,8 @@ def _op_setup(name, tsd, torch, synth, dev):
                                      with_grad=grad, workspace=ws)
 
 
-OPS = ("build_lse", "build_mixture", "build_forest", "exit_loss", "exit_loss_grad")
+OPS = ("build_lse", "build_mixture", "build_forest", "exit_loss", "exit_loss_grad", "tev_b64",
+       "build_b64")
 
 
 def run_op(args):

@@ -499,24 +499,30 @@ cudaError_t launch_rows(const void* logits, tsd_dtype dtype, int n_trees, int B,
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
     const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
-    // grid-stride over a few waves of CTAs (measured slightly faster here than
-    // one persistent wave of resident CTAs)
-    const int grid = row_grid((int64_t)n_trees * (B + 1) * nch);
+    const int64_t items = (int64_t)n_trees * (B + 1) * nch;
+    // A batch that fits in about one wave of resident CTAs runs as exactly that
+    // wave: the grid-stride loop takes the few extra items, with their loads
+    // issued early, instead of a second wave of CTAs starting cold.  Larger
+    // batches stream over a few waves of CTAs (measured slightly faster there
+    // than one persistent wave).
+    auto launch = [&](auto kernel, const auto* p) {
+        const int64_t want = (items + kRowThreads / kWarp - 1) / (kRowThreads / kWarp);
+        const int wave = resident_grid((const void*)kernel, kRowThreads, 0, INT64_MAX);
+        const int grid = want <= 2 * (int64_t)wave ? (int)(want < wave ? (want > 0 ? want : 1) : wave)
+                                                   : row_grid(items);
+        return launch_pdl(kernel, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok,
+                          n_nodes, ws);
+    };
+    cudaError_t e;
     if (dtype == TSD_BF16) {
         const auto* p = static_cast<const __nv_bfloat16*>(logits);
-        if (greedy) {
-            if (cudaError_t e_ = launch_pdl(rows_kernel<__nv_bfloat16, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
-        } else {
-            if (cudaError_t e_ = launch_pdl(rows_kernel<__nv_bfloat16, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
-        }
+        e = greedy ? launch(rows_kernel<__nv_bfloat16, true>, p)
+                   : launch(rows_kernel<__nv_bfloat16, false>, p);
     } else {
         const auto* p = static_cast<const float*>(logits);
-        if (greedy) {
-            if (cudaError_t e_ = launch_pdl(rows_kernel<float, true>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
-        } else {
-            if (cudaError_t e_ = launch_pdl(rows_kernel<float, false>, grid, kRowThreads, 0, stream, p, n_trees, B, V, nch, c, vec_ok, n_nodes, ws); e_ != cudaSuccess) return e_;
-        }
+        e = greedy ? launch(rows_kernel<float, true>, p) : launch(rows_kernel<float, false>, p);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
