@@ -872,6 +872,28 @@ def _op_setup(name, tsd, torch, synth, dev):
         return lambda: tsd.tsd_build_forest(drafter, topk=k, B=B, M_max=nt * B, l0=1.0,
                                             c1=1.0 / 2048, workspace=ws)
     tr = tsd.tsd_build_tree(drafter, topk=k, B=B)
+    if name.startswith("verify_"):
+        # the workload's verification: its 32 trees, targets as the step's
+        T = WORKLOAD["temperature"]
+        target = torch.zeros(nt, B + 1, V, dtype=torch.bfloat16, device=dev)
+        for t in range(nt):
+            n = int(tr["n_nodes"][t])
+            synth.target_from_rows(drafter[t, 0], tr["depth"][t, :n], 1.5, synth.seed_for(2, t) + 1,
+                                   out=target[t, :n])
+        wv = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, nt, 1, 1, V, 1, B,
+                                                torch.bfloat16), dtype=torch.uint8, device=dev)
+        args = (target, tr["parent"], tr["token"], tr["n_nodes"], T)
+        if name == "verify_tev":
+            return lambda: tsd.tsd_verify_tev(*args, seed=1, workspace=wv)
+        if name == "verify_seqres":
+            return lambda: tsd.tsd_verify_seqres(*args, seed=1, workspace=wv)
+        d = tr["depth"].clamp(min=1).long() - 1
+        logq = torch.log_softmax(drafter[:, 0].float(), dim=-1)
+        q = torch.stack([logq[t, d[t], tr["token"][t].clamp(min=0).long()].exp()
+                         for t in range(nt)]).float().contiguous()
+        del logq
+        return lambda: tsd.tsd_verify_proposal(target, tr["parent"], tr["token"], tr["n_nodes"], q,
+                                               T, seed=1, workspace=wv)
     w = torch.rand(nt, B + 1, generator=torch.Generator(device=dev).manual_seed(5),
                    device=dev) * (tr["depth"] >= 0)
     ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_EXIT_LOSS, nt, 1, L, V, 1, B,
@@ -882,7 +904,7 @@ def _op_setup(name, tsd, torch, synth, dev):
 
 
 OPS = ("build_lse", "build_mixture", "build_forest", "exit_loss", "exit_loss_grad", "tev_b64",
-       "build_b64")
+       "build_b64", "verify_tev", "verify_seqres", "verify_proposal")
 
 
 def run_op(args):
