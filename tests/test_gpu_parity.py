@@ -76,6 +76,27 @@ def test_build_single_mode(tsd, dev, orc, V, B, k, temp):
     assert flips <= 2, flips
 
 
+def test_build_batched_b256(tsd, dev, orc):
+    """The bench's launch: 32 trees, V=151936, L=16, top-k 8, B=256, one call;
+    every tree prefix-closed with falling scores, four sampled trees against
+    the oracle node by node."""
+    nt, B = 32, 256
+    seeds = [synth.seed_for(2, t) for t in range(nt)]
+    dr = synth.zipf_drafter(nt, 16, V_Q, 0, device=dev, seeds=seeds)
+    out = tsd.tsd_build_tree(dr, topk=8, B=B)
+    assert _np(out["status"]).tolist() == [0] * nt
+    assert _np(out["n_nodes"]).tolist() == [B + 1] * nt
+    par, sc = _np(out["parent"]), _np(out["score"])
+    for t in range(nt):
+        assert np.all((par[t, 1:] >= 0) & (par[t, 1:] < np.arange(1, B + 1)))
+        assert np.all(sc[t, 1:] <= sc[t, par[t, 1:]] + 1e-6)
+    flips = 0
+    for t in (0, 7, 19, 31):
+        ref, lists = oracle_build(orc, dr[t].cpu(), 8, B)
+        flips += compare_trees(_tree_np(out, t), ref, lists)
+    assert flips <= 2, flips
+
+
 def test_build_fp32_and_misaligned(tsd, dev, orc):
     """fp32 logits, and a row start that is not 16-byte aligned (generic path)."""
     dr = synth.zipf_drafter(1, 6, 5000, synth.seed_for(1, 3), device="cpu", dtype=torch.float32)
