@@ -126,3 +126,28 @@ def test_exit_loss_statuses_and_host_logits(tsd, dev, orc):
         assert torch.equal(host[k], dev_out[k]), k
     # the gathered terms are added with float atomics, whose order may vary
     assert torch.allclose(host["grad"], dev_out["grad"], rtol=1e-6, atol=0)
+
+
+def test_exit_loss_in_the_bench_launch(tsd, dev, orc):
+    """32 trees x 16 rows, V=151936, B=256, bf16 (the bench's launch), weighted
+    by TEV's exit masses: every tree's numerator and the scalar loss against
+    the oracle; the gradient of two sampled trees at sampled columns and at
+    every gathered token."""
+    nt, L, V, B = 32, 16, synth.V_QWEN, 256
+    dr, tr, w = _case(tsd, dev, nt, L, V, B, torch.bfloat16, 4)
+    out = tsd.tsd_exit_loss(dr, tr["token"], tr["depth"], tr["n_nodes"], w, with_grad=True)
+    nums, _ = _oracle(orc, dr, tr, w, 1.0)
+    assert np.allclose(out["loss_tree"].cpu().numpy(), nums, rtol=RTOL, atol=0)
+    N = float((tr["n_nodes"] - 1).sum())
+    assert abs(float(out["loss"]) - nums.sum() / N) <= RTOL * abs(nums.sum() / N)
+    cols = np.random.default_rng(1).integers(0, V, 2000)
+    for t in (3, 30):
+        sub = {k: v[t:t + 1] for k, v in tr.items()}
+        _, grads = _oracle(orc, dr[t:t + 1], sub, w[t:t + 1], 1.0, grad=True)
+        want = grads[0] / N
+        scale = np.abs(want).max()
+        got = out["grad"][t].cpu().numpy().astype(np.float64)
+        toks = tr["token"][t, 1:int(tr["n_nodes"][t])].cpu().numpy()
+        for m in range(L):
+            assert np.allclose(got[m, cols], want[m, cols], rtol=1e-4, atol=1e-6 * scale)
+            assert np.allclose(got[m, toks], want[m, toks], rtol=1e-4, atol=1e-6 * scale)

@@ -105,3 +105,20 @@ def test_forest_limits_and_failed_requests(tsd, dev, orc):
     assert int(out["n_nodes"][2]) == 0 and int(out["total"]) == 3 * B
     with pytest.raises(tsd.TsdError):
         tsd.tsd_build_forest(torch.zeros(64, 1, 4, 512, device=dev), topk=4, B=200, M_max=10, l0=1.0, c1=0.1)
+
+
+def test_forest_in_the_bench_launch(tsd, dev, orc):
+    """The bench's launch: 32 requests, V=151936, L=16, top-k 8, cap B=256
+    (8192 candidates), l(M) = 1 + M/2048: the oracle builds every request's
+    tree and selects; M* and every width must agree."""
+    R, L, k, B, l0, c1 = 32, 16, 8, 256, 1.0, 1.0 / 2048
+    seeds = [synth.seed_for(2, t) for t in range(R)]
+    dr = synth.zipf_drafter(R, L, synth.V_QWEN, 0, device=dev, seeds=seeds)
+    out = tsd.tsd_build_forest(dr, topk=k, B=B, M_max=R * B, l0=l0, c1=c1)
+    sel, trees, lists, scores, depth, n = _oracle_forest(orc, dr[:, 0], k, B, R * B, l0, c1)
+    M = int(out["total"])
+    assert out["status"].cpu().tolist() == [0] * R
+    if M != sel["M"]:
+        assert abs(M - sel["M"]) == 1 and _margin(scores, depth, n, min(M, sel["M"]), l0, c1) < 1e-6
+        return
+    assert (out["n_nodes"] - 1).cpu().numpy().tolist() == sel["width"].tolist()

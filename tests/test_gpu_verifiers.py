@@ -179,3 +179,41 @@ def test_proposal_rejects_non_positive_q(tsd, dev, orc):
     out = tsd.tsd_verify_proposal(full, par, tok, nn, q, 1.0, seed=1)
     assert _np(out["status"]).tolist() == [0, 5, 4]
     assert int(out["exit_node"][1]) == -1
+
+
+def test_verifiers_in_the_bench_launch(tsd, dev, orc):
+    """32 trees, V=151936, B=256, T=0.6, bf16 (the bench's verification
+    launch): four sampled trees against the oracle for both walk rules."""
+    nt, B, T = 32, 256, 0.6
+    seeds = [synth.seed_for(2, t) for t in range(nt)]
+    dr = synth.zipf_drafter(nt, 16, synth.V_QWEN, 0, device=dev, seeds=seeds)
+    tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+    tgt = torch.zeros(nt, B + 1, synth.V_QWEN, dtype=torch.bfloat16, device=dev)
+    for t in range(nt):
+        n = int(tr["n_nodes"][t])
+        synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=tgt[t, :n])
+    sample = (0, 11, 20, 31)
+    q = np.ones((nt, B + 1))
+    for t in sample:
+        q[t] = _q_child(dr, tr, t, int(tr["n_nodes"][t]), B)
+    qd = torch.tensor(q, dtype=torch.float32, device=dev)
+    flips = 0
+    for seed in (5, 6):
+        s_out = tsd.tsd_verify_seqres(tgt, tr["parent"], tr["token"], tr["n_nodes"], T, seed=seed)
+        p_out = tsd.tsd_verify_proposal(tgt, tr["parent"], tr["token"], tr["n_nodes"], qd, T,
+                                        seed=seed)
+        assert _np(s_out["status"]).tolist() == [0] * nt
+        assert _np(p_out["status"]).tolist() == [0] * nt
+        for t in sample:
+            n = int(tr["n_nodes"][t])
+            par, tok = _np(tr["parent"][t]), _np(tr["token"][t])
+            z64 = tgt[t, :n].float().cpu().numpy().astype(np.float64)
+            o = orc.seqres(z64, par, tok, n, T, seed=seed, tree=t)
+            got = (int(s_out["exit_node"][t]), int(s_out["bonus_token"][t]), int(s_out["accept_len"][t]))
+            if got != (o["exit_node"], o["bonus"], o["accept_len"]):
+                assert _seqres_margin(orc, z64, par, tok, n, T, seed, t) < 1e-6, (t, got, o)
+                flips += 1
+            o = orc.proposal(z64, par, tok, n, T, q[t], seed=seed, tree=t)
+            got = (int(p_out["exit_node"][t]), int(p_out["bonus_token"][t]), int(p_out["accept_len"][t]))
+            flips += got != (o["exit_node"], o["bonus"], o["accept_len"])
+    assert flips <= 1, flips
