@@ -561,6 +561,12 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
             lat.append(a.elapsed_time(b))
     out["b64_single_tree"]["round_graph_ms"] = statistics.median(lat)
     out["b64_single_tree"]["round_graph_ms_best"] = min(lat)
+    # the oracle beside it: the same round, float64, one host thread
+    z1 = dr[0, 0].float().cpu().numpy()
+    tg1 = copies[0][0, :n].float().cpu().numpy()
+    out["b64_single_tree"].update(
+        oracle_round_ms=oracle_ms(lambda orc: oracle_round(orc, z1, tg1, 8, B1, 1.0, 0)),
+        oracle_sample="one round (drafter statistics, heap, mask, TEV at T=1), float64, one thread")
     del copies, graph
     # mixture-of-futures workload: 16 trees, K = 8 modes from two latent
     # futures, B = 128; the mixture builder, then TEV at T = 1 on its trees
@@ -594,7 +600,20 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         "rounds_per_s": nt_m / ((build_ms + tev_ms) * 1e-3),
         "mean_accept_len": float(ov["accept_len"].float().mean()),
         "mean_coverage_plus_1": float(ov["coverage"].mean()) + 1.0,
-        "status_ok": int((ov["status"] == 0).sum())}
+        "status_ok": int((ov["status"] == 0).sum()),
+        "ms_per_tree": (build_ms + tev_ms) / nt_m}
+    # the oracle beside it: tree 0's round (merged-heap build over K = 8 modes, TEV)
+    zm0 = mix[0].float().cpu().numpy()
+    n0 = int(tm["n_nodes"][0])
+    tg0 = tgt_m[0, :n0].float().cpu().numpy()
+
+    def mix_round(orc):
+        ref = orc.build_tree(orc.drafter_lists(zm0, 1.0, 8), B_m)
+        orc.tev(tg0[:ref["n_nodes"]], ref["parent"], ref["token"], ref["n_nodes"], 1.0, seed=0)
+
+    out["mixture_k8_b128_x16"].update(
+        oracle_ms_per_tree=oracle_ms(mix_round),
+        oracle_sample="tree 0 of the 16 (K=8, B=128): build and TEV, float64, one host thread")
     # the same workload under the log-sum-exp score ([MFD] Eq. 6): build time,
     # and TEV at T = 1 on its trees against targets built the same way
     ws_l = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_BUILD_LSE, nt_m, K_m, 16, V, 8, B_m,
