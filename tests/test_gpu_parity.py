@@ -582,3 +582,38 @@ def test_logits_in_pinned_host_memory(tsd, dev, orc):
         p_d = tsd.tsd_verify_ddtree(tgt.to(dev), tr_d["parent"], tr_d["token"], tr_d["n_nodes"], T, seed=5)
         for key in p_d:
             assert torch.equal(p_d[key], p_h[key]), (T, key)
+
+
+def test_deep_trees(tsd, dev, orc):
+    """The deepest shapes the limits allow: L = 28 with top-4 (56 bits of rank
+    sequence) in the builder; L = 31 with top-2 in the log-sum-exp tree (two
+    modes) and in the exit loss."""
+    dr = synth.zipf_drafter(2, 28, 5000, synth.seed_for(6), device="cpu")
+    out = tsd.tsd_build_tree(dr.to(dev), topk=4, B=300)
+    for t in range(2):
+        ref, lists = oracle_build(orc, dr[t], 4, 300)
+        assert compare_trees(_tree_np(out, t), ref, lists) <= 1
+        assert int(out["depth"][t].max()) <= 28
+    mix, _, _ = synth.mixture_drafter(1, 2, 31, 3000, synth.seed_for(6, 1), device="cpu")
+    lt = tsd.tsd_build_lse_tree(mix.to(dev), topk=2, B=200)
+    ref = orc.lse_tree(mix[0].double().numpy(), 1.0, 2, 200)
+    assert int(lt["n_cand"][0]) == ref["n_cand"] and int(lt["n_nodes"][0]) == ref["n_nodes"]
+    seq_g = sequences_of(_np(lt["parent"][0]), _np(lt["token"][0]), ref["n_nodes"])
+    seq_o = sequences_of(ref["parent"], ref["token"], ref["n_nodes"])
+    assert len(set(seq_g) ^ set(seq_o)) <= 2  # a near-tie at the cut may swap one prefix
+    z = synth.zipf_drafter(2, 31, 3000, synth.seed_for(6, 2), device="cpu", dtype=torch.float32)
+    tr = tsd.tsd_build_tree(z.to(dev), topk=2, B=120)
+    w = torch.rand(2, 121, generator=torch.Generator().manual_seed(3)).to(dev) * (tr["depth"] >= 0)
+    ex = tsd.tsd_exit_loss(z.to(dev), tr["token"], tr["depth"], tr["n_nodes"], w)
+    for t in range(2):
+        n = int(tr["n_nodes"][t])
+        num = orc.exit_loss(z[t, 0].double().numpy(), 1.0, _np(tr["token"][t]), _np(tr["depth"][t]),
+                            n, w[t].double().cpu().numpy())
+        assert abs(float(ex["loss_tree"][t]) - num) <= 1e-5 * abs(num)
+
+
+def sequences_of(parent, token, n):
+    seqs = [()]
+    for u in range(1, n):
+        seqs.append(seqs[int(parent[u])] + (int(token[u]),))
+    return seqs
