@@ -115,3 +115,46 @@ def test_secondary_operations_replay_from_a_graph(tsd, dev):
     torch.cuda.synchronize()
     assert torch.allclose(eg["loss_tree"], ref["loss_tree"], rtol=1e-12, atol=0)
     assert torch.allclose(eg["grad"], ref["grad"], rtol=1e-5, atol=1e-9)
+
+
+def test_calls_on_concurrent_streams(tsd, dev):
+    """Two independent batches issued on two streams from two host threads at
+    once, each with its own workspace, give what one stream gives."""
+    import threading
+    nt, L, V, B, T = 3, 16, 9000, 48, 1.0
+    jobs = []
+    for j in range(2):
+        dr, tgt, seeds = _inputs(nt, L, V, B, 20 + j, dev)
+        tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+        for t in range(nt):
+            n = int(tr["n_nodes"][t])
+            synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=tgt[t, :n])
+        jobs.append((dr, tgt))
+    torch.cuda.synchronize()
+
+    def run(dr, tgt):
+        tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+        out = tsd.tsd_verify_tev(tgt, tr["parent"], tr["token"], tr["n_nodes"], T, seed=4)
+        return tr, out
+
+    want = [run(*j) for j in jobs]
+    torch.cuda.synchronize()
+    got = [None, None]
+    streams = [torch.cuda.Stream(dev) for _ in range(2)]
+
+    def worker(i):
+        with torch.cuda.stream(streams[i]):
+            for _ in range(5):
+                got[i] = run(*jobs[i])
+
+    ths = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    torch.cuda.synchronize()
+    for i in range(2):
+        for key in ("parent", "token", "n_nodes"):
+            assert torch.equal(got[i][0][key], want[i][0][key]), (i, key)
+        for key in ("exit_node", "bonus_token", "accept_len", "exit_mass"):
+            assert torch.equal(got[i][1][key], want[i][1][key]), (i, key)
