@@ -4,14 +4,18 @@
  *
  * Pages the operations restate:
  *   [EXIT] "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
- *          Decoding": Sec. 3 Eq. 1-2, Sec. 3.1 Eq. 4, Eq. 6-7, App. A.4.1,
- *          App. B Algorithm 1.
+ *          Decoding": Sec. 3 Eq. 1-2, Sec. 3.1 Eq. 4, Eq. 6-7, App. A.4.1
+ *          (predraw-and-follow), App. A.4.2 Eq. 45-53 (sequential residual
+ *          verification), App. B Algorithm 1 (TEV), Sec. 5 Eq. 14 and App. C.2
+ *          Eq. 66-67 (the exit-guided loss).
  *   [CAST] "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters":
  *          Sec. 2 Eq. 1, Thm. 1, App. C ("Candidate construction",
- *          "Packed verification"), App. B Lemma 1.
+ *          "Packed verification"), App. B Lemma 1, Sec. 3.3 Thm. 2 and App.
+ *          B.4 Prop. 2-3 (cost-aware width, shared budget), App. B.1 Thm. 3
+ *          (proposal-aware verification).
  *   [MFD]  "Multi-Future Drafting: Mixture Block Drafters for Tree-Verified
  *          Speculative Decoding": Sec. 3.4 Eq. 2, Prop. 4, Sec. 4.3,
- *          App. B "Merged heap", Prop. 6.
+ *          App. B "Merged heap", Prop. 6, "Max or log-sum-exp" Eq. 6.
  *
  * Conventions shared by every entry point:
  *   - Every array argument is DEVICE memory owned by the caller, contiguous and
@@ -22,7 +26,8 @@
  *     runtime maps for them.  Each call resolves the logits pointer with
  *     cudaPointerGetAttributes; pageable host memory, or a pointer the runtime
  *     does not know, is TSD_ERR_INVALID_ARG.  The library allocates nothing
- *     and keeps no state between calls.
+ *     and keeps no state between calls, apart from a host-side cache of each
+ *     kernel's occupancy per device (thread-safe).
  *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
  *     host before anything is launched and returned at once; nothing is
  *     written in that case.  TSD_ERR_CUDA reports a launch failure.
