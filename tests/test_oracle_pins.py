@@ -101,6 +101,9 @@ def _numpy_philox_block(counter, key):
     ((2**64 - 1, 2**64 - 1, 3, 0), (2**64 - 1, 17)),
 ])
 def test_philox_matches_numpy(orc, counter, key):
+    """The generator's published known-answer vectors are not available to
+    these tests, so the pin is an independent implementation instead:
+    numpy's Philox4x64-10, including a carry through all four counter words."""
     ours = orc.philox4x64_10(counter, key)
     ref = _numpy_philox_block(counter, key)
     assert [int(x) for x in ours] == [int(x) for x in ref]
