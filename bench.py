@@ -906,6 +906,8 @@ def _op_setup(name, tsd, torch, synth, dev):
             return lambda: tsd.tsd_verify_tev(*args, seed=1, workspace=wv)
         if name == "verify_seqres":
             return lambda: tsd.tsd_verify_seqres(*args, seed=1, workspace=wv)
+        if name == "verify_ddtree":
+            return lambda: tsd.tsd_verify_ddtree(*args, seed=1, workspace=wv)
         d = tr["depth"].clamp(min=1).long() - 1
         logq = torch.log_softmax(drafter[:, 0].float(), dim=-1)
         q = torch.stack([logq[t, d[t], tr["token"][t].clamp(min=0).long()].exp()
@@ -923,7 +925,7 @@ def _op_setup(name, tsd, torch, synth, dev):
 
 
 OPS = ("build_lse", "build_mixture", "build_forest", "exit_loss", "exit_loss_grad", "tev_b64",
-       "build_b64", "verify_tev", "verify_seqres", "verify_proposal")
+       "build_b64", "verify_tev", "verify_seqres", "verify_proposal", "verify_ddtree")
 
 
 def run_op(args):

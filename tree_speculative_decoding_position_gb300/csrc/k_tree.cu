@@ -297,7 +297,8 @@ constexpr int kDrawThreads = 256;
 template <typename T>
 __global__ void __launch_bounds__(kDrawThreads)
 predraw_nodes_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
-                     bool greedy, uint64_t seed, const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+                     bool greedy, uint64_t seed, const int32_t* __restrict__ n_nodes, bool vec_ok,
+                     VerifyWs ws) {
     pdl_entry();
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     constexpr int PER = CE / kWarp;  // tokens per lane in one chunk (128 bf16, 64 fp32)
@@ -338,7 +339,79 @@ predraw_nodes_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V
         if (sel < 0) sel = lastc;
         frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
         int r = -1;
-        if (sel >= 0) {
+        if (sel >= 0 && vec_ok) {
+            // the chunk in 16-byte vectors, all loads in flight: vector i of
+            // lane l holds tokens (i*32 + l)*VEC .. +VEC, so (i, lane, element)
+            // is token order
+            constexpr int VEC = Lanes<T>::kVec;
+            const int64_t c0 = (int64_t)sel * CE;
+            const int cn = (int)min((int64_t)CE, V - c0);
+            const float mc = __fmul_rn(cs[sel].m, c);
+            const T* rp = logits + row * V + c0;
+            uint4 buf[kVecPerLane];
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const int e = (i * kWarp + lane) * VEC;
+                buf[i] = e < cn ? ld_stream16(rp + e) : Lanes<T>::neg_inf();
+            }
+            float vs[kVecPerLane], mine = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                float a = 0.0f;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) a += ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mc));
+                vs[i] = a;
+                mine += a;
+            }
+            const float target = frac * warp_sum(mine);
+            float base = 0.0f;
+            int found = -1, last_i = -1, last_l = -1;
+            bool done = false;  // warp-uniform
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                if (done) continue;
+                const float inc = warp_incl_scan(vs[i], lane) + base;
+                const unsigned pos = __ballot_sync(0xffffffffu, vs[i] > 0.0f);
+                if (pos) {
+                    last_i = i;
+                    last_l = 31 - __clz(pos);
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, inc > target && vs[i] > 0.0f);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    if (lane == l) {  // the crossing is inside this lane's vector (re-read)
+                        const uint4 q = ld_stream16(rp + (i * kWarp + lane) * VEC);
+                        float run = inc - vs[i];
+                        int lastp = -1, f = -1;
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const float e = ex2(fmaf(Lanes<T>::get(q, j), c, -mc));
+                            run += e;
+                            if (e > 0.0f) lastp = (i * kWarp + lane) * VEC + j;
+                            if (f < 0 && run > target && e > 0.0f) f = (i * kWarp + lane) * VEC + j;
+                        }
+                        found = f >= 0 ? f : lastp;
+                    }
+                    found = __shfl_sync(0xffffffffu, found, l);
+                    done = true;
+                }
+                base = __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (found < 0 && last_i >= 0) {  // rounding left the target past the total
+#pragma unroll
+                for (int i = 0; i < kVecPerLane; ++i) {
+                    if (i != last_i) continue;
+                    if (lane == last_l) {
+                        const uint4 q = ld_stream16(rp + (i * kWarp + lane) * VEC);
+                        for (int j = 0; j < VEC; ++j)
+                            if (ex2(fmaf(Lanes<T>::get(q, j), c, -mc)) > 0.0f)
+                                found = (i * kWarp + lane) * VEC + j;
+                    }
+                }
+                found = __shfl_sync(0xffffffffu, found, last_l);
+            }
+            r = found >= 0 ? found + (int)c0 : -1;
+        } else if (sel >= 0) {
             const int64_t c0 = (int64_t)sel * CE;
             const int cn = (int)min((int64_t)CE, V - c0);
             const float mc = __fmul_rn(cs[sel].m, c);
@@ -387,14 +460,14 @@ __global__ void predraw_walk_kernel(int n_trees, int B, const int32_t* __restric
                                     int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
                                     int32_t* __restrict__ draws, int32_t* __restrict__ status) {
     pdl_entry();
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= n_trees) return;
+    const int t = blockIdx.x;  // one CTA per tree: the block copies the draws, thread 0 walks
     const int stride = B + 1;
     const int n = n_nodes[t];
     const int st = ws.tstat[t];
     if (draws)
-        for (int v = 0; v < stride; ++v)
+        for (int v = threadIdx.x; v < stride; v += blockDim.x)
             draws[(int64_t)t * stride + v] = (st == kStatOk && v < n) ? ws.draws[(int64_t)t * stride + v] : -1;
+    if (threadIdx.x != 0) return;
     if (st != kStatOk) {
         exit_node[t] = -1;
         bonus[t] = -1;
@@ -430,20 +503,21 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
                            cudaStream_t stream) {
     const int es = dtype == TSD_BF16 ? 2 : 4;
     const int nch = (int)n_chunks(V, es);
+    const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((V * es) % 16 == 0);
     const int64_t rows = (int64_t)n_trees * (B + 1);
     const int wpb = kDrawThreads / kWarp;
     const int64_t want = (rows + wpb - 1) / wpb;
     const int grid = (int)(want < 65535 * 8 ? want : 65535 * 8);
     if (dtype == TSD_BF16) {
         if (cudaError_t e_ = launch_pdl(predraw_nodes_kernel<__nv_bfloat16>, grid, kDrawThreads, 0, stream, 
-            static_cast<const __nv_bfloat16*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws); e_ != cudaSuccess) return e_;
+            static_cast<const __nv_bfloat16*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, vec_ok, ws); e_ != cudaSuccess) return e_;
     } else {
         if (cudaError_t e_ = launch_pdl(predraw_nodes_kernel<float>, grid, kDrawThreads, 0, stream, 
-            static_cast<const float*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, ws); e_ != cudaSuccess) return e_;
+            static_cast<const float*>(logits), n_trees, B, V, nch, c, greedy, seed, n_nodes, vec_ok, ws); e_ != cudaSuccess) return e_;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (cudaError_t e_ = launch_pdl(predraw_walk_kernel, (n_trees + 127) / 128, 128, 0, stream, n_trees, B, n_nodes, ws, exit_node,
+    if (cudaError_t e_ = launch_pdl(predraw_walk_kernel, (unsigned)n_trees, 128, 0, stream, n_trees, B, n_nodes, ws, exit_node,
                                                                  bonus, accept_len, draws, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
