@@ -561,38 +561,92 @@ __device__ __forceinline__ bool tree_failed(int t, int st, int32_t* exit_node, i
 // when u_j (1 - M_{j-1}) < p_j (Eq. 49, uniform stream 3, sub j-1), where p_j
 // = p_v(x_j) and M_{j-1} sums the earlier p's.  With every child rejected the
 // walk exits and the bonus is drawn from the Eq. 53 residual (stream 4).
+// The walk verifiers' view of one tree, staged in shared memory by the whole
+// block so that the single walking thread never waits on global memory: CSR
+// child offsets and nodes, every node's edge probability, and for every CSR
+// edge q = cptr[v] + j the uniforms of the walk at node v, step j (streams
+// given by the caller; one uniform per edge and stream).
+struct WalkTree {
+    int* cptr;    // [n + 1]
+    int* cnode;   // [n - 1]
+    float* pedge; // [n]
+    float* u0;    // [n - 1] stream s0 at (v, j)
+    float* u1;    // [n - 1] stream s1 at (v, j), when s1 >= 0
+};
+
+// 4-byte words of the staging: child offsets, child nodes, edge
+// probabilities and one uniform stream; a second stream adds B + 1.
+static size_t walk_smem_words(int B) { return (size_t)(B + 2) + 3 * (size_t)(B + 1); }
+
+__device__ void stage_walk_tree(const VerifyWs& ws, int t, int n, int B, uint64_t seed, int s0,
+                                int s1, float* sm, WalkTree& wt) {
+    wt.cptr = reinterpret_cast<int*>(sm);
+    wt.cnode = wt.cptr + (B + 2);
+    wt.pedge = reinterpret_cast<float*>(wt.cnode + (B + 1));
+    wt.u0 = wt.pedge + (B + 1);
+    wt.u1 = wt.u0 + (B + 1);
+    const int m = n - 1;
+    for (int i = threadIdx.x; i <= n; i += blockDim.x) wt.cptr[i] = ws.child_ptr[(int64_t)t * (B + 2) + i];
+    for (int i = threadIdx.x; i < m; i += blockDim.x) wt.cnode[i] = ws.child_node[(int64_t)t * (B + 1) + i];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) wt.pedge[i] = ws.pedge[(int64_t)t * (B + 1) + i];
+    __syncthreads();
+    for (int q = threadIdx.x; q < m; q += blockDim.x) {
+        int lo = 0, hi = n;  // the node v with cptr[v] <= q < cptr[v+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (wt.cptr[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        wt.u0[q] = uniform24(seed, t, lo, s0, q - wt.cptr[lo]);
+        if (s1 >= 0) wt.u1[q] = uniform24(seed, t, lo, s1, q - wt.cptr[lo]);
+    }
+    __syncthreads();
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kTreeThreads)
 seqres_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, bool greedy,
-                   uint64_t seed, VerifyWs ws, int32_t* __restrict__ exit_node,
-                   int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
-                   int32_t* __restrict__ status) {
+                   uint64_t seed, const int32_t* __restrict__ n_nodes, VerifyWs ws,
+                   int32_t* __restrict__ exit_node, int32_t* __restrict__ bonus,
+                   int32_t* __restrict__ accept_len, int32_t* __restrict__ status) {
     pdl_entry();
+    extern __shared__ float shw[];
     __shared__ float red[33];
     __shared__ int pick[2];
     __shared__ int exit_v;
     const int t = blockIdx.x;
     if (tree_failed(t, ws.tstat[t], exit_node, bonus, accept_len, status)) return;
-    if (threadIdx.x == 0) {
-        const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-        const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
-        const float* pedge = ws.pedge + (int64_t)t * (B + 1);
+    WalkTree wt;
+    stage_walk_tree(ws, t, n_nodes[t], B, seed, 3, -1, shw, wt);
+    // Warp 0 walks: lane l tests the children j = l, l + 32, ... of the
+    // current node against their rejected mass M_j (an exclusive warp scan),
+    // and the first child that passes is followed.
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int* cptr = wt.cptr;
+        const int* cnode = wt.cnode;
         int v = 0;
         for (;;) {
+            const int b0 = cptr[v], k = cptr[v + 1] - b0;
             float M = 0.0f;
             int next = -1;
-            for (int q = cptr[v]; q < cptr[v + 1]; ++q) {
-                const float pj = pedge[cnode[q]];
-                if (uniform24(seed, t, v, 3, q - cptr[v]) * (1.0f - M) < pj) {
-                    next = cnode[q];
+            for (int j0 = 0; j0 < k; j0 += 32) {
+                const int q = b0 + j0 + lane;
+                const float pj = j0 + lane < k ? wt.pedge[cnode[q]] : 0.0f;
+                const float incl = warp_incl_scan(pj, lane);
+                const float Mj = M + (incl - pj);
+                const unsigned hit =
+                    __ballot_sync(0xffffffffu, j0 + lane < k && wt.u0[q] * (1.0f - Mj) < pj);
+                if (hit) {
+                    next = cnode[b0 + j0 + __ffs(hit) - 1];
                     break;
                 }
-                M += pj;
+                M += __shfl_sync(0xffffffffu, incl, 31);
             }
             if (next < 0) break;
             v = next;
         }
-        exit_v = v;
+        if (lane == 0) exit_v = v;
     }
     __syncthreads();
     const int v = exit_v;
@@ -613,78 +667,110 @@ seqres_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, floa
 template <typename T>
 __global__ void __launch_bounds__(kTreeThreads)
 proposal_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c,
-                     bool greedy, uint64_t seed, const float* __restrict__ q_child, VerifyWs ws,
+                     bool greedy, uint64_t seed, const float* __restrict__ q_child,
+                     const int32_t* __restrict__ n_nodes, VerifyWs ws,
                      int32_t* __restrict__ exit_node, int32_t* __restrict__ bonus,
                      int32_t* __restrict__ accept_len, int32_t* __restrict__ status) {
     pdl_entry();
-    extern __shared__ float shp[];  // mu_c and q of the current node's children, [2][B]
+    // the staged tree (see stage_walk_tree), then q and rho per node, then the
+    // current node's children's mu and q, [2][B]
+    extern __shared__ float shp[];
     __shared__ float red[33];
     __shared__ int pick[2];
     __shared__ int exit_v, bad;
     const int t = blockIdx.x;
     if (tree_failed(t, ws.tstat[t], exit_node, bonus, accept_len, status)) return;
-    if (threadIdx.x == 0) {
-        const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-        const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
-        const float* pedge = ws.pedge + (int64_t)t * (B + 1);
-        const float* qc = q_child + (int64_t)t * (B + 1);
-        float* mu = shp;
-        float* qv = shp + B;
-        int v = 0;
-        bad = 0;
+    const int n = n_nodes[t];
+    WalkTree wt;
+    stage_walk_tree(ws, t, n, B, seed, 5, 6, shp, wt);
+    float* qn = wt.u1 + (B + 1);      // [n] q_child per node
+    float* rhon = qn + (B + 1);       // [n] rho per node
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        qn[i] = q_child[(int64_t)t * (B + 1) + i];
+        rhon[i] = ws.rho[(int64_t)t * (B + 1) + i];
+    }
+    __syncthreads();
+    // Warp 0 walks; lane l owns the children j = l, l + 32, ... of the current
+    // node, so the sums over the children are shuffles and the inverse-CDF
+    // pick is a warp scan with a ballot.
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int* cptr = wt.cptr;
+        const int* cnode = wt.cnode;
+        float* mu = rhon + (B + 1);
+        float* qv = mu + B;
+        int v = 0, fail = 0;
         for (;;) {
             const int b0 = cptr[v], k = cptr[v + 1] - b0;
-            for (int j = 0; j < k; ++j) {
-                mu[j] = pedge[cnode[b0 + j]];
-                qv[j] = qc[cnode[b0 + j]];
-                if (!(qv[j] > 0.0f) || isinf(qv[j])) bad = 1;
+            for (int j = lane; j < k; j += 32) {
+                const int u = cnode[b0 + j];
+                mu[j] = wt.pedge[u];
+                qv[j] = qn[u];
+                if (!(qv[j] > 0.0f) || isinf(qv[j])) fail = 1;
             }
-            if (bad) break;
-            const float rho = ws.rho[(int64_t)t * (B + 1) + v];
+            if (__any_sync(0xffffffffu, fail)) {
+                fail = 1;
+                break;
+            }
+            __syncwarp();
+            const float rho = rhon[v];
             float s = 1.0f;  // scale of the non-child tokens
             int next = -1;
             for (int step = 0; step < k; ++step) {
                 float Q = 0.0f;
-                for (int j = 0; j < k; ++j)
+                for (int j = lane; j < k; j += 32)
                     if (qv[j] > 0.0f) Q += qv[j];
-                const float thr = uniform24(seed, t, v, 5, step) * Q;
-                float cum = 0.0f;
+                Q = warp_sum(Q);
+                const float thr = wt.u0[b0 + step] * Q;
+                // first live child whose running proposal mass passes thr,
+                // else the last live child
+                float carry = 0.0f;
                 int cand = -1, lastj = -1;
-                for (int j = 0; j < k; ++j) {
-                    if (!(qv[j] > 0.0f)) continue;  // retired
-                    lastj = j;
-                    cum += qv[j];
-                    if (cum > thr) {
-                        cand = j;
-                        break;
-                    }
+                for (int j0 = 0; j0 < k && cand < 0; j0 += 32) {
+                    const int j = j0 + lane;
+                    const bool live = j < k && qv[j] > 0.0f;
+                    const float run = carry + warp_incl_scan(live ? qv[j] : 0.0f, lane);
+                    const unsigned hit = __ballot_sync(0xffffffffu, live && run > thr);
+                    const unsigned alive = __ballot_sync(0xffffffffu, live);
+                    if (hit) cand = j0 + __ffs(hit) - 1;
+                    else if (alive) lastj = j0 + 31 - __clz(alive);
+                    carry = __shfl_sync(0xffffffffu, run, 31);
                 }
                 if (cand < 0) cand = lastj;
                 const float qt = qv[cand] / Q;
-                if (uniform24(seed, t, v, 6, step) * qt < mu[cand]) {
+                if (wt.u1[b0 + step] * qt < mu[cand]) {
                     next = cnode[b0 + cand];
                     break;
                 }
-                float z = s * rho;  // (mu - q~)_+ and its total
-                for (int j = 0; j < k; ++j) {
+                float z = 0.0f;  // (mu - q~)_+ and its total
+                for (int j = lane; j < k; j += 32) {
                     if (!(qv[j] > 0.0f)) continue;
                     mu[j] = fmaxf(mu[j] - qv[j] / Q, 0.0f);
                     z += mu[j];
                 }
+                z = s * rho + warp_sum(z);
                 if (!(z > 0.0f)) {
-                    bad = 1;
+                    fail = 1;
                     break;
                 }
                 const float inv = 1.0f / z;
                 s *= inv;
-                for (int j = 0; j < k; ++j) mu[j] *= inv;
-                mu[cand] = 0.0f;
-                qv[cand] = -1.0f;  // retired
+                for (int j = lane; j < k; j += 32) mu[j] *= inv;
+                __syncwarp();
+                if (lane == (cand & 31)) {
+                    mu[cand] = 0.0f;
+                    qv[cand] = -1.0f;  // retired
+                }
+                __syncwarp();
             }
-            if (bad || next < 0) break;
+            __syncwarp();
+            if (fail || next < 0) break;
             v = next;
         }
-        exit_v = v;
+        if (lane == 0) {
+            exit_v = v;
+            bad = fail;
+        }
     }
     __syncthreads();
     if (bad) {
@@ -697,25 +783,34 @@ proposal_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, fl
 }
 
 cudaError_t launch_seqres_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
-                               float c, bool greedy, uint64_t seed, const VerifyWs& ws,
-                               int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
-                               int32_t* status, cudaStream_t stream) {
+                               float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
+                               const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                               int32_t* accept_len, int32_t* status, cudaStream_t stream) {
     const int nch = (int)n_chunks(V, dtype == TSD_BF16 ? 2 : 4);
+    const size_t smem = sizeof(float) * walk_smem_words(B);
+    cudaError_t e = cudaFuncSetAttribute(dtype == TSD_BF16
+                                             ? (const void*)seqres_tree_kernel<__nv_bfloat16>
+                                             : (const void*)seqres_tree_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     if (dtype == TSD_BF16)
-        return launch_pdl(seqres_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kTreeThreads, 0,
+        return launch_pdl(seqres_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kTreeThreads, smem,
                           stream, static_cast<const __nv_bfloat16*>(logits), B, V, nch, c, greedy,
-                          seed, ws, exit_node, bonus, accept_len, status);
-    return launch_pdl(seqres_tree_kernel<float>, (unsigned)n_trees, kTreeThreads, 0, stream,
-                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, ws, exit_node,
-                      bonus, accept_len, status);
+                          seed, n_nodes, ws, exit_node, bonus, accept_len, status);
+    return launch_pdl(seqres_tree_kernel<float>, (unsigned)n_trees, kTreeThreads, smem, stream,
+                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, n_nodes, ws,
+                      exit_node, bonus, accept_len, status);
 }
-
 cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
                                  float c, bool greedy, uint64_t seed, const float* q_child,
-                                 const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
-                                 int32_t* accept_len, int32_t* status, cudaStream_t stream) {
+                                 const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                                 int32_t* bonus, int32_t* accept_len, int32_t* status,
+                                 cudaStream_t stream) {
     const int nch = (int)n_chunks(V, dtype == TSD_BF16 ? 2 : 4);
-    const size_t smem = 2 * sizeof(float) * (size_t)(B > 0 ? B : 1);
+    // staging with two uniform streams, q and rho per node, then mu and q of
+    // the current node's children
+    const size_t smem =
+        sizeof(float) * (walk_smem_words(B) + 3 * (size_t)(B + 1) + 2 * (size_t)(B > 0 ? B : 1));
     cudaError_t e = cudaFuncSetAttribute(dtype == TSD_BF16
                                              ? (const void*)proposal_tree_kernel<__nv_bfloat16>
                                              : (const void*)proposal_tree_kernel<float>,
@@ -724,10 +819,10 @@ cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_tree
     if (dtype == TSD_BF16)
         return launch_pdl(proposal_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kTreeThreads,
                           smem, stream, static_cast<const __nv_bfloat16*>(logits), B, V, nch, c,
-                          greedy, seed, q_child, ws, exit_node, bonus, accept_len, status);
+                          greedy, seed, q_child, n_nodes, ws, exit_node, bonus, accept_len, status);
     return launch_pdl(proposal_tree_kernel<float>, (unsigned)n_trees, kTreeThreads, smem, stream,
-                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, q_child, ws,
-                      exit_node, bonus, accept_len, status);
+                      static_cast<const float*>(logits), B, V, nch, c, greedy, seed, q_child,
+                      n_nodes, ws, exit_node, bonus, accept_len, status);
 }
 
 }  // namespace tsd

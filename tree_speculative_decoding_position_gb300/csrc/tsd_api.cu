@@ -485,8 +485,8 @@ tsd_status tsd_verify_seqres(const void* target_logits, tsd_dtype dtype, const i
                                        temperature, exit_node, bonus_token, accept_len, status,
                                        workspace, ws_bytes, stream, &ws, &c, &greedy);
     if (st != TSD_OK) return st;
-    if (launch_seqres_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, ws, exit_node,
-                           bonus_token, accept_len, status, stream) != cudaSuccess)
+    if (launch_seqres_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, n_nodes, ws,
+                           exit_node, bonus_token, accept_len, status, stream) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
 }
@@ -505,8 +505,9 @@ tsd_status tsd_verify_proposal(const void* target_logits, tsd_dtype dtype, const
                                        temperature, exit_node, bonus_token, accept_len, status,
                                        workspace, ws_bytes, stream, &ws, &c, &greedy);
     if (st != TSD_OK) return st;
-    if (launch_proposal_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, q_child, ws,
-                             exit_node, bonus_token, accept_len, status, stream) != cudaSuccess)
+    if (launch_proposal_tree(target_logits, dtype, n_trees, B, V, c, greedy, seed, q_child,
+                             n_nodes, ws, exit_node, bonus_token, accept_len, status,
+                             stream) != cudaSuccess)
         return TSD_ERR_CUDA;
     return TSD_OK;
 }

@@ -314,13 +314,14 @@ cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t ro
                                  int topk, float c, double temp, const BuildWs& ws,
                                  cudaStream_t stream);
 cudaError_t launch_seqres_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
-                               float c, bool greedy, uint64_t seed, const VerifyWs& ws,
-                               int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
-                               int32_t* status, cudaStream_t stream);
+                               float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
+                               const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
+                               int32_t* accept_len, int32_t* status, cudaStream_t stream);
 cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
                                  float c, bool greedy, uint64_t seed, const float* q_child,
-                                 const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
-                                 int32_t* accept_len, int32_t* status, cudaStream_t stream);
+                                 const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                                 int32_t* bonus, int32_t* accept_len, int32_t* status,
+                                 cudaStream_t stream);
 // Shared-budget selection over the trees of a launch (CAST App. B.4): each
 // tree's candidates get their rank in the global merge and the batched
 // stopping rule is tested there; every tree keeps its candidates ranked below
