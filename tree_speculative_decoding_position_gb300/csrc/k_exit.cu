@@ -22,10 +22,13 @@ namespace tsd {
 
 constexpr int kExitThreads = 256;
 
-// LSE of one row of z / T_d, ln 2 * (mc + log2 S), from its chunk statistics
-// as the builder's row kernel forms it, by one warp; NaN when a chunk saw a
-// NaN or +inf or the row has no mass.
-__device__ double row_lse(const ChunkStat* __restrict__ cs, int nch, float c, int lane) {
+// Statistics of one row of z / T_d from its chunk statistics as the
+// builder's row kernel forms them, by one warp: the scaled maximum mc and the
+// float64 sum S = sum over chunks of s 2^(m c - mc), so that
+// LSE = ln 2 * (mc + log2 S).  *bad when a chunk saw a NaN or +inf or the row
+// has no mass.
+__device__ void row_stats(const ChunkStat* __restrict__ cs, int nch, float c, int lane, float* mc_out,
+                          double* s_out, bool* bad_out) {
     float m = -INFINITY;
     bool bad = false;
     for (int q = lane; q < nch; q += kWarp) {
@@ -38,25 +41,34 @@ __device__ double row_lse(const ChunkStat* __restrict__ cs, int nch, float c, in
     for (int q = lane; q < nch; q += kWarp)
         if (cs[q].m != -INFINITY) s += (double)cs[q].s * (double)ex2(__fmul_rn(cs[q].m, c) - mc);
     s = warp_sum_d(s);
-    bad = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0);
-    return bad ? __longlong_as_double(0x7ff8000000000000ll)
-               : 0.6931471805599453 * ((double)mc + log2(s));
+    *mc_out = mc;
+    *s_out = s;
+    *bad_out = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0);
 }
 
-// One CTA per tree: the LSE of its L rows (one warp per row), then the
-// tree's numerator and the per-row weights W_m.  The last CTA to finish
-// (a completion counter; no CTA waits for another) forms the scalar loss
-// from the valid trees' numerators and (n_nodes - 1).
+// One CTA per tree.  The float64 pipe is narrow, so each float64 step is
+// taken once where it can be: one warp per row forms (mc, S); one warp then
+// takes the logarithm of every row at once (row m on lane m, L <= 32); the
+// nodes' terms follow, and the per-row weights W_m are summed by one warp per
+// row over the staged (depth, weight) pairs in node order (deterministic, no
+// atomics).  The last CTA to finish (a completion counter; no CTA waits for
+// another) forms the scalar loss from the valid trees' numerators and
+// (n_nodes - 1).
 template <typename T>
 __global__ void __launch_bounds__(kExitThreads)
 exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, int nch, float c,
-                 double temp, const int32_t* __restrict__ token, const int32_t* __restrict__ depth,
-                 const int32_t* __restrict__ n_nodes, int B, const float* __restrict__ omega,
-                 double* __restrict__ loss_tree, double* __restrict__ loss,
-                 int32_t* __restrict__ status, ExitWs ws) {
+                 double inv_temp, const int32_t* __restrict__ token,
+                 const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes, int B,
+                 const float* __restrict__ omega, double* __restrict__ loss_tree,
+                 double* __restrict__ loss, int32_t* __restrict__ status, ExitWs ws) {
     pdl_entry();
     __shared__ double W[TSD_MAX_L];
     __shared__ double lse[TSD_MAX_L];
+    __shared__ double srow[TSD_MAX_L];
+    __shared__ float mcrow[TSD_MAX_L];
+    __shared__ int badrow[TSD_MAX_L];
+    __shared__ int8_t sdep[TSD_MAX_B + 1];   // depth of node v (0 where it scores nothing)
+    __shared__ float sw[TSD_MAX_B + 1];      // its weight
     __shared__ double red[kExitThreads / kWarp], red2[kExitThreads / kWarp];
     __shared__ int bad, last;
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), wid = tid / kWarp;
@@ -64,39 +76,57 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
     const int stride = B + 1;
     const int n = n_nodes[t];
     if (tid == 0) bad = (n < 1 || n > stride) ? kStatBadTree : kStatOk;
-    for (int m = tid; m < L; m += blockDim.x) W[m] = 0.0;
     for (int m = wid; m < L; m += nw) {
-        const int64_t row = (int64_t)t * L + m;
-        const double l = row_lse(ws.rows.chunk + row * nch, nch, c, lane);
+        float mc;
+        double s;
+        bool b;
+        row_stats(ws.rows.chunk + ((int64_t)t * L + m) * nch, nch, c, lane, &mc, &s, &b);
         if (lane == 0) {
-            lse[m] = l;
-            ws.lse[row] = l;
+            mcrow[m] = mc;
+            srow[m] = s;
+            badrow[m] = b;
         }
     }
     __syncthreads();
-    const double inv_temp = 1.0 / temp;  // z / T_d as one multiply per node
+    if (wid == 0 && lane < L) {
+        const double l = badrow[lane] ? __longlong_as_double(0x7ff8000000000000ll)
+                                      : 0.6931471805599453 * ((double)mcrow[lane] + log2(srow[lane]));
+        lse[lane] = l;
+        ws.lse[(int64_t)t * L + lane] = l;
+    }
+    __syncthreads();
     double part = 0.0;
-    if (bad == kStatOk) {
-        for (int v = 1 + tid; v < n; v += blockDim.x) {
-            const int d = depth[(int64_t)t * stride + v];
-            const int x = token[(int64_t)t * stride + v];
-            if (d < 1 || d > L || x < 0 || (int64_t)x >= V) {
-                atomicExch(&bad, kStatBadTree);
-                continue;
-            }
-            const double w = (double)omega[(int64_t)t * stride + v];
-            const int64_t row = (int64_t)t * L + d - 1;
-            const double z = (double)load_logit(logits + row * V + x);
-            const double term = w * (lse[d - 1] - z * inv_temp);  // w(v) * -log q_{depth(v)}(x_v)
-            if (!(term == term) || isinf(term)) atomicCAS(&bad, kStatOk, kStatNonFinite);
-            part += term;
-            atomicAdd(&W[d - 1], w);
+    const int nv = bad == kStatOk ? n : 1;
+    for (int v = 1 + tid; v < nv; v += blockDim.x) {
+        const int d = depth[(int64_t)t * stride + v];
+        const int x = token[(int64_t)t * stride + v];
+        sdep[v] = 0;
+        if (d < 1 || d > L || x < 0 || (int64_t)x >= V) {
+            atomicExch(&bad, kStatBadTree);
+            continue;
         }
+        const float wf = omega[(int64_t)t * stride + v];
+        sdep[v] = (int8_t)d;
+        sw[v] = wf;
+        const double w = (double)wf;
+        const int64_t row = (int64_t)t * L + d - 1;
+        const double z = (double)load_logit(logits + row * V + x);
+        const double term = w * (lse[d - 1] - z * inv_temp);  // w(v) * -log q_{depth(v)}(x_v)
+        if (!(term == term) || isinf(term)) atomicCAS(&bad, kStatOk, kStatNonFinite);
+        part += term;
     }
     part = warp_sum_d(part);
     if (lane == 0) red[wid] = part;
     __syncthreads();
     const int st = bad;
+    for (int m = wid; m < L; m += nw) {
+        double a = 0.0;
+        if (st == kStatOk)
+            for (int v = 1 + lane; v < nv; v += kWarp)
+                if (sdep[v] == m + 1) a += (double)sw[v];
+        a = warp_sum_d(a);
+        if (lane == 0) ws.wrow[(int64_t)t * L + m] = a;
+    }
     if (tid == 0) {
         double num = 0.0;
         for (int i = 0; i < nw; ++i) num += red[i];
@@ -104,7 +134,6 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
         status[t] = st;
         ws.tstat[t] = st;
     }
-    for (int m = tid; m < L; m += blockDim.x) ws.wrow[(int64_t)t * L + m] = st == kStatOk ? W[m] : 0.0;
     // completion: the last CTA reads every tree's results
     __threadfence();
     __syncthreads();
@@ -228,14 +257,15 @@ cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, i
     if (cudaError_t e = launch_drafter_chunks(logits, dtype, rows, V, c, ws.rows, stream);
         e != cudaSuccess)
         return e;
+    const double inv_temp = 1.0 / temp;  // z / T_d as one multiply per node
     cudaError_t e;
     if (dtype == TSD_BF16)
         e = launch_pdl(exit_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kExitThreads, 0, stream,
-                       static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, temp,
+                       static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, inv_temp,
                        token, depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     else
         e = launch_pdl(exit_tree_kernel<float>, (unsigned)n_trees, kExitThreads, 0, stream,
-                       static_cast<const float*>(logits), n_trees, L, V, nch, c, temp, token,
+                       static_cast<const float*>(logits), n_trees, L, V, nch, c, inv_temp, token,
                        depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     if (e != cudaSuccess) return e;
     if (grad) {
