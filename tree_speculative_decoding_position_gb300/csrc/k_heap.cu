@@ -42,7 +42,9 @@
 
 namespace tsd {
 
-constexpr int kBuildThreads = 256;
+constexpr int kBuildThreads = 512;
+// successor slots per thread in child generation (the plan keeps M * k <= 512)
+constexpr int kSlotsPerThread = (512 + kBuildThreads - 1) / kBuildThreads;
 
 struct __align__(16) FEntry {
     unsigned long long key;   // order-preserving image of the score
@@ -93,8 +95,8 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.M = (n_modes > 1 ? 256 : 512) / topk;
     if (p.M < 8) p.M = 8;
     if (p.M > 128) p.M = 128;
-    // M * topk <= 512 (TSD_MAX_TOPK = 32): child generation gives each of the
-    // 256 threads at most two slots
+    // M * topk <= 512 (TSD_MAX_TOPK = 32): child generation gives each
+    // thread at most kSlotsPerThread slots
     p.xcap = n_modes * (B + 1) + p.M;
     p.fcap = n_modes * (B + 1) + topk * p.M + n_modes * topk + 32;
     p.hcap = pow2_at_least(p.xcap + p.xcap / 2);  // load factor at most 2/3
@@ -390,7 +392,7 @@ __device__ int hash_bucket(unsigned long long h, unsigned long long* hkey, int h
     return -1;
 }
 
-__global__ void __launch_bounds__(kBuildThreads)
+__global__ void __launch_bounds__(kBuildThreads, 1)
 build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bits,
                   int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, float* __restrict__ score,
@@ -495,13 +497,15 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const FEntry thr = s_thr;
             const bool thr_on = s_thr_on != 0;
             const int nslot = bn * k;
-            // at most 2 slots per thread (the plan keeps M * k <= 512), kept in
-            // slot order: thread tid owns slots 2 tid and 2 tid + 1
-            FEntry ch[2];
-            int okc[2] = {0, 0};
+            // kSlotsPerThread slots per thread, kept in slot order: thread
+            // tid owns slots kSlotsPerThread * tid + u
+            FEntry ch[kSlotsPerThread];
+            int okc[kSlotsPerThread];
+            int nok = 0;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int c = 2 * tid + u;
+            for (int u = 0; u < kSlotsPerThread; ++u) {
+                okc[u] = 0;
+                const int c = kSlotsPerThread * tid + u;
                 if (c < nslot) {
                     const int i = c / k, r = c - i * k;
                     const FEntry e = F[fc][i];
@@ -520,10 +524,13 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                     }
                 }
             }
+#pragma unroll
+            for (int u = 0; u < kSlotsPerThread; ++u) nok += okc[u];
             int written;
-            int pos = block_incl_scan_int(okc[0] + okc[1], red, &written) - (okc[0] + okc[1]);
-            if (okc[0]) S[pos++] = ch[0];
-            if (okc[1]) S[pos] = ch[1];
+            int pos = block_incl_scan_int(nok, red, &written) - nok;
+#pragma unroll
+            for (int u = 0; u < kSlotsPerThread; ++u)
+                if (okc[u]) S[pos++] = ch[u];
             if (tid == 0) s_nS = written;
             __syncthreads();
             const int nS = s_nS;
