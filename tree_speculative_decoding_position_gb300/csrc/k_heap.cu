@@ -104,7 +104,8 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.lists = r16((size_t)n_modes * L * topk * (sizeof(double) + sizeof(int32_t)) +
                   sizeof(double) * (size_t)n_modes * (L + 1));
     const size_t n2s = (size_t)pow2_at_least(topk * p.M < 32 ? 32 : topk * p.M);
-    p.scode_bytes = r16(sizeof(unsigned long long) * n2s);  // successor order codes
+    // successor order codes and the sort's second buffer
+    p.scode_bytes = r16(2 * sizeof(unsigned long long) * n2s);
     p.sbytes = r16(sizeof(FEntry) * n2s) + p.scode_bytes;
     p.hbytes = r16((size_t)p.hcap * (sizeof(unsigned long long) + sizeof(int32_t)));
     p.flag_bytes = r16(sizeof(int32_t) * 2 * (size_t)p.xcap + 64);
@@ -241,63 +242,69 @@ __device__ int warp_first_false(int lo, int hi, P pred) {
     return lo + __popc(__ballot_sync(0xffffffffu, tr));
 }
 
-// Bitonic sort of 64-bit codes c[0, n2) ascending (n2 a power of two, at
-// least 32); sub-32 distances in registers, the rest through memory.
-__device__ void sort_codes(unsigned long long* c, int n2) {
+// Sort of 64-bit codes c[0, n2) ascending (n2 a power of two, at least 32).
+// Each 32-block is sorted in registers by one warp (bitonic, shuffles only);
+// then sorted blocks of width w merge pairwise, w = 32, 64, ..., n2 / 2: an
+// element's place in the merged block is its offset in its own block plus
+// the number of partner-block elements before it (a binary search; left
+// elements precede equal right ones, so equal codes keep distinct places).
+// One barrier per doubling.  The blocks ping-pong between c and tmp; returns
+// the buffer that holds the result.
+__device__ unsigned long long* sort_codes(unsigned long long* c, unsigned long long* tmp, int n2) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nblk = n2 >> 5;
-    auto lane_steps = [&](unsigned long long x, int e, int k, int jtop) {
-        for (int j = jtop; j > 0; j >>= 1) {
-            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
-            const bool lower = (lane & j) == 0;
-            const bool asc = (e & k) == 0;
-            const unsigned long long lo = x < y ? x : y, hi = x < y ? y : x;
-            x = (lower == asc) ? lo : hi;
-        }
-        return x;
-    };
-    for (int b = wid; b < nblk; b += nw) {
+    for (int b = wid; b < (n2 >> 5); b += nw) {
         const int e = (b << 5) + lane;
         unsigned long long x = c[e];
-        for (int k = 2; k <= 32; k <<= 1) x = lane_steps(x, e, k, k >> 1);
+        for (int k = 2; k <= 32; k <<= 1) {
+            const bool asc = (lane & k) == 0;  // every 32-block ends ascending
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+                const bool lower = (lane & j) == 0;
+                const unsigned long long lo = x < y ? x : y, hi = x < y ? y : x;
+                x = (lower == asc) ? lo : hi;
+            }
+        }
         c[e] = x;
     }
     __syncthreads();
-    for (int k = 64; k <= n2; k <<= 1) {
-        for (int j = k >> 1; j >= 32; j >>= 1) {
-            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const unsigned long long x = c[i], y = c[l];
-                    if (((i & k) == 0) == (y < x)) {
-                        c[i] = y;
-                        c[l] = x;
-                    }
-                }
+    unsigned long long *src = c, *dst = tmp;
+    for (int w = 32; w < n2; w <<= 1) {
+        for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+            const unsigned long long x = src[i];
+            const int o = i & (w - 1), blk = i - o;
+            const bool right = (blk & w) != 0;
+            const unsigned long long* pb = src + (blk ^ w);
+            int lo = 0, hi = w;
+            while (lo < hi) {  // partner elements before x
+                const int mid = (lo + hi) >> 1;
+                if (right ? pb[mid] <= x : pb[mid] < x) lo = mid + 1;
+                else hi = mid;
             }
-            __syncthreads();
-        }
-        for (int b = wid; b < nblk; b += nw) {
-            const int e = (b << 5) + lane;
-            c[e] = lane_steps(c[e], e, k, 16);
+            dst[(blk & ~w) + o + lo] = x;
         }
         __syncthreads();
+        unsigned long long* t = src;
+        src = dst;
+        dst = t;
     }
+    return src;
 }
 
-// The total order of a[0, n) (n <= 65536) as codes ord[0, n): bits 63..16
+// The total order of a[0, n) (n <= 65536) as codes in *out[0, n): bits 63..16
 // hold the complement of the top 48 bits of the score image (ascending code =
 // descending score), bits 15..0 the entry's index.  Runs of equal 48-bit
 // prefixes (scores within 2^-36 relative, exact ties among them) are then
 // re-ordered by the full total order, one thread per run.  Returns false,
-// leaving ord unusable, when a run is longer than 32 (the caller then sorts
-// the entries themselves).  ord must hold n2 = pow2 >= max(n, 32) codes.
-__device__ bool sort_order(const FEntry* a, int n, unsigned long long* ord, int n2, int* flag) {
+// leaving the codes unusable, when a run is longer than 32 (the caller then
+// sorts the entries themselves).  buf holds 2 n2 codes, n2 = pow2 >= max(n, 32);
+// *out points into it.
+__device__ bool sort_order(const FEntry* a, int n, unsigned long long* buf, int n2, int* flag,
+                           const unsigned long long** out) {
     for (int i = threadIdx.x; i < n2; i += blockDim.x)
-        ord[i] = i < n ? ((~a[i].key & 0xffffffffffff0000ull) | (unsigned long long)i) : ~0ull;
+        buf[i] = i < n ? ((~a[i].key & 0xffffffffffff0000ull) | (unsigned long long)i) : ~0ull;
     if (threadIdx.x == 0) *flag = 0;
     __syncthreads();
-    sort_codes(ord, n2);
+    unsigned long long* ord = sort_codes(buf, buf + n2, n2);
     for (int p = threadIdx.x; p < n; p += blockDim.x) {
         const unsigned long long hp = ord[p] >> 16;
         if ((p > 0 && (ord[p - 1] >> 16) == hp) || p + 1 >= n || (ord[p + 1] >> 16) != hp) continue;
@@ -320,6 +327,7 @@ __device__ bool sort_order(const FEntry* a, int n, unsigned long long* ord, int 
     __syncthreads();
     const bool ok = *flag == 0;
     __syncthreads();
+    *out = ord;
     return ok;
 }
 
@@ -539,9 +547,8 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             const unsigned long long* Sord = nullptr;
             if (nS > 1) {
                 const int n2S = pow2_at_least(nS < 32 ? 32 : nS);
-                if (sort_order(S, nS, Scode, n2S, &red[31])) {
-                    Sord = Scode;
-                } else {
+                if (!sort_order(S, nS, Scode, n2S, &red[31], &Sord)) {
+                    Sord = nullptr;
                     for (int i = nS + tid; i < n2S; i += blockDim.x) {
                         S[i].key = kSentinelKey;
                         S[i].tb = ~0ull;
