@@ -50,8 +50,11 @@ __device__ void row_stats(const ChunkStat* __restrict__ cs, int nch, float c, in
 // taken once where it can be: one warp per row forms (mc, S); one warp then
 // takes the logarithm of every row at once (row m on lane m, L <= 32); the
 // nodes' terms follow, and the per-row weights W_m are summed by one warp per
-// row over the staged (depth, weight) pairs in node order (deterministic, no
-// atomics).  The last CTA to finish (a completion counter; no CTA waits for
+// row over the nodes' (depth, weight) pairs in node order (deterministic, no
+// atomics), re-read from global memory rather than staged in shared memory:
+// this kernel launches early behind the persistent chunk pass, and a CTA that
+// needs more shared memory than that pass's carveout leaves free waits for
+// its SM to drain.  The last CTA to finish (a completion counter; no CTA waits for
 // another) forms the scalar loss from the valid trees' numerators and
 // (n_nodes - 1).
 template <typename T>
@@ -67,8 +70,6 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
     __shared__ double srow[TSD_MAX_L];
     __shared__ float mcrow[TSD_MAX_L];
     __shared__ int badrow[TSD_MAX_L];
-    __shared__ int8_t sdep[TSD_MAX_B + 1];   // depth of node v (0 where it scores nothing)
-    __shared__ float sw[TSD_MAX_B + 1];      // its weight
     __shared__ double red[kExitThreads / kWarp], red2[kExitThreads / kWarp];
     __shared__ int bad, last;
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), wid = tid / kWarp;
@@ -100,14 +101,11 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
     for (int v = 1 + tid; v < nv; v += blockDim.x) {
         const int d = depth[(int64_t)t * stride + v];
         const int x = token[(int64_t)t * stride + v];
-        sdep[v] = 0;
         if (d < 1 || d > L || x < 0 || (int64_t)x >= V) {
             atomicExch(&bad, kStatBadTree);
             continue;
         }
         const float wf = omega[(int64_t)t * stride + v];
-        sdep[v] = (int8_t)d;
-        sw[v] = wf;
         const double w = (double)wf;
         const int64_t row = (int64_t)t * L + d - 1;
         const double z = (double)load_logit(logits + row * V + x);
@@ -123,7 +121,8 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
         double a = 0.0;
         if (st == kStatOk)
             for (int v = 1 + lane; v < nv; v += kWarp)
-                if (sdep[v] == m + 1) a += (double)sw[v];
+                if (__ldg(depth + (int64_t)t * stride + v) == m + 1)
+                    a += (double)__ldg(omega + (int64_t)t * stride + v);
         a = warp_sum_d(a);
         if (lane == 0) ws.wrow[(int64_t)t * L + m] = a;
     }
