@@ -217,3 +217,87 @@ def test_verifiers_in_the_bench_launch(tsd, dev, orc):
             got = (int(p_out["exit_node"][t]), int(p_out["bonus_token"][t]), int(p_out["accept_len"][t]))
             flips += got != (o["exit_node"], o["bonus"], o["accept_len"])
     assert flips <= 1, flips
+
+
+def _wide_trees(rng, V, B):
+    """Three hand-shaped trees in one B = 4095 launch: a star of 4095 children
+    (the largest budget; more than 32 children per node), a 40-wide root whose
+    three largest-token children hold 50 children each, and a chain into a
+    70-wide node.  Node order is not token order: tokens are drawn at random,
+    distinct among siblings."""
+    trees = []
+    # star
+    toks = rng.permutation(V)[:B]
+    trees.append(([-1] + [0] * B, [-1] + toks.tolist()))
+    # two wide levels
+    par, tok = [-1], [-1]
+    kids = rng.permutation(V)[:40]
+    for x in kids:
+        par.append(0)
+        tok.append(int(x))
+    for u in sorted(range(1, 41), key=lambda u: -tok[u])[:3]:
+        for x in rng.permutation(V)[:50]:
+            par.append(u)
+            tok.append(int(x))
+    trees.append((par, tok))
+    # chain into a wide node
+    par, tok = [-1, 0, 1], [-1, int(rng.integers(V)), int(rng.integers(V))]
+    for x in rng.permutation(V)[:70]:
+        par.append(2)
+        tok.append(int(x))
+    trees.append((par, tok))
+    return trees
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_verifiers_wide_nodes_and_largest_budget(tsd, dev, orc, T):
+    """Nodes with 40 to 4095 children (the walks' lanes cover several
+    32-child chunks per node) at B = TSD_MAX_B (the largest staging), bf16,
+    V = 5000.  Each internal node's row favours its largest-token child, so
+    the sequential rule rejects most siblings before it accepts and the
+    proposal rule draws many candidates; both match the oracle."""
+    V, B = 5000, 4095
+    rng = np.random.default_rng(synth.seed_for(8, 4095))
+    trees = _wide_trees(rng, V, B)
+    nt = len(trees)
+    par = np.full((nt, B + 1), -1, dtype=np.int32)
+    tok = np.full((nt, B + 1), -1, dtype=np.int32)
+    nn = np.zeros(nt, dtype=np.int32)
+    for t, (p_, x_) in enumerate(trees):
+        nn[t] = len(p_)
+        par[t, :nn[t]] = p_
+        tok[t, :nn[t]] = x_
+    g = torch.Generator(device="cpu").manual_seed(int(synth.seed_for(8, 4096)))
+    z = torch.randn(nt, B + 1, V, generator=g)
+    for t in range(nt):
+        for v in range(nn[t]):
+            ch = [int(tok[t, u]) for u in range(1, nn[t]) if par[t, u] == v]
+            if ch:
+                z[t, v, max(ch)] += 10.0
+    tgt = z.to(torch.bfloat16).to(dev)
+    q = rng.uniform(0.5, 1.5, size=(nt, B + 1))
+    pd, xd = torch.tensor(par, device=dev), torch.tensor(tok, device=dev)
+    nd = torch.tensor(nn, device=dev)
+    qd = torch.tensor(q, dtype=torch.float32, device=dev)
+    flips, deep = 0, 0
+    for seed in range(3):
+        s_out = tsd.tsd_verify_seqres(tgt, pd, xd, nd, T, seed=seed)
+        p_out = tsd.tsd_verify_proposal(tgt, pd, xd, nd, qd, T, seed=seed)
+        assert _np(s_out["status"]).tolist() == [0] * nt
+        assert _np(p_out["status"]).tolist() == [0] * nt
+        for t in range(nt):
+            n = int(nn[t])
+            z64 = tgt[t, :n].float().cpu().numpy().astype(np.float64)
+            o = orc.seqres(z64, par[t], tok[t], n, T, seed=seed, tree=t)
+            got = (int(s_out["exit_node"][t]), int(s_out["bonus_token"][t]), int(s_out["accept_len"][t]))
+            if got != (o["exit_node"], o["bonus"], o["accept_len"]):
+                assert T > 0 and _seqres_margin(orc, z64, par[t], tok[t], n, T, seed, t) < 1e-6, (t, got, o)
+                flips += 1
+            deep += o["accept_len"] > 1
+            o = orc.proposal(z64, par[t], tok[t], n, T, q[t], seed=seed, tree=t)
+            got = (int(p_out["exit_node"][t]), int(p_out["bonus_token"][t]), int(p_out["accept_len"][t]))
+            if got != (o["exit_node"], o["bonus"], o["accept_len"]):
+                assert T > 0, (t, got, o)
+                flips += 1
+    assert flips <= 1, flips
+    assert deep >= 3  # the walks do pass the wide nodes
