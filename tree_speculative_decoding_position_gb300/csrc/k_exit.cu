@@ -60,12 +60,11 @@ __device__ void row_stats(const ChunkStat* __restrict__ cs, int nch, float c, in
 template <typename T>
 __global__ void __launch_bounds__(kExitThreads)
 exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, int nch, float c,
-                 double inv_temp, const int32_t* __restrict__ token,
+                 double temp, double inv_temp, const int32_t* __restrict__ token,
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes, int B,
                  const float* __restrict__ omega, double* __restrict__ loss_tree,
                  double* __restrict__ loss, int32_t* __restrict__ status, ExitWs ws) {
     pdl_entry();
-    __shared__ double W[TSD_MAX_L];
     __shared__ double lse[TSD_MAX_L];
     __shared__ double srow[TSD_MAX_L];
     __shared__ float mcrow[TSD_MAX_L];
@@ -161,25 +160,26 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
             A += red[i];
             Bn += red2[i];
         }
-        *ws.norm = Bn;
+        ws.norm[0] = Bn;
+        ws.norm[1] = Bn > 0.0 ? 1.0 / (temp * Bn) : 0.0;  // the gradient's factor, formed once
         *loss = Bn > 0.0 ? A / Bn : 0.0;
     }
 }
 
 // Dense part of the gradient, streaming: grad[row][a] = W_row softmax(z/T_d)(a)
-// / (T_d N), with softmax = 2^(z c - LSE_row log2 e); rows of invalid trees
+// / (T_d N) (1 / (T_d N) formed once by the per-tree kernel), with softmax = 2^(z c - LSE_row log2 e); rows of invalid trees
 // and rows no node scores are zero.  One warp per (row, 8 KB chunk of logits)
 // with all of the chunk's 16-byte loads in flight, then 16-byte streaming
 // stores; rows that are not 16-byte aligned take an element-wise loop.
 template <typename T>
 __global__ void __launch_bounds__(kExitThreads)
 exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, int nch, float c,
-                 double temp, float* __restrict__ grad, ExitWs ws) {
+                 float* __restrict__ grad, ExitWs ws) {
     pdl_entry();
     constexpr int VEC = Lanes<T>::kVec;
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     const int lane = threadIdx.x & (kWarp - 1);
-    const double nrm = *ws.norm;
+    const double nrm = ws.norm[0], inv = ws.norm[1];
     const bool vec = ((uintptr_t)logits % 16 == 0) && ((V * (int64_t)sizeof(T)) % 16 == 0) &&
                      ((uintptr_t)grad % 16 == 0);
     const int64_t total = rows * nch;
@@ -194,7 +194,7 @@ exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, i
         float* g = grad + row * V + c0;
         const T* z = logits + row * V + c0;
         const bool zero = ws.tstat[t] != kStatOk || wr == 0.0 || !(nrm > 0.0);
-        const float scale = zero ? 0.0f : (float)(wr / (temp * nrm));
+        const float scale = zero ? 0.0f : (float)(wr * inv);
         const float l2 = zero ? 0.0f : (float)(ws.lse[row] * 1.4426950408889634);
         if (vec) {
             uint4 buf[kVecPerLane];
@@ -227,18 +227,18 @@ exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, i
 
 // The gathered part: grad[row(v)][x_v] -= w(v) / (T_d N) for every node.
 __global__ void __launch_bounds__(kExitThreads)
-exit_scatter_kernel(int n_trees, int L, int64_t V, double temp, const int32_t* __restrict__ token,
+exit_scatter_kernel(int n_trees, int L, int64_t V, const int32_t* __restrict__ token,
                     const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes, int B,
                     const float* __restrict__ omega, float* __restrict__ grad, ExitWs ws) {
     pdl_entry();
-    const double nrm = *ws.norm;
+    const double nrm = ws.norm[0], inv = ws.norm[1];
     const int64_t total = (int64_t)n_trees * (B + 1);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / (B + 1)), v = (int)(i - (int64_t)t * (B + 1));
         if (v == 0 || v >= n_nodes[t] || ws.tstat[t] != kStatOk || !(nrm > 0.0)) continue;
         const int d = depth[i], x = token[i];
-        atomicAdd(grad + ((int64_t)t * L + d - 1) * V + x, (float)(-(double)omega[i] / (temp * nrm)));
+        atomicAdd(grad + ((int64_t)t * L + d - 1) * V + x, (float)(-(double)omega[i] * inv));
     }
 }
 
@@ -260,11 +260,11 @@ cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, i
     cudaError_t e;
     if (dtype == TSD_BF16)
         e = launch_pdl(exit_tree_kernel<__nv_bfloat16>, (unsigned)n_trees, kExitThreads, 0, stream,
-                       static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, inv_temp,
+                       static_cast<const __nv_bfloat16*>(logits), n_trees, L, V, nch, c, temp, inv_temp,
                        token, depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     else
         e = launch_pdl(exit_tree_kernel<float>, (unsigned)n_trees, kExitThreads, 0, stream,
-                       static_cast<const float*>(logits), n_trees, L, V, nch, c, inv_temp, token,
+                       static_cast<const float*>(logits), n_trees, L, V, nch, c, temp, inv_temp, token,
                        depth, n_nodes, B, omega, loss_tree, loss, status, ws);
     if (e != cudaSuccess) return e;
     if (grad) {
@@ -277,16 +277,16 @@ cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, i
         const unsigned g2 = (unsigned)(want < cap ? want : cap);
         if (dtype == TSD_BF16)
             e = launch_pdl(exit_grad_kernel<__nv_bfloat16>, g2, kExitThreads, 0, stream,
-                           static_cast<const __nv_bfloat16*>(logits), rows, L, V, nch, c, temp,
-                           grad, ws);
+                           static_cast<const __nv_bfloat16*>(logits), rows, L, V, nch, c, grad,
+                           ws);
         else
             e = launch_pdl(exit_grad_kernel<float>, g2, kExitThreads, 0, stream,
-                           static_cast<const float*>(logits), rows, L, V, nch, c, temp, grad, ws);
+                           static_cast<const float*>(logits), rows, L, V, nch, c, grad, ws);
         if (e != cudaSuccess) return e;
         const int64_t nodes = (int64_t)n_trees * (B + 1);
         const int64_t gs = (nodes + kExitThreads - 1) / kExitThreads;
         if ((e = launch_pdl(exit_scatter_kernel, (unsigned)(gs < 65535 ? (gs > 0 ? gs : 1) : 65535),
-                            kExitThreads, 0, stream, n_trees, L, V, temp, token, depth, n_nodes, B,
+                            kExitThreads, 0, stream, n_trees, L, V, token, depth, n_nodes, B,
                             omega, grad, ws)) != cudaSuccess)
             return e;
     }

@@ -124,7 +124,7 @@ size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* bas
     ws.lse = cv.take<double>(rows);
     ws.wrow = cv.take<double>(rows);
     ws.tstat = cv.take<int32_t>((size_t)n_trees);
-    ws.norm = cv.take<double>(1);
+    ws.norm = cv.take<double>(2);
     ws.done = cv.take<unsigned>(1);
     if (out) *out = ws;
     return (cv.off + kAlign - 1) & ~(kAlign - 1);

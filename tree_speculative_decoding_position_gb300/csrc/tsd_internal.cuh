@@ -379,7 +379,7 @@ struct ExitWs {
     double* lse;        // [n_trees][L] row log-normalisers of z / T_d
     double* wrow;       // [n_trees][L] summed weight of the nodes each row scores
     int32_t* tstat;     // [n_trees]
-    double* norm;       // [1] sum over valid trees of (n_nodes - 1)
+    double* norm;       // [2] N = sum over valid trees of (n_nodes - 1), then 1 / (T_d N) (0 if N = 0)
     unsigned* done;     // [1] completion counter of the per-tree kernel (zero between calls)
 };
 size_t exit_ws_layout(int n_trees, int L, int64_t V, int B, int esize, void* base, ExitWs* out);
