@@ -525,11 +525,12 @@ cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int
 // ---------------------------------------------------------------------------
 // Exact sequential residual verification ([EXIT] App. A.4.2) and
 // proposal-aware verification ([CAST] App. B.1 Thm. 3): one CTA per tree.
-// Thread 0 walks from the root on the per-node statistics of the row
-// reduction (p_v(x_u) of every child, rho(v)); the whole block then draws the
-// bonus token from the exit node's residual, as TEV's last step does.  At
-// each node the children are taken in ascending token order (the CSR lists
-// are sorted by token).
+// Warp 0 walks from the root on the per-node statistics of the row
+// reduction (p_v(x_u) of every child, rho(v)), staged with the tree and its
+// uniforms in shared memory; the whole block then draws the bonus token from
+// the exit node's residual, as TEV's last step does.  At each node the
+// children are taken in ascending token order (the CSR lists are sorted by
+// token).
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ void finish_walk(const T* __restrict__ logits, int t, int v, int B, int64_t V, int nch,
