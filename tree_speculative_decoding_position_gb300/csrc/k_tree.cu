@@ -108,10 +108,17 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
         // Line 9: residual draw.  Chunk sums relative to the row reference.
         const ChunkStat* cs = ws.chunk + row * nch;
         const float thr2 = u * ns.r;
-        __shared__ int chunk_sel;
+        constexpr int CE = kChunkBytes / (int)sizeof(T);
+        const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
+        __shared__ int chunk_sel, chunk_clo, chunk_chh;
         __shared__ float chunk_frac;
         if (threadIdx.x < kWarp) {
             const int lane = threadIdx.x;
+            // the exit node's children (sorted by token): the first 32 tokens
+            // are loaded now, beside the chunk sums, one per lane
+            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
+            const int kids_lo = cptr[V_], kids_hi = cptr[V_ + 1];
+            const int32_t tk0 = kids_lo + lane < kids_hi ? ctok[kids_lo + lane] : 0;
             float base = 0.0f;
             int sel = -1, lastc = -1;
             float frac = 0.0f;
@@ -136,27 +143,35 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
                 sel = lastc;
                 frac = 1.0f;
             }
+            // [clo, chh): the children whose tokens fall in the chosen chunk,
+            // counted 32 children per step
+            int clo = kids_lo, chh = kids_lo;
+            if (sel >= 0) {
+                const int64_t c0 = (int64_t)sel * CE, c1 = c0 + CE;
+                int32_t tk = tk0;
+                for (int j0 = kids_lo; j0 < kids_hi; j0 += kWarp) {
+                    const bool valid = j0 + lane < kids_hi;
+                    if (j0 > kids_lo) tk = valid ? ctok[j0 + lane] : 0;
+                    clo += __popc(__ballot_sync(0xffffffffu, valid && (int64_t)tk < c0));
+                    chh += __popc(__ballot_sync(0xffffffffu, valid && (int64_t)tk < c1));
+                }
+            }
             if (lane == 0) {
                 chunk_sel = sel;
                 chunk_frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
+                chunk_clo = clo;
+                chunk_chh = chh;
             }
         }
         __syncthreads();
         const int q = chunk_sel;
         y = -1;
         if (q >= 0) {
-            constexpr int CE = kChunkBytes / (int)sizeof(T);
             const int64_t c0 = (int64_t)q * CE;
             const int cn = (int)min((int64_t)CE, V - c0);
-            const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-            const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
-            int clo = cptr[V_], chi = cptr[V_ + 1];
-            while (clo < chi && ctok[clo] < c0) ++clo;  // children are sorted by token
-            int chh = clo;
-            while (chh < chi && ctok[chh] < c0 + cn) ++chh;
             const int o = draw_in_chunk_block<T>(logits + row * V + c0, c0, cn, c,
-                                                 __fmul_rn(cs[q].m, c), chunk_frac, ctok, clo,
-                                                 chh, red, pick);
+                                                 __fmul_rn(cs[q].m, c), chunk_frac, ctok,
+                                                 chunk_clo, chunk_chh, red, pick);
             y = o >= 0 ? (int)(c0 + o) : -1;
         }
     }
@@ -213,9 +228,10 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
     for (int u = threadIdx.x; u < stride; u += blockDim.x) {
         float P = 0.0f, wu = 0.0f;
         if (u < n) {
+            const float ru = rho[u];  // issued before the walk
             P = 1.0f;
             for (int x = u; x > 0; x = par[x]) P *= pedge[x];
-            wu = P * rho[u];
+            wu = P * ru;
             if (u > 0) cov_part += P;
         }
         w[u] = wu;
