@@ -561,13 +561,39 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
             lat.append(a.elapsed_time(b))
     out["b64_single_tree"]["round_graph_ms"] = statistics.median(lat)
     out["b64_single_tree"]["round_graph_ms_best"] = min(lat)
+    del graph
+    # the verifier stage alone at batch 1: TEV against predraw-and-follow on
+    # the same tree and logits, each captured in a CUDA graph and replayed with
+    # L2 flushed first (the pages compare the two at batch 1)
+    for name, vfn in (("tev", tsd.tsd_verify_tev), ("predraw", tsd.tsd_verify_ddtree)):
+        with torch.cuda.stream(cap):
+            for i in range(3):
+                vfn(copies[0], t1["parent"], t1["token"], t1["n_nodes"], 1.0, seed=i,
+                    workspace=ws1)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            vfn(copies[0], t1["parent"], t1["token"], t1["n_nodes"], 1.0, seed=0, workspace=ws1)
+        lat = []
+        for i in range(45):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 5:
+                lat.append(a.elapsed_time(b))
+        out["b64_single_tree"]["verify_graph_ms_" + name] = statistics.median(lat)
+        del graph
     # the oracle beside it: the same round, float64, one host thread
     z1 = dr[0, 0].float().cpu().numpy()
     tg1 = copies[0][0, :n].float().cpu().numpy()
     out["b64_single_tree"].update(
         oracle_round_ms=oracle_ms(lambda orc: oracle_round(orc, z1, tg1, 8, B1, 1.0, 0)),
         oracle_sample="one round (drafter statistics, heap, mask, TEV at T=1), float64, one thread")
-    del copies, graph
+    del copies
     # mixture-of-futures workload: 16 trees, K = 8 modes from two latent
     # futures, B = 128; the mixture builder, then TEV at T = 1 on its trees
     nt_m, K_m, B_m = 16, 8, 128
