@@ -161,6 +161,46 @@ def test_tree_mask(tsd, dev, orc, B, P):
     assert _np(out["status"]).tolist() == [0, 0, 0]
 
 
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tev_and_mask_at_the_largest_budget(tsd, dev, orc, T):
+    """B = TSD_MAX_B (4096 nodes per tree, the largest child-list sort and
+    bit rows of 128 words): a random recursive tree (parent of u uniform
+    below u), one ragged tree, bf16 target logits at V = 5000.  TEV against
+    the oracle (masses within tolerance, draws exact up to counted flips)
+    and the mask bit for bit."""
+    V, B = 5000, 4095
+    rng = np.random.default_rng(synth.seed_for(4, 4095))
+    nt = 2
+    parent = np.full((nt, B + 1), -1, dtype=np.int32)
+    token = np.full((nt, B + 1), -1, dtype=np.int32)
+    nn = [B + 1, 3001]
+    for t in range(nt):
+        parent[t, 1:nn[t]] = [int(rng.integers(u)) for u in range(1, nn[t])]
+        token[t, 1:nn[t]] = rng.permutation(V)[:nn[t] - 1]
+    g = torch.Generator().manual_seed(int(synth.seed_for(4, 4096)))
+    z = (torch.randn(nt, B + 1, V, generator=g) * 2).to(torch.bfloat16)
+    for t in range(nt):  # raise about a third of the drafted tokens so that paths carry mass
+        for u in range(1, nn[t]):
+            if int(parent[t, u]) >= 0 and rng.random() < 0.3:
+                z[t, int(parent[t, u]), int(token[t, u])] = 6.0
+    pd, xd = torch.tensor(parent, device=dev), torch.tensor(token, device=dev)
+    nd = torch.tensor(nn, dtype=torch.int32, device=dev)
+    out = tsd.tsd_verify_tev(z.to(dev), pd, xd, nd, T, seed=3)
+    flips = 0
+    for t in range(nt):
+        n = nn[t]
+        z64 = z[t, :n].float().numpy().astype(np.float64)
+        o = orc.tev(z64, parent[t], token[t], n, T, seed=3, tree=t)
+        flips += _check_tev(out, t, o, z64, parent[t], token[t], n, T)
+    assert flips <= 1, flips
+    m = tsd.tsd_tree_mask(pd, nd, prefix_len=77)
+    for t in range(nt):
+        bits, pos, _ = orc.tree_mask(parent[t], nn[t], B, 77)
+        assert np.array_equal(_np(m["anc_bits"][t]).view(np.uint32), bits)
+        assert np.array_equal(_np(m["position_ids"][t]), pos)
+    assert _np(m["status"]).tolist() == [0] * nt
+
+
 def test_tree_mask_bad_tree(tsd, dev):
     par = torch.tensor([[-1, 0, 2, 1]], dtype=torch.int32, device=dev)  # parent after child
     out = tsd.tsd_tree_mask(par, torch.tensor([4], dtype=torch.int32, device=dev))
