@@ -395,6 +395,26 @@ tsd_status tsd_verify_tev_noalloc(const void *target_logits, tsd_dtype dtype,
                                   float *prefix_prob, float *coverage, int32_t *status,
                                   cudaStream_t stream);
 
+/*
+ * tsd_debug_check_failures -- the bounds checks of a checked build.  A
+ * debugging aid with no counterpart on the pages.
+ *
+ * A library compiled with -DTSD_CHECKS (the package's checked build,
+ * libtsd_checks.so) tests every index that a kernel takes from memory before
+ * using it: parents, CSR child offsets and child ids, tokens used as columns,
+ * node ids, list, chunk and candidate positions.  A failing check sets one bit
+ * per site class and skips the access; no kernel traps.  This call
+ * synchronises the current device, returns the OR of the bits set since the
+ * previous call (0 when every check passed) and clears them.  Bit i is site
+ * class i: 0 work item of the row pass, 1 CSR child list, 2 verify
+ * preparation, 3 ancestor walk, 4 exit node / chunk / bonus, 5 walk verifiers,
+ * 6 predraw-and-follow, 7 builder, 8 tree mask, 9 drafter statistics,
+ * 10 log-sum-exp tree, 11 shared-budget selection, 12 exit loss.
+ * In the default build the checks are compiled out and the call returns 0
+ * without touching the device.
+ */
+unsigned tsd_debug_check_failures(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "tsd_build_forest", "tsd_build_lse_tree", "tsd_build_tree", "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
+        "tsd_build_forest", "tsd_build_lse_tree", "tsd_build_tree", "tsd_debug_check_failures",
+        "tsd_status_string", "tsd_tree_mask", "tsd_verify_ddtree",
         "tsd_exit_loss", "tsd_verify_proposal", "tsd_verify_seqres", "tsd_verify_tev",
         "tsd_verify_tev_noalloc", "tsd_verify_tev_timed", "tsd_workspace_size"])
 
@@ -36,6 +37,12 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_default_build_has_no_checks(lib):
+    """The product library compiles the bounds checks out: the reader returns 0
+    without touching a device (this runs with no GPU)."""
+    assert tsd.tsd_debug_check_failures() == 0
 
 
 def test_status_strings(lib):

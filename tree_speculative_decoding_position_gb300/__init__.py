@@ -19,9 +19,13 @@ import torch
 __all__ = ["TsdError", "load", "tsd_status_string", "tsd_workspace_size", "tsd_build_tree",
            "tsd_tree_mask", "tsd_verify_tev", "tsd_verify_tev_timed", "tsd_verify_ddtree",
            "tsd_verify_tev_noalloc", "tsd_exit_loss", "tsd_verify_seqres",
-           "tsd_verify_proposal", "tsd_build_forest", "LIB_PATH"]
+           "tsd_verify_proposal", "tsd_build_forest", "tsd_debug_check_failures", "LIB_PATH"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtsd.so")
+# TSD_LIBRARY=checks selects the bounds-checked build (libtsd_checks.so, made by
+# build.build(checks=True)); the default is the product library.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libtsd_checks.so" if os.environ.get("TSD_LIBRARY") == "checks"
+                        else "libtsd.so")
 
 TSD_OK, TSD_ERR_INVALID_ARG, TSD_ERR_CUDA, TSD_ERR_WORKSPACE = 0, 1, 2, 3
 TSD_ERR_BAD_TREE, TSD_ERR_NONFINITE, TSD_ERR_TIMEOUT = 4, 5, 6
@@ -39,18 +43,22 @@ class TsdError(RuntimeError):
 
 
 def load():
-    """Load libtsd.so; raises if it has not been built (no fallback exists)."""
+    """Load the library; raises if it has not been built (no fallback exists)."""
     global _lib
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError("libtsd.so is missing: build it with "
-                           "`python -m tree_speculative_decoding_position_gb300.build`")
+        raise RuntimeError("%s is missing: build it with "
+                           "`python -m tree_speculative_decoding_position_gb300.build%s`"
+                           % (os.path.basename(LIB_PATH),
+                              " --checks" if LIB_PATH.endswith("_checks.so") else ""))
     lib = ctypes.CDLL(LIB_PATH)
     P, i32, i64, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                  ctypes.c_uint64, ctypes.c_size_t)
     lib.tsd_status_string.argtypes = [i32]
     lib.tsd_status_string.restype = ctypes.c_char_p
+    lib.tsd_debug_check_failures.argtypes = []
+    lib.tsd_debug_check_failures.restype = ctypes.c_uint
     lib.tsd_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32]
     lib.tsd_workspace_size.restype = sz
     lib.tsd_build_tree.argtypes = [P, i32, i32, i32, i32, i64, i32, i32, f32,
@@ -79,6 +87,12 @@ def load():
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
+
+
+def tsd_debug_check_failures() -> int:
+    """Bits of the bounds-check site classes that failed since the last call
+    (a checked build only; 0 in the default build).  Synchronises the device."""
+    return int(load().tsd_debug_check_failures())
 
 
 def tsd_status_string(code: int) -> str:

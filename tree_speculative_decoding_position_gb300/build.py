@@ -1,7 +1,9 @@
 """Build step for the CUDA library: compiles csrc/*.cu for sm_103a in parallel
-and links them into ``libtsd.so`` next to this file.
+and links them into ``libtsd.so`` next to this file.  ``checks=True`` builds
+the bounds-checked variant instead (``-DTSD_CHECKS``, ``libtsd_checks.so``,
+objects in ``_build_checks``); see tsd_debug_check_failures in tsd.h.
 
-    python -m tree_speculative_decoding_position_gb300.build [--force] [-v]
+    python -m tree_speculative_decoding_position_gb300.build [--force] [--checks] [-v]
 """
 from __future__ import annotations
 
@@ -17,6 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtsd.so")
+CHECKS_OUT_DIR = os.path.join(HERE, "_build_checks")
+CHECKS_LIB = os.path.join(HERE, "libtsd_checks.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -38,23 +42,26 @@ def _headers():
     return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "tsd.h")])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checks: bool = False) -> str:
     """Compile and link; returns the library path."""
-    if not force and up_to_date():
-        return LIB
+    lib, out_dir = (CHECKS_LIB, CHECKS_OUT_DIR) if checks else (LIB, OUT_DIR)
+    if checks:
+        extra_flags = tuple(extra_flags) + ("-DTSD_CHECKS",)
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -67,16 +74,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checks="--checks" in sys.argv))

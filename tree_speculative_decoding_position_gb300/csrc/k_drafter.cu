@@ -125,7 +125,8 @@ drafter_chunk_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int 
     uint4 buf[kVecPerLane];
     auto load = [&]() {
         const int64_t c0 = (int64_t)ch * CE;
-        const int cn = (int)min((int64_t)CE, V - c0);
+        const bool in = TSD_IN(row, rows, kChkDrafter) && TSD_IN(ch, nch, kChkDrafter);
+        const int cn = in ? (int)min((int64_t)CE, V - c0) : 0;
         const T* rp = logits + row * V + c0;
 #pragma unroll
         for (int i = 0; i < kVecPerLane; ++i) {
@@ -262,7 +263,10 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
     __syncthreads();
     const float theta = s_theta;
     for (int q = tid; q < nch; q += kRThreads)
-        if (cm[q] >= theta) qlist[atomicAdd(&n_q, 1)] = q;
+        if (cm[q] >= theta) {
+            const int pos = atomicAdd(&n_q, 1);
+            if (TSD_IN(pos, kMaxDrafterChunks, kChkDrafter)) qlist[pos] = q;
+        }
     __syncthreads();
     // (2) qualifying slices
     const int nq = n_q;
@@ -401,5 +405,7 @@ cudaError_t launch_drafter_stats(const void* logits, tsd_dtype dtype, int64_t ro
     return launch_pdl(drafter_row_kernel<float>, (unsigned)rows, kRThreads, 0, stream,
                       static_cast<const float*>(logits), rows, V, nch, topk, c, temp, vec_ok, ws);
 }
+
+TSD_CHECK_READER(checks_drafter)
 
 }  // namespace tsd

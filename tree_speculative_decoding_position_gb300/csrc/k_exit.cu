@@ -238,6 +238,7 @@ exit_scatter_kernel(int n_trees, int L, int64_t V, const int32_t* __restrict__ t
         const int t = (int)(i / (B + 1)), v = (int)(i - (int64_t)t * (B + 1));
         if (v == 0 || v >= n_nodes[t] || ws.tstat[t] != kStatOk || !(nrm > 0.0)) continue;
         const int d = depth[i], x = token[i];
+        if (!(TSD_IN(d - 1, L, kChkExit) && TSD_IN(x, V, kChkExit))) continue;
         atomicAdd(grad + ((int64_t)t * L + d - 1) * V + x, (float)(-(double)omega[i] * inv));
     }
 }
@@ -292,5 +293,7 @@ cudaError_t launch_exit_loss(const void* logits, tsd_dtype dtype, int n_trees, i
     }
     return cudaGetLastError();
 }
+
+TSD_CHECK_READER(checks_exit)
 
 }  // namespace tsd

@@ -120,6 +120,7 @@ forest_rank_kernel(const int32_t* __restrict__ depth,
             // first node of request q that does not precede this candidate
             const int64_t qb = (int64_t)q * stride;
             int lo = 0, hi = ws.cnt[q];
+            if (!TSD_IN(hi, stride, kChkForest)) hi = 0;
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
                 const unsigned long long sx = ws.img[qb + mid];
@@ -176,7 +177,7 @@ forest_finish_kernel(int B, ForestWs ws, int32_t* __restrict__ n_nodes,
                 if (rk[mid] < M) lo = mid + 1;
                 else hi = mid;
             }
-            keep = lo + 1;
+            keep = TSD_IN(lo, stride, kChkForest) ? lo + 1 : 1;
             n_nodes[r] = keep;
         } else {
             keep = n_nodes[r];
@@ -207,5 +208,7 @@ cudaError_t launch_forest_select(const double* score64, int32_t* depth, int n_tr
     return launch_pdl(forest_finish_kernel, (unsigned)n_trees, kForestThreads, 0, stream, B, ws,
                       n_nodes, status, total, parent, token, depth, score);
 }
+
+TSD_CHECK_READER(checks_forest)
 
 }  // namespace tsd

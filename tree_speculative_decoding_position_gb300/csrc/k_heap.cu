@@ -538,7 +538,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             int pos = block_incl_scan_int(nok, red, &written) - nok;
 #pragma unroll
             for (int u = 0; u < kSlotsPerThread; ++u)
-                if (okc[u]) S[pos++] = ch[u];
+                if (okc[u] && TSD_IN(pos, M * k, kChkBuild)) S[pos++] = ch[u];
             if (tid == 0) s_nS = written;
             __syncthreads();
             const int nS = s_nS;
@@ -697,7 +697,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         };
         for (int i = tid; i < nX; i += blockDim.x) {
             const int node = (K == 1) ? i + 1 : flag[plan.xcap + i] + 1;
-            if (node <= 0) continue;
+            if (node <= 0 || !TSD_IN(node, stride, kChkBuild)) continue;
             const FEntry e = X[xc][i];
             const unsigned long long h = node_key(e);
             unsigned int b = first_bucket(h);
@@ -723,7 +723,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         __syncthreads();
         for (int i = tid; i < nX; i += blockDim.x) {
             const int node = (K == 1) ? i + 1 : flag[plan.xcap + i] + 1;
-            if (node <= 0) continue;
+            if (node <= 0 || !TSD_IN(node, stride, kChkBuild)) continue;
             const FEntry e = X[xc][i];
             const int d = tb_depth(e.tb);
             int pn = 0;
@@ -751,6 +751,7 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
             }
             par[node] = pn;
             if (pn < 0) s_bad = 2;
+            else if (!TSD_IN(pn, node, kChkBuild)) s_bad = 2;  // a parent precedes its child
         }
         __syncthreads();
         if (tid == 0) {
@@ -793,5 +794,7 @@ cudaError_t launch_build_heap(const BuildWs& ws, int n_trees, int n_modes, int L
         ws, p, n_modes, L, topk, B, bits, parent, token, depth, score, rank, mode, n_nodes, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
+
+TSD_CHECK_READER(checks_heap)
 
 }  // namespace tsd

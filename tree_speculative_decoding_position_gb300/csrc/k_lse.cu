@@ -224,6 +224,7 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
         double* npm = pm[cur];
         for (int e = tid; e < nb * K; e += blockDim.x) {
             const int j = e / K, m2 = e - j * K;
+            if (!(TSD_IN(par[j], B, kChkLse) && TSD_IN(rk[j], k, kChkLse))) continue;
             npm[e] = (d == 0 ? 0.0 : opm[par[j] * K + m2]) + zall[rk[j] * K + m2];
         }
         __syncthreads();
@@ -428,7 +429,7 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             if (!lv[q]) continue;
             const int e = S * tid + q, m = e / B;
             const int f = d * KB + e;
-            const int pr = d == 0 ? -1 : rep_prev[m * B + pp[q]];
+            const int pr = d == 0 ? -1 : (TSD_IN(pp[q], B, kChkLse) ? rep_prev[m * B + pp[q]] : -1);
             const unsigned long long key =
                 ((unsigned long long)(unsigned)(pr + 1) << 32) | (unsigned)tk[q];
             unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (unsigned)(H - 1);
@@ -611,9 +612,13 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             const int64_t f = (int64_t)sk1[q];
             const int d = (int)(f / KB), e = (int)(f - (int64_t)d * KB), m = e / B;
             int pn = 0;
-            if (d > 0)
-                pn = ws.node_of[base + ws.rep[base + (int64_t)(d - 1) * KB + (int64_t)m * B +
-                                              ws.par[base + f]]];
+            if (d > 0) {
+                const int pp = ws.par[base + f];
+                const int64_t r =
+                    TSD_IN(pp, B, kChkLse) ? ws.rep[base + (int64_t)(d - 1) * KB + (int64_t)m * B + pp] : 0;
+                pn = TSD_IN(r, N, kChkLse) ? ws.node_of[base + r] : 0;
+            }
+            if (!TSD_IN(pn, q + 1, kChkLse)) pn = 0;  // a parent precedes its child
             parent[o] = pn;
             token[o] = ws.tok[base + f];
             depth[o] = d + 1;
@@ -656,5 +661,7 @@ cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, in
     return launch_pdl(lse_select_kernel, (unsigned)n_trees, kSelThreads, ss, stream, K, L, k, B, bws,
                       ws, parent, token, depth, score, n_nodes, status, n_cand);
 }
+
+TSD_CHECK_READER(checks_lse)
 
 }  // namespace tsd

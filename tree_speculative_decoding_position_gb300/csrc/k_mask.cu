@@ -42,7 +42,8 @@ tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__
             // children), so the row's words are written from the last down.
             int w = W - 1;
             uint32_t acc = 0;
-            for (int u = v; u >= 0; u = (u > 0 ? par[u] : -1)) {
+            for (int u = v; u >= 0;
+                 u = (u > 0 && TSD_IN(par[u], u, kChkMask) ? par[u] : -1)) {
                 const int wu = u >> 5;
                 while (w > wu) {
                     row[w--] = acc;
@@ -88,5 +89,7 @@ cudaError_t launch_tree_mask(const int32_t* parent, const int32_t* n_nodes, int 
                                                            mask_ld, status); e_ != cudaSuccess) return e_;
     return cudaGetLastError();
 }
+
+TSD_CHECK_READER(checks_mask)
 
 }  // namespace tsd

@@ -126,7 +126,8 @@ verify_prep_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
     int32_t* dep = ws.depth + (int64_t)t * (B + 1);
     for (int i = threadIdx.x; i < m; i += blockDim.x) {
         ctok[i] = (int32_t)((keys[i] >> 12) & 0x7fffffffu);
-        cnode[i] = (int32_t)(keys[i] & 0xfffu);
+        const int32_t u = (int32_t)(keys[i] & 0xfffu);
+        cnode[i] = TSD_IN(u, nn, kChkPrep) ? u : 0;
     }
     // child_ptr[v] = first sorted edge whose parent is >= v
     for (int v = threadIdx.x; v <= nn; v += blockDim.x) {
@@ -428,7 +429,9 @@ rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch
     }
     ItemPos p = item_pos((int64_t)blockIdx.x * wpb + threadIdx.x / kWarp, R, nch);
     auto live = [&](const ItemPos& q) {
-        return __ldg(n_nodes + q.t) > q.v && ws.tstat[q.t] == kStatOk;
+        return TSD_IN(q.t, n_trees, kChkRowsItem) && TSD_IN(q.v, R, kChkRowsItem) &&
+               TSD_IN(q.ch, nch, kChkRowsItem) && __ldg(n_nodes + q.t) > q.v &&
+               ws.tstat[q.t] == kStatOk;
     };
     auto children = [&](const ItemPos& q, int64_t c0, int cn, int& clo, int& chi) {
         clo = chi = 0;
@@ -436,7 +439,7 @@ rows_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch
             const int32_t* cptr = ws.child_ptr + (int64_t)q.t * (B + 2);
             const int32_t* ctok = ws.child_tok + (int64_t)q.t * R;
             const int b0 = cptr[q.v], b1 = cptr[q.v + 1];
-            if (b1 > b0) {
+            if (b1 > b0 && TSD_IN(b0, R, kChkChildList) && TSD_IN(b1, R, kChkChildList)) {
                 clo = lower_bound_i32(ctok, b0, b1, c0);
                 chi = lower_bound_i32(ctok, clo, b1, c0 + cn);
             }
@@ -547,7 +550,8 @@ node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V,
         const int32_t* ctok = ws.child_tok + (int64_t)t * (B + 1);
         const int32_t* cnode = ws.child_node + (int64_t)t * (B + 1);
         float* pedge = ws.pedge + (int64_t)t * (B + 1);
-        const int b0 = cptr[v], b1 = cptr[v + 1];
+        int b0 = cptr[v], b1 = cptr[v + 1];
+        if (!(TSD_IN(b0, B + 1, kChkChildList) && TSD_IN(b1, B + 1, kChkChildList))) b0 = b1 = 0;
         NodeStat ns;
         bool bad = false;
         if (GREEDY) {
@@ -569,7 +573,7 @@ node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V,
             bool hit = false;  // is the arg-max a drafted child?
             for (int q = b0 + lane; q < b1; q += kWarp) {
                 const bool h = (ctok[q] == bi);
-                pedge[cnode[q]] = h ? 1.0f : 0.0f;
+                if (TSD_IN(cnode[q], B + 1, kChkChildList)) pedge[cnode[q]] = h ? 1.0f : 0.0f;
                 hit |= h;
             }
             ns.r = __any_sync(0xffffffffu, hit) ? 0.0f : 1.0f;
@@ -599,6 +603,8 @@ node_combine_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V,
                 const T* rp = logits + row * V;
                 const float inv_s = 1.0f / s;
                 for (int q = b0 + lane; q < b1; q += kWarp) {
+                    if (!(TSD_IN(ctok[q], V, kChkChildList) && TSD_IN(cnode[q], B + 1, kChkChildList)))
+                        continue;
                     const float z = load_logit(rp + ctok[q]);
                     pedge[cnode[q]] = ex2(fmaf(z, c, -mc)) * inv_s;
                 }
@@ -636,5 +642,7 @@ cudaError_t launch_node_combine(const void* logits, tsd_dtype dtype, int n_trees
     }
     return cudaGetLastError();
 }
+
+TSD_CHECK_READER(checks_rows)
 
 }  // namespace tsd

@@ -99,6 +99,7 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
                                    int nch, float c, bool greedy, float u, const VerifyWs& ws,
                                    float* red, int* pick) {
     const int stride = B + 1;
+    if (!TSD_IN(V_, stride, kChkExitNode)) return -1;
     const int64_t row = (int64_t)t * stride + V_;
     const NodeStat ns = ws.node[row];
     int y;
@@ -117,7 +118,9 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
             // the exit node's children (sorted by token): the first 32 tokens
             // are loaded now, beside the chunk sums, one per lane
             const int32_t* cptr = ws.child_ptr + (int64_t)t * (B + 2);
-            const int kids_lo = cptr[V_], kids_hi = cptr[V_ + 1];
+            int kids_lo = cptr[V_], kids_hi = cptr[V_ + 1];
+            if (!(TSD_IN(kids_lo, B + 1, kChkChildList) && TSD_IN(kids_hi, B + 1, kChkChildList)))
+                kids_lo = kids_hi = 0;
             const int32_t tk0 = kids_lo + lane < kids_hi ? ctok[kids_lo + lane] : 0;
             float base = 0.0f;
             int sel = -1, lastc = -1;
@@ -166,7 +169,7 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
         __syncthreads();
         const int q = chunk_sel;
         y = -1;
-        if (q >= 0) {
+        if (q >= 0 && TSD_IN(q, nch, kChkExitNode)) {
             const int64_t c0 = (int64_t)q * CE;
             const int cn = (int)min((int64_t)CE, V - c0);
             const int o = draw_in_chunk_block<T>(logits + row * V + c0, c0, cn, c,
@@ -230,7 +233,12 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
         if (u < n) {
             const float ru = rho[u];  // issued before the walk
             P = 1.0f;
-            for (int x = u; x > 0; x = par[x]) P *= pedge[x];
+            for (int x = u; x > 0;) {
+                P *= pedge[x];
+                const int px = par[x];
+                if (!TSD_IN(px, x, kChkAncestor)) break;
+                x = px;
+            }
             wu = P * ru;
             if (u > 0) cov_part += P;
         }
@@ -470,7 +478,8 @@ predraw_nodes_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V
     }
 }
 
-// One thread per tree: follow R_v from the root.
+// One CTA per tree: the block copies the draws, thread 0 follows R_v from the
+// root.
 __global__ void predraw_walk_kernel(int n_trees, int B, const int32_t* __restrict__ n_nodes,
                                     VerifyWs ws, int32_t* __restrict__ exit_node,
                                     int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
@@ -498,12 +507,13 @@ __global__ void predraw_walk_kernel(int n_trees, int B, const int32_t* __restric
     for (int step = 0; step < n; ++step) {
         const int r = ws.draws[(int64_t)t * stride + v];
         int lo = cptr[v], hi = cptr[v + 1];
+        if (!(TSD_IN(lo, stride, kChkPredraw) && TSD_IN(hi, stride, kChkPredraw))) break;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             if (ctok[mid] < r) lo = mid + 1;
             else hi = mid;
         }
-        if (lo < cptr[v + 1] && ctok[lo] == r) v = cnode[lo];
+        if (lo < cptr[v + 1] && ctok[lo] == r && TSD_IN(cnode[lo], n, kChkPredraw)) v = cnode[lo];
         else break;
     }
     exit_node[t] = v;
@@ -603,11 +613,15 @@ __device__ void stage_walk_tree(const VerifyWs& ws, int t, int n, int B, uint64_
     wt.u0 = wt.pedge + (B + 1);
     wt.u1 = wt.u0 + (B + 1);
     const int m = n - 1;
-    for (int i = threadIdx.x; i <= n; i += blockDim.x) wt.cptr[i] = ws.child_ptr[(int64_t)t * (B + 2) + i];
+    for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+        const int x = ws.child_ptr[(int64_t)t * (B + 2) + i];
+        wt.cptr[i] = TSD_IN(x, n, kChkWalk) ? x : 0;  // offsets into the n - 1 edges
+    }
     for (int i = threadIdx.x; i < m; i += blockDim.x) wt.cnode[i] = ws.child_node[(int64_t)t * (B + 1) + i];
     for (int i = threadIdx.x; i < n; i += blockDim.x) wt.pedge[i] = ws.pedge[(int64_t)t * (B + 1) + i];
     __syncthreads();
     for (int q = threadIdx.x; q < m; q += blockDim.x) {
+        if (!TSD_IN(wt.cnode[q], n, kChkWalk)) wt.cnode[q] = 0;
         int lo = 0, hi = n;  // the node v with cptr[v] <= q < cptr[v+1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -841,5 +855,7 @@ cudaError_t launch_proposal_tree(const void* logits, tsd_dtype dtype, int n_tree
                       static_cast<const float*>(logits), B, V, nch, c, greedy, seed, q_child,
                       n_nodes, ws, exit_node, bonus, accept_len, status);
 }
+
+TSD_CHECK_READER(checks_tree)
 
 }  // namespace tsd

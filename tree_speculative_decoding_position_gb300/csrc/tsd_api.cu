@@ -201,6 +201,14 @@ using namespace tsd;
 
 extern "C" {
 
+unsigned tsd_debug_check_failures(void) {
+#ifdef TSD_CHECKS
+    cudaDeviceSynchronize();
+#endif
+    return checks_rows() | checks_tree() | checks_heap() | checks_mask() | checks_drafter() |
+           checks_lse() | checks_forest() | checks_exit();
+}
+
 const char* tsd_status_string(tsd_status s) {
     switch (s) {
         case TSD_OK: return "ok";

@@ -12,6 +12,60 @@ namespace tsd {
 
 constexpr int kWarp = 32;
 
+// ---------------------------------------------------------------------------
+// Bounds checks of a checked build (-DTSD_CHECKS).  Every index a kernel
+// takes from memory (a parent, a child list offset, a token used as a
+// column, a node id, a chunk or list position) passes TSD_IN(i, n, site)
+// before its access: in a checked build a failing check sets bit `site` of
+// this translation unit's check word and the access is skipped (no trap);
+// in the default build the macro is the constant true and costs nothing.
+// tsd_debug_check_failures() ORs and clears the words of every unit.
+// ---------------------------------------------------------------------------
+enum CheckSite : unsigned {
+    kChkRowsItem = 0,   // rows_kernel: (tree, node, chunk) of a work item
+    kChkChildList,      // a node's CSR child range and its child ids / tokens
+    kChkPrep,           // verify_prep_kernel: sort keys, parents, node ids
+    kChkAncestor,       // a parent read during an ancestor walk
+    kChkExitNode,       // a drawn exit node, chunk or bonus token
+    kChkWalk,           // the walk verifiers' staged tree, uniforms, children
+    kChkPredraw,        // predraw-and-follow: draws and the followed child
+    kChkBuild,          // the builder: list, frontier, successor, node positions
+    kChkMask,           // tree_mask_kernel: ancestor bits
+    kChkDrafter,        // drafter kernels: chunk, slice and candidate positions
+    kChkLse,            // log-sum-exp lists and selection: places, reps, nodes
+    kChkForest,         // shared-budget selection: ranks and kept nodes
+    kChkExit,           // exit loss: rows and gathered tokens
+};
+#ifdef TSD_CHECKS
+static __device__ unsigned int g_tsd_check_word;  // one per translation unit
+__device__ __forceinline__ bool tsd_in_range(long long i, long long n, unsigned site) {
+    if (i >= 0 && i < n) return true;
+    atomicOr(&g_tsd_check_word, 1u << site);
+    return false;
+}
+#define TSD_IN(i, n, site) ::tsd::tsd_in_range((long long)(i), (long long)(n), (site))
+// The host reader of this unit's word: returns it and clears it.
+#define TSD_CHECK_READER(name)                                                   \
+    unsigned name() {                                                            \
+        unsigned v = 0, z = 0;                                                   \
+        cudaMemcpyFromSymbol(&v, g_tsd_check_word, sizeof(v));                   \
+        cudaMemcpyToSymbol(g_tsd_check_word, &z, sizeof(z));                     \
+        return v;                                                                \
+    }
+#else
+#define TSD_IN(i, n, site) true
+#define TSD_CHECK_READER(name) \
+    unsigned name() { return 0u; }
+#endif
+unsigned checks_rows();
+unsigned checks_tree();
+unsigned checks_heap();
+unsigned checks_mask();
+unsigned checks_drafter();
+unsigned checks_lse();
+unsigned checks_forest();
+unsigned checks_exit();
+
 // A logits row is processed in chunks of 8 KB (4096 bf16 or 2048 fp32
 // tokens); one warp reduces one chunk with sixteen 16-byte loads per lane.
 constexpr int kChunkBytes = 8192;
