@@ -316,7 +316,7 @@ def run_ours(args):
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(drafter, target, last[0], k, B, T)
+        cpu = cpu_baseline(drafter, target, last[0], k, B, T, out=last[1], seed=1000 + args.steps - 1)
     line = {
         "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -776,20 +776,43 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-def oracle_round(oracle, z, tg, k, B, T, t):
+def oracle_round(oracle, z, tg, k, B, T, t, seed=0):
     """One round of the workload in the float64 oracle: drafter statistics and
-    heap, mask, TEV.  z: [L, V] drafter logits, tg: [n, V] target rows."""
+    heap, mask, TEV.  z: [L, V] drafter logits, tg: [n, V] target rows.
+    Returns the oracle's tree and TEV result."""
     ref = oracle.build_tree(oracle.drafter_lists(z, 1.0, k), B)
     oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
-    oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=0, tree=t)
+    return ref, oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=seed, tree=t)
 
 
-def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0):
+def agreement(ref, o, tree, out, t):
+    """The GPU's tree t and its TEV outputs against the oracle's, for the
+    benchmark line: (same tree structure, same exit/bonus/accepted length,
+    largest relative error of the exit masses; values below 1e-30 compared
+    absolutely)."""
+    import numpy as np
+    n = int(tree["n_nodes"][t])
+    same_tree = n == ref["n_nodes"] and \
+        np.array_equal(tree["parent"][t, :n].cpu().numpy(), ref["parent"][:n]) and \
+        np.array_equal(tree["token"][t, :n].cpu().numpy(), ref["token"][:n])
+    if not same_tree:
+        return False, None, None
+    same_draw = (int(out["exit_node"][t]), int(out["bonus_token"][t]), int(out["accept_len"][t])) == \
+        (o["exit_node"], o["bonus"], o["accept_len"])
+    w = out["exit_mass"][t, :n].double().cpu().numpy()
+    err = np.abs(w - o["w"]) / np.maximum(np.abs(o["w"]), 1e-30)
+    err[np.abs(o["w"]) < 1e-30] = np.abs(w - o["w"])[np.abs(o["w"]) < 1e-30]
+    return True, same_draw, float(err.max())
+
+
+def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0, out=None, seed=0):
     """The float64 oracle as it stands on the host, on a bounded sample of the
     same workload (whole rounds: drafter statistics, heap, mask, TEV): first
     single-threaded, then with one thread per host core over trees (the
     oracle's C code runs outside the interpreter lock).  About budget_s
-    seconds each."""
+    seconds each.  The single-threaded rounds use the timed step's last seed,
+    and their results are compared, outside the timing, with that step's GPU
+    outputs `out` on the same trees."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -800,15 +823,28 @@ def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0):
         n = int(tree["n_nodes"][t])
         inputs.append((drafter[t, 0].float().cpu().numpy(), target[t, :n].float().cpu().numpy()))
     done, spent = 0, 0.0
+    trees_same, draws_same, max_err = 0, 0, 0.0
     for t in range(nt):
         t0 = time.perf_counter()
-        oracle_round(oracle, *inputs[t], k, B, T, t)
+        ref, o = oracle_round(oracle, *inputs[t], k, B, T, t, seed=seed)
         spent += time.perf_counter() - t0
         done += 1
+        if out is not None:
+            same_tree, same_draw, err = agreement(ref, o, tree, out, t)
+            trees_same += same_tree
+            if same_tree:
+                draws_same += same_draw
+                max_err = max(max_err, err)
         if spent >= budget_s:
             break
     single = {"value": done / spent, "cores": 1,
               "sample": "%d of the %d trees of one step, %.1f s" % (done, nt, spent)}
+    agree = None
+    if out is not None:
+        agree = {"trees": done, "same_tree": trees_same, "same_exit_bonus_accept": draws_same,
+                 "max_rel_err_exit_mass": max_err,
+                 "note": "the oracle's float64 build and TEV of the first trees of the timed step's "
+                         "last call, with its seed, against the GPU's outputs"}
     nth = host_threads()
     n_rounds = max(nth, int(round(budget_s * single["value"] * nth)))
     with ThreadPoolExecutor(max_workers=nth) as pool:
@@ -818,7 +854,7 @@ def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0):
     return {"value": n_rounds / wall, "unit": "rounds/s", "cores": nth, "kind": "oracle",
             "sample": "%d rounds over the workload's %d trees (build + mask + TEV per tree), "
                       "float64, %d threads over trees, %.1f s wall" % (n_rounds, nt, nth, wall),
-            "single_thread": single}
+            "single_thread": single, "agreement_with_gpu": agree}
 
 
 # ---------------------------------------------------------------------------

@@ -36,5 +36,9 @@ def test_bench_prints_one_contract_line():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
+    ag = cb["agreement_with_gpu"]  # the oracle's rounds against the timed step's outputs
+    assert ag["trees"] >= 1 and ag["same_tree"] == ag["trees"], ag
+    assert ag["same_exit_bonus_accept"] >= ag["same_tree"] - 1, ag  # a CDF-boundary flip at most
+    assert ag["max_rel_err_exit_mass"] < 1e-5, ag
     assert d["gpu_launches"] == 8 * 3
     assert d["clocks"]["sm_max_mhz"] > 0
