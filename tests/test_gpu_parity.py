@@ -296,12 +296,15 @@ def test_tev_midsize(tsd, dev, orc, V, dtype, T):
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
-def test_tev_qwen_vocab_b64(tsd, dev, orc, T):
-    """The batch-1 Qwen-vocabulary round: V=151936, L=16, k=8, B=64, bf16."""
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_tev_qwen_vocab_b64(tsd, dev, orc, T, dtype):
+    """The batch-1 Qwen-vocabulary round: V=151936, L=16, k=8, B=64, target
+    logits in bf16 (38 chunks per row) and fp32 (75 chunks: the per-chunk
+    warp loops take three rounds)."""
     B = 64
     dr = synth.zipf_drafter(1, 16, V_Q, synth.seed_for(1), device="cpu")
     ref, _ = oracle_build(orc, dr[0], 8, B)
-    tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 1), B, torch.bfloat16)
+    tgt = _target_for(orc, ref, dr[0, 0], 1.5, synth.seed_for(1, 1), B, dtype)
     n = ref["n_nodes"]
     par = torch.tensor(ref["parent"][None], dtype=torch.int32, device=dev)
     tok = torch.tensor(ref["token"][None], dtype=torch.int32, device=dev)
