@@ -51,15 +51,35 @@ def measured_peaks():
         return HBM_PEAK_FALLBACK, "fallback"
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "rows_kernel_b256_traffic.json")
+ROWS_SOURCES = ("tree_speculative_decoding_position_gb300/csrc/k_rows.cu",
+                "tree_speculative_decoding_position_gb300/csrc/tsd_internal.cuh")
+
+
+def rows_source_digest() -> str:
+    """SHA-256 over the source files that define the node-row reduction."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ROWS_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def committed_traffic():
-    """Per-launch DRAM bytes of the node-row reduction from the committed ncu
-    summary (null when absent)."""
-    p = os.path.join(ROOT, "profiles", "rows_kernel_b256.md")
+    """Per-launch DRAM bytes (read + write) of the node-row reduction on the
+    workload's launch, from the ncu capture recorded in
+    profiles/rows_kernel_b256_traffic.json, and a note.  The figure is null
+    when no capture is recorded or when the kernel's sources have changed
+    since it was taken (the record carries their digest)."""
     try:
-        m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", open(p).read())
-        return float(m.group(1)) if m else None
-    except OSError:
-        return None
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no ncu capture recorded"
+    if rec.get("source_sha256") != rows_source_digest():
+        return None, "the kernel's sources changed since the recorded ncu capture"
+    return float(rec["dram_bytes_per_launch"]), rec.get("how", "")
 
 
 # ---------------------------------------------------------------------------
@@ -211,9 +231,10 @@ def run_ours(args):
 
     for i in range(args.warmup):
         step(i)
-    evsets = [new_events(7) for _ in range(args.steps)]
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    # the headline: K steps of the plain public calls, nothing recorded between
+    # their kernels
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -223,7 +244,7 @@ def run_ours(args):
     start.record(stream)
     last = None
     for i in range(args.steps):
-        last = step(1000 + i, evsets[i])
+        last = step(1000 + i)
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -232,7 +253,14 @@ def run_ours(args):
     total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     assert int((last[1]["status"] != 0).sum()) == 0, "a tree failed in the timed region"
 
-    # stage durations from the events inside each step
+    # the stage breakdown, from a second timed region of K steps in which TEV
+    # is the instrumented call (events recorded between its kernels)
+    evsets = [new_events(7) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(3000 + i, evsets[i])
+    torch.cuda.synchronize()
+
     def avg(a, b):
         return statistics.mean(evsets[i][a].elapsed_time(evsets[i][b]) for i in range(args.steps))
     stage = dict(build=avg(0, 1), tev_prep=avg(2, 3), tev_rows=avg(3, 4),
@@ -314,6 +342,7 @@ def run_ours(args):
 
     if rank != 0:
         return
+    traffic, traffic_note = committed_traffic()
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(drafter, target, last[0], k, B, T, out=last[1], seed=1000 + args.steps - 1)
@@ -323,10 +352,14 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": dict(W, parallelism="replicas: dp%d over trees" % world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": committed_traffic(),
+                     "frac": achieved / peak, "traffic": traffic,
                      "kernel": "rows_kernel (node-row reduction)",
                      "algorithmic_bytes_per_launch": rows_bytes,
-                     "peak_kind": peak_kind},
+                     "duration_ms": stage["tev_rows"],
+                     "duration_from": "CUDA events around the kernel on its stream, mean over a "
+                                      "second timed region of K steps with the instrumented TEV "
+                                      "call (the headline steps record nothing between kernels)",
+                     "traffic_note": traffic_note, "peak_kind": peak_kind},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 8 * args.steps,
         "clocks": clk, "extra": extra,
     }
@@ -776,33 +809,105 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-def oracle_round(oracle, z, tg, k, B, T, t, seed=0):
+def oracle_round(oracle, z, tg, k, B, T, t, seed=0, keep_lists=False):
     """One round of the workload in the float64 oracle: drafter statistics and
     heap, mask, TEV.  z: [L, V] drafter logits, tg: [n, V] target rows.
-    Returns the oracle's tree and TEV result."""
-    ref = oracle.build_tree(oracle.drafter_lists(z, 1.0, k), B)
+    Returns the oracle's tree and TEV result (and the drafter lists)."""
+    lists = oracle.drafter_lists(z, 1.0, k)
+    ref = oracle.build_tree(lists, B)
     oracle.tree_mask(ref["parent"], ref["n_nodes"], B, 1024)
-    return ref, oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=seed, tree=t)
+    o = oracle.tev(tg, ref["parent"], ref["token"], ref["n_nodes"], T, seed=seed, tree=t)
+    return (ref, o, lists) if keep_lists else (ref, o)
 
 
-def agreement(ref, o, tree, out, t):
-    """The GPU's tree t and its TEV outputs against the oracle's, for the
-    benchmark line: (same tree structure, same exit/bonus/accepted length,
-    largest relative error of the exit masses; values below 1e-30 compared
-    absolutely)."""
+SCORE_TOL = 1e-6   # builder order may differ only between prefixes this close (relative)
+FLIP_TOL = 1e-6    # a draw may differ only where the CDF is this close to u * total
+
+
+def _prefix_score(seq, lists):
+    """float64 score of a token sequence in the one-mode capped universe
+    (path sum of z / T_d minus the summed log-normalisers), None outside it."""
+    import numpy as np
+    z, c = 0.0, 0.0
+    for j, x in enumerate(seq):
+        hit = np.nonzero(lists["top_id"][0, j] == x)[0]
+        if hit.size == 0:
+            return None
+        z += lists["top_zt"][0, j, hit[0]]
+        c += lists["lse"][0, j]
+    return z - c
+
+
+def _sequences(parent, token, n):
+    seqs = [()]
+    for u in range(1, n):
+        seqs.append(seqs[int(parent[u])] + (int(token[u]),))
+    return seqs
+
+
+def builder_flips(ref, lists, par, tok, n):
+    """Node-by-node comparison of a GPU tree with the oracle's: the number of
+    positions whose prefixes differ, each allowed only between prefixes whose
+    float64 scores are within SCORE_TOL; None if any difference is not such a
+    near-tie (a builder error)."""
+    if n != ref["n_nodes"]:
+        return None
+    sg, so = _sequences(par, tok, n), _sequences(ref["parent"], ref["token"], n)
+    flips = 0
+    for a, b in zip(sg, so):
+        if a == b:
+            continue
+        sa, sb = _prefix_score(a, lists), _prefix_score(b, lists)
+        if sa is None or sb is None or abs(sa - sb) > SCORE_TOL * max(1.0, abs(sb)):
+            return None
+        flips += 1
+    return flips
+
+
+def _draw_flip(got, want, masses, u):
+    """0 if the two inverse-CDF draws agree, 1 if they differ only across a
+    CDF boundary within FLIP_TOL of u * total, None otherwise."""
+    import numpy as np
+    if got == want:
+        return 0
+    if got < 0 or want < 0:
+        return None
+    cum = np.cumsum(np.asarray(masses, dtype=np.float64))
+    lo, hi = min(got, want), max(got, want)
+    if hi >= cum.size:
+        return None
+    ok = abs(cum[lo] - u * cum[-1]) <= FLIP_TOL * cum[-1] and \
+        cum[hi - 1] - cum[lo] <= FLIP_TOL * cum[-1]
+    return 1 if ok else None
+
+
+def agreement(oracle, ref, lists, tg, tree, out, t, T, seed):
+    """The GPU's tree t and its TEV outputs against the float64 oracle, for
+    the benchmark line.  The builder: node by node, near-tie flips counted
+    (builder_flips).  TEV: the oracle's TEV on the GPU's own tree and target
+    rows, against the GPU's exit node, bonus token and accepted length (exact
+    up to counted near-boundary draw flips) and exit masses (largest relative
+    error; values below 1e-30 compared absolutely).  Returns a dict."""
     import numpy as np
     n = int(tree["n_nodes"][t])
-    same_tree = n == ref["n_nodes"] and \
-        np.array_equal(tree["parent"][t, :n].cpu().numpy(), ref["parent"][:n]) and \
-        np.array_equal(tree["token"][t, :n].cpu().numpy(), ref["token"][:n])
-    if not same_tree:
-        return False, None, None
-    same_draw = (int(out["exit_node"][t]), int(out["bonus_token"][t]), int(out["accept_len"][t])) == \
-        (o["exit_node"], o["bonus"], o["accept_len"])
+    par = tree["parent"][t, :n].cpu().numpy()
+    tok = tree["token"][t, :n].cpu().numpy()
+    bf = builder_flips(ref, lists, par, tok, n)
+    o = oracle.tev(tg[:n], par, tok, n, T, seed=seed, tree=t)
+    ex, by = int(out["exit_node"][t]), int(out["bonus_token"][t])
+    df = _draw_flip(ex, o["exit_node"], o["w"], o["u_exit"])
+    if df == 0:
+        p = oracle.row_probs(tg[ex].astype(np.float64), T)
+        p[[int(tok[u]) for u in range(1, n) if int(par[u]) == ex]] = 0.0
+        bflip = _draw_flip(by, o["bonus"], p, o["u_bonus"])
+        df = None if bflip is None else bflip
+        if df is not None and int(out["accept_len"][t]) != o["accept_len"]:
+            df = None
     w = out["exit_mass"][t, :n].double().cpu().numpy()
     err = np.abs(w - o["w"]) / np.maximum(np.abs(o["w"]), 1e-30)
-    err[np.abs(o["w"]) < 1e-30] = np.abs(w - o["w"])[np.abs(o["w"]) < 1e-30]
-    return True, same_draw, float(err.max())
+    small = np.abs(o["w"]) < 1e-30
+    err[small] = np.abs(w - o["w"])[small]
+    return {"builder_flips": bf, "draw_flips": df, "err": float(err.max())}
 
 
 def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0, out=None, seed=0):
@@ -823,28 +928,39 @@ def cpu_baseline(drafter, target, tree, k, B, T, budget_s=8.0, out=None, seed=0)
         n = int(tree["n_nodes"][t])
         inputs.append((drafter[t, 0].float().cpu().numpy(), target[t, :n].float().cpu().numpy()))
     done, spent = 0, 0.0
-    trees_same, draws_same, max_err = 0, 0, 0.0
+    same_tree, builder_err, flips_b, flips_d, draw_err, max_err = 0, 0, 0, 0, 0, 0.0
     for t in range(nt):
         t0 = time.perf_counter()
-        ref, o = oracle_round(oracle, *inputs[t], k, B, T, t, seed=seed)
+        ref, o, lists = oracle_round(oracle, *inputs[t], k, B, T, t, seed=seed, keep_lists=True)
         spent += time.perf_counter() - t0
         done += 1
-        if out is not None:
-            same_tree, same_draw, err = agreement(ref, o, tree, out, t)
-            trees_same += same_tree
-            if same_tree:
-                draws_same += same_draw
-                max_err = max(max_err, err)
-        if spent >= budget_s:
+        if out is not None:  # outside the timing
+            a = agreement(oracle, ref, lists, inputs[t][1], tree, out, t, T, seed)
+            if a["builder_flips"] is None:
+                builder_err += 1
+            else:
+                same_tree += a["builder_flips"] == 0
+                flips_b += a["builder_flips"]
+            if a["draw_flips"] is None:
+                draw_err += 1
+            else:
+                flips_d += a["draw_flips"]
+            max_err = max(max_err, a["err"])
+        if spent >= budget_s and done >= 2:
             break
     single = {"value": done / spent, "cores": 1,
               "sample": "%d of the %d trees of one step, %.1f s" % (done, nt, spent)}
     agree = None
     if out is not None:
-        agree = {"trees": done, "same_tree": trees_same, "same_exit_bonus_accept": draws_same,
+        agree = {"trees": done, "same_tree": same_tree, "builder_mismatch": builder_err,
+                 "builder_flips": flips_b, "draw_mismatch": draw_err, "draw_flips": flips_d,
                  "max_rel_err_exit_mass": max_err,
-                 "note": "the oracle's float64 build and TEV of the first trees of the timed step's "
-                         "last call, with its seed, against the GPU's outputs"}
+                 "note": "the first trees of the timed step's last call: the oracle's float64 "
+                         "build against the GPU's tree node by node (flips = positions that "
+                         "differ between prefixes whose oracle scores are within 1e-6), and the "
+                         "oracle's TEV on the GPU's tree with that call's seed against its "
+                         "outputs (flips = draws that differ across a CDF boundary within 1e-6 "
+                         "of u * total)"}
     nth = host_threads()
     n_rounds = max(nth, int(round(budget_s * single["value"] * nth)))
     with ThreadPoolExecutor(max_workers=nth) as pool:

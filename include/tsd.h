@@ -377,10 +377,15 @@ tsd_status tsd_exit_loss(const void *drafter_logits, tsd_dtype dtype, int n_tree
  *   tsd_workspace_size(TSD_OP_VERIFY_TEV, n_trees, 1, 1, V, 1, B, dtype)
  *   exceeds TSD_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 64 trees of B = 256 at
  *   V = 151936 fit); other argument errors as tsd_verify_tev.
- * - Set-up: the first call on a device (the current device, which must own
- *   `stream` and the pointers) looks up the device address of the static
- *   array once, with cudaGetSymbolAddress, and caches it; make that first
- *   call before any stream capture.  TSD_ERR_CUDA if the look-up fails.
+ * - Set-up: each call outside stream capture looks up the device address of
+ *   the static array on the current device (which must own `stream` and the
+ *   pointers) with cudaGetSymbolAddress and remembers it for that device; a
+ *   call whose stream is being captured uses the remembered address instead.
+ *   So make the first call on a device before any stream capture, and after
+ *   a cudaDeviceReset (which reloads the library's device code and makes the
+ *   remembered address stale) make the next call outside a capture.
+ *   TSD_ERR_CUDA if the look-up fails, or if a call under capture finds no
+ *   remembered address.
  * - Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents; nothing in it needs to start at zero.  Calls that overlap
  *   on the GPU (on different streams, or from several host threads without

@@ -11,7 +11,8 @@
  *   [EXIT]  "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
  *           Decoding" -- Sec. 3 Eq. 1-2 (p_v, P), Sec. 3.1 Eq. 4 (rho, w),
  *           Eq. 6 (target coverage), Eq. 7 (residual law), App. A.4.1
- *           (predraw-and-follow), App. B Algorithm 1 (TEV).
+ *           (predraw-and-follow), Sec. 3.1 Lemma 1 (the canonical exit
+ *           law that Tree Exit Verification samples).
  *   [CAST]  "CAST: Cost-Aware Speculative Trees from One-Pass Block Drafters"
  *           -- Sec. 2 Eq. 1 (plug-in score), Thm. 1 (tie order), App. C
  *           "Candidate construction" (top-K heap, push all K children) and
@@ -39,7 +40,8 @@
  *   - The sequential-residual and proposal-aware verifiers take a node's
  *     children in ascending token order; their decisions compare without
  *     dividing (u (1 - M) < p, u q~ < mu).
- *   - "Draw" (Alg. 1 lines 8-9) is inverse-CDF sampling: nodes in index
+ *   - The pages leave the two draws of TEV (exit node, bonus token)
+ *     unspecified beyond their laws; both are inverse-CDF sampling: nodes in index
  *     (build) order for the exit, token ids ascending (skipping the drafted
  *     children) for the bonus; strict '>' so zero-mass items are never drawn;
  *     the normaliser is the computed total, not 1.
@@ -444,7 +446,10 @@ static void orc_unmark_children(const int32_t *parent, const int32_t *token, int
 }
 
 /* ------------------------------------------------------------------------ */
-/* Tree Exit Verification [EXIT App. B Algorithm 1] on one tree.             */
+/* Tree Exit Verification on one tree: one draw from the canonical exit     */
+/* law [EXIT Sec. 3.1 Lemma 1] -- exit at node v with probability w(v) =     */
+/* P(v) rho(v) (Eq. 2, Eq. 4) -- then the bonus token from the residual law  */
+/* of the exit node (Eq. 7).                                                 */
 /*   z: [n][V] target logits, row v = node v.                                */
 /* Outputs (length n unless noted):                                          */
 /*   P      prefix probability, P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u)     */
@@ -467,9 +472,10 @@ int orc_tev(const double *z, const int32_t *parent, const int32_t *token, int n,
     double *p = (double *)malloc(sizeof(double) * (size_t)V);
     int32_t *mark = (int32_t *)calloc((size_t)V, sizeof(int32_t));
 
-    /* Alg. 1 lines 3-7: node-local quantities, then P by depth order.  Node
-     * indices are parent-before-child, so one pass in index order visits every
-     * parent before its children. */
+    /* The node-local quantities of Eq. 1 and Eq. 4 (p_v, rho(v)), the prefix
+     * probabilities of Eq. 2 and the exit masses w = P rho.  Node indices are
+     * parent-before-child, so one pass in index order visits every parent
+     * before its children. */
     P[0] = 1.0;
     pedge[0] = 1.0;
     for (int v = 0; v < n; ++v) {
@@ -493,7 +499,7 @@ int orc_tev(const double *z, const int32_t *parent, const int32_t *token, int n,
     for (int u = 1; u < n; ++u) cp += P[u];
     *coverage = cp;
 
-    /* Alg. 1 line 8: V ~ Categorical(w), inverse CDF in node order. */
+    /* The exit node: V ~ Categorical(w) [Lemma 1], inverse CDF in node order. */
     double wsum = 0.0;
     for (int v = 0; v < n; ++v) wsum += w[v];
     double u1 = orc_uniform(seed, tree, 0, 0);
@@ -508,7 +514,7 @@ int orc_tev(const double *z, const int32_t *parent, const int32_t *token, int n,
             if (w[v] > 0.0) { ex = v; break; }
     }
 
-    /* Alg. 1 line 9: Y ~ p_V at a leaf, else the residual law of Eq. 7
+    /* The bonus token: Y ~ p_V at a leaf, else the residual law of Eq. 7
      * (children's tokens removed, renormalised by rho(V)). */
     st = orc_row_probs(z + (int64_t)ex * V, V, T, p);
     double u2 = orc_uniform(seed, tree, 0, 1);

@@ -101,3 +101,65 @@ def check_draw(idx_gpu, idx_ref, masses, u, tol=FLIP_TOL):
     assert abs(cum[lo] - thr) <= tol * total, ("draw", idx_gpu, idx_ref, cum[lo], thr)
     assert masses[lo + 1:hi].sum() <= tol * total, ("draw skips mass", idx_gpu, idx_ref)
     return 1
+
+
+def to_np(t):
+    return t.detach().cpu().numpy()
+
+
+def tree_np(out, t=0):
+    """One tree of a tsd_build_tree result as numpy arrays."""
+    return {k: to_np(out[k][t]) for k in ("parent", "token", "depth", "score", "rank", "mode")} | \
+        {"n_nodes": int(out["n_nodes"][t])}
+
+
+def oracle_build(orc, drafter, k, B, temp=1.0):
+    """drafter: [K, L, V] torch (any float dtype) -> oracle tree + lists."""
+    z = drafter.float().cpu().numpy().astype(np.float64)
+    lists = orc.drafter_lists(z, temp, k)
+    return orc.build_tree(lists, B), lists
+
+
+def check_tev(out, t, o, tgt64, parent, token, n, T):
+    """One tree of a tsd_verify_tev result against the oracle's TEV `o` on the
+    same tree: masses within RTOL; exit node, bonus token and accepted length
+    exact up to counted near-boundary draw flips (returned)."""
+    import oracle
+    ok, err = close(to_np(out["exit_mass"][t])[:n], o["w"])
+    assert ok, ("w", err)
+    ok, err = close(to_np(out["prefix_prob"][t])[:n], o["P"])
+    assert ok, ("P", err)
+    ok, err = close(float(out["coverage"][t]), o["coverage"])
+    assert ok, ("C_p", err)
+    assert int(out["status"][t]) == 0
+    ex = int(out["exit_node"][t])
+    flips = check_draw(ex, o["exit_node"], o["w"], o["u_exit"])
+    if ex == o["exit_node"]:
+        p = oracle.row_probs(tgt64[ex], T)
+        kids = [int(token[u]) for u in range(1, n) if int(parent[u]) == ex]
+        p[kids] = 0.0
+        flips += check_draw(int(out["bonus_token"][t]), o["bonus"], p, o["u_bonus"])
+        assert int(out["accept_len"][t]) == o["accept_len"]
+    return flips
+
+
+def check_batch_valid(out, tree, T):
+    """Whole-launch validity of a TEV result on GPU-built trees: every tree's
+    status is ok, its exit masses sum to one, its exit node is a node, its
+    accepted length is the exit node's depth + 1, and its bonus token is not a
+    drafted child of the exit node (at T = 0 as well: the arg-max is then not a
+    child)."""
+    nt = int(tree["n_nodes"].shape[0])
+    st = to_np(out["status"])
+    assert st.tolist() == [0] * nt, st
+    w = to_np(out["exit_mass"]).astype(np.float64)
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-4), w.sum(axis=1)
+    nn = to_np(tree["n_nodes"])
+    par, tok, dep = to_np(tree["parent"]), to_np(tree["token"]), to_np(tree["depth"])
+    ex, bon, acc = to_np(out["exit_node"]), to_np(out["bonus_token"]), to_np(out["accept_len"])
+    for t in range(nt):
+        n = int(nn[t])
+        assert 0 <= ex[t] < n and w[t, ex[t]] > 0.0
+        assert acc[t] == dep[t, ex[t]] + 1
+        kids = tok[t, 1:n][par[t, 1:n] == ex[t]]
+        assert bon[t] >= 0 and bon[t] not in kids, (t, bon[t])

@@ -37,11 +37,14 @@ def test_bench_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
     ag = cb["agreement_with_gpu"]  # the oracle's rounds against the timed step's outputs
-    # the number of trees sampled follows the host's speed; a builder order flip
-    # between near-tied prefixes (counted, not failed, in the parity tests) may
-    # change one tree
-    assert ag["trees"] >= 1 and ag["same_tree"] >= ag["trees"] - 1, ag
-    assert ag["same_exit_bonus_accept"] >= ag["same_tree"] - 1, ag  # a CDF-boundary flip at most
+    # at least two trees are sampled; every difference from the oracle must be
+    # a counted near-tie (builder) or near-boundary (draw) flip, and flips stay
+    # rare
+    assert ag["trees"] >= 2, ag
+    assert ag["builder_mismatch"] == 0 and ag["draw_mismatch"] == 0, ag
+    assert ag["builder_flips"] <= 2 and ag["draw_flips"] <= 1, ag
     assert ag["max_rel_err_exit_mass"] < 1e-5, ag
+    rf_src = rf.get("duration_from", "")
+    assert "second timed region" in rf_src, rf
     assert d["gpu_launches"] == 8 * 3
     assert d["clocks"]["sm_max_mhz"] > 0

@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import RTOL, check_draw, close, compare_trees
+from gpu_helpers import check_draw, check_tev as _check_tev, compare_trees
+from gpu_helpers import oracle_build, to_np as _np, tree_np as _tree_np
 
 pytestmark = pytest.mark.gpu
 
@@ -33,22 +34,6 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _np(t):
-    return t.detach().cpu().numpy()
-
-
-def _tree_np(out, t=0):
-    return {k: _np(out[k][t]) for k in ("parent", "token", "depth", "score", "rank", "mode")} | \
-        {"n_nodes": int(out["n_nodes"][t])}
-
-
-def oracle_build(orc, drafter, k, B, temp=1.0):
-    """drafter: [K, L, V] torch (any float dtype) -> oracle tree + lists."""
-    z = drafter.float().cpu().numpy().astype(np.float64)
-    lists = orc.drafter_lists(z, temp, k)
-    return orc.build_tree(lists, B), lists
-
-
 # ---------------------------------------------------------------------------
 # builder
 # ---------------------------------------------------------------------------
@@ -68,15 +53,16 @@ def test_build_tiny(tsd, dev, orc, seed):
 
 @pytest.mark.parametrize("V,B,k,temp", [(12805, 64, 8, 1.0), (4096 * 3, 200, 8, 0.7),
                                          (1001, 40, 5, 1.0), (V_Q, 64, 8, 1.0)])
-def test_build_single_mode(tsd, dev, orc, V, B, k, temp):
+def test_build_single_mode(tsd, dev, orc, flip_log, V, B, k, temp):
     dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1), device="cpu")  # [1, 1, 16, V] bf16
     out = tsd.tsd_build_tree(dr.to(dev), topk=k, B=B, drafter_temp=temp)
     ref, lists = oracle_build(orc, dr[0], k, B, temp)
     flips = compare_trees(_tree_np(out), ref, lists)
+    flip_log("builder", flips)
     assert flips <= 2, flips
 
 
-def test_build_batched_b256(tsd, dev, orc):
+def test_build_batched_b256(tsd, dev, orc, flip_log):
     """The bench's launch: 32 trees, V=151936, L=16, top-k 8, B=256, one call;
     every tree prefix-closed with falling scores, four sampled trees against
     the oracle node by node."""
@@ -94,6 +80,7 @@ def test_build_batched_b256(tsd, dev, orc):
     for t in (0, 7, 19, 31):
         ref, lists = oracle_build(orc, dr[t].cpu(), 8, B)
         flips += compare_trees(_tree_np(out, t), ref, lists)
+    flip_log("builder", flips)
     assert flips <= 2, flips
 
 
@@ -108,7 +95,7 @@ def test_build_fp32_and_misaligned(tsd, dev, orc):
     assert compare_trees(_tree_np(out), ref, lists) <= 1
 
 
-def test_build_mixture(tsd, dev, orc):
+def test_build_mixture(tsd, dev, orc, flip_log):
     """K=8 modes from two latent futures (the mixture workload), B=128."""
     dr, _, _ = synth.mixture_drafter(2, 8, 16, V_Q, synth.seed_for(3), device="cpu")
     out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=128)
@@ -116,6 +103,7 @@ def test_build_mixture(tsd, dev, orc):
     for t in range(2):
         ref, lists = oracle_build(orc, dr[t], 8, 128)
         flips += compare_trees(_tree_np(out, t), ref, lists)
+    flip_log("builder", flips)
     assert flips <= 2
 
 
@@ -162,7 +150,7 @@ def test_tree_mask(tsd, dev, orc, B, P):
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
-def test_tev_and_mask_at_the_largest_budget(tsd, dev, orc, T):
+def test_tev_and_mask_at_the_largest_budget(tsd, dev, orc, flip_log, T):
     """B = TSD_MAX_B (4096 nodes per tree, the largest child-list sort and
     bit rows of 128 words): a random recursive tree (parent of u uniform
     below u), one ragged tree, bf16 target logits at V = 5000.  TEV against
@@ -192,6 +180,7 @@ def test_tev_and_mask_at_the_largest_budget(tsd, dev, orc, T):
         z64 = z[t, :n].float().numpy().astype(np.float64)
         o = orc.tev(z64, parent[t], token[t], n, T, seed=3, tree=t)
         flips += _check_tev(out, t, o, z64, parent[t], token[t], n, T)
+    flip_log("draw", flips)
     assert flips <= 1, flips
     m = tsd.tsd_tree_mask(pd, nd, prefix_len=77)
     for t in range(nt):
@@ -217,27 +206,6 @@ def _target_for(orc, tree, drafter_rows, sigma, seed, B, dtype):
     full = torch.zeros(B + 1, rows.shape[1], dtype=dtype)
     full[:n] = rows
     return full
-
-
-def _check_tev(out, t, o, tgt64, parent, token, n, T):
-    """One tree: masses within RTOL; exit/bonus exact up to counted flips."""
-    ok, err = close(_np(out["exit_mass"][t])[:n], o["w"])
-    assert ok, ("w", err)
-    ok, err = close(_np(out["prefix_prob"][t])[:n], o["P"])
-    assert ok, ("P", err)
-    ok, err = close(float(out["coverage"][t]), o["coverage"])
-    assert ok, ("C_p", err)
-    assert int(out["status"][t]) == 0
-    ex = int(out["exit_node"][t])
-    flips = check_draw(ex, o["exit_node"], o["w"], o["u_exit"])
-    if ex == o["exit_node"]:
-        import oracle
-        p = oracle.row_probs(tgt64[ex], T)
-        kids = [int(token[u]) for u in range(1, n) if int(parent[u]) == ex]
-        p[kids] = 0.0
-        flips += check_draw(int(out["bonus_token"][t]), o["bonus"], p, o["u_bonus"])
-        assert int(out["accept_len"][t]) == o["accept_len"]
-    return flips
 
 
 @pytest.mark.parametrize("T", [1.0, 0.6, 0.0])
@@ -268,7 +236,7 @@ def test_tev_tiny(tsd, dev, orc, T, seed):
 @pytest.mark.parametrize("V,dtype", [(12805, torch.bfloat16), (4096 * 2 + 100, torch.float32),
                                      (3001, torch.bfloat16)])
 @pytest.mark.parametrize("T", [1.0, 0.0])
-def test_tev_midsize(tsd, dev, orc, V, dtype, T):
+def test_tev_midsize(tsd, dev, orc, flip_log, V, dtype, T):
     """Several chunks and a ragged tail (V=3001 bf16 is not a multiple of 8:
     the generic path)."""
     B = 64
@@ -292,12 +260,13 @@ def test_tev_midsize(tsd, dev, orc, V, dtype, T):
                 p = orc.row_probs(z64[v], T)
                 flips += check_draw(int(d["draws"][0, v]), int(od["draws"][v]), p,
                                     orc.uniform(sd, 0, v, 2))
+    flip_log("draw", flips)
     assert flips <= 2, flips
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_tev_qwen_vocab_b64(tsd, dev, orc, T, dtype):
+def test_tev_qwen_vocab_b64(tsd, dev, orc, flip_log, T, dtype):
     """The batch-1 Qwen-vocabulary round: V=151936, L=16, k=8, B=64, target
     logits in bf16 (38 chunks per row) and fp32 (75 chunks: the per-chunk
     warp loops take three rounds)."""
@@ -315,10 +284,11 @@ def test_tev_qwen_vocab_b64(tsd, dev, orc, T, dtype):
         out = tsd.tsd_verify_tev(tgt[None].to(dev), par, tok, nn, T, seed=sd)
         o = orc.tev(z64[:n], ref["parent"], ref["token"], n, T, seed=sd)
         flips += _check_tev(out, 0, o, z64, ref["parent"], ref["token"], n, T)
+    flip_log("draw", flips)
     assert flips <= 1
 
 
-def test_tev_batched_b256(tsd, dev, orc):
+def test_tev_batched_b256(tsd, dev, orc, flip_log):
     """32 independent trees, V=151936, B=256, T=0.6, bf16: every tree checked
     for validity, four sampled trees against the oracle element by element."""
     nt, B, T = 32, 256, 0.6
@@ -348,6 +318,7 @@ def test_tev_batched_b256(tsd, dev, orc):
         z64 = tgt[t, :n].float().cpu().numpy().astype(np.float64)
         o = orc.tev(z64, par, tok, n, T, seed=123, tree=t)
         flips += _check_tev(out, t, o, z64, par, tok, n, T)
+    flip_log("draw", flips)
     assert flips <= 1
 
 
@@ -540,7 +511,7 @@ def test_tev_and_predraw_law_on_gpu(tsd, dev, orc):
         assert scipy.stats.chisquare(obs, ex * obs.sum() / ex.sum()).pvalue > 1e-4, fn.__name__
 
 
-def test_build_edge_budgets(tsd, dev, orc):
+def test_build_edge_budgets(tsd, dev, orc, flip_log):
     """B = 0 (the root alone); budgets whose search buffers spill from shared
     to global memory (8 modes at B = 512, one mode at the largest B); and rows
     of equal logits, where every token ties (the drafter kernel's exact
@@ -556,7 +527,7 @@ def test_build_edge_budgets(tsd, dev, orc):
     out = tsd.tsd_build_tree(dr.to(dev), topk=8, B=4095)
     ref, lists = oracle_build(orc, dr[0], 8, 4095)
     flips = compare_trees(_tree_np(out), ref, lists)  # each within SCORE_TOL
-    print("B=4095 order flips within tolerance:", flips)
+    flip_log("builder", flips)
     assert flips <= 2
     flat = torch.zeros(2, 1, 5, 9000)
     flat[1, 0, 2, 4444] = 1.0

@@ -591,7 +591,7 @@ def _numpy_uniform(seed, tree, node, stream):
 
 @pytest.mark.parametrize("T", [1.0, 0.6])
 def test_draws_are_inverse_cdf_of_the_stated_uniforms(orc, T):
-    """The reading of Alg. 1's two draws [EXIT App. B]: inverse CDF over nodes
+    """The reading of TEV's two draws [EXIT App. B]: inverse CDF over nodes
     in index order (exit) and over non-child token ids ascending (bonus), with
     the uniforms of the counter layout above.  Exit law and residual law come
     from brute force, the uniforms from numpy -- nothing from the oracle."""

@@ -5,13 +5,17 @@ cudaMalloc because cudaMalloc can synchronise the device).  Its scratch is a
 static array inside the library instead of a caller workspace.
 
 The test calls the entry point through the C ABI (ctypes, with PyTorch only
-holding the inputs and outputs) twice in a row -- the second call meets the
-first call's leftovers in the shared scratch -- and checks each result against
-tsd_verify_tev with a caller workspace, within the parity tests' tolerance.
-It lives in a file of its own that pytest collects last."""
+holding the inputs and outputs) three times in a row, and each call meets the
+previous call's leftovers in the shared scratch: a large launch (12 trees,
+B = 200, bf16), then a smaller one (3 trees, B = 16, fp32 logits, so every
+array of the scratch layout sits at another offset and the large call's data
+lies past the small call's extent), then the large launch again at another
+temperature.  Each result is checked against tsd_verify_tev with a freshly
+allocated workspace, within the parity tests' tolerance.  The file is named so
+that pytest collects it last.
+"""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -41,21 +45,26 @@ def _call_noalloc(lib, x, par, tok, nn, T, seed):
     return st, o
 
 
+def _case(tsd, dev, nt, B, V, dtype, cfg):
+    seeds = [synth.seed_for(cfg, 50 + t) for t in range(nt)]
+    dr = synth.zipf_drafter(nt, 16, V, 0, device=dev, seeds=seeds)
+    tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+    x = torch.zeros(nt, B + 1, V, dtype=dtype, device=dev)
+    for t in range(nt):
+        n = int(tr["n_nodes"][t])
+        synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=x[t, :n])
+    return x, tr
+
+
 def test_noalloc_matches_workspace_entry_point():
     import tree_speculative_decoding_position_gb300 as tsd
     from tree_speculative_decoding_position_gb300 import build
     build.build()
     lib = tsd.load()
     dev = torch.device("cuda:0")
-    nt, V, B = 4, 12805, 64
-    seeds = [synth.seed_for(1, 50 + t) for t in range(nt)]
-    dr = synth.zipf_drafter(nt, 16, V, 0, device=dev, seeds=seeds)
-    tr = tsd.tsd_build_tree(dr, topk=8, B=B)
-    x = torch.zeros(nt, B + 1, V, dtype=torch.bfloat16, device=dev)
-    for t in range(nt):
-        n = int(tr["n_nodes"][t])
-        synth.target_from_rows(dr[t, 0], tr["depth"][t, :n], 1.5, seeds[t] + 1, out=x[t, :n])
-    for call, (T, seed) in enumerate([(1.0, 77), (0.6, 78)]):
+    big = _case(tsd, dev, 12, 200, 12805, torch.bfloat16, 1)
+    small = _case(tsd, dev, 3, 16, 12805, torch.float32, 7)
+    for call, ((x, tr), T, seed) in enumerate([(big, 1.0, 77), (small, 0.6, 78), (big, 0.0, 79)]):
         st, got = _call_noalloc(lib, x, tr["parent"], tr["token"], tr["n_nodes"], T, seed)
         assert st == tsd.TSD_OK, (call, st)
         ref = tsd.tsd_verify_tev(x, tr["parent"], tr["token"], tr["n_nodes"], T, seed=seed)

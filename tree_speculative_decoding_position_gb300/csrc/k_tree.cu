@@ -2,14 +2,14 @@
 // predraw-and-follow check.
 //
 // TEV, "Where Draft Trees Lose Target Mass: Exit-Guided Speculative
-// Decoding", App. B Algorithm 1:
-//   lines 3-7  P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u) (Eq. 2), rho(v) from the
-//              row reduction, w(v) = P(v) rho(v) (Eq. 4), C_p (Eq. 6);
-//   line 8     V ~ Categorical(w): inverse CDF over node index;
-//   line 9     Y ~ p_V restricted to non-child tokens and renormalised (Eq. 7;
-//              p_V at a leaf), inverse CDF over token id: the chunk is found
-//              from the stored per-chunk residual sums, then only that chunk
-//              of row V is read again.
+// Decoding", Sec. 3.1 Lemma 1 (the canonical exit law) and App. B:
+//   prefix mass  P(root) = 1, P(u) = P(pa u) p_pa(u)(x_u) (Eq. 2), rho(v) from
+//                the row reduction, w(v) = P(v) rho(v) (Eq. 4), C_p (Eq. 6);
+//   exit draw    V ~ Categorical(w): inverse CDF over node index;
+//   bonus draw   Y ~ p_V restricted to non-child tokens and renormalised (Eq. 7;
+//                p_V at a leaf), inverse CDF over token id: the chunk is found
+//                from the stored per-chunk residual sums, then only that chunk
+//                of row V is read again.
 // Predraw-and-follow (same page, Sec. 2 and App. A.4.1): R_v ~ p_v at every
 // node, then a walk from the root into the child whose token is R_v.
 #include "tsd_internal.cuh"
@@ -104,9 +104,9 @@ __device__ int residual_draw_block(const T* __restrict__ logits, int t, int V_, 
     const NodeStat ns = ws.node[row];
     int y;
     if (greedy) {
-        y = ns.amax;  // Line 9 at T = 0: the arg-max is not a child of the exit node
+        y = ns.amax;  // T = 0: the arg-max, which is not a child of the exit node
     } else {
-        // Line 9: residual draw.  Chunk sums relative to the row reference.
+        // Residual draw (Eq. 7).  Chunk sums relative to the row reference.
         const ChunkStat* cs = ws.chunk + row * nch;
         const float thr2 = u * ns.r;
         constexpr int CE = kChunkBytes / (int)sizeof(T);
@@ -225,7 +225,7 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
         pedge[u] = gpedge[u];
     }
     __syncthreads();
-    // Alg. 1 lines 3-7: P(u) as the product of the edge probabilities on the
+    // Eq. 2: P(u) as the product of the edge probabilities on the
     // root path (depth-parallel: every node walks its own ancestors).
     float cov_part = 0.0f;
     for (int u = threadIdx.x; u < stride; u += blockDim.x) {
@@ -248,7 +248,7 @@ tev_tree_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c
     }
     float cov;
     block_excl_scan(cov_part, red, &cov);
-    // Line 8: inverse CDF over nodes.  Each thread owns a contiguous run of
+    // Exit draw: inverse CDF over nodes.  Each thread owns a contiguous run of
     // nodes so that the block scan follows node order.
     const int per = (n + blockDim.x - 1) / blockDim.x;
     const int nb = threadIdx.x * per, ne = min(n, nb + per);
