@@ -53,6 +53,7 @@ def measured_peaks():
 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "rows_kernel_b256_traffic.json")
 ROWS_SOURCES = ("tree_speculative_decoding_position_gb300/csrc/k_rows.cu",
+                "tree_speculative_decoding_position_gb300/csrc/chunk_reduce.cuh",
                 "tree_speculative_decoding_position_gb300/csrc/tsd_internal.cuh")
 
 

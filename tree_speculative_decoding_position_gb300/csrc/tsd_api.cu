@@ -5,6 +5,7 @@
 
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "tsd_internal.cuh"
@@ -13,13 +14,15 @@ namespace tsd {
 
 int resident_grid(const void* kernel, int threads, size_t smem, int64_t want) {
     static std::mutex mu;
-    static std::map<std::pair<int, const void*>, std::pair<int, int>> cache;  // -> (SMs, CTAs/SM)
+    // (device, kernel, block size, dynamic shared memory) -> (SMs, CTAs per SM)
+    static std::map<std::tuple<int, const void*, int, size_t>, std::pair<int, int>> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     std::pair<int, int> r;
     {
         std::lock_guard<std::mutex> lock(mu);
-        auto it = cache.find({dev, kernel});
+        const auto key = std::make_tuple(dev, kernel, threads, smem);
+        auto it = cache.find(key);
         if (it == cache.end()) {
             int sms = 0, per = 0;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -29,7 +32,7 @@ int resident_grid(const void* kernel, int threads, size_t smem, int64_t want) {
                     cudaSuccess ||
                 per < 1)
                 per = 1;
-            it = cache.emplace(std::make_pair(dev, kernel), std::make_pair(sms, per)).first;
+            it = cache.emplace(key, std::make_pair(sms, per)).first;
         }
         r = it->second;
     }
@@ -38,6 +41,21 @@ int resident_grid(const void* kernel, int threads, size_t smem, int64_t want) {
 }
 
 size_t heap_spill_bytes(int n_modes, int L, int topk, int B);  // k_heap.cu
+
+// Which launches of Tree Exit Verification run the two-kernel path
+// (k_tev_fused.cu), given its layout conditions (B <= 128 among them): every
+// launch with B <= TSD_FUSED_ANY_SIZE_MAX_B (64), and launches of at most
+// TSD_FUSED_MAX_ITEMS (node row, 8 KB chunk) items above that.  Measured on the V = 151936 grid: at B <= 64
+// the two-kernel path was as fast or faster from 1 to 256 trees; at B = 128
+// it was faster for one tree and 5-14% slower from 16 trees up (each tree's
+// finish block then has more rows to combine than the batched combine
+// kernel spreads over the GPU).  A build may set both bounds to compare paths.
+#ifndef TSD_FUSED_MAX_ITEMS
+#define TSD_FUSED_MAX_ITEMS 32768
+#endif
+#ifndef TSD_FUSED_ANY_SIZE_MAX_B
+#define TSD_FUSED_ANY_SIZE_MAX_B 64
+#endif
 
 namespace {
 
@@ -206,7 +224,7 @@ unsigned tsd_debug_check_failures(void) {
     cudaDeviceSynchronize();
 #endif
     return checks_rows() | checks_tree() | checks_heap() | checks_mask() | checks_drafter() |
-           checks_lse() | checks_forest() | checks_exit();
+           checks_lse() | checks_forest() | checks_exit() | checks_fused();
 }
 
 const char* tsd_status_string(tsd_status s) {
@@ -360,6 +378,19 @@ static tsd_status verify_tev_impl(const void* target_logits, tsd_dtype dtype,
     const bool greedy = temperature == 0.0f;
     const float c = greedy ? 1.0f : exp2_scale(temperature);
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+    if (tev_fused_fits(target_logits, dtype, n_trees, B, V) &&
+        (B <= TSD_FUSED_ANY_SIZE_MAX_B ||
+         (int64_t)n_trees * (B + 1) * n_chunks(V, es) <= TSD_FUSED_MAX_ITEMS)) {
+        // a launch of a few waves of row chunks: the two-kernel path
+        if (mark(0) != cudaSuccess || mark(1) != cudaSuccess ||
+            launch_tev_fused(target_logits, dtype, n_trees, B, V, c, greedy, seed, parent, token,
+                             n_nodes, ws, exit_node, bonus_token, accept_len, exit_mass,
+                             prefix_prob, coverage, status, stream,
+                             ev ? ev[2] : nullptr) != cudaSuccess ||
+            mark(3) != cudaSuccess || mark(4) != cudaSuccess)
+            return TSD_ERR_CUDA;
+        return TSD_OK;
+    }
     if (mark(0) != cudaSuccess ||
         launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
         mark(1) != cudaSuccess ||

@@ -65,6 +65,7 @@ unsigned checks_drafter();
 unsigned checks_lse();
 unsigned checks_forest();
 unsigned checks_exit();
+unsigned checks_fused();
 
 // A logits row is processed in chunks of 8 KB (4096 bf16 or 2048 fp32
 // tokens); one warp reduces one chunk with sixteen 16-byte loads per lane.
@@ -148,13 +149,25 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of this library is launched
 // with programmatic stream serialization (launch_pdl below): it may be
-// scheduled while the previous kernel in the stream is still finishing, and
-// its first statement is pdl_entry(), which lets the next kernel be scheduled
-// as early and then waits until the previous kernel has completed and its
-// memory is visible.  No global memory is touched before that wait, so the
-// stream's ordering is unchanged; only launch latency is hidden.
+// scheduled while the previous kernel in the stream is still finishing.  Its
+// first statement is pdl_entry(), which waits until the previous kernel has
+// completed and its memory is visible, and then lets the next kernel be
+// scheduled.  No global memory is touched before that wait, so the stream's
+// ordering is unchanged; only launch latency is hidden, one kernel ahead.
+// (Letting the next kernel be scheduled before the wait instead hides a
+// little more latency for a pair of kernels timed alone, but in a chain such
+// as build, mask and verify, grids launched two or three kernels ahead sat on
+// the SMs and slowed the whole step by about a tenth: measured 0.525 against
+// 0.476 ms for the 32-tree B = 256 step.)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_entry() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// The variant that lets the next kernel be scheduled first: for a kernel
+// whose dependent is a handful of blocks that should already be resident
+// when it completes (the per-tree finish of the small-launch verifier).
+__device__ __forceinline__ void pdl_entry_early() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -359,6 +372,20 @@ cudaError_t launch_tev_tree(const void* logits, tsd_dtype dtype, int n_trees, in
                             int32_t* bonus, int32_t* accept_len, float* exit_mass,
                             float* prefix_prob, float* coverage, int32_t* status,
                             cudaStream_t stream);
+// The two-kernel verifier of small launches (k_tev_fused.cu): a streaming
+// row kernel that finds each row's children itself, then one block per tree.
+// Usable when the logits rows are 16-byte aligned with V a multiple of the
+// vector width, B <= kFusedMaxB (above it the batched chain is faster,
+// measured) and a row has at most 128 chunks.  The event
+// ev_between, if given, is recorded between its two kernels.
+constexpr int kFusedMaxB = 128;
+bool tev_fused_fits(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V);
+cudaError_t launch_tev_fused(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
+                             float c, bool greedy, uint64_t seed, const int32_t* parent,
+                             const int32_t* token, const int32_t* n_nodes, const VerifyWs& ws,
+                             int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
+                             float* exit_mass, float* prefix_prob, float* coverage,
+                             int32_t* status, cudaStream_t stream, cudaEvent_t ev_between);
 cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
                            float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
                            const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
