@@ -549,8 +549,10 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
     ms = s.elapsed_time(e) / 48
     rows_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
     out["b64_single_tree"] = {"tev_rounds_per_s": 1000.0 / ms, "tev_ms": ms,
-                              "rows_kernel_ms": rows_ms,
-                              "rows_kernel_gbs": n * V * 2 / (rows_ms * 1e-3) / 1e9}
+                              "row_reduction_ms": rows_ms,
+                              "row_reduction_gbs": n * V * 2 / (rows_ms * 1e-3) / 1e9,
+                              "row_reduction_kernel": "tev_stream_kernel (a launch this small "
+                                                      "takes the two-kernel path)"}
     # the same round, greedy (T = 0)
     s.record(stream)
     for i in range(48):
@@ -621,6 +623,7 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
                 lat.append(a.elapsed_time(b))
         out["b64_single_tree"]["verify_graph_ms_" + name] = statistics.median(lat)
         del graph
+    out["batch1_tev_vs_predraw"] = batch1_grid(tsd, torch, synth, dev, stream, flush, cap, V)
     # the oracle beside it: the same round, float64, one host thread
     z1 = dr[0, 0].float().cpu().numpy()
     tg1 = copies[0][0, :n].float().cpu().numpy()
@@ -713,6 +716,69 @@ def secondary(tsd, torch, synth, dev, stream, tree, target, T, ws_v, V):
         oracle_ms_per_tree=oracle_ms(lambda orc: orc.lse_tree(zm, 1.0, 8, B_m)),
         oracle_sample="tree 0 of the 16 (K=8, L=16, B=128), float64, one host thread")
     return out
+
+
+# [EXIT] App. D.1: verifier-stage latency reductions of TEV against
+# predraw-and-follow at batch 1 (H20, Qwen3-4B target), context only
+PAGES_TEV_VS_PREDRAW = {0.6: {32: -12.9, 64: -15.2, 128: -24.3}, 1.0: {32: -12.0, 64: -14.0, 128: -17.1}}
+
+
+def graph_latency(torch, stream, flush, cap, fn, reps=40):
+    """Median (and best) latency of fn captured in a CUDA graph and replayed,
+    L2 flushed before every replay; CUDA events on the launching stream."""
+    with torch.cuda.stream(cap):
+        for i in range(3):
+            fn()
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    lat = []
+    for i in range(reps + 5):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            lat.append(a.elapsed_time(b))
+    del graph
+    return statistics.median(lat), min(lat)
+
+
+def batch1_grid(tsd, torch, synth, dev, stream, flush, cap, V):
+    """The pages' batch-1 comparison ([EXIT] App. D.1): the verifier stage of
+    TEV against predraw-and-follow on one tree, B in {32, 64, 128} x T in
+    {0.6, 1.0}, each call captured in a CUDA graph and replayed with L2
+    flushed first.  Both verifiers share the row reduction; they differ in
+    the draws (one exit draw and one bonus draw, against a draw at every
+    node)."""
+    rows = []
+    for B in (32, 64, 128):
+        dr = synth.zipf_drafter(1, 16, V, synth.seed_for(1, 300 + B), device=dev)
+        tr = tsd.tsd_build_tree(dr, topk=8, B=B)
+        n = int(tr["n_nodes"][0])
+        x = torch.zeros(1, B + 1, V, dtype=torch.bfloat16, device=dev)
+        synth.target_from_rows(dr[0, 0], tr["depth"][0, :n], 1.5, synth.seed_for(1, 400 + B),
+                               out=x[0, :n])
+        ws = torch.empty(tsd.tsd_workspace_size(tsd.TSD_OP_VERIFY_TEV, 1, 1, 1, V, 1, B,
+                                                torch.bfloat16), dtype=torch.uint8, device=dev)
+        for T in (0.6, 1.0):
+            tev = graph_latency(torch, stream, flush, cap, lambda: tsd.tsd_verify_tev(
+                x, tr["parent"], tr["token"], tr["n_nodes"], T, seed=1, workspace=ws))
+            pre = graph_latency(torch, stream, flush, cap, lambda: tsd.tsd_verify_ddtree(
+                x, tr["parent"], tr["token"], tr["n_nodes"], T, seed=1, workspace=ws))
+            rows.append({"B": B, "T": T, "tev_ms": tev[0], "tev_ms_best": tev[1],
+                         "predraw_ms": pre[0], "predraw_ms_best": pre[1],
+                         "tev_vs_predraw_pct": 100.0 * (tev[0] / pre[0] - 1.0),
+                         "pages_pct_h20": PAGES_TEV_VS_PREDRAW[T][B],
+                         "logits_mb": n * V * 2 / 1e6})
+        del x, ws, tr, dr
+    return {"points": rows,
+            "how": "one tree, V=151936 bf16, CUDA graph replay with L2 flushed before each, "
+                   "median of 40; pages_pct_h20 is [EXIT] App. D.1 on an H20 (context only)"}
 
 
 def run_sweep(args):

@@ -178,6 +178,11 @@ tsd_status tsd_tree_mask(const int32_t *parent, const int32_t *n_nodes, int n_tr
  *                          failed tree gets exit_node = bonus = -1,
  *                          accept_len = 0.
  * The accepted path is the parent chain of exit_node.
+ * Two internal paths give the same results: launches with B <= 64 (and other
+ * launches of at most 32768 row chunks with B <= 128), with 16-byte aligned
+ * rows and V a multiple of 8 (bf16) or 4 (fp32), run as two kernels (a
+ * streaming row kernel, then one block per tree); the rest run as the
+ * batched chain of four kernels.
  */
 tsd_status tsd_verify_tev(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
                           const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
@@ -188,13 +193,15 @@ tsd_status tsd_verify_tev(const void *target_logits, tsd_dtype dtype, const int3
 
 /*
  * tsd_verify_tev_timed -- tsd_verify_tev that also records five caller-created
- * CUDA events on `stream` around its four kernels, for measuring each stage
- * with cudaEventElapsedTime: stage_events[0] before the tree preparation,
- * [1] before the node-row reduction (Algorithm 1's node-local reductions over
- * the logits), [2] after it, [3] after the per-node combination, [4] after the
- * exit and bonus draws.  Same arguments, outputs and errors as
- * tsd_verify_tev; TSD_ERR_INVALID_ARG if stage_events or one of its five
- * entries is null.
+ * CUDA events on `stream` around its kernels, for measuring each stage with
+ * cudaEventElapsedTime.  On the batched path: stage_events[0] before the tree
+ * preparation, [1] before the node-row reduction (the node-local reductions
+ * over the logits), [2] after it, [3] after the per-node combination, [4]
+ * after the exit and bonus draws.  On the two-kernel path of small launches
+ * (see tsd_verify_tev): [0] and [1] before the streaming row kernel, [2]
+ * after it, [3] and [4] after the per-tree kernel.  Same arguments, outputs
+ * and errors as tsd_verify_tev; TSD_ERR_INVALID_ARG if stage_events or one of
+ * its five entries is null.
  */
 tsd_status tsd_verify_tev_timed(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
                                 const int32_t *token, const int32_t *n_nodes, int n_trees, int B,
@@ -212,6 +219,8 @@ tsd_status tsd_verify_tev_timed(const void *target_logits, tsd_dtype dtype, cons
  * at the first node without one, returning R_v as the bonus token.
  * Inputs as tsd_verify_tev.  Outputs: exit_node, bonus_token, accept_len
  * [n_trees]; draws nullable [n_trees][B+1] (R_v; -1 past n_nodes); status.
+ * Small launches take the same two-kernel path as tsd_verify_tev (the same
+ * streaming row kernel, then one block per tree drawing at every node).
  */
 tsd_status tsd_verify_ddtree(const void *target_logits, tsd_dtype dtype, const int32_t *parent,
                              const int32_t *token, const int32_t *n_nodes, int n_trees, int B,

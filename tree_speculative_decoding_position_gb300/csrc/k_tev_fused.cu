@@ -98,7 +98,7 @@ template <typename T, bool GREEDY>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 tev_stream_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch, float c,
                   const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
-                  const int32_t* __restrict__ n_nodes, VerifyWs ws) {
+                  const int32_t* __restrict__ n_nodes, VerifyWs ws, bool capture) {
     pdl_entry_early();  // the per-tree finish blocks become resident now
     constexpr int CE = kChunkBytes / (int)sizeof(T);
     const int lane = threadIdx.x & (kWarp - 1);
@@ -134,11 +134,11 @@ tev_stream_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, i
         const int t = p.t, v = p.v;
         ExclMask<T> excl;
         bool kids, dup;
-        // T > 0: the children's logits go to ws.pedge, where the finish
-        // kernel turns them into edge probabilities
+        // TEV at T > 0 (capture): the children's logits go to ws.pedge,
+        // where the finish kernel turns them into edge probabilities
         mark_tree_children<T>(parent + (int64_t)t * R, token + (int64_t)t * R,
                               fused_rows(__ldg(n_nodes + t), B), v, c0, cn, lane, excl, kids, dup,
-                              rp, GREEDY ? nullptr : ws.pedge + (int64_t)t * R);
+                              rp, (GREEDY || !capture) ? nullptr : ws.pedge + (int64_t)t * R);
         const LanePart lp = chunk_lane_marked<T, GREEDY>(buf, cn, c, excl, kids, c0, lane);
         const int64_t done = p.item;
         do {
@@ -188,50 +188,59 @@ __host__ __device__ inline size_t fused_finish_smem(int B, int nch, bool greedy)
     return R * 32 + 16 + (greedy ? 0 : R * (size_t)nch * 8);
 }
 
-// One block per tree, in two phases.
-//  1. Every load at once: thread u reads node u's parent, token and (T > 0)
-//     logit; each warp reads the chunk statistics of its rows, G rows at a
-//     time, and reduces each row (its maximum and sums relative to the row's
-//     reference, or its arg-max at T = 0) into shared memory.
-//  2. From shared memory, by the whole block: validation; p_pa(u)(x_u) from
-//     the parent row's statistics and the child's logit (Eq. 1); rho (Eq. 4,
-//     the residual sum over the row sum); P along the root path (Eq. 2);
-//     w = P rho (Eq. 4); C_p (Eq. 6); the exit draw by inverse CDF over node
-//     index; the bonus draw by inverse CDF over the exit row's residual
-//     (Eq. 7): the chunk from the staged chunk sums, then that chunk alone is
-//     read again, one 16-byte vector per thread.  (Done by one warp instead,
-//     this phase took longer: a lone warp's chain of dependent steps cannot
-//     hide its own latencies.)
-template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(kFinishThreads)
-tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, uint64_t seed,
-                  const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
-                  const int32_t* __restrict__ n_nodes, VerifyWs ws, int32_t* __restrict__ exit_node,
-                  int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
-                  float* __restrict__ exit_mass, float* __restrict__ prefix_prob,
-                  float* __restrict__ coverage, int32_t* __restrict__ status) {
-    pdl_entry();
-    constexpr int CE = kChunkBytes / (int)sizeof(T);
-    constexpr int VEC = Lanes<T>::kVec;
-    extern __shared__ float4 finish_smem[];
-    __shared__ int flags;  // bit 0: malformed tree, bit 1: a row without mass
-    const int t = blockIdx.x;
+// Shared memory layout of a finish block (pointers into the dynamic array).
+struct FinishSmem {
+    float* Mc;    // [R] row reference mc (T = 0: arg-max bits)
+    float* Sv;    // [R] row sum S
+    float* Rv;    // [R] row residual sum (T = 0: rho)
+    float* Dv;    // [R] the child's logit, then p_pa(u)(x_u)
+    float* Pv;    // [R] P
+    float* Wv;    // [R] w (predraw: the draws)
+    int32_t* tk;  // [R] tokens
+    int16_t* pa;  // [R] parents
+    float2* cm;   // [R][nch] (chunk maximum, chunk residual sum; predraw: chunk sum)
+};
+__device__ __forceinline__ FinishSmem finish_smem_layout(void* base, int R) {
+    FinishSmem f;
+    f.Mc = reinterpret_cast<float*>(base);
+    f.Sv = f.Mc + R;
+    f.Rv = f.Sv + R;
+    f.Dv = f.Rv + R;
+    f.Pv = f.Dv + R;
+    f.Wv = f.Pv + R;
+    f.tk = reinterpret_cast<int32_t*>(f.Wv + R);
+    f.pa = reinterpret_cast<int16_t*>(f.tk + R);
+    f.cm = reinterpret_cast<float2*>(base) + ((size_t)R * 32 + 16) / 8;
+    return f;
+}
+
+// Phase 1 of a finish block, every load at once: thread u reads node u's
+// parent, token and (T > 0, TEV) logit; each warp reads the chunk statistics
+// of its rows, G rows at a time, and reduces each row (its maximum and sums
+// relative to the row's reference, or its arg-max at T = 0) into shared
+// memory, with each chunk's maximum and residual sum (PRED: its sum).  flags
+// gets bit 0 for a malformed tree, bit 1 for a row without mass.  Returns
+// the number of live nodes; ends with a block barrier.
+template <typename T, bool GREEDY, bool PRED>
+__device__ __forceinline__ int finish_stage(int t, int B, int64_t V, int nch, float c,
+                                            const int32_t* __restrict__ parent,
+                                            const int32_t* __restrict__ token,
+                                            const int32_t* __restrict__ n_nodes,
+                                            const VerifyWs& ws, const FinishSmem& f, int* flags) {
     const int R = B + 1;
     const int lane = threadIdx.x & (kWarp - 1), wid = threadIdx.x / kWarp;
     const int nw = blockDim.x / kWarp;
-    float* Mc = reinterpret_cast<float*>(finish_smem);  // row reference mc (T = 0: arg-max bits)
-    float* Sv = Mc + R;   // row sum S
-    float* Rv = Sv + R;   // row residual sum (T = 0: rho)
-    float* Dv = Rv + R;   // the child's logit, then p_pa(u)(x_u)
-    float* Pv = Dv + R;   // P
-    float* Wv = Pv + R;   // w
-    int32_t* tk = reinterpret_cast<int32_t*>(Wv + R);
-    int16_t* pa = reinterpret_cast<int16_t*>(tk + R);
-    float2* cmr = reinterpret_cast<float2*>(finish_smem) + (R * 32 + 16) / 8;  // [R][nch] (m, r)
+    float* Mc = f.Mc;
+    float* Sv = f.Sv;
+    float* Rv = f.Rv;
+    float* Dv = f.Dv;
+    int32_t* tk = f.tk;
+    int16_t* pa = f.pa;
+    float2* cmr = f.cm;
     const int n_raw = n_nodes[t];
     const bool n_ok = n_raw >= 1 && n_raw <= R;
     const int n = n_ok ? n_raw : 1;
-    if (threadIdx.x == 0) flags = n_ok ? 0 : 1;
+    if (threadIdx.x == 0) *flags = n_ok ? 0 : 1;
     __syncthreads();
     // ---- phase 1: all loads ------------------------------------------------
     {
@@ -241,7 +250,7 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
         if (u < n) {
             p = parent[(int64_t)t * R + u];
             x = token[(int64_t)t * R + u];
-            if (!GREEDY && u > 0) z = ws.pedge[(int64_t)t * R + u];
+            if (!GREEDY && !PRED && u > 0) z = ws.pedge[(int64_t)t * R + u];
         }
         constexpr int G = 4;   // rows per round of a warp
         constexpr int KL = 2;  // chunks per lane and row (rows of at most 64 chunks)
@@ -289,7 +298,7 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
                         r += xs[k].r * f;
                     }
                     const int q = q0 + k * kWarp;
-                    if (q < nch) cmr[(size_t)v * nch + q] = make_float2(xs[k].m, xs[k].r);
+                    if (q < nch) cmr[(size_t)v * nch + q] = make_float2(xs[k].m, PRED ? xs[k].s : xs[k].r);
                 }
                 sm = warp_sum(sm);
                 r = warp_sum(r);
@@ -302,7 +311,7 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
             }
             bad = __any_sync(0xffffffffu, bad);
             dup = __any_sync(0xffffffffu, dup);
-            if (lane == 0 && (bad || dup)) atomicOr(&flags, (dup ? 1 : 0) | (bad ? 2 : 0));
+            if (lane == 0 && (bad || dup)) atomicOr(flags, (dup ? 1 : 0) | (bad ? 2 : 0));
         };
         if (nch <= KL * kWarp) {
             for (int v0 = wid * G; v0 < n; v0 += nw * G) {
@@ -327,13 +336,57 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
             bool bad;
             if (u == 0) bad = p != -1;
             else bad = p < 0 || p >= u || x < 0 || (int64_t)x >= V;
-            if (bad) atomicOr(&flags, 1);
+            if (bad) atomicOr(flags, 1);
             pa[u] = (int16_t)(u == 0 ? -1 : (p >= 0 && p < u ? p : 0));
             tk[u] = x;
             Dv[u] = z;
         }
     }
     __syncthreads();
+    return n;
+}
+
+// One block per tree, in two phases.
+//  1. Every load at once: thread u reads node u's parent, token and (T > 0)
+//     logit; each warp reads the chunk statistics of its rows, G rows at a
+//     time, and reduces each row (its maximum and sums relative to the row's
+//     reference, or its arg-max at T = 0) into shared memory.
+//  2. From shared memory, by the whole block: validation; p_pa(u)(x_u) from
+//     the parent row's statistics and the child's logit (Eq. 1); rho (Eq. 4,
+//     the residual sum over the row sum); P along the root path (Eq. 2);
+//     w = P rho (Eq. 4); C_p (Eq. 6); the exit draw by inverse CDF over node
+//     index; the bonus draw by inverse CDF over the exit row's residual
+//     (Eq. 7): the chunk from the staged chunk sums, then that chunk alone is
+//     read again, one 16-byte vector per thread.  (Done by one warp instead,
+//     this phase took longer: a lone warp's chain of dependent steps cannot
+//     hide its own latencies.)
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kFinishThreads)
+tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float c, uint64_t seed,
+                  const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
+                  const int32_t* __restrict__ n_nodes, VerifyWs ws, int32_t* __restrict__ exit_node,
+                  int32_t* __restrict__ bonus, int32_t* __restrict__ accept_len,
+                  float* __restrict__ exit_mass, float* __restrict__ prefix_prob,
+                  float* __restrict__ coverage, int32_t* __restrict__ status) {
+    pdl_entry();
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    constexpr int VEC = Lanes<T>::kVec;
+    extern __shared__ float4 finish_smem[];
+    __shared__ int flags;  // bit 0: malformed tree, bit 1: a row without mass
+    const int t = blockIdx.x;
+    const int R = B + 1;
+    const int lane = threadIdx.x & (kWarp - 1), wid = threadIdx.x / kWarp;
+    const FinishSmem f = finish_smem_layout(finish_smem, R);
+    float* Mc = f.Mc;
+    float* Sv = f.Sv;
+    float* Rv = f.Rv;
+    float* Dv = f.Dv;
+    float* Wv = f.Wv;
+    int32_t* tk = f.tk;
+    int16_t* pa = f.pa;
+    const float2* cmr = f.cm;
+    const int n = finish_stage<T, GREEDY, false>(t, B, V, nch, c, parent, token, n_nodes, ws, f,
+                                                 &flags);
     // ---- phase 2: from shared memory, the whole block ----------------------
     const int fl = flags;
     const int st = (fl & 1) ? kStatBadTree : ((fl & 2) ? kStatNonFinite : kStatOk);
@@ -528,6 +581,259 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
     }
 }
 
+// Predraw-and-follow on the small-launch path ([EXIT] Sec. 2 and App. A.4.1),
+// kept as the equivalence check of TEV.  After the same streaming kernel:
+//   predraw_nodes_fused_kernel  a warp per node: the row's maximum and sum
+//                               from its chunk statistics, then R_v ~ p_v by
+//                               inverse CDF over token id (the chunk from the
+//                               chunk sums, then that chunk read again; at
+//                               T = 0 the arg-max).  ws.draws[v] gets R_v, or
+//                               -1 for a row without mass, -2 for a row with
+//                               a repeated child token.
+//   predraw_walk_fused_kernel   a block per tree: validation, then warp 0
+//                               follows the draws from the root into the child
+//                               whose token is R_v; the first node without one
+//                               is the exit and R_v its bonus token.
+// (The draws run over the whole GPU, a warp per node, as in the batched chain:
+// drawn inside one block per tree they took longer than the rest of the
+// verifier, each warp re-reading several chunks one after another.)
+constexpr int kDrawFusedThreads = 256;
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kDrawFusedThreads)
+predraw_nodes_fused_kernel(const T* __restrict__ logits, int n_trees, int B, int64_t V, int nch,
+                           float c, uint64_t seed, const int32_t* __restrict__ n_nodes,
+                           VerifyWs ws) {
+    pdl_entry();
+    constexpr int CE = kChunkBytes / (int)sizeof(T);
+    constexpr int VEC = Lanes<T>::kVec;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int wpb = blockDim.x / kWarp;
+    const int R = B + 1;
+    const int64_t rows = (int64_t)n_trees * R;
+    for (int64_t row = (int64_t)blockIdx.x * wpb + threadIdx.x / kWarp; row < rows;
+         row += (int64_t)gridDim.x * wpb) {
+        const int t = (int)(row / R);
+        const int v = (int)(row - (int64_t)t * R);
+        if (v >= fused_rows(__ldg(n_nodes + t), B)) continue;
+        const ChunkStat* cs = ws.chunk + row * nch;
+        ChunkStat x[kFusedStatsPerLane];
+#pragma unroll
+        for (int k = 0; k < kFusedStatsPerLane; ++k) {
+            const int q = lane + k * kWarp;
+            if (q < nch) {
+                x[k] = cs[q];
+            } else {
+                x[k].m = -INFINITY;
+                x[k].s = 0.0f;
+                x[k].r = 0.0f;
+                x[k].amax = GREEDY ? INT_MAX : -1;
+            }
+        }
+        bool bad = false, dup = false;
+        int r = -1;
+        if (GREEDY) {
+            float bm = -INFINITY;
+            int bi = INT_MAX;
+#pragma unroll
+            for (int k = 0; k < kFusedStatsPerLane; ++k) {
+                bad |= (x[k].s != x[k].s);
+                dup |= (x[k].r != 0.0f);
+                if (better(x[k].m, x[k].amax, bm, bi)) {
+                    bm = x[k].m;
+                    bi = x[k].amax;
+                }
+            }
+            warp_argmax(bm, bi);
+            bad = __any_sync(0xffffffffu, bad) || bm == -INFINITY;
+            r = bi;
+        } else {
+            float m = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kFusedStatsPerLane; ++k) m = fmaxf(m, x[k].m);
+            m = warp_max(m);
+            const float mc = __fmul_rn(m, c);
+            float sum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kFusedStatsPerLane; ++k) {
+                bad |= (x[k].s != x[k].s);
+                dup |= (x[k].amax == -2);
+                if (x[k].m != -INFINITY) sum += x[k].s * ex2(__fmul_rn(x[k].m, c) - mc);
+            }
+            sum = warp_sum(sum);
+            bad = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(sum > 0.0f);
+            if (!bad) {
+                // the chunk where the running sum first exceeds u * S
+                const float thr = uniform24(seed, t, v, 2) * sum;
+                float base = 0.0f, frac = 1.0f;
+                int sel = -1, lastc = -1;
+                for (int q0 = 0; q0 < nch && sel < 0; q0 += kWarp) {
+                    const int q = q0 + lane;
+                    float sq = 0.0f;
+                    if (q < nch) {
+                        const ChunkStat y = cs[q];
+                        if (y.m != -INFINITY) sq = y.s * ex2(__fmul_rn(y.m, c) - mc);
+                    }
+                    const float inc = warp_incl_scan(sq, lane) + base;
+                    const unsigned hit = __ballot_sync(0xffffffffu, inc > thr && sq > 0.0f);
+                    const unsigned pos = __ballot_sync(0xffffffffu, sq > 0.0f);
+                    if (pos) lastc = q0 + 31 - __clz(pos);
+                    if (hit) {
+                        const int l = __ffs(hit) - 1;
+                        sel = q0 + l;
+                        const float incl = __shfl_sync(0xffffffffu, inc, l);
+                        const float own = __shfl_sync(0xffffffffu, sq, l);
+                        frac = (thr - (incl - own)) / own;
+                    }
+                    base = __shfl_sync(0xffffffffu, inc, 31);
+                }
+                if (sel < 0) sel = lastc;
+                frac = fminf(fmaxf(frac, 0.0f), 0.99999994f);
+                if (sel >= 0 && TSD_IN(sel, nch, kChkPredraw)) {
+                    // vector i of lane l holds tokens (i*32 + l)*VEC .. +VEC,
+                    // so (i, lane, element) is token order
+                    const int64_t c0 = (int64_t)sel * CE;
+                    const int cn = (int)min((int64_t)CE, V - c0);
+                    const float mcq = __fmul_rn(cs[sel].m, c);
+                    uint4 buf[kVecPerLane];
+                    load_chunk<T>(buf, logits + row * V + c0, cn, lane);
+                    float vs[kVecPerLane], lsum = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kVecPerLane; ++i) {
+                        float a = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            a += ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mcq));
+                        vs[i] = a;
+                        lsum += a;
+                    }
+                    const float target = frac * warp_sum(lsum);
+                    float run0 = 0.0f;
+                    int found = -1, last_i = -1, last_l = -1;
+                    bool done = false;  // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < kVecPerLane; ++i) {
+                        if (done) continue;
+                        const float inc = warp_incl_scan(vs[i], lane) + run0;
+                        const unsigned pos = __ballot_sync(0xffffffffu, vs[i] > 0.0f);
+                        if (pos) {
+                            last_i = i;
+                            last_l = 31 - __clz(pos);
+                        }
+                        const unsigned hit = __ballot_sync(0xffffffffu, inc > target && vs[i] > 0.0f);
+                        if (hit) {
+                            const int l = __ffs(hit) - 1;
+                            if (lane == l) {  // the crossing is inside this lane's vector
+                                float r2 = inc - vs[i];
+                                int lastp = -1, fi = -1;
+#pragma unroll
+                                for (int j = 0; j < VEC; ++j) {
+                                    const float e = ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mcq));
+                                    r2 += e;
+                                    if (e > 0.0f) lastp = (i * kWarp + lane) * VEC + j;
+                                    if (fi < 0 && r2 > target && e > 0.0f)
+                                        fi = (i * kWarp + lane) * VEC + j;
+                                }
+                                found = fi >= 0 ? fi : lastp;
+                            }
+                            found = __shfl_sync(0xffffffffu, found, l);
+                            done = true;
+                        }
+                        run0 = __shfl_sync(0xffffffffu, inc, 31);
+                    }
+                    if (found < 0 && last_i >= 0) {  // rounding left the target past the total
+#pragma unroll
+                        for (int i = 0; i < kVecPerLane; ++i) {
+                            if (i != last_i) continue;
+                            if (lane == last_l)
+                                for (int j = 0; j < VEC; ++j)
+                                    if (ex2(fmaf(Lanes<T>::get(buf[i], j), c, -mcq)) > 0.0f)
+                                        found = (i * kWarp + lane) * VEC + j;
+                        }
+                        found = __shfl_sync(0xffffffffu, found, last_l);
+                    }
+                    r = found >= 0 ? (int)(c0 + found) : -1;
+                }
+            }
+        }
+        dup = __any_sync(0xffffffffu, dup);
+        if (lane == 0) ws.draws[row] = dup ? -2 : (bad || r < 0 ? -1 : r);
+    }
+}
+
+constexpr int kWalkFusedThreads = 256;
+static_assert(kFusedMaxB + 1 <= kWalkFusedThreads, "the walk block gives each node a thread");
+
+__global__ void __launch_bounds__(kWalkFusedThreads)
+predraw_walk_fused_kernel(int B, int64_t V, const int32_t* __restrict__ parent,
+                          const int32_t* __restrict__ token, const int32_t* __restrict__ n_nodes,
+                          VerifyWs ws, int32_t* __restrict__ exit_node, int32_t* __restrict__ bonus,
+                          int32_t* __restrict__ accept_len, int32_t* __restrict__ draws,
+                          int32_t* __restrict__ status) {
+    pdl_entry();
+    __shared__ int16_t pa[kWalkFusedThreads];
+    __shared__ int32_t tk[kWalkFusedThreads], rd[kWalkFusedThreads];
+    __shared__ int flags;  // bit 0: malformed tree, bit 1: a row without mass
+    const int t = blockIdx.x;
+    const int R = B + 1;
+    const int lane = threadIdx.x & (kWarp - 1), wid = threadIdx.x / kWarp;
+    const int n_raw = n_nodes[t];
+    const bool n_ok = n_raw >= 1 && n_raw <= R;
+    const int n = n_ok ? n_raw : 1;
+    if (threadIdx.x == 0) flags = n_ok ? 0 : 1;
+    __syncthreads();
+    const int u = threadIdx.x;
+    if (u < n) {
+        const int p = parent[(int64_t)t * R + u];
+        const int x = token[(int64_t)t * R + u];
+        const int r = ws.draws[(int64_t)t * R + u];
+        bool bad;
+        if (u == 0) bad = p != -1;
+        else bad = p < 0 || p >= u || x < 0 || (int64_t)x >= V;
+        if (bad || r == -2) atomicOr(&flags, 1);
+        if (r == -1) atomicOr(&flags, 2);
+        pa[u] = (int16_t)(u == 0 ? -1 : (p >= 0 && p < u ? p : 0));
+        tk[u] = x;
+        rd[u] = r;
+    }
+    __syncthreads();
+    const int fl = flags;
+    const int st = (fl & 1) ? kStatBadTree : ((fl & 2) ? kStatNonFinite : kStatOk);
+    if (draws)
+        for (int v = threadIdx.x; v < R; v += blockDim.x)
+            draws[(int64_t)t * R + v] = (st == kStatOk && v < n) ? rd[v] : -1;
+    if (wid != 0) return;
+    if (st != kStatOk) {
+        if (lane == 0) {
+            exit_node[t] = -1;
+            bonus[t] = -1;
+            accept_len[t] = 0;
+            status[t] = st;
+        }
+        return;
+    }
+    // follow the draws from the root: the child of v whose token is R_v
+    int v = 0, d = 0;
+    for (int step = 0; step < n; ++step) {
+        const int r = rd[v];
+        int next = -1;
+        for (int x0 = 1; x0 < n && next < 0; x0 += kWarp) {
+            const int x = x0 + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, x < n && pa[x] == v && tk[x] == r);
+            if (m) next = x0 + __ffs(m) - 1;
+        }
+        if (next < 0) break;
+        v = next;
+        ++d;
+    }
+    if (lane == 0) {
+        exit_node[t] = v;
+        bonus[t] = rd[v];
+        accept_len[t] = d + 1;
+        status[t] = kStatOk;
+    }
+}
+
 bool tev_fused_fits(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V) {
     const int es = dtype == TSD_BF16 ? 2 : 4;
     return n_trees >= 1 && B >= 0 && B <= kFusedMaxB && ((uintptr_t)logits % 16) == 0 &&
@@ -555,7 +861,7 @@ cudaError_t launch_tev_fused(const void* logits, tsd_dtype dtype, int n_trees, i
         const int64_t want = (items + wpb - 1) / wpb;
         const int grid = resident_grid((const void*)skernel, wpb * kWarp, 0, want);
         cudaError_t e = launch_pdl(skernel, grid, wpb * kWarp, 0, stream, p, n_trees, B, V, nch, c,
-                                   parent, token, n_nodes, ws);
+                                   parent, token, n_nodes, ws, true);
         if (e != cudaSuccess) return e;
         if (ev_between && (e = cudaEventRecord(ev_between, stream)) != cudaSuccess) return e;
         if (fsmem > 48 * 1024 &&
@@ -577,6 +883,55 @@ cudaError_t launch_tev_fused(const void* logits, tsd_dtype dtype, int n_trees, i
         const auto* p = static_cast<const float*>(logits);
         e = greedy ? launch(tev_stream_kernel<float, true>, tev_finish_kernel<float, true>, p)
                    : launch(tev_stream_kernel<float, false>, tev_finish_kernel<float, false>, p);
+    }
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_predraw_fused(const void* logits, tsd_dtype dtype, int n_trees, int B,
+                                 int64_t V, float c, bool greedy, uint64_t seed,
+                                 const int32_t* parent, const int32_t* token,
+                                 const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                                 int32_t* bonus, int32_t* accept_len, int32_t* draws,
+                                 int32_t* status, cudaStream_t stream) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    const int nch = (int)n_chunks(V, es);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t rows = (int64_t)n_trees * (B + 1);
+    const int64_t items = rows * nch;
+    int wpb = (int)((items + sms - 1) / (sms > 0 ? sms : 1));
+    wpb = wpb < 1 ? 1 : (wpb > kStreamThreads / kWarp ? kStreamThreads / kWarp : wpb);
+    auto launch = [&](auto skernel, auto dkernel, const auto* p) {
+        const int64_t want = (items + wpb - 1) / wpb;
+        const int grid = resident_grid((const void*)skernel, wpb * kWarp, 0, want);
+        cudaError_t e = launch_pdl(skernel, grid, wpb * kWarp, 0, stream, p, n_trees, B, V, nch, c,
+                                   parent, token, n_nodes, ws, false);
+        if (e != cudaSuccess) return e;
+        // a warp per node; few warps per block when there are few nodes, so
+        // that the draws spread over the SMs
+        int dw = (int)((rows + sms - 1) / (sms > 0 ? sms : 1));
+        dw = dw < 1 ? 1 : (dw > kDrawFusedThreads / kWarp ? kDrawFusedThreads / kWarp : dw);
+        const int64_t dwant = (rows + dw - 1) / dw;
+        const int dgrid = resident_grid((const void*)dkernel, dw * kWarp, 0, dwant);
+        e = launch_pdl(dkernel, dgrid, dw * kWarp, 0, stream, p, n_trees, B, V, nch, c, seed,
+                       n_nodes, ws);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(predraw_walk_fused_kernel, n_trees, kWalkFusedThreads, 0, stream, B, V,
+                          parent, token, n_nodes, ws, exit_node, bonus, accept_len, draws, status);
+    };
+    cudaError_t e;
+    if (dtype == TSD_BF16) {
+        const auto* p = static_cast<const __nv_bfloat16*>(logits);
+        e = greedy ? launch(tev_stream_kernel<__nv_bfloat16, true>,
+                            predraw_nodes_fused_kernel<__nv_bfloat16, true>, p)
+                   : launch(tev_stream_kernel<__nv_bfloat16, false>,
+                            predraw_nodes_fused_kernel<__nv_bfloat16, false>, p);
+    } else {
+        const auto* p = static_cast<const float*>(logits);
+        e = greedy ? launch(tev_stream_kernel<float, true>, predraw_nodes_fused_kernel<float, true>, p)
+                   : launch(tev_stream_kernel<float, false>, predraw_nodes_fused_kernel<float, false>, p);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -42,8 +42,8 @@ int resident_grid(const void* kernel, int threads, size_t smem, int64_t want) {
 
 size_t heap_spill_bytes(int n_modes, int L, int topk, int B);  // k_heap.cu
 
-// Which launches of Tree Exit Verification run the two-kernel path
-// (k_tev_fused.cu), given its layout conditions (B <= 128 among them): every
+// Which launches of Tree Exit Verification (and of predraw-and-follow) run the
+// two-kernel path (k_tev_fused.cu), given its layout conditions (B <= 128 among them): every
 // launch with B <= TSD_FUSED_ANY_SIZE_MAX_B (64), and launches of at most
 // TSD_FUSED_MAX_ITEMS (node row, 8 KB chunk) items above that.  Measured on the V = 151936 grid: at B <= 64
 // the two-kernel path was as fast or faster from 1 to 256 trees; at B = 128
@@ -56,6 +56,12 @@ size_t heap_spill_bytes(int n_modes, int L, int topk, int B);  // k_heap.cu
 #ifndef TSD_FUSED_ANY_SIZE_MAX_B
 #define TSD_FUSED_ANY_SIZE_MAX_B 64
 #endif
+bool use_two_kernel_path(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V) {
+    const int es = dtype == TSD_BF16 ? 2 : 4;
+    return tev_fused_fits(logits, dtype, n_trees, B, V) &&
+           (B <= TSD_FUSED_ANY_SIZE_MAX_B ||
+            (int64_t)n_trees * (B + 1) * n_chunks(V, es) <= TSD_FUSED_MAX_ITEMS);
+}
 
 namespace {
 
@@ -378,9 +384,7 @@ static tsd_status verify_tev_impl(const void* target_logits, tsd_dtype dtype,
     const bool greedy = temperature == 0.0f;
     const float c = greedy ? 1.0f : exp2_scale(temperature);
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
-    if (tev_fused_fits(target_logits, dtype, n_trees, B, V) &&
-        (B <= TSD_FUSED_ANY_SIZE_MAX_B ||
-         (int64_t)n_trees * (B + 1) * n_chunks(V, es) <= TSD_FUSED_MAX_ITEMS)) {
+    if (use_two_kernel_path(target_logits, dtype, n_trees, B, V)) {
         // a launch of a few waves of row chunks: the two-kernel path
         if (mark(0) != cudaSuccess || mark(1) != cudaSuccess ||
             launch_tev_fused(target_logits, dtype, n_trees, B, V, c, greedy, seed, parent, token,
@@ -450,6 +454,13 @@ tsd_status tsd_verify_ddtree(const void* target_logits, tsd_dtype dtype, const i
     verify_ws_layout(n_trees, B, V, es, workspace, &ws);
     const bool greedy = temperature == 0.0f;
     const float c = greedy ? 1.0f : exp2_scale(temperature);
+    if (use_two_kernel_path(target_logits, dtype, n_trees, B, V)) {
+        if (launch_predraw_fused(target_logits, dtype, n_trees, B, V, c, greedy, seed, parent, token,
+                                 n_nodes, ws, exit_node, bonus_token, accept_len, draws, status,
+                                 stream) != cudaSuccess)
+            return TSD_ERR_CUDA;
+        return TSD_OK;
+    }
     if (launch_verify_prep(parent, token, n_nodes, n_trees, B, V, ws, stream) != cudaSuccess ||
         launch_rows(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||
         launch_node_combine(target_logits, dtype, n_trees, B, V, c, greedy, n_nodes, ws, stream) != cudaSuccess ||

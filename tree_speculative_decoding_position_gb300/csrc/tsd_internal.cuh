@@ -386,6 +386,12 @@ cudaError_t launch_tev_fused(const void* logits, tsd_dtype dtype, int n_trees, i
                              int32_t* exit_node, int32_t* bonus, int32_t* accept_len,
                              float* exit_mass, float* prefix_prob, float* coverage,
                              int32_t* status, cudaStream_t stream, cudaEvent_t ev_between);
+cudaError_t launch_predraw_fused(const void* logits, tsd_dtype dtype, int n_trees, int B,
+                                 int64_t V, float c, bool greedy, uint64_t seed,
+                                 const int32_t* parent, const int32_t* token,
+                                 const int32_t* n_nodes, const VerifyWs& ws, int32_t* exit_node,
+                                 int32_t* bonus, int32_t* accept_len, int32_t* draws,
+                                 int32_t* status, cudaStream_t stream);
 cudaError_t launch_predraw(const void* logits, tsd_dtype dtype, int n_trees, int B, int64_t V,
                            float c, bool greedy, uint64_t seed, const int32_t* n_nodes,
                            const VerifyWs& ws, int32_t* exit_node, int32_t* bonus,
