@@ -214,136 +214,151 @@ __device__ __forceinline__ FinishSmem finish_smem_layout(void* base, int R) {
     return f;
 }
 
-// Phase 1 of a finish block, every load at once: thread u reads node u's
-// parent, token and (T > 0, TEV) logit; each warp reads the chunk statistics
-// of its rows, G rows at a time, and reduces each row (its maximum and sums
-// relative to the row's reference, or its arg-max at T = 0) into shared
-// memory, with each chunk's maximum and residual sum (PRED: its sum).  flags
-// gets bit 0 for a malformed tree, bit 1 for a row without mass.  Returns
-// the number of live nodes; ends with a block barrier.
+// One row's statistics from its chunk statistics xs[0..KL) (chunks lane +
+// 32 k), by a warp: the maximum and the sums relative to the row's reference
+// (or the arg-max at T = 0) into shared memory, each chunk's maximum and
+// residual sum (PRED: its sum) beside them; flags gets bit 0 for a repeated
+// child token, bit 1 for a row without mass.
+template <bool GREEDY, bool PRED, int KL>
+__device__ __forceinline__ void finish_row(int v, const ChunkStat (&xs)[KL], int nch, float c,
+                                           const FinishSmem& f, int* flags, int lane) {
+    bool bad = false, dup = false;
+    if (GREEDY) {
+        float bm = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int k = 0; k < KL; ++k) {
+            bad |= (xs[k].s != xs[k].s);
+            dup |= (xs[k].r != 0.0f);
+            if (better(xs[k].m, xs[k].amax, bm, bi)) {
+                bm = xs[k].m;
+                bi = xs[k].amax;
+            }
+        }
+        warp_argmax(bm, bi);
+        bad |= (bm == -INFINITY);  // every token masked: no arg-max
+        if (lane == 0) {
+            f.Mc[v] = __int_as_float(bi);
+            f.Rv[v] = 1.0f;
+        }
+    } else {
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KL; ++k) m = fmaxf(m, xs[k].m);
+        m = warp_max(m);
+        const float mc = __fmul_rn(m, c);
+        float sm = 0.0f, r = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KL; ++k) {
+            bad |= (xs[k].s != xs[k].s);
+            dup |= (xs[k].amax == -2);
+            if (xs[k].m != -INFINITY) {
+                const float e = ex2(__fmul_rn(xs[k].m, c) - mc);
+                sm += xs[k].s * e;
+                r += xs[k].r * e;
+            }
+            const int q = lane + k * kWarp;
+            if (q < nch) f.cm[(size_t)v * nch + q] = make_float2(xs[k].m, PRED ? xs[k].s : xs[k].r);
+        }
+        sm = warp_sum(sm);
+        r = warp_sum(r);
+        bad = bad || m == -INFINITY || !(sm > 0.0f);
+        if (lane == 0) {
+            f.Mc[v] = mc;
+            f.Sv[v] = sm;
+            f.Rv[v] = r;
+        }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    dup = __any_sync(0xffffffffu, dup);
+    if (lane == 0 && (bad || dup)) atomicOr(flags, (dup ? 1 : 0) | (bad ? 2 : 0));
+}
+
+// Phase 1 of a finish block: every load is issued at once, before the tree's
+// size is known -- the size, each node's parent, token and (T > 0, TEV)
+// logit, and the chunk statistics of the rows up to B+1 (slots past n_nodes
+// are in bounds and their values are never used) -- G rows per warp and
+// round, rows strided over the warps.  Then the rows below n_nodes are
+// reduced (finish_row) and the tree is validated; flags gets bit 0 for a
+// malformed tree, bit 1 for a row without mass.  Returns the number of live
+// nodes; ends with a block barrier.
+template <typename T, bool GREEDY, bool PRED, int G, int KL>
+__device__ __forceinline__ int finish_stage_g(int t, int B, int64_t V, int nch, float c,
+                                              const int32_t* __restrict__ parent,
+                                              const int32_t* __restrict__ token,
+                                              const int32_t* __restrict__ n_nodes,
+                                              const VerifyWs& ws, const FinishSmem& f, int* flags) {
+    const int R = B + 1;
+    const int lane = threadIdx.x & (kWarp - 1), wid = threadIdx.x / kWarp;
+    const int nw = blockDim.x / kWarp;
+    const int u = threadIdx.x;  // R <= kFinishThreads
+    const int n_raw = n_nodes[t];
+    int p = -1, x = 0;
+    float z = 0.0f;
+    if (u < R) {
+        p = parent[(int64_t)t * R + u];
+        x = token[(int64_t)t * R + u];
+        if (!GREEDY && !PRED && u > 0) z = ws.pedge[(int64_t)t * R + u];
+    }
+    ChunkStat xs[G][KL];
+    auto load_round = [&](int g0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int v = g0 + wid + nw * g;
+#pragma unroll
+            for (int k = 0; k < KL; ++k) {
+                const int q = lane + k * kWarp;
+                if (v < R && q < nch) {
+                    xs[g][k] = ws.chunk[((int64_t)t * R + v) * nch + q];
+                } else {
+                    xs[g][k].m = -INFINITY;
+                    xs[g][k].s = 0.0f;
+                    xs[g][k].r = 0.0f;
+                    xs[g][k].amax = GREEDY ? INT_MAX : -1;
+                }
+            }
+        }
+    };
+    load_round(0);
+    if (threadIdx.x == 0) *flags = 0;
+    __syncthreads();
+    const bool n_ok = n_raw >= 1 && n_raw <= R;
+    const int n = n_ok ? n_raw : 1;
+    if (threadIdx.x == 0 && !n_ok) atomicOr(flags, 1);
+    if (u < n) {
+        bool bad;
+        if (u == 0) bad = p != -1;
+        else bad = p < 0 || p >= u || x < 0 || (int64_t)x >= V;
+        if (bad) atomicOr(flags, 1);
+        f.pa[u] = (int16_t)(u == 0 ? -1 : (p >= 0 && p < u ? p : 0));
+        f.tk[u] = x;
+        f.Dv[u] = z;
+    }
+    for (int g0 = 0;;) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int v = g0 + wid + nw * g;
+            if (v < n) finish_row<GREEDY, PRED, KL>(v, xs[g], nch, c, f, flags, lane);
+        }
+        g0 += nw * G;
+        if (g0 >= n) break;
+        load_round(g0);
+    }
+    __syncthreads();
+    return n;
+}
+
 template <typename T, bool GREEDY, bool PRED>
 __device__ __forceinline__ int finish_stage(int t, int B, int64_t V, int nch, float c,
                                             const int32_t* __restrict__ parent,
                                             const int32_t* __restrict__ token,
                                             const int32_t* __restrict__ n_nodes,
                                             const VerifyWs& ws, const FinishSmem& f, int* flags) {
-    const int R = B + 1;
-    const int lane = threadIdx.x & (kWarp - 1), wid = threadIdx.x / kWarp;
-    const int nw = blockDim.x / kWarp;
-    float* Mc = f.Mc;
-    float* Sv = f.Sv;
-    float* Rv = f.Rv;
-    float* Dv = f.Dv;
-    int32_t* tk = f.tk;
-    int16_t* pa = f.pa;
-    float2* cmr = f.cm;
-    const int n_raw = n_nodes[t];
-    const bool n_ok = n_raw >= 1 && n_raw <= R;
-    const int n = n_ok ? n_raw : 1;
-    if (threadIdx.x == 0) *flags = n_ok ? 0 : 1;
-    __syncthreads();
-    // ---- phase 1: all loads ------------------------------------------------
-    {
-        const int u = threadIdx.x;  // R <= kFinishThreads
-        int p = -1, x = 0;
-        float z = 0.0f;
-        if (u < n) {
-            p = parent[(int64_t)t * R + u];
-            x = token[(int64_t)t * R + u];
-            if (!GREEDY && !PRED && u > 0) z = ws.pedge[(int64_t)t * R + u];
-        }
-        constexpr int G = 4;   // rows per round of a warp
-        constexpr int KL = 2;  // chunks per lane and row (rows of at most 64 chunks)
-        auto load_stat = [&](int v, int q, ChunkStat& cs) {
-            if (v < n && q < nch) {
-                cs = ws.chunk[((int64_t)t * R + v) * nch + q];
-            } else {
-                cs.m = -INFINITY;
-                cs.s = 0.0f;
-                cs.r = 0.0f;
-                cs.amax = GREEDY ? INT_MAX : -1;
-            }
-        };
-        auto row_reduce = [&](int v, const ChunkStat* xs, int kl, int q0) {
-            bool bad = false, dup = false;
-            if (GREEDY) {
-                float bm = -INFINITY;
-                int bi = INT_MAX;
-                for (int k = 0; k < kl; ++k) {
-                    bad |= (xs[k].s != xs[k].s);
-                    dup |= (xs[k].r != 0.0f);
-                    if (better(xs[k].m, xs[k].amax, bm, bi)) {
-                        bm = xs[k].m;
-                        bi = xs[k].amax;
-                    }
-                }
-                warp_argmax(bm, bi);
-                bad |= (bm == -INFINITY);  // every token masked: no arg-max
-                if (lane == 0) {
-                    Mc[v] = __int_as_float(bi);
-                    Rv[v] = 1.0f;
-                }
-            } else {
-                float m = -INFINITY;
-                for (int k = 0; k < kl; ++k) m = fmaxf(m, xs[k].m);
-                m = warp_max(m);
-                const float mc = __fmul_rn(m, c);
-                float sm = 0.0f, r = 0.0f;
-                for (int k = 0; k < kl; ++k) {
-                    bad |= (xs[k].s != xs[k].s);
-                    dup |= (xs[k].amax == -2);
-                    if (xs[k].m != -INFINITY) {
-                        const float f = ex2(__fmul_rn(xs[k].m, c) - mc);
-                        sm += xs[k].s * f;
-                        r += xs[k].r * f;
-                    }
-                    const int q = q0 + k * kWarp;
-                    if (q < nch) cmr[(size_t)v * nch + q] = make_float2(xs[k].m, PRED ? xs[k].s : xs[k].r);
-                }
-                sm = warp_sum(sm);
-                r = warp_sum(r);
-                bad = bad || m == -INFINITY || !(sm > 0.0f);
-                if (lane == 0) {
-                    Mc[v] = mc;
-                    Sv[v] = sm;
-                    Rv[v] = r;
-                }
-            }
-            bad = __any_sync(0xffffffffu, bad);
-            dup = __any_sync(0xffffffffu, dup);
-            if (lane == 0 && (bad || dup)) atomicOr(flags, (dup ? 1 : 0) | (bad ? 2 : 0));
-        };
-        if (nch <= KL * kWarp) {
-            for (int v0 = wid * G; v0 < n; v0 += nw * G) {
-                ChunkStat xs[G][KL];
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int k = 0; k < KL; ++k) load_stat(v0 + g, lane + k * kWarp, xs[g][k]);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if (v0 + g < n) row_reduce(v0 + g, xs[g], KL, lane);
-            }
-        } else {
-            for (int v = wid; v < n; v += nw) {
-                ChunkStat xs[kFusedStatsPerLane];
-#pragma unroll
-                for (int k = 0; k < kFusedStatsPerLane; ++k) load_stat(v, lane + k * kWarp, xs[k]);
-                row_reduce(v, xs, kFusedStatsPerLane, lane);
-            }
-        }
-        if (u < n) {
-            bool bad;
-            if (u == 0) bad = p != -1;
-            else bad = p < 0 || p >= u || x < 0 || (int64_t)x >= V;
-            if (bad) atomicOr(flags, 1);
-            pa[u] = (int16_t)(u == 0 ? -1 : (p >= 0 && p < u ? p : 0));
-            tk[u] = x;
-            Dv[u] = z;
-        }
-    }
-    __syncthreads();
-    return n;
+    if (nch <= 2 * kWarp)  // five rows of up to 64 chunks per warp and round
+        return finish_stage_g<T, GREEDY, PRED, 5, 2>(t, B, V, nch, c, parent, token, n_nodes, ws,
+                                                     f, flags);
+    return finish_stage_g<T, GREEDY, PRED, 2, kFusedStatsPerLane>(t, B, V, nch, c, parent, token,
+                                                                  n_nodes, ws, f, flags);
 }
 
 // One block per tree, in two phases.
@@ -420,14 +435,13 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
     // P(u): the product of the edge probabilities on the root path, every
     // node walking its own ancestors (parents precede children, so a walk
     // ends within u steps)
-    float cov_part = 0.0f;
     for (int u = threadIdx.x; u < R; u += blockDim.x) {
         float P = 0.0f, wu = 0.0f;
         if (u < n) {
             P = 1.0f;
             for (int x = u; x > 0; x = pa[x]) P *= Dv[x];
             wu = GREEDY ? P * Rv[u] : P * (Rv[u] / Sv[u]);
-            if (u > 0) cov_part += P;
+            f.Pv[u] = P;
             Wv[u] = wu;
         }
         if (exit_mass) exit_mass[(int64_t)t * R + u] = wu;
@@ -436,36 +450,40 @@ tev_finish_kernel(const T* __restrict__ logits, int B, int64_t V, int nch, float
     __shared__ float red[33];
     __shared__ int pick[2];
     __shared__ int exit_v, chunk_sel, n_kids;
-    __shared__ float chunk_frac;
-    float cov;
-    fused_block_scan(cov_part, red, &cov);
-    // the exit draw: inverse CDF over nodes; each thread owns a contiguous
-    // run of nodes so that the block scan follows node order
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int nb = threadIdx.x * per, ne = min(n, nb + per);
-    float mine = 0.0f;
-    for (int v = nb; v < ne; ++v) mine += Wv[v];
-    float wsum;
-    float run = fused_block_scan(mine, red, &wsum);
-    const float thr = uniform24(seed, t, 0, 0) * wsum;
-    if (threadIdx.x == 0) {
-        pick[0] = INT_MAX;
-        pick[1] = -1;
-    }
+    __shared__ float chunk_frac, cov_sh;
     __syncthreads();
-    int last = -1;
-    for (int v = nb; v < ne; ++v) {
-        run += Wv[v];
-        if (Wv[v] > 0.0f) last = v;
-        if (run > thr && Wv[v] > 0.0f) {
-            atomicMin(pick, v);
-            break;
+    // C_p and the exit draw by warp 0: inverse CDF over nodes, lane l owning a
+    // contiguous run of them
+    if (wid == 0) {
+        const int per = (n + kWarp - 1) / kWarp;
+        const int nb = lane * per, ne = min(n, nb + per);
+        float mine = 0.0f, pc = 0.0f;
+        for (int v = nb; v < ne; ++v) {
+            mine += Wv[v];
+            if (v > 0) pc += f.Pv[v];
+        }
+        const float cov_all = warp_sum(pc);
+        const float incl = warp_incl_scan(mine, lane);
+        const float wsum = __shfl_sync(0xffffffffu, incl, 31);
+        const float thr = uniform24(seed, t, 0, 0) * wsum;
+        float run = incl - mine;
+        int first = INT_MAX, last = -1;
+        for (int v = nb; v < ne; ++v) {
+            run += Wv[v];
+            if (Wv[v] > 0.0f) {
+                last = v;
+                if (first == INT_MAX && run > thr) first = v;
+            }
+        }
+        first = __reduce_min_sync(0xffffffffu, first);
+        last = __reduce_max_sync(0xffffffffu, last);
+        if (lane == 0) {
+            exit_v = first != INT_MAX ? first : (last >= 0 ? last : 0);
+            cov_sh = cov_all;
         }
     }
-    if (last >= 0) atomicMax(pick + 1, last);
     __syncthreads();
-    if (threadIdx.x == 0) exit_v = pick[0] != INT_MAX ? pick[0] : (pick[1] >= 0 ? pick[1] : 0);
-    __syncthreads();
+    const float cov = cov_sh;
     const int V_ = exit_v;
     int y = -1;
     if (GREEDY) {
