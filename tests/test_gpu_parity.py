@@ -84,6 +84,37 @@ def test_build_batched_b256(tsd, dev, orc, flip_log):
     assert flips <= 2, flips
 
 
+@pytest.mark.parametrize("B", [99, 100, 127, 128, 129])
+def test_build_crowded_bound(tsd, dev, orc, flip_log, B):
+    """A drafter whose best prefixes crowd the B-th score (an exact tie
+    between two depth-4 prefixes at places 98 and 99, many candidates just
+    below): once the taken list holds B prefixes the frontier must stay
+    within its buffer.  Before the frontier was capped at K*B entries there,
+    these budgets overflowed it and the tree came back empty (status 5)."""
+    dr = synth.zipf_drafter(1, 16, V_Q, 0, device=dev, seeds=[synth.seed_for(4, 127000)])
+    out = tsd.tsd_build_tree(dr, topk=8, B=B)
+    assert int(out["status"][0]) == 0 and int(out["n_nodes"][0]) == B + 1
+    ref, lists = oracle_build(orc, dr[0].cpu(), 8, B)
+    flips = compare_trees(_tree_np(out), ref, lists)
+    flip_log("builder", flips)
+    assert flips <= 1, flips
+
+
+def test_build_budget_sweep(tsd, dev, orc):
+    """Every budget from 90 to 140 on four drafters, one call per budget with
+    the four trees: each tree full (B+1 nodes, status 0) and the first of
+    them equal to the oracle's."""
+    seeds = [synth.seed_for(4, 127000)] + [synth.seed_for(8, t) for t in range(3)]
+    dr = synth.zipf_drafter(4, 16, V_Q, 0, device=dev, seeds=seeds)
+    for B in range(90, 141):
+        out = tsd.tsd_build_tree(dr, topk=8, B=B)
+        assert _np(out["status"]).tolist() == [0] * 4, (B, _np(out["status"]))
+        assert _np(out["n_nodes"]).tolist() == [B + 1] * 4, B
+        if B % 10 == 0:
+            ref, lists = oracle_build(orc, dr[1].cpu(), 8, B)
+            assert compare_trees(_tree_np(out, 1), ref, lists) <= 1, B
+
+
 def test_build_fp32_and_misaligned(tsd, dev, orc):
     """fp32 logits, and a row start that is not 16-byte aligned (generic path)."""
     dr = synth.zipf_drafter(1, 6, 5000, synth.seed_for(1, 3), device="cpu", dtype=torch.float32)

@@ -21,8 +21,10 @@
 // one-at-a-time heap would not reach, but never misses one: every entry not
 // yet taken is worse than the frontier head, and the search stops only when
 // the frontier holds nothing better than the B-th distinct prefix of X.  The
-// frontier is pruned every round to entries no worse than the (K*B)-th entry
-// of X and the frontier merged (at least B distinct prefixes are that good).
+// frontier is pruned every round: until X holds B distinct prefixes, to
+// entries no worse than the (K*B)-th entry of X and the frontier merged (at
+// least B distinct prefixes are that good); after, to entries better than the
+// B-th distinct prefix of X, and to at most its first K*B entries.
 // The result is exactly the heap's: the B best distinct prefixes under the
 // total order (score desc, depth asc, mode asc, rank sequence asc), listed in
 // that order (= pop order).
@@ -623,12 +625,17 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                 const int posB = s_posB;
                 const FEntry th = X[xc][posB];
                 nXn = posB + 1;
-                // frontier entries not before the bound can never be kept
+                // frontier entries not before the bound can never be kept;
+                // nor can entries past the frontier's first K*B: at most B of
+                // its distinct prefixes can still be kept, and each prefix
+                // appears at most K times (once per mode), so the best B are
+                // among the first K*B.  (Without this cap the frontier can
+                // outgrow its buffer when many candidates crowd the bound.)
                 if (tid < 32) {
                     const FEntry* Fc = F[fc];
                     const int lo = warp_first_false(0, nFn, [&](int i) { return before(Fc[i], th); });
                     if (tid == 0) {
-                        s_nF = lo;
+                        s_nF = min(lo, K * B);
                         s_thr = th;
                         s_thr_on = 1;
                     }
