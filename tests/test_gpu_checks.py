@@ -1,7 +1,12 @@
 """The bounds-checked build (-DTSD_CHECKS, libtsd_checks.so): every entry
 point on representative and edge-case inputs must pass every check, and give
 the same outputs as the product library.  Each library runs in its own
-process (the binding loads one library per process)."""
+process (the binding loads one library per process).
+
+The checked build also narrows the log-sum-exp selection's group hash to 6
+bits, so that its exact check fails and the depth-by-depth merge runs; the
+outputs of that merge are compared here with the default build's grouped
+merge."""
 import json
 import os
 import subprocess
@@ -59,7 +64,12 @@ for V, dtype in ((synth.V_QWEN, torch.bfloat16), (12805, torch.bfloat16), (4097,
 
 mix, _, _ = synth.mixture_drafter(3, 4, 6, 3000, synth.seed_for(11, 1), device=dev)
 keep("mixture", tsd.tsd_build_tree(mix, topk=8, B=100), ("parent", "token", "n_nodes", "status"))
-keep("lse", tsd.tsd_build_lse_tree(mix, topk=8, B=100), ("parent", "token", "n_nodes", "status"))
+keep("lse", tsd.tsd_build_lse_tree(mix, topk=8, B=100), ("parent", "token", "n_nodes", "status", "n_cand"))
+# the mixture workload's shape (two groups of eight depths in the selection's
+# merge); the checked build always takes the depth-by-depth merge
+mix, _, _ = synth.mixture_drafter(2, 8, 16, synth.V_QWEN, synth.seed_for(11, 2), device=dev)
+keep("lse_k8", tsd.tsd_build_lse_tree(mix, topk=8, B=128), ("parent", "token", "depth", "n_nodes", "status",
+                                                           "n_cand"))
 dr = synth.zipf_drafter(6, 8, 3000, 0, device=dev, seeds=[synth.seed_for(11, 50 + t) for t in range(6)])
 keep("forest", tsd.tsd_build_forest(dr, topk=8, B=64, M_max=200, l0=1.0, c1=1.0 / 256),
      ("parent", "n_nodes", "status", "total"))

@@ -57,7 +57,6 @@ struct __align__(16) FEntry {
 static_assert(sizeof(FEntry) == 32, "entry layout");
 
 constexpr unsigned long long kSentinelKey = 0ull;  // below every real key
-constexpr unsigned long long kRootHash = 0x243F6A8885A308D3ull;
 constexpr unsigned long long kRsMask = (1ull << 56) - 1;
 
 __device__ __forceinline__ bool before(const FEntry& a, const FEntry& b) {
@@ -65,16 +64,6 @@ __device__ __forceinline__ bool before(const FEntry& a, const FEntry& b) {
 }
 __device__ __forceinline__ int tb_depth(unsigned long long tb) { return (int)(tb >> 59); }
 __device__ __forceinline__ int tb_mode(unsigned long long tb) { return (int)((tb >> 56) & 7); }
-// A strong 64-bit mix of (parent hash, token) (a SplitMix64-style finaliser).
-__device__ __forceinline__ unsigned long long hash_step(unsigned long long h, int tok) {
-    unsigned long long x = h ^ ((unsigned long long)(uint32_t)tok * 0x9E3779B97F4A7C15ull);
-    x ^= x >> 30;
-    x *= 0xBF58476D1CE4E5B9ull;
-    x ^= x >> 27;
-    x *= 0x94D049BB133111EBull;
-    x ^= x >> 31;
-    return x;
-}
 
 struct BuildPlan {
     int M;          // entries taken per round

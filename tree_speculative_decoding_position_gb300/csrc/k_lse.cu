@@ -97,7 +97,7 @@ size_t lse_beam_smem(int K, int B, int k) {
     return sizeof(double) * (size_t)(2 * B * K + 4 * B + TSD_MAX_TOPK * (1 + TSD_MAX_MODES) +
                                      3 * TSD_MAX_MODES) +
            2 * (sizeof(unsigned long long) + sizeof(unsigned)) * (size_t)lse_sort_cap(B, k) +
-           sizeof(int) * (size_t)(2 * B);
+           sizeof(int) * (size_t)(2 * B) + sizeof(unsigned long long) * (size_t)(2 * B);
 }
 
 __global__ void __launch_bounds__(kBeamThreads, 1)
@@ -120,6 +120,8 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
     unsigned* cidx2 = cidx + lse_sort_cap(B, k);
     int* par = reinterpret_cast<int*>(cidx2 + lse_sort_cap(B, k));  // [B] parent place of each kept child
     int* rk = par + B;                                        // [B] token rank of each kept child
+    unsigned long long* ph[2] = {reinterpret_cast<unsigned long long*>(rk + B),
+                                 reinterpret_cast<unsigned long long*>(rk + B) + B};  // path hashes
     __shared__ int s_n, s_bad, s_kf;
     __shared__ int s_off[TSD_MAX_TOPK + 1];  // offsets of the ranks' possible children
     const int64_t KB = (int64_t)K * B;
@@ -250,9 +252,13 @@ lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, 
             const double key = s < up ? s : up;
             nsk[j] = key;
             const int64_t f = (int64_t)t * L * KB + (int64_t)d * KB + (int64_t)m * B + j;
-            ws.tok[f] = bws.top_id[row * k + rk[j]];
+            const int32_t x = bws.top_id[row * k + rk[j]];
+            const unsigned long long hv = hash_step(d == 0 ? kRootHash : ph[cur ^ 1][par[j]], x);
+            ph[cur][j] = hv;
+            ws.tok[f] = x;
             ws.par[f] = par[j];
             ws.kimg[f] = ~order_key(key);
+            ws.phash[f] = hv;
         }
         if (tid == 0) *nb_out = nb;
         np = nb;
@@ -334,11 +340,45 @@ __device__ __forceinline__ bool pair_less(unsigned long long a0, unsigned long l
 constexpr unsigned long long kEmpty = ~0ull;
 constexpr int kMaxSlotsPerThread = 4;  // n_modes * B <= 4096 over 1024 threads
 
-size_t lse_select_smem(int K, int B) {
+// The merge over groups of depths: one table of kGroupSlots packed words
+// (bits 19-63 a 45-bit hash of (depth, token sequence), bits 0-18 the flat
+// index of the first appearance; equal prefixes agree above bit 18, so a
+// 32-bit minimum of the low half keeps the first appearance), and each
+// group entry's slot.  A group holds kGroupSlots / (2 K B) depths, so the
+// table is at most half full.
+constexpr int kGroupSlots = 16384;
+constexpr int kFlatBits = 19;
+constexpr unsigned long long kFlatMask = (1ull << kFlatBits) - 1;
+static_assert((long long)TSD_MAX_L * kMaxLseModeBudget <= (long long)kFlatMask, "flat index in 19 bits");
+static_assert(kGroupSlots >= 2 * kMaxLseModeBudget, "a group holds at least one depth");
+constexpr int kGroupPer = kGroupSlots / 2 / kSelThreads;  // group entries a thread
+#ifdef TSD_CHECKS
+// The checked build keeps 6 bits of the group hash: matches then collide, the
+// exact check fails and the depth-by-depth merge runs, and its test compares
+// those outputs with the default build's.
+constexpr unsigned long long kGroupKeyMask = 0x3Full;
+#else
+constexpr unsigned long long kGroupKeyMask = ~0ull >> kFlatBits;
+#endif
+
+// After the merge, the candidates (image, flat index) stay in shared memory,
+// after the sort buffer, when every list entry fits there.
+constexpr size_t kSelSmemCap = 200 * 1024;
+static __host__ __device__ size_t lse_sel_sort_bytes(int B) {
+    return (size_t)2 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
+}
+static __host__ __device__ bool lse_cands_in_smem(int K, int B, int L) {
+    return lse_sel_sort_bytes(B) + (size_t)L * K * B * (sizeof(unsigned long long) + sizeof(int32_t)) <=
+           kSelSmemCap;
+}
+size_t lse_select_smem(int K, int B, int L) {
     const size_t H = (size_t)pow2_ceil(2 * K * B);
     const size_t dedupe = H * (sizeof(unsigned long long) + sizeof(int)) + sizeof(int) * 2 * K * B;
-    const size_t sel = (size_t)2 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
-    return dedupe > sel ? dedupe : sel;
+    const size_t group = (size_t)kGroupSlots * sizeof(unsigned long long) + sizeof(int16_t) * (size_t)kGroupSlots / 2;
+    size_t m = dedupe > group ? dedupe : group;
+    const size_t sel = lse_sel_sort_bytes(B) +
+                       (lse_cands_in_smem(K, B, L) ? (size_t)L * K * B * (sizeof(unsigned long long) + sizeof(int32_t)) : 0);
+    return m > sel ? m : sel;
 }
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -387,10 +427,134 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         }
         return;
     }
-    // 1. distinct prefixes, depth by depth: rep = flat index of the first
-    //    appearance; every list entry is compacted, in flat order, into the
-    //    candidate arrays when it is its own representative with mass
+    // 1. distinct prefixes: rep = flat index of the first appearance; every
+    //    list entry is compacted, in flat order, into the candidate arrays
+    //    when it is its own representative with mass.
+    //    First, all depths of a group at once, keyed by each entry's hash of
+    //    (depth, token sequence).  Every merge is then checked exactly: an
+    //    entry and its representative have the same depth, the same token and
+    //    parents with the same representative.  If all pass, a group's
+    //    classes are exactly its distinct prefixes (by induction over depth).
+    //    If one fails (a hash collision), the merge runs again depth by depth
+    //    on (parent's representative, token), which needs no hash.
+    __shared__ int s_fail;
     int n_f = 0;
+    // the candidates: in shared memory after the sort buffer when they fit
+    // (the grouped merge's table is dead by then), else in the workspace
+    const bool cand_smem = lse_cands_in_smem(K, B, L);
+    unsigned long long* cimg_p = cand_smem ? reinterpret_cast<unsigned long long*>(sms + lse_sel_sort_bytes(B))
+                                           : ws.cimg + base;
+    int32_t* cflat_p = cand_smem ? reinterpret_cast<int32_t*>(cimg_p + N) : ws.cflat + base;
+    if (tid == 0) s_fail = KB == 0;
+    {
+        unsigned long long* gtab = reinterpret_cast<unsigned long long*>(sms);
+        int16_t* gslot = reinterpret_cast<int16_t*>(gtab + kGroupSlots);
+        const int G = KB > 0 ? kGroupSlots / (2 * KB) : 1;
+        for (int h = tid; h < kGroupSlots; h += blockDim.x) gtab[h] = kEmpty;
+        __syncthreads();
+        for (int d0 = 0; d0 < L && KB > 0; d0 += G) {
+            const int nd = min(G, L - d0), ne = nd * KB;
+            // the group's hashes first (at most kGroupPer a thread), then the inserts
+            unsigned long long hv[kGroupPer];
+            bool in[kGroupPer];
+#pragma unroll
+            for (int q = 0; q < kGroupPer; ++q) {
+                const int i = tid + q * kSelThreads;
+                const int d = d0 + i / KB, e = i % KB;
+                in[q] = i < ne && e % B < nbs[d * K + e / B];
+                hv[q] = in[q] ? ws.phash[base + (int64_t)d0 * KB + i] : 0ull;
+            }
+#pragma unroll
+            for (int q = 0; q < kGroupPer; ++q) {
+                const int i = tid + q * kSelThreads;
+                if (i >= ne) continue;
+                const int d = d0 + i / KB;
+                int slot = -1;
+                if (in[q]) {
+                    const int f = d0 * KB + i;
+                    const unsigned long long key = (hash_step(hv[q], d) >> kFlatBits) & kGroupKeyMask;
+                    const unsigned long long word = (key << kFlatBits) | (unsigned long long)f;
+                    unsigned h = (unsigned)key & (unsigned)(kGroupSlots - 1);
+                    for (int probe = 0; probe < kGroupSlots; ++probe) {
+                        const unsigned long long old = atomicCAS(&gtab[h], kEmpty, word);
+                        if (old == kEmpty) {
+                            slot = (int)h;
+                            break;
+                        }
+                        if ((old >> kFlatBits) == key) {
+                            atomicMin(reinterpret_cast<unsigned*>(&gtab[h]), (unsigned)word);
+                            slot = (int)h;
+                            break;
+                        }
+                        h = (h + 1) & (unsigned)(kGroupSlots - 1);
+                    }
+                }
+                gslot[i] = (int16_t)slot;
+            }
+            __syncthreads();
+            for (int i = tid; i < ne; i += blockDim.x)
+                if (gslot[i] >= 0) ws.rep[base + (int64_t)d0 * KB + i] = (int)(gtab[gslot[i]] & kFlatMask);
+            __syncthreads();
+            // the exact check, while the table is cleared for the next group
+            bool fail = false;
+            for (int i = tid; i < ne; i += blockDim.x) {
+                if (gslot[i] < 0) continue;
+                const int f = d0 * KB + i, d = f / KB;
+                const int r = ws.rep[base + f];
+                if (r == f) continue;
+                const int dr = r / KB;
+                bool same = dr == d && r < f && ws.tok[base + r] == ws.tok[base + f];
+                if (same && d > 0) {
+                    const int pf = ws.par[base + f], pr = ws.par[base + r];
+                    const int mf = (f - d * KB) / B, mr = (r - d * KB) / B;
+                    same = TSD_IN(pf, B, kChkLse) && TSD_IN(pr, B, kChkLse) &&
+                           ws.rep[base + (int64_t)(d - 1) * KB + mf * B + pf] ==
+                               ws.rep[base + (int64_t)(d - 1) * KB + mr * B + pr];
+                }
+                fail |= !same;
+            }
+            if (fail) s_fail = 1;
+            for (int h = tid; h < kGroupSlots; h += blockDim.x) gtab[h] = kEmpty;
+            __syncthreads();
+        }
+        if (!s_fail) {
+            // compaction in flat order, four consecutive entries a thread; an
+            // entry's representative and image are loaded together
+            for (int64_t c0 = 0; c0 < N; c0 += 4 * blockDim.x) {
+                int cnt = 0;
+                bool kp[4];
+                unsigned long long im[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t c = c0 + 4 * tid + q;
+                    bool lv = false;
+                    if (c < N) {
+                        const int d = (int)(c / KB), e = (int)(c - (int64_t)d * KB);
+                        lv = e % B < nbs[d * K + e / B];
+                    }
+                    const int r = lv ? ws.rep[base + c] : -1;
+                    im[q] = lv ? ws.kimg[base + c] : ~kNegInfImage;
+                    kp[q] = r == (int)c && im[q] != ~kNegInfImage;
+                    cnt += kp[q];
+                }
+                int tot;
+                int pos = n_f + block_excl_scan_i(cnt, red, &tot);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (!kp[q]) continue;
+                    cimg_p[pos] = im[q];
+                    cflat_p[pos] = (int32_t)(c0 + 4 * tid + q);
+                    ++pos;
+                }
+                n_f += tot;
+            }
+        }
+    }
+    if (s_fail && KB > 0) {
+    // (the hash of this merge overlaps the shared candidate buffer: its
+    // candidates go to the workspace)
+    cimg_p = ws.cimg + base;
+    cflat_p = ws.cflat + base;
     // thread tid holds entries e = S tid + q, q < S, of each depth (S = K B /
     // threads rounded up, at most 4); the next depth's tokens, parents and
     // images are loaded while this one hashes
@@ -476,8 +640,9 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             lv[q] = d + 1 < L && lv2[q];
         }
     }
-    const unsigned long long* cimg = ws.cimg + base;
-    const int32_t* cflat = ws.cflat + base;
+    }  // the depth-by-depth merge
+    const unsigned long long* cimg = cimg_p;
+    const int32_t* cflat = cflat_p;
     // 2. radix select of the B-th best image among the candidates
     int take = n_f < B ? n_f : B;
     unsigned long long prefix = 0, mask = 0;
@@ -655,7 +820,7 @@ cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, in
     e = launch_pdl(lse_beam_kernel, dim3((unsigned)K, (unsigned)n_trees), kBeamThreads, sb, stream,
                    logits, dtype, K, L, V, k, B, temp, log_prior, bws, ws);
     if (e != cudaSuccess) return e;
-    const size_t ss = lse_select_smem(K, B);
+    const size_t ss = lse_select_smem(K, B, L);
     e = cudaFuncSetAttribute(lse_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (e != cudaSuccess) return e;
     return launch_pdl(lse_select_kernel, (unsigned)n_trees, kSelThreads, ss, stream, K, L, k, B, bws,

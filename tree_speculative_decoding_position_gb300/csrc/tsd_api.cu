@@ -196,6 +196,7 @@ size_t lse_ws_layout(int n_trees, int n_modes, int L, int64_t V, int topk, int B
     l.cimg = cv.take<unsigned long long>(ent);
     l.cflat = cv.take<int32_t>(ent);
     l.nb = cv.take<int32_t>(rows);
+    l.phash = cv.take<unsigned long long>(ent);
     if (out) *out = ws;
     if (lout) *lout = l;
     return (cv.off + kAlign - 1) & ~(kAlign - 1);

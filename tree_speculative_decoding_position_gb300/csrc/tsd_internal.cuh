@@ -271,6 +271,19 @@ struct Lanes<float> {
 
 // Order-preserving 64-bit image of a float64 score (larger score, larger
 // key; -inf the smallest of the finite-or-infinite values), and its inverse.
+// Hash of a token sequence, one token at a time from the root's value: a
+// strong 64-bit mix of (parent hash, token), a SplitMix64-style finaliser.
+// Equal sequences get equal hashes; users confirm every match exactly.
+constexpr unsigned long long kRootHash = 0x243F6A8885A308D3ull;
+__device__ __forceinline__ unsigned long long hash_step(unsigned long long h, int tok) {
+    unsigned long long x = h ^ ((unsigned long long)(uint32_t)tok * 0x9E3779B97F4A7C15ull);
+    x ^= x >> 30;
+    x *= 0xBF58476D1CE4E5B9ull;
+    x ^= x >> 27;
+    x *= 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    return x;
+}
 __device__ __forceinline__ unsigned long long order_key(double s) {
     const unsigned long long u = (unsigned long long)__double_as_longlong(s);
     return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
@@ -442,6 +455,7 @@ struct LseWs {
     unsigned long long* cimg;  // [n_trees][L*K*B] candidates' images, compacted in flat order
     int32_t* cflat;            // [n_trees][L*K*B] their flat indices
     int32_t* nb;       // [n_trees][L][K] list sizes
+    unsigned long long* phash;  // [n_trees][L*K*B] hash of each entry's token sequence
 };
 __host__ __device__ inline int pow2_ceil(int x) {
     int p = 1;
@@ -450,7 +464,7 @@ __host__ __device__ inline int pow2_ceil(int x) {
 }
 size_t lse_beam_smem(int K, int B, int k);
 constexpr size_t kMaxLseSmem = 227 * 1024;
-size_t lse_select_smem(int K, int B);
+size_t lse_select_smem(int K, int B, int L);
 cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, int K, int L,
                             int64_t V, int k, int B, double temp, const float* log_prior,
                             const BuildWs& bws, const LseWs& ws, int32_t* parent, int32_t* token,
