@@ -13,28 +13,36 @@
 // token rank asc).  Within one mode and depth every child carries the same
 // summed log-normaliser, so path sums of z/T decide the order.
 //
-// lse_beam_kernel    one CTA per (mode, tree), depth by depth.  The children
-//                    of the previous list form k runs, one per token rank,
-//                    each already sorted; only children with (r+1)(i+1) <= B
-//                    can be kept, and those runs are merged in log2(k) rounds
-//                    of binary searches.  The first B are kept.  Each kept
-//                    entry then gathers its token's logit under every mode
-//                    (full rows), extends the per-mode path sums, and takes
-//                    s_lse = log sum_m exp(log pi_m + path sum - summed LSE),
-//                    clamped to its parent's key.  Equal prefixes reached by
-//                    several modes get bit-identical keys.
+// lse_beam_kernel    one CTA per (mode, tree), depth by depth, in two warp
+//                    groups.  Twelve warps rank: the children of the previous
+//                    list form k runs, one per token rank, each already
+//                    sorted; only children with (r+1)(i+1) <= B can be kept,
+//                    and those runs are merged in log2(k) rounds of binary
+//                    searches.  The first B are the new list, handed over
+//                    (double-buffered, on named barriers) to four warps that
+//                    score it while the next depth is ranked: each entry
+//                    gathers its token's logit under every mode (full rows),
+//                    extends the per-mode path sums, and takes s_lse = log
+//                    sum_m exp(log pi_m + path sum - summed LSE), clamped to
+//                    its parent's key; it also extends a hash of its token
+//                    sequence.  Equal prefixes reached by several modes get
+//                    bit-identical keys and hashes.
 // lse_select_kernel  one CTA per tree.  Duplicates across modes are merged
-//                    depth by depth through a shared-memory hash on (parent's
-//                    representative, token) that keeps the first appearance
-//                    in (depth, mode, place) order.  A radix select on the
-//                    64-bit key image finds the B-th best, ties at it go by
-//                    that order, and a bitonic sort of the kept entries gives
-//                    the node order (parents first).
+//                    over groups of depths at once through a shared-memory
+//                    hash on (depth, token-sequence hash), every merge then
+//                    checked exactly (same depth, token and parent
+//                    representative; by induction over depth that makes the
+//                    classes exact); on a failed check the merge runs again
+//                    depth by depth on (parent's representative, token).  The
+//                    first appearance in (depth, mode, place) order represents
+//                    a prefix.  A radix select on the 64-bit key image finds
+//                    the B-th best, ties at it go by that order, and a
+//                    bitonic sort of the kept entries gives the node order
+//                    (parents first).
 #include "tsd_internal.cuh"
 
 namespace tsd {
 
-constexpr int kBeamThreads = 512;
 constexpr int kSelThreads = 1024;
 
 __device__ __forceinline__ double load_logit(const void* logits, tsd_dtype dtype, int64_t off) {
@@ -43,12 +51,27 @@ __device__ __forceinline__ double load_logit(const void* logits, tsd_dtype dtype
     return (double)reinterpret_cast<const float*>(logits)[off];
 }
 
+// Named barriers of the list kernel (0 is __syncthreads): the ranking warps
+// among themselves, and per list buffer "full" (a depth's list is ready for
+// scoring) and "free" (its scoring has read it).
+constexpr int kBeamThreads = 512;
+constexpr int kScoreThreads = 128;                          // the last four warps
+constexpr int kRankThreads = kBeamThreads - kScoreThreads;  // the first twelve
+constexpr int kBarRank = 1, kBarScore = 2, kBarFull = 3, kBarFree = 5;
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Merge of kf sorted runs of (k0, k1) pairs, run r at [off[r], off[r+1]), in
-// ceil(log2 kf) rounds: each round merges neighbouring groups of runs, and
-// every element finds its place by one binary search in the other half of its
-// group (keys are unique, so "less than" decides).  The second key is
-// (i << 5) | r, so an element's run is its rank r (its low 5 bits).  Returns 1 when the result is
-// in (d0, d1), 0 when in (k0, k1).
+// ceil(log2 kf) rounds, by the ranking threads: each round merges
+// neighbouring groups of runs, and every element finds its place by one
+// binary search in the other half of its group (keys are unique, so "less
+// than" decides).  The second key is (i << 5) | r, so an element's run is its
+// rank r (its low 5 bits).  Returns 1 when the result is in (d0, d1), 0 when
+// in (k0, k1).
 __device__ int merge_runs(unsigned long long* k0, unsigned* k1, unsigned long long* d0,
                           unsigned* d1, const int* off, int kf) {
     int flip = 0;
@@ -58,7 +81,7 @@ __device__ int merge_runs(unsigned long long* k0, unsigned* k1, unsigned long lo
         unsigned long long* b0 = flip ? k0 : d0;
         unsigned* b1 = flip ? k1 : d1;
         const int n = off[kf];
-        for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        for (int j = threadIdx.x; j < n; j += kRankThreads) {
             const unsigned long long x0 = a0[j];
             const unsigned x1 = a1[j];
             const int g = (int)(x1 & 31u) / (2 * w);  // the element's run is its rank
@@ -76,7 +99,7 @@ __device__ int merge_runs(unsigned long long* k0, unsigned* k1, unsigned long lo
             b0[pos] = x0;
             b1[pos] = x1;
         }
-        __syncthreads();
+        named_sync(kBarRank, kRankThreads);
         flip ^= 1;
     }
     return flip;
@@ -94,181 +117,203 @@ static __host__ __device__ int lse_sort_cap(int B, int k) {
 }
 
 size_t lse_beam_smem(int K, int B, int k) {
-    return sizeof(double) * (size_t)(2 * B * K + 4 * B + TSD_MAX_TOPK * (1 + TSD_MAX_MODES) +
-                                     3 * TSD_MAX_MODES) +
+    return sizeof(double) * (size_t)(2 * B * K + 4 * B + TSD_MAX_TOPK * (1 + TSD_MAX_MODES) + TSD_MAX_MODES) +
+           sizeof(unsigned long long) * (size_t)(2 * B) +
            2 * (sizeof(unsigned long long) + sizeof(unsigned)) * (size_t)lse_sort_cap(B, k) +
-           sizeof(int) * (size_t)(2 * B) + sizeof(unsigned long long) * (size_t)(2 * B);
+           sizeof(int) * (size_t)(4 * B + TSD_MAX_TOPK);
 }
 
+// One CTA per (mode, tree).  The first twelve warps rank: depth by depth they
+// build the mode's list (own-mode path sums only).  The last four score: a
+// depth's list, once handed over, gets its path sums under every mode, its
+// s_lse keys and its outputs, while the ranking warps already build the next
+// depth's list.  The hand-over is double-buffered (parent places, ranks and
+// the list size, by depth parity) on the "full" and "free" barriers.
 __global__ void __launch_bounds__(kBeamThreads, 1)
 lse_beam_kernel(const void* __restrict__ logits, tsd_dtype dtype, int K, int L, int64_t V, int k,
                 int B, double temp, const float* __restrict__ log_prior, BuildWs bws, LseWs ws) {
     pdl_entry();
     extern __shared__ __align__(16) unsigned char sml[];
     const int m = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
-    double* pm[2] = {reinterpret_cast<double*>(sml), reinterpret_cast<double*>(sml) + B * K};
-    double* ps[2] = {pm[1] + B * K, pm[1] + B * K + B};
-    double* sk[2] = {ps[1] + B, ps[1] + 2 * B};
-    double* zt = sk[1] + B;                     // [k] this mode's kept z/T at the current position
-    double* zall = zt + TSD_MAX_TOPK;           // [k][K] those tokens' z/T under every mode
-    double* cum = zall + TSD_MAX_TOPK * TSD_MAX_MODES;  // [K] summed log-normalisers so far
-    double* lp = cum + TSD_MAX_MODES;           // [K] log prior
-    double* cst = lp + TSD_MAX_MODES;           // [K] log prior - summed log-normalisers
-    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(cst + TSD_MAX_MODES);
+    double* pm = reinterpret_cast<double*>(sml);  // [2][B][K] path sums under every mode (scoring)
+    double* ps = pm + 2 * B * K;                  // [2][B] own-mode path sums (ranking)
+    double* sk = ps + 2 * B;                      // [2][B] keys (scoring)
+    double* zt = sk + 2 * B;                      // [k] this mode's kept z/T (ranking)
+    double* zall = zt + TSD_MAX_TOPK;             // [k][K] those tokens' z/T under every mode (scoring)
+    double* cst = zall + TSD_MAX_TOPK * TSD_MAX_MODES;  // [K] log prior - summed log-normalisers
+    unsigned long long* ph = reinterpret_cast<unsigned long long*>(cst + TSD_MAX_MODES);  // [2][B] path hashes
+    unsigned long long* ckey = ph + 2 * B;
     unsigned long long* ckey2 = ckey + lse_sort_cap(B, k);  // merge buffer
     unsigned* cidx = reinterpret_cast<unsigned*>(ckey2 + lse_sort_cap(B, k));
     unsigned* cidx2 = cidx + lse_sort_cap(B, k);
-    int* par = reinterpret_cast<int*>(cidx2 + lse_sort_cap(B, k));  // [B] parent place of each kept child
-    int* rk = par + B;                                        // [B] token rank of each kept child
-    unsigned long long* ph[2] = {reinterpret_cast<unsigned long long*>(rk + B),
-                                 reinterpret_cast<unsigned long long*>(rk + B) + B};  // path hashes
-    __shared__ int s_n, s_bad, s_kf;
+    int* par = reinterpret_cast<int*>(cidx2 + lse_sort_cap(B, k));  // [2][B] parent places (hand-over)
+    int* rk = par + 2 * B;                                          // [2][B] token ranks (hand-over)
+    int* tks = rk + 2 * B;                                          // [k] this mode's kept ids (scoring)
+    __shared__ int s_bad, s_kf;
+    __shared__ int s_nb[2];                  // list sizes (hand-over)
     __shared__ int s_off[TSD_MAX_TOPK + 1];  // offsets of the ranks' possible children
     const int64_t KB = (int64_t)K * B;
     const int64_t tree_rows = (int64_t)t * K * L;
     if (tid == 0) s_bad = 0;
-    if (tid < K) {
-        cum[tid] = 0.0;
-        lp[tid] = log_prior ? (double)log_prior[(int64_t)t * K + tid] : -log((double)K);
-    }
     __syncthreads();
     // a row without a finite log-normaliser poisons the tree: no lists at all
     for (int i = tid; i < K * L; i += blockDim.x)
         if (bws.lse[tree_rows + i] != bws.lse[tree_rows + i]) s_bad = 1;
     __syncthreads();
-    int np = 1, cur = 0;
-    // one depth ahead: this mode's kept z/T, every mode's log-normaliser, and
-    // the kept tokens' logits under every mode (gathered from the full rows);
-    // the kept tokens' ids two depths ahead, so that no gather waits for them
-    double f_zt = 0.0, f_lse = 0.0, f_z = 0.0;
-    int32_t f_tok = 0;
+    if (s_bad) {
+        for (int d = tid; d < L; d += blockDim.x) ws.nb[((int64_t)t * L + d) * K + m] = 0;
+        return;
+    }
+    if (tid < kRankThreads) {
+        // ranking: this mode's kept z/T one depth ahead
+        double f_zt = 0.0;
+        if (tid < k) f_zt = bws.top_zt[(tree_rows + (int64_t)m * L) * k + tid];
+        int np = 1, cur = 0;
+        for (int d = 0; d < L; ++d) {
+            const int buf = d & 1;
+            if (tid < k) zt[tid] = f_zt;
+            if (tid < k && d + 1 < L) f_zt = bws.top_zt[(tree_rows + (int64_t)m * L + d + 1) * k + tid];
+            const double* prev = ps + (cur ^ 1) * B;
+            named_sync(kBarRank, kRankThreads);
+            // Lists are sorted, and a lower rank has a larger z/T, so every
+            // child (i', r2) with i' <= i and r2 < r precedes child (i, r): its
+            // place is at least (r+1)(i+1) - 1, and only children with
+            // (r+1)(i+1) <= B can be kept.  Those with mass are ordered by
+            // (path sum desc, i asc, r asc) -- complemented order image, then
+            // (i << 5) | r -- by merging the per-rank runs, and the first B
+            // form the new list.
+            if (tid < kWarp) {  // ranks with mass come first: kf of them
+                const bool fin = tid < k && zt[tid] != -INFINITY;
+                const int kf = __popc(__ballot_sync(0xffffffffu, fin));
+                const int len = tid < kf ? min(np, B / (tid + 1)) : 0;
+                int incl = len;
+                for (int o = 1; o < kWarp; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                if (tid < kf) s_off[tid] = incl - len;  // exclusive offsets
+                if (tid == kWarp - 1) {                 // lane 31's inclusive sum is the total
+                    s_off[kf] = incl;
+                    s_kf = kf;
+                }
+            }
+            named_sync(kBarRank, kRankThreads);
+            const int kf = s_kf, nc = s_off[kf];
+            // run r holds rank r's possible children in parent order: already
+            // sorted by (complemented path-sum image, i k + r)
+            for (int j = tid; j < nc; j += kRankThreads) {
+                int r = 0;
+                while (s_off[r + 1] <= j) ++r;
+                const int i = j - s_off[r];
+                ckey[j] = ~order_key((d == 0 ? 0.0 : prev[i]) + zt[r]);
+                cidx[j] = ((unsigned)i << 5) | (unsigned)r;  // orders as (i, r); k <= 32
+            }
+            named_sync(kBarRank, kRankThreads);
+            const bool in2 = merge_runs(ckey, cidx, ckey2, cidx2, s_off, kf) != 0;
+            const unsigned long long* sk0 = in2 ? ckey2 : ckey;
+            const unsigned* sk1 = in2 ? cidx2 : cidx;
+            double* nps = ps + cur * B;
+            const int nkeep = nc < B ? nc : B;
+            if (d >= 2) named_sync(kBarFree + buf, kBeamThreads);  // depth d-2's list is scored
+            int* bpar = par + buf * B;
+            int* brk = rk + buf * B;
+            for (int j = tid; j < nkeep; j += kRankThreads) {
+                nps[j] = key_score(~sk0[j]);
+                bpar[j] = (int)(sk1[j] >> 5);
+                brk[j] = (int)(sk1[j] & 31u);
+            }
+            if (tid == 0) s_nb[buf] = nkeep;
+            named_arrive(kBarFull + buf, kBeamThreads);
+            np = nkeep;
+            cur ^= 1;
+        }
+        return;
+    }
+    // scoring: every mode's log-normaliser and this mode's kept ids one depth
+    // ahead, and the kept tokens' logits under every mode (gathered from the
+    // full rows); the ids behind that gather two depths ahead
+    const int st = tid - kRankThreads;
+    double cum = 0.0, lpv = 0.0;
+    if (st < K) lpv = log_prior ? (double)log_prior[(int64_t)t * K + st] : -log((double)K);
+    double f_lse = 0.0, f_z = 0.0;
+    int32_t f_tok = 0, f_id = 0;
     auto fetch_tok = [&](int d) {
-        if (tid < k * K) f_tok = bws.top_id[(tree_rows + (int64_t)m * L + d) * k + tid / K];
+        if (st < k * K) f_tok = bws.top_id[(tree_rows + (int64_t)m * L + d) * k + st / K];
     };
     auto fetch = [&](int d) {
         const int64_t row = tree_rows + (int64_t)m * L + d;
-        if (tid < k) f_zt = bws.top_zt[row * k + tid];
-        if (tid < K) f_lse = bws.lse[tree_rows + (int64_t)tid * L + d];
-        if (tid < k * K)
-            f_z = load_logit(logits, dtype, (tree_rows + (int64_t)(tid % K) * L + d) * V + f_tok);
+        if (st < k) f_id = bws.top_id[row * k + st];
+        if (st < K) f_lse = bws.lse[tree_rows + (int64_t)st * L + d];
+        if (st < k * K)
+            f_z = load_logit(logits, dtype, (tree_rows + (int64_t)(st % K) * L + d) * V + f_tok);
     };
-    if (!s_bad) {
-        fetch_tok(0);
-        fetch(0);
-        if (L > 1) fetch_tok(1);
-    }
+    fetch_tok(0);
+    fetch(0);
+    if (L > 1) fetch_tok(1);
+    int cur = 0;
     for (int d = 0; d < L; ++d) {
-        const int64_t row = tree_rows + (int64_t)m * L + d;
-        int32_t* nb_out = ws.nb + ((int64_t)t * L + d) * K + m;
-        if (s_bad) {
-            if (tid == 0) *nb_out = 0;
-            continue;
+        const int buf = d & 1;
+        if (st < k) tks[st] = f_id;
+        if (st < K) {
+            cum += f_lse;
+            cst[st] = lpv - cum;
         }
-        if (tid < k) zt[tid] = f_zt;
-        if (tid < K) {
-            cum[tid] = cum[tid] + f_lse;
-            cst[tid] = lp[tid] - cum[tid];
-        }
-        if (tid < k * K) zall[tid] = temp == 1.0 ? f_z : f_z / temp;  // z / T_d
+        if (st < k * K) zall[st] = temp == 1.0 ? f_z : f_z / temp;  // z / T_d
         if (d + 1 < L) fetch(d + 1);  // f_tok holds depth d+1's ids
         if (d + 2 < L) fetch_tok(d + 2);
-        if (tid == 0) s_n = 0;
-        const double* prev = ps[cur ^ 1];
-        __syncthreads();
-        // Lists are sorted, and a lower rank has a larger z/T, so every child
-        // (i', r2) with i' <= i and r2 < r precedes child (i, r): its place is
-        // at least (r+1)(i+1) - 1, and only children with (r+1)(i+1) <= B can
-        // be kept.  Those with mass are ordered by (path sum desc, i asc, r
-        // asc) -- complemented order image, then (i << 5) | r -- by merging
-        // the per-rank runs, and the first B form the new list.
-        if (tid < kWarp) {  // ranks with mass come first: kf of them
-            const bool fin = tid < k && zt[tid] != -INFINITY;
-            const int kf = __popc(__ballot_sync(0xffffffffu, fin));
-            const int len = tid < kf ? min(np, B / (tid + 1)) : 0;
-            int incl = len;
-            for (int o = 1; o < kWarp; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += y;
-            }
-            if (tid < kf) s_off[tid] = incl - len;  // exclusive offsets
-            if (tid == kWarp - 1) {                 // lane 31's inclusive sum is the total
-                s_off[kf] = incl;
-                s_kf = kf;
-            }
-        }
-        __syncthreads();
-        const int kf = s_kf, nc = s_off[kf];
-        // run r holds rank r's possible children in parent order: already
-        // sorted by (complemented path-sum image, i k + r)
-        for (int j = tid; j < nc; j += blockDim.x) {
-            int r = 0;
-            while (s_off[r + 1] <= j) ++r;
-            const int i = j - s_off[r];
-            ckey[j] = ~order_key((d == 0 ? 0.0 : prev[i]) + zt[r]);
-            cidx[j] = ((unsigned)i << 5) | (unsigned)r;  // orders as (i, r); k <= 32
-        }
-        __syncthreads();
-        const bool in2 = merge_runs(ckey, cidx, ckey2, cidx2, s_off, kf) != 0;
-        const unsigned long long* sk0 = in2 ? ckey2 : ckey;
-        const unsigned* sk1 = in2 ? cidx2 : cidx;
-        double* nps = ps[cur];
-        const int nkeep = nc < B ? nc : B;
-        for (int j = tid; j < nkeep; j += blockDim.x) {
-            nps[j] = key_score(~sk0[j]);
-            par[j] = (int)(sk1[j] >> 5);
-            rk[j] = (int)(sk1[j] & 31u);
-        }
-        if (tid == 0) s_n = nkeep;
-        __syncthreads();
-        const int nb = s_n;
-        // path sums under every mode
-        const double* opm = pm[cur ^ 1];
-        double* npm = pm[cur];
-        for (int e = tid; e < nb * K; e += blockDim.x) {
-            const int j = e / K, m2 = e - j * K;
-            if (!(TSD_IN(par[j], B, kChkLse) && TSD_IN(rk[j], k, kChkLse))) continue;
-            npm[e] = (d == 0 ? 0.0 : opm[par[j] * K + m2]) + zall[rk[j] * K + m2];
-        }
-        __syncthreads();
-        const double* osk = sk[cur ^ 1];
-        double* nsk = sk[cur];
+        named_sync(kBarFull + buf, kBeamThreads);  // the list, and this group's inputs
+        const int nb = s_nb[buf];
+        const int* bpar = par + buf * B;
+        const int* brk = rk + buf * B;
+        const double* opm = pm + (cur ^ 1) * B * K;
+        double* npm = pm + cur * B * K;
+        const double* osk = sk + (cur ^ 1) * B;
+        double* nsk = sk + cur * B;
+        const unsigned long long* oph = ph + (cur ^ 1) * B;
+        unsigned long long* nph = ph + cur * B;
         // s_lse of each entry: the terms log pi + log Q in float64 (path sum
         // plus the depth's constant log pi - summed LSE), the sum of
-        // exp(term - largest) in fp32
-        for (int j = tid; j < nb; j += blockDim.x) {
+        // exp(term - largest) in fp32; one thread per entry, so that the
+        // float64 instructions run on full warps
+        for (int j = st; j < nb; j += kScoreThreads) {
+            const int pj = bpar[j], rj = brk[j];
+            if (!(TSD_IN(pj, B, kChkLse) && TSD_IN(rj, k, kChkLse))) continue;
             double a[TSD_MAX_MODES];
             double amax = -INFINITY;
-            for (int m2 = 0; m2 < K; ++m2) {
-                a[m2] = npm[j * K + m2] + cst[m2];
+#pragma unroll
+            for (int m2 = 0; m2 < TSD_MAX_MODES; ++m2) {
+                if (m2 >= K) break;
+                const double P = (d == 0 ? 0.0 : opm[pj * K + m2]) + zall[rj * K + m2];
+                npm[j * K + m2] = P;
+                a[m2] = P + cst[m2];
                 amax = fmax(amax, a[m2]);
             }
             double s = -INFINITY;
             if (amax > -INFINITY) {
                 float acc = 0.0f;
-                for (int m2 = 0; m2 < K; ++m2) acc += expf((float)(a[m2] - amax));
+#pragma unroll
+                for (int m2 = 0; m2 < TSD_MAX_MODES; ++m2) {
+                    if (m2 >= K) break;
+                    acc += expf((float)(a[m2] - amax));
+                }
                 s = amax + (double)logf(acc);
             }
-            const double up = d == 0 ? INFINITY : osk[par[j]];
+            const double up = d == 0 ? INFINITY : osk[pj];
             const double key = s < up ? s : up;
             nsk[j] = key;
             const int64_t f = (int64_t)t * L * KB + (int64_t)d * KB + (int64_t)m * B + j;
-            const int32_t x = bws.top_id[row * k + rk[j]];
-            const unsigned long long hv = hash_step(d == 0 ? kRootHash : ph[cur ^ 1][par[j]], x);
-            ph[cur][j] = hv;
+            const int32_t x = tks[rj];
+            const unsigned long long hv = hash_step(d == 0 ? kRootHash : oph[pj], x);
+            nph[j] = hv;
             ws.tok[f] = x;
-            ws.par[f] = par[j];
+            ws.par[f] = pj;
             ws.kimg[f] = ~order_key(key);
             ws.phash[f] = hv;
         }
-        if (tid == 0) *nb_out = nb;
-        np = nb;
+        if (st == 0) ws.nb[((int64_t)t * L + d) * K + m] = nb;
+        if (d + 2 < L) named_arrive(kBarFree + buf, kBeamThreads);
+        named_sync(kBarScore, kScoreThreads);  // this depth's sums before the next depth's inputs
         cur ^= 1;
-        __syncthreads();
-        if (np == 0) {  // nothing finite at this depth: deeper lists are empty too
-            for (int d2 = d + 1 + tid; d2 < L; d2 += blockDim.x)
-                ws.nb[((int64_t)t * L + d2) * K + m] = 0;
-            break;
-        }
     }
 }
 
