@@ -377,6 +377,32 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long x, unsigned
     return r;
 }
 
+// Block-wide AND and OR of one 64-bit value per thread, into *band / *bor.
+__device__ void block_and_or(unsigned long long a, unsigned long long o, unsigned long long* red,
+                             unsigned long long* band, unsigned long long* bor) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int k = 1; k < 32; k <<= 1) {
+        a &= __shfl_xor_sync(0xffffffffu, a, k);
+        o |= __shfl_xor_sync(0xffffffffu, o, k);
+    }
+    if (lane == 0) {
+        red[wid] = a;
+        red[32 + wid] = o;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long A = ~0ull, O = 0ull;
+        for (int w = 0; w < nw; ++w) {
+            A &= red[w];
+            O |= red[32 + w];
+        }
+        *band = A;
+        *bor = O;
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ bool pair_less(unsigned long long a0, unsigned long long a1,
                                           unsigned long long b0, unsigned long long b1) {
     return a0 < b0 || (a0 == b0 && a1 < b1);
@@ -409,8 +435,8 @@ constexpr unsigned long long kGroupKeyMask = ~0ull >> kFlatBits;
 // After the merge, the candidates (image, flat index) stay in shared memory,
 // after the sort buffer, when every list entry fits there.
 constexpr size_t kSelSmemCap = 200 * 1024;
-static __host__ __device__ size_t lse_sel_sort_bytes(int B) {
-    return (size_t)2 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
+static __host__ __device__ size_t lse_sel_sort_bytes(int B) {  // the kept entries, twice
+    return (size_t)4 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
 }
 static __host__ __device__ bool lse_cands_in_smem(int K, int B, int L) {
     return lse_sel_sort_bytes(B) + (size_t)L * K * B * (sizeof(unsigned long long) + sizeof(int32_t)) <=
@@ -483,6 +509,11 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
     //    If one fails (a hash collision), the merge runs again depth by depth
     //    on (parent's representative, token), which needs no hash.
     __shared__ int s_fail;
+    __shared__ unsigned long long red64a[2 * 32], s_and, s_or;
+    if (tid == 0) {
+        s_and = 0ull;  // no common leading bits known (the depth-by-depth merge)
+        s_or = ~0ull;
+    }
     int n_f = 0;
     // the candidates: in shared memory after the sort buffer when they fit
     // (the grouped merge's table is dead by then), else in the workspace
@@ -563,36 +594,64 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             __syncthreads();
         }
         if (!s_fail) {
-            // compaction in flat order, four consecutive entries a thread; an
-            // entry's representative and image are loaded together
-            for (int64_t c0 = 0; c0 < N; c0 += 4 * blockDim.x) {
-                int cnt = 0;
-                bool kp[4];
-                unsigned long long im[4];
+            // compaction in flat order, in the candidate buffer itself: first
+            // every entry's image and keep mark at its own flat index (the
+            // representatives and images loaded eight at a time), then the
+            // kept ones moved forward chunk by chunk (a candidate's place
+            // never exceeds its flat index, and a chunk is read before its
+            // scan's barriers)
+            unsigned long long and_img = ~0ull, or_img = 0ull;
+            for (int64_t c0 = 0; c0 < N; c0 += 8 * blockDim.x) {
+                int r[8];
+                unsigned long long im[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int64_t c = c0 + 4 * tid + q;
+                for (int q = 0; q < 8; ++q) {
+                    const int64_t c = c0 + q * blockDim.x + tid;
                     bool lv = false;
                     if (c < N) {
                         const int d = (int)(c / KB), e = (int)(c - (int64_t)d * KB);
                         lv = e % B < nbs[d * K + e / B];
                     }
-                    const int r = lv ? ws.rep[base + c] : -1;
+                    r[q] = lv ? ws.rep[base + c] : -1;
                     im[q] = lv ? ws.kimg[base + c] : ~kNegInfImage;
-                    kp[q] = r == (int)c && im[q] != ~kNegInfImage;
-                    cnt += kp[q];
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int64_t c = c0 + q * blockDim.x + tid;
+                    if (c >= N) continue;
+                    const bool kp = r[q] == (int)c && im[q] != ~kNegInfImage;
+                    cimg_p[c] = im[q];
+                    cflat_p[c] = kp ? (int32_t)c : -1;
+                    if (kp) {
+                        and_img &= im[q];
+                        or_img |= im[q];
+                    }
+                }
+            }
+            block_and_or(and_img, or_img, red64a, &s_and, &s_or);  // also orders the marks
+            for (int64_t c0 = 0; c0 < N; c0 += 4 * blockDim.x) {
+                int32_t fl[4];
+                unsigned long long im[4];
+                int cnt = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t c = c0 + 4 * tid + q;
+                    fl[q] = c < N ? cflat_p[c] : -1;
+                    im[q] = c < N ? cimg_p[c] : 0ull;
+                    cnt += fl[q] >= 0;
                 }
                 int tot;
                 int pos = n_f + block_excl_scan_i(cnt, red, &tot);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    if (!kp[q]) continue;
+                    if (fl[q] < 0) continue;
                     cimg_p[pos] = im[q];
-                    cflat_p[pos] = (int32_t)(c0 + 4 * tid + q);
+                    cflat_p[pos] = fl[q];
                     ++pos;
                 }
                 n_f += tot;
             }
+            __syncthreads();
         }
     }
     if (s_fail && KB > 0) {
@@ -693,8 +752,25 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
     unsigned long long prefix = 0, mask = 0;
     int need = take;  // 1-based rank of the threshold among the remaining
     const bool cut = n_f > B;
+    // the candidates' images agree above the highest bit where they differ:
+    // the select starts at that bit's byte
+    const unsigned long long diff = s_and ^ s_or;
+    int shift0 = 56;
     if (take > 0 && cut) {
-        for (int shift = 56; shift >= 0; shift -= 8) {
+        if (diff == 0ull) {  // every candidate has the same image: it is the threshold
+            shift0 = -8;
+            mask = ~0ull;
+            prefix = s_and;
+        } else {
+            shift0 = ((63 - __clzll((long long)diff)) / 8) * 8;
+            if (shift0 < 56) {
+                mask = ~((1ull << (shift0 + 8)) - 1);  // the bits above byte shift0
+                prefix = s_and & mask;
+            }
+        }
+    }
+    if (take > 0 && cut) {
+        for (int shift = shift0; shift >= 0; shift -= 8) {
             if (tid < 256) hist[tid] = 0;
             __syncthreads();
             for (int c0 = 0; c0 < n_f; c0 += 4 * blockDim.x) {
@@ -794,32 +870,38 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         sk1[i] = kEmpty;
     }
     __syncthreads();
-    // 4. order the kept entries by (image asc, flat index asc)
-    for (int kk = 2; kk <= n2; kk <<= 1) {
-        for (int j = kk >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < n2; i += blockDim.x) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const unsigned long long a0 = sk0[i], a1 = sk1[i], b0 = sk0[l], b1 = sk1[l];
-                    if (((i & kk) == 0) == pair_less(b0, b1, a0, a1)) {
-                        sk0[i] = b0;
-                        sk1[i] = b1;
-                        sk0[l] = a0;
-                        sk1[l] = a1;
-                    }
-                }
+    // 4. order the kept entries by (image asc, flat index asc): an entry's
+    //    place is the number of entries before it, counted by P threads
+    unsigned long long* so0 = sk0 + 2 * pow2_ceil(B < 32 ? 32 : B);
+    unsigned long long* so1 = so0 + pow2_ceil(B < 32 ? 32 : B);
+    {
+        int P = 1;
+        while (P < 32 && take > 0 && 2 * P * take <= (int)blockDim.x) P <<= 1;
+        for (int i0 = 0; i0 < take; i0 += blockDim.x / P) {  // block-uniform
+            const int i = i0 + tid / P, sub = tid % P;
+            int cnt = 0;
+            unsigned long long a0 = 0ull, a1 = 0ull;
+            if (i < take) {
+                a0 = sk0[i];
+                a1 = sk1[i];
+                for (int j = sub; j < take; j += P) cnt += pair_less(sk0[j], sk1[j], a0, a1) ? 1 : 0;
             }
-            __syncthreads();
+            for (int o = 1; o < P; o <<= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (i < take && sub == 0 && cnt < take) {
+                so0[cnt] = a0;
+                so1[cnt] = a1;
+            }
         }
     }
+    __syncthreads();
     // 5. emit: node q+1 is the q-th kept entry; parents come first
     for (int q = tid; q < take; q += blockDim.x)
-        if (sk1[q] < (unsigned long long)N) ws.node_of[base + (int64_t)sk1[q]] = q + 1;
+        if (so1[q] < (unsigned long long)N) ws.node_of[base + (int64_t)so1[q]] = q + 1;
     __syncthreads();
     for (int q = tid; q < B; q += blockDim.x) {
         const int64_t o = out0 + 1 + q;
-        if (q < take && sk1[q] < (unsigned long long)N) {
-            const int64_t f = (int64_t)sk1[q];
+        if (q < take && so1[q] < (unsigned long long)N) {
+            const int64_t f = (int64_t)so1[q];
             const int d = (int)(f / KB), e = (int)(f - (int64_t)d * KB), m = e / B;
             int pn = 0;
             if (d > 0) {
