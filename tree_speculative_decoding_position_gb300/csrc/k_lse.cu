@@ -434,9 +434,12 @@ constexpr unsigned long long kGroupKeyMask = ~0ull >> kFlatBits;
 
 // After the merge, the candidates (image, flat index) stay in shared memory,
 // after the sort buffer, when every list entry fits there.
-constexpr size_t kSelSmemCap = 200 * 1024;
-static __host__ __device__ size_t lse_sel_sort_bytes(int B) {  // the kept entries, twice
-    return (size_t)4 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B);
+constexpr size_t kSelSmemCap = 220 * 1024;
+constexpr int kSurvivors = 2048;  // the radix select's gathered bucket
+// the kept entries twice (merged order, node order), then the gathered bucket
+static __host__ __device__ size_t lse_sel_sort_bytes(int B) {
+    return (size_t)4 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B) +
+           sizeof(unsigned long long) * kSurvivors;
 }
 static __host__ __device__ bool lse_cands_in_smem(int K, int B, int L) {
     return lse_sel_sort_bytes(B) + (size_t)L * K * B * (sizeof(unsigned long long) + sizeof(int32_t)) <=
@@ -462,7 +465,7 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
     __shared__ int red[33];
     __shared__ unsigned hist[256];
     __shared__ int nbs[TSD_MAX_L * TSD_MAX_MODES];
-    __shared__ int s_bad, s_bucket, s_need;
+    __shared__ int s_bad, s_bucket, s_need, s_count, s_ns;
     const int t = blockIdx.x, tid = threadIdx.x;
     const int KB = K * B;
     const int64_t N = (int64_t)L * KB;
@@ -526,6 +529,13 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         unsigned long long* gtab = reinterpret_cast<unsigned long long*>(sms);
         int16_t* gslot = reinterpret_cast<int16_t*>(gtab + kGroupSlots);
         const int G = KB > 0 ? kGroupSlots / (2 * KB) : 1;
+        const FastDiv fKB((unsigned)(KB > 0 ? KB : 1)), fB((unsigned)(B > 0 ? B : 1));
+        // an entry i of the group (flat index d0 K B + i): its depth offset,
+        // mode and place, and whether its place is in the mode's list
+        auto in_list = [&](int d, int e) {
+            const int mm = (int)fB.div((unsigned)e);
+            return e - mm * B < nbs[d * K + mm];
+        };
         for (int h = tid; h < kGroupSlots; h += blockDim.x) gtab[h] = kEmpty;
         __syncthreads();
         for (int d0 = 0; d0 < L && KB > 0; d0 += G) {
@@ -536,15 +546,15 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
 #pragma unroll
             for (int q = 0; q < kGroupPer; ++q) {
                 const int i = tid + q * kSelThreads;
-                const int d = d0 + i / KB, e = i % KB;
-                in[q] = i < ne && e % B < nbs[d * K + e / B];
+                const int qd = (int)fKB.div((unsigned)i);
+                in[q] = i < ne && in_list(d0 + qd, i - qd * KB);
                 hv[q] = in[q] ? ws.phash[base + (int64_t)d0 * KB + i] : 0ull;
             }
 #pragma unroll
             for (int q = 0; q < kGroupPer; ++q) {
                 const int i = tid + q * kSelThreads;
                 if (i >= ne) continue;
-                const int d = d0 + i / KB;
+                const int d = d0 + (int)fKB.div((unsigned)i);
                 int slot = -1;
                 if (in[q]) {
                     const int f = d0 * KB + i;
@@ -575,14 +585,14 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             bool fail = false;
             for (int i = tid; i < ne; i += blockDim.x) {
                 if (gslot[i] < 0) continue;
-                const int f = d0 * KB + i, d = f / KB;
+                const int f = d0 * KB + i, d = (int)fKB.div((unsigned)f);
                 const int r = ws.rep[base + f];
                 if (r == f) continue;
-                const int dr = r / KB;
+                const int dr = (int)fKB.div((unsigned)r);
                 bool same = dr == d && r < f && ws.tok[base + r] == ws.tok[base + f];
                 if (same && d > 0) {
                     const int pf = ws.par[base + f], pr = ws.par[base + r];
-                    const int mf = (f - d * KB) / B, mr = (r - d * KB) / B;
+                    const int mf = (int)fB.div((unsigned)(f - d * KB)), mr = (int)fB.div((unsigned)(r - d * KB));
                     same = TSD_IN(pf, B, kChkLse) && TSD_IN(pr, B, kChkLse) &&
                            ws.rep[base + (int64_t)(d - 1) * KB + mf * B + pf] ==
                                ws.rep[base + (int64_t)(d - 1) * KB + mr * B + pr];
@@ -609,8 +619,8 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
                     const int64_t c = c0 + q * blockDim.x + tid;
                     bool lv = false;
                     if (c < N) {
-                        const int d = (int)(c / KB), e = (int)(c - (int64_t)d * KB);
-                        lv = e % B < nbs[d * K + e / B];
+                        const int d = (int)fKB.div((unsigned)c);
+                        lv = in_list(d, (int)c - d * KB);
                     }
                     r[q] = lv ? ws.rep[base + c] : -1;
                     im[q] = lv ? ws.kimg[base + c] : ~kNegInfImage;
@@ -770,20 +780,27 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         }
     }
     if (take > 0 && cut) {
+        // the passes read the candidates until the selected bucket holds at
+        // most kSurvivors of them; those are then gathered (in any order: a
+        // histogram needs none) and the later passes read only them
+        unsigned long long* surv = reinterpret_cast<unsigned long long*>(sms) + 4 * pow2_ceil(B < 32 ? 32 : B);
+        const unsigned long long* src = cimg;
+        int nsrc = n_f;
+        bool gathered = false;
         for (int shift = shift0; shift >= 0; shift -= 8) {
             if (tid < 256) hist[tid] = 0;
             __syncthreads();
-            for (int c0 = 0; c0 < n_f; c0 += 4 * blockDim.x) {
+            for (int c0 = 0; c0 < nsrc; c0 += 4 * blockDim.x) {
                 unsigned long long v[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c = c0 + q * blockDim.x + tid;
-                    v[q] = c < n_f ? cimg[c] : ~0ull;
+                    v[q] = c < nsrc ? src[c] : ~0ull;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c = c0 + q * blockDim.x + tid;
-                    if (c < n_f && (v[q] & mask) == prefix)
+                    if (c < nsrc && (v[q] & mask) == prefix)
                         atomicAdd(&hist[(unsigned)(v[q] >> shift) & 255u], 1u);
                 }
             }
@@ -807,16 +824,31 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
                         if ((unsigned)need <= before + v[q]) {
                             s_bucket = tid * 8 + q;
                             s_need = need - (int)before;
+                            s_count = (int)v[q];
                             break;
                         }
                         before += v[q];
                     }
                 }
             }
+            if (tid == 0) s_ns = 0;
             __syncthreads();
             prefix |= (unsigned long long)s_bucket << shift;
             mask |= 255ull << shift;
             need = s_need;
+            if (!gathered && shift > 0 && s_count <= kSurvivors) {
+                for (int c = tid; c < nsrc; c += blockDim.x) {
+                    const unsigned long long v = src[c];
+                    if ((v & mask) == prefix) {
+                        const int pos = atomicAdd(&s_ns, 1);
+                        if (pos < kSurvivors) surv[pos] = v;
+                    }
+                }
+                __syncthreads();
+                src = surv;
+                nsrc = min(s_ns, kSurvivors);
+                gathered = true;
+            }
             __syncthreads();
         }
     }

@@ -271,6 +271,27 @@ struct Lanes<float> {
 
 // Order-preserving 64-bit image of a float64 score (larger score, larger
 // key; -inf the smallest of the finite-or-infinite values), and its inverse.
+// Division of 32-bit unsigned integers by a divisor fixed at run time, as a
+// multiply-high and two shifts (Granlund and Montgomery, "Division by
+// Invariant Integers using Multiplication", 1994, Sec. 4): with l = ceil(log2
+// d) and m = floor(2^32 (2^l - d) / d) + 1, t = mulhi(m, x) gives
+// x / d = (t + ((x - t) >> min(l, 1))) >> max(l - 1, 0) for every 32-bit x.
+struct FastDiv {
+    unsigned d = 1, m = 1, s1 = 0, s2 = 0;
+    FastDiv() = default;
+    __host__ __device__ explicit FastDiv(unsigned div) : d(div) {
+        unsigned l = 0;
+        while (l < 32 && (1ull << l) < div) ++l;
+        m = (unsigned)(((((1ull << l) - div) << 32) / div) + 1);
+        s1 = l < 1 ? l : 1;
+        s2 = l > 1 ? l - 1 : 0;
+    }
+    __device__ __forceinline__ unsigned div(unsigned x) const {
+        const unsigned t = __umulhi(m, x);
+        return (t + ((x - t) >> s1)) >> s2;
+    }
+};
+
 // Hash of a token sequence, one token at a time from the root's value: a
 // strong 64-bit mix of (parent hash, token), a SplitMix64-style finaliser.
 // Equal sequences get equal hashes; users confirm every match exactly.
