@@ -157,3 +157,25 @@ def test_lse_tree_large_budget_from_pinned_host(tsd, dev, orc):
         assert int(out["n_cand"][t]) == ref["n_cand"]
         flips += _compare(out, t, ref, z, 1.0, k, None)
     assert flips <= 4
+
+
+@pytest.mark.parametrize("case", ["k8_b128_l11", "k3_b100_l28"])
+def test_lse_tree_merge_groups(tsd, dev, orc, case):
+    """The selection merges duplicates over groups of kGroupSlots / (2 K B)
+    depths: a last group shorter than the others (K = 8, B = 128, L = 11:
+    groups of 8 and 3 depths) and a K B that does not divide the table
+    (K = 3, B = 100, L = 28: groups of 27 and 1)."""
+    if case == "k8_b128_l11":
+        nt, K, L, V, k, B = 2, 8, 11, 3000, 8, 128
+    else:
+        nt, K, L, V, k, B = 2, 3, 28, 2000, 4, 100  # L ceil(log2 k) <= 56
+    dr, _, _ = synth.mixture_drafter(nt, K, L, V, synth.seed_for(14, K), dtype=torch.float32)
+    out = tsd.tsd_build_lse_tree(dr.to(dev), topk=k, B=B)
+    assert out["status"].cpu().tolist() == [0] * nt
+    flips = 0
+    for t in range(nt):
+        z = dr[t].double().numpy()
+        ref = orc.lse_tree(z, 1.0, k, B)
+        assert int(out["n_cand"][t]) == ref["n_cand"]
+        flips += _compare(out, t, ref, z, 1.0, k, None)
+    assert flips <= 4
