@@ -22,41 +22,66 @@ namespace tsd {
 
 constexpr int kExitThreads = 256;
 
-// Statistics of one row of z / T_d from its chunk statistics as the
-// builder's row kernel forms them, by one warp: the scaled maximum mc and the
-// float64 sum S = sum over chunks of s 2^(m c - mc), so that
-// LSE = ln 2 * (mc + log2 S).  *bad when a chunk saw a NaN or +inf or the row
-// has no mass.
-__device__ void row_stats(const ChunkStat* __restrict__ cs, int nch, float c, int lane, float* mc_out,
-                          double* s_out, bool* bad_out) {
-    float m = -INFINITY;
-    bool bad = false;
+// Statistics of two rows of z / T_d from their chunk statistics as the
+// builder's row kernel forms them, by one warp (the second row at cs + off2;
+// off2 < 0: none, its results unused): the scaled maximum mc and the float64
+// sum S = sum over chunks of s 2^(m c - mc), so that LSE = ln 2 * (mc +
+// log2 S); bad when a chunk saw a NaN or +inf or the row has no mass.  The
+// two rows' loads and float64 sums are interleaved so that their latencies
+// overlap.
+__device__ void row_stats_pair(const ChunkStat* __restrict__ cs, int64_t off2, int nch, float c,
+                               int lane, float* mc_out, double* s_out, bool* bad_out) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+    bool b0 = false, b1 = false;
+    const ChunkStat* cs1 = off2 >= 0 ? cs + off2 : cs;
     for (int q = lane; q < nch; q += kWarp) {
-        m = fmaxf(m, cs[q].m);
-        bad |= (cs[q].s != cs[q].s);
+        const ChunkStat x0 = cs[q], x1 = cs1[q];
+        m0 = fmaxf(m0, x0.m);
+        b0 |= (x0.s != x0.s);
+        m1 = fmaxf(m1, x1.m);
+        b1 |= (x1.s != x1.s);
     }
-    m = warp_max(m);
-    const float mc = __fmul_rn(m, c);
-    double s = 0.0;
-    for (int q = lane; q < nch; q += kWarp)
-        if (cs[q].m != -INFINITY) s += (double)cs[q].s * (double)ex2(__fmul_rn(cs[q].m, c) - mc);
-    s = warp_sum_d(s);
-    *mc_out = mc;
-    *s_out = s;
-    *bad_out = __any_sync(0xffffffffu, bad) || m == -INFINITY || !(s > 0.0);
+    m0 = warp_max(m0);
+    m1 = warp_max(m1);
+    const float mc0 = __fmul_rn(m0, c), mc1 = __fmul_rn(m1, c);
+    double s0 = 0.0, s1 = 0.0;
+    for (int q = lane; q < nch; q += kWarp) {
+        const ChunkStat x0 = cs[q], x1 = cs1[q];
+        if (x0.m != -INFINITY) s0 += (double)x0.s * (double)ex2(__fmul_rn(x0.m, c) - mc0);
+        if (x1.m != -INFINITY) s1 += (double)x1.s * (double)ex2(__fmul_rn(x1.m, c) - mc1);
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+    mc_out[0] = mc0;
+    mc_out[1] = mc1;
+    s_out[0] = s0;
+    s_out[1] = s1;
+    bad_out[0] = __any_sync(0xffffffffu, b0) || m0 == -INFINITY || !(s0 > 0.0);
+    bad_out[1] = __any_sync(0xffffffffu, b1) || m1 == -INFINITY || !(s1 > 0.0);
 }
 
-// One CTA per tree.  The float64 pipe is narrow, so each float64 step is
-// taken once where it can be: one warp per row forms (mc, S); one warp then
-// takes the logarithm of every row at once (row m on lane m, L <= 32); the
-// nodes' terms follow, and the per-row weights W_m are summed by one warp per
-// row over the nodes' (depth, weight) pairs in node order (deterministic, no
-// atomics), re-read from global memory rather than staged in shared memory:
-// this kernel launches early behind the persistent chunk pass, and a CTA that
-// needs more shared memory than that pass's carveout leaves free waits for
-// its SM to drain.  The last CTA to finish (a completion counter; no CTA waits for
+// One CTA per tree.  A tree's numerator sum_v w(v) (LSE_{d(v)} - z_v / T_d)
+// is sum_m LSE_m W_m - (1 / T_d) sum_v w(v) z_v, with W_m the weight on row m
+// (Eq. 67).  Both W_m and sum_v w(v) z_v need only this call's inputs, so the
+// kernel forms them before it waits for the chunk pass: that pass lets this
+// kernel be scheduled only after its own wait, so every input is complete by
+// then, and the work overlaps the pass.  After the wait: one warp per row
+// forms (mc, S) from the chunk statistics, one warp takes the logarithm of
+// every row at once (row m on lane m, L <= 32) and the L products.  The float64
+// pipe is narrow (64 clocks a warp instruction), so each float64 step is taken
+// once, on full warps where it can be.  W_m is summed by one warp per row over
+// the nodes in node order (deterministic, no atomics), reading (depth, weight)
+// from global memory rather than staging them in shared memory: this kernel
+// launches early behind the persistent chunk pass, and a CTA that needs more
+// shared memory than that pass's carveout leaves free waits for its SM to
+// drain.  The last CTA to finish (a completion counter; no CTA waits for
 // another) forms the scalar loss from the valid trees' numerators and
-// (n_nodes - 1).
+// (n_nodes - 1).  A tree is malformed when n_nodes or a node's depth or token
+// is out of range, and non-finite when some w(v) z_v is, or a row holding a
+// node has no finite log-normaliser.
 template <typename T>
 __global__ void __launch_bounds__(kExitThreads)
 exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, int nch, float c,
@@ -64,8 +89,9 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes, int B,
                  const float* __restrict__ omega, double* __restrict__ loss_tree,
                  double* __restrict__ loss, int32_t* __restrict__ status, ExitWs ws) {
-    pdl_entry();
     __shared__ double lse[TSD_MAX_L];
+    __shared__ double wrow[TSD_MAX_L];
+    __shared__ int nrow[TSD_MAX_L];
     __shared__ double srow[TSD_MAX_L];
     __shared__ float mcrow[TSD_MAX_L];
     __shared__ int badrow[TSD_MAX_L];
@@ -74,29 +100,12 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), wid = tid / kWarp;
     const int nw = blockDim.x / kWarp;
     const int stride = B + 1;
+    // ---- before the wait: this call's inputs only ----
     const int n = n_nodes[t];
     if (tid == 0) bad = (n < 1 || n > stride) ? kStatBadTree : kStatOk;
-    for (int m = wid; m < L; m += nw) {
-        float mc;
-        double s;
-        bool b;
-        row_stats(ws.rows.chunk + ((int64_t)t * L + m) * nch, nch, c, lane, &mc, &s, &b);
-        if (lane == 0) {
-            mcrow[m] = mc;
-            srow[m] = s;
-            badrow[m] = b;
-        }
-    }
     __syncthreads();
-    if (wid == 0 && lane < L) {
-        const double l = badrow[lane] ? __longlong_as_double(0x7ff8000000000000ll)
-                                      : 0.6931471805599453 * ((double)mcrow[lane] + log2(srow[lane]));
-        lse[lane] = l;
-        ws.lse[(int64_t)t * L + lane] = l;
-    }
-    __syncthreads();
-    double part = 0.0;
     const int nv = bad == kStatOk ? n : 1;
+    double azp = 0.0;  // sum of w(v) z_v over this thread's nodes
     for (int v = 1 + tid; v < nv; v += blockDim.x) {
         const int d = depth[(int64_t)t * stride + v];
         const int x = token[(int64_t)t * stride + v];
@@ -104,33 +113,78 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
             atomicExch(&bad, kStatBadTree);
             continue;
         }
-        const float wf = omega[(int64_t)t * stride + v];
-        const double w = (double)wf;
-        const int64_t row = (int64_t)t * L + d - 1;
-        const double z = (double)load_logit(logits + row * V + x);
-        const double term = w * (lse[d - 1] - z * inv_temp);  // w(v) * -log q_{depth(v)}(x_v)
-        if (!(term == term) || isinf(term)) atomicCAS(&bad, kStatOk, kStatNonFinite);
-        part += term;
+        const double w = (double)omega[(int64_t)t * stride + v];
+        const double az = w * (double)load_logit(logits + ((int64_t)t * L + d - 1) * V + x);
+        if (!(az == az) || isinf(az)) atomicCAS(&bad, kStatOk, kStatNonFinite);
+        azp += az;
     }
-    part = warp_sum_d(part);
-    if (lane == 0) red[wid] = part;
+    azp = warp_sum_d(azp);
+    if (lane == 0) red[wid] = azp;
     __syncthreads();
-    const int st = bad;
+    const int st0 = bad;
     for (int m = wid; m < L; m += nw) {
         double a = 0.0;
-        if (st == kStatOk)
+        int cnt = 0;
+        if (st0 != kStatBadTree)
             for (int v = 1 + lane; v < nv; v += kWarp)
-                if (__ldg(depth + (int64_t)t * stride + v) == m + 1)
+                if (__ldg(depth + (int64_t)t * stride + v) == m + 1) {
                     a += (double)__ldg(omega + (int64_t)t * stride + v);
+                    ++cnt;
+                }
         a = warp_sum_d(a);
-        if (lane == 0) ws.wrow[(int64_t)t * L + m] = a;
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (lane == 0) {
+            wrow[m] = a;
+            nrow[m] = cnt;
+            ws.wrow[(int64_t)t * L + m] = st0 == kStatOk ? a : 0.0;
+        }
     }
-    if (tid == 0) {
-        double num = 0.0;
-        for (int i = 0; i < nw; ++i) num += red[i];
-        loss_tree[t] = st == kStatOk ? num : 0.0;
-        status[t] = st;
-        ws.tstat[t] = st;
+    // ---- the chunk pass's statistics ----
+    pdl_entry();
+    // two rows a warp at once (m and m + nw), so that their loads and float64
+    // sums overlap
+    for (int m = wid; m < L; m += 2 * nw) {
+        float mc[2];
+        double s[2];
+        bool b[2];
+        row_stats_pair(ws.rows.chunk + ((int64_t)t * L + m) * nch, m + nw < L ? nw * nch : -1, nch, c,
+                       lane, mc, s, b);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (lane == 0 && m + j * nw < L) {
+                mcrow[m + j * nw] = mc[j];
+                srow[m + j * nw] = s[j];
+                badrow[m + j * nw] = b[j];
+            }
+    }
+    __syncthreads();
+    if (wid == 0) {
+        double term = 0.0;
+        bool nf = false;
+        if (lane < L) {
+            const double l = badrow[lane] ? __longlong_as_double(0x7ff8000000000000ll)
+                                          : 0.6931471805599453 * ((double)mcrow[lane] + log2(srow[lane]));
+            lse[lane] = l;
+            ws.lse[(int64_t)t * L + lane] = l;
+            if (nrow[lane] > 0) {  // a row holding a node contributes LSE_m W_m
+                term = l * wrow[lane];
+                nf = !(term == term) || isinf(term);
+            }
+        }
+        term = warp_sum_d(term);
+        nf = __any_sync(0xffffffffu, nf);
+        if (lane == 0) {
+            double az = 0.0;
+            for (int i = 0; i < nw; ++i) az += red[i];
+            int st = bad;
+            if (st == kStatOk && nf) st = kStatNonFinite;
+            const double num = term - az * inv_temp;
+            loss_tree[t] = st == kStatOk ? num : 0.0;
+            status[t] = st;
+            ws.tstat[t] = st;
+            if (st != kStatOk)
+                for (int m = 0; m < L; ++m) ws.wrow[(int64_t)t * L + m] = 0.0;
+        }
     }
     // completion: the last CTA reads every tree's results
     __threadfence();
@@ -166,11 +220,6 @@ exit_tree_kernel(const T* __restrict__ logits, int n_trees, int L, int64_t V, in
     }
 }
 
-// Dense part of the gradient, streaming: grad[row][a] = W_row softmax(z/T_d)(a)
-// / (T_d N) (1 / (T_d N) formed once by the per-tree kernel), with softmax = 2^(z c - LSE_row log2 e); rows of invalid trees
-// and rows no node scores are zero.  One warp per (row, 8 KB chunk of logits)
-// with all of the chunk's 16-byte loads in flight, then 16-byte streaming
-// stores; rows that are not 16-byte aligned take an element-wise loop.
 template <typename T>
 __global__ void __launch_bounds__(kExitThreads)
 exit_grad_kernel(const T* __restrict__ logits, int64_t rows, int L, int64_t V, int nch, float c,

@@ -154,6 +154,9 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // completed and its memory is visible, and then lets the next kernel be
 // scheduled.  No global memory is touched before that wait, so the stream's
 // ordering is unchanged; only launch latency is hidden, one kernel ahead.
+// (One exception, argued where it is: the exit loss's per-tree kernel reads
+// its inputs before the wait, because its predecessor is always the chunk
+// pass, which lets it be scheduled only after that pass's own wait.)
 // (Letting the next kernel be scheduled before the wait instead hides a
 // little more latency for a pair of kernels timed alone, but in a chain such
 // as build, mask and verify, grids launched two or three kernels ahead sat on
