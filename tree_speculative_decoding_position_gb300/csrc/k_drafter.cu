@@ -188,6 +188,7 @@ __device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
 }
 
 constexpr int kRThreads = 256;   // one CTA per drafter row
+constexpr int kRTopThreads = kRThreads - kWarp;  // the warps that find the top-k (the last forms the LSE)
 constexpr int kSliceCap = 2048;  // qualifying lane slices listed per row
 constexpr int kRowCandCap = 1024;
 
@@ -199,9 +200,11 @@ constexpr int kRowCandCap = 1024;
 // 16-byte vectors (or tokens) of the listed slices are read at once, and the
 // tokens at or above theta are listed.  Every token of the row's top-k is at
 // or above theta, so (4) warp 0 selecting the top-k of that list by (logit
-// desc, id asc) is exact; meanwhile warp 1 forms the log-normaliser from the
-// chunk sums in float64.  A row whose lists overflow (many equal logits)
-// is scanned token by token instead, still exactly.
+// desc, id asc) is exact.  A row whose lists overflow (many equal logits) is
+// scanned token by token instead, still exactly.  The last warp leaves after
+// (1) and forms the log-normaliser from the chunk sums in float64 (a chain of
+// about 3k clocks on this GPU's narrow float64 pipe) while the others run
+// (2)-(4) among themselves on a named barrier.
 template <typename T>
 __global__ void __launch_bounds__(kRThreads)
 drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nch, int k, float c,
@@ -250,7 +253,22 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
         m = fmaxf(m, wmax[w]);
         bad |= wbad[w] != 0;
     }
-    for (int q = tid; q < nch; q += kRThreads) {
+    if (wid == kRThreads / kWarp - 1) {  // the log-normaliser, beside (2)-(4)
+        const float mc = __fmul_rn(m, c);
+        double sum = 0.0;
+        for (int q = lane; q < nch; q += kWarp)
+            if (cm[q] != -INFINITY) sum += (double)cs[q].s * (double)ex2(__fmul_rn(cm[q], c) - mc);
+        sum = warp_sum_d(sum);
+        if (lane == 0) {
+            const bool b = bad || m == -INFINITY || !(sum > 0.0);
+            // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
+            ws.lse[row] = b ? __longlong_as_double(0x7ff8000000000000ll)
+                            : 0.6931471805599453 * ((double)mc + log2(sum));
+        }
+        return;
+    }
+    auto top_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kRTopThreads) : "memory"); };
+    for (int q = tid; q < nch; q += kRTopThreads) {
         const float v = cm[q];
         if (v != v) continue;  // a NaN maximum ranks nowhere
         int rank = 0;
@@ -260,24 +278,24 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
         }
         if (rank == k - 1) s_theta = v;
     }
-    __syncthreads();
+    top_sync();
     const float theta = s_theta;
-    for (int q = tid; q < nch; q += kRThreads)
+    for (int q = tid; q < nch; q += kRTopThreads)
         if (cm[q] >= theta) {
             const int pos = atomicAdd(&n_q, 1);
             if (TSD_IN(pos, kMaxDrafterChunks, kChkDrafter)) qlist[pos] = q;
         }
-    __syncthreads();
+    top_sync();
     // (2) qualifying slices
     const int nq = n_q;
-    for (int t = tid; t < nq * kWarp; t += kRThreads) {
+    for (int t = tid; t < nq * kWarp; t += kRTopThreads) {
         const int q = qlist[t / kWarp], l = t & (kWarp - 1);
         if (ws.lane_max[(row * nch + q) * kWarp + l] >= theta) {
             const int pos = atomicAdd(&n_s, 1);
             if (pos < kSliceCap) slist[pos] = q * kWarp + l;
         }
     }
-    __syncthreads();
+    top_sync();
     const int ns = n_s;
     bool overflow = ns > kSliceCap;
     // (3) candidate tokens
@@ -291,7 +309,7 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
             }
         };
         if (vec_ok) {
-            for (int t = tid; t < ns * kVecPerLane; t += kRThreads) {
+            for (int t = tid; t < ns * kVecPerLane; t += kRTopThreads) {
                 const int sl = slist[t / kVecPerLane], i = t % kVecPerLane;
                 const int q = sl / kWarp, l = sl & (kWarp - 1);
                 const int64_t c0 = (int64_t)q * CE;
@@ -309,7 +327,7 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
             }
         } else {
             constexpr int per = CE / kWarp;  // tokens of one slice: l, l+32, ...
-            for (int t = tid; t < ns * per; t += kRThreads) {
+            for (int t = tid; t < ns * per; t += kRTopThreads) {
                 const int sl = slist[t / per], jj = t % per;
                 const int q = sl / kWarp, l = sl & (kWarp - 1);
                 const int64_t c0 = (int64_t)q * CE;
@@ -321,7 +339,7 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
             }
         }
     }
-    __syncthreads();
+    top_sync();
     const int nc = n_c;
     overflow |= nc > kRowCandCap;
     // (4) selection | log-normaliser
@@ -355,18 +373,6 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
         if (lane < k) {
             ws.top_id[row * k + lane] = ei;
             ws.top_zt[row * k + lane] = temp == 1.0 ? (double)ev : (double)ev / temp;  // z / T_d
-        }
-    } else if (wid == 1) {
-        const float mc = __fmul_rn(m, c);
-        double sum = 0.0;
-        for (int q = lane; q < nch; q += kWarp)
-            if (cm[q] != -INFINITY) sum += (double)cs[q].s * (double)ex2(__fmul_rn(cm[q], c) - mc);
-        sum = warp_sum_d(sum);
-        if (lane == 0) {
-            const bool b = bad || m == -INFINITY || !(sum > 0.0);
-            // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
-            ws.lse[row] = b ? __longlong_as_double(0x7ff8000000000000ll)
-                            : 0.6931471805599453 * ((double)mc + log2(sum));
         }
     }
 }

@@ -39,11 +39,16 @@
 //                    the B-th best, ties at it go by that order, and a
 //                    bitonic sort of the kept entries gives the node order
 //                    (parents first).
+#include <cooperative_groups.h>
+
 #include "tsd_internal.cuh"
 
 namespace tsd {
 
+namespace cg = cooperative_groups;
+
 constexpr int kSelThreads = 1024;
+constexpr int kSelCluster = 2;  // CTAs per tree in the selection (a thread-block cluster)
 
 __device__ __forceinline__ double load_logit(const void* logits, tsd_dtype dtype, int64_t off) {
     if (dtype == TSD_BF16)
@@ -441,6 +446,8 @@ static __host__ __device__ size_t lse_sel_sort_bytes(int B) {
     return (size_t)4 * sizeof(unsigned long long) * pow2_ceil(B < 32 ? 32 : B) +
            sizeof(unsigned long long) * kSurvivors;
 }
+// Each CTA of a tree's pair compacts the candidates of its half of the
+// depths there; rank 0 then appends rank 1's, so the buffer holds a tree's.
 static __host__ __device__ bool lse_cands_in_smem(int K, int B, int L) {
     return lse_sel_sort_bytes(B) + (size_t)L * K * B * (sizeof(unsigned long long) + sizeof(int32_t)) <=
            kSelSmemCap;
@@ -466,7 +473,9 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
     __shared__ unsigned hist[256];
     __shared__ int nbs[TSD_MAX_L * TSD_MAX_MODES];
     __shared__ int s_bad, s_bucket, s_need, s_count, s_ns;
-    const int t = blockIdx.x, tid = threadIdx.x;
+    cg::cluster_group cl = cg::this_cluster();
+    const int cr = (int)cl.block_rank();  // rank 0 merges the first half of the depths and finishes
+    const int t = blockIdx.x / kSelCluster, tid = threadIdx.x;
     const int KB = K * B;
     const int64_t N = (int64_t)L * KB;
     const int64_t base = (int64_t)t * N;
@@ -487,7 +496,8 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         if (x != x) s_bad = 1;
     }
     __syncthreads();
-    if (s_bad) {
+    if (s_bad) {  // both CTAs of the pair see it and leave
+        if (cr != 0) return;
         for (int i = tid; i <= B; i += blockDim.x) {
             parent[out0 + i] = -1;
             token[out0 + i] = -1;
@@ -511,35 +521,43 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
     //    classes are exactly its distinct prefixes (by induction over depth).
     //    If one fails (a hash collision), the merge runs again depth by depth
     //    on (parent's representative, token), which needs no hash.
-    __shared__ int s_fail;
+    __shared__ int s_fail, s_nf;
     __shared__ unsigned long long red64a[2 * 32], s_and, s_or;
     if (tid == 0) {
         s_and = 0ull;  // no common leading bits known (the depth-by-depth merge)
         s_or = ~0ull;
+        s_nf = 0;
     }
     int n_f = 0;
-    // the candidates: in shared memory after the sort buffer when they fit
-    // (the grouped merge's table is dead by then), else in the workspace
+    // The pair splits the depths: rank 0 the first Lh, rank 1 the rest.  Each
+    // merges its depths in groups, the pair checks every merge, and each
+    // compacts its own candidates, in shared memory after the sort buffer when
+    // they fit (the grouped merge's table is dead by then), else in the
+    // workspace at their flat places.
+    const int Lh = (L + 1) / 2;
+    const int dlo = cr == 0 ? 0 : Lh, dhi = cr == 0 ? Lh : L;
+    const int64_t flo = (int64_t)dlo * KB, nloc = (int64_t)(dhi - dlo) * KB;
     const bool cand_smem = lse_cands_in_smem(K, B, L);
     unsigned long long* cimg_p = cand_smem ? reinterpret_cast<unsigned long long*>(sms + lse_sel_sort_bytes(B))
-                                           : ws.cimg + base;
-    int32_t* cflat_p = cand_smem ? reinterpret_cast<int32_t*>(cimg_p + N) : ws.cflat + base;
+                                           : ws.cimg + base + flo;
+    int32_t* cflat_p = cand_smem ? reinterpret_cast<int32_t*>(cimg_p + N) : ws.cflat + base + flo;
     if (tid == 0) s_fail = KB == 0;
+    bool fail;
     {
         unsigned long long* gtab = reinterpret_cast<unsigned long long*>(sms);
         int16_t* gslot = reinterpret_cast<int16_t*>(gtab + kGroupSlots);
         const int G = KB > 0 ? kGroupSlots / (2 * KB) : 1;
         const FastDiv fKB((unsigned)(KB > 0 ? KB : 1)), fB((unsigned)(B > 0 ? B : 1));
-        // an entry i of the group (flat index d0 K B + i): its depth offset,
-        // mode and place, and whether its place is in the mode's list
+        // an entry of depth d at e = mode * B + place: whether its place is
+        // in the mode's list
         auto in_list = [&](int d, int e) {
             const int mm = (int)fB.div((unsigned)e);
             return e - mm * B < nbs[d * K + mm];
         };
         for (int h = tid; h < kGroupSlots; h += blockDim.x) gtab[h] = kEmpty;
         __syncthreads();
-        for (int d0 = 0; d0 < L && KB > 0; d0 += G) {
-            const int nd = min(G, L - d0), ne = nd * KB;
+        for (int d0 = dlo; d0 < dhi && KB > 0; d0 += G) {
+            const int nd = min(G, dhi - d0), ne = nd * KB;
             // the group's hashes first (at most kGroupPer a thread), then the inserts
             unsigned long long hv[kGroupPer];
             bool in[kGroupPer];
@@ -581,73 +599,72 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
             for (int i = tid; i < ne; i += blockDim.x)
                 if (gslot[i] >= 0) ws.rep[base + (int64_t)d0 * KB + i] = (int)(gtab[gslot[i]] & kFlatMask);
             __syncthreads();
-            // the exact check, while the table is cleared for the next group
-            bool fail = false;
-            for (int i = tid; i < ne; i += blockDim.x) {
-                if (gslot[i] < 0) continue;
-                const int f = d0 * KB + i, d = (int)fKB.div((unsigned)f);
-                const int r = ws.rep[base + f];
-                if (r == f) continue;
-                const int dr = (int)fKB.div((unsigned)r);
-                bool same = dr == d && r < f && ws.tok[base + r] == ws.tok[base + f];
-                if (same && d > 0) {
-                    const int pf = ws.par[base + f], pr = ws.par[base + r];
-                    const int mf = (int)fB.div((unsigned)(f - d * KB)), mr = (int)fB.div((unsigned)(r - d * KB));
-                    same = TSD_IN(pf, B, kChkLse) && TSD_IN(pr, B, kChkLse) &&
-                           ws.rep[base + (int64_t)(d - 1) * KB + mf * B + pf] ==
-                               ws.rep[base + (int64_t)(d - 1) * KB + mr * B + pr];
-                }
-                fail |= !same;
-            }
-            if (fail) s_fail = 1;
             for (int h = tid; h < kGroupSlots; h += blockDim.x) gtab[h] = kEmpty;
             __syncthreads();
         }
-        if (!s_fail) {
-            // compaction in flat order, in the candidate buffer itself: first
-            // every entry's image and keep mark at its own flat index (the
-            // representatives and images loaded eight at a time), then the
-            // kept ones moved forward chunk by chunk (a candidate's place
-            // never exceeds its flat index, and a chunk is read before its
-            // scan's barriers)
-            unsigned long long and_img = ~0ull, or_img = 0ull;
-            for (int64_t c0 = 0; c0 < N; c0 += 8 * blockDim.x) {
-                int r[8];
-                unsigned long long im[8];
+        cl.sync();  // every representative of the tree is in the workspace
+        // The exact check of every merge of this CTA's depths (a parent of
+        // the first may be the other CTA's), with each entry's image and keep
+        // mark staged at its place in this CTA's candidate buffer.
+        bool bad_merge = false;
+        unsigned long long and_img = ~0ull, or_img = 0ull;
+        for (int64_t c0 = 0; c0 < nloc; c0 += 8 * blockDim.x) {
+            int r[8];
+            unsigned long long im[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int64_t c = c0 + q * blockDim.x + tid;
-                    bool lv = false;
-                    if (c < N) {
-                        const int d = (int)fKB.div((unsigned)c);
-                        lv = in_list(d, (int)c - d * KB);
-                    }
-                    r[q] = lv ? ws.rep[base + c] : -1;
-                    im[q] = lv ? ws.kimg[base + c] : ~kNegInfImage;
+            for (int q = 0; q < 8; ++q) {
+                const int64_t i = c0 + q * blockDim.x + tid, c = flo + i;
+                bool lv = false;
+                if (i < nloc) {
+                    const int d = (int)fKB.div((unsigned)c);
+                    lv = in_list(d, (int)c - d * KB);
                 }
+                r[q] = lv ? ws.rep[base + c] : -1;
+                im[q] = lv ? ws.kimg[base + c] : ~kNegInfImage;
+            }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int64_t c = c0 + q * blockDim.x + tid;
-                    if (c >= N) continue;
-                    const bool kp = r[q] == (int)c && im[q] != ~kNegInfImage;
-                    cimg_p[c] = im[q];
-                    cflat_p[c] = kp ? (int32_t)c : -1;
-                    if (kp) {
-                        and_img &= im[q];
-                        or_img |= im[q];
+            for (int q = 0; q < 8; ++q) {
+                const int64_t i = c0 + q * blockDim.x + tid;
+                if (i >= nloc) continue;
+                const int f = (int)(flo + i);
+                if (r[q] >= 0 && r[q] != f) {
+                    const int rr = r[q], d = (int)fKB.div((unsigned)f), dr = (int)fKB.div((unsigned)rr);
+                    bool same = dr == d && rr < f && ws.tok[base + rr] == ws.tok[base + f];
+                    if (same && d > 0) {
+                        const int pf = ws.par[base + f], pr = ws.par[base + rr];
+                        const int mf = (int)fB.div((unsigned)(f - d * KB)), mr = (int)fB.div((unsigned)(rr - d * KB));
+                        same = TSD_IN(pf, B, kChkLse) && TSD_IN(pr, B, kChkLse) &&
+                               ws.rep[base + (int64_t)(d - 1) * KB + mf * B + pf] ==
+                                   ws.rep[base + (int64_t)(d - 1) * KB + mr * B + pr];
                     }
+                    bad_merge |= !same;
+                }
+                const bool kp = r[q] == f && im[q] != ~kNegInfImage;
+                cimg_p[i] = im[q];
+                cflat_p[i] = kp ? (int32_t)f : -1;
+                if (kp) {
+                    and_img &= im[q];
+                    or_img |= im[q];
                 }
             }
-            block_and_or(and_img, or_img, red64a, &s_and, &s_or);  // also orders the marks
-            for (int64_t c0 = 0; c0 < N; c0 += 4 * blockDim.x) {
+        }
+        if (__syncthreads_or(bad_merge) && tid == 0) s_fail = 1;
+        block_and_or(and_img, or_img, red64a, &s_and, &s_or);  // also orders the marks
+        cl.sync();  // both CTAs' checks are in
+        fail = s_fail != 0 || *cl.map_shared_rank(&s_fail, (unsigned)(cr ^ 1)) != 0;
+        if (!fail) {
+            // the kept ones moved forward chunk by chunk (a candidate's place
+            // never exceeds its own, and a chunk is read before its scan's
+            // barriers)
+            for (int64_t c0 = 0; c0 < nloc; c0 += 4 * blockDim.x) {
                 int32_t fl[4];
                 unsigned long long im[4];
                 int cnt = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int64_t c = c0 + 4 * tid + q;
-                    fl[q] = c < N ? cflat_p[c] : -1;
-                    im[q] = c < N ? cimg_p[c] : 0ull;
+                    fl[q] = c < nloc ? cflat_p[c] : -1;
+                    im[q] = c < nloc ? cimg_p[c] : 0ull;
                     cnt += fl[q] >= 0;
                 }
                 int tot;
@@ -661,12 +678,13 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
                 }
                 n_f += tot;
             }
+            if (tid == 0) s_nf = n_f;
             __syncthreads();
         }
     }
-    if (s_fail && KB > 0) {
-    // (the hash of this merge overlaps the shared candidate buffer: its
-    // candidates go to the workspace)
+    if (fail && KB > 0 && cr == 0) {
+    // rank 0 alone, over every depth (the hash of this merge overlaps the
+    // shared candidate buffer: its candidates go to the workspace)
     cimg_p = ws.cimg + base;
     cflat_p = ws.cflat + base;
     // thread tid holds entries e = S tid + q, q < S, of each depth (S = K B /
@@ -755,6 +773,45 @@ lse_select_kernel(int K, int L, int k, int B, BuildWs bws, LseWs ws, int32_t* __
         }
     }
     }  // the depth-by-depth merge
+    cl.sync();  // each CTA's candidates are compacted (or rank 0 merged them all)
+    if (cr != 0) {
+        cl.sync();  // rank 0 has copied this CTA's candidates
+        return;
+    }
+    // rank 0 appends rank 1's candidates to its own: the tree's, in flat
+    // order (in the workspace the copy moves them down, chunk by chunk, each
+    // read before it is written)
+    if (!fail) {
+        const int n1 = *cl.map_shared_rank(&s_nf, 1u);
+        const unsigned long long* img1 = cand_smem ? cl.map_shared_rank(cimg_p, 1u) : ws.cimg + base + (int64_t)Lh * KB;
+        const int32_t* fl1 = cand_smem ? cl.map_shared_rank(cflat_p, 1u) : ws.cflat + base + (int64_t)Lh * KB;
+        for (int j0 = 0; j0 < n1; j0 += 4 * (int)blockDim.x) {
+            unsigned long long im[4];
+            int32_t fl[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + q * blockDim.x + tid;
+                im[q] = j < n1 ? img1[j] : 0ull;
+                fl[q] = j < n1 ? fl1[j] : -1;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + q * blockDim.x + tid;
+                if (j < n1) {
+                    cimg_p[n_f + j] = im[q];
+                    cflat_p[n_f + j] = fl[q];
+                }
+            }
+        }
+        if (tid == 0) {
+            s_and &= *cl.map_shared_rank(&s_and, 1u);
+            s_or |= *cl.map_shared_rank(&s_or, 1u);
+        }
+        n_f += n1;
+        __syncthreads();
+    }
+    cl.sync();  // rank 1's candidates are copied: it may leave
     const unsigned long long* cimg = cimg_p;
     const int32_t* cflat = cflat_p;
     // 2. radix select of the B-th best image among the candidates
@@ -982,8 +1039,9 @@ cudaError_t launch_lse_tree(const void* logits, tsd_dtype dtype, int n_trees, in
     const size_t ss = lse_select_smem(K, B, L);
     e = cudaFuncSetAttribute(lse_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (e != cudaSuccess) return e;
-    return launch_pdl(lse_select_kernel, (unsigned)n_trees, kSelThreads, ss, stream, K, L, k, B, bws,
-                      ws, parent, token, depth, score, n_nodes, status, n_cand);
+    return launch_pdl_cluster(lse_select_kernel, (unsigned)(n_trees * kSelCluster), kSelCluster, kSelThreads,
+                              ss, stream, K, L, k, B, bws, ws, parent, token, depth, score, n_nodes, status,
+                              n_cand);
 }
 
 TSD_CHECK_READER(checks_lse)
