@@ -27,18 +27,20 @@
 //                    its parent's key; it also extends a hash of its token
 //                    sequence.  Equal prefixes reached by several modes get
 //                    bit-identical keys and hashes.
-// lse_select_kernel  one CTA per tree.  Duplicates across modes are merged
-//                    over groups of depths at once through a shared-memory
-//                    hash on (depth, token-sequence hash), every merge then
-//                    checked exactly (same depth, token and parent
-//                    representative; by induction over depth that makes the
-//                    classes exact); on a failed check the merge runs again
-//                    depth by depth on (parent's representative, token).  The
-//                    first appearance in (depth, mode, place) order represents
-//                    a prefix.  A radix select on the 64-bit key image finds
-//                    the B-th best, ties at it go by that order, and a
-//                    bitonic sort of the kept entries gives the node order
-//                    (parents first).
+// lse_select_kernel  a cluster of two CTAs per tree, each taking half the
+//                    depths.  Duplicates across modes are merged over groups
+//                    of depths at once through a shared-memory hash on
+//                    (depth, token-sequence hash), every merge then checked
+//                    exactly (same depth, token and parent representative; by
+//                    induction over depth that makes the classes exact); on a
+//                    failed check rank 0 merges again depth by depth on
+//                    (parent's representative, token).  The first appearance
+//                    in (depth, mode, place) order represents a prefix.  Each
+//                    CTA compacts its candidates; rank 0 appends rank 1's
+//                    (distributed shared memory), a radix select on the 64-bit
+//                    key image finds the B-th best, ties at it go by that
+//                    order, and the kept entries ordered by counting give the
+//                    node order (parents first).
 #include <cooperative_groups.h>
 
 #include "tsd_internal.cuh"
