@@ -159,16 +159,22 @@ def test_lse_tree_large_budget_from_pinned_host(tsd, dev, orc):
     assert flips <= 4
 
 
-@pytest.mark.parametrize("case", ["k8_b128_l11", "k3_b100_l28"])
+@pytest.mark.parametrize("case", ["k8_b128_l11", "k3_b100_l28", "k8_b256_l12", "k4_b64_l1"])
 def test_lse_tree_merge_groups(tsd, dev, orc, case):
-    """The selection merges duplicates over groups of kGroupSlots / (2 K B)
-    depths: a last group shorter than the others (K = 8, B = 128, L = 11:
-    groups of 8 and 3 depths) and a K B that does not divide the table
-    (K = 3, B = 100, L = 28: groups of 27 and 1)."""
+    """The selection runs on a pair of CTAs per tree, each merging half the
+    depths in groups of kGroupSlots / (2 K B): a last group shorter than the
+    others (K = 8, B = 128, L = 11), a K B that does not divide the table
+    (K = 3, B = 100, L = 28), candidates too many for shared memory, kept in
+    the workspace (K = 8, B = 256, L = 12: 24576 entries, groups of 4
+    depths), and one depth, the second CTA holding none (L = 1)."""
     if case == "k8_b128_l11":
         nt, K, L, V, k, B = 2, 8, 11, 3000, 8, 128
-    else:
+    elif case == "k3_b100_l28":
         nt, K, L, V, k, B = 2, 3, 28, 2000, 4, 100  # L ceil(log2 k) <= 56
+    elif case == "k8_b256_l12":
+        nt, K, L, V, k, B = 2, 8, 12, 3000, 8, 256
+    else:
+        nt, K, L, V, k, B = 3, 4, 1, 500, 8, 64
     dr, _, _ = synth.mixture_drafter(nt, K, L, V, synth.seed_for(14, K), dtype=torch.float32)
     out = tsd.tsd_build_lse_tree(dr.to(dev), topk=k, B=B)
     assert out["status"].cpu().tolist() == [0] * nt
