@@ -151,3 +151,37 @@ def test_exit_loss_in_the_bench_launch(tsd, dev, orc):
         for m in range(L):
             assert np.allclose(got[m, cols], want[m, cols], rtol=1e-4, atol=1e-6 * scale)
             assert np.allclose(got[m, toks], want[m, toks], rtol=1e-4, atol=1e-6 * scale)
+
+
+def test_exit_loss_non_finite_rows_and_terms(tsd, dev, orc):
+    """The kernel forms a tree's numerator as sum_m LSE_m W_m - sum_v w z / T
+    (Eq. 67).  A row whose logits hold a NaN makes its tree non-finite only if
+    some node lies on that row, as in the oracle's node-by-node Eq. 66; a
+    drafted token at -inf makes its tree non-finite whatever its weight."""
+    L, V, B = 5, 3000, 6
+    g = torch.Generator().manual_seed(synth.seed_for(7, 900))
+    z = torch.randn(4, 1, L, V, generator=g) * 2
+    parent = torch.full((4, B + 1), -1, dtype=torch.int32)
+    token = torch.full((4, B + 1), -1, dtype=torch.int32)
+    depth = torch.full((4, B + 1), -1, dtype=torch.int32)
+    depth[:, 0] = 0
+    # every tree: root, two children (depth 1), one grandchild each (depth 2)
+    parent[:, 1:5] = torch.tensor([0, 0, 1, 2], dtype=torch.int32)
+    token[:, 1:5] = torch.tensor([11, 22, 33, 44], dtype=torch.int32)
+    depth[:, 1:5] = torch.tensor([1, 1, 2, 2], dtype=torch.int32)
+    n_nodes = torch.full((4,), 5, dtype=torch.int32)
+    z[1, 0, 4, 100] = float("nan")  # row 5: no node there
+    z[2, 0, 1, 7] = float("nan")  # row 2: the grandchildren's
+    z[3, 0, 0, 22] = -float("inf")  # a drafted token at -inf
+    w = torch.rand(4, B + 1, generator=g) * (depth >= 1)
+    w[3, 2] = 0.0  # weight zero on the -inf token: still non-finite
+    out = tsd.tsd_exit_loss(z.to(dev), token.to(dev), depth.to(dev), n_nodes.to(dev), w.to(dev))
+    assert out["status"].cpu().tolist() == [0, 0, 5, 5]
+    for t in (0, 1):
+        want = orc.exit_loss(z[t, 0].double().numpy(), 1.0, token[t].numpy(), depth[t].numpy(), 5,
+                             w[t].double().numpy())
+        assert float(out["loss_tree"][t]) == pytest.approx(want, rel=RTOL)
+    for t in (2, 3):
+        with pytest.raises(Exception):
+            orc.exit_loss(z[t, 0].double().numpy(), 1.0, token[t].numpy(), depth[t].numpy(), 5,
+                          w[t].double().numpy())
