@@ -40,6 +40,8 @@
 // the prefix within its mode), the prefix's z / T_d sum, and a 64-bit hash of
 // the parent's token sequence (to tell equal prefixes of different modes
 // apart; every hash match is confirmed by comparing the token sequences).
+#include <float.h>
+
 #include "tsd_internal.cuh"
 
 namespace tsd {
@@ -72,7 +74,29 @@ struct BuildPlan {
     size_t lists, fbytes, xbytes, sbytes, scode_bytes, hbytes, flag_bytes, smem_total;
     bool big_in_smem;
     size_t global_per_tree;
+    // threshold expansion (one mode): candidate capacity (0 = rounds only),
+    // depth of the fully enumerated levels and their prefix count
+    int tcap, d0, n0;
+    FastDiv kdiv;  // division by topk
 };
+
+// Threshold expansion: key bins of the selections, candidates kept at most,
+// and the largest enumeration of the first levels.
+constexpr int kThrBinBits = 11;
+constexpr int kThrBins = 1 << kThrBinBits;
+// bin counts in 32 rows of 64 plus one pad word: lane l of a warp owns row
+// l, and a warp reading one word per lane across a row hits distinct banks
+constexpr int kThrBinWords = kThrBins + kThrBins / 64;
+constexpr int kThrCapMax = 3072;
+constexpr int kThrSlots = 4096;  // (parent, rank) pairs evaluated per level
+constexpr int kThrEnumMax = 1024;
+// per candidate: key, tie key, z sum (8 B each); parent, node, bin-order
+// slot, float z sum (4 B each)
+constexpr size_t kThrBytesPer = 3 * sizeof(unsigned long long) + 4 * sizeof(int32_t);
+// bin counts and bases, row sums, pair slots; float lists, their magnitudes
+// and the float log-normalisers
+constexpr size_t kThrFixed = sizeof(int32_t) * (2 * kThrBinWords + 32 + kThrSlots) +
+                             sizeof(float) * (TSD_MAX_L * TSD_MAX_TOPK + 2 * (TSD_MAX_L + 1));
 
 __host__ __device__ inline int pow2_at_least(int x) {
     int p = 1;
@@ -108,6 +132,34 @@ static BuildPlan build_plan(int n_modes, int L, int topk, int B) {
     p.big_in_smem = p.lists + p.sbytes + big <= 225 * 1024;  // of 227 KB per block
     p.smem_total = p.lists + p.sbytes + (p.big_in_smem ? big : 0);
     p.global_per_tree = p.big_in_smem ? 0 : big;
+    // Threshold expansion for one mode: enumerate levels 1..d0 until they hold
+    // B prefixes (one more while the enumeration stays within kThrEnumMax)
+    p.tcap = p.d0 = p.n0 = 0;
+    p.kdiv = FastDiv((unsigned)topk);
+    if (n_modes == 1 && B > 0) {
+        long long n = 0, lev = 1;
+        int d = 0;
+        while (d < L && n < B && n <= (1 << 22)) {
+            ++d;
+            lev *= topk;
+            n += lev;
+        }
+        while (n >= B && d < L && n + lev * topk <= kThrEnumMax) {
+            ++d;
+            lev *= topk;
+            n += lev;
+        }
+        const size_t fixed = r16(p.lists) + r16(kThrFixed);
+        long long cap = fixed < 225 * 1024 ? (long long)((225 * 1024 - fixed) / kThrBytesPer) : 0;
+        cap = (cap < kThrCapMax ? cap : kThrCapMax) & ~31LL;
+        if (n >= B && 2 * n <= cap && 2LL * B <= cap) {
+            p.tcap = (int)cap;
+            p.d0 = d;
+            p.n0 = (int)n;
+            const size_t need = fixed + (size_t)cap * kThrBytesPer;
+            if (need > p.smem_total) p.smem_total = need;
+        }
+    }
     return p;
 }
 
@@ -391,6 +443,380 @@ __device__ int hash_bucket(unsigned long long h, unsigned long long* hkey, int h
     return -1;
 }
 
+// ---------------------------------------------------------------------------
+// Threshold expansion (one mode).
+//
+// Scores never rise along a path (each log q is at most 0, and at equal score
+// a parent's shorter tie key comes first), so for any lower bound theta of the
+// B-th best key, the B best prefixes are the B best among the prefixes whose
+// key is at least theta, and that set is closed under taking parents.  Every
+// set of B prefixes gives such a bound: the key of its worst member.  The
+// first d0 levels are enumerated in full and give the first bound; each
+// further level keeps the children of the last level's kept prefixes whose
+// key reaches the bound, and the bound then rises to the B-th best key of
+// everything kept so far.  Keys are counted in bins of equal width below the
+// best enumerated key; a bound is the lower edge of the bin that holds the
+// B-th best key.  The B best kept prefixes under (key desc, tie key asc) are
+// the tree, in that order: the same set and order as the rounds.
+//
+// A child's key is exact float64 (the rounds' arithmetic).  Float64 issues at
+// one warp instruction per 64 clocks per SM quarter whatever the active lanes,
+// so each level first bounds, in float32, how many of a parent's children can
+// pass (they pass as a run from rank 0: its list is sorted), and evaluates
+// only those (parent, rank) pairs, packed densely over the warps.
+//
+// Returns false when the candidates outgrow their arrays or rounding made a
+// child score above its parent; the caller then runs the rounds, which
+// rewrite every output.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int thr_pidx(int b) { return b + (b >> 6); }
+
+__device__ __forceinline__ int warp_incl_scan(int x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// One warp: the bin that holds the B-th key (bin 0 holds the best keys), from
+// the row sums and then the crossing row's bins; *upto = keys in bins up to
+// it.  -1 when the counts read do not reach B.  Counts read while other warps
+// add to them are at most the true counts of real candidates, so a bin found
+// from them still has at least B real keys at or above it.
+__device__ int thr_warp_bin(const int* hist, const int* rows, int B, int* upto) {
+    const int lane = threadIdx.x & 31;
+    const int rs = rows[lane];
+    const int incl = warp_incl_scan(rs), excl = incl - rs;
+    const unsigned int hit = __ballot_sync(0xffffffffu, excl < B && incl >= B);
+    if (hit == 0u) return -1;
+    const int c = __ffs(hit) - 1;
+    const int cex = __shfl_sync(0xffffffffu, excl, c);
+    const int h0 = hist[c * 65 + 2 * lane], h1 = hist[c * 65 + 2 * lane + 1];
+    const int ex2 = cex + warp_incl_scan(h0 + h1) - h0 - h1;
+    const int q = (ex2 < B && ex2 + h0 >= B) ? 0 : ((ex2 + h0 < B && ex2 + h0 + h1 >= B) ? 1 : -1);
+    const unsigned int hit2 = __ballot_sync(0xffffffffu, q >= 0);
+    if (hit2 == 0u) return -1;
+    const int l2 = __ffs(hit2) - 1;
+    const int q2 = __shfl_sync(0xffffffffu, q, l2);
+    *upto = __shfl_sync(0xffffffffu, q == 0 ? ex2 + h0 : ex2 + h0 + h1, l2);
+    return 64 * c + 2 * l2 + q2;
+}
+
+// float32 of a float64, rounded toward zero (integer operations only): within
+// one float32 unit of the value, 0 below float32's normal range, infinite above it.
+__device__ __forceinline__ float f32_trunc(double x) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(x);
+    const unsigned int sign = (unsigned int)(u >> 32) & 0x80000000u;
+    const int e = (int)((u >> 52) & 0x7FF);
+    if (e == 0x7FF) return __uint_as_float(sign | 0x7F800000u | ((u << 12) != 0ull ? 0x400000u : 0u));
+    const int E = e - 1023 + 127;
+    if (E >= 255) return __uint_as_float(sign | 0x7F800000u);
+    if (E <= 0) return __uint_as_float(sign);
+    return __uint_as_float(sign | ((unsigned int)E << 23) | (unsigned int)((u >> 29) & 0x7FFFFFull));
+}
+
+__device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan, int L, int k,
+                          int B, int bits, int32_t* par, int32_t* tok, int32_t* dep, float* sc,
+                          double* sc64, int32_t* rk, int32_t* md) {
+    __shared__ unsigned long long s_whi[32], s_wlo[32];
+    __shared__ int s_wlive[32], s_lev[3], s_slot[3], s_fail;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
+    const int nw = nthr >> 5;
+    const int cap = plan.tcap, n0 = plan.n0, d0 = plan.d0;
+    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(base);
+    unsigned long long* ctb = ckey + cap;
+    double* czs = reinterpret_cast<double*>(ctb + cap);
+    int* cpar = reinterpret_cast<int*>(czs + cap);
+    int* cnode = cpar + cap;  // node of a kept candidate, 0 otherwise
+    int* sidx = cnode + cap;  // candidates in bin order
+    float* czf = reinterpret_cast<float*>(sidx + cap);  // z sums in float32
+    int* hist = reinterpret_cast<int*>(czf + cap);
+    int* hbase = hist + kThrBinWords;
+    int* rows = hbase + kThrBinWords;                  // bins per row of 64
+    int* slot = rows + 32;                             // parent << 5 | rank
+    float* ztf = reinterpret_cast<float*>(slot + kThrSlots);  // the lists' z / T_d in float32
+    float* zmag = ztf + L * k;                         // per depth: largest finite |ztf|
+    float* cf = zmag + L;                              // C(d) in float32, d = 0..L
+    const unsigned long long live_min = order_key(-DBL_MAX);  // below: -inf
+    if (tid == 0) {
+        s_lev[0] = s_lev[1] = s_lev[2] = 0;
+        s_slot[0] = s_slot[1] = s_slot[2] = 0;
+        s_fail = 0;
+    }
+    for (int i = tid; i < kThrBinWords; i += nthr) hist[i] = 0;
+    if (tid < 32) rows[tid] = 0;
+    for (int i = tid; i < L * k; i += nthr) ztf[i] = f32_trunc(ls.zlog(0, i / k + 1, i % k));
+    if (tid >= 32 && tid < 32 + L) {
+        // a finite value that float32 cannot hold turns the bound off (infinite margin)
+        float m = 0.0f;
+        for (int r = 0; r < k; ++r) {
+            const double x = ls.zlog(0, tid - 31, r);
+            const float xf = fabsf(f32_trunc(x));
+            if (x > -INFINITY && x < INFINITY) m = xf < INFINITY ? fmaxf(m, xf) : INFINITY;
+        }
+        zmag[tid - 32] = m;
+    }
+    if (tid >= 64 && tid <= 64 + L) cf[tid - 64] = f32_trunc(ls.c(0, tid - 64));
+    __syncthreads();
+
+    // ---- levels 1..d0 in full, one level at a time (prefix i of level d is
+    // child i mod k of prefix i / k of level d-1) ----
+    unsigned long long hi = 0ull, lo = ~0ull;
+    int live = 0;
+    bool bad = false;
+    if (tid < L) {
+        const double c = ls.c(0, tid + 1);
+        bad = !(c > -INFINITY && c < INFINITY);
+    }
+    {
+        int off = 0, poff = 0, lev = k;
+        for (int d = 1; d <= d0; ++d) {
+            const double cd = ls.c(0, d);
+            for (int i = tid; i < lev; i += nthr) {
+                const unsigned int q = plan.kdiv.div((unsigned int)i);
+                const int r = i - (int)q * k;
+                const int pp = d == 1 ? -1 : poff + (int)q;
+                const double z = (d == 1 ? 0.0 : czs[pp]) + ls.zlog(0, d, r);
+                const double sv = z - cd;
+                const unsigned long long key = order_key(sv);
+                if (sv != sv) bad = true;
+                const int idx = off + i;
+                ckey[idx] = key;
+                ctb[idx] = ((unsigned long long)d << 59) |
+                           (d == 1 ? 0ull : (((ctb[pp] & kRsMask) << bits) & kRsMask)) |
+                           (unsigned long long)r;
+                czs[idx] = z;
+                czf[idx] = f32_trunc(z);
+                cpar[idx] = pp;
+                cnode[idx] = 0;
+                if (key >= live_min) {
+                    hi = max(hi, key);
+                    lo = min(lo, key);
+                    ++live;
+                }
+            }
+            poff = off;
+            off += lev;
+            lev *= k;
+            if (d < d0) __syncthreads();  // the next level reads this one's sums
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        live += __shfl_xor_sync(0xffffffffu, live, o);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) s_fail = 1;
+    if (lane == 0) {
+        s_whi[wid] = hi;
+        s_wlo[wid] = lo;
+        s_wlive[wid] = live;
+    }
+    __syncthreads();
+    if (s_fail != 0) return false;
+    unsigned long long top = 0ull, bot = ~0ull;
+    int nlive = 0;
+    for (int w = 0; w < nw; ++w) {
+        top = max(top, s_whi[w]);
+        bot = min(bot, s_wlo[w]);
+        nlive += s_wlive[w];
+    }
+    if (nlive < B) return false;
+    // bins of width 2^sh below the best key: bin(key) = (top - key) >> sh
+    const unsigned long long span = top - bot;
+    const int sh = span == 0ull ? 0 : max(0, 64 - __clzll((long long)span) - kThrBinBits);
+    auto bin_of = [&](unsigned long long key) {
+        const unsigned long long b = (top - key) >> sh;
+        return (int)(b < (unsigned long long)kThrBins ? b : kThrBins - 1);
+    };
+    auto count_key = [&](unsigned long long key) {
+        const int b = bin_of(key);
+        atomicAdd(&hist[thr_pidx(b)], 1);
+        atomicAdd(&rows[b >> 6], 1);
+    };
+    // the smallest key of bin b
+    auto bin_floor = [&](int b) {
+        if (b < 0) return live_min;
+        const unsigned long long off = ((unsigned long long)b << sh) + ((1ull << sh) - 1ull);
+        const unsigned long long f = top > off ? top - off : 0ull;
+        return f > live_min ? f : live_min;
+    };
+    for (int i = tid; i < n0; i += nthr) {
+        const unsigned long long key = ckey[i];
+        if (key >= live_min) count_key(key);
+    }
+    __syncthreads();
+    int upto = 0;
+    unsigned long long theta = bin_floor(thr_warp_bin(hist, rows, B, &upto));
+
+    // ---- levels d0+1, ...: kept children of the last level's kept prefixes ----
+    int pa = n0, pe = n0;
+    {
+        int lev = 1;
+        for (int j = 0; j < d0; ++j) lev *= k;
+        pa = n0 - lev;  // level d0
+    }
+    for (int d = d0 + 1; d <= L && pa < pe; ++d) {
+        const double cd = ls.c(0, d);
+        int* cnt = &s_lev[d % 3];
+        int* nslot = &s_slot[d % 3];
+        if (tid == 0) {  // both last read before the previous barrier
+            s_lev[(d + 1) % 3] = 0;
+            s_slot[(d + 1) % 3] = 0;
+        }
+        // (1) Per parent, a float32 bound on its passing children: child r can
+        // pass only if ztf[r] >= g.  The margin covers the error of every
+        // float32 operand and step (a few units of 2^-24 of the magnitudes
+        // involved, against 2^-18 here; the absolute term covers values below
+        // float32's normal range) and that of the float64 evaluation.  Where an
+        // operand does not fit float32, g is not finite and every rank is
+        // evaluated.  The (parent, rank) pairs go to one list for the block.
+        const float thf = f32_trunc(key_score(theta)), cdf = cf[d], zm = zmag[d - 1];
+        const float* zr = ztf + (d - 1) * k;
+        for (int p0 = pa; p0 < pe; p0 += nthr) {
+            const int p = p0 + tid;
+            int cb = 0;
+            if (p < pe && ckey[p] >= theta) {
+                const float zsf = czf[p];
+                const float m = 0x1p-18f * (fabsf(thf) + fabsf(cdf) + fabsf(zsf) + zm) + 1e-30f;
+                const float g = ((thf - m) + cdf) - zsf;
+                if (g > -INFINITY && g < INFINITY) {
+                    while (cb < k && zr[cb] >= g) ++cb;
+                } else {
+                    cb = k;
+                }
+            }
+            const int inc = warp_incl_scan(cb);
+            int at = 0;
+            if (lane == 31 && inc > 0) at = atomicAdd(nslot, inc);
+            at = __shfl_sync(0xffffffffu, at, 31) + inc - cb;
+            for (int r = 0; r < cb; ++r) {
+                if (at + r < kThrSlots) slot[at + r] = (p << 5) | r;
+                else s_fail = 1;
+            }
+        }
+        __syncthreads();
+        if (s_fail != 0) return false;
+        // (2) the exact keys of the listed pairs, packed over all threads
+        const int ns = *nslot;
+        for (int j0 = 0; j0 < ns; j0 += nthr) {
+            const int j = j0 + tid;
+            bool ok = false;
+            int p = 0, r = 0;
+            double z = 0.0;
+            unsigned long long key = 0ull;
+            if (j < ns) {
+                p = slot[j] >> 5;
+                r = slot[j] & 31;
+                z = czs[p] + ls.zlog(0, d, r);
+                key = order_key(z - cd);
+                ok = key >= theta;
+            }
+            const unsigned int ball = __ballot_sync(0xffffffffu, ok);
+            int at = 0;
+            if (lane == 0 && ball != 0u) at = atomicAdd(cnt, __popc(ball));
+            at = __shfl_sync(0xffffffffu, at, 0);
+            if (ok) {
+                const int pos = pe + at + __popc(ball & ((1u << lane) - 1u));
+                if (pos < cap && key <= ckey[p]) {
+                    ckey[pos] = key;
+                    ctb[pos] = ((unsigned long long)d << 59) |
+                               (((ctb[p] & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
+                    czs[pos] = z;
+                    czf[pos] = f32_trunc(z);
+                    cpar[pos] = p;
+                    cnode[pos] = 0;
+                    count_key(key);
+                } else {
+                    s_fail = 1;  // out of room, or a child above its parent
+                }
+            }
+        }
+        __syncthreads();
+        if (s_fail != 0) return false;
+        pa = pe;
+        pe += *cnt;
+        // the bound rises to the B-th best key kept so far (each warp on its
+        // own; a warp already on the next level only adds real candidates)
+        const unsigned long long th = bin_floor(thr_warp_bin(hist, rows, B, &upto));
+        theta = th > theta ? th : theta;
+    }
+    const int N = pe;
+
+    // ---- the B best: candidates of bins up to the B-th key's, ranked within bins ----
+    // (no warp adds to the counts any more: every warp reads the same values)
+    const int b1 = thr_warp_bin(hist, rows, B, &upto);
+    const int M2 = upto;
+    if (b1 < 0) return false;  // cannot happen: the counts hold at least B live keys
+    for (int row = wid; row < 32; row += nw) {  // bases: keys in earlier bins
+        const int rs = rows[lane];
+        const int rbase = __shfl_sync(0xffffffffu, warp_incl_scan(rs) - rs, row);
+        const int h0 = hist[row * 65 + 2 * lane], h1 = hist[row * 65 + 2 * lane + 1];
+        const int ex2 = rbase + warp_incl_scan(h0 + h1) - h0 - h1;
+        hbase[row * 65 + 2 * lane] = ex2;
+        hbase[row * 65 + 2 * lane + 1] = ex2 + h0;
+    }
+    __syncthreads();
+    for (int i = tid; i < N; i += nthr) {
+        const unsigned long long key = ckey[i];
+        if (key < live_min) continue;
+        const int b = bin_of(key);
+        if (b > b1) continue;
+        const int sl = hbase[thr_pidx(b)] + atomicSub(&hist[thr_pidx(b)], 1) - 1;
+        if (TSD_IN(sl, M2, kChkBuild)) sidx[sl] = i;
+    }
+    __syncthreads();
+    int* ord = reinterpret_cast<int*>(czs);  // z sums are spent; 2 * cap >= B slots
+    for (int sl = tid; sl < M2; sl += nthr) {
+        const int c = sidx[sl];
+        const unsigned long long key = ckey[c], tb = ctb[c];
+        const int b = bin_of(key);
+        const int lo = hbase[thr_pidx(b)], hi = b + 1 < kThrBins ? hbase[thr_pidx(b + 1)] : M2;
+        int rank = lo;
+        for (int j = lo; j < hi; ++j) {
+            const int cj = sidx[j];
+            const unsigned long long kj = ckey[cj];
+            rank += (kj > key || (kj == key && ctb[cj] < tb)) ? 1 : 0;
+        }
+        if (rank < B) {
+            ord[rank] = c;
+            cnode[c] = rank + 1;
+        }
+    }
+    __syncthreads();
+    for (int pos = tid; pos < B; pos += nthr) {
+        const int c = ord[pos], node = pos + 1;
+        const unsigned long long tb = ctb[c];
+        const int d = tb_depth(tb), r = ls.last_rank(tb);
+        const double sv = key_score(ckey[c]);
+        const int pp = cpar[c];
+        const int pn = pp < 0 ? 0 : cnode[pp];
+        if (pp >= 0 && (pn <= 0 || pn >= node)) s_fail = 1;  // a child before its parent
+        par[node] = pn;
+        tok[node] = ls.token(0, d, r);
+        dep[node] = d;
+        sc[node] = (float)sv;
+        if (sc64) sc64[node] = sv;
+        if (rk) rk[node] = r;
+        if (md) md[node] = 0;
+    }
+    if (tid == 0) {
+        par[0] = -1;
+        tok[0] = -1;
+        dep[0] = 0;
+        sc[0] = 0.0f;
+        if (sc64) sc64[0] = 0.0;
+        if (rk) rk[0] = -1;
+        if (md) md[0] = -1;
+    }
+    __syncthreads();
+    return s_fail == 0;
+}
+
 __global__ void __launch_bounds__(kBuildThreads, 1)
 build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bits,
                   int32_t* __restrict__ parent, int32_t* __restrict__ token,
@@ -454,7 +880,18 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     __syncthreads();
     const bool bad = s_bad != 0;
     int fc = 0, xc = 0;  // current buffer indices
-    if (!bad && B > 0) {  // B = 0: the tree is the root alone
+    int32_t* par = parent + (int64_t)t * stride;
+    int32_t* tok = token + (int64_t)t * stride;
+    int32_t* dep = depth + (int64_t)t * stride;
+    float* sc = score + (int64_t)t * stride;
+    int32_t* rk = rank ? rank + (int64_t)t * stride : nullptr;
+    int32_t* md = mode ? mode + (int64_t)t * stride : nullptr;
+    // one mode: threshold expansion first, the rounds when it declines
+    bool done = false;
+    if (!bad && B > 0 && K == 1 && plan.tcap > 0)
+        done = thr_build(ls, smem + plan.lists, plan, L, k, B, bits, par, tok, dep, sc,
+                         ws.score64 ? ws.score64 + (int64_t)t * stride : nullptr, rk, md);
+    if (!bad && B > 0 && !done) {  // B = 0: the tree is the root alone
         // seeds: the root's children, all k first tokens of every mode
         const int n2 = pow2_at_least(K * k < 32 ? 32 : K * k);
         for (int i = tid; i < n2; i += blockDim.x) {
@@ -666,14 +1103,8 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     // ---- output: nodes in X order (first occurrences), parents resolved ----
     const bool failed = bad || s_bad != 0;
     const int nX = failed ? 0 : s_nX;
-    const int nn = failed ? 0 : s_D + 1;
-    int32_t* par = parent + (int64_t)t * stride;
-    int32_t* tok = token + (int64_t)t * stride;
-    int32_t* dep = depth + (int64_t)t * stride;
-    float* sc = score + (int64_t)t * stride;
-    int32_t* rk = rank ? rank + (int64_t)t * stride : nullptr;
-    int32_t* md = mode ? mode + (int64_t)t * stride : nullptr;
-    if (!failed) {
+    const int nn = failed ? 0 : (done ? B + 1 : s_D + 1);
+    if (!failed && !done) {
         // node index of each kept entry: K == 1 -> position + 1; K > 1 ->
         // distinct rank + 1 for first occurrences
         // table: prefix -> node (keyed by the prefix hash, confirmed by tokens)
