@@ -93,9 +93,9 @@ constexpr int kThrEnumMax = 1024;
 // per candidate: key, tie key, z sum (8 B each); parent, node, bin-order
 // slot, float z sum (4 B each)
 constexpr size_t kThrBytesPer = 3 * sizeof(unsigned long long) + 4 * sizeof(int32_t);
-// bin counts and bases, row sums, pair slots; float lists, their magnitudes
-// and the float log-normalisers
-constexpr size_t kThrFixed = sizeof(int32_t) * (2 * kThrBinWords + 32 + kThrSlots) +
+// bin counts and bases, row sums, two pair lists; float lists, their
+// magnitudes and the float log-normalisers
+constexpr size_t kThrFixed = sizeof(int32_t) * (2 * kThrBinWords + 32 + 2 * kThrSlots) +
                              sizeof(float) * (TSD_MAX_L * TSD_MAX_TOPK + 2 * (TSD_MAX_L + 1));
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -518,52 +518,72 @@ __device__ __forceinline__ float f32_trunc(double x) {
     return __uint_as_float(sign | ((unsigned int)E << 23) | (unsigned int)((u >> 29) & 0x7FFFFFull));
 }
 
-__device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan, int L, int k,
-                          int B, int bits, int32_t* par, int32_t* tok, int32_t* dep, float* sc,
-                          double* sc64, int32_t* rk, int32_t* md) {
-    __shared__ unsigned long long s_whi[32], s_wlo[32];
-    __shared__ int s_wlive[32], s_lev[3], s_slot[3], s_fail;
+// Shared scalars of the threshold expansion (set before the kernel's first barrier).
+struct ThrState {
+    unsigned long long whi[32], wlo[32];  // per warp: largest and least live key
+    int wlive[32];                        // per warp: live keys
+    int lev[3], slot[3];                  // per depth (mod 3): candidates, listed pairs
+    int fail;
+};
+// The candidate arrays and tables, laid out after the lists in shared memory.
+struct ThrMem {
+    unsigned long long *key, *tb;
+    double* zs;
+    int *par, *node, *sidx;
+    float* zf;  // z sums in float32
+    int *hist, *hbase, *rows, *slots;
+    float *ztf, *zmag, *cf;
+};
+__device__ __forceinline__ ThrMem thr_mem(uint8_t* base, int cap, int L, int k) {
+    ThrMem m;
+    m.key = reinterpret_cast<unsigned long long*>(base);
+    m.tb = m.key + cap;
+    m.zs = reinterpret_cast<double*>(m.tb + cap);
+    m.par = reinterpret_cast<int*>(m.zs + cap);
+    m.node = m.par + cap;  // node of a kept candidate, 0 otherwise
+    m.sidx = m.node + cap;  // candidates in bin order
+    m.zf = reinterpret_cast<float*>(m.sidx + cap);
+    m.hist = reinterpret_cast<int*>(m.zf + cap);
+    m.hbase = m.hist + kThrBinWords;
+    m.rows = m.hbase + kThrBinWords;  // bins per row of 64
+    m.slots = m.rows + 32;  // two lists of parent << 5 | rank, one per level parity
+    m.ztf = reinterpret_cast<float*>(m.slots + 2 * kThrSlots);  // the lists' z / T_d in float32
+    m.zmag = m.ztf + L * k;  // per depth: largest finite |ztf| (formed by integer maxima)
+    m.cf = m.zmag + L;       // C(d) in float32, d = 0..L
+    return m;
+}
+
+// The caller has zeroed the bin counts, row sums and magnitudes, set ztf and
+// zmag from the lists and the state's counters to 0, behind one barrier.
+__device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const BuildPlan& plan,
+                          int L, int k, int B, int bits, int32_t* par, int32_t* tok,
+                          int32_t* dep, float* sc, double* sc64, int32_t* rk, int32_t* md) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
     const int nw = nthr >> 5;
     const int cap = plan.tcap, n0 = plan.n0, d0 = plan.d0;
-    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(base);
-    unsigned long long* ctb = ckey + cap;
-    double* czs = reinterpret_cast<double*>(ctb + cap);
-    int* cpar = reinterpret_cast<int*>(czs + cap);
-    int* cnode = cpar + cap;  // node of a kept candidate, 0 otherwise
-    int* sidx = cnode + cap;  // candidates in bin order
-    float* czf = reinterpret_cast<float*>(sidx + cap);  // z sums in float32
-    int* hist = reinterpret_cast<int*>(czf + cap);
-    int* hbase = hist + kThrBinWords;
-    int* rows = hbase + kThrBinWords;                  // bins per row of 64
-    int* slot = rows + 32;                             // parent << 5 | rank
-    float* ztf = reinterpret_cast<float*>(slot + kThrSlots);  // the lists' z / T_d in float32
-    float* zmag = ztf + L * k;                         // per depth: largest finite |ztf|
-    float* cf = zmag + L;                              // C(d) in float32, d = 0..L
+    unsigned long long* ckey = tm.key;
+    unsigned long long* ctb = tm.tb;
+    double* czs = tm.zs;
+    int* cpar = tm.par;
+    int* cnode = tm.node;
+    int* sidx = tm.sidx;
+    float* czf = tm.zf;
+    int* hist = tm.hist;
+    int* hbase = tm.hbase;
+    int* rows = tm.rows;
+    int* slots = tm.slots;
+    const float* ztf = tm.ztf;
+    const float* zmag = tm.zmag;
+    float* cf = tm.cf;
+    int* s_lev = ts.lev;
+    int* s_slot = ts.slot;
+    int& s_fail = ts.fail;
     const unsigned long long live_min = order_key(-DBL_MAX);  // below: -inf
-    if (tid == 0) {
-        s_lev[0] = s_lev[1] = s_lev[2] = 0;
-        s_slot[0] = s_slot[1] = s_slot[2] = 0;
-        s_fail = 0;
-    }
-    for (int i = tid; i < kThrBinWords; i += nthr) hist[i] = 0;
-    if (tid < 32) rows[tid] = 0;
-    for (int i = tid; i < L * k; i += nthr) ztf[i] = f32_trunc(ls.zlog(0, i / k + 1, i % k));
-    if (tid >= 32 && tid < 32 + L) {
-        // a finite value that float32 cannot hold turns the bound off (infinite margin)
-        float m = 0.0f;
-        for (int r = 0; r < k; ++r) {
-            const double x = ls.zlog(0, tid - 31, r);
-            const float xf = fabsf(f32_trunc(x));
-            if (x > -INFINITY && x < INFINITY) m = xf < INFINITY ? fmaxf(m, xf) : INFINITY;
-        }
-        zmag[tid - 32] = m;
-    }
-    if (tid >= 64 && tid <= 64 + L) cf[tid - 64] = f32_trunc(ls.c(0, tid - 64));
-    __syncthreads();
+    if (tid <= L) cf[tid] = f32_trunc(ls.c(0, tid));
 
-    // ---- levels 1..d0 in full, one level at a time (prefix i of level d is
-    // child i mod k of prefix i / k of level d-1) ----
+    // ---- levels 1..d0 in full, two levels a pass: level d from level d-1's
+    // stored sums, level d+1 from them too (its parent's sum formed again,
+    // by the same operations) ----
     unsigned long long hi = 0ull, lo = ~0ull;
     int live = 0;
     bool bad = false;
@@ -572,22 +592,48 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
         bad = !(c > -INFINITY && c < INFINITY);
     }
     {
-        int off = 0, poff = 0, lev = k;
-        for (int d = 1; d <= d0; ++d) {
-            const double cd = ls.c(0, d);
-            for (int i = tid; i < lev; i += nthr) {
-                const unsigned int q = plan.kdiv.div((unsigned int)i);
-                const int r = i - (int)q * k;
-                const int pp = d == 1 ? -1 : poff + (int)q;
-                const double z = (d == 1 ? 0.0 : czs[pp]) + ls.zlog(0, d, r);
-                const double sv = z - cd;
+        int off = 0, poff = 0, lev = k;  // level d starts at off, level d-1 at poff
+        for (int d = 1; d <= d0; d += 2) {
+            const bool two = d + 1 <= d0;
+            const int n1 = lev, n2 = two ? lev * k : 0;
+            const double c1 = ls.c(0, d), c2 = two ? ls.c(0, d + 1) : 0.0;
+            for (int i = tid; i < n1 + n2; i += nthr) {
+                int idx, pp;
+                double z, cc;
+                unsigned long long tb;
+                if (i < n1) {
+                    const unsigned int q = plan.kdiv.div((unsigned int)i);
+                    const int r = i - (int)q * k;
+                    pp = d == 1 ? -1 : poff + (int)q;
+                    z = (d == 1 ? 0.0 : czs[pp]) + ls.zlog(0, d, r);
+                    tb = ((unsigned long long)d << 59) |
+                         (d == 1 ? 0ull : (((ctb[pp] & kRsMask) << bits) & kRsMask)) |
+                         (unsigned long long)r;
+                    idx = off + i;
+                    cc = c1;
+                } else {
+                    const int j = i - n1;
+                    const unsigned int q = plan.kdiv.div((unsigned int)j);  // parent in level d
+                    const int r2 = j - (int)q * k;
+                    const unsigned int q1 = plan.kdiv.div(q);  // grandparent in level d-1
+                    const int r1 = (int)q - (int)q1 * k;
+                    const int gp = d == 1 ? -1 : poff + (int)q1;
+                    const double z1 = (d == 1 ? 0.0 : czs[gp]) + ls.zlog(0, d, r1);
+                    z = z1 + ls.zlog(0, d + 1, r2);
+                    const unsigned long long t1 =
+                        (d == 1 ? 0ull : (((ctb[gp] & kRsMask) << bits) & kRsMask)) |
+                        (unsigned long long)r1;
+                    tb = ((unsigned long long)(d + 1) << 59) | ((t1 << bits) & kRsMask) |
+                         (unsigned long long)r2;
+                    pp = off + (int)q;
+                    idx = off + n1 + j;
+                    cc = c2;
+                }
+                const double sv = z - cc;
                 const unsigned long long key = order_key(sv);
                 if (sv != sv) bad = true;
-                const int idx = off + i;
                 ckey[idx] = key;
-                ctb[idx] = ((unsigned long long)d << 59) |
-                           (d == 1 ? 0ull : (((ctb[pp] & kRsMask) << bits) & kRsMask)) |
-                           (unsigned long long)r;
+                ctb[idx] = tb;
                 czs[idx] = z;
                 czf[idx] = f32_trunc(z);
                 cpar[idx] = pp;
@@ -598,10 +644,10 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
                     ++live;
                 }
             }
-            poff = off;
-            off += lev;
-            lev *= k;
-            if (d < d0) __syncthreads();  // the next level reads this one's sums
+            poff = two ? off + n1 : off;  // the pass's last level
+            off += n1 + n2;
+            lev = two ? n2 * k : n1 * k;
+            if (d + 2 <= d0) __syncthreads();  // the next pass reads these sums
         }
     }
 #pragma unroll
@@ -612,18 +658,18 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) s_fail = 1;
     if (lane == 0) {
-        s_whi[wid] = hi;
-        s_wlo[wid] = lo;
-        s_wlive[wid] = live;
+        ts.whi[wid] = hi;
+        ts.wlo[wid] = lo;
+        ts.wlive[wid] = live;
     }
     __syncthreads();
     if (s_fail != 0) return false;
     unsigned long long top = 0ull, bot = ~0ull;
     int nlive = 0;
     for (int w = 0; w < nw; ++w) {
-        top = max(top, s_whi[w]);
-        bot = min(bot, s_wlo[w]);
-        nlive += s_wlive[w];
+        top = max(top, ts.whi[w]);
+        bot = min(bot, ts.wlo[w]);
+        nlive += ts.wlive[w];
     }
     if (nlive < B) return false;
     // bins of width 2^sh below the best key: bin(key) = (top - key) >> sh
@@ -654,55 +700,63 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
     unsigned long long theta = bin_floor(thr_warp_bin(hist, rows, B, &upto));
 
     // ---- levels d0+1, ...: kept children of the last level's kept prefixes ----
-    int pa = n0, pe = n0;
-    {
+    // Per prefix, a float32 bound on its passing children: child r can pass
+    // only if ztf[r] >= g.  The margin covers the error of every float32
+    // operand and step (a few units of 2^-24 of the magnitudes involved,
+    // against 2^-18 here; the absolute term covers values below float32's
+    // normal range) and that of the float64 evaluation.  Where an operand does
+    // not fit float32, g is not finite and every rank is evaluated.  A bound
+    // formed with an earlier (lower) theta only lists more pairs: each pair's
+    // exact key is tested against the current theta.
+    auto bound = [&](float zsf, float thf, int dc) {  // dc: the children's depth
+        const float cdf = cf[dc];
+        const float m = 0x1p-18f * (fabsf(thf) + fabsf(cdf) + fabsf(zsf) + zmag[dc - 1]) + 1e-30f;
+        const float g = ((thf - m) + cdf) - zsf;
+        if (!(g > -INFINITY && g < INFINITY)) return k;
+        const float* zr = ztf + (dc - 1) * k;
+        int cb = 0;  // the list is sorted: the ranks that pass are a run from 0
+        for (int r = 0; r < k; ++r) cb += zr[r] >= g ? 1 : 0;
+        return cb;
+    };
+    // list the (prefix, rank) pairs of the lanes' prefixes for depth dc (all lanes call)
+    auto list_pairs = [&](int p, int cb, int dc) {
+        const int inc = warp_incl_scan(cb);
+        int at = 0;
+        if (lane == 31 && inc > 0) at = atomicAdd(&s_slot[dc % 3], inc);
+        at = __shfl_sync(0xffffffffu, at, 31) + inc - cb;
+        int* sl = slots + (dc & 1) * kThrSlots;
+        for (int r = 0; r < cb; ++r) {
+            if (at + r < kThrSlots) sl[at + r] = (p << 5) | r;
+            else s_fail = 1;
+        }
+    };
+    int pe = n0;
+    if (d0 < L) {
         int lev = 1;
         for (int j = 0; j < d0; ++j) lev *= k;
-        pa = n0 - lev;  // level d0
+        const float thf = f32_trunc(key_score(theta));
+        for (int p0 = n0 - lev; p0 < n0; p0 += nthr) {  // level d0
+            const int p = p0 + tid;
+            const int cb = p < n0 && ckey[p] >= theta ? bound(czf[p], thf, d0 + 1) : 0;
+            list_pairs(p, cb, d0 + 1);
+        }
     }
-    for (int d = d0 + 1; d <= L && pa < pe; ++d) {
+    __syncthreads();
+    if (s_fail != 0) return false;
+    for (int d = d0 + 1; d <= L; ++d) {
+        const int ns = s_slot[d % 3];
+        if (ns == 0) break;
         const double cd = ls.c(0, d);
         int* cnt = &s_lev[d % 3];
-        int* nslot = &s_slot[d % 3];
-        if (tid == 0) {  // both last read before the previous barrier
+        if (tid == 0) {  // last read before the previous barrier
             s_lev[(d + 1) % 3] = 0;
-            s_slot[(d + 1) % 3] = 0;
+            s_slot[(d + 2) % 3] = 0;
         }
-        // (1) Per parent, a float32 bound on its passing children: child r can
-        // pass only if ztf[r] >= g.  The margin covers the error of every
-        // float32 operand and step (a few units of 2^-24 of the magnitudes
-        // involved, against 2^-18 here; the absolute term covers values below
-        // float32's normal range) and that of the float64 evaluation.  Where an
-        // operand does not fit float32, g is not finite and every rank is
-        // evaluated.  The (parent, rank) pairs go to one list for the block.
-        const float thf = f32_trunc(key_score(theta)), cdf = cf[d], zm = zmag[d - 1];
-        const float* zr = ztf + (d - 1) * k;
-        for (int p0 = pa; p0 < pe; p0 += nthr) {
-            const int p = p0 + tid;
-            int cb = 0;
-            if (p < pe && ckey[p] >= theta) {
-                const float zsf = czf[p];
-                const float m = 0x1p-18f * (fabsf(thf) + fabsf(cdf) + fabsf(zsf) + zm) + 1e-30f;
-                const float g = ((thf - m) + cdf) - zsf;
-                if (g > -INFINITY && g < INFINITY) {
-                    while (cb < k && zr[cb] >= g) ++cb;
-                } else {
-                    cb = k;
-                }
-            }
-            const int inc = warp_incl_scan(cb);
-            int at = 0;
-            if (lane == 31 && inc > 0) at = atomicAdd(nslot, inc);
-            at = __shfl_sync(0xffffffffu, at, 31) + inc - cb;
-            for (int r = 0; r < cb; ++r) {
-                if (at + r < kThrSlots) slot[at + r] = (p << 5) | r;
-                else s_fail = 1;
-            }
-        }
-        __syncthreads();
-        if (s_fail != 0) return false;
-        // (2) the exact keys of the listed pairs, packed over all threads
-        const int ns = *nslot;
+        // the exact keys of the listed pairs, packed over all threads; each
+        // kept child lists its own pairs for the next depth (bounded with the
+        // theta of this depth: later rises only drop more of them)
+        const int* sl = slots + (d & 1) * kThrSlots;
+        const float thf = f32_trunc(key_score(theta));
         for (int j0 = 0; j0 < ns; j0 += nthr) {
             const int j = j0 + tid;
             bool ok = false;
@@ -710,8 +764,8 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
             double z = 0.0;
             unsigned long long key = 0ull;
             if (j < ns) {
-                p = slot[j] >> 5;
-                r = slot[j] & 31;
+                p = sl[j] >> 5;
+                r = sl[j] & 31;
                 z = czs[p] + ls.zlog(0, d, r);
                 key = order_key(z - cd);
                 ok = key >= theta;
@@ -720,30 +774,35 @@ __device__ bool thr_build(const Lists& ls, uint8_t* base, const BuildPlan& plan,
             int at = 0;
             if (lane == 0 && ball != 0u) at = atomicAdd(cnt, __popc(ball));
             at = __shfl_sync(0xffffffffu, at, 0);
+            int pos = -1, cb = 0;
             if (ok) {
-                const int pos = pe + at + __popc(ball & ((1u << lane) - 1u));
+                pos = pe + at + __popc(ball & ((1u << lane) - 1u));
                 if (pos < cap && key <= ckey[p]) {
+                    const float zf = f32_trunc(z);
                     ckey[pos] = key;
                     ctb[pos] = ((unsigned long long)d << 59) |
                                (((ctb[p] & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
                     czs[pos] = z;
-                    czf[pos] = f32_trunc(z);
+                    czf[pos] = zf;
                     cpar[pos] = p;
                     cnode[pos] = 0;
                     count_key(key);
+                    if (d < L) cb = bound(zf, thf, d + 1);
                 } else {
                     s_fail = 1;  // out of room, or a child above its parent
                 }
             }
+            list_pairs(pos, cb, d + 1);
+        }
+        {
+            // the bound rises to the B-th best key kept so far, as each warp
+            // sees the counts before the barrier (while others still add)
+            const unsigned long long th = bin_floor(thr_warp_bin(hist, rows, B, &upto));
+            theta = th > theta ? th : theta;
         }
         __syncthreads();
         if (s_fail != 0) return false;
-        pa = pe;
         pe += *cnt;
-        // the bound rises to the B-th best key kept so far (each warp on its
-        // own; a warp already on the next level only adds real candidates)
-        const unsigned long long th = bin_floor(thr_warp_bin(hist, rows, B, &upto));
-        theta = th > theta ? th : theta;
     }
     const int N = pe;
 
@@ -849,12 +908,23 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     int* flag = reinterpret_cast<int*>(big);  // [xcap] first-occurrence marks, then ranks
     const Lists ls{zt, cum, ids, L, k, bits};
     const int stride = B + 1;
+    // one mode: the threshold expansion's tables are set up beside the lists
+    __shared__ ThrState s_ts;
+    const bool thr_on = K == 1 && B > 0 && plan.tcap > 0;
+    const ThrMem tm = thr_mem(smem + plan.lists, plan.tcap, L, k);
 
     if (tid == 0) {
         s_bad = 0;
         s_nF = 0;
         s_nX = 0;
         s_D = 0;
+        for (int j = 0; j < 3; ++j) s_ts.lev[j] = s_ts.slot[j] = 0;
+        s_ts.fail = 0;
+    }
+    if (thr_on) {
+        for (int i = tid; i < kThrBinWords; i += blockDim.x) tm.hist[i] = 0;
+        if (tid < 32) tm.rows[tid] = 0;
+        if (tid < L) tm.zmag[tid] = 0.0f;
     }
     __syncthreads();
     for (int i = tid; i < nl; i += blockDim.x) {
@@ -862,19 +932,41 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
         zt[i] = x;
         ids[i] = ws.top_id[(int64_t)t * nl + i];
         if (x != x) s_bad = 1;
+        if (thr_on) {
+            // largest finite |z / T_d| per depth in float32; a finite value that
+            // float32 cannot hold makes it infinite (the bound then lists every rank)
+            const float xf = f32_trunc(x);
+            tm.ztf[i] = xf;
+            if (x > -INFINITY && x < INFINITY)
+                atomicMax(reinterpret_cast<int*>(tm.zmag) + i / k, __float_as_int(fabsf(xf)));
+        }
     }
-    for (int i = tid; i < K * L; i += blockDim.x) {  // the row log-normalisers, all at once
-        const double l = ws.lse[(int64_t)t * K * L + i];
-        if (l != l) s_bad = 1;
-        cum[(i / L) * (L + 1) + i % L + 1] = l;
-    }
-    __syncthreads();
-    for (int m = tid; m < K; m += blockDim.x) {  // C_m(d), summed left to right in place
-        double c = 0.0;
-        cum[m * (L + 1)] = 0.0;
-        for (int d = 1; d <= L; ++d) {
-            c = c + cum[m * (L + 1) + d];
-            cum[m * (L + 1) + d] = c;
+    if (K == 1) {
+        // C(d), summed left to right: warp 0 loads the L normalisers at once
+        if (tid < 32) {
+            const double l = tid < L ? ws.lse[(int64_t)t * L + tid] : 0.0;
+            if (l != l) s_bad = 1;
+            double c = 0.0;
+            if (tid == 0) cum[0] = 0.0;
+            for (int d = 0; d < L; ++d) {
+                c = c + __shfl_sync(0xffffffffu, l, d);
+                if (tid == d) cum[d + 1] = c;
+            }
+        }
+    } else {
+        for (int i = tid; i < K * L; i += blockDim.x) {  // the row log-normalisers, all at once
+            const double l = ws.lse[(int64_t)t * K * L + i];
+            if (l != l) s_bad = 1;
+            cum[(i / L) * (L + 1) + i % L + 1] = l;
+        }
+        __syncthreads();
+        for (int m = tid; m < K; m += blockDim.x) {  // C_m(d), summed left to right in place
+            double c = 0.0;
+            cum[m * (L + 1)] = 0.0;
+            for (int d = 1; d <= L; ++d) {
+                c = c + cum[m * (L + 1) + d];
+                cum[m * (L + 1) + d] = c;
+            }
         }
     }
     __syncthreads();
@@ -888,8 +980,8 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
     int32_t* md = mode ? mode + (int64_t)t * stride : nullptr;
     // one mode: threshold expansion first, the rounds when it declines
     bool done = false;
-    if (!bad && B > 0 && K == 1 && plan.tcap > 0)
-        done = thr_build(ls, smem + plan.lists, plan, L, k, B, bits, par, tok, dep, sc,
+    if (!bad && thr_on)
+        done = thr_build(ls, tm, s_ts, plan, L, k, B, bits, par, tok, dep, sc,
                          ws.score64 ? ws.score64 + (int64_t)t * stride : nullptr, rk, md);
     if (!bad && B > 0 && !done) {  // B = 0: the tree is the root alone
         // seeds: the root's children, all k first tokens of every mode
