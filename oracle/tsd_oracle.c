@@ -185,6 +185,7 @@ typedef struct {
     double score;        /* s_m(v) = zsum - C_m(depth) */
     double zsum;         /* sum of z/T along v */
     double pzsum;        /* the same sum along v's parent */
+    double pscore;       /* the score of v's parent (the root's is 0) */
     int32_t mode;
     int32_t depth;       /* |v| >= 1 */
     int32_t rank;        /* rank of v's last token in mode m's list */
@@ -280,6 +281,7 @@ int orc_build_tree(const int32_t *top_id, const double *top_zt, const double *ls
             x.mode = m; x.depth = 1; x.rank = r; x.pnode = 0;
             x.pzsum = 0.0; x.zsum = 0.0 + ZT(m, 0, r);
             x.score = x.zsum - CUM(m, 1);
+            x.pscore = 0.0;
             x.ranks[0] = (uint8_t)r;
             heap_push(&h, &x);
         }
@@ -314,6 +316,13 @@ int orc_build_tree(const int32_t *top_id, const double *top_zt, const double *ls
                 s.ranks[e.depth - 1] = (uint8_t)(e.rank + 1);
                 s.zsum = e.pzsum + ZT(e.mode, e.depth - 1, e.rank + 1);
                 s.score = s.zsum - CUM(e.mode, e.depth);
+                /* A child's sum of log q cannot exceed its parent's (each
+                 * log q <= 0, [CAST] Sec. 2 Eq. 1); where the rounding of the
+                 * two path sums would put it above, it takes the parent's
+                 * score, so that a parent always precedes its children in the
+                 * (score desc, depth asc, ...) order.  Depth 1 is below the
+                 * root's 0 already (z/T <= LSE). */
+                if (e.depth > 1 && s.score > s.pscore) s.score = s.pscore;
                 heap_push(&h, &s);
             }
             if (e.depth < L) { /* first child: rank 0 at the next position */
@@ -321,6 +330,8 @@ int orc_build_tree(const int32_t *top_id, const double *top_zt, const double *ls
                 c.depth = e.depth + 1; c.rank = 0; c.pnode = node;
                 c.pzsum = e.zsum; c.zsum = e.zsum + ZT(e.mode, e.depth, 0);
                 c.score = c.zsum - CUM(e.mode, e.depth + 1);
+                c.pscore = e.score;
+                if (c.score > e.score) c.score = e.score;  /* as for siblings */
                 c.ranks[e.depth] = 0;
                 heap_push(&h, &c);
             }
@@ -331,6 +342,8 @@ int orc_build_tree(const int32_t *top_id, const double *top_zt, const double *ls
                     c.depth = e.depth + 1; c.rank = r; c.pnode = node;
                     c.pzsum = e.zsum; c.zsum = e.zsum + ZT(e.mode, e.depth, r);
                     c.score = c.zsum - CUM(e.mode, e.depth + 1);
+                    c.pscore = e.score;  /* clamped as for siblings */
+                    if (c.score > e.score) c.score = e.score;
                     c.ranks[e.depth] = (uint8_t)r;
                     heap_push(&h, &c);
                 }

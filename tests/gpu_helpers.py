@@ -9,7 +9,9 @@ Tolerances (stated once, used by every GPU test):
     tests bound their number;
   * builder order: two prefixes may swap only when their oracle scores differ
     by at most SCORE_TOL relative (the kernel's log-normaliser is accumulated
-    in fp32, the oracle's in fp64);
+    in fp32, the oracle's in fp64); builder scores agree within SCORE_TOL
+    relative, absolute below magnitude 1 (the normaliser's error is at the
+    scale of the logits, while a path of near-certain tokens scores near 0);
   * probabilities, exit masses, coverage: RTOL relative; values below TINY
     compared absolutely.
 """
@@ -69,8 +71,10 @@ def compare_trees(gpu, ref, lists):
     so = sequences(ref["parent"], ref["token"], n_o)
     if sg == so:
         assert np.array_equal(gpu["depth"][:n_g], ref["depth"][:n_o])
-        ok, err = close(gpu["score"][1:n_g], ref["score"][1:n_o], rtol=SCORE_TOL)
-        assert ok, ("scores", err)
+        g = np.asarray(gpu["score"][1:n_g], dtype=np.float64)
+        w = np.asarray(ref["score"][1:n_o], dtype=np.float64)
+        err = np.abs(g - w)
+        assert np.all(err <= SCORE_TOL * np.maximum(1.0, np.abs(w))), ("scores", float(err.max(initial=0.0)))
         return 0
     flips = 0
     for i in range(1, n_g):

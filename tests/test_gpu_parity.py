@@ -149,6 +149,54 @@ def test_build_masked_and_small_universe(tsd, dev, orc):
     assert compare_trees(_tree_np(out), ref, lists) == 0
 
 
+@pytest.mark.parametrize("V,L,k,B", [(V_Q, 16, 8, 256), (V_Q, 16, 8, 64), (5000, 16, 2, 200),
+                                     (5000, 16, 4, 340), (5000, 12, 16, 256), (5000, 16, 8, 1),
+                                     (5000, 16, 8, 700), (5000, 16, 8, 1500)])
+def test_build_one_mode_equals_duplicated_modes(tsd, dev, V, L, k, B):
+    """One mode takes the threshold expansion where it applies; the same
+    drafter given as two identical modes takes the rounds, whose merged heap
+    keeps each prefix's first (mode 0) entry, in the one-mode order.  The two
+    trees must be identical bit for bit: nodes, parents, tokens, depths,
+    ranks and scores.  Budgets span one node, several depths
+    of full enumeration (k = 2, 4, 16), and budgets past the expansion's
+    capacity (the rounds on both sides)."""
+    seeds = [synth.seed_for(4, 500 + t) for t in range(3)]
+    dr = synth.zipf_drafter(3, L, V, 0, device=dev, seeds=seeds)
+    one = tsd.tsd_build_tree(dr, topk=k, B=B)
+    two = tsd.tsd_build_tree(torch.cat([dr, dr], dim=1), topk=k, B=B)
+    assert _np(one["status"]).tolist() == [0] * 3
+    assert _np(two["status"]).tolist() == [0] * 3
+    for key in ("n_nodes", "parent", "token", "depth", "rank", "score"):
+        assert np.array_equal(_np(one[key]), _np(two[key])), key
+
+
+@pytest.mark.parametrize("case", ["peaked_then_flat", "uniform", "flat_deep"])
+def test_build_threshold_edge_drafters(tsd, dev, orc, case):
+    """Drafters at the edges of the one-mode threshold expansion, against the
+    oracle: near-certain first three positions then eight equal tokens a
+    position (the candidates within the bound multiply by eight a depth, the
+    pair lists can outgrow their capacity and the rounds take the tree);
+    every logit equal (all prefixes of a depth tie, one key bin holds
+    hundreds of candidates ranked by their tie keys); and eight equal tokens
+    at every position of a 16-row drafter with B = 1000 (the rounds)."""
+    V, L = 64, 12
+    z = torch.zeros(1, 1, L, V)
+    B = 256
+    if case == "peaked_then_flat":
+        z[0, 0, :3, 0] = 30.0
+        z[0, 0, 3:, :] = -30.0
+        z[0, 0, 3:, :8] = 5.0
+    elif case == "flat_deep":
+        L = 16
+        z = torch.full((1, 1, L, V), -30.0)
+        z[0, 0, :, :8] = 1.0
+        B = 1000
+    out = tsd.tsd_build_tree(z.to(dev), topk=8, B=B)
+    assert int(out["status"][0]) == 0
+    ref, lists = oracle_build(orc, z[0], 8, B)
+    assert compare_trees(_tree_np(out), ref, lists) == 0
+
+
 def test_build_nonfinite_status(tsd, dev):
     z = torch.randn(2, 1, 4, 32)
     z[1, 0, 2, 5] = float("nan")

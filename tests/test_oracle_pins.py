@@ -232,6 +232,47 @@ def test_builder_single_mode_equals_exhaustive(orc, seed):
         assert tr["depth"][u] == tr["depth"][tr["parent"][u]] + 1
 
 
+def test_builder_scores_never_rise_along_a_path(orc):
+    """A prefix's sum of log q cannot exceed its parent's ([CAST] Sec. 2
+    Eq. 1: every log q is at most 0).  Fixture: depth 1 has z/T = 0.8758...
+    under LSE 3.5232... (log q < 0); depth 2's only token has z/T equal to
+    its LSE (q = 1).  Evaluated as (path sum) - C(d), the depth-2 score
+    rounds 4.4e-16 above the depth-1 score; the builder takes the parent's
+    score there, under both push rules, so the child ties its parent and
+    follows it.  Found by a random search over float64 values."""
+    a, b, x = 0.8758060614355943, 3.5232430639311674, 3.461974184283127
+    assert (a + x) - (b + x) > a - b  # the fixture does round upward
+    ls = dict(top_id=np.array([[[5], [9]]], dtype=np.int32),
+              top_zt=np.array([[[a], [x]]]), lse=np.array([[b, x]]))
+    for rule in (0, 1):
+        tr = orc.build_tree(ls, 2, push_rule=rule)
+        assert tr["n_nodes"] == 3
+        assert tr["parent"][1:3].tolist() == [0, 1]
+        assert tr["token"][1:3].tolist() == [5, 9]
+        assert tr["score"][1] == a - b and tr["score"][2] == tr["score"][1]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_builder_scores_never_rise_random(orc, seed):
+    """The same property on random lists whose rows are certain (q = 1,
+    z/T = LSE) at random positions: every node's score is at most its
+    parent's, and parents precede children."""
+    rng = np.random.default_rng(900 + seed)
+    K, L, k = 1 + seed % 2, 6, 3
+    zt = rng.uniform(-8.0, 8.0, size=(K, L, k))
+    zt = -np.sort(-zt, axis=-1)
+    lse = zt[..., 0] + rng.uniform(0.0, 2.0, size=(K, L))
+    certain = rng.random((K, L)) < 0.5
+    lse = np.where(certain, zt[..., 0], lse)  # rank 0 carries all the mass
+    ids = np.broadcast_to(np.arange(k, dtype=np.int32), (K, L, k)).copy()
+    tr = orc.build_tree(dict(top_id=ids, top_zt=zt, lse=lse), 60)
+    for u in range(1, tr["n_nodes"]):
+        p = tr["parent"][u]
+        assert 0 <= p < u
+        if p > 0:
+            assert tr["score"][u] <= tr["score"][p]
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_push_rules_agree(orc, seed):
     """Sibling+first-child pushes [MFD App. B] and push-all-k-children

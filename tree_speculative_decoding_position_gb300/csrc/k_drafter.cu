@@ -262,8 +262,12 @@ drafter_row_kernel(const T* __restrict__ logits, int64_t rows, int64_t V, int nc
         if (lane == 0) {
             const bool b = bad || m == -INFINITY || !(sum > 0.0);
             // LSE_j = ln 2 * (mc + log2 S), all relative to the same reference mc.
-            ws.lse[row] = b ? __longlong_as_double(0x7ff8000000000000ll)
-                            : 0.6931471805599453 * ((double)mc + log2(sum));
+            // The exponents are float32, so the result can fall a few 1e-6
+            // below the largest z / T_d, which the exact value never does: it
+            // is raised to that floor (every kept token's log q is then <= 0).
+            const double l = 0.6931471805599453 * ((double)mc + log2(sum));
+            const double zmax = temp == 1.0 ? (double)m : (double)m / temp;
+            ws.lse[row] = b ? __longlong_as_double(0x7ff8000000000000ll) : (l > zmax ? l : zmax);
         }
         return;
     }

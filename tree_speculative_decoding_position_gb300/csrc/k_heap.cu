@@ -33,7 +33,10 @@
 // its tokens' z / T_d) - C_m(depth), with C_m(d) the sum of mode m's first d
 // row log-normalisers.  Two prefixes of one depth and mode whose scaled logits
 // sum to the same value therefore tie exactly (as they do in exact
-// arithmetic), and the tie order decides them.
+// arithmetic), and the tie order decides them.  A child's key is at most its
+// parent's: each log q is at most 0, and where the rounding of the two path
+// sums would put a child above its parent, the child takes the parent's key,
+// so that a parent always precedes its children.
 //
 // Entries are 32 bytes: a 64-bit order-preserving image of the float64 score,
 // the 64-bit tie key depth << 59 | mode << 56 | rank digits (which also names
@@ -459,15 +462,16 @@ __device__ int hash_bucket(unsigned long long h, unsigned long long* hkey, int h
 // B-th best key.  The B best kept prefixes under (key desc, tie key asc) are
 // the tree, in that order: the same set and order as the rounds.
 //
-// A child's key is exact float64 (the rounds' arithmetic).  Float64 issues at
+// A child's key is exact float64 (the rounds' arithmetic, clamped to its
+// parent's key as there).  Float64 issues at
 // one warp instruction per 64 clocks per SM quarter whatever the active lanes,
 // so each level first bounds, in float32, how many of a parent's children can
 // pass (they pass as a run from rank 0: its list is sorted), and evaluates
 // only those (parent, rank) pairs, packed densely over the warps.
 //
-// Returns false when the candidates outgrow their arrays or rounding made a
-// child score above its parent; the caller then runs the rounds, which
-// rewrite every output.
+// Returns false when the candidates outgrow their arrays (or, which the
+// clamped keys exclude, a child would precede its parent); the caller then
+// runs the rounds, which rewrite every output.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int thr_pidx(int b) { return b + (b >> 6); }
 
@@ -600,12 +604,13 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
             for (int i = tid; i < n1 + n2; i += nthr) {
                 int idx, pp;
                 double z, cc;
-                unsigned long long tb;
+                unsigned long long tb, kpar;  // kpar: the parent's key
                 if (i < n1) {
                     const unsigned int q = plan.kdiv.div((unsigned int)i);
                     const int r = i - (int)q * k;
                     pp = d == 1 ? -1 : poff + (int)q;
                     z = (d == 1 ? 0.0 : czs[pp]) + ls.zlog(0, d, r);
+                    kpar = d == 1 ? ~0ull : ckey[pp];
                     tb = ((unsigned long long)d << 59) |
                          (d == 1 ? 0ull : (((ctb[pp] & kRsMask) << bits) & kRsMask)) |
                          (unsigned long long)r;
@@ -620,6 +625,8 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
                     const int gp = d == 1 ? -1 : poff + (int)q1;
                     const double z1 = (d == 1 ? 0.0 : czs[gp]) + ls.zlog(0, d, r1);
                     z = z1 + ls.zlog(0, d + 1, r2);
+                    const unsigned long long k1 = order_key(z1 - c1);  // the parent's key
+                    kpar = d == 1 ? k1 : min(k1, ckey[gp]);
                     const unsigned long long t1 =
                         (d == 1 ? 0ull : (((ctb[gp] & kRsMask) << bits) & kRsMask)) |
                         (unsigned long long)r1;
@@ -630,7 +637,9 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
                     cc = c2;
                 }
                 const double sv = z - cc;
-                const unsigned long long key = order_key(sv);
+                // a child's key is never above its parent's: where the rounding
+                // of the two path sums would put it there, it takes the parent's
+                const unsigned long long key = min(order_key(sv), kpar);
                 if (sv != sv) bad = true;
                 ckey[idx] = key;
                 ctb[idx] = tb;
@@ -767,7 +776,7 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
                 p = sl[j] >> 5;
                 r = sl[j] & 31;
                 z = czs[p] + ls.zlog(0, d, r);
-                key = order_key(z - cd);
+                key = min(order_key(z - cd), ckey[p]);  // never above the parent
                 ok = key >= theta;
             }
             const unsigned int ball = __ballot_sync(0xffffffffu, ok);
@@ -777,7 +786,7 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
             int pos = -1, cb = 0;
             if (ok) {
                 pos = pe + at + __popc(ball & ((1u << lane) - 1u));
-                if (pos < cap && key <= ckey[p]) {
+                if (pos < cap) {
                     const float zf = f32_trunc(z);
                     ckey[pos] = key;
                     ctb[pos] = ((unsigned long long)d << 59) |
@@ -789,7 +798,7 @@ __device__ bool thr_build(const Lists& ls, const ThrMem& tm, ThrState& ts, const
                     count_key(key);
                     if (d < L) cb = bound(zf, thf, d + 1);
                 } else {
-                    s_fail = 1;  // out of room, or a child above its parent
+                    s_fail = 1;  // out of room
                 }
             }
             list_pairs(pos, cb, d + 1);
@@ -1041,7 +1050,9 @@ build_tree_kernel(BuildWs ws, BuildPlan plan, int K, int L, int k, int B, int bi
                     if (d < L) {
                         const double z = e.zsum + ls.zlog(m, d + 1, r);
                         const double sv = z - ls.c(m, d + 1);
-                        ch[u].key = order_key(sv);
+                        // never above the parent (rounding of the two path sums)
+                        const unsigned long long kc = order_key(sv);
+                        ch[u].key = kc < e.key ? kc : e.key;
                         ch[u].tb = ((unsigned long long)(d + 1) << 59) |
                                    ((unsigned long long)m << 56) |
                                    (((e.tb & kRsMask) << bits) & kRsMask) | (unsigned long long)r;
