@@ -11,7 +11,10 @@
 // position); a prefix taken again from another mode keeps its first node.
 //
 // The pages run this as a sequential heap on the host.  Here one CTA per tree
-// runs it in rounds over a sorted frontier: each round takes the frontier's
+// builds it.  One mode takes the threshold expansion (below, thr_build): every
+// prefix that can still reach the B best, depth by depth, under a rising bound.
+// Several modes, and one mode when that declines, take rounds over a sorted
+// frontier: each round takes the frontier's
 // best M entries at once, merges them into the sorted list X of taken
 // entries, and merges all k children of each (CAST App. C's push rule; the
 // oracle's pins show it pops the same prefixes in the same order as the
